@@ -1,0 +1,227 @@
+/*
+ * moe.h -- C ABI of libmoe, the GB300 (sm_103a) routed-expert MoE layer.
+ *
+ * The layer, as the Hebrus "Agent Field Notes" state it:
+ *   router logits -> float32 softmax over the selected experts, top-k in rank
+ *   order -> token rows grouped by expert -> per expert SwiGLU
+ *   (gate and up together, then down) -> weighted sum in route-rank order;
+ *   plus deduplication of repeated routes across a verifier block.
+ *
+ * Conventions shared by every call:
+ *  - Every pointer is a DEVICE pointer owned by the caller, except where a
+ *    comment says otherwise.  The library allocates no device memory: where a
+ *    call needs scratch space the caller passes it in (see *_workspace_size).
+ *  - bf16 values travel as uint16_t bit patterns; all arrays are dense and
+ *    row-major with the shapes given in brackets.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the calls return before it completes.
+ *  - Arguments are checked on the host BEFORE anything is enqueued.  A call
+ *    that returns anything but MOE_OK has enqueued nothing and written
+ *    nothing: the rule of AFN-010 "One bank flip is enough: make the whole
+ *    inference chunk transactional", section "The publication model" (output
+ *    remains caller-private while work is fallible), applied to rejection.
+ *  - Errors seen on the device (an expert ID outside [0,E), a non-finite
+ *    output, a bounded wait that ran out) are OR-ed into *dev_status as
+ *    MOE_DEV_* bits; the caller reads it after synchronising.  No kernel
+ *    traps.  dev_status may be NULL where a call says so.
+ *  - Supported geometry (anything else returns MOE_ENOTSUP):
+ *      1 <= k <= 32, k <= E <= 1024, H % 128 == 0, I % 64 == 0,
+ *      T * k < 2^31, 16-byte aligned pointers for every bf16/f32 array.
+ *    T == 0 is accepted and enqueues nothing.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_EINVAL = 1,          /* null pointer, misaligned pointer, bad enum       */
+  MOE_ESHAPE = 2,          /* inconsistent or non-positive sizes               */
+  MOE_ERANGE = 3,          /* reserved: device-side range errors use dev_status */
+  MOE_ECUDA = 4,           /* a CUDA runtime/driver call failed                */
+  MOE_ENOTSUP = 5,         /* geometry outside the supported envelope          */
+  MOE_EDEVICE_TIMEOUT = 6, /* reserved: device-side timeouts use dev_status    */
+  MOE_EWORKSPACE = 7       /* workspace pointer null or smaller than required  */
+} moe_status;
+
+/* Bits OR-ed into *dev_status by kernels. */
+#define MOE_DEV_BAD_EXPERT 0x1 /* an expert ID outside [0, E) was seen       */
+#define MOE_DEV_NONFINITE 0x2  /* a layer output was NaN or infinite         */
+#define MOE_DEV_TIMEOUT 0x4    /* a bounded pipeline wait ran out            */
+
+typedef enum moe_wfmt {
+  MOE_W_BF16 = 0,    /* bf16 weights                                         */
+  MOE_W_INT4_G64 = 1 /* int4 codes, one bf16 scale per 64 inputs of a row    */
+} moe_wfmt;
+
+/* ABI version of this header (major * 100 + minor). */
+MOE_API int moe_abi_version(void);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+MOE_API const char *moe_status_str(moe_status s);
+
+/* Number of streaming multiprocessors of the current device, or -1. */
+MOE_API int moe_device_sm_count(void);
+
+/* ---------------------------------------------------------------------------
+ * moe_route -- router logits, top-k in rank order, renormalised weights.
+ *
+ * Source: AFN-001 "Porting Qwen3.8-Flash-Next to Hebrus: evidence before
+ * execution", section "Phase 1: separate math from acceleration" (float32
+ * router softmax and normalized top-10 selection); AFN-021 "Replay decode as
+ * prefill", section "The key equivalence -- and where it breaks" (IDs and
+ * their rank order are the label; weights compared within a tolerance).
+ *
+ *   L[t,e]  = sum_h x[t,h] * w_router[e,h] + bias[e]      (fp32 accumulate)
+ *   ids[t]  = the k experts with the largest L[t,:], ordered by logit
+ *             descending, ties broken by the lower expert ID
+ *   w[t,j]  = exp(L[t,ids_j] - L[t,ids_0]) / sum_j' exp(L[t,ids_j'] - L[t,ids_0])
+ *   gap[t]  = L(k-th) - L((k+1)-th), +inf when k == E
+ *
+ *   x          [T,H] bf16          w_router [E,H] bf16
+ *   bias       [E] f32, or NULL    topk_ids [T,k] int32 (out)
+ *   topk_w     [T,k] f32 (out)     gap      [T] f32 (out) or NULL
+ *   workspace  >= moe_route_workspace_size(T,E) bytes, 256-byte aligned;
+ *              contents need no initialisation and are clobbered.
+ * ------------------------------------------------------------------------- */
+MOE_API size_t moe_route_workspace_size(int T, int E);
+MOE_API moe_status moe_route(const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int H,
+                     int E, int k, int32_t *topk_ids, float *topk_w, float *gap, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_permute -- group token rows by expert (count, exclusive scan, stable
+ * scatter), optionally gathering the rows of x into expert order.
+ *
+ * Source: AFN-019 "Hide SSD misses before the router knows they exist",
+ * section "Why overlap alone cannot defeat the byte roofline" (grouping token
+ * rows by expert as a byte owner).
+ *
+ * With R = T*k and flat route index r = t*k + j:
+ *   counts[e]   = #{r : topk_ids[r] == e}                       [E] int32 (out)
+ *   offsets[e]  = sum_{e' < e} counts[e'], offsets[E] = R       [E+1] int32 (out)
+ *   perm[s]     = the route stored in slot s; the slots of expert e are
+ *                 offsets[e] .. offsets[e+1]-1 in ascending r    [R] int32 (out)
+ *   inv_perm[r] = the slot of route r (perm[inv_perm[r]] == r)   [R] int32 (out)
+ *   x_perm[s,:] = x[perm[s] / k, :]  if x_perm != NULL          [R,H] bf16 (out)
+ * x may be NULL only when x_perm is NULL.  An ID outside [0,E) sets
+ * MOE_DEV_BAD_EXPERT in *dev_status (required, 4 bytes) and the kernel then
+ * writes none of counts/offsets/perm/inv_perm/x_perm.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_permute(const int32_t *topk_ids, int T, int k, int E, const uint16_t *x, int H,
+                       int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                       uint16_t *x_perm, int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Expert contractions (tensor cores: tcgen05 MMA, TMEM accumulators, TMA).
+ *
+ * Source: AFN-019, section "Why overlap alone cannot defeat the byte roofline"
+ * (one expert = gate [I,H] + up [I,H] + down [H,I]) and section "Hypothesis
+ * H4: ExpertMajor should stream as a wavefront, not a barrier" (gate and up
+ * are used together; down only once the SwiGLU intermediate exists).
+ *
+ * Expert weight record layout (one contiguous record per expert):
+ *   MOE_W_BF16:     w_gateup [E, 2I, H] bf16: rows 0..I-1 gate, I..2I-1 up
+ *                   w_down   [E, H, I]  bf16
+ *                   s_gateup = s_down = NULL
+ *   MOE_W_INT4_G64: w_gateup [E, 2I, H/2] uint8, w_down [E, H, I/2] uint8:
+ *                   two signed 4-bit codes per byte, even input index in the
+ *                   low nibble; s_gateup [E, 2I, H/64] bf16 and
+ *                   s_down [E, H, I/64] bf16 scales; w = scale * code.
+ *                   (AFN-001, section "Phase 2": affine4 with group size 64,
+ *                   read as symmetric codes with one bf16 scale per group.)
+ *
+ * moe_expert_gateup:  for every slot s of expert e (offsets from moe_permute)
+ *     g = Wgate_e . x_perm[s],  u = Wup_e . x_perm[s]      (fp32 accumulate)
+ *     h[s,i] = bf16( silu(g_i) * u_i ),  silu(z) = z / (1 + exp(-z))
+ *   x_perm [R,H] bf16, offsets [E+1] int32, h [R,I] bf16 (out)
+ *
+ * moe_expert_down:  y_perm[s,:] = Wdown_e . h[s]           (fp32 accumulate)
+ *   h [R,I] bf16, offsets [E+1] int32, y_perm [R,H] f32 (out)
+ *
+ * moe_grouped_swiglu: moe_expert_gateup then moe_expert_down on one stream;
+ *   h is caller-owned scratch of R*I bf16.
+ *
+ * R is T*k of the routing call; slots past offsets[E] are not touched.
+ * dev_status (4 bytes, required) gets MOE_DEV_TIMEOUT if a bounded pipeline
+ * wait ran out (the kernel then stops early; outputs are incomplete).
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_expert_gateup(const uint16_t *x_perm, const int32_t *offsets, int R, int E, int H,
+                             int I, int fmt, const void *w_gateup, const uint16_t *s_gateup,
+                             uint16_t *h, int32_t *dev_status, void *stream);
+MOE_API moe_status moe_expert_down(const uint16_t *h, const int32_t *offsets, int R, int E, int H, int I,
+                           int fmt, const void *w_down, const uint16_t *s_down, float *y_perm,
+                           int32_t *dev_status, void *stream);
+MOE_API moe_status moe_grouped_swiglu(const uint16_t *x_perm, const int32_t *offsets, int R, int E, int H,
+                              int I, int fmt, const void *w_gateup, const uint16_t *s_gateup,
+                              const void *w_down, const uint16_t *s_down, uint16_t *h,
+                              float *y_perm, int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_combine -- weighted sum of expert outputs in route-rank order.
+ *
+ * Source: AFN-019, section "Hypothesis H4" (the final weighted sum follows a
+ * deterministic route-rank order).
+ *
+ *   acc[t,:] = sum_{j=0}^{k-1} topk_w[t,j] * y_perm[inv_perm[t*k+j], :]
+ *              (fp32, accumulated in j order)
+ *   out_f32[t,:] = acc + residual[t,:]   (residual [T,H] f32 or NULL -> 0)
+ *   out_bf16[t,:] = bf16(out_f32[t,:])
+ * At least one of out_bf16 / out_f32 must be non-NULL.  A non-finite result
+ * sets MOE_DEV_NONFINITE in *dev_status (may be NULL to skip the check).
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_combine(const float *y_perm, const int32_t *inv_perm, const float *topk_w, int T,
+                       int k, int H, const float *residual, uint16_t *out_bf16, float *out_f32,
+                       int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * route_block_dedup -- unique experts per (layer, verifier block) and the
+ * exact routed bytes each block needs.
+ *
+ * Source: AFN-019, section "Why overlap alone cannot defeat the byte roofline"
+ * (deduplication of repeated routes across a verifier block; ideal payload at
+ * two and four bits) and section "Hypothesis H7: DFlash block size must follow
+ * I/O cost" (48 * U_B * record bytes per block; break-even U_B < 10 tau(B)).
+ *
+ *   ids     [L, T_tot, k] int32; block b holds tokens [b*block, (b+1)*block)
+ *           (the last block may be shorter); nb = ceil(T_tot / block)
+ *   mask    [L, nb, ceil(E/32)] uint32 (out): bit e set iff expert e is routed
+ *   U       [L, nb] int32 (out): popcount of the mask
+ *   bytes2  [nb] int64 (out): sum_l U[l,b] * 3*H*I * 2 / 8
+ *   bytes4  [nb] int64 (out): sum_l U[l,b] * 3*H*I * 4 / 8
+ * An ID outside [0,E) sets MOE_DEV_BAD_EXPERT in *dev_status (required);
+ * that block's outputs are then not written.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status route_block_dedup(const int32_t *ids, int L, int T_tot, int k, int E, int block, int H,
+                             int I, uint32_t *mask, int32_t *U, int64_t *bytes2, int64_t *bytes4,
+                             int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_rmsnorm -- zero-centred RMS normalisation feeding the router and the
+ * experts of a residual stack layer  x <- x + MoE(RMSNorm(x)).
+ *
+ * Source: AFN-001, section "Phase 1: separate math from acceleration"
+ * (zero-centred RMS normalisation: the gain is 1 + gamma).
+ *
+ *   out[t,h] = bf16( x[t,h] / sqrt(mean_h x[t,:]^2 + eps) * (1 + gamma[h]) )
+ *   x [T,H] f32, gamma [H] f32 or NULL (-> 0), out [T,H] bf16
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_rmsnorm(const float *x, const float *gamma, float eps, int T, int H, uint16_t *out,
+                       void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -23,6 +23,7 @@ Functions and the page passages they follow (Hebrus "Agent Field Notes"):
                         (48 * U_B * record bytes).
   dequant_int4(...)     AFN-001, section "Phase 2" (affine4, group 64), in the
                         symmetric-scale reading.
+  combine(...)          AFN-019, section "Hypothesis H4" (weighted sum in route-rank order).
   rmsnorm(...)          AFN-001, section "Phase 1" (zero-centred RMS normalisation).
 
 Parity pins: every function above is pinned in tests/test_oracle_pins.py
@@ -58,6 +59,7 @@ def _load():
         lib.oracle_experts_combine.argtypes = [p, i, i, i, i, p, p, p, p, p, p, p, p, p]
         lib.oracle_expert_rows.argtypes = [p, i, i, i, p, p, i, p]
         lib.oracle_dequant_int4.argtypes = [p, p, i, i, p]
+        lib.oracle_combine.argtypes = [p, p, p, i, i, i, p, p]
         lib.oracle_rmsnorm.argtypes = [p, p, i, i, C.c_double, p]
         lib.oracle_dedup.argtypes = [p, i, i, i, i, i, i, i, p, p, p, p]
         lib.oracle_dedup.restype = i
@@ -161,6 +163,18 @@ def expert_rows(xin, wgu_bits, wd_bits, e, H, I):
     _load().oracle_expert_rows(_ptr(x), n, H, I, _ptr(_c(wgu_bits, np.uint16)),
                                _ptr(_c(wd_bits, np.uint16)), e, _ptr(y))
     return y
+
+
+def combine(y, inv, w, residual=None):
+    """out[t] = sum_j w[t,j] * y[inv[t*k+j]] (+ residual) in rank order j."""
+    yc = _c(y, np.float32)
+    H = yc.shape[1]
+    wc = _c(w, np.float32)
+    T, k = wc.shape
+    ic = _c(inv, np.int32)
+    out = np.empty((T, H), np.float32)
+    _load().oracle_combine(_ptr(yc), _ptr(ic), _ptr(wc), T, k, H, _ptr(_c(residual, np.float32)), _ptr(out))
+    return out
 
 
 def dequant_int4(q, s_bits):

@@ -265,6 +265,20 @@ void oracle_expert_rows(const float *xin, int n, int H, int I, const uint16_t *w
   free(g); free(u); free(d); free(xd); free(hb); free(yd);
 }
 
+/* ---- combine alone: out[t] = sum_j w[t,j] * y[inv[t*k+j]] in rank order j.
+ * y [R,H] holds one expert output per slot.                                */
+void oracle_combine(const float *y, const int32_t *inv, const float *w, int T, int k, int H,
+                    const float *residual, float *out) {
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h) {
+      double acc = 0.0;
+      for (int j = 0; j < k; ++j)
+        acc += (double)w[(size_t)t * k + j] * (double)y[(size_t)inv[(size_t)t * k + j] * H + h];
+      if (residual) acc += (double)residual[(size_t)t * H + h];
+      out[(size_t)t * H + h] = (float)acc;
+    }
+}
+
 /* ---- zero-centred RMSNorm: n = x / sqrt(mean(x^2) + eps) * (1 + gamma) --- */
 void oracle_rmsnorm(const float *x, const float *gamma, int T, int H, double eps, float *out) {
   for (int t = 0; t < T; ++t) {

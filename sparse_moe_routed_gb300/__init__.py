@@ -1,0 +1,12 @@
+"""GB300-native routed-expert MoE layer (sm_103a CUDA kernels behind a C ABI).
+
+Importing this package does not load the CUDA library; the first call does
+(building it in-tree if needed).  There is no CPU path.
+"""
+from . import _lib
+from ._lib import (MoEError, moe_combine, moe_expert_down, moe_expert_gateup, moe_grouped_swiglu,
+                   moe_permute, moe_rmsnorm, moe_route, route_block_dedup)
+from .layer import MoELayer
+
+__all__ = ["_lib", "MoEError", "MoELayer", "moe_route", "moe_permute", "moe_expert_gateup", "moe_expert_down",
+           "moe_grouped_swiglu", "moe_combine", "route_block_dedup", "moe_rmsnorm"]

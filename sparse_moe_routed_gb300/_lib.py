@@ -1,0 +1,166 @@
+"""ctypes binding of libmoe: the same names as include/moe.h, marshalling only.
+
+Every function takes torch tensors that already live on the GPU (PyTorch is
+used here only for device memory and streams), passes their raw pointers to
+the C ABI on the current stream and raises ``MoEError`` on a non-OK status.
+No arithmetic happens in Python.  If the shared library is missing it is
+built in-tree; if it cannot be built or loaded the call raises: there is no
+CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+import threading
+
+from . import build as _build
+
+MOE_OK, MOE_EINVAL, MOE_ESHAPE, MOE_ERANGE, MOE_ECUDA, MOE_ENOTSUP, MOE_EDEVICE_TIMEOUT, MOE_EWORKSPACE = range(8)
+MOE_DEV_BAD_EXPERT, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
+MOE_W_BF16, MOE_W_INT4_G64 = 0, 1
+
+HEADER = os.path.join(_build.INCLUDE, "moe.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+        self.status = status
+
+
+def declared_functions():
+    """Names of the functions include/moe.h declares (parsed from the header)."""
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]*?\b((?:moe|route)_\w+)\s*\(", txt)))
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) libmoe.so and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if path is None:
+            path = _build.build()
+        lib = C.CDLL(path)
+        p, i, sz = C.c_void_p, C.c_int, C.c_size_t
+        f = C.c_float
+        sig = {
+            "moe_abi_version": ([], i),
+            "moe_status_str": ([i], C.c_char_p),
+            "moe_device_sm_count": ([], i),
+            "moe_route_workspace_size": ([i, i], sz),
+            "moe_route": ([p, p, p, i, i, i, i, p, p, p, p, sz, p], i),
+            "moe_permute": ([p, i, i, i, p, i, p, p, p, p, p, p, p], i),
+            "moe_expert_gateup": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
+            "moe_expert_down": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
+            "moe_grouped_swiglu": ([p, p, i, i, i, i, i, p, p, p, p, p, p, p, p], i),
+            "moe_combine": ([p, p, p, i, i, i, p, p, p, p, p], i),
+            "route_block_dedup": ([p, i, i, i, i, i, i, i, p, p, p, p, p, p], i),
+            "moe_rmsnorm": ([p, p, f, i, i, p, p], i),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, st):
+    if st != MOE_OK:
+        msg = load().moe_status_str(st).decode()
+        raise MoEError(fn, st, msg)
+
+
+def status_str(st: int) -> str:
+    return load().moe_status_str(st).decode()
+
+
+def abi_version() -> int:
+    return load().moe_abi_version()
+
+
+def device_sm_count() -> int:
+    return load().moe_device_sm_count()
+
+
+def route_workspace_size(T: int, E: int) -> int:
+    return load().moe_route_workspace_size(T, E)
+
+
+def moe_route(x, w_router, bias, k, topk_ids, topk_w, gap, workspace, stream=None):
+    T, H = x.shape
+    E = w_router.shape[0]
+    st = load().moe_route(_ptr(x), _ptr(w_router), _ptr(bias), T, H, E, k, _ptr(topk_ids), _ptr(topk_w),
+                          _ptr(gap), _ptr(workspace), workspace.numel() * workspace.element_size()
+                          if workspace is not None else 0, _stream(stream))
+    _check("moe_route", st)
+
+
+def moe_permute(topk_ids, E, x, counts, offsets, perm, inv_perm, x_perm, dev_status, stream=None):
+    T, k = topk_ids.shape
+    H = x.shape[1] if x is not None else 0
+    st = load().moe_permute(_ptr(topk_ids), T, k, E, _ptr(x), H, _ptr(counts), _ptr(offsets), _ptr(perm),
+                            _ptr(inv_perm), _ptr(x_perm), _ptr(dev_status), _stream(stream))
+    _check("moe_permute", st)
+
+
+def moe_expert_gateup(x_perm, offsets, E, H, I, w_gateup, h, dev_status, fmt=MOE_W_BF16, s_gateup=None,
+                      stream=None):
+    R = x_perm.shape[0]
+    st = load().moe_expert_gateup(_ptr(x_perm), _ptr(offsets), R, E, H, I, fmt, _ptr(w_gateup), _ptr(s_gateup),
+                                  _ptr(h), _ptr(dev_status), _stream(stream))
+    _check("moe_expert_gateup", st)
+
+
+def moe_expert_down(h, offsets, E, H, I, w_down, y_perm, dev_status, fmt=MOE_W_BF16, s_down=None, stream=None):
+    R = h.shape[0]
+    st = load().moe_expert_down(_ptr(h), _ptr(offsets), R, E, H, I, fmt, _ptr(w_down), _ptr(s_down),
+                                _ptr(y_perm), _ptr(dev_status), _stream(stream))
+    _check("moe_expert_down", st)
+
+
+def moe_grouped_swiglu(x_perm, offsets, E, H, I, w_gateup, w_down, h, y_perm, dev_status, fmt=MOE_W_BF16,
+                       s_gateup=None, s_down=None, stream=None):
+    R = x_perm.shape[0]
+    st = load().moe_grouped_swiglu(_ptr(x_perm), _ptr(offsets), R, E, H, I, fmt, _ptr(w_gateup), _ptr(s_gateup),
+                                   _ptr(w_down), _ptr(s_down), _ptr(h), _ptr(y_perm), _ptr(dev_status),
+                                   _stream(stream))
+    _check("moe_grouped_swiglu", st)
+
+
+def moe_combine(y_perm, inv_perm, topk_w, residual, out_bf16, out_f32, dev_status, stream=None):
+    T, k = topk_w.shape
+    H = y_perm.shape[1]
+    st = load().moe_combine(_ptr(y_perm), _ptr(inv_perm), _ptr(topk_w), T, k, H, _ptr(residual), _ptr(out_bf16),
+                            _ptr(out_f32), _ptr(dev_status), _stream(stream))
+    _check("moe_combine", st)
+
+
+def route_block_dedup(ids, E, block, H, I, mask, U, bytes2, bytes4, dev_status, stream=None):
+    L, Tt, k = ids.shape
+    st = load().route_block_dedup(_ptr(ids), L, Tt, k, E, block, H, I, _ptr(mask), _ptr(U), _ptr(bytes2),
+                                  _ptr(bytes4), _ptr(dev_status), _stream(stream))
+    _check("route_block_dedup", st)
+
+
+def moe_rmsnorm(x, gamma, eps, out, stream=None):
+    T, H = x.shape
+    st = load().moe_rmsnorm(_ptr(x), _ptr(gamma), float(eps), T, H, _ptr(out), _stream(stream))
+    _check("moe_rmsnorm", st)

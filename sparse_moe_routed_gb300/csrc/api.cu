@@ -1,0 +1,224 @@
+// extern "C" boundary of libmoe: host-side admission of every argument, then
+// the kernel launches on the caller's stream.  Nothing is enqueued and nothing
+// is written unless every check passes (AFN-010 "One bank flip is enough:
+// make the whole inference chunk transactional", section "The publication
+// model": output stays caller-private while work is fallible; AFN-001, section
+// "Phase 3: reject before the GPU exists": admission happens before any GPU
+// work).  Declarations and argument contracts: include/moe.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev < 0 || dev >= 64) return -1;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+}  // namespace moe
+
+namespace {
+
+inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool a4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline bool a8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ECUDA; }
+
+// Geometry envelope shared by the layer calls.
+inline moe_status check_geometry(int H, int E, int k, int I_or_zero) {
+  if (H <= 0 || E <= 0 || k <= 0 || I_or_zero < 0) return MOE_ESHAPE;
+  if (k > moe::kMaxK || k > E || E > moe::kMaxE) return MOE_ENOTSUP;
+  if (H % 128 != 0 || H > 16384) return MOE_ENOTSUP;
+  if (I_or_zero > 0 && (I_or_zero % 64 != 0 || I_or_zero > 16384)) return MOE_ENOTSUP;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return 100; }
+
+const char* moe_status_str(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_EINVAL: return "MOE_EINVAL: null or misaligned pointer, or bad enum";
+    case MOE_ESHAPE: return "MOE_ESHAPE: inconsistent or non-positive sizes";
+    case MOE_ERANGE: return "MOE_ERANGE: value out of range";
+    case MOE_ECUDA: return "MOE_ECUDA: a CUDA call failed";
+    case MOE_ENOTSUP: return "MOE_ENOTSUP: geometry outside the supported envelope";
+    case MOE_EDEVICE_TIMEOUT: return "MOE_EDEVICE_TIMEOUT: a bounded device wait ran out";
+    case MOE_EWORKSPACE: return "MOE_EWORKSPACE: workspace missing or too small";
+  }
+  return "MOE_UNKNOWN";
+}
+
+int moe_device_sm_count(void) { return moe::sm_count(); }
+
+size_t moe_route_workspace_size(int T, int E) {
+  if (T <= 0 || E <= 0) return 0;
+  const size_t logits = static_cast<size_t>(T) * static_cast<size_t>(E) * sizeof(float);
+  return (logits + 255) & ~static_cast<size_t>(255);
+}
+
+moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E, int k,
+                     int32_t* topk_ids, float* topk_w, float* gap, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  if (T < 0) return MOE_ESHAPE;
+  moe_status g = check_geometry(H, E, k, 0);
+  if (g != MOE_OK) return g;
+  if (static_cast<long long>(T) * k >= (1LL << 31)) return MOE_ENOTSUP;
+  if (!x || !w_router || !topk_ids || !topk_w) return MOE_EINVAL;
+  if (!a16(x) || !a16(w_router) || !a4(topk_ids) || !a4(topk_w)) return MOE_EINVAL;
+  if ((bias && !a4(bias)) || (gap && !a4(gap))) return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  if (!workspace || !a16(workspace)) return workspace ? MOE_EINVAL : MOE_EWORKSPACE;
+  if (workspace_bytes < moe_route_workspace_size(T, E)) return MOE_EWORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* logits = static_cast<float*>(workspace);
+  cudaError_t e;
+  if (T > 64 && E % 128 == 0)
+    e = moe::launch_grouped_gemm(moe::GemmKind::kRouter, w_router, x, nullptr, 1, T, H, 0, E, logits, nullptr, st);
+  else
+    e = moe::launch_router_logits_simt(x, w_router, T, H, E, logits, st);
+  if (e != cudaSuccess) return MOE_ECUDA;
+  return cuda_status(moe::launch_topk(logits, bias, T, E, k, topk_ids, topk_w, gap, st));
+}
+
+moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, const uint16_t* x, int H, int32_t* counts,
+                       int32_t* offsets, int32_t* perm, int32_t* inv_perm, uint16_t* x_perm, int32_t* dev_status,
+                       void* stream) {
+  if (T < 0 || k <= 0 || E <= 0) return MOE_ESHAPE;
+  if (k > moe::kMaxK || k > E || E > moe::kMaxE) return MOE_ENOTSUP;
+  if (static_cast<long long>(T) * k >= (1LL << 31)) return MOE_ENOTSUP;
+  if (!topk_ids || !counts || !offsets || !perm || !inv_perm || !dev_status) return MOE_EINVAL;
+  if (!a4(topk_ids) || !a4(counts) || !a4(offsets) || !a4(perm) || !a4(inv_perm) || !a4(dev_status))
+    return MOE_EINVAL;
+  if (x_perm) {
+    if (!x) return MOE_EINVAL;
+    if (H <= 0) return MOE_ESHAPE;
+    if (H % 128 != 0 || H > 16384) return MOE_ENOTSUP;
+    if (!a16(x) || !a16(x_perm)) return MOE_EINVAL;
+  }
+  if (T == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int R = T * k;
+  cudaError_t e = moe::launch_permute(topk_ids, R, k, E, counts, offsets, perm, inv_perm, dev_status, st);
+  if (e != cudaSuccess) return MOE_ECUDA;
+  if (x_perm) {
+    e = moe::launch_gather_rows(x, perm, R, k, T, H, x_perm, st);
+    if (e != cudaSuccess) return MOE_ECUDA;
+  }
+  return MOE_OK;
+}
+
+static moe_status check_expert_args(int R, int E, int H, int I, int fmt) {
+  if (R < 0 || E <= 0 || H <= 0 || I <= 0) return MOE_ESHAPE;
+  if (fmt != MOE_W_BF16 && fmt != MOE_W_INT4_G64) return MOE_EINVAL;
+  if (fmt != MOE_W_BF16) return MOE_ENOTSUP;
+  if (E > moe::kMaxE) return MOE_ENOTSUP;
+  if (H % 128 != 0 || H > 16384 || I % 64 != 0 || I > 16384) return MOE_ENOTSUP;
+  if (static_cast<long long>(E) * H >= (1LL << 31)) return MOE_ENOTSUP;
+  return MOE_OK;
+}
+
+moe_status moe_expert_gateup(const uint16_t* x_perm, const int32_t* offsets, int R, int E, int H, int I, int fmt,
+                             const void* w_gateup, const uint16_t* s_gateup, uint16_t* h, int32_t* dev_status,
+                             void* stream) {
+  moe_status c = check_expert_args(R, E, H, I, fmt);
+  if (c != MOE_OK) return c;
+  if (!x_perm || !offsets || !w_gateup || !h || !dev_status) return MOE_EINVAL;
+  if (s_gateup) return MOE_EINVAL;
+  if (!a16(x_perm) || !a16(w_gateup) || !a16(h) || !a4(offsets) || !a4(dev_status)) return MOE_EINVAL;
+  if (R == 0) return MOE_OK;
+  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kGateUp, w_gateup, x_perm, offsets, E, R, H, I, 0, h,
+                                           dev_status, static_cast<cudaStream_t>(stream));
+  return cuda_status(e);
+}
+
+moe_status moe_expert_down(const uint16_t* h, const int32_t* offsets, int R, int E, int H, int I, int fmt,
+                           const void* w_down, const uint16_t* s_down, float* y_perm, int32_t* dev_status,
+                           void* stream) {
+  moe_status c = check_expert_args(R, E, H, I, fmt);
+  if (c != MOE_OK) return c;
+  if (!h || !offsets || !w_down || !y_perm || !dev_status) return MOE_EINVAL;
+  if (s_down) return MOE_EINVAL;
+  if (!a16(h) || !a16(w_down) || !a16(y_perm) || !a4(offsets) || !a4(dev_status)) return MOE_EINVAL;
+  if (R == 0) return MOE_OK;
+  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kDown, w_down, h, offsets, E, R, H, I, 0, y_perm,
+                                           dev_status, static_cast<cudaStream_t>(stream));
+  return cuda_status(e);
+}
+
+moe_status moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets, int R, int E, int H, int I, int fmt,
+                              const void* w_gateup, const uint16_t* s_gateup, const void* w_down,
+                              const uint16_t* s_down, uint16_t* h, float* y_perm, int32_t* dev_status,
+                              void* stream) {
+  moe_status c = check_expert_args(R, E, H, I, fmt);
+  if (c != MOE_OK) return c;
+  if (!x_perm || !offsets || !w_gateup || !w_down || !h || !y_perm || !dev_status) return MOE_EINVAL;
+  if (s_gateup || s_down) return MOE_EINVAL;
+  if (!a16(x_perm) || !a16(w_gateup) || !a16(w_down) || !a16(h) || !a16(y_perm) || !a4(offsets) ||
+      !a4(dev_status))
+    return MOE_EINVAL;
+  if (R == 0) return MOE_OK;
+  c = moe_expert_gateup(x_perm, offsets, R, E, H, I, fmt, w_gateup, s_gateup, h, dev_status, stream);
+  if (c != MOE_OK) return c;
+  return moe_expert_down(h, offsets, R, E, H, I, fmt, w_down, s_down, y_perm, dev_status, stream);
+}
+
+moe_status moe_combine(const float* y_perm, const int32_t* inv_perm, const float* topk_w, int T, int k, int H,
+                       const float* residual, uint16_t* out_bf16, float* out_f32, int32_t* dev_status,
+                       void* stream) {
+  if (T < 0 || k <= 0 || H <= 0) return MOE_ESHAPE;
+  if (k > moe::kMaxK || H % 128 != 0 || H > 16384) return MOE_ENOTSUP;
+  if (static_cast<long long>(T) * k >= (1LL << 31)) return MOE_ENOTSUP;
+  if (!y_perm || !inv_perm || !topk_w || (!out_bf16 && !out_f32)) return MOE_EINVAL;
+  if (!a16(y_perm) || !a4(inv_perm) || !a4(topk_w)) return MOE_EINVAL;
+  if ((residual && !a16(residual)) || (out_bf16 && !a16(out_bf16)) || (out_f32 && !a16(out_f32)) ||
+      (dev_status && !a4(dev_status)))
+    return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  return cuda_status(moe::launch_combine(y_perm, inv_perm, topk_w, T, k, H, T * k, residual, out_bf16, out_f32,
+                                         dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status route_block_dedup(const int32_t* ids, int L, int T_tot, int k, int E, int block, int H, int I,
+                             uint32_t* mask, int32_t* U, int64_t* bytes2, int64_t* bytes4, int32_t* dev_status,
+                             void* stream) {
+  if (L <= 0 || T_tot < 0 || k <= 0 || E <= 0 || block <= 0 || H <= 0 || I <= 0) return MOE_ESHAPE;
+  if (k > moe::kMaxK || E > moe::kMaxE) return MOE_ENOTSUP;
+  if (static_cast<long long>(L) * T_tot * k >= (1LL << 31)) return MOE_ENOTSUP;
+  if (!ids || !mask || !U || !bytes2 || !bytes4 || !dev_status) return MOE_EINVAL;
+  if (!a4(ids) || !a4(mask) || !a4(U) || !a8(bytes2) || !a8(bytes4) || !a4(dev_status)) return MOE_EINVAL;
+  if (T_tot == 0) return MOE_OK;
+  const long long P = 3LL * H * I;
+  return cuda_status(moe::launch_dedup(ids, L, T_tot, k, E, block, P, mask, U, bytes2, bytes4, dev_status,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_rmsnorm(const float* x, const float* gamma, float eps, int T, int H, uint16_t* out, void* stream) {
+  if (T < 0 || H <= 0) return MOE_ESHAPE;
+  if (H % 128 != 0 || H > 16384) return MOE_ENOTSUP;
+  if (!(eps >= 0.0f)) return MOE_EINVAL;
+  if (!x || !out) return MOE_EINVAL;
+  if (!a16(x) || !a16(out) || (gamma && !a16(gamma))) return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  return cuda_status(moe::launch_rmsnorm(x, gamma, eps, T, H, out, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

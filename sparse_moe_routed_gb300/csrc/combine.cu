@@ -1,0 +1,133 @@
+// Weighted combine in route-rank order, and the zero-centred RMSNorm that
+// feeds a residual stack layer.
+//
+// AFN-019 "Hide SSD misses before the router knows they exist", section
+// "Hypothesis H4: ExpertMajor should stream as a wavefront, not a barrier":
+// expert results may be produced in any order into separate slots, but the
+// final weighted sum follows a deterministic route-rank order.  Here every
+// output element is summed by one thread over j = 0..k-1 in order, so the
+// result is bit-identical from run to run whatever order the experts ran in.
+//
+// AFN-001 "Porting Qwen3.8-Flash-Next to Hebrus", section "Phase 1: separate
+// math from acceleration": zero-centred RMS normalisation (gain 1 + gamma).
+//
+// Both kernels are HBM/L2-bound gathers: 16-byte loads, one CTA per
+// (token, 512 columns) for the combine, one CTA per token row for RMSNorm.
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kCombineThreads = 128;  // x 4 floats = 512 columns per CTA
+
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const float* __restrict__ w, int T,
+                   int k, int H, int R, const float* __restrict__ residual, uint16_t* __restrict__ out_bf16,
+                   float* __restrict__ out_f32, int32_t* status) {
+  __shared__ int slot[kMaxK];
+  __shared__ float wt[kMaxK];
+  const int t = blockIdx.y;
+  if (threadIdx.x < k) {
+    int s = inv[static_cast<size_t>(t) * k + threadIdx.x];
+    if (s < 0 || s >= R) s = -1;
+    slot[threadIdx.x] = s;
+    wt[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
+  }
+  __syncthreads();
+  const int c4 = blockIdx.x * kCombineThreads + threadIdx.x;
+  if (c4 * 4 >= H) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  bool bad = false;
+  for (int j = 0; j < k; ++j) {
+    const int s = slot[j];
+    if (s < 0) {
+      bad = true;
+      continue;
+    }
+    const float4 v = reinterpret_cast<const float4*>(y + static_cast<size_t>(s) * H)[c4];
+    const float wj = wt[j];
+    acc.x = fmaf(wj, v.x, acc.x);
+    acc.y = fmaf(wj, v.y, acc.y);
+    acc.z = fmaf(wj, v.z, acc.z);
+    acc.w = fmaf(wj, v.w, acc.w);
+  }
+  if (residual) {
+    const float4 r = reinterpret_cast<const float4*>(residual + static_cast<size_t>(t) * H)[c4];
+    acc.x += r.x;
+    acc.y += r.y;
+    acc.z += r.z;
+    acc.w += r.w;
+  }
+  if (status && (bad || !isfinite(acc.x) || !isfinite(acc.y) || !isfinite(acc.z) || !isfinite(acc.w)))
+    set_status(status, bad ? MOE_DEV_BAD_EXPERT : MOE_DEV_NONFINITE);
+  if (out_f32) reinterpret_cast<float4*>(out_f32 + static_cast<size_t>(t) * H)[c4] = acc;
+  if (out_bf16) {
+    uint2 pk;
+    pk.x = static_cast<uint32_t>(f32_to_bf16(acc.x)) | (static_cast<uint32_t>(f32_to_bf16(acc.y)) << 16);
+    pk.y = static_cast<uint32_t>(f32_to_bf16(acc.z)) | (static_cast<uint32_t>(f32_to_bf16(acc.w)) << 16);
+    reinterpret_cast<uint2*>(out_bf16 + static_cast<size_t>(t) * H)[c4] = pk;
+  }
+}
+
+constexpr int kNormThreads = 256;
+
+__global__ void __launch_bounds__(kNormThreads)
+    rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ gamma, float eps, int H,
+                   uint16_t* __restrict__ out) {
+  __shared__ float part[kNormThreads / 32];
+  const int t = blockIdx.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(t) * H);
+  const int n4 = H / 4;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < n4; c += kNormThreads) {
+    const float4 v = xr[c];
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) tot += part[i];
+  const float r = 1.0f / sqrtf(tot / static_cast<float>(H) + eps);
+  for (int c = threadIdx.x; c < n4; c += kNormThreads) {
+    const float4 v = xr[c];
+    float g[4] = {0.f, 0.f, 0.f, 0.f};
+    if (gamma) {
+      const float4 gv = reinterpret_cast<const float4*>(gamma)[c];
+      g[0] = gv.x; g[1] = gv.y; g[2] = gv.z; g[3] = gv.w;
+    }
+    uint2 pk;
+    pk.x = static_cast<uint32_t>(f32_to_bf16(v.x * r * (1.f + g[0]))) |
+           (static_cast<uint32_t>(f32_to_bf16(v.y * r * (1.f + g[1]))) << 16);
+    pk.y = static_cast<uint32_t>(f32_to_bf16(v.z * r * (1.f + g[2]))) |
+           (static_cast<uint32_t>(f32_to_bf16(v.w * r * (1.f + g[3]))) << 16);
+    reinterpret_cast<uint2*>(out + static_cast<size_t>(t) * H)[c] = pk;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int k, int H, int R,
+                           const float* residual, uint16_t* out_bf16, float* out_f32, int32_t* st_word,
+                           cudaStream_t st) {
+  const dim3 grid((H / 4 + kCombineThreads - 1) / kCombineThreads, T);
+  combine_kernel<<<grid, kCombineThreads, 0, st>>>(y, inv, w, T, k, H, R, residual, out_bf16, out_f32, st_word);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, int T, int H, uint16_t* out,
+                           cudaStream_t st) {
+  rmsnorm_kernel<<<T, kNormThreads, 0, st>>>(x, gamma, eps, H, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,48 @@
+// Internal launchers of libmoe (host side).  Each returns the CUDA error of
+// its launch; the extern "C" layer in api.cu validates arguments first.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+int sm_count();
+
+// route.cu
+cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* wr, int T, int H, int E,
+                                      float* logits, cudaStream_t st);
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
+                        float* w, float* gap, cudaStream_t st);
+
+// permute.cu
+cudaError_t launch_permute(const int32_t* ids, int R, int k, int E, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* st_word,
+                           cudaStream_t st);
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int R, int k, int T, int H,
+                               uint16_t* x_perm, cudaStream_t st);
+
+// gemm.cu (tcgen05 grouped GEMM)
+enum class GemmKind { kGateUp = 0, kDown = 1, kRouter = 2 };
+// Grouped weight-stationary GEMM: for every (segment e, 128-row weight block,
+// chunk of token rows) tile, D = W_e[rows] . B[rows of segment]^T on the
+// tensor cores; epilogue per kind.  Returns cudaErrorInvalidValue when a
+// tensor map cannot be encoded.
+cudaError_t launch_grouped_gemm(GemmKind kind, const void* w, const uint16_t* b_rows,
+                                const int32_t* offsets, int E, int R, int H, int I,
+                                int router_E, void* out, int32_t* st_word, cudaStream_t st);
+
+// combine.cu
+cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int k, int H,
+                           int R, const float* residual, uint16_t* out_bf16, float* out_f32,
+                           int32_t* st_word, cudaStream_t st);
+cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, int T, int H,
+                           uint16_t* out, cudaStream_t st);
+
+// dedup.cu
+cudaError_t launch_dedup(const int32_t* ids, int L, int Ttot, int k, int E, int B, long long P,
+                         uint32_t* mask, int32_t* U, int64_t* bytes2, int64_t* bytes4,
+                         int32_t* st_word, cudaStream_t st);
+
+}  // namespace moe

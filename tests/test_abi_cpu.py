@@ -1,0 +1,157 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load, export every function include/moe.h declares, and
+reject bad arguments on the host before anything is enqueued.  The rejection
+cases here use placeholder addresses and every one of them must be refused by
+host admission; with a GPU present these run in test_gpu_negative.py instead,
+on real buffers.
+"""
+import ctypes as C
+
+import pytest
+import torch
+
+from sparse_moe_routed_gb300 import _lib
+
+pytestmark = pytest.mark.skipif(torch.cuda.is_available(), reason="placeholder pointers: CPU-only host checks")
+
+P = C.c_void_p(1 << 20)      # 16-byte aligned placeholder address
+PM = C.c_void_p((1 << 20) + 2)  # misaligned placeholder address
+NUL = None
+
+
+def lib():
+    return _lib.load()
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    L = lib()
+    names = _lib.declared_functions()
+    assert len(names) == 12
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.moe_abi_version() == 100
+    assert L.moe_status_str(0).decode() == "MOE_OK"
+    assert L.moe_status_str(5).decode().startswith("MOE_ENOTSUP")
+
+
+def test_exports_match_header_exactly():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib._build.LIB], capture_output=True, text=True).stdout
+    exported = sorted(l.split()[-1] for l in out.splitlines() if " T " in l)
+    assert exported == _lib.declared_functions()
+
+
+def test_workspace_size():
+    L = lib()
+    assert L.moe_route_workspace_size(16, 512) == 16 * 512 * 4
+    assert L.moe_route_workspace_size(3, 7) == 256
+    assert L.moe_route_workspace_size(0, 512) == 0
+
+
+def _route(**kw):
+    a = dict(x=P, wr=P, bias=NUL, T=16, H=2560, E=512, k=10, ids=P, w=P, gap=NUL, ws=P,
+             wsb=16 * 512 * 4, st=NUL)
+    a.update(kw)
+    return lib().moe_route(a["x"], a["wr"], a["bias"], a["T"], a["H"], a["E"], a["k"], a["ids"], a["w"],
+                           a["gap"], a["ws"], a["wsb"], a["st"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=NUL), _lib.MOE_EINVAL),
+    (dict(wr=NUL), _lib.MOE_EINVAL),
+    (dict(ids=NUL), _lib.MOE_EINVAL),
+    (dict(w=NUL), _lib.MOE_EINVAL),
+    (dict(x=PM), _lib.MOE_EINVAL),
+    (dict(T=-1), _lib.MOE_ESHAPE),
+    (dict(H=0), _lib.MOE_ESHAPE),
+    (dict(H=2500), _lib.MOE_ENOTSUP),
+    (dict(k=0), _lib.MOE_ESHAPE),
+    (dict(k=33), _lib.MOE_ENOTSUP),
+    (dict(E=8, k=10), _lib.MOE_ENOTSUP),
+    (dict(E=1025), _lib.MOE_ENOTSUP),
+    (dict(ws=NUL), _lib.MOE_EWORKSPACE),
+    (dict(wsb=16 * 512 * 4 - 1), _lib.MOE_EWORKSPACE),
+])
+def test_route_rejections(kw, code):
+    assert _route(**kw) == code
+
+
+def test_route_zero_tokens_is_noop():
+    assert _route(T=0, ws=NUL, wsb=0) == _lib.MOE_OK
+
+
+def _permute(**kw):
+    a = dict(ids=P, T=16, k=10, E=512, x=P, H=2560, counts=P, offsets=P, perm=P, inv=P, xp=P, st=P)
+    a.update(kw)
+    return lib().moe_permute(a["ids"], a["T"], a["k"], a["E"], a["x"], a["H"], a["counts"], a["offsets"],
+                             a["perm"], a["inv"], a["xp"], a["st"], NUL)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ids=NUL), _lib.MOE_EINVAL),
+    (dict(st=NUL), _lib.MOE_EINVAL),
+    (dict(x=NUL), _lib.MOE_EINVAL),
+    (dict(xp=PM), _lib.MOE_EINVAL),
+    (dict(T=-3), _lib.MOE_ESHAPE),
+    (dict(k=11, E=10), _lib.MOE_ENOTSUP),
+    (dict(H=100), _lib.MOE_ENOTSUP),
+    (dict(E=2048), _lib.MOE_ENOTSUP),
+    (dict(T=1 << 28, k=10), _lib.MOE_ENOTSUP),
+])
+def test_permute_rejections(kw, code):
+    assert _permute(**kw) == code
+
+
+def _gateup(**kw):
+    a = dict(xp=P, off=P, R=160, E=512, H=2560, I=640, fmt=0, w=P, s=NUL, h=P, st=P)
+    a.update(kw)
+    return lib().moe_expert_gateup(a["xp"], a["off"], a["R"], a["E"], a["H"], a["I"], a["fmt"], a["w"], a["s"],
+                                   a["h"], a["st"], NUL)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(xp=NUL), _lib.MOE_EINVAL),
+    (dict(off=NUL), _lib.MOE_EINVAL),
+    (dict(h=PM), _lib.MOE_EINVAL),
+    (dict(fmt=7), _lib.MOE_EINVAL),
+    (dict(s=P), _lib.MOE_EINVAL),
+    (dict(R=-1), _lib.MOE_ESHAPE),
+    (dict(I=600), _lib.MOE_ENOTSUP),
+    (dict(H=2496), _lib.MOE_ENOTSUP),
+])
+def test_gateup_rejections(kw, code):
+    assert _gateup(**kw) == code
+
+
+def test_expert_zero_rows_is_noop():
+    assert _gateup(R=0) == _lib.MOE_OK
+
+
+def test_combine_rejections():
+    L = lib()
+    assert L.moe_combine(P, P, P, 16, 10, 2560, NUL, NUL, NUL, NUL, NUL) == _lib.MOE_EINVAL
+    assert L.moe_combine(PM, P, P, 16, 10, 2560, NUL, P, NUL, NUL, NUL) == _lib.MOE_EINVAL
+    assert L.moe_combine(P, P, P, 16, 40, 2560, NUL, P, NUL, NUL, NUL) == _lib.MOE_ENOTSUP
+    assert L.moe_combine(P, P, P, 0, 10, 2560, NUL, P, NUL, NUL, NUL) == _lib.MOE_OK
+
+
+def test_dedup_rejections():
+    L = lib()
+    assert L.route_block_dedup(P, 48, 512, 10, 512, 0, 2560, 640, P, P, P, P, P, NUL) == _lib.MOE_ESHAPE
+    assert L.route_block_dedup(NUL, 48, 512, 10, 512, 4, 2560, 640, P, P, P, P, P, NUL) == _lib.MOE_EINVAL
+    assert L.route_block_dedup(P, 48, 512, 10, 512, 4, 2560, 640, P, P, C.c_void_p((1 << 20) + 4), P, P,
+                               NUL) == _lib.MOE_EINVAL
+    assert L.route_block_dedup(P, 48, 512, 10, 4096, 4, 2560, 640, P, P, P, P, P, NUL) == _lib.MOE_ENOTSUP
+
+
+def test_rmsnorm_rejections():
+    L = lib()
+    assert L.moe_rmsnorm(P, NUL, C.c_float(-1.0), 4, 2560, P, NUL) == _lib.MOE_EINVAL
+    assert L.moe_rmsnorm(P, NUL, C.c_float(1e-6), 4, 2500, P, NUL) == _lib.MOE_ENOTSUP
+    assert L.moe_rmsnorm(NUL, NUL, C.c_float(1e-6), 4, 2560, P, NUL) == _lib.MOE_EINVAL
+
+
+def test_no_device_gives_cuda_error_not_a_crash():
+    """Past admission, a machine without a GPU gets MOE_ECUDA back."""
+    assert lib().moe_device_sm_count() == -1

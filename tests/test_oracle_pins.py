@@ -331,3 +331,22 @@ def test_dedup_brute_force_sets(B):
 def test_dedup_rejects_bad_id():
     with pytest.raises(ValueError):
         oracle.dedup(np.array([[[0, 9]]], np.int32), 9, 1, 8, 8)
+
+
+def test_combine_alone_linearity_and_hand_case():
+    """Constant expert outputs v: out = v * sum(w) = v; a 2-route case by hand."""
+    rng = np.random.default_rng(8)
+    T, k, H = 3, 4, 8
+    ids = np.array([[0, 1, 2, 3], [3, 2, 1, 0], [1, 3, 0, 2]], np.int32)
+    _, _, perm, inv = oracle.permute(ids, 4)
+    v = rng.standard_normal(H).astype(np.float32)
+    y = np.tile(v, (T * k, 1))
+    w = np.full((T, k), 0.25, np.float32)
+    out = oracle.combine(y, inv, w)
+    assert np.allclose(out, np.tile(v, (T, 1)), rtol=1e-6)
+    y2 = np.zeros((2, 2), np.float32)
+    y2[0] = [1.0, 2.0]
+    y2[1] = [10.0, 20.0]
+    out2 = oracle.combine(y2, np.array([1, 0], np.int32), np.array([[0.75, 0.25]], np.float32),
+                          residual=np.array([[100.0, 200.0]], np.float32))
+    assert np.allclose(out2[0], [100 + 0.75 * 10 + 0.25 * 1, 200 + 0.75 * 20 + 0.25 * 2])
