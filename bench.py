@@ -46,7 +46,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode", choices=["decode", "prefill"])
     ap.add_argument("--layers", type=int, default=0, help="distinct layer weight sets rotated (0 = auto)")
+    ap.add_argument("--experts", type=int, default=0, help="override the expert count (small profiling case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -245,6 +247,9 @@ def main():
     import workloads as wl
 
     cfg = wl.CONFIGS[args.config]
+    if args.experts:
+        from dataclasses import replace
+        cfg = replace(cfg, E=args.experts)
     NL = args.layers or (8 if args.config == "decode" else 1)
     layers, xs, host_w = [], [], None
     for l in range(NL):
@@ -298,6 +303,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
+    t_issue0 = time.perf_counter()
     e_start.record(st)
     for i in range(K):
         L = layers[i % NL]
@@ -311,6 +317,7 @@ def main():
         ev_d1[i].record(st)
         L.combine(cfg.T)
     e_end.record(st)
+    t_issue1 = time.perf_counter()
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
@@ -343,7 +350,7 @@ def main():
 
     # e2e: host buffers in, host result out, through the public layer call
     e2e = None
-    if rank == 0 or world > 1:
+    if not args.no_e2e:
         x_host = [xs[l].cpu().pin_memory() for l in range(NL)]
         out_host = torch.empty((cfg.T, H), dtype=torch.bfloat16).pin_memory()
         Ke = max(10, min(K, 2000))
@@ -392,6 +399,7 @@ def main():
                            "tflops": flops_step / (step_ms / 1e3) / 1e12,
                            "frac_tensor": flops_step / (step_ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
                            "down_avg_us": dn_avg * 1e3},
+        "host_issue_us_per_step": 1e6 * (t_issue1 - t_issue0) / K,
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": 7 * K,
     }

@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(kCombineThreads)
                    float* __restrict__ out_f32, int32_t* status) {
   __shared__ int slot[kMaxK];
   __shared__ float wt[kMaxK];
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.y;
   if (threadIdx.x < k) {
     int s = inv[static_cast<size_t>(t) * k + threadIdx.x];
@@ -79,6 +81,8 @@ __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ gamma, float eps, int H,
                    uint16_t* __restrict__ out) {
   __shared__ float part[kNormThreads / 32];
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(t) * H);
   const int n4 = H / 4;
@@ -120,14 +124,13 @@ cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, i
                            const float* residual, uint16_t* out_bf16, float* out_f32, int32_t* st_word,
                            cudaStream_t st) {
   const dim3 grid((H / 4 + kCombineThreads - 1) / kCombineThreads, T);
-  combine_kernel<<<grid, kCombineThreads, 0, st>>>(y, inv, w, T, k, H, R, residual, out_bf16, out_f32, st_word);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, st, y, inv, w, T, k, H, R, residual, out_bf16,
+                    out_f32, st_word);
 }
 
 cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, int T, int H, uint16_t* out,
                            cudaStream_t st) {
-  rmsnorm_kernel<<<T, kNormThreads, 0, st>>>(x, gamma, eps, H, out);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_kernel, dim3(T), dim3(kNormThreads), 0, st, x, gamma, eps, H, out);
 }
 
 }  // namespace moe

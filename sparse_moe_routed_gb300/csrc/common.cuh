@@ -33,4 +33,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  Every kernel of the layer is launched with
+// programmatic stream serialization: its prologue (barrier init, TMEM
+// allocation, reads of constant weights) may overlap the previous kernel's
+// tail, and pdl_wait() blocks until every earlier kernel in the stream has
+// completed and its writes are visible.  Each kernel calls pdl_wait() before
+// its first read of data produced upstream and before its first global write.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace moe

@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kDedupThreads)
   const int t1 = min(Ttot, t0 + B);
   const int n = (t1 - t0) * k;
   if (threadIdx.x == 0) bad = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   for (int l = 0; l < L; ++l) {
     const int32_t* src = ids + (static_cast<size_t>(l) * Ttot + t0) * k;
@@ -83,8 +85,8 @@ __global__ void __launch_bounds__(kDedupThreads)
 cudaError_t launch_dedup(const int32_t* ids, int L, int Ttot, int k, int E, int B, long long P, uint32_t* mask,
                          int32_t* U, int64_t* bytes2, int64_t* bytes4, int32_t* st_word, cudaStream_t st) {
   const int nb = (Ttot + B - 1) / B;
-  dedup_kernel<<<nb, kDedupThreads, 0, st>>>(ids, L, Ttot, k, E, B, P, mask, U, bytes2, bytes4, st_word);
-  return cudaGetLastError();
+  return launch_pdl(dedup_kernel, dim3(nb), dim3(kDedupThreads), 0, st, ids, L, Ttot, k, E, B, P, mask, U, bytes2,
+                    bytes4, st_word);
 }
 
 }  // namespace moe

@@ -56,8 +56,9 @@ struct Cfg {
   static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
   static constexpr int kBarBytes = (2 * kStages + 5) * 8;
   static constexpr int kMiscBytes = 16;
+  // tile prefix [E+1] and clamped segment offsets [E+1]
   static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + kBarBytes + kMiscBytes + (kMaxE + 1) * 4;
+      1024 + kStages * kStageBytes + kBarBytes + kMiscBytes + 2 * (kMaxE + 1) * 4;
   static_assert(kBBytes % 1024 == 0, "B stage must keep 1024-byte alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -146,36 +147,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(&misc[0])), C::kTmemCols);
     ptx::tmem_relinquish();
   }
-  // Tile prefix over segments (warp 0).  Segment bounds are clamped into
-  // [0, R] so that corrupt offsets can never address rows outside the buffers.
+  // Everything above overlaps the previous kernel's tail; from here on the
+  // kernel reads upstream data (offsets, activation rows) and writes outputs.
+  pdl_wait();
+  pdl_trigger();
+  // Segment offsets into shared memory, clamped into [0, R] (a segment's
+  // length is never negative), so that corrupt offsets can never address rows
+  // outside the buffers; then the per-segment tile prefix (warp 0).
+  int* soff = prefix + (kMaxE + 1);
+  for (int i = threadIdx.x; i <= E; i += blockDim.x)
+    soff[i] = dense ? (i == 0 ? 0 : p.R) : min(max(p.offsets[i], 0), p.R);
+  __syncthreads();
   if (warp == 0) {
-    if (dense) {
-      if (lane == 0) {
-        prefix[0] = 0;
-        prefix[1] = ((p.R + NMAX - 1) / NMAX) * p.mblocks;
-      }
-    } else {
-      int running = 0;
-      for (int e0 = 0; e0 < E; e0 += 32) {
-        const int e = e0 + lane;
-        int n = 0;
-        if (e < E) {
-          int a = min(max(p.offsets[e], 0), p.R);
-          int b = min(max(p.offsets[e + 1], a), p.R);
-          n = b - a;
-        }
-        const int tiles = ((n + NMAX - 1) / NMAX) * p.mblocks;
-        int incl = tiles;
+    int running = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      int n = 0;
+      if (e < E) n = max(soff[e + 1] - soff[e], 0);
+      const int tiles = ((n + NMAX - 1) / NMAX) * p.mblocks;
+      int incl = tiles;
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, d);
-          if (lane >= d) incl += y;
-        }
-        if (e < E) prefix[e] = running + incl - tiles;
-        running += __shfl_sync(0xffffffffu, incl, 31);
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
       }
-      if (lane == 0) prefix[E] = running;
+      if (e < E) prefix[e] = running + incl - tiles;
+      running += __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (lane == 0) prefix[E] = running;
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -184,18 +183,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = misc[0];
   const int total = prefix[E];
 
-  // Segment starts/lengths: re-derived per tile from offsets (clamped).
-  auto seg_bounds = [&](int e, int& start, int& len) {
-    if (dense) {
-      start = 0;
-      len = p.R;
-    } else {
-      const int a = min(max(p.offsets[e], 0), p.R);
-      const int b = min(max(p.offsets[e + 1], a), p.R);
-      start = a;
-      len = b - a;
-    }
-  };
   auto tile_of = [&](int t) {
     int lo = 0, hi = E;
     while (hi - lo > 1) {
@@ -204,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int local = t - prefix[lo];
     const int chunk = local / p.mblocks;
-    int start, len;
-    seg_bounds(lo, start, len);
+    const int start = soff[lo];
+    const int len = max(soff[lo + 1] - start, 0);
     Tile tl;
     tl.e = lo;
     tl.mb = local - chunk * p.mblocks;
@@ -416,8 +403,7 @@ cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args
   if (e != cudaSuccess) return e;
   const int grid = sm_count();
   if (grid <= 0) return cudaErrorNoDevice;
-  kern<<<grid, kThreads, Cfg<NMAX>::kSmemBytes, st>>>(a, b, args);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), Cfg<NMAX>::kSmemBytes, st, a, b, args);
 }
 
 template <int KIND>

@@ -6,7 +6,7 @@
 // flat route order r = t*k + j, which makes the grouping deterministic and
 // comparable bit for bit.
 //
-// One CTA of 32 warps.  Warp w owns a contiguous run of routes.  Pass 1: each
+// One CTA of up to 32 route-owning warps.  Warp w owns a contiguous run of routes.  Pass 1: each
 // warp counts its routes per expert with __match_any_sync (one shared-memory
 // add per distinct expert per 32 routes, no atomics).  Pass 2: per expert, an
 // exclusive prefix over the 32 warps, then one exclusive scan over experts
@@ -14,6 +14,8 @@
 // every route at offsets[e] + (routes of e in earlier warps) + (earlier routes
 // of e in this warp), which is the stable order.  Integer work only, a few
 // microseconds even at 40,960 routes, so one CTA is enough.
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -28,21 +30,26 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                    int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                    int32_t* status) {
   extern __shared__ int32_t sh[];
-  int32_t* hist = sh;               // [kWarps][E]
-  int32_t* base = sh + kWarps * E;  // [E]
+  // Only as many warps own routes as there are 32-route steps (a decode
+  // block of 160 routes uses 5), which keeps the per-warp tables small.
+  const int W = min(kWarps, max(1, (R + 31) / 32));
+  int32_t* hist = sh;          // [W][E]
+  int32_t* base = sh + W * E;  // [E]
   __shared__ int bad;
   __shared__ int warp_tot[kWarps];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  for (int i = tid; i < kWarps * E; i += blockDim.x) hist[i] = 0;
+  for (int i = tid; i < W * E; i += blockDim.x) hist[i] = 0;
   if (tid == 0) bad = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
 
-  const int per = (R + kWarps - 1) / kWarps;
-  const int r0 = min(R, warp * per);
-  const int r1 = min(R, r0 + per);
-  int32_t* my_hist = hist + warp * E;
+  const int per = (R + W - 1) / W;
+  const int r0 = (warp < W) ? min(R, warp * per) : R;
+  const int r1 = (warp < W) ? min(R, r0 + per) : R;
+  int32_t* my_hist = hist + min(warp, W - 1) * E;
 
   // pass 1: per-warp histogram
   for (int b = r0; b < r1; b += 32) {
@@ -68,7 +75,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   // pass 2: per-expert prefix over warps, then an exclusive scan over experts
   for (int e = tid; e < E; e += blockDim.x) {
     int s = 0;
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < W; ++w) {
       const int c = hist[w * E + e];
       hist[w * E + e] = s;
       s += c;
@@ -127,6 +134,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int R, int k,
                                    int T, int H, uint16_t* __restrict__ xp) {
+  pdl_wait();
+  pdl_trigger();
   const int vpr = H / 8;
   const size_t n = static_cast<size_t>(R) * vpr;
   for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n;
@@ -146,12 +155,13 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t
 cudaError_t launch_permute(const int32_t* ids, int R, int k, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
                            int32_t* inv, int32_t* st_word, cudaStream_t st) {
   (void)k;
-  const size_t smem = static_cast<size_t>(kWarps + 1) * E * sizeof(int32_t);
+  const int W = std::min(kWarps, std::max(1, (R + 31) / 32));
+  const size_t smem = static_cast<size_t>(W + 1) * E * sizeof(int32_t);
   cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+                                       static_cast<int>((kWarps + 1) * kMaxE * sizeof(int32_t)));
   if (e != cudaSuccess) return e;
-  permute_kernel<<<1, kWarps * 32, smem, st>>>(ids, R, E, counts, offsets, perm, inv, st_word);
-  return cudaGetLastError();
+  return launch_pdl(permute_kernel, dim3(1), dim3(kWarps * 32), smem, st, ids, R, E, counts, offsets, perm, inv,
+                    st_word);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int R, int k, int T, int H, uint16_t* x_perm,
@@ -162,8 +172,8 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int R, in
   const size_t cap = static_cast<size_t>(sm_count() > 0 ? sm_count() : 148) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks == 0) blocks = 1;
-  gather_rows_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(x, perm, R, k, T, H, x_perm);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, x, perm, R, k, T,
+                    H, x_perm);
 }
 
 }  // namespace moe

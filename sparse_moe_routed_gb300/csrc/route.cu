@@ -7,12 +7,12 @@
 // order are the label, so selection is exact on the fp32 logits with a fixed
 // tie rule (lower expert ID first), not on rounded probabilities.
 //
-// Small token counts (decode blocks) use CUDA cores: one warp per expert row,
-// the block's token rows staged once in shared memory, 16-byte loads of the
-// router row.  Large token counts use the tcgen05 grouped kernel in its dense
-// router mode (gemm.cu).  Selection is one warp per token: each lane keeps
-// ceil(E/32) logits in registers and k+1 rounds of warp arg-max pick the
-// route and the next logit (for the decision gap).
+// Small token counts (decode blocks) use CUDA cores: two warps per expert row,
+// all router-row loads in flight at once, the block's token rows staged once
+// in shared memory.  Large token counts use the tcgen05 grouped kernel in its
+// dense router mode (gemm.cu).  Selection is one warp per token: each lane
+// keeps ceil(E/32) logits in registers and k+1 rounds of warp-wide max/min
+// reductions pick the route and the next logit (for the decision gap).
 #include <math.h>
 
 #include "common.cuh"
@@ -31,38 +31,74 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   }
 }
 
+// One CTA = 8 warps = 4 experts x 2 halves of K.  The router rows are
+// constant, so each lane issues all of its (up to 8 x 16-byte) weight loads
+// before waiting on the upstream kernel; the token tile is then staged once
+// in shared memory and every lane runs TT dot products over its K range.
+constexpr int kLogitThreads = 256;
+constexpr int kLogitExperts = 4;
+constexpr int kWChunk = 8;  // 16-byte weight vectors a lane keeps in flight
+
 template <int TT>
-__global__ void __launch_bounds__(256) router_logits_simt_kernel(const uint16_t* __restrict__ x,
-                                                                 const uint16_t* __restrict__ wr, int T, int H,
-                                                                 int E, float* __restrict__ logits) {
+__global__ void __launch_bounds__(kLogitThreads) router_logits_simt_kernel(const uint16_t* __restrict__ x,
+                                                                           const uint16_t* __restrict__ wr,
+                                                                           int T, int H, int E,
+                                                                           float* __restrict__ logits) {
   extern __shared__ uint4 xs[];  // [TT][H/8]
+  __shared__ float part[kLogitExperts][TT];
   const int vpr = H / 8;
+  const int hv = vpr / 2;  // 16-byte vectors per K half
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kLogitExperts + (warp >> 1);
+  const int half = warp & 1;
   const int t0 = blockIdx.y * TT;
   const int nt = min(TT, T - t0);
-  for (int idx = threadIdx.x; idx < TT * vpr; idx += blockDim.x) {
+  const bool active = e < E;
+  const uint4* wrow = reinterpret_cast<const uint4*>(wr + static_cast<size_t>(active ? e : 0) * H) + half * hv;
+
+  uint4 wv[kWChunk];
+#pragma unroll
+  for (int j = 0; j < kWChunk; ++j) {
+    const int c = lane + 32 * j;
+    wv[j] = (active && c < hv) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+  }
+
+  pdl_wait();
+  pdl_trigger();
+  for (int idx = threadIdx.x; idx < TT * vpr; idx += kLogitThreads) {
     const int r = idx / vpr;
     const int c = idx - r * vpr;
     xs[idx] = (r < nt) ? reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + r) * H)[c]
                        : make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + warp;
-  if (e >= E) return;
+
   float acc[TT];
 #pragma unroll
   for (int t = 0; t < TT; ++t) acc[t] = 0.f;
-  const uint4* wrow = reinterpret_cast<const uint4*>(wr + static_cast<size_t>(e) * H);
-  for (int c = lane; c < vpr; c += 32) {
-    float wf[8];
-    unpack8(__ldg(wrow + c), wf);
+  for (int c0 = 0; c0 < hv; c0 += 32 * kWChunk) {
+    if (c0 > 0) {
 #pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      float xf[8];
-      unpack8(xs[t * vpr + c], xf);
+      for (int j = 0; j < kWChunk; ++j) {
+        const int c = c0 + lane + 32 * j;
+        wv[j] = (active && c < hv) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+      }
+    }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
+    for (int j = 0; j < kWChunk; ++j) {
+      const int c = c0 + lane + 32 * j;
+      if (c < hv) {
+        float wf[8];
+        unpack8(wv[j], wf);
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          float xf[8];
+          unpack8(xs[t * vpr + half * hv + c], xf);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
+        }
+      }
     }
   }
 #pragma unroll
@@ -74,22 +110,38 @@ __global__ void __launch_bounds__(256) router_logits_simt_kernel(const uint16_t*
 #pragma unroll
   for (int t = 0; t < TT; ++t)
     if (lane == t) mine = acc[t];
-  if (lane < nt) logits[static_cast<size_t>(t0 + lane) * E + e] = mine;
+  if (half == 1 && lane < TT) part[warp >> 1][lane] = mine;
+  __syncthreads();
+  if (half == 0 && active && lane < nt)
+    logits[static_cast<size_t>(t0 + lane) * E + e] = mine + part[warp >> 1][lane];
 }
 
-// better(a, b): larger logit, ties to the lower expert ID
-__device__ __forceinline__ bool better(float va, int ea, float vb, int eb) {
-  return va > vb || (va == vb && ea < eb);
+// Order-preserving map of a float to an unsigned key (NaN mapped to -inf by
+// the caller, -0 to +0), so that warp-wide unsigned max/min reductions select
+// the largest logit and, among equal logits, the lowest expert ID.
+__device__ __forceinline__ uint32_t f2key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+__device__ __forceinline__ float key2f(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// One warp per token.  Lane l holds the logits of experts l, l+32, ...; each
+// round one __reduce_max_sync finds the largest remaining logit and one
+// __reduce_min_sync the lowest expert ID holding it; only the winning lane
+// rescans its own EPL values.
 template <int EPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                                                    int T, int E, int k, int32_t* __restrict__ ids,
                                                    float* __restrict__ w, float* __restrict__ gap) {
+  pdl_wait();
+  pdl_trigger();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  float v[EPL];
+  uint32_t key[EPL];
   uint32_t taken = 0;
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
@@ -97,41 +149,46 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     if (e < E) {
       float l = logits[static_cast<size_t>(t) * E + e];
       if (bias) l += bias[e];
-      v[j] = isnan(l) ? -INFINITY : l;
+      if (isnan(l)) l = -INFINITY;
+      if (l == 0.0f) l = 0.0f;
+      key[j] = f2key(l);
     } else {
-      v[j] = -INFINITY;
+      key[j] = 0u;
       taken |= 1u << j;
     }
   }
-  float my_v = -INFINITY, next_v = -INFINITY;
-  int my_e = 0;
-  const int rounds = min(k + 1, E);
-  for (int r = 0; r < rounds; ++r) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
+  auto local_best = [&](uint32_t& bk, int& be) {
+    bk = 0u;
+    be = 0x7fffffff;
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
-      if (!((taken >> j) & 1u) && better(v[j], j * 32 + lane, bv, be)) {
-        bv = v[j];
+      if (!((taken >> j) & 1u) && (be == 0x7fffffff || key[j] > bk)) {
+        bk = key[j];
         be = j * 32 + lane;
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (better(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
-      }
+  };
+  uint32_t bk;
+  int be;
+  local_best(bk, be);
+  uint32_t my_key = 0u, next_key = 0u;
+  int my_e = 0;
+  const int rounds = min(k + 1, E);
+  for (int r = 0; r < rounds; ++r) {
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const int cand = (be != 0x7fffffff && bk == m) ? be : 0x7fffffff;
+    const int emin = __reduce_min_sync(0xffffffffu, cand);
+    if ((emin & 31) == lane) {
+      taken |= 1u << (emin >> 5);
+      local_best(bk, be);
     }
-    if (be != 0x7fffffff && (be & 31) == lane) taken |= 1u << (be >> 5);
     if (r < k && lane == r) {
-      my_v = bv;
-      my_e = be;
+      my_key = m;
+      my_e = emin;
     }
-    if (r == k) next_v = bv;
+    if (r == k) next_key = m;
   }
+  const float my_v = key2f(my_key);
   const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
   const float ex = (lane < k) ? expf(my_v - v0) : 0.f;
   float sum = ex;
@@ -142,40 +199,37 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     ids[static_cast<size_t>(t) * k + lane] = my_e;
     w[static_cast<size_t>(t) * k + lane] = ex / sum;
   }
-  if (gap && lane == 0) gap[t] = (k < E) ? (vk1 - next_v) : INFINITY;
+  if (gap && lane == 0) gap[t] = (k < E) ? (vk1 - key2f(next_key)) : INFINITY;
 }
 
 template <int EPL>
 cudaError_t run_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids, float* w, float* gap,
                      cudaStream_t st) {
   const int blocks = (T + 7) / 8;
-  topk_kernel<EPL><<<blocks, 256, 0, st>>>(logits, bias, T, E, k, ids, w, gap);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel<EPL>, dim3(blocks), dim3(256), 0, st, logits, bias, T, E, k, ids, w, gap);
 }
 
 }  // namespace
 
 cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* wr, int T, int H, int E, float* logits,
                                       cudaStream_t st) {
-  const dim3 block(256);
+  const dim3 grid((E + kLogitExperts - 1) / kLogitExperts, 1);
   if (H <= 6144) {
     constexpr int TT = 16;
     const size_t smem = static_cast<size_t>(TT) * H * 2;
     cudaError_t e = cudaFuncSetAttribute(router_logits_simt_kernel<TT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const dim3 grid((E + 7) / 8, (T + TT - 1) / TT);
-    router_logits_simt_kernel<TT><<<grid, block, smem, st>>>(x, wr, T, H, E, logits);
-  } else {
-    constexpr int TT = 8;
-    const size_t smem = static_cast<size_t>(TT) * H * 2;
-    cudaError_t e = cudaFuncSetAttribute(router_logits_simt_kernel<TT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const dim3 grid((E + 7) / 8, (T + TT - 1) / TT);
-    router_logits_simt_kernel<TT><<<grid, block, smem, st>>>(x, wr, T, H, E, logits);
+    return launch_pdl(router_logits_simt_kernel<TT>, dim3(grid.x, (T + TT - 1) / TT), dim3(kLogitThreads), smem,
+                      st, x, wr, T, H, E, logits);
   }
-  return cudaGetLastError();
+  constexpr int TT = 8;
+  const size_t smem = static_cast<size_t>(TT) * H * 2;
+  cudaError_t e = cudaFuncSetAttribute(router_logits_simt_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(router_logits_simt_kernel<TT>, dim3(grid.x, (T + TT - 1) / TT), dim3(kLogitThreads), smem, st,
+                    x, wr, T, H, E, logits);
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids, float* w,
