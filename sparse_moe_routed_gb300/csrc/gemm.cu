@@ -28,6 +28,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -378,15 +380,51 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // bf16 tensor map with 128-byte swizzle; dims/strides innermost first.
+// Encoding costs several microseconds of host time, so maps are cached by
+// everything they encode (address, rank, dims, strides, box).  A map holds
+// no data, so a cached map stays valid for any buffer later placed at the
+// same address with the same shape.
+struct MapKey {
+  const void* ptr;
+  int rank;
+  cuuint64_t dims[5];
+  cuuint64_t strides[4];
+  cuuint32_t box[5];
+  bool operator<(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) < 0; }
+};
+
 bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
               const cuuint32_t* box) {
+  MapKey key;
+  std::memset(&key, 0, sizeof key);
+  key.ptr = ptr;
+  key.rank = rank;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+    if (i + 1 < rank) key.strides[i] = strides_bytes[i];
+  }
+  static std::mutex mu;
+  static std::map<MapKey, CUtensorMap> cache;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *m = it->second;
+      return true;
+    }
+  }
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides_bytes, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() > 4096) cache.clear();
+  cache.emplace(key, *m);
+  return true;
 }
 
 bool make_rows_map(CUtensorMap* m, const void* ptr, int K, int rows, int box_rows) {
@@ -399,7 +437,7 @@ bool make_rows_map(CUtensorMap* m, const void* ptr, int K, int rows, int box_row
 template <int NMAX, int KIND>
 cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, cudaStream_t st) {
   auto kern = grouped_gemm_kernel<NMAX, KIND>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NMAX>::kSmemBytes);
+  cudaError_t e = ensure_smem(kern, Cfg<NMAX>::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = sm_count();
   if (grid <= 0) return cudaErrorNoDevice;

@@ -10,6 +10,14 @@ namespace moe {
 
 int sm_count();
 
+// Raise a kernel's dynamic shared memory limit once per (kernel, device):
+// the attribute call is not free, and the limit only ever needs to grow.
+cudaError_t ensure_smem_fn(const void* kern, int bytes);
+template <typename... KArgs>
+cudaError_t ensure_smem(void (*kern)(KArgs...), int bytes) {
+  return ensure_smem_fn(reinterpret_cast<const void*>(kern), bytes);
+}
+
 // Launch with programmatic stream serialization (see pdl_wait in common.cuh).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

@@ -157,8 +157,7 @@ cudaError_t launch_permute(const int32_t* ids, int R, int k, int E, int32_t* cou
   (void)k;
   const int W = std::min(kWarps, std::max(1, (R + 31) / 32));
   const size_t smem = static_cast<size_t>(W + 1) * E * sizeof(int32_t);
-  cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>((kWarps + 1) * kMaxE * sizeof(int32_t)));
+  cudaError_t e = ensure_smem(permute_kernel, static_cast<int>((kWarps + 1) * kMaxE * sizeof(int32_t)));
   if (e != cudaSuccess) return e;
   return launch_pdl(permute_kernel, dim3(1), dim3(kWarps * 32), smem, st, ids, R, E, counts, offsets, perm, inv,
                     st_word);

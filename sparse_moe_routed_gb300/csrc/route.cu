@@ -217,16 +217,14 @@ cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* wr, int
   if (H <= 6144) {
     constexpr int TT = 16;
     const size_t smem = static_cast<size_t>(TT) * H * 2;
-    cudaError_t e = cudaFuncSetAttribute(router_logits_simt_kernel<TT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = ensure_smem(router_logits_simt_kernel<TT>, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     return launch_pdl(router_logits_simt_kernel<TT>, dim3(grid.x, (T + TT - 1) / TT), dim3(kLogitThreads), smem,
                       st, x, wr, T, H, E, logits);
   }
   constexpr int TT = 8;
   const size_t smem = static_cast<size_t>(TT) * H * 2;
-  cudaError_t e = cudaFuncSetAttribute(router_logits_simt_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_smem(router_logits_simt_kernel<TT>, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return launch_pdl(router_logits_simt_kernel<TT>, dim3(grid.x, (T + TT - 1) / TT), dim3(kLogitThreads), smem, st,
                     x, wr, T, H, E, logits);

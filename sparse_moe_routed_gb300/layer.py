@@ -11,6 +11,8 @@ Every step runs in the CUDA library; this class only owns memory.
 """
 from __future__ import annotations
 
+import ctypes as C
+
 import torch
 
 from . import _lib
@@ -43,46 +45,65 @@ class MoELayer:
         self.y_perm = torch.empty((R, H), dtype=torch.float32, device=dev)
         self.out = torch.empty((T_max, H), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self._bound = {}
 
-    # -- the five calls, exposed one by one so callers can time each --------
-    def route(self, x, stream=None):
-        T = x.shape[0]
-        _lib.moe_route(x, self.w_router, self.bias, self.k, self.ids[:T], self.w[:T], self.gap[:T], self.ws,
-                       stream)
+    # -- the five boundary calls, bound once per (T, x, out, stream) ---------
+    def bound_calls(self, x, T=None, out=None, stream=None):
+        """[(name, fn, args)] of the five C-ABI calls for this input.
 
-    def permute(self, x, stream=None):
-        T = x.shape[0]
-        R = T * self.k
-        _lib.moe_permute(self.ids[:T], self.E, x, self.counts, self.offsets, self.perm[:R], self.inv[:R],
-                         self.x_perm[:R], self.status, stream)
-
-    def gateup(self, T, stream=None):
-        R = T * self.k
-        _lib.moe_expert_gateup(self.x_perm[:R], self.offsets, self.E, self.H, self.I, self.w_gateup, self.h[:R],
-                               self.status, stream=stream)
-
-    def down(self, T, stream=None):
-        R = T * self.k
-        _lib.moe_expert_down(self.h[:R], self.offsets, self.E, self.H, self.I, self.w_down, self.y_perm[:R],
-                             self.status, stream=stream)
-
-    def combine(self, T, out=None, stream=None):
-        R = T * self.k
+        Pointers and sizes are converted to ctypes once and cached, so issuing
+        a layer costs five foreign calls and nothing else on the host.
+        """
+        T = x.shape[0] if T is None else T
+        s = torch.cuda.current_stream() if stream is None else stream
         out = self.out[:T] if out is None else out
-        _lib.moe_combine(self.y_perm[:R], self.inv[:R], self.w[:T], None, out, None, self.status, stream)
-        return out
+        key = (T, x.data_ptr(), out.data_ptr(), s.cuda_stream)
+        calls = self._bound.get(key)
+        if calls is not None:
+            return calls
+        if len(self._bound) > 64:
+            self._bound.clear()
+        lib = _lib.load()
+        P = _lib._ptr
+        st = C.c_void_p(s.cuda_stream)
+        R = T * self.k
+        E, H, I, k = self.E, self.H, self.I, self.k
+        ws_bytes = self.ws.numel()
+        calls = [
+            ("moe_route", lib.moe_route,
+             (P(x), P(self.w_router), P(self.bias), T, H, E, k, P(self.ids), P(self.w), P(self.gap), P(self.ws),
+              ws_bytes, st)),
+            ("moe_permute", lib.moe_permute,
+             (P(self.ids), T, k, E, P(x), H, P(self.counts), P(self.offsets), P(self.perm), P(self.inv),
+              P(self.x_perm), P(self.status), st)),
+            ("moe_expert_gateup", lib.moe_expert_gateup,
+             (P(self.x_perm), P(self.offsets), R, E, H, I, _lib.MOE_W_BF16, P(self.w_gateup), None, P(self.h),
+              P(self.status), st)),
+            ("moe_expert_down", lib.moe_expert_down,
+             (P(self.h), P(self.offsets), R, E, H, I, _lib.MOE_W_BF16, P(self.w_down), None, P(self.y_perm),
+              P(self.status), st)),
+            ("moe_combine", lib.moe_combine,
+             (P(self.y_perm), P(self.inv), P(self.w), T, k, H, None, P(out), None, P(self.status), st)),
+        ]
+        self._bound[key] = calls
+        return calls
+
+    @staticmethod
+    def issue(call):
+        name, fn, args = call
+        st = fn(*args)
+        if st != 0:
+            raise _lib.MoEError(name, st, _lib.status_str(st))
 
     def forward(self, x, out=None, stream=None):
         """out[T,H] bf16 = MoE(x) for x [T,H] bf16 on the GPU (asynchronous)."""
         T = x.shape[0]
-        assert T <= self.T_max and x.shape[1] == self.H
+        assert T <= self.T_max and x.shape[1] == self.H and x.dtype == torch.bfloat16
         if T == 0:
             return self.out[:0] if out is None else out
-        self.route(x, stream)
-        self.permute(x, stream)
-        self.gateup(T, stream)
-        self.down(T, stream)
-        return self.combine(T, out, stream)
+        for call in self.bound_calls(x, T, out, stream):
+            self.issue(call)
+        return self.out[:T] if out is None else out
 
     def forward_host(self, x_host, out_host, x_dev=None, stream=None):
         """Host in, host out: pinned x_host [T,H] bf16 -> out_host [T,H] bf16.
