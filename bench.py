@@ -291,7 +291,7 @@ def main():
         return u * (gu_w_bytes + dn_w_bytes) + router_bytes + 2 * cfg.T * H * 2 + R * 8
 
     K = args.steps
-    EV_EVERY = 8 if K >= 64 else 1
+    EV_EVERY = 7 if K >= 64 else 1  # coprime with the 8 rotated layers
     KE = (K + EV_EVERY - 1) // EV_EVERY
     ev_g0 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
     ev_g1 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
