@@ -102,6 +102,27 @@ MOE_API moe_status moe_route(const uint16_t *x, const uint16_t *w_router, const 
                      size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_route_noalloc -- moe_route for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this entry point; it exists for
+ * callers that are handed their inputs and outputs but have no way to
+ * allocate a workspace (a host framework that owns every device buffer, or a
+ * path on which allocating is not allowed).
+ *
+ * Same arguments and results as moe_route, without the workspace: the
+ * [T,E] fp32 logits scratch lives in a fixed 256 KB array inside the library
+ * (held by every GPU that loads it, until exit).  Limits: T <= 64 and
+ * E <= 1024; larger calls return MOE_EWORKSPACE and enqueue nothing.  The
+ * first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the array: calls that overlap on the GPU (e.g. on two streams)
+ * race.  Nothing in the array needs to start at zero.  No allocation of any
+ * kind is made.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_route_noalloc(const uint16_t *x, const uint16_t *w_router, const float *bias, int T,
+                                     int H, int E, int k, int32_t *topk_ids, float *topk_w, float *gap,
+                                     void *stream);
+
+/* ---------------------------------------------------------------------------
  * moe_permute -- group token rows by expert (count, exclusive scan, stable
  * scatter), optionally gathering the rows of x into expert order.
  *

@@ -55,6 +55,7 @@ def load(path: str | None = None):
             "moe_device_sm_count": ([], i),
             "moe_route_workspace_size": ([i, i], sz),
             "moe_route": ([p, p, p, i, i, i, i, p, p, p, p, sz, p], i),
+            "moe_route_noalloc": ([p, p, p, i, i, i, i, p, p, p, p], i),
             "moe_permute": ([p, i, i, i, p, i, p, p, p, p, p, p, p], i),
             "moe_expert_gateup": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
             "moe_expert_down": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
@@ -111,6 +112,16 @@ def moe_route(x, w_router, bias, k, topk_ids, topk_w, gap, workspace, stream=Non
                           _ptr(gap), _ptr(workspace), workspace.numel() * workspace.element_size()
                           if workspace is not None else 0, _stream(stream))
     _check("moe_route", st)
+
+
+def moe_route_noalloc(x, w_router, bias, k, topk_ids, topk_w, gap, stream=None):
+    """moe_route without a workspace: scratch lives in a fixed array in the
+    library (T <= 64, E <= 1024), for callers that cannot allocate."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    st = load().moe_route_noalloc(_ptr(x), _ptr(w_router), _ptr(bias), T, H, E, k, _ptr(topk_ids), _ptr(topk_w),
+                                  _ptr(gap), _stream(stream))
+    _check("moe_route_noalloc", st)
 
 
 def moe_permute(topk_ids, E, x, counts, offsets, perm, inv_perm, x_perm, dev_status, stream=None):

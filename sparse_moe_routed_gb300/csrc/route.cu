@@ -15,6 +15,8 @@
 // reductions pick the route and the next logit (for the decision gap).
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -242,3 +244,67 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free router entry point.
+//
+// Some callers cannot allocate device memory when they call the router: a
+// host framework that owns every device buffer and hands a plugin only its
+// inputs and outputs, or code that must not allocate while it runs (for
+// example on a path where an allocator call could block or is forbidden).
+// For them, moe_route_noalloc() keeps its scratch (the [T, E] fp32 logits)
+// in the fixed array below instead of in a caller-provided workspace.
+//
+//  * Limit: T <= 64 tokens and E <= 1024 experts (64 x 1024 fp32 = 256 KB).
+//    Every GPU that loads the library holds this array until the process
+//    exits.  Larger calls are rejected with MOE_EWORKSPACE.
+//  * The host-side name g_route_scratch is not a device address; the first
+//    call on a device looks the device address up with
+//    cudaGetSymbolAddress() (with that device current) and remembers it, so
+//    that first call should come before any stream capture.
+//  * All calls share the array and it keeps the last call's contents.
+//    Nothing in it needs to start at zero: the logits kernel overwrites the
+//    whole [T, E] region before the selection kernel reads it.  Calls that
+//    overlap on the GPU (for instance on two streams at once) race on it.
+//  * No cudaMalloc, cudaFree or allocating library routine is called.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocMaxT = 64;
+constexpr int kNoAllocMaxE = 1024;
+static __device__ __align__(256) float g_route_scratch[kNoAllocMaxT * kNoAllocMaxE];
+
+// Device address of g_route_scratch on the current device (nullptr on error).
+float* noalloc_scratch_for_current_device() {
+  static std::mutex mu;
+  static float* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<float*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" moe_status moe_route_noalloc(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H,
+                                        int E, int k, int32_t* topk_ids, float* topk_w, float* gap, void* stream) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ESHAPE;
+  if (k > moe::kMaxK || k > E || E > moe::kMaxE || H % 128 != 0 || H > 16384) return MOE_ENOTSUP;
+  if (!x || !w_router || !topk_ids || !topk_w) return MOE_EINVAL;
+  auto aligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(topk_ids, 4) || !aligned(topk_w, 4)) return MOE_EINVAL;
+  if ((bias && !aligned(bias, 4)) || (gap && !aligned(gap, 4))) return MOE_EINVAL;
+  if (T > kNoAllocMaxT || E > kNoAllocMaxE) return MOE_EWORKSPACE;
+  if (T == 0) return MOE_OK;
+  float* logits = noalloc_scratch_for_current_device();
+  if (!logits) return MOE_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (moe::launch_router_logits_simt(x, w_router, T, H, E, logits, st) != cudaSuccess) return MOE_ECUDA;
+  if (moe::launch_topk(logits, bias, T, E, k, topk_ids, topk_w, gap, st) != cudaSuccess) return MOE_ECUDA;
+  return MOE_OK;
+}
