@@ -158,9 +158,13 @@ MOE_API moe_status moe_permute(const int32_t *topk_ids, int T, int k, int E, con
  *                   w_down   [E, H, I]  bf16
  *                   s_gateup = s_down = NULL
  *   MOE_W_INT4_G64: w_gateup [E, 2I, H/2] uint8, w_down [E, H, I/2] uint8:
- *                   two signed 4-bit codes per byte, even input index in the
- *                   low nibble; s_gateup [E, 2I, H/64] bf16 and
- *                   s_down [E, H, I/64] bf16 scales; w = scale * code.
+ *                   two signed 4-bit codes per byte (two's complement, -8..7),
+ *                   even input index in the low nibble; one bf16 scale per 64
+ *                   consecutive inputs of a row, stored group-major so that the
+ *                   scales of one group are contiguous:
+ *                   s_gateup [E, H/64, 2I] bf16 (for each group: gate rows,
+ *                   then up rows) and s_down [E, I/64, H] bf16.
+ *                   The tensor cores see w = bf16(scale * code).
  *                   (AFN-001, section "Phase 2": affine4 with group size 64,
  *                   read as symmetric codes with one bf16 scale per group.)
  *
@@ -200,7 +204,8 @@ MOE_API moe_status moe_grouped_swiglu(const uint16_t *x_perm, const int32_t *off
  *              (fp32, accumulated in j order)
  *   out_f32[t,:] = acc + residual[t,:]   (residual [T,H] f32 or NULL -> 0)
  *   out_bf16[t,:] = bf16(out_f32[t,:])
- * At least one of out_bf16 / out_f32 must be non-NULL.  A non-finite result
+ * At least one of out_bf16 / out_f32 must be non-NULL; residual may be the
+ * same buffer as out_f32 (an in-place residual stream).  A non-finite result
  * sets MOE_DEV_NONFINITE in *dev_status (may be NULL to skip the check).
  * ------------------------------------------------------------------------- */
 MOE_API moe_status moe_combine(const float *y_perm, const int32_t *inv_perm, const float *topk_w, int T,

@@ -25,6 +25,8 @@ Functions and the page passages they follow (Hebrus "Agent Field Notes"):
                         symmetric-scale reading.
   combine(...)          AFN-019, section "Hypothesis H4" (weighted sum in route-rank order).
   rmsnorm(...)          AFN-001, section "Phase 1" (zero-centred RMS normalisation).
+  round_bf16_bits(...)  bf16 rounding of the normalised stack input (reading: router and
+                        experts consume bf16 activations).
 
 Parity pins: every function above is pinned in tests/test_oracle_pins.py
 against closed forms, brute force on tiny inputs, special cases reducing to
@@ -61,6 +63,7 @@ def _load():
         lib.oracle_dequant_int4.argtypes = [p, p, i, i, p]
         lib.oracle_combine.argtypes = [p, p, p, i, i, i, p, p]
         lib.oracle_rmsnorm.argtypes = [p, p, i, i, C.c_double, p]
+        lib.oracle_round_bf16.argtypes = [p, C.c_size_t, p]
         lib.oracle_dedup.argtypes = [p, i, i, i, i, i, i, i, p, p, p, p]
         lib.oracle_dedup.restype = i
         _lib = lib
@@ -192,6 +195,14 @@ def rmsnorm(x, gamma=None, eps=1e-6):
     T, H = xc.shape
     out = np.empty_like(xc)
     _load().oracle_rmsnorm(_ptr(xc), _ptr(_c(gamma, np.float32)), T, H, float(eps), _ptr(out))
+    return out
+
+
+def round_bf16_bits(x):
+    """fp32 array -> bf16 bit patterns (uint16), round to nearest even."""
+    xc = _c(x, np.float32)
+    out = np.empty(xc.shape, np.uint16)
+    _load().oracle_round_bf16(_ptr(xc), xc.size, _ptr(out))
     return out
 
 

@@ -279,6 +279,22 @@ void oracle_combine(const float *y, const int32_t *inv, const float *w, int T, i
     }
 }
 
+/* fp32 -> bf16 bit patterns, round to nearest, ties to even (NaN kept
+ * quiet).  The router and experts of a stack layer read the RMS-normalised
+ * residual rounded to bf16, as their tensor-core inputs are bf16.           */
+void oracle_round_bf16(const float *x, size_t n, uint16_t *out) {
+  for (size_t i = 0; i < n; ++i) {
+    uint32_t u;
+    memcpy(&u, &x[i], 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u) {
+      out[i] = (uint16_t)((u >> 16) | 0x40u);
+      continue;
+    }
+    uint32_t lsb = (u >> 16) & 1u;
+    out[i] = (uint16_t)((u + 0x7fffu + lsb) >> 16);
+  }
+}
+
 /* ---- zero-centred RMSNorm: n = x / sqrt(mean(x^2) + eps) * (1 + gamma) --- */
 void oracle_rmsnorm(const float *x, const float *gamma, int T, int H, double eps, float *out) {
   for (int t = 0; t < T; ++t) {

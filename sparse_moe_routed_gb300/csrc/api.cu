@@ -109,7 +109,8 @@ moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* b
   float* logits = static_cast<float*>(workspace);
   cudaError_t e;
   if (T > 64 && E % 128 == 0)
-    e = moe::launch_grouped_gemm(moe::GemmKind::kRouter, w_router, x, nullptr, 1, T, H, 0, E, logits, nullptr, st);
+    e = moe::launch_grouped_gemm(moe::GemmKind::kRouter, MOE_W_BF16, w_router, nullptr, x, nullptr, 1, T, H, 0, E,
+                                 logits, nullptr, st);
   else
     e = moe::launch_router_logits_simt(x, w_router, T, H, E, logits, st);
   if (e != cudaSuccess) return MOE_ECUDA;
@@ -146,11 +147,15 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, const uint1
 static moe_status check_expert_args(int R, int E, int H, int I, int fmt) {
   if (R < 0 || E <= 0 || H <= 0 || I <= 0) return MOE_ESHAPE;
   if (fmt != MOE_W_BF16 && fmt != MOE_W_INT4_G64) return MOE_EINVAL;
-  if (fmt != MOE_W_BF16) return MOE_ENOTSUP;
   if (E > moe::kMaxE) return MOE_ENOTSUP;
   if (H % 128 != 0 || H > 16384 || I % 64 != 0 || I > 16384) return MOE_ENOTSUP;
   if (static_cast<long long>(E) * H >= (1LL << 31)) return MOE_ENOTSUP;
   return MOE_OK;
+}
+
+// Scales are given exactly for the int4 format, 16-byte aligned.
+static bool scales_ok(int fmt, const uint16_t* s) {
+  return fmt == MOE_W_INT4_G64 ? (s != nullptr && a16(s)) : (s == nullptr);
 }
 
 moe_status moe_expert_gateup(const uint16_t* x_perm, const int32_t* offsets, int R, int E, int H, int I, int fmt,
@@ -159,11 +164,11 @@ moe_status moe_expert_gateup(const uint16_t* x_perm, const int32_t* offsets, int
   moe_status c = check_expert_args(R, E, H, I, fmt);
   if (c != MOE_OK) return c;
   if (!x_perm || !offsets || !w_gateup || !h || !dev_status) return MOE_EINVAL;
-  if (s_gateup) return MOE_EINVAL;
+  if (!scales_ok(fmt, s_gateup)) return MOE_EINVAL;
   if (!a16(x_perm) || !a16(w_gateup) || !a16(h) || !a4(offsets) || !a4(dev_status)) return MOE_EINVAL;
   if (R == 0) return MOE_OK;
-  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kGateUp, w_gateup, x_perm, offsets, E, R, H, I, 0, h,
-                                           dev_status, static_cast<cudaStream_t>(stream));
+  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kGateUp, fmt, w_gateup, s_gateup, x_perm, offsets, E, R, H,
+                                           I, 0, h, dev_status, static_cast<cudaStream_t>(stream));
   return cuda_status(e);
 }
 
@@ -173,11 +178,11 @@ moe_status moe_expert_down(const uint16_t* h, const int32_t* offsets, int R, int
   moe_status c = check_expert_args(R, E, H, I, fmt);
   if (c != MOE_OK) return c;
   if (!h || !offsets || !w_down || !y_perm || !dev_status) return MOE_EINVAL;
-  if (s_down) return MOE_EINVAL;
+  if (!scales_ok(fmt, s_down)) return MOE_EINVAL;
   if (!a16(h) || !a16(w_down) || !a16(y_perm) || !a4(offsets) || !a4(dev_status)) return MOE_EINVAL;
   if (R == 0) return MOE_OK;
-  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kDown, w_down, h, offsets, E, R, H, I, 0, y_perm,
-                                           dev_status, static_cast<cudaStream_t>(stream));
+  cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kDown, fmt, w_down, s_down, h, offsets, E, R, H, I, 0,
+                                           y_perm, dev_status, static_cast<cudaStream_t>(stream));
   return cuda_status(e);
 }
 
@@ -188,7 +193,7 @@ moe_status moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets, in
   moe_status c = check_expert_args(R, E, H, I, fmt);
   if (c != MOE_OK) return c;
   if (!x_perm || !offsets || !w_gateup || !w_down || !h || !y_perm || !dev_status) return MOE_EINVAL;
-  if (s_gateup || s_down) return MOE_EINVAL;
+  if (!scales_ok(fmt, s_gateup) || !scales_ok(fmt, s_down)) return MOE_EINVAL;
   if (!a16(x_perm) || !a16(w_gateup) || !a16(w_down) || !a16(h) || !a16(y_perm) || !a4(offsets) ||
       !a4(dev_status))
     return MOE_EINVAL;

@@ -26,8 +26,10 @@ constexpr int kCombineThreads = 128;  // x 4 floats = 512 columns per CTA
 
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const float* __restrict__ w, int T,
-                   int k, int H, int R, const float* __restrict__ residual, uint16_t* __restrict__ out_bf16,
-                   float* __restrict__ out_f32, int32_t* status) {
+                   int k, int H, int R, const float* residual, uint16_t* __restrict__ out_bf16, float* out_f32,
+                   int32_t* status) {
+  // residual and out_f32 may be the same buffer (an in-place residual
+  // stream): each element is read and then written by the same thread.
   __shared__ int slot[kMaxK];
   __shared__ float wt[kMaxK];
   pdl_wait();

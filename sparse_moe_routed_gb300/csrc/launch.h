@@ -54,8 +54,8 @@ enum class GemmKind { kGateUp = 0, kDown = 1, kRouter = 2 };
 // chunk of token rows) tile, D = W_e[rows] . B[rows of segment]^T on the
 // tensor cores; epilogue per kind.  Returns cudaErrorInvalidValue when a
 // tensor map cannot be encoded.
-cudaError_t launch_grouped_gemm(GemmKind kind, const void* w, const uint16_t* b_rows,
-                                const int32_t* offsets, int E, int R, int H, int I,
+cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uint16_t* scales,
+                                const uint16_t* b_rows, const int32_t* offsets, int E, int R, int H, int I,
                                 int router_E, void* out, int32_t* st_word, cudaStream_t st);
 
 // combine.cu

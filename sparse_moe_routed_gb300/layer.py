@@ -19,12 +19,30 @@ from . import _lib
 
 
 class MoELayer:
-    def __init__(self, w_router, bias, w_gateup, w_down, k: int, T_max: int):
+    """Buffers and calls of one layer.
+
+    bf16 weights: w_gateup [E,2I,H] bf16, w_down [E,H,I] bf16.
+    int4 weights (fmt=MOE_W_INT4_G64): w_gateup [E,2I,H/2] uint8 codes,
+    w_down [E,H,I/2] uint8 codes, s_gateup [E,H/64,2I] and s_down [E,I/64,H]
+    bf16 scales (group-major).
+    """
+
+    def __init__(self, w_router, bias, w_gateup, w_down, k: int, T_max: int, fmt: int = _lib.MOE_W_BF16,
+                 s_gateup=None, s_down=None):
         assert w_router.is_cuda and w_router.dtype == torch.bfloat16
         self.E, self.H = w_router.shape
         self.I = w_gateup.shape[1] // 2
-        assert w_gateup.shape == (self.E, 2 * self.I, self.H)
-        assert w_down.shape == (self.E, self.H, self.I)
+        self.fmt = fmt
+        if fmt == _lib.MOE_W_BF16:
+            assert w_gateup.shape == (self.E, 2 * self.I, self.H)
+            assert w_down.shape == (self.E, self.H, self.I)
+            assert s_gateup is None and s_down is None
+        else:
+            assert w_gateup.dtype == torch.uint8 and w_gateup.shape == (self.E, 2 * self.I, self.H // 2)
+            assert w_down.dtype == torch.uint8 and w_down.shape == (self.E, self.H, self.I // 2)
+            assert s_gateup.shape == (self.E, self.H // 64, 2 * self.I)
+            assert s_down.shape == (self.E, self.I // 64, self.H)
+        self.s_gateup, self.s_down = s_gateup, s_down
         self.k = k
         self.T_max = T_max
         self.w_router, self.bias, self.w_gateup, self.w_down = w_router, bias, w_gateup, w_down
@@ -48,16 +66,22 @@ class MoELayer:
         self._bound = {}
 
     # -- the five boundary calls, bound once per (T, x, out, stream) ---------
-    def bound_calls(self, x, T=None, out=None, stream=None):
-        """[(name, fn, args)] of the five C-ABI calls for this input.
+    def bound_calls(self, x, T=None, out=None, stream=None, residual=None, out_f32=None, route=True):
+        """[(name, fn, args)] of the C-ABI calls for this input.
 
         Pointers and sizes are converted to ctypes once and cached, so issuing
-        a layer costs five foreign calls and nothing else on the host.
+        a layer costs five foreign calls and nothing else on the host.  With
+        residual/out_f32 the combine adds the fp32 residual and writes fp32
+        (the residual stream of a stack); route=False leaves out moe_route
+        (the caller filled self.ids / self.w).
         """
         T = x.shape[0] if T is None else T
         s = torch.cuda.current_stream() if stream is None else stream
-        out = self.out[:T] if out is None else out
-        key = (T, x.data_ptr(), out.data_ptr(), s.cuda_stream)
+        if out_f32 is None:
+            out = self.out[:T] if out is None else out
+        key = (T, x.data_ptr(), None if out is None else out.data_ptr(), s.cuda_stream,
+               None if residual is None else residual.data_ptr(), None if out_f32 is None else out_f32.data_ptr(),
+               route)
         calls = self._bound.get(key)
         if calls is not None:
             return calls
@@ -69,21 +93,23 @@ class MoELayer:
         R = T * self.k
         E, H, I, k = self.E, self.H, self.I, self.k
         ws_bytes = self.ws.numel()
-        calls = [
-            ("moe_route", lib.moe_route,
-             (P(x), P(self.w_router), P(self.bias), T, H, E, k, P(self.ids), P(self.w), P(self.gap), P(self.ws),
-              ws_bytes, st)),
+        calls = []
+        if route:
+            calls.append(("moe_route", lib.moe_route,
+                          (P(x), P(self.w_router), P(self.bias), T, H, E, k, P(self.ids), P(self.w), P(self.gap),
+                           P(self.ws), ws_bytes, st)))
+        calls += [
             ("moe_permute", lib.moe_permute,
              (P(self.ids), T, k, E, P(x), H, P(self.counts), P(self.offsets), P(self.perm), P(self.inv),
               P(self.x_perm), P(self.status), st)),
             ("moe_expert_gateup", lib.moe_expert_gateup,
-             (P(self.x_perm), P(self.offsets), R, E, H, I, _lib.MOE_W_BF16, P(self.w_gateup), None, P(self.h),
+             (P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt, P(self.w_gateup), P(self.s_gateup), P(self.h),
               P(self.status), st)),
             ("moe_expert_down", lib.moe_expert_down,
-             (P(self.h), P(self.offsets), R, E, H, I, _lib.MOE_W_BF16, P(self.w_down), None, P(self.y_perm),
+             (P(self.h), P(self.offsets), R, E, H, I, self.fmt, P(self.w_down), P(self.s_down), P(self.y_perm),
               P(self.status), st)),
             ("moe_combine", lib.moe_combine,
-             (P(self.y_perm), P(self.inv), P(self.w), T, k, H, None, P(out), None, P(self.status), st)),
+             (P(self.y_perm), P(self.inv), P(self.w), T, k, H, P(residual), P(out), P(out_f32), P(self.status), st)),
         ]
         self._bound[key] = calls
         return calls
@@ -131,3 +157,53 @@ class MoELayer:
 
     def clear_status(self):
         self.status.zero_()
+
+
+class MoEStack:
+    """A residual stack of MoE layers: x <- x + MoE_l(RMSNorm(x)), l = 0..L-1.
+
+    x is an fp32 residual stream [T,H] updated in place; each layer runs
+    moe_rmsnorm (fp32 -> bf16, zero-centred gain 1 + gamma) and the five layer
+    calls, the combine adding the residual and writing fp32 back into x.
+    """
+
+    def __init__(self, layers, T_max: int, eps: float = 1e-6, gammas=None):
+        self.layers = list(layers)
+        self.eps = eps
+        self.gammas = gammas
+        H = self.layers[0].H
+        dev = self.layers[0].w_router.device
+        self.T_max = T_max
+        self.n = torch.empty((T_max, H), dtype=torch.bfloat16, device=dev)
+        self._norm_bound = {}
+
+    def _norm_call(self, x, l, s):
+        key = (x.data_ptr(), x.shape[0], l, s.cuda_stream)
+        c = self._norm_bound.get(key)
+        if c is None:
+            lib = _lib.load()
+            P = _lib._ptr
+            g = None if self.gammas is None else self.gammas[l]
+            T, H = x.shape
+            c = ("moe_rmsnorm", lib.moe_rmsnorm,
+                 (P(x), P(g), C.c_float(self.eps), T, H, P(self.n), C.c_void_p(s.cuda_stream)))
+            if len(self._norm_bound) > 4096:
+                self._norm_bound.clear()
+            self._norm_bound[key] = c
+        return c
+
+    def layer_calls(self, x, l, stream=None, route=True):
+        s = torch.cuda.current_stream() if stream is None else stream
+        T = x.shape[0]
+        L = self.layers[l]
+        return [self._norm_call(x, l, s)] + L.bound_calls(self.n[:T], T, stream=s, residual=x, out_f32=x,
+                                                         route=route)
+
+    def forward(self, x, stream=None, layers=None):
+        """x [T,H] fp32 on the GPU, updated in place through the layers."""
+        assert x.dtype == torch.float32 and x.is_contiguous()
+        for l in (range(len(self.layers)) if layers is None else layers):
+            for call in self.layer_calls(x, l, stream):
+                MoELayer.issue(call)
+        return x
+

@@ -1,0 +1,148 @@
+"""GPU parity of the int4 g64 path and of the residual stack.
+
+A stack layer is x <- x + MoE(RMSNorm(x)) with int4 g64 expert weights and a
+bf16 router (the 48-layer workload of the Qwen4Exp routed stack).  The oracle
+dequantises exactly and runs in fp64; the router and experts on both sides
+read the RMS-normalised residual rounded to bf16.  Tolerances: tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from parity import GAP_TOL, assert_output_close, compare_routes
+from sparse_moe_routed_gb300 import MoELayer, MoEStack, _lib
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+CFG = wl.STACK48
+_W = {}
+
+
+def layer_weights(l):
+    if l not in _W:
+        w = wl.stack_layer_weights(l, DEV)
+        torch.cuda.synchronize()
+        w["host"] = {
+            "wr": oracle.bf16_bits(w["w_router"]),
+            "wgu_q": w["w_gateup_q"].cpu().numpy(), "sgu": oracle.bf16_bits(w["s_gateup"]),
+            "wd_q": w["w_down_q"].cpu().numpy(), "sd": oracle.bf16_bits(w["s_down"]),
+        }
+        _W[l] = w
+    return _W[l]
+
+
+def make_stack(L, T):
+    mls = []
+    for l in range(L):
+        w = layer_weights(l)
+        mls.append(MoELayer(w["w_router"], None, w["w_gateup_q"], w["w_down_q"], CFG.k, T, fmt=_lib.MOE_W_INT4_G64,
+                            s_gateup=wl.scales_group_major(w["s_gateup"]),
+                            s_down=wl.scales_group_major(w["s_down"])))
+    return MoEStack(mls, T)
+
+
+def oracle_layer(x_np, l, ids=None, w=None):
+    """One oracle stack layer on fp32 residual rows x_np: (x + MoE(n), ids, w, gap, logits)."""
+    h = layer_weights(l)["host"]
+    n_bits = oracle.round_bf16_bits(oracle.rmsnorm(x_np, None, eps=1e-6))
+    ids_r, w_r, gap_r, L_r = oracle.route(n_bits, h["wr"], None, CFG.k)
+    if ids is None:
+        ids, w = ids_r, w_r
+    moe = oracle.experts_combine(oracle.bits_to_f32(n_bits), ids, w, CFG.H, CFG.I, wgu_q=h["wgu_q"],
+                                 sgu_bits=h["sgu"], wd_q=h["wd_q"], sd_bits=h["sd"])
+    return (x_np.astype(np.float64) + moe).astype(np.float32), moe, ids_r, w_r, gap_r, L_r
+
+
+@pytest.mark.parametrize("T", [16, 37])
+def test_int4_stack_layer_parity(T):
+    stack = make_stack(1, T)
+    x0 = wl.token_batch(CFG, DEV, index=5, T=T).float()
+    x = x0.clone()
+    stack.forward(x)
+    torch.cuda.synchronize()
+    L0 = stack.layers[0]
+    assert L0.read_status() == 0
+    x0_np = x0.cpu().numpy()
+    x_ref, moe_ref, ids_r, w_r, gap_r, L_r = oracle_layer(x0_np, 0)
+    rep = compare_routes(L0.ids[:T].cpu().numpy(), L0.w[:T].cpu().numpy(), ids_r, w_r, gap_r, L_r)
+    keep = np.array(rep["exact_rows"])
+    assert len(keep) >= 0.9 * T, rep
+    moe_gpu = (x.cpu().numpy().astype(np.float64) - x0_np)[keep]
+    rel_max, mean_rel = assert_output_close(moe_gpu, moe_ref[keep], what="int4 stack layer MoE output")
+    print(f"T={T}: {len(keep)}/{T} tokens graded, max err {rel_max:.2e} of max|ref|, mean rel {mean_rel:.2e}")
+
+
+def test_int4_expert_stage_tiny_geometry():
+    """int4 contraction on the tiny geometry (one 128-row block, K = 256 / 64)."""
+    cfg = wl.TINY
+    d = wl.layer_inputs(cfg, DEV)
+    q_gu, s_gu = wl.quantize_int4_g64(d["w_gateup"])
+    q_d, s_d = wl.quantize_int4_g64(d["w_down"])
+    rng = np.random.default_rng(3)
+    ids_np = np.stack([rng.choice(cfg.E, size=cfg.k, replace=False) for _ in range(cfg.T)]).astype(np.int32)
+    _, offsets_r, perm_r, _ = oracle.permute(ids_np, cfg.E)
+    R = cfg.T * cfg.k
+    ids = torch.from_numpy(ids_np).to(DEV)
+    counts = torch.empty((cfg.E,), dtype=torch.int32, device=DEV)
+    offsets = torch.empty((cfg.E + 1,), dtype=torch.int32, device=DEV)
+    perm = torch.empty((R,), dtype=torch.int32, device=DEV)
+    inv = torch.empty((R,), dtype=torch.int32, device=DEV)
+    xp = torch.empty((R, cfg.H), dtype=torch.bfloat16, device=DEV)
+    h = torch.empty((R, cfg.I), dtype=torch.bfloat16, device=DEV)
+    y = torch.full((R, cfg.H), float("nan"), dtype=torch.float32, device=DEV)
+    st = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    _lib.moe_permute(ids, cfg.E, d["x"], counts, offsets, perm, inv, xp, st)
+    _lib.moe_grouped_swiglu(xp, offsets, cfg.E, cfg.H, cfg.I, q_gu, q_d, h, y, st, fmt=_lib.MOE_W_INT4_G64,
+                            s_gateup=wl.scales_group_major(s_gu), s_down=wl.scales_group_major(s_d))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    xin = oracle.bits_to_f32(oracle.bf16_bits(d["x"]))
+    wgu = oracle.dequant_int4(q_gu.cpu().numpy(), oracle.bf16_bits(s_gu))
+    wdn = oracle.dequant_int4(q_d.cpu().numpy(), oracle.bf16_bits(s_d))
+    # expected per slot through the oracle's int4 expert (one route per row, weight 1)
+    seg_e = np.searchsorted(offsets_r, np.arange(R), side="right") - 1
+    tok = perm_r // cfg.k
+    ref = oracle.experts_combine(xin[tok], seg_e.reshape(R, 1).astype(np.int32), np.ones((R, 1), np.float32),
+                                 cfg.H, cfg.I, wgu_q=q_gu.cpu().numpy(), sgu_bits=oracle.bf16_bits(s_gu),
+                                 wd_q=q_d.cpu().numpy(), sd_bits=oracle.bf16_bits(s_d))
+    assert np.isfinite(wgu).all() and np.isfinite(wdn).all()
+    assert_output_close(y.cpu().numpy(), ref, what="int4 expert outputs (tiny)")
+
+
+def test_int4_stack_forced_routes_six_layers():
+    """Six layers free-running with the oracle's routes imposed on the GPU:
+    the residual streams must agree to the stated tolerance."""
+    T, L = 16, 6
+    stack = make_stack(L, T)
+    x0 = wl.token_batch(CFG, DEV, index=9, T=T).float()
+    x = x0.clone()
+    x_o = x0.cpu().numpy()
+    for l in range(L):
+        x_o_next, _, ids_r, w_r, _, _ = oracle_layer(x_o, l)
+        ml = stack.layers[l]
+        ml.ids[:T].copy_(torch.from_numpy(ids_r))
+        ml.w[:T].copy_(torch.from_numpy(w_r))
+        for call in stack.layer_calls(x, l, route=False):
+            MoELayer.issue(call)
+        x_o = x_o_next
+    torch.cuda.synchronize()
+    for ml in stack.layers:
+        assert ml.read_status() == 0
+    x0_np = x0.cpu().numpy().astype(np.float64)
+    rel_max, mean_rel = assert_output_close(x.cpu().numpy() - x0_np, x_o - x0_np, what="6-layer residual update")
+    print(f"6 layers forced routes: max err {rel_max:.2e} of max|ref|, mean rel {mean_rel:.2e}")
+
+
+def test_stack_is_deterministic():
+    T = 16
+    stack = make_stack(3, T)
+    x0 = wl.token_batch(CFG, DEV, index=2, T=T).float()
+    a = x0.clone()
+    b = x0.clone()
+    stack.forward(a)
+    stack.forward(b)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)

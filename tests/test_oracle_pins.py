@@ -350,3 +350,16 @@ def test_combine_alone_linearity_and_hand_case():
     out2 = oracle.combine(y2, np.array([1, 0], np.int32), np.array([[0.75, 0.25]], np.float32),
                           residual=np.array([[100.0, 200.0]], np.float32))
     assert np.allclose(out2[0], [100 + 0.75 * 10 + 0.25 * 1, 200 + 0.75 * 20 + 0.25 * 2])
+
+
+def test_round_bf16_hand_cases_and_library():
+    import torch
+    vals = np.array([1.0, 1.0 + 2**-8, 1.0 + 3 * 2**-8, -2.5, 3.0e38, 0.0, -0.0, 1.0 + 2**-8 + 2**-20],
+                    np.float32)
+    got = oracle.round_bf16_bits(vals)
+    assert list(got[:7]) == [0x3F80, 0x3F80, 0x3F82, 0xC020, 0x7F62, 0x0000, 0x8000]
+    assert got[7] == 0x3F81  # just above the tie rounds up
+    rng = np.random.default_rng(12)
+    r = (rng.standard_normal(4096) * 10.0 ** rng.integers(-6, 6, 4096)).astype(np.float32)
+    ref = torch.from_numpy(r).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.round_bf16_bits(r), ref)
