@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="decode", choices=["decode", "prefill"])
+    ap.add_argument("--config", default="decode", choices=["decode", "prefill", "stack48", "sweep"])
     ap.add_argument("--layers", type=int, default=0, help="distinct layer weight sets rotated (0 = auto)")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (small profiling case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -246,6 +246,8 @@ def main():
         dist.barrier()
     import workloads as wl
 
+    if args.config in ("stack48", "sweep"):
+        return run_stack(args, rank, world, local, dev)
     cfg = wl.CONFIGS[args.config]
     if args.experts:
         from dataclasses import replace
@@ -417,6 +419,139 @@ def main():
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": 7 * K,
     }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_stack(args, rank, world, local, dev):
+    """48-layer int4 g64 residual stack over 32 decode blocks of 16 tokens
+    (stack48), or the route-prediction / dedup sweep over it (sweep)."""
+    import torch
+    import torch.distributed as dist
+    import workloads as wl
+    from sparse_moe_routed_gb300 import MoELayer, MoEStack, _lib
+    from sparse_moe_routed_gb300.sweep import route_sweep
+
+    cfg = wl.STACK48
+    L = args.layers or wl.STACK_LAYERS
+    NB = wl.STACK_BLOCKS
+    T = cfg.T if args.config == "stack48" else NB * cfg.T
+    mls = []
+    for l in range(L):
+        w = wl.stack_layer_weights(l, dev)
+        mls.append(MoELayer(w["w_router"], None, w["w_gateup_q"], w["w_down_q"], cfg.k, T, fmt=_lib.MOE_W_INT4_G64,
+                            s_gateup=wl.scales_group_major(w["s_gateup"]),
+                            s_down=wl.scales_group_major(w["s_down"])))
+        del w
+    stack = MoEStack(mls, T)
+    torch.cuda.synchronize()
+    pk = peaks()
+    st = torch.cuda.current_stream()
+    rec_bytes = 2 * cfg.I * cfg.H // 2 + cfg.H * cfg.I // 2 + (2 * cfg.I * cfg.H // 64 + cfg.H * cfg.I // 64) * 2
+    router_bytes = cfg.E * cfg.H * 2
+
+    if args.config == "sweep":
+        preds = [wl.predictor_weights(cfg.H, cfg.E, l, dev) for l in range(L)]
+        x0 = torch.cat([wl.token_batch(cfg, dev, index=b, T=cfg.T) for b in range(NB)]).float()
+        for _ in range(max(args.warmup, 1)):
+            route_sweep(stack, x0, preds)
+        torch.cuda.synchronize()
+        reps = max(1, min(args.steps, 5))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            res = route_sweep(stack, x0, preds)
+        el = (time.perf_counter() - t0) / reps
+        line = {"metric": METRIC, "value": T / el, "unit": UNIT, "n_gpus": world, "steps": reps,
+                "warmup": args.warmup, "ms_per_step": 1e3 * el, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "int4 g64 experts, bf16 router", "data": "synthetic",
+                "config": {"workload": f"route_sweep_L{L}_T{T}_blocks1-4-16-64", "layers": L, "tokens": T},
+                "sweep": res["summary"], "device_status": res["status"]}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    xs = [wl.token_batch(cfg, dev, index=b, T=T).float() for b in range(NB)]
+    xw = torch.empty_like(xs[0])
+    for i in range(max(args.warmup, 3)):
+        xw.copy_(xs[i % NB])
+        stack.forward(xw)
+    torch.cuda.synchronize()
+    # unique experts per layer of one block (for the byte accounting)
+    xw.copy_(xs[0])
+    Ul = []
+    for l in range(L):
+        for call in stack.layer_calls(xw, l):
+            MoELayer.issue(call)
+        torch.cuda.synchronize()
+        Ul.append(int((stack.layers[l].counts > 0).sum().item()))
+    bytes_block = sum(u * rec_bytes for u in Ul) + L * router_bytes
+    K = args.steps
+    EV = 7 if K >= 64 else 1
+    KE = (K + EV - 1) // EV
+    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_uuid(local))
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    tw0 = time.time()
+    e0.record(st)
+    for i in range(K):
+        xw.copy_(xs[i % NB])
+        lt = i % L
+        for l in range(L):
+            calls = stack.layer_calls(xw, l, stream=st)
+            if l == lt and i % EV == 0:
+                for c in calls[:3]:
+                    MoELayer.issue(c)
+                g0[i // EV].record(st)
+                MoELayer.issue(calls[3])
+                g1[i // EV].record(st)
+                for c in calls[4:]:
+                    MoELayer.issue(c)
+            else:
+                for c in calls:
+                    MoELayer.issue(c)
+    e1.record(st)
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    sampler.stop()
+    total_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    for ml in stack.layers:
+        assert ml.read_status() == 0, f"device status {ml.read_status():#x}"
+    gu = [g0[j].elapsed_time(g1[j]) for j in range(KE)]
+    gu_avg = sum(gu) / KE
+    R = T * cfg.k
+    gu_bytes = sum((Ul[(j * EV) % L] * (2 * cfg.I * cfg.H // 2 + 2 * cfg.I * cfg.H // 64 * 2) + R * cfg.H * 2 +
+                    R * cfg.I * 2) for j in range(KE)) / KE
+    step_ms = total_ms / K
+    line = {"metric": METRIC, "value": T * K * world / (total_ms / 1e3), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int4 g64 experts (bf16 tensor-core operands), bf16 router, fp32 residual",
+            "data": "synthetic (seeded)",
+            "config": {"workload": f"stack48_int4g64_L{L}_T{T}_blocks{NB}", "layers": L, "T": T, "blocks": NB,
+                       "unique_experts_per_layer_block0": Ul,
+                       "l2": f"inputs larger than L2: {L} layers of int4 experts "
+                             f"({L * (cfg.E * rec_bytes + router_bytes) / 1e9:.1f} GB) streamed per block"},
+            "roofline": {"bound": "hbm", "kernel": "grouped_gemm_kernel int4 (moe_expert_gateup)",
+                         "achieved": gu_bytes / (gu_avg / 1e3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gu_bytes / (gu_avg / 1e3) / 1e9 / pk["hbm_gbs"], "traffic": None,
+                         "bytes_per_launch": gu_bytes, "avg_launch_us": gu_avg * 1e3},
+            "layer_roofline": {"bytes_per_block": bytes_block,
+                               "achieved_gbs": bytes_block / (step_ms / 1e3) / 1e9,
+                               "frac_hbm": bytes_block / (step_ms / 1e3) / 1e9 / pk["hbm_gbs"]},
+            "clocks": sampler.summary(tw0, tw1), "gpu_launches": 6 * L * K}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -242,10 +242,28 @@ MOE_API moe_status route_block_dedup(const int32_t *ids, int L, int T_tot, int k
  * (zero-centred RMS normalisation: the gain is 1 + gamma).
  *
  *   out[t,h] = bf16( x[t,h] / sqrt(mean_h x[t,:]^2 + eps) * (1 + gamma[h]) )
- *   x [T,H] f32, gamma [H] f32 or NULL (-> 0), out [T,H] bf16
+ *   raw_bf16[t,h] = bf16( x[t,h] )  if raw_bf16 != NULL (the representation
+ *                   before normalisation, read by a route predictor)
+ *   x [T,H] f32, gamma [H] f32 or NULL (-> 0), out / raw_bf16 [T,H] bf16
  * ------------------------------------------------------------------------- */
 MOE_API moe_status moe_rmsnorm(const float *x, const float *gamma, float eps, int T, int H, uint16_t *out,
-                       void *stream);
+                               uint16_t *raw_bf16, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_route_recall -- how many of a token's native experts a predicted route
+ * names.
+ *
+ * Source: AFN-019, section "Hypothesis H2: predict expert routes before
+ * attention, not after it" (a pre-attention predictor may move bytes but
+ * never chooses experts; zero-training controls: the previous token's
+ * same-layer route, the native router on an earlier representation).
+ *
+ *   hits[t] = | {pred_ids[t,:]} intersect {ref_ids[t,:]} |   (0..k)
+ *   pred_ids, ref_ids [T,k] int32, each row k distinct IDs; hits [T] int32.
+ *   recall = hits / k; exact top-k set match = (hits == k).
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_route_recall(const int32_t *pred_ids, const int32_t *ref_ids, int T, int k,
+                                    int32_t *hits, void *stream);
 
 #ifdef __cplusplus
 }

@@ -25,6 +25,7 @@ Functions and the page passages they follow (Hebrus "Agent Field Notes"):
                         symmetric-scale reading.
   combine(...)          AFN-019, section "Hypothesis H4" (weighted sum in route-rank order).
   rmsnorm(...)          AFN-001, section "Phase 1" (zero-centred RMS normalisation).
+  recall_hits(...)      AFN-019, section "Hypothesis H2" (predicted vs exact top-k).
   round_bf16_bits(...)  bf16 rounding of the normalised stack input (reading: router and
                         experts consume bf16 activations).
 
@@ -64,6 +65,7 @@ def _load():
         lib.oracle_combine.argtypes = [p, p, p, i, i, i, p, p]
         lib.oracle_rmsnorm.argtypes = [p, p, i, i, C.c_double, p]
         lib.oracle_round_bf16.argtypes = [p, C.c_size_t, p]
+        lib.oracle_recall.argtypes = [p, p, i, i, p]
         lib.oracle_dedup.argtypes = [p, i, i, i, i, i, i, i, p, p, p, p]
         lib.oracle_dedup.restype = i
         _lib = lib
@@ -196,6 +198,16 @@ def rmsnorm(x, gamma=None, eps=1e-6):
     out = np.empty_like(xc)
     _load().oracle_rmsnorm(_ptr(xc), _ptr(_c(gamma, np.float32)), T, H, float(eps), _ptr(out))
     return out
+
+
+def recall_hits(pred, ref):
+    """hits[t] = |set(pred[t]) & set(ref[t])| for [T,k] routes."""
+    pc = _c(pred, np.int32)
+    rc = _c(ref, np.int32)
+    T, k = rc.shape
+    hits = np.empty((T,), np.int32)
+    _load().oracle_recall(_ptr(pc), _ptr(rc), T, k, _ptr(hits))
+    return hits
 
 
 def round_bf16_bits(x):

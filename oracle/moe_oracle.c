@@ -279,6 +279,22 @@ void oracle_combine(const float *y, const int32_t *inv, const float *w, int T, i
     }
 }
 
+/* ---- recall of a predicted route ------------------------------------------
+ * hits[t] = |{pred[t,:]} intersect {ref[t,:]}| (AFN-019, section
+ * "Hypothesis H2": a predictor is scored against the exact top-k).          */
+void oracle_recall(const int32_t *pred, const int32_t *ref, int T, int k, int32_t *hits) {
+  for (int t = 0; t < T; ++t) {
+    int h = 0;
+    for (int j = 0; j < k; ++j)
+      for (int i = 0; i < k; ++i)
+        if (ref[(size_t)t * k + j] == pred[(size_t)t * k + i]) {
+          ++h;
+          break;
+        }
+    hits[t] = h;
+  }
+}
+
 /* fp32 -> bf16 bit patterns, round to nearest, ties to even (NaN kept
  * quiet).  The router and experts of a stack layer read the RMS-normalised
  * residual rounded to bf16, as their tensor-core inputs are bf16.           */

@@ -62,7 +62,8 @@ def load(path: str | None = None):
             "moe_grouped_swiglu": ([p, p, i, i, i, i, i, p, p, p, p, p, p, p, p], i),
             "moe_combine": ([p, p, p, i, i, i, p, p, p, p, p], i),
             "route_block_dedup": ([p, i, i, i, i, i, i, i, p, p, p, p, p, p], i),
-            "moe_rmsnorm": ([p, p, f, i, i, p, p], i),
+            "moe_rmsnorm": ([p, p, f, i, i, p, p, p], i),
+            "moe_route_recall": ([p, p, i, i, p, p], i),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -171,7 +172,13 @@ def route_block_dedup(ids, E, block, H, I, mask, U, bytes2, bytes4, dev_status, 
     _check("route_block_dedup", st)
 
 
-def moe_rmsnorm(x, gamma, eps, out, stream=None):
+def moe_rmsnorm(x, gamma, eps, out, raw_bf16=None, stream=None):
     T, H = x.shape
-    st = load().moe_rmsnorm(_ptr(x), _ptr(gamma), float(eps), T, H, _ptr(out), _stream(stream))
+    st = load().moe_rmsnorm(_ptr(x), _ptr(gamma), float(eps), T, H, _ptr(out), _ptr(raw_bf16), _stream(stream))
     _check("moe_rmsnorm", st)
+
+
+def moe_route_recall(pred_ids, ref_ids, hits, stream=None):
+    T, k = ref_ids.shape
+    st = load().moe_route_recall(_ptr(pred_ids), _ptr(ref_ids), T, k, _ptr(hits), _stream(stream))
+    _check("moe_route_recall", st)

@@ -233,14 +233,25 @@ moe_status route_block_dedup(const int32_t* ids, int L, int T_tot, int k, int E,
                                        static_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_rmsnorm(const float* x, const float* gamma, float eps, int T, int H, uint16_t* out, void* stream) {
+moe_status moe_rmsnorm(const float* x, const float* gamma, float eps, int T, int H, uint16_t* out,
+                       uint16_t* raw_bf16, void* stream) {
   if (T < 0 || H <= 0) return MOE_ESHAPE;
   if (H % 128 != 0 || H > 16384) return MOE_ENOTSUP;
   if (!(eps >= 0.0f)) return MOE_EINVAL;
   if (!x || !out) return MOE_EINVAL;
-  if (!a16(x) || !a16(out) || (gamma && !a16(gamma))) return MOE_EINVAL;
+  if (!a16(x) || !a16(out) || (gamma && !a16(gamma)) || (raw_bf16 && !a16(raw_bf16))) return MOE_EINVAL;
   if (T == 0) return MOE_OK;
-  return cuda_status(moe::launch_rmsnorm(x, gamma, eps, T, H, out, static_cast<cudaStream_t>(stream)));
+  return cuda_status(moe::launch_rmsnorm(x, gamma, eps, T, H, out, raw_bf16, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_route_recall(const int32_t* pred_ids, const int32_t* ref_ids, int T, int k, int32_t* hits,
+                            void* stream) {
+  if (T < 0 || k <= 0) return MOE_ESHAPE;
+  if (k > moe::kMaxK) return MOE_ENOTSUP;
+  if (!pred_ids || !ref_ids || !hits) return MOE_EINVAL;
+  if (!a4(pred_ids) || !a4(ref_ids) || !a4(hits)) return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  return cuda_status(moe::launch_recall(pred_ids, ref_ids, T, k, hits, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

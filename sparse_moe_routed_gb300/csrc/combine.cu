@@ -13,6 +13,11 @@
 //
 // Both kernels are HBM/L2-bound gathers: 16-byte loads, one CTA per
 // (token, 512 columns) for the combine, one CTA per token row for RMSNorm.
+//
+// The recall kernel scores a predicted route against the native one (AFN-019,
+// section "Hypothesis H2: predict expert routes before attention, not after
+// it": a predictor may move bytes but never chooses experts; it is judged by
+// how many of the exact top-k it names).
 #include <math.h>
 
 #include "common.cuh"
@@ -81,7 +86,7 @@ constexpr int kNormThreads = 256;
 
 __global__ void __launch_bounds__(kNormThreads)
     rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ gamma, float eps, int H,
-                   uint16_t* __restrict__ out) {
+                   uint16_t* __restrict__ out, uint16_t* __restrict__ raw) {
   __shared__ float part[kNormThreads / 32];
   pdl_wait();
   pdl_trigger();
@@ -117,7 +122,32 @@ __global__ void __launch_bounds__(kNormThreads)
     pk.y = static_cast<uint32_t>(f32_to_bf16(v.z * r * (1.f + g[2]))) |
            (static_cast<uint32_t>(f32_to_bf16(v.w * r * (1.f + g[3]))) << 16);
     reinterpret_cast<uint2*>(out + static_cast<size_t>(t) * H)[c] = pk;
+    if (raw) {
+      uint2 rk;
+      rk.x = static_cast<uint32_t>(f32_to_bf16(v.x)) | (static_cast<uint32_t>(f32_to_bf16(v.y)) << 16);
+      rk.y = static_cast<uint32_t>(f32_to_bf16(v.z)) | (static_cast<uint32_t>(f32_to_bf16(v.w)) << 16);
+      reinterpret_cast<uint2*>(raw + static_cast<size_t>(t) * H)[c] = rk;
+    }
   }
+}
+
+// Recall of a predicted route against the native one: one warp per token;
+// lane j < k holds the j-th native expert and tests it against the k
+// predicted experts (both routes hold k distinct IDs).
+__global__ void __launch_bounds__(256) recall_kernel(const int32_t* __restrict__ pred,
+                                                     const int32_t* __restrict__ ref, int T, int k,
+                                                     int32_t* __restrict__ hits) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int mine = (lane < k) ? ref[static_cast<size_t>(t) * k + lane] : -1;
+  const int p = (lane < k) ? pred[static_cast<size_t>(t) * k + lane] : -2;
+  bool found = false;
+  for (int i = 0; i < k; ++i) found |= (__shfl_sync(0xffffffffu, p, i) == mine);
+  const unsigned m = __ballot_sync(0xffffffffu, found && lane < k);
+  if (lane == 0) hits[t] = __popc(m);
 }
 
 }  // namespace
@@ -131,8 +161,12 @@ cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, i
 }
 
 cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, int T, int H, uint16_t* out,
-                           cudaStream_t st) {
-  return launch_pdl(rmsnorm_kernel, dim3(T), dim3(kNormThreads), 0, st, x, gamma, eps, H, out);
+                           uint16_t* raw, cudaStream_t st) {
+  return launch_pdl(rmsnorm_kernel, dim3(T), dim3(kNormThreads), 0, st, x, gamma, eps, H, out, raw);
+}
+
+cudaError_t launch_recall(const int32_t* pred, const int32_t* ref, int T, int k, int32_t* hits, cudaStream_t st) {
+  return launch_pdl(recall_kernel, dim3((T + 7) / 8), dim3(256), 0, st, pred, ref, T, k, hits);
 }
 
 }  // namespace moe

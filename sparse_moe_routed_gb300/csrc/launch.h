@@ -63,7 +63,9 @@ cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, i
                            int R, const float* residual, uint16_t* out_bf16, float* out_f32,
                            int32_t* st_word, cudaStream_t st);
 cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, int T, int H,
-                           uint16_t* out, cudaStream_t st);
+                           uint16_t* out, uint16_t* raw, cudaStream_t st);
+cudaError_t launch_recall(const int32_t* pred, const int32_t* ref, int T, int k, int32_t* hits,
+                          cudaStream_t st);
 
 // dedup.cu
 cudaError_t launch_dedup(const int32_t* ids, int L, int Ttot, int k, int E, int B, long long P,

@@ -177,8 +177,8 @@ class MoEStack:
         self.n = torch.empty((T_max, H), dtype=torch.bfloat16, device=dev)
         self._norm_bound = {}
 
-    def _norm_call(self, x, l, s):
-        key = (x.data_ptr(), x.shape[0], l, s.cuda_stream)
+    def _norm_call(self, x, l, s, raw=None):
+        key = (x.data_ptr(), x.shape[0], l, s.cuda_stream, None if raw is None else raw.data_ptr())
         c = self._norm_bound.get(key)
         if c is None:
             lib = _lib.load()
@@ -186,18 +186,20 @@ class MoEStack:
             g = None if self.gammas is None else self.gammas[l]
             T, H = x.shape
             c = ("moe_rmsnorm", lib.moe_rmsnorm,
-                 (P(x), P(g), C.c_float(self.eps), T, H, P(self.n), C.c_void_p(s.cuda_stream)))
+                 (P(x), P(g), C.c_float(self.eps), T, H, P(self.n), P(raw), C.c_void_p(s.cuda_stream)))
             if len(self._norm_bound) > 4096:
                 self._norm_bound.clear()
             self._norm_bound[key] = c
         return c
 
-    def layer_calls(self, x, l, stream=None, route=True):
+    def layer_calls(self, x, l, stream=None, route=True, raw=None):
+        """Calls of layer l on the residual stream x; raw (optional, [T,H]
+        bf16) receives x rounded to bf16 before normalisation."""
         s = torch.cuda.current_stream() if stream is None else stream
         T = x.shape[0]
         L = self.layers[l]
-        return [self._norm_call(x, l, s)] + L.bound_calls(self.n[:T], T, stream=s, residual=x, out_f32=x,
-                                                         route=route)
+        return [self._norm_call(x, l, s, raw)] + L.bound_calls(self.n[:T], T, stream=s, residual=x, out_f32=x,
+                                                              route=route)
 
     def forward(self, x, stream=None, layers=None):
         """x [T,H] fp32 on the GPU, updated in place through the layers."""

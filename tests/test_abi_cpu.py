@@ -27,7 +27,7 @@ def lib():
 def test_library_loads_and_exports_every_declared_symbol():
     L = lib()
     names = _lib.declared_functions()
-    assert len(names) == 13
+    assert len(names) == 14
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 100
@@ -147,9 +147,18 @@ def test_dedup_rejections():
 
 def test_rmsnorm_rejections():
     L = lib()
-    assert L.moe_rmsnorm(P, NUL, C.c_float(-1.0), 4, 2560, P, NUL) == _lib.MOE_EINVAL
-    assert L.moe_rmsnorm(P, NUL, C.c_float(1e-6), 4, 2500, P, NUL) == _lib.MOE_ENOTSUP
-    assert L.moe_rmsnorm(NUL, NUL, C.c_float(1e-6), 4, 2560, P, NUL) == _lib.MOE_EINVAL
+    assert L.moe_rmsnorm(P, NUL, C.c_float(-1.0), 4, 2560, P, NUL, NUL) == _lib.MOE_EINVAL
+    assert L.moe_rmsnorm(P, NUL, C.c_float(1e-6), 4, 2500, P, NUL, NUL) == _lib.MOE_ENOTSUP
+    assert L.moe_rmsnorm(NUL, NUL, C.c_float(1e-6), 4, 2560, P, NUL, NUL) == _lib.MOE_EINVAL
+    assert L.moe_rmsnorm(P, NUL, C.c_float(1e-6), 4, 2560, P, PM, NUL) == _lib.MOE_EINVAL
+
+
+def test_recall_rejections():
+    L = lib()
+    assert L.moe_route_recall(P, NUL, 4, 10, P, NUL) == _lib.MOE_EINVAL
+    assert L.moe_route_recall(P, P, 4, 33, P, NUL) == _lib.MOE_ENOTSUP
+    assert L.moe_route_recall(P, P, -1, 10, P, NUL) == _lib.MOE_ESHAPE
+    assert L.moe_route_recall(P, P, 0, 10, P, NUL) == _lib.MOE_OK
 
 
 def test_no_device_gives_cuda_error_not_a_crash():

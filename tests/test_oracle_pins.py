@@ -363,3 +363,15 @@ def test_round_bf16_hand_cases_and_library():
     r = (rng.standard_normal(4096) * 10.0 ** rng.integers(-6, 6, 4096)).astype(np.float32)
     ref = torch.from_numpy(r).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(oracle.round_bf16_bits(r), ref)
+
+
+def test_recall_brute_force_and_extremes():
+    rng = np.random.default_rng(13)
+    T, k, E = 50, 10, 64
+    a = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    b = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    hits = oracle.recall_hits(a, b)
+    assert list(hits) == [len(set(a[t]) & set(b[t])) for t in range(T)]
+    assert np.all(oracle.recall_hits(a, a) == k)
+    assert np.all(oracle.recall_hits(a, a[:, ::-1]) == k)  # order does not matter
+    assert np.all(oracle.recall_hits(a % 32, a % 32 + 32) == 0)
