@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--config", default="decode", choices=["decode", "prefill", "stack48", "sweep"])
     ap.add_argument("--layers", type=int, default=0, help="distinct layer weight sets rotated (0 = auto)")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (small profiling case)")
+    ap.add_argument("--plain", action="store_true",
+                    help="stream bf16 weights from the plain record layout through TMA tensor maps "
+                         "instead of the tile-packed records")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -239,7 +242,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    from sparse_moe_routed_gb300 import MoELayer, build as gbuild
+    from sparse_moe_routed_gb300 import MoELayer, _lib, build as gbuild, pack_layer_experts
     if rank == 0:
         gbuild.build()
     if world > 1:
@@ -256,10 +259,18 @@ def main():
     layers, xs, host_w = [], [], None
     for l in range(NL):
         d = wl.layer_inputs(cfg, dev, layer=l, x_seed_offset=l)
-        layers.append(MoELayer(d["w_router"], d["bias"], d["w_gateup"], d["w_down"], cfg.k, cfg.T))
+        if args.plain:
+            layers.append(MoELayer(d["w_router"], d["bias"], d["w_gateup"], d["w_down"], cfg.k, cfg.T))
+        else:
+            gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, cfg.E, cfg.H, cfg.I)
+            layers.append(MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, cfg.T, fmt=_lib.MOE_W_BF16_TILED,
+                                   I=cfg.I))
         xs.append(d["x"])
         if l == 0 and rank == 0 and world == 1 and not args.no_cpu_baseline:
             host_w = host_weights(d)
+        if not args.plain:
+            del d["w_gateup"], d["w_down"]
+        torch.cuda.synchronize()
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
 
@@ -399,6 +410,8 @@ def main():
         "dtype": "bf16", "data": "synthetic (seeded; x~N(0,1), weights~N(0,0.02) bf16)",
         "config": {"workload": wl_name, "T": cfg.T, "H": H, "E": E, "k": cfg.k, "I": I,
                    "router_bias": cfg.bias or "none", "layer_weight_sets": NL,
+                   "weights": "plain bf16 records (TMA tensor maps)" if args.plain else
+                              "tile-packed bf16 records (one bulk copy per stage)",
                    "l2": f"inputs larger than L2: {NL} distinct layer weight sets rotated "
                          f"({NL * (E * 3 * H * I * 2 + router_bytes) / 1e9:.1f} GB)",
                    "parallelism": f"replicas x{world}", "unique_experts_per_step": U},
@@ -433,7 +446,7 @@ def run_stack(args, rank, world, local, dev):
     import torch
     import torch.distributed as dist
     import workloads as wl
-    from sparse_moe_routed_gb300 import MoELayer, MoEStack, _lib
+    from sparse_moe_routed_gb300 import MoELayer, MoEStack, _lib, pack_layer_experts
     from sparse_moe_routed_gb300.sweep import route_sweep
 
     cfg = wl.STACK48
@@ -443,9 +456,9 @@ def run_stack(args, rank, world, local, dev):
     mls = []
     for l in range(L):
         w = wl.stack_layer_weights(l, dev)
-        mls.append(MoELayer(w["w_router"], None, w["w_gateup_q"], w["w_down_q"], cfg.k, T, fmt=_lib.MOE_W_INT4_G64,
-                            s_gateup=wl.scales_group_major(w["s_gateup"]),
-                            s_down=wl.scales_group_major(w["s_down"])))
+        gu, dn = pack_layer_experts(w["w_gateup_q"], w["w_down_q"], _lib.MOE_W_INT4_G64, cfg.E, cfg.H, cfg.I,
+                                    s_gateup=w["s_gateup"], s_down=w["s_down"])
+        mls.append(MoELayer(w["w_router"], None, gu, dn, cfg.k, T, fmt=_lib.MOE_W_INT4_G64_TILED, I=cfg.I))
         del w
     stack = MoEStack(mls, T)
     torch.cuda.synchronize()

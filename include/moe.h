@@ -62,8 +62,11 @@ typedef enum moe_status {
 #define MOE_DEV_TIMEOUT 0x4    /* a bounded pipeline wait ran out            */
 
 typedef enum moe_wfmt {
-  MOE_W_BF16 = 0,    /* bf16 weights                                         */
-  MOE_W_INT4_G64 = 1 /* int4 codes, one bf16 scale per 64 inputs of a row    */
+  MOE_W_BF16 = 0,          /* bf16 weights, plain record layout                  */
+  MOE_W_INT4_G64 = 1,      /* int4 codes + bf16 scale per 64 inputs, plain layout
+                              (input of moe_pack_experts only)                   */
+  MOE_W_BF16_TILED = 2,    /* bf16 weights packed by moe_pack_experts            */
+  MOE_W_INT4_G64_TILED = 3 /* int4 g64 weights packed by moe_pack_experts        */
 } moe_wfmt;
 
 /* ABI version of this header (major * 100 + minor). */
@@ -157,16 +160,17 @@ MOE_API moe_status moe_permute(const int32_t *topk_ids, int T, int k, int E, con
  *   MOE_W_BF16:     w_gateup [E, 2I, H] bf16: rows 0..I-1 gate, I..2I-1 up
  *                   w_down   [E, H, I]  bf16
  *                   s_gateup = s_down = NULL
- *   MOE_W_INT4_G64: w_gateup [E, 2I, H/2] uint8, w_down [E, H, I/2] uint8:
+ *   MOE_W_BF16_TILED, MOE_W_INT4_G64_TILED: the records as moe_pack_experts
+ *                   writes them (w_* its output, s_* NULL).
+ *   MOE_W_INT4_G64 (plain; accepted by moe_pack_experts only):
+ *                   w_gateup [E, 2I, H/2] uint8, w_down [E, H, I/2] uint8,
  *                   two signed 4-bit codes per byte (two's complement, -8..7),
- *                   even input index in the low nibble; one bf16 scale per 64
- *                   consecutive inputs of a row, stored group-major so that the
- *                   scales of one group are contiguous:
- *                   s_gateup [E, H/64, 2I] bf16 (for each group: gate rows,
- *                   then up rows) and s_down [E, I/64, H] bf16.
- *                   The tensor cores see w = bf16(scale * code).
- *                   (AFN-001, section "Phase 2": affine4 with group size 64,
- *                   read as symmetric codes with one bf16 scale per group.)
+ *                   even input index in the low nibble; s_gateup [E, 2I, H/64]
+ *                   and s_down [E, H, I/64] bf16, one scale per 64 consecutive
+ *                   inputs of a row; w = scale * code.  (AFN-001, section
+ *                   "Phase 2": affine4 with group size 64, read as symmetric
+ *                   codes with one bf16 scale per group.)  The tensor cores
+ *                   see w = bf16(scale * code).
  *
  * moe_expert_gateup:  for every slot s of expert e (offsets from moe_permute)
  *     g = Wgate_e . x_perm[s],  u = Wup_e . x_perm[s]      (fp32 accumulate)
@@ -193,6 +197,30 @@ MOE_API moe_status moe_grouped_swiglu(const uint16_t *x_perm, const int32_t *off
                               int I, int fmt, const void *w_gateup, const uint16_t *s_gateup,
                               const void *w_down, const uint16_t *s_down, uint16_t *h,
                               float *y_perm, int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_pack_experts -- reorder one component of every expert record into the
+ * tile order the contraction streams (done once, like loading a checkpoint).
+ *
+ * Source: AFN-019, section "Hypothesis H4" (ExpertMajor: one contiguous record
+ * per expert with explicit component extents).  Each expert's component stays
+ * contiguous; inside it, bytes are ordered by (128-row weight block, 64-input
+ * step) so that every pipeline stage is one contiguous chunk:
+ *   MOE_W_BF16 in -> MOE_W_BF16_TILED out: 16,384-byte chunks, the 128-byte-
+ *     swizzled image of a 128 x 64 bf16 tile;
+ *   MOE_W_INT4_G64 in -> MOE_W_INT4_G64_TILED out: 4,352-byte chunks, 128 rows
+ *     x 32 code bytes followed by the 128 rows' bf16 scales of that group; in
+ *     each 32-bit word the eight codes are stored offset by +8, nibble j
+ *     holding element 0,2,4,6,1,3,5,7 of the word's eight inputs.
+ * which = 0: gate/up (w [E,2I,H] or codes [E,2I,H/2] + s [E,2I,H/64]); gate/up
+ *   tiles hold 16 gate rows then the 16 matching up rows, four times.
+ * which = 1: down (w [E,H,I] or codes [E,H,I/2] + s [E,H,I/64]).
+ * out must hold moe_pack_size(...) bytes, 16-byte aligned, and must not
+ * overlap the input.
+ * ------------------------------------------------------------------------- */
+MOE_API size_t moe_pack_size(int fmt_in, int E, int H, int I, int which);
+MOE_API moe_status moe_pack_experts(int fmt_in, const void *w, const uint16_t *s, int E, int H, int I,
+                                    int which, void *out, size_t out_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * moe_combine -- weighted sum of expert outputs in route-rank order.

@@ -6,8 +6,8 @@ Importing this package does not load the CUDA library; the first call does
 from . import _lib
 from ._lib import (MoEError, moe_combine, moe_expert_down, moe_expert_gateup, moe_grouped_swiglu,
                    moe_permute, moe_rmsnorm, moe_route, moe_route_noalloc, moe_route_recall, route_block_dedup)
-from .layer import MoELayer, MoEStack
+from .layer import MoELayer, MoEStack, pack_layer_experts
 
-__all__ = ["_lib", "MoEError", "MoELayer", "MoEStack", "moe_route", "moe_permute", "moe_expert_gateup", "moe_expert_down",
+__all__ = ["_lib", "MoEError", "MoELayer", "MoEStack", "pack_layer_experts", "moe_route", "moe_permute", "moe_expert_gateup", "moe_expert_down",
            "moe_grouped_swiglu", "moe_combine", "route_block_dedup", "moe_rmsnorm", "moe_route_noalloc",
            "moe_route_recall"]

@@ -18,7 +18,7 @@ from . import build as _build
 
 MOE_OK, MOE_EINVAL, MOE_ESHAPE, MOE_ERANGE, MOE_ECUDA, MOE_ENOTSUP, MOE_EDEVICE_TIMEOUT, MOE_EWORKSPACE = range(8)
 MOE_DEV_BAD_EXPERT, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
-MOE_W_BF16, MOE_W_INT4_G64 = 0, 1
+MOE_W_BF16, MOE_W_INT4_G64, MOE_W_BF16_TILED, MOE_W_INT4_G64_TILED = 0, 1, 2, 3
 
 HEADER = os.path.join(_build.INCLUDE, "moe.h")
 
@@ -63,6 +63,8 @@ def load(path: str | None = None):
             "moe_combine": ([p, p, p, i, i, i, p, p, p, p, p], i),
             "route_block_dedup": ([p, i, i, i, i, i, i, i, p, p, p, p, p, p], i),
             "moe_rmsnorm": ([p, p, f, i, i, p, p, p], i),
+            "moe_pack_size": ([i, i, i, i, i], sz),
+            "moe_pack_experts": ([i, p, p, i, i, i, i, p, sz, p], i),
             "moe_route_recall": ([p, p, i, i, p, p], i),
         }
         for name, (args, res) in sig.items():
@@ -182,3 +184,20 @@ def moe_route_recall(pred_ids, ref_ids, hits, stream=None):
     T, k = ref_ids.shape
     st = load().moe_route_recall(_ptr(pred_ids), _ptr(ref_ids), T, k, _ptr(hits), _stream(stream))
     _check("moe_route_recall", st)
+
+
+def pack_size(fmt_in: int, E: int, H: int, I: int, which: int) -> int:
+    return load().moe_pack_size(fmt_in, E, H, I, which)
+
+
+def moe_pack_experts(fmt_in, w, s, E, H, I, which, out=None, stream=None):
+    """Pack one expert component (which = 0 gate/up, 1 down) into tile order;
+    returns the packed uint8 tensor (allocated with torch if out is None)."""
+    import torch
+    n = pack_size(fmt_in, E, H, I, which)
+    if out is None:
+        out = torch.empty((n,), dtype=torch.uint8, device=w.device)
+    st = load().moe_pack_experts(fmt_in, _ptr(w), _ptr(s), E, H, I, which, _ptr(out), out.numel(), _stream(stream))
+    _check("moe_pack_experts", st)
+    return out
+

@@ -146,16 +146,20 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, const uint1
 
 static moe_status check_expert_args(int R, int E, int H, int I, int fmt) {
   if (R < 0 || E <= 0 || H <= 0 || I <= 0) return MOE_ESHAPE;
-  if (fmt != MOE_W_BF16 && fmt != MOE_W_INT4_G64) return MOE_EINVAL;
+  if (fmt != MOE_W_BF16 && fmt != MOE_W_INT4_G64 && fmt != MOE_W_BF16_TILED && fmt != MOE_W_INT4_G64_TILED)
+    return MOE_EINVAL;
+  if (fmt == MOE_W_INT4_G64) return MOE_ENOTSUP;  // plain int4 records are packed first
   if (E > moe::kMaxE) return MOE_ENOTSUP;
   if (H % 128 != 0 || H > 16384 || I % 64 != 0 || I > 16384) return MOE_ENOTSUP;
   if (static_cast<long long>(E) * H >= (1LL << 31)) return MOE_ENOTSUP;
   return MOE_OK;
 }
 
-// Scales are given exactly for the int4 format, 16-byte aligned.
+// The contraction takes weights only: every format carries its scales
+// inside the (packed) record.
 static bool scales_ok(int fmt, const uint16_t* s) {
-  return fmt == MOE_W_INT4_G64 ? (s != nullptr && a16(s)) : (s == nullptr);
+  (void)fmt;
+  return s == nullptr;
 }
 
 moe_status moe_expert_gateup(const uint16_t* x_perm, const int32_t* offsets, int R, int E, int H, int I, int fmt,
@@ -201,6 +205,27 @@ moe_status moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets, in
   c = moe_expert_gateup(x_perm, offsets, R, E, H, I, fmt, w_gateup, s_gateup, h, dev_status, stream);
   if (c != MOE_OK) return c;
   return moe_expert_down(h, offsets, R, E, H, I, fmt, w_down, s_down, y_perm, dev_status, stream);
+}
+
+size_t moe_pack_size(int fmt_in, int E, int H, int I, int which) {
+  if (E <= 0 || H <= 0 || I <= 0 || (which != 0 && which != 1)) return 0;
+  if (H % 128 != 0 || I % 64 != 0) return 0;
+  if (fmt_in == MOE_W_BF16) return moe::packed_component_bytes(MOE_W_BF16_TILED, E, H, I, which);
+  if (fmt_in == MOE_W_INT4_G64) return moe::packed_component_bytes(MOE_W_INT4_G64_TILED, E, H, I, which);
+  return 0;
+}
+
+moe_status moe_pack_experts(int fmt_in, const void* w, const uint16_t* s, int E, int H, int I, int which, void* out,
+                            size_t out_bytes, void* stream) {
+  if (E <= 0 || H <= 0 || I <= 0) return MOE_ESHAPE;
+  if (which != 0 && which != 1) return MOE_EINVAL;
+  if (fmt_in != MOE_W_BF16 && fmt_in != MOE_W_INT4_G64) return MOE_EINVAL;
+  if (E > moe::kMaxE || H % 128 != 0 || H > 16384 || I % 64 != 0 || I > 16384) return MOE_ENOTSUP;
+  if (!w || !out || !a16(w) || !a16(out)) return MOE_EINVAL;
+  if (fmt_in == MOE_W_INT4_G64 ? (!s || !a4(s)) : (s != nullptr)) return MOE_EINVAL;
+  const size_t need = moe_pack_size(fmt_in, E, H, I, which);
+  if (out_bytes < need) return MOE_EWORKSPACE;
+  return cuda_status(moe::launch_pack(fmt_in, w, s, E, H, I, which, out, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_combine(const float* y_perm, const int32_t* inv_perm, const float* topk_w, int T, int k, int H,

@@ -14,24 +14,29 @@
 //    weights stream once from HBM (L2 evict-first hint on weights).
 //  * Persistent CTAs (one per SM) walk the tile list round-robin.  Tile
 //    counts come from the device-side expert offsets, never from the host.
-//  * Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
-//    warps 2..5 = epilogue, and for int4 weights warps 6..13 = dequantisers.
-//    A STAGES-deep shared-memory ring (mbarriers) feeds the tensor core; two
-//    TMEM accumulators let the epilogue of one tile overlap the main loop of
-//    the next.
-//  * Gate/up tiles interleave 16 gate rows with the 16 matching up rows (a 4-D
-//    TMA box over [E][2][I][K]), so each epilogue warp holds g in lanes 0..15
-//    and u in lanes 16..31 of the same intermediate index: SwiGLU needs one
-//    shuffle, no shared-memory exchange.
+//  * Warp roles: warp 0 = producer (TMA / bulk copies), warp 1 = MMA issuer
+//    (and TMEM owner), warps 2..5 = epilogue; for int4 weights warp 6 also
+//    produces (token rows) and warps 7.. dequantise.  Shared-memory rings with mbarriers feed the tensor
+//    core; two TMEM accumulators let the epilogue of one tile overlap the main
+//    loop of the next.
+//  * Gate/up tiles interleave 16 gate rows with the 16 matching up rows, so
+//    each epilogue warp holds g in lanes 0..15 and u in lanes 16..31 of the
+//    same intermediate index: SwiGLU needs one shuffle, no shared-memory
+//    exchange.
+//  * Weight tiles come either through TMA tensor maps from the plain bf16
+//    record layout, or as one bulk copy per stage from a tile-packed record
+//    (pack.cu): a 16 KB pre-swizzled bf16 tile, or a 4,352-byte int4 g64
+//    chunk (128 rows x 64 codes + the rows' bf16 group scales).
 //  * int4 g64 weights (AFN-001 "Porting Qwen3.8-Flash-Next to Hebrus", section
 //    "Phase 2": affine4 with group size 64, read as symmetric codes with one
-//    bf16 scale per group): TMA brings the packed codes (4 KB per stage instead
-//    of 16 KB) and the group's scales into a staging area; eight dequantiser
-//    warps turn them into the 128-byte-swizzled bf16 operand tile
-//    (w = bf16(code * scale)), fence the generic-proxy writes for the async
-//    proxy and arrive on the stage's barrier; the MMA and epilogue are shared
-//    with the bf16 path.
-//  * Every mbarrier wait is bounded (2 s of globaltimer); on expiry the CTA
+//    bf16 scale per group) move 4.25x fewer bytes per stage, so their packed
+//    chunks get a deep ring of their own (~70 KB in flight per SM); dequantiser
+//    warps turn each chunk into a 128-byte-swizzled bf16 operand tile in a
+//    short second ring (w = bf16(code * scale)), fence the generic-proxy
+//    writes for the async proxy and arrive on the tile's barrier; token rows
+//    have a third ring fed by a second producer warp.
+//  * Every mbarrier wait is bounded (2 s of globaltimer, read sparingly; waits
+//    of the many-thread roles back off with __nanosleep); on expiry the CTA
 //    flags MOE_DEV_TIMEOUT, waits (bounded) for its copies and MMAs in flight,
 //    frees its TMEM and returns.
 #include <cuda.h>
@@ -50,33 +55,56 @@ namespace moe {
 
 namespace {
 
-constexpr int kBM = 128;                              // weight rows per tile (MMA M)
-constexpr int kBK = 64;                               // K per stage: one 128-byte swizzled row of bf16
-constexpr int kUK = 16;                               // K per MMA instruction
-constexpr int kABytes = kBM * kBK * 2;                // 16 KB bf16 operand tile
-constexpr int kBoxRows = 16;                          // token rows per B TMA box
-constexpr int kBBoxBytes = kBoxRows * kBK * 2;        // 2 KB
-constexpr int kGUBoxBytes = 2 * kBoxRows * kBK * 2;   // 16 gate + 16 up rows: 4 KB
-constexpr int kQBytes = kBM * kBK / 2;                // int4 codes of one stage: 4 KB
-constexpr int kQGUBoxBytes = 2 * kBoxRows * kBK / 2;  // codes of 16 gate + 16 up rows: 1 KB
-constexpr int kSBytes = kBM * 2;                      // one bf16 scale per row: 256 B
-constexpr int kCoreThreads = 192;                     // producer, MMA, 4 epilogue warps
-constexpr int kQuantWarps = 8;                        // dequantiser warps (int4 only)
+constexpr int kBM = 128;                             // weight rows per tile (MMA M)
+constexpr int kBK = 64;                              // K per stage: one 128-byte swizzled row of bf16
+constexpr int kUK = 16;                              // K per MMA instruction
+constexpr int kABytes = kBM * kBK * 2;               // 16 KB bf16 operand tile
+constexpr int kBoxRows = 16;                         // token rows per B TMA box
+constexpr int kBBoxBytes = kBoxRows * kBK * 2;       // 2 KB
+constexpr int kGUBoxBytes = 2 * kBoxRows * kBK * 2;  // 16 gate + 16 up rows: 4 KB
+constexpr int kQBytes = kBM * kBK / 2;               // int4 codes of one stage: 4 KB
+constexpr int kSBytes = kBM * 2;                     // one bf16 scale per row: 256 B
+constexpr int kQChunk = kQBytes + kSBytes;           // one packed int4 stage chunk: 4,352 B
+constexpr int kCoreThreads = 192;                    // producers, MMA, 4 epilogue warps
+constexpr int kSmemTail = 16 + 2 * (kMaxE + 1) * 4;  // misc words + tile prefix + segment offsets
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-template <int NMAX, bool Q4>
-struct Cfg {
-  static constexpr int kThreads = kCoreThreads + (Q4 ? 32 * kQuantWarps : 0);
+// bf16 weights: one ring; a stage holds G consecutive K steps: A (G x 16 KB)
+// + B (G x NMAX token rows).  Tile-packed weights take G = 2 (one 32 KB bulk
+// copy per stage), halving the per-request and per-handoff costs.
+template <int NMAX, int G>
+struct CfgB {
+  static constexpr int kThreads = kCoreThreads;
   static constexpr int kBBytes = NMAX * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes + (Q4 ? kQBytes + kSBytes : 0);
-  static constexpr int kStagesBf16 = NMAX <= 32 ? 10 : (NMAX <= 64 ? 8 : (NMAX <= 128 ? 6 : 4));
-  static constexpr int kStagesQ4 = NMAX <= 32 ? 8 : (NMAX <= 64 ? 7 : 5);
-  static constexpr int kStages = Q4 ? kStagesQ4 : kStagesBf16;
+  static constexpr int kStageBytes = G * (kABytes + kBBytes);
+  static constexpr int kBudget = 196 * 1024;
+  static constexpr int kStages = kBudget / kStageBytes < 2 ? 2 : (kBudget / kStageBytes > 10 ? 10 : kBudget / kStageBytes);
   static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
-  static constexpr int kNumBars = (Q4 ? 3 : 2) * kStages + 5;
-  static constexpr int kMiscBytes = 16;
-  // tile prefix [E+1] and clamped segment offsets [E+1]
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + kMiscBytes + 2 * (kMaxE + 1) * 4;
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + kSmemTail;
+  static_assert(kBBytes % 1024 == 0, "B stage must keep 1024-byte alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+// int4 g64 weights: a deep ring of packed chunks, a ring of bf16 operand
+// tiles with one slot per dequantiser warp (SA), a ring of token rows (SB).
+// One bulk copy fills a ring slot with QG consecutive K steps' chunks (QG = 4
+// for gate/up, 2 for down: runtime, kQRingBytes / (QG x 4,352) slots).
+// Dequantiser warp w owns every SA-th K step, so SA steps are dequantised at
+// once.
+template <int NMAX>
+struct CfgQ {
+  static constexpr int kDqWarps = NMAX <= 64 ? 8 : 4;
+  static constexpr int kDqWarp0 = 7;  // warp 6 produces token rows
+  static constexpr int kThreads = 32 * (kDqWarp0 + kDqWarps);
+  static constexpr int kBBytes = NMAX * kBK * 2;
+  static constexpr int SA = kDqWarps;
+  static constexpr int SQmax = NMAX <= 16 ? 16 : 8;  // ring capacity in single-step chunks
+  static constexpr int kQRingBytes = SQmax * kQChunk;
+  static constexpr int SB = NMAX <= 32 ? 8 : (NMAX <= 64 ? 6 : 4);
+  static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
+  static constexpr int kNumBars = 2 * (SQmax + SA + SB) + 5;
+  static constexpr int kSmemBytes = 1024 + SA * kABytes + SB * kBBytes + kQRingBytes + kNumBars * 8 + kSmemTail;
   static_assert(kBBytes % 1024 == 0, "B stage must keep 1024-byte alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -88,21 +116,31 @@ struct GemmArgs {
   int ksteps;              // K / 64
   int mblocks;             // 128-row weight blocks per segment
   int seg_rows;            // weight rows per segment in the A map (down: H)
-  int seg_groups;          // scale groups per weight row (int4 down: I / 64)
+  const uint8_t* tiles;    // tile-packed weights (bulk-copy modes), chunk per (e, mb, ks)
+  int qgroup;              // int4: K steps per bulk copy (divides ksteps)
   void* out;
   int ldo;                 // leading dimension of out (elements)
   int32_t* status;
 };
 
+// Bounded mbarrier wait.  Polls back off with __nanosleep(kSleepNs) so that
+// waiting warps leave issue slots to the warps doing work (0 for the
+// single-thread producer and MMA roles, whose latency matters most).  The
+// (slow) %globaltimer is read only every 1024 polls, starting the clock at
+// the first read; after kWaitNs the wait flags MOE_DEV_TIMEOUT and gives up.
+template <uint32_t kSleepNs>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                              int32_t* status) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
+    if (kSleepNs != 0 && it >= 2) __nanosleep(kSleepNs);
+    if ((it & 1023u) == 1023u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitNs) {
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitNs) {
         *abort_flag = 1;
         set_status(status, MOE_DEV_TIMEOUT);
         return false;
@@ -111,10 +149,15 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
   }
 }
 
+constexpr uint32_t kSpin = 0;         // producer / MMA threads
+constexpr uint32_t kSleepQuant = 32;  // dequantiser warps
+constexpr uint32_t kSleepEpi = 256;   // epilogue warps (one wait per tile)
+
 // Drain wait used during teardown after an abort: ignores the abort flag.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (!ptx::mbar_try_wait(bar, parity)) {
+    __nanosleep(256);
     if (globaltimer_ns() - t0 > kWaitNs) return;
   }
 }
@@ -123,23 +166,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Eight signed 4-bit codes (one 32-bit word, element 0 in the low nibble)
-// times one bf16 scale -> eight bf16 (a 16-byte chunk, element 0 first).
-// Code q is placed in the mantissa of 128 + (q + 8) (exact in bf16), the
-// offset is removed exactly, and the product with the scale is rounded once.
+// One packed 32-bit word of eight int4 g64 codes -> eight bf16 (16 bytes).
+// The packer stores each code offset by +8 and orders a word's nibbles as
+// elements 0,2,4,6,1,3,5,7, so one mask-and-or per pair places two codes in
+// the mantissas of 128 + (q + 8) (exact in bf16); subtracting 136 is exact and
+// the product with the group scale is rounded once.
 __device__ __forceinline__ uint4 dequant8(uint32_t word, __nv_bfloat162 scale2) {
-  const uint32_t v = word ^ 0x88888888u;  // two's complement nibble -> q + 8
-  const __nv_bfloat162 one2 = __floats2bfloat162_rn(1.0f, 1.0f);
-  const __nv_bfloat162 off2 = __floats2bfloat162_rn(-136.0f, -136.0f);
+  const __nv_bfloat162 off2 = __floats2bfloat162_rn(136.0f, 136.0f);
   uint32_t out[4];
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
-    const uint32_t t = v >> (8 * p);
-    const uint32_t bits = 0x43004300u | (t & 0xFu) | ((t & 0xF0u) << 12);
+    const uint32_t bits = ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
     __nv_bfloat162 b;
     std::memcpy(&b, &bits, 4);
-    const __nv_bfloat162 q = __hfma2(b, one2, off2);
-    const __nv_bfloat162 w = __hmul2(q, scale2);
+    const __nv_bfloat162 w = __hmul2(__hsub2(b, off2), scale2);
     std::memcpy(&out[p], &w, 4);
   }
   return make_uint4(out[0], out[1], out[2], out[3]);
@@ -149,62 +189,42 @@ struct Tile {
   int e, mb, row0, nrows;
 };
 
-template <int NMAX, int KIND, bool Q4>
-__global__ void __launch_bounds__(Cfg<NMAX, Q4>::kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmS, GemmArgs p) {
-  using C = Cfg<NMAX, Q4>;
-  constexpr int S = C::kStages;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = base;                         // [S][16 KB] bf16 operand tiles (swizzled)
-  uint8_t* sB = sA + S * kABytes;             // [S][NMAX x 128 B] token rows (swizzled)
-  uint8_t* sQ = sB + S * C::kBBytes;          // [S][4 KB] int4 codes (Q4)
-  uint8_t* sS = sQ + (Q4 ? S * kQBytes : 0);  // [S][256 B] scales (Q4)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + (Q4 ? S * kSBytes : 0));
-  const uint32_t full0 = ptx::smem_u32(bars);  // operand tiles ready for the MMA
-  const uint32_t empty0 = full0 + 8 * S;       // MMA finished with a stage
-  const uint32_t accf0 = empty0 + 8 * S;
-  const uint32_t acce0 = accf0 + 16;
-  const uint32_t drain = acce0 + 16;
-  const uint32_t tfull0 = drain + 8;  // Q4: codes + scales + token rows landed
-  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
-  int* prefix = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
-  int* soff = prefix + (kMaxE + 1);
+// Shared per-CTA scheduling state: clamped segment offsets and the tile
+// prefix over segments, both in shared memory.
+struct Sched {
+  const int* prefix;
+  const int* soff;
+  int E;
+  int mblocks;
+  int nmax;
 
+  __device__ __forceinline__ Tile tile(int t) const {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int local = t - prefix[lo];
+    const int chunk = local / mblocks;
+    const int start = soff[lo];
+    const int len = max(soff[lo + 1] - start, 0);
+    Tile tl;
+    tl.e = lo;
+    tl.mb = local - chunk * mblocks;
+    tl.row0 = start + chunk * nmax;
+    tl.nrows = min(nmax, len - chunk * nmax);
+    return tl;
+  }
+};
+
+// Segment offsets into shared memory, clamped into [0, R] (a segment's length
+// is never negative) so that corrupt offsets can never address rows outside
+// the buffers; then the per-segment tile prefix (warp 0).  Ends with a
+// CTA-wide barrier.  Returns the total number of tiles.
+template <int NMAX>
+__device__ __forceinline__ int build_schedule(const GemmArgs& p, bool dense, int E, int* prefix, int* soff) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool dense = (p.offsets == nullptr);
-  const int E = dense ? 1 : p.E;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(full0 + 8 * s, Q4 ? kQuantWarps : 1);
-      ptx::mbar_init(empty0 + 8 * s, 1);
-      if (Q4) ptx::mbar_init(tfull0 + 8 * s, 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(accf0 + 8 * a, 1);
-      ptx::mbar_init(acce0 + 8 * a, 128);
-    }
-    ptx::mbar_init(drain, 1);
-    misc[1] = 0;
-    ptx::fence_mbar_init();
-    ptx::prefetch_tmap(&tmA);
-    ptx::prefetch_tmap(&tmB);
-    if (Q4) ptx::prefetch_tmap(&tmS);
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(&misc[0])), C::kTmemCols);
-    ptx::tmem_relinquish();
-  }
-  // Everything above overlaps the previous kernel's tail; from here on the
-  // kernel reads upstream data (offsets, activation rows) and writes outputs.
-  pdl_wait();
-  pdl_trigger();
-  // Segment offsets into shared memory, clamped into [0, R] (a segment's
-  // length is never negative), so that corrupt offsets can never address rows
-  // outside the buffers; then the per-segment tile prefix (warp 0).
   for (int i = threadIdx.x; i <= E; i += blockDim.x)
     soff[i] = dense ? (i == 0 ? 0 : p.R) : min(max(p.offsets[i], 0), p.R);
   __syncthreads();
@@ -229,27 +249,134 @@ __global__ void __launch_bounds__(Cfg<NMAX, Q4>::kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  return prefix[E];
+}
 
-  const uint32_t tmem_base = misc[0];
-  const int total = prefix[E];
-
-  auto tile_of = [&](int t) {
-    int lo = 0, hi = E;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (prefix[mid] <= t) lo = mid; else hi = mid;
+// Epilogue warps (2..5): drain finished accumulators from TMEM.  Gate/up
+// (KIND 0): h = bf16(silu(g) * u); down (KIND 1) and router logits (KIND 2):
+// fp32 rows, one 128-byte store per warp per token row.
+template <int NMAX, int KIND>
+__device__ __forceinline__ void epilogue_role(const GemmArgs& p, const Sched& sc, int total, uint32_t tmem_base,
+                                              uint32_t accf0, uint32_t acce0, volatile uint32_t* abort_flag) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q = warp & 3;  // TMEM lane quarter this warp may access
+  const int row_in_tile = q * 32 + lane;
+  int acc = 0;
+  uint32_t aph = 0;
+  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    const Tile tl = sc.tile(t);
+    const bool ok = wait_bounded<kSleepEpi>(accf0 + 8 * acc, aph, abort_flag, p.status);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    ptx::tc_fence_after();
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * NMAX);
+    if (KIND == 0) {
+      uint16_t* hout = static_cast<uint16_t*>(p.out);
+      const bool up_lane = lane >= 16;
+      const int i = tl.mb * 64 + q * 16 + (lane & 15);
+      for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
+        float v[16];
+        ptx::tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+        float recv[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const float send = up_lane ? v[jj] : v[8 + jj];
+          recv[jj] = __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int col = c0 + (up_lane ? 8 : 0) + jj;
+          const float g = up_lane ? recv[jj] : v[jj];
+          const float u = up_lane ? v[8 + jj] : recv[jj];
+          if (col < tl.nrows) {
+            const float hval = g / (1.0f + expf(-g)) * u;
+            hout[static_cast<size_t>(tl.row0 + col) * p.ldo + i] = f32_to_bf16(hval);
+          }
+        }
+      }
+    } else {
+      float* yout = static_cast<float*>(p.out);
+      const int j = tl.mb * kBM + row_in_tile;
+      for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
+        float v[16];
+        ptx::tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int col = c0 + jj;
+          if (col < tl.nrows) yout[static_cast<size_t>(tl.row0 + col) * p.ldo + j] = v[jj];
+        }
+      }
     }
-    const int local = t - prefix[lo];
-    const int chunk = local / p.mblocks;
-    const int start = soff[lo];
-    const int len = max(soff[lo + 1] - start, 0);
-    Tile tl;
-    tl.e = lo;
-    tl.mb = local - chunk * p.mblocks;
-    tl.row0 = start + chunk * NMAX;
-    tl.nrows = min(NMAX, len - chunk * NMAX);
-    return tl;
-  };
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(acce0 + 8 * acc);
+    if (++acc == 2) {
+      acc = 0;
+      aph ^= 1u;
+    }
+  }
+}
+
+__device__ __forceinline__ void issue_k_step(uint32_t d_tmem, uint32_t a0, uint32_t b0, uint32_t idesc, int ks) {
+#pragma unroll
+  for (int kk = 0; kk < kBK / kUK; ++kk)
+    ptx::umma_bf16(d_tmem, ptx::sdesc_k_sw128(a0 + kk * kUK * 2), ptx::sdesc_k_sw128(b0 + kk * kUK * 2), idesc,
+                   (ks | kk) != 0 ? 1u : 0u);
+}
+
+// ============================================================== bf16 kernel
+// AMODE 0: weight tiles through the TMA tensor map tmA (plain bf16 record);
+// AMODE 1: one 16 KB bulk copy per stage (tile-packed bf16 record).
+template <int NMAX, int KIND, int AMODE, int G>
+__global__ void __launch_bounds__(kCoreThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        GemmArgs p) {
+  using C = CfgB<NMAX, G>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;                  // [S][G][16 KB] bf16 operand tiles (swizzled)
+  uint8_t* sB = sA + S * G * kABytes;  // [S][G][NMAX x 128 B] token rows (swizzled)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * G * C::kBBytes);
+  const uint32_t full0 = ptx::smem_u32(bars);  // operand tiles landed
+  const uint32_t empty0 = full0 + 8 * S;       // MMA finished with a stage
+  const uint32_t accf0 = empty0 + 8 * S;
+  const uint32_t acce0 = accf0 + 16;
+  const uint32_t drain = acce0 + 16;
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
+  int* prefix = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
+  int* soff = prefix + (kMaxE + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool dense = (p.offsets == nullptr);
+  const int E = dense ? 1 : p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(full0 + 8 * s, 1);
+      ptx::mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(accf0 + 8 * a, 1);
+      ptx::mbar_init(acce0 + 8 * a, 128);
+    }
+    ptx::mbar_init(drain, 1);
+    misc[1] = 0;
+    ptx::fence_mbar_init();
+    if (AMODE == 0) ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(&misc[0])), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  // Everything above overlaps the previous kernel's tail; from here on the
+  // kernel reads upstream data (offsets, activation rows) and writes outputs.
+  pdl_wait();
+  pdl_trigger();
+  const int total = build_schedule<NMAX>(p, dense, E, prefix, soff);
+  const uint32_t tmem_base = misc[0];
+  const Sched sc{prefix, soff, E, p.mblocks, NMAX};
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -262,51 +389,42 @@ __global__ void __launch_bounds__(Cfg<NMAX, Q4>::kThreads, 1)
     uint32_t ph = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = tile_of(t);
+      const Tile tl = sc.tile(t);
       const int nblk = (tl.nrows + kBoxRows - 1) / kBoxRows;
-      for (int ks = 0; ks < p.ksteps; ++ks) {
-        if (!wait_bounded(empty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
+      for (int ks = 0; ks < p.ksteps; ks += G) {
+        if (!wait_bounded<kSpin>(empty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
           ok = false;
           break;
         }
-        const uint32_t b_dst = ptx::smem_u32(sB + s * C::kBBytes);
-        if (!Q4) {
-          const uint32_t fb = full0 + 8 * s;
-          ptx::mbar_arrive_expect_tx(fb, kABytes + nblk * kBBoxBytes);
-          armed[s] = static_cast<int>(ph);
-          const uint32_t a_dst = ptx::smem_u32(sA + s * kABytes);
-          if (KIND == 0) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-              ptx::tma_load_4d(a_dst + b * kGUBoxBytes, &tmA, fb, ks * kBK, tl.mb * 64 + b * 16, 0, tl.e, pol_w);
-          } else if (KIND == 1) {
-            ptx::tma_load_2d(a_dst, &tmA, fb, ks * kBK, tl.e * p.seg_rows + tl.mb * kBM, pol_w);
-          } else {
-            ptx::tma_load_2d(a_dst, &tmA, fb, ks * kBK, tl.mb * kBM, pol_w);
-          }
-          for (int b = 0; b < nblk; ++b)
-            ptx::tma_load_2d(b_dst + b * kBBoxBytes, &tmB, fb, ks * kBK, tl.row0 + b * kBoxRows, pol_x);
+        const uint32_t fb = full0 + 8 * s;
+        ptx::mbar_arrive_expect_tx(fb, G * (kABytes + nblk * kBBoxBytes));
+        armed[s] = static_cast<int>(ph);
+        const uint32_t a_dst = ptx::smem_u32(sA + s * G * kABytes);
+        const uint32_t b_dst = ptx::smem_u32(sB + s * G * C::kBBytes);
+        if (AMODE == 1) {
+          const size_t chunk = (static_cast<size_t>(tl.e) * p.mblocks + tl.mb) * p.ksteps + ks;
+          ptx::bulk_load(a_dst, p.tiles + chunk * kABytes, G * kABytes, fb, pol_w);
         } else {
-          const uint32_t fb = tfull0 + 8 * s;
-          ptx::mbar_arrive_expect_tx(fb, kQBytes + kSBytes + nblk * kBBoxBytes);
-          armed[s] = static_cast<int>(ph);
-          const uint32_t q_dst = ptx::smem_u32(sQ + s * kQBytes);
-          const uint32_t s_dst = ptx::smem_u32(sS + s * kSBytes);
-          if (KIND == 0) {
-            // codes [E][2][I][K/2] bytes, scales group-major [E][K/64][2][I]
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-              ptx::tma_load_4d(q_dst + b * kQGUBoxBytes, &tmA, fb, ks * (kBK / 2), tl.mb * 64 + b * 16, 0, tl.e,
-                               pol_w);
-            ptx::tma_load_4d(s_dst, &tmS, fb, tl.mb * 64, 0, ks, tl.e, pol_w);
-          } else {
-            // codes [E*H][I/2] bytes, scales group-major [E][I/64][H]
-            ptx::tma_load_2d(q_dst, &tmA, fb, ks * (kBK / 2), tl.e * p.seg_rows + tl.mb * kBM, pol_w);
-            ptx::tma_load_2d(s_dst, &tmS, fb, tl.mb * kBM, tl.e * p.seg_groups + ks, pol_w);
+          for (int j = 0; j < G; ++j) {
+            const uint32_t aj = a_dst + j * kABytes;
+            if (KIND == 0) {
+#pragma unroll
+              for (int b = 0; b < 4; ++b)
+                ptx::tma_load_4d(aj + b * kGUBoxBytes, &tmA, fb, (ks + j) * kBK, tl.mb * 64 + b * 16, 0, tl.e,
+                                 pol_w);
+            } else if (KIND == 1) {
+              ptx::tma_load_2d(aj, &tmA, fb, (ks + j) * kBK, tl.e * p.seg_rows + tl.mb * kBM, pol_w);
+            } else {
+              ptx::tma_load_2d(aj, &tmA, fb, (ks + j) * kBK, tl.mb * kBM, pol_w);
+            }
           }
-          for (int b = 0; b < nblk; ++b)
-            ptx::tma_load_2d(b_dst + b * kBBoxBytes, &tmB, fb, ks * kBK, tl.row0 + b * kBoxRows, pol_x);
         }
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+          for (int b = 0; b < nblk; ++b)
+            ptx::tma_load_2d(b_dst + j * C::kBBytes + b * kBBoxBytes, &tmB, fb, (ks + j) * kBK,
+                             tl.row0 + b * kBoxRows, pol_x);
         if (++s == S) {
           s = 0;
           ph ^= 1u;
@@ -315,10 +433,9 @@ __global__ void __launch_bounds__(Cfg<NMAX, Q4>::kThreads, 1)
     }
     if (!ok || misc[1]) {
       // abort: let every copy already issued land before the CTA exits
-      const uint32_t landed0 = Q4 ? tfull0 : full0;
 #pragma unroll
       for (int q = 0; q < S; ++q)
-        if (armed[q] >= 0) wait_drain(landed0 + 8 * q, static_cast<uint32_t>(armed[q]));
+        if (armed[q] >= 0) wait_drain(full0 + 8 * q, static_cast<uint32_t>(armed[q]));
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -329,28 +446,24 @@ __global__ void __launch_bounds__(Cfg<NMAX, Q4>::kThreads, 1)
     bool ok = true;
     bool issued = false;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = tile_of(t);
-      const uint32_t npad = static_cast<uint32_t>((tl.nrows + 15) & ~15);
-      const uint32_t idesc = ptx::idesc_bf16_f32(kBM, npad);
-      if (!wait_bounded(acce0 + 8 * acc, aph ^ 1u, misc + 1, p.status)) {
+      const Tile tl = sc.tile(t);
+      const uint32_t idesc = ptx::idesc_bf16_f32(kBM, static_cast<uint32_t>((tl.nrows + 15) & ~15));
+      if (!wait_bounded<kSpin>(acce0 + 8 * acc, aph ^ 1u, misc + 1, p.status)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NMAX);
-      for (int ks = 0; ks < p.ksteps; ++ks) {
-        if (!wait_bounded(full0 + 8 * s, ph, misc + 1, p.status)) {
+      for (int ks = 0; ks < p.ksteps; ks += G) {
+        if (!wait_bounded<kSpin>(full0 + 8 * s, ph, misc + 1, p.status)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t a0 = ptx::smem_u32(sA + s * kABytes);
-        const uint32_t b0 = ptx::smem_u32(sB + s * C::kBBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBK / kUK; ++kk) {
-          ptx::umma_bf16(d_tmem, ptx::sdesc_k_sw128(a0 + kk * kUK * 2), ptx::sdesc_k_sw128(b0 + kk * kUK * 2),
-                         idesc, (ks | kk) != 0 ? 1u : 0u);
-        }
+        for (int j = 0; j < G; ++j)
+          issue_k_step(d_tmem, ptx::smem_u32(sA + (s * G + j) * kABytes), ptx::smem_u32(sB + (s * G + j) * C::kBBytes),
+                       idesc, ks + j);
         issued = true;
         ptx::umma_commit(empty0 + 8 * s);
         if (++s == S) {
@@ -369,101 +482,232 @@ __global__ void __launch_bounds__(Cfg<NMAX, Q4>::kThreads, 1)
       ptx::umma_commit(drain);
       wait_drain(drain, 0);
     }
-  } else if (warp >= 2 && warp < 6) {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row_in_tile = q * 32 + lane;
-    int acc = 0;
-    uint32_t aph = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = tile_of(t);
-      bool ok = wait_bounded(accf0 + 8 * acc, aph, misc + 1, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      ptx::tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * NMAX);
-      if (KIND == 0) {
-        uint16_t* hout = static_cast<uint16_t*>(p.out);
-        const bool up_lane = lane >= 16;
-        const int i = tl.mb * 64 + q * 16 + (lane & 15);
-        for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
-          float v[16];
-          ptx::tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
-          float recv[8];
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const float send = up_lane ? v[jj] : v[8 + jj];
-            recv[jj] = __shfl_xor_sync(0xffffffffu, send, 16);
-          }
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int col = c0 + (up_lane ? 8 : 0) + jj;
-            const float g = up_lane ? recv[jj] : v[jj];
-            const float u = up_lane ? v[8 + jj] : recv[jj];
-            if (col < tl.nrows) {
-              const float hval = g / (1.0f + expf(-g)) * u;
-              hout[static_cast<size_t>(tl.row0 + col) * p.ldo + i] = f32_to_bf16(hval);
-            }
-          }
+  } else if (warp >= 2) {
+    epilogue_role<NMAX, KIND>(p, sc, total, tmem_base, accf0, acce0, misc + 1);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ============================================================== int4 kernel
+template <int NMAX, int KIND>
+__global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
+    grouped_gemm_q4_kernel(const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
+  using C = CfgQ<NMAX>;
+  constexpr int SA = C::SA, SB = C::SB;
+  const int QG = p.qgroup;
+  const int SQ = C::SQmax / QG;  // logical slots of QG chunks each
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;               // [SA][16 KB] dequantised operand tiles (swizzled)
+  uint8_t* sB = sA + SA * kABytes;  // [SB][NMAX x 128 B] token rows (swizzled)
+  uint8_t* sQ = sB + SB * C::kBBytes;  // [SQ][QG x 4,352 B] packed codes + scales
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + C::kQRingBytes);
+  const uint32_t qfull0 = ptx::smem_u32(bars);      // packed chunks landed
+  const uint32_t qempty0 = qfull0 + 8 * C::SQmax;   // dequantisers done reading them
+  const uint32_t afull0 = qempty0 + 8 * C::SQmax;   // operand tile written
+  const uint32_t aempty0 = afull0 + 8 * SA;     // MMA done with the tile
+  const uint32_t bfull0 = aempty0 + 8 * SA;     // token rows landed
+  const uint32_t bempty0 = bfull0 + 8 * SB;     // MMA done with the rows
+  const uint32_t accf0 = bempty0 + 8 * SB;
+  const uint32_t acce0 = accf0 + 16;
+  const uint32_t drain = acce0 + 16;
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
+  int* prefix = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
+  int* soff = prefix + (kMaxE + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SQ; ++s) {
+      ptx::mbar_init(qfull0 + 8 * s, 1);
+      ptx::mbar_init(qempty0 + 8 * s, QG);
+    }
+    for (int s = 0; s < SA; ++s) {
+      ptx::mbar_init(afull0 + 8 * s, 1);
+      ptx::mbar_init(aempty0 + 8 * s, 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      ptx::mbar_init(bfull0 + 8 * s, 1);
+      ptx::mbar_init(bempty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(accf0 + 8 * a, 1);
+      ptx::mbar_init(acce0 + 8 * a, 128);
+    }
+    ptx::mbar_init(drain, 1);
+    misc[1] = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(&misc[0])), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  pdl_wait();
+  pdl_trigger();
+  const int total = build_schedule<NMAX>(p, false, E, prefix, soff);
+  const uint32_t tmem_base = misc[0];
+  const Sched sc{prefix, soff, E, p.mblocks, NMAX};
+
+  if ((warp == 0 || warp == 6) && lane == 0) {
+    // ------------------------------------------------- producers: warp 0 moves
+    // packed weight chunks (deep ring), warp 6 moves token rows (B ring); one
+    // thread each, in separate warps so neither spin starves the other
+    const bool weights = (warp == 0);
+    const int S = weights ? SQ : SB;
+    const uint32_t full0 = weights ? qfull0 : bfull0;
+    const uint32_t empty0 = weights ? qempty0 : bempty0;
+    const uint64_t pol = weights ? ptx::policy_evict_first() : ptx::policy_evict_last();
+    uint32_t armed_mask = 0, armed_ph = 0;  // bit s: stage s armed / its parity
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = sc.tile(t);
+      const int nblk = (tl.nrows + kBoxRows - 1) / kBoxRows;
+      for (int ks = 0; ks < p.ksteps; ks += (weights ? QG : 1)) {
+        if (!wait_bounded<kSpin>(empty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
+          ok = false;
+          break;
         }
-      } else {
-        float* yout = static_cast<float*>(p.out);
-        const int j = tl.mb * kBM + row_in_tile;
-        for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
-          float v[16];
-          ptx::tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int col = c0 + jj;
-            if (col < tl.nrows) yout[static_cast<size_t>(tl.row0 + col) * p.ldo + j] = v[jj];
-          }
+        const uint32_t fb = full0 + 8 * s;
+        armed_mask |= 1u << s;
+        armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+        if (weights) {
+          ptx::mbar_arrive_expect_tx(fb, QG * kQChunk);
+          const size_t chunk = (static_cast<size_t>(tl.e) * p.mblocks + tl.mb) * p.ksteps + ks;
+          ptx::bulk_load(ptx::smem_u32(sQ + s * QG * kQChunk), p.tiles + chunk * kQChunk, QG * kQChunk, fb, pol);
+        } else {
+          ptx::mbar_arrive_expect_tx(fb, nblk * kBBoxBytes);
+          const uint32_t b_dst = ptx::smem_u32(sB + s * C::kBBytes);
+          for (int b = 0; b < nblk; ++b)
+            ptx::tma_load_2d(b_dst + b * kBBoxBytes, &tmB, fb, ks * kBK, tl.row0 + b * kBoxRows, pol);
+        }
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
         }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(acce0 + 8 * acc);
+    }
+    if (!ok || misc[1]) {
+      for (int q = 0; q < S; ++q)
+        if ((armed_mask >> q) & 1u) wait_drain(full0 + 8 * q, (armed_ph >> q) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    int sa = 0, sb = 0;
+    uint32_t pha = 0, phb = 0;
+    int acc = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    bool issued = false;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = sc.tile(t);
+      const uint32_t idesc = ptx::idesc_bf16_f32(kBM, static_cast<uint32_t>((tl.nrows + 15) & ~15));
+      if (!wait_bounded<kSpin>(acce0 + 8 * acc, aph ^ 1u, misc + 1, p.status)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NMAX);
+      for (int ks = 0; ks < p.ksteps; ++ks) {
+        if (!wait_bounded<kSpin>(afull0 + 8 * sa, pha, misc + 1, p.status) ||
+            !wait_bounded<kSpin>(bfull0 + 8 * sb, phb, misc + 1, p.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        issue_k_step(d_tmem, ptx::smem_u32(sA + sa * kABytes), ptx::smem_u32(sB + sb * C::kBBytes), idesc, ks);
+        issued = true;
+        ptx::umma_commit(aempty0 + 8 * sa);
+        ptx::umma_commit(bempty0 + 8 * sb);
+        if (++sa == SA) {
+          sa = 0;
+          pha ^= 1u;
+        }
+        if (++sb == SB) {
+          sb = 0;
+          phb ^= 1u;
+        }
+      }
+      if (!ok) break;
+      ptx::umma_commit(accf0 + 8 * acc);
       if (++acc == 2) {
         acc = 0;
         aph ^= 1u;
       }
     }
-  } else if (Q4 && warp >= 6) {
+    if ((!ok || misc[1]) && issued) {
+      ptx::umma_commit(drain);
+      wait_drain(drain, 0);
+    }
+  } else if (warp >= 2 && warp < 6) {
+    epilogue_role<NMAX, KIND>(p, sc, total, tmem_base, accf0, acce0, misc + 1);
+  } else if (warp >= C::kDqWarp0) {
     // ------------------------------------------------------------ dequantisers
-    // 256 threads, two per weight row: each turns 32 codes (16 bytes) of its
-    // row into 4 swizzled 16-byte chunks of the bf16 operand tile.
-    const int tt = threadIdx.x - kCoreThreads;
-    const int row = tt >> 1;
-    const int half = tt & 1;
-    // scale slot of this row: gate/up tiles hold [2][64] (gate rows, up rows)
-    // for the tile's four 16-row block pairs; down tiles hold one per row
-    const int sidx = (KIND == 0) ? (((row >> 4) & 1) * 64 + (row >> 5) * 16 + (row & 15)) : row;
-    int s = 0;
-    uint32_t ph = 0;
+    // Warp w takes K steps g = w, w + SA, w + 2 SA, ... of this CTA's stream
+    // and always writes operand slot w.  Each lane handles rows lane,
+    // lane + 32, lane + 64, lane + 96: it reads their codes and scales, frees
+    // the packed chunk, then writes 4 x 8 swizzled 16-byte pieces.
+    const int dw = warp - C::kDqWarp0;
+    uint32_t g = 0;  // this CTA's running K-step index
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      for (int ks = 0; ks < p.ksteps; ++ks) {
-        const bool got = wait_bounded(tfull0 + 8 * s, ph, misc + 1, p.status);
+      for (int ks = 0; ks < p.ksteps; ++ks, ++g) {
+        if (static_cast<int>(g % SA) != dw) continue;
+        const uint32_t gg = g / QG;  // ring group (QG consecutive K steps)
+        const uint32_t sq = gg % SQ;
+        const uint32_t phq = (gg / SQ) & 1u;
+        const uint32_t pha = (g / SA) & 1u;
+        bool got = wait_bounded<kSleepQuant>(qfull0 + 8 * sq, phq, misc + 1, p.status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        const uint4 pk = *reinterpret_cast<const uint4*>(sQ + s * kQBytes + row * 32 + half * 16);
-        const uint16_t sbits = reinterpret_cast<const uint16_t*>(sS + s * kSBytes)[sidx];
-        __nv_bfloat16 sc;
-        std::memcpy(&sc, &sbits, 2);
-        const __nv_bfloat162 sc2 = __halves2bfloat162(sc, sc);
-        uint8_t* arow = sA + s * kABytes + row * 128;
-        const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
+        const uint8_t* chunk = sQ + (sq * QG + (g - gg * QG)) * kQChunk;
+        uint4 pk[4][2];
+        uint16_t sbits[4];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int chunk = (4 * half + w) ^ (row & 7);
-          *reinterpret_cast<uint4*>(arow + chunk * 16) = dequant8(words[w], sc2);
+        for (int rr = 0; rr < 4; ++rr) {
+          const int row = lane + 32 * rr;
+          pk[rr][0] = reinterpret_cast<const uint4*>(chunk + row * 32)[0];
+          pk[rr][1] = reinterpret_cast<const uint4*>(chunk + row * 32)[1];
+          sbits[rr] = reinterpret_cast<const uint16_t*>(chunk + kQBytes)[row];
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(qempty0 + 8 * sq);
+        got = wait_bounded<kSleepQuant>(aempty0 + 8 * dw, pha ^ 1u, misc + 1, p.status);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        uint8_t* atile = sA + dw * kABytes;
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int row = lane + 32 * rr;
+          __nv_bfloat16 scv;
+          std::memcpy(&scv, &sbits[rr], 2);
+          const __nv_bfloat162 sc2 = __halves2bfloat162(scv, scv);
+          uint8_t* arow = atile + row * 128;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t words[4] = {pk[rr][half].x, pk[rr][half].y, pk[rr][half].z, pk[rr][half].w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+              *reinterpret_cast<uint4*>(arow + (((4 * half + w) ^ (row & 7)) * 16)) = dequant8(words[w], sc2);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(full0 + 8 * s);
-        if (++s == S) {
-          s = 0;
-          ph ^= 1u;
-        }
+        if (lane == 0) ptx::mbar_arrive(afull0 + 8 * dw);
       }
     }
   }
@@ -552,31 +796,66 @@ bool make_rows_map(CUtensorMap* m, const void* ptr, int K, int rows, int box_row
   return make_map(m, ptr, 2, dims, str, box);
 }
 
-template <int NMAX, int KIND, bool Q4>
-cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& sc, const GemmArgs& args,
-                cudaStream_t st) {
-  using C = Cfg<NMAX, Q4>;
-  auto kern = grouped_gemm_kernel<NMAX, KIND, Q4>;
+template <int NMAX, int KIND, int AMODE, int G>
+cudaError_t run_bf16(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, cudaStream_t st) {
+  using C = CfgB<NMAX, G>;
+  auto kern = grouped_gemm_kernel<NMAX, KIND, AMODE, G>;
   cudaError_t e = ensure_smem(kern, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = sm_count();
   if (grid <= 0) return cudaErrorNoDevice;
-  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, st, a, b, sc, args);
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, st, a, b, args);
 }
 
-template <int KIND, bool Q4>
-cudaError_t run_nmax(int nmax, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& sc,
-                     const GemmArgs& args, cudaStream_t st) {
+template <int NMAX, int KIND>
+cudaError_t run_q4(const CUtensorMap& b, const GemmArgs& args, cudaStream_t st) {
+  using C = CfgQ<NMAX>;
+  auto kern = grouped_gemm_q4_kernel<NMAX, KIND>;
+  cudaError_t e = ensure_smem(kern, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = sm_count();
+  if (grid <= 0) return cudaErrorNoDevice;
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, st, b, args);
+}
+
+template <int KIND>
+cudaError_t run_fmt(int fmt, int nmax, const CUtensorMap& a, const CUtensorMap& b, GemmArgs args,
+                    cudaStream_t st) {
+  if (fmt == MOE_W_INT4_G64_TILED) {
+    args.qgroup = args.ksteps % 4 == 0 ? 4 : (args.ksteps % 2 == 0 ? 2 : 1);
+    switch (nmax) {
+      case 16: return run_q4<16, KIND>(b, args, st);
+      case 32: return run_q4<32, KIND>(b, args, st);
+      case 64: return run_q4<64, KIND>(b, args, st);
+      default: return run_q4<128, KIND>(b, args, st);
+    }
+  }
+  if (fmt == MOE_W_BF16_TILED && args.ksteps % 2 == 0) {
+    switch (nmax) {
+      case 16: return run_bf16<16, KIND, 1, 2>(a, b, args, st);
+      case 32: return run_bf16<32, KIND, 1, 2>(a, b, args, st);
+      case 64: return run_bf16<64, KIND, 1, 2>(a, b, args, st);
+      default: return run_bf16<128, KIND, 1, 2>(a, b, args, st);
+    }
+  }
+  if (fmt == MOE_W_BF16_TILED) {
+    switch (nmax) {
+      case 16: return run_bf16<16, KIND, 1, 1>(a, b, args, st);
+      case 32: return run_bf16<32, KIND, 1, 1>(a, b, args, st);
+      case 64: return run_bf16<64, KIND, 1, 1>(a, b, args, st);
+      default: return run_bf16<128, KIND, 1, 1>(a, b, args, st);
+    }
+  }
   switch (nmax) {
-    case 16: return run<16, KIND, Q4>(a, b, sc, args, st);
-    case 32: return run<32, KIND, Q4>(a, b, sc, args, st);
-    case 64: return run<64, KIND, Q4>(a, b, sc, args, st);
-    default: return run<128, KIND, Q4>(a, b, sc, args, st);
+    case 16: return run_bf16<16, KIND, 0, 1>(a, b, args, st);
+    case 32: return run_bf16<32, KIND, 0, 1>(a, b, args, st);
+    case 64: return run_bf16<64, KIND, 0, 1>(a, b, args, st);
+    default: return run_bf16<128, KIND, 0, 1>(a, b, args, st);
   }
 }
 
 // Token rows per tile: small when experts see few rows (decode), so the
-// B operand and TMEM footprint stay small and the ring can run deeper.
+// B operand and TMEM footprint stay small and the rings can run deeper.
 int pick_nmax(int rows_hint) {
   if (rows_hint <= 320) return 16;
   if (rows_hint <= 1280) return 32;
@@ -589,69 +868,42 @@ int pick_nmax(int rows_hint) {
 cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uint16_t* scales, const uint16_t* b_rows,
                                 const int32_t* offsets, int E, int R, int H, int I, int router_E, void* out,
                                 int32_t* st_word, cudaStream_t st) {
-  CUtensorMap ma, mb, ms;
+  (void)scales;
+  CUtensorMap ma, mb;
   GemmArgs args{};
   args.offsets = offsets;
   args.E = E;
   args.R = R;
   args.status = st_word;
   args.out = out;
-  const bool q4 = (fmt == MOE_W_INT4_G64);
+  args.tiles = static_cast<const uint8_t*>(w);
+  args.qgroup = 1;
+  const bool plain = (fmt == MOE_W_BF16);
+  if (!plain && fmt != MOE_W_BF16_TILED && fmt != MOE_W_INT4_G64_TILED) return cudaErrorInvalidValue;
   switch (kind) {
     case GemmKind::kGateUp: {
-      if (!q4) {
+      if (plain) {
         // A: [E][2][I][H] bf16 viewed 4-D, box = 16 gate rows + the 16 matching up rows
         cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)I, 2, (cuuint64_t)E};
         cuuint64_t str[3] = {(cuuint64_t)H * 2, (cuuint64_t)I * H * 2, (cuuint64_t)2 * I * H * 2};
         cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)kBoxRows, 2, 1};
         if (!make_map(&ma, w, 4, dims, str, box)) return cudaErrorInvalidValue;
-      } else {
-        // codes: [E][2][I][H/2] bytes, same 16 + 16 row box, 32 bytes (64 codes) wide
-        cuuint64_t dims[4] = {(cuuint64_t)H / 2, (cuuint64_t)I, 2, (cuuint64_t)E};
-        cuuint64_t str[3] = {(cuuint64_t)H / 2, (cuuint64_t)I * H / 2, (cuuint64_t)2 * I * H / 2};
-        cuuint32_t box[4] = {(cuuint32_t)kBK / 2, (cuuint32_t)kBoxRows, 2, 1};
-        if (!make_map(&ma, w, 4, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE))
-          return cudaErrorInvalidValue;
-        // scales: group-major [E][H/64][2][I] bf16; box = 64 rows of gate and of up for one group
-        cuuint64_t sd[4] = {(cuuint64_t)I, 2, (cuuint64_t)H / 64, (cuuint64_t)E};
-        cuuint64_t ss[3] = {(cuuint64_t)I * 2, (cuuint64_t)2 * I * 2, (cuuint64_t)(H / 64) * 2 * I * 2};
-        cuuint32_t sb[4] = {64, 2, 1, 1};
-        if (!make_map(&ms, scales, 4, sd, ss, sb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_NONE))
-          return cudaErrorInvalidValue;
       }
       if (!make_rows_map(&mb, b_rows, H, R, kBoxRows)) return cudaErrorInvalidValue;
       args.ksteps = H / kBK;
       args.mblocks = I / 64;
       args.seg_rows = 2 * I;
-      args.seg_groups = H / 64;
       args.ldo = I;
-      if (q4) return run_nmax<0, true>(pick_nmax(R), ma, mb, ms, args, st);
-      return run_nmax<0, false>(pick_nmax(R), ma, mb, ma, args, st);
+      return run_fmt<0>(fmt, pick_nmax(R), plain ? ma : mb, mb, args, st);
     }
     case GemmKind::kDown: {
-      if (!q4) {
-        if (!make_rows_map(&ma, w, I, E * H, kBM)) return cudaErrorInvalidValue;
-      } else {
-        cuuint64_t dims[2] = {(cuuint64_t)I / 2, (cuuint64_t)E * H};
-        cuuint64_t str[1] = {(cuuint64_t)I / 2};
-        cuuint32_t box[2] = {(cuuint32_t)kBK / 2, (cuuint32_t)kBM};
-        if (!make_map(&ma, w, 2, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE))
-          return cudaErrorInvalidValue;
-        // scales: group-major [E][I/64][H] bf16; box = 128 rows of one group
-        cuuint64_t sd[2] = {(cuuint64_t)H, (cuuint64_t)E * (I / 64)};
-        cuuint64_t ss[1] = {(cuuint64_t)H * 2};
-        cuuint32_t sb[2] = {(cuuint32_t)kBM, 1};
-        if (!make_map(&ms, scales, 2, sd, ss, sb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_NONE))
-          return cudaErrorInvalidValue;
-      }
+      if (plain && !make_rows_map(&ma, w, I, E * H, kBM)) return cudaErrorInvalidValue;
       if (!make_rows_map(&mb, b_rows, I, R, kBoxRows)) return cudaErrorInvalidValue;
       args.ksteps = I / kBK;
       args.mblocks = H / kBM;
       args.seg_rows = H;
-      args.seg_groups = I / 64;
       args.ldo = H;
-      if (q4) return run_nmax<1, true>(pick_nmax(R), ma, mb, ms, args, st);
-      return run_nmax<1, false>(pick_nmax(R), ma, mb, ma, args, st);
+      return run_fmt<1>(fmt, pick_nmax(R), plain ? ma : mb, mb, args, st);
     }
     case GemmKind::kRouter: {
       // one dense segment: all T token rows against all router_E expert rows
@@ -662,9 +914,8 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uin
       args.ksteps = H / kBK;
       args.mblocks = router_E / kBM;
       args.seg_rows = router_E;
-      args.seg_groups = 0;
       args.ldo = router_E;
-      return run<128, 2, false>(ma, mb, ma, args, st);
+      return run_bf16<128, 2, 0, 1>(ma, mb, args, st);
     }
   }
   return cudaErrorInvalidValue;

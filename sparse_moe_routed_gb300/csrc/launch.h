@@ -58,6 +58,11 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uin
                                 const uint16_t* b_rows, const int32_t* offsets, int E, int R, int H, int I,
                                 int router_E, void* out, int32_t* st_word, cudaStream_t st);
 
+// pack.cu
+size_t packed_component_bytes(int fmt_tiled, int E, int H, int I, int which);
+cudaError_t launch_pack(int fmt_in, const void* w, const uint16_t* s, int E, int H, int I, int which, void* out,
+                        cudaStream_t st);
+
 // combine.cu
 cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int k, int H,
                            int R, const float* residual, uint16_t* out_bf16, float* out_f32,

@@ -22,27 +22,25 @@ class MoELayer:
     """Buffers and calls of one layer.
 
     bf16 weights: w_gateup [E,2I,H] bf16, w_down [E,H,I] bf16.
-    int4 weights (fmt=MOE_W_INT4_G64): w_gateup [E,2I,H/2] uint8 codes,
-    w_down [E,H,I/2] uint8 codes, s_gateup [E,H/64,2I] and s_down [E,I/64,H]
-    bf16 scales (group-major).
+    packed weights (fmt=MOE_W_BF16_TILED or MOE_W_INT4_G64_TILED): the uint8
+    buffers moe_pack_experts wrote for the gate/up and down components (pass I).
     """
 
     def __init__(self, w_router, bias, w_gateup, w_down, k: int, T_max: int, fmt: int = _lib.MOE_W_BF16,
-                 s_gateup=None, s_down=None):
+                 I: int = None):
         assert w_router.is_cuda and w_router.dtype == torch.bfloat16
         self.E, self.H = w_router.shape
-        self.I = w_gateup.shape[1] // 2
         self.fmt = fmt
         if fmt == _lib.MOE_W_BF16:
+            self.I = w_gateup.shape[1] // 2
             assert w_gateup.shape == (self.E, 2 * self.I, self.H)
             assert w_down.shape == (self.E, self.H, self.I)
-            assert s_gateup is None and s_down is None
         else:
-            assert w_gateup.dtype == torch.uint8 and w_gateup.shape == (self.E, 2 * self.I, self.H // 2)
-            assert w_down.dtype == torch.uint8 and w_down.shape == (self.E, self.H, self.I // 2)
-            assert s_gateup.shape == (self.E, self.H // 64, 2 * self.I)
-            assert s_down.shape == (self.E, self.I // 64, self.H)
-        self.s_gateup, self.s_down = s_gateup, s_down
+            assert fmt in (_lib.MOE_W_BF16_TILED, _lib.MOE_W_INT4_G64_TILED) and I is not None
+            self.I = I
+            src = _lib.MOE_W_BF16 if fmt == _lib.MOE_W_BF16_TILED else _lib.MOE_W_INT4_G64
+            assert w_gateup.numel() * w_gateup.element_size() == _lib.pack_size(src, self.E, self.H, I, 0)
+            assert w_down.numel() * w_down.element_size() == _lib.pack_size(src, self.E, self.H, I, 1)
         self.k = k
         self.T_max = T_max
         self.w_router, self.bias, self.w_gateup, self.w_down = w_router, bias, w_gateup, w_down
@@ -103,10 +101,10 @@ class MoELayer:
              (P(self.ids), T, k, E, P(x), H, P(self.counts), P(self.offsets), P(self.perm), P(self.inv),
               P(self.x_perm), P(self.status), st)),
             ("moe_expert_gateup", lib.moe_expert_gateup,
-             (P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt, P(self.w_gateup), P(self.s_gateup), P(self.h),
+             (P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt, P(self.w_gateup), None, P(self.h),
               P(self.status), st)),
             ("moe_expert_down", lib.moe_expert_down,
-             (P(self.h), P(self.offsets), R, E, H, I, self.fmt, P(self.w_down), P(self.s_down), P(self.y_perm),
+             (P(self.h), P(self.offsets), R, E, H, I, self.fmt, P(self.w_down), None, P(self.y_perm),
               P(self.status), st)),
             ("moe_combine", lib.moe_combine,
              (P(self.y_perm), P(self.inv), P(self.w), T, k, H, P(residual), P(out), P(out_f32), P(self.status), st)),
@@ -208,4 +206,11 @@ class MoEStack:
             for call in self.layer_calls(x, l, stream):
                 MoELayer.issue(call)
         return x
+
+
+def pack_layer_experts(w_gateup, w_down, fmt_in, E, H, I, s_gateup=None, s_down=None, stream=None):
+    """(packed gate/up, packed down) uint8 device tensors for MoELayer."""
+    gu = _lib.moe_pack_experts(fmt_in, w_gateup, s_gateup, E, H, I, 0, stream=stream)
+    dn = _lib.moe_pack_experts(fmt_in, w_down, s_down, E, H, I, 1, stream=stream)
+    return gu, dn
 

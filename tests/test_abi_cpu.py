@@ -27,7 +27,7 @@ def lib():
 def test_library_loads_and_exports_every_declared_symbol():
     L = lib()
     names = _lib.declared_functions()
-    assert len(names) == 14
+    assert len(names) == 16
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 100
@@ -164,3 +164,18 @@ def test_recall_rejections():
 def test_no_device_gives_cuda_error_not_a_crash():
     """Past admission, a machine without a GPU gets MOE_ECUDA back."""
     assert lib().moe_device_sm_count() == -1
+
+
+def test_pack_rejections_and_sizes():
+    L = lib()
+    assert L.moe_pack_size(0, 512, 2560, 640, 0) == 512 * 10 * 40 * 16384
+    assert L.moe_pack_size(1, 512, 2560, 640, 1) == 512 * 20 * 10 * 4352
+    assert L.moe_pack_size(2, 512, 2560, 640, 0) == 0  # packed formats are outputs, not inputs
+    n = L.moe_pack_size(0, 64, 256, 64, 0)
+    assert L.moe_pack_experts(0, P, NUL, 64, 256, 64, 0, P, n - 1, NUL) == _lib.MOE_EWORKSPACE
+    assert L.moe_pack_experts(1, P, NUL, 64, 256, 64, 0, P, n, NUL) == _lib.MOE_EINVAL  # int4 needs scales
+    assert L.moe_pack_experts(0, P, P, 64, 256, 64, 0, P, n, NUL) == _lib.MOE_EINVAL   # bf16 takes none
+    assert L.moe_pack_experts(0, P, NUL, 64, 256, 64, 2, P, n, NUL) == _lib.MOE_EINVAL
+    assert L.moe_pack_experts(0, P, NUL, 64, 250, 64, 0, P, n, NUL) == _lib.MOE_ENOTSUP
+    assert _gateup(fmt=1) == _lib.MOE_ENOTSUP  # plain int4 must be packed first
+

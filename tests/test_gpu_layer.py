@@ -12,7 +12,7 @@ import torch
 import oracle
 import workloads as wl
 from parity import GAP_TOL, assert_output_close, compare_routes
-from sparse_moe_routed_gb300 import MoELayer, _lib
+from sparse_moe_routed_gb300 import MoELayer, _lib, pack_layer_experts
 
 pytestmark = pytest.mark.gpu
 
@@ -49,8 +49,12 @@ def case(name, T=None):
     return _CACHE[key]
 
 
-def run_layer(cfg, d):
-    layer = MoELayer(d["w_router"], d["bias"], d["w_gateup"], d["w_down"], cfg.k, cfg.T)
+def run_layer(cfg, d, tiled=False):
+    if tiled:
+        gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, cfg.E, cfg.H, cfg.I)
+        layer = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, cfg.T, fmt=_lib.MOE_W_BF16_TILED, I=cfg.I)
+    else:
+        layer = MoELayer(d["w_router"], d["bias"], d["w_gateup"], d["w_down"], cfg.k, cfg.T)
     layer.clear_status()
     out = layer.forward(d["x"]).clone()
     torch.cuda.synchronize()
@@ -260,11 +264,13 @@ def test_combine_nonfinite_flag():
 # --------------------------------------------------------------------------
 # Whole layer
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("name,T,nsample", [("tiny", None, 16), ("decode", None, 16), ("decode", 37, 37),
-                                            ("prefill", None, 24)])
-def test_layer_parity(name, T, nsample):
+@pytest.mark.parametrize("name,T,nsample,tiled", [("tiny", None, 16, False), ("decode", None, 16, False),
+                                                  ("decode", 37, 37, False), ("prefill", None, 24, False),
+                                                  ("tiny", None, 16, True), ("decode", None, 16, True),
+                                                  ("prefill", None, 24, True)])
+def test_layer_parity(name, T, nsample, tiled):
     cfg, d, host = case(name, T)
-    layer, out = run_layer(cfg, d)
+    layer, out = run_layer(cfg, d, tiled)
     ids = layer.ids[:cfg.T].cpu().numpy()
     toks = sample_tokens(cfg.T, nsample, seed=1)
     ids_r, w_r, gap_r, L_r = oracle.route(host["x"][toks], host["wr"], host["bias"], cfg.k)
@@ -277,8 +283,8 @@ def test_layer_parity(name, T, nsample):
     assert keep.sum() >= 0.9 * len(toks)
     got = out.float().cpu().numpy()[toks][keep]
     rel_max, mean_rel = assert_output_close(got, ref[keep], what=f"{name} layer output")
-    print(f"{name} T={cfg.T}: {keep.sum()}/{len(toks)} tokens graded, max err {rel_max:.2e} of max|ref|, "
-          f"mean rel {mean_rel:.2e}")
+    print(f"{name} T={cfg.T} tiled={tiled}: {keep.sum()}/{len(toks)} tokens graded, max err {rel_max:.2e} "
+          f"of max|ref|, mean rel {mean_rel:.2e}")
 
 
 def _adjacent_swap_ok(ids_gpu, ids_ref, L_ref):
@@ -296,8 +302,12 @@ def test_layer_deterministic():
     layer = MoELayer(d["w_router"], d["bias"], d["w_gateup"], d["w_down"], cfg.k, cfg.T)
     a = layer.forward(d["x"]).clone()
     b = layer.forward(d["x"]).clone()
+    tl, _ = run_layer(cfg, d, tiled=True)
+    c = tl.forward(d["x"]).clone()
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # packing changes where weights live, not the arithmetic: identical bits
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
 
 
 def test_layer_single_token_and_empty():

@@ -12,7 +12,7 @@ import torch
 import oracle
 import workloads as wl
 from parity import GAP_TOL, assert_output_close, compare_routes
-from sparse_moe_routed_gb300 import MoELayer, MoEStack, _lib
+from sparse_moe_routed_gb300 import MoELayer, MoEStack, _lib, pack_layer_experts
 
 pytestmark = pytest.mark.gpu
 
@@ -38,9 +38,9 @@ def make_stack(L, T):
     mls = []
     for l in range(L):
         w = layer_weights(l)
-        mls.append(MoELayer(w["w_router"], None, w["w_gateup_q"], w["w_down_q"], CFG.k, T, fmt=_lib.MOE_W_INT4_G64,
-                            s_gateup=wl.scales_group_major(w["s_gateup"]),
-                            s_down=wl.scales_group_major(w["s_down"])))
+        gu, dn = pack_layer_experts(w["w_gateup_q"], w["w_down_q"], _lib.MOE_W_INT4_G64, CFG.E, CFG.H, CFG.I,
+                                    s_gateup=w["s_gateup"], s_down=w["s_down"])
+        mls.append(MoELayer(w["w_router"], None, gu, dn, CFG.k, T, fmt=_lib.MOE_W_INT4_G64_TILED, I=CFG.I))
     return MoEStack(mls, T)
 
 
@@ -95,8 +95,8 @@ def test_int4_expert_stage_tiny_geometry():
     y = torch.full((R, cfg.H), float("nan"), dtype=torch.float32, device=DEV)
     st = torch.zeros((1,), dtype=torch.int32, device=DEV)
     _lib.moe_permute(ids, cfg.E, d["x"], counts, offsets, perm, inv, xp, st)
-    _lib.moe_grouped_swiglu(xp, offsets, cfg.E, cfg.H, cfg.I, q_gu, q_d, h, y, st, fmt=_lib.MOE_W_INT4_G64,
-                            s_gateup=wl.scales_group_major(s_gu), s_down=wl.scales_group_major(s_d))
+    gu, dn = pack_layer_experts(q_gu, q_d, _lib.MOE_W_INT4_G64, cfg.E, cfg.H, cfg.I, s_gateup=s_gu, s_down=s_d)
+    _lib.moe_grouped_swiglu(xp, offsets, cfg.E, cfg.H, cfg.I, gu, dn, h, y, st, fmt=_lib.MOE_W_INT4_G64_TILED)
     torch.cuda.synchronize()
     assert st.item() == 0
     xin = oracle.bits_to_f32(oracle.bf16_bits(d["x"]))
@@ -146,3 +146,60 @@ def test_stack_is_deterministic():
     stack.forward(b)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def _repack_codes(codes):
+    """Packed int4 word order: code + 8, nibble j holds element 0,2,4,6,1,3,5,7."""
+    words = codes.reshape(codes.shape[0], -1, 4).view(np.uint32)[..., 0].astype(np.uint64)
+    out = np.zeros_like(words)
+    for e in range(8):
+        n = ((words >> np.uint64(4 * e)) & np.uint64(0xF)) ^ np.uint64(8)
+        pos = 4 + e // 2 if e % 2 else e // 2
+        out |= n << np.uint64(4 * pos)
+    return out.astype(np.uint32).view(np.uint8).reshape(codes.shape)
+
+
+def _expected_pack(w_np, E, rows, K, I, which, s_np=None):
+    """Test-side restatement of the packed layout (see include/moe.h)."""
+    MB = (I // 64) if which == 0 else (rows // 128)
+    KS = K // 64
+    out = []
+    for e in range(E):
+        for mb in range(MB):
+            for ks in range(KS):
+                tile_rows = []
+                for r in range(128):
+                    if which == 0:
+                        src = ((r >> 4) & 1) * I + mb * 64 + (r >> 5) * 16 + (r & 15)
+                    else:
+                        src = mb * 128 + r
+                    tile_rows.append(src)
+                if s_np is None:  # bf16: swizzled 128-byte rows
+                    t = np.zeros((128, 64), np.uint16)
+                    for r, src in enumerate(tile_rows):
+                        row = w_np[e, src, ks * 64:(ks + 1) * 64].reshape(8, 8)
+                        for c in range(8):
+                            t[r, (c ^ (r & 7)) * 8:(c ^ (r & 7)) * 8 + 8] = row[c]
+                    out.append(t.view(np.uint8).reshape(-1))
+                else:
+                    codes = np.stack([w_np[e, src, ks * 32:(ks + 1) * 32] for src in tile_rows])
+                    codes = _repack_codes(codes)
+                    sc = np.array([s_np[e, src, ks] for src in tile_rows], np.uint16)
+                    out.append(np.concatenate([codes.reshape(-1), sc.view(np.uint8)]))
+    return np.concatenate(out)
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_pack_layouts_bit_exact(which):
+    cfg = wl.TINY
+    d = wl.layer_inputs(cfg, DEV)
+    w = d["w_gateup"] if which == 0 else d["w_down"]
+    rows, K = (2 * cfg.I, cfg.H) if which == 0 else (cfg.H, cfg.I)
+    got = _lib.moe_pack_experts(_lib.MOE_W_BF16, w, None, cfg.E, cfg.H, cfg.I, which).cpu().numpy()
+    exp = _expected_pack(oracle.bf16_bits(w), cfg.E, rows, K, cfg.I, which)
+    assert np.array_equal(got, exp)
+    q, sc = wl.quantize_int4_g64(w)
+    got4 = _lib.moe_pack_experts(_lib.MOE_W_INT4_G64, q, sc, cfg.E, cfg.H, cfg.I, which).cpu().numpy()
+    exp4 = _expected_pack(q.cpu().numpy(), cfg.E, rows, K, cfg.I, which, s_np=oracle.bf16_bits(sc))
+    assert np.array_equal(got4, exp4)
+

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 import workloads as wl
-from sparse_moe_routed_gb300 import MoELayer, MoEStack, _lib
+from sparse_moe_routed_gb300 import MoELayer, MoEStack, _lib, pack_layer_experts
 from sparse_moe_routed_gb300.sweep import route_sweep
 
 pytestmark = pytest.mark.gpu
@@ -41,9 +41,9 @@ def test_sweep_small_stack_properties():
     mls = []
     for l in range(L):
         w = wl.stack_layer_weights(l, DEV)
-        mls.append(MoELayer(w["w_router"], None, w["w_gateup_q"], w["w_down_q"], cfg.k, T,
-                            fmt=_lib.MOE_W_INT4_G64, s_gateup=wl.scales_group_major(w["s_gateup"]),
-                            s_down=wl.scales_group_major(w["s_down"])))
+        gu, dn = pack_layer_experts(w["w_gateup_q"], w["w_down_q"], _lib.MOE_W_INT4_G64, cfg.E, cfg.H, cfg.I,
+                                    s_gateup=w["s_gateup"], s_down=w["s_down"])
+        mls.append(MoELayer(w["w_router"], None, gu, dn, cfg.k, T, fmt=_lib.MOE_W_INT4_G64_TILED, I=cfg.I))
     stack = MoEStack(mls, T)
     preds = [wl.predictor_weights(cfg.H, cfg.E, l, DEV) for l in range(L)]
     x0 = wl.token_batch(cfg, DEV, index=21, T=T).float()

@@ -176,12 +176,6 @@ def quantize_int4_g64(w: torch.Tensor):
     return packed, s.squeeze(-1)
 
 
-def scales_group_major(s: torch.Tensor) -> torch.Tensor:
-    """[..., rows, K/64] scales -> [..., K/64, rows] (layout only, same values):
-    the form the GPU reads, so that one group's scales are contiguous."""
-    return s.transpose(-1, -2).contiguous()
-
-
 def stack_layer_weights(layer: int, device="cpu", cfg: LayerConfig = STACK48) -> dict:
     """One layer of the 48-layer int4 stack: bf16 router, int4 g64 experts."""
     dev = torch.device(device)
