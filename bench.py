@@ -79,8 +79,9 @@ def gemm_source_sha():
     return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+def recorded_traffic(kernel: str, workload: str, units: float):
+    """DRAM bytes per launch from a committed ncu summary (per distinct expert,
+    scaled by the launch's units), if the kernel source is unchanged."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -88,7 +89,7 @@ def recorded_traffic(kernel: str, workload: str):
         d = json.load(open(p))
         ent = d.get(kernel, {}).get(workload)
         if ent and ent.get("gemm_src_sha") == gemm_source_sha():
-            return ent.get("dram_bytes_per_launch")
+            return ent["dram_bytes_per_unit"] * units
     except Exception:
         return None
     return None
@@ -403,7 +404,8 @@ def main():
                          f"{el:.1f} s; fp64 C oracle, OpenMP"}
 
     wl_name = workload_name(cfg)
-    traffic = recorded_traffic("gateup", wl_name)
+    U_ev = sum(U[(j * EV_EVERY) % NL] for j in range(KE)) / KE
+    traffic = recorded_traffic("gateup", wl_name, U_ev)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
