@@ -300,6 +300,10 @@ def main():
     def gateup_bytes(u):
         return u * gu_w_bytes + R * H * 2 + R * I * 2
 
+    def fused_bytes(u):
+        # both components of the distinct experts + token rows + h out and back + y out
+        return u * (gu_w_bytes + dn_w_bytes) + R * H * 2 + 2 * R * I * 2 + R * H * 4
+
     def layer_bytes(u):
         # distinct experts' weights + router + x in + out + route labels
         return u * (gu_w_bytes + dn_w_bytes) + router_bytes + 2 * cfg.T * H * 2 + R * 8
@@ -322,26 +326,31 @@ def main():
     t_issue0 = time.perf_counter()
     e_start.record(st)
     bound = [layers[l].bound_calls(xs[l], cfg.T, stream=st) for l in range(NL)]
+    names = [c[0] for c in bound[0]]
+    fused = "moe_expert_swiglu_fused" in names
+    # the dominant kernel(s): the fused contraction, or gate/up then down
+    i_main = names.index("moe_expert_swiglu_fused" if fused else "moe_expert_gateup")
     issue = MoELayer.issue
-    # Per-kernel events bracket the two expert contractions on every
-    # EV_EVERY-th step (an event between kernels ends the overlap that
-    # programmatic dependent launch gives the next kernel, so the other steps
-    # run without them).
+    # Per-kernel events bracket the contraction(s) on every EV_EVERY-th step
+    # (an event between kernels ends the overlap that programmatic dependent
+    # launch gives the next kernel, so the other steps run without them).
     for i in range(K):
-        c_route, c_perm, c_gu, c_dn, c_comb = bound[i % NL]
-        issue(c_route)
-        issue(c_perm)
+        calls = bound[i % NL]
         if i % EV_EVERY == 0:
             j = i // EV_EVERY
+            for c in calls[:i_main]:
+                issue(c)
             ev_g0[j].record(st)
-            issue(c_gu)
+            issue(calls[i_main])
             ev_g1[j].record(st)
-            issue(c_dn)
+            if not fused:
+                issue(calls[i_main + 1])
             ev_d1[j].record(st)
+            for c in calls[i_main + (1 if fused else 2):]:
+                issue(c)
         else:
-            issue(c_gu)
-            issue(c_dn)
-        issue(c_comb)
+            for c in calls:
+                issue(c)
     e_end.record(st)
     t_issue1 = time.perf_counter()
     torch.cuda.synchronize()
@@ -366,7 +375,8 @@ def main():
     value = tokens / (total_ms / 1e3)
     pk = peaks()
     U_steps = [U[i % NL] for i in range(K)]
-    gu_bytes_avg = sum(gateup_bytes(U[(j * EV_EVERY) % NL]) for j in range(KE)) / KE
+    main_bytes = fused_bytes if fused else gateup_bytes
+    gu_bytes_avg = sum(main_bytes(U[(j * EV_EVERY) % NL]) for j in range(KE)) / KE
     layer_bytes_avg = sum(layer_bytes(u) for u in U_steps) / K
     achieved = gu_bytes_avg / (gu_avg / 1e3) / 1e9
     step_ms = total_ms / K
@@ -405,7 +415,7 @@ def main():
 
     wl_name = workload_name(cfg)
     U_ev = sum(U[(j * EV_EVERY) % NL] for j in range(KE)) / KE
-    traffic = recorded_traffic("gateup", wl_name, U_ev)
+    traffic = recorded_traffic("fused" if fused else "gateup", wl_name, U_ev)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -417,7 +427,9 @@ def main():
                    "l2": f"inputs larger than L2: {NL} distinct layer weight sets rotated "
                          f"({NL * (E * 3 * H * I * 2 + router_bytes) / 1e9:.1f} GB)",
                    "parallelism": f"replicas x{world}", "unique_experts_per_step": U},
-        "roofline": {"bound": "hbm", "kernel": "grouped_gemm_kernel (moe_expert_gateup)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "grouped_swiglu_fused_kernel (moe_expert_swiglu_fused: gate/up + SwiGLU + down)"
+                     if fused else "grouped_gemm_kernel (moe_expert_gateup)",
                      "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                      "peak_source": pk["source"] + " hbm_gbs",
@@ -432,7 +444,7 @@ def main():
         "host_issue_us_per_step": 1e6 * (t_issue1 - t_issue0) / K,
         "events_every": EV_EVERY,
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": 7 * K,
+        "gpu_launches": (6 if fused else 7) * K,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

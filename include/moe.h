@@ -199,6 +199,21 @@ MOE_API moe_status moe_grouped_swiglu(const uint16_t *x_perm, const int32_t *off
                               float *y_perm, int32_t *dev_status, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_expert_swiglu_fused -- moe_grouped_swiglu in one persistent launch for
+ * tile-packed bf16 records (fmt = MOE_W_BF16_TILED): the down tiles of an
+ * expert start as soon as that expert's gate/up tiles have stored h, so the
+ * two contractions share the GPU instead of meeting at a kernel boundary.
+ * Same inputs and outputs as moe_grouped_swiglu, plus
+ *   sync_ws  [E+1] int32 scratch, zero-filled before its first use; every
+ *            call that completes leaves it zero-filled again.  Calls that share
+ *            one sync_ws must not overlap on the GPU.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_expert_swiglu_fused(const uint16_t *x_perm, const int32_t *offsets, int R, int E, int H,
+                                           int I, int fmt, const void *w_gateup, const void *w_down,
+                                           uint16_t *h, float *y_perm, int32_t *sync_ws, int32_t *dev_status,
+                                           void *stream);
+
+/* ---------------------------------------------------------------------------
  * moe_pack_experts -- reorder one component of every expert record into the
  * tile order the contraction streams (done once, like loading a checkpoint).
  *

@@ -60,6 +60,7 @@ def load(path: str | None = None):
             "moe_expert_gateup": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
             "moe_expert_down": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
             "moe_grouped_swiglu": ([p, p, i, i, i, i, i, p, p, p, p, p, p, p, p], i),
+            "moe_expert_swiglu_fused": ([p, p, i, i, i, i, i, p, p, p, p, p, p, p], i),
             "moe_combine": ([p, p, p, i, i, i, p, p, p, p, p], i),
             "route_block_dedup": ([p, i, i, i, i, i, i, i, p, p, p, p, p, p], i),
             "moe_rmsnorm": ([p, p, f, i, i, p, p, p], i),
@@ -157,6 +158,14 @@ def moe_grouped_swiglu(x_perm, offsets, E, H, I, w_gateup, w_down, h, y_perm, de
                                    _ptr(w_down), _ptr(s_down), _ptr(h), _ptr(y_perm), _ptr(dev_status),
                                    _stream(stream))
     _check("moe_grouped_swiglu", st)
+
+
+def moe_expert_swiglu_fused(x_perm, offsets, E, H, I, w_gateup, w_down, h, y_perm, sync_ws, dev_status,
+                            fmt=MOE_W_BF16_TILED, stream=None):
+    R = x_perm.shape[0]
+    st = load().moe_expert_swiglu_fused(_ptr(x_perm), _ptr(offsets), R, E, H, I, fmt, _ptr(w_gateup), _ptr(w_down),
+                                        _ptr(h), _ptr(y_perm), _ptr(sync_ws), _ptr(dev_status), _stream(stream))
+    _check("moe_expert_swiglu_fused", st)
 
 
 def moe_combine(y_perm, inv_perm, topk_w, residual, out_bf16, out_f32, dev_status, stream=None):

@@ -494,6 +494,363 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
   }
 }
 
+// ============================================================== fused SwiGLU
+// Gate/up and down of every routed expert in one persistent launch (tile-
+// packed bf16 records).  The tile list is all gate/up tiles (expert-major)
+// followed by all down tiles (expert-major).  A down tile of expert e may
+// start once the gate/up tiles of e have stored their h rows: each of their
+// epilogue warps fences its generic stores for the async proxy and bumps
+// ready[e]; the
+// producer of a down tile polls ready[e] (acquire, bounded) before its TMA
+// loads of h.  Down tiles thus fill the SMs the gate/up tail would leave
+// idle, and there is no kernel boundary between the two contractions.  The
+// last CTA to exit resets ready[0..E] to zero for the next call.
+struct FusedArgs {
+  const int32_t* offsets;
+  int E, R;
+  const uint8_t* tiles_gu;  // packed gate/up records
+  const uint8_t* tiles_dn;  // packed down records
+  int ks_gu, ks_dn;         // K steps per tile: H/64, I/64
+  int mb_gu, mb_dn;         // weight blocks per expert: I/64, H/128
+  uint16_t* h;              // [R, I]
+  float* y;                 // [R, H]
+  int I, H;
+  int* ready;               // [E+1]
+  int32_t* status;
+};
+
+template <int NMAX, int GG>
+struct CfgF {
+  static constexpr int G = GG;
+  static constexpr int kBBytes = NMAX * kBK * 2;
+  static constexpr int kStageBytes = G * (kABytes + kBBytes);
+  static constexpr int kBudget = 196 * 1024;
+  static constexpr int kStages = kBudget / kStageBytes < 2 ? 2 : (kBudget / kStageBytes > 10 ? 10 : kBudget / kStageBytes);
+  static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kTail = 16 + 3 * (kMaxE + 1) * 4;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + kTail;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+struct FTile {
+  int kind;  // 0 gate/up, 1 down
+  int e, mb, row0, nrows;
+};
+
+template <int NMAX, int GG>
+__global__ void __launch_bounds__(kCoreThreads, 1)
+    grouped_swiglu_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmH,
+                                FusedArgs p) {
+  using C = CfgF<NMAX, GG>;
+  constexpr int S = C::kStages;
+  constexpr int G = C::G;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = sA + S * G * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S * G * C::kBBytes);
+  const uint32_t full0 = ptx::smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * S;
+  const uint32_t accf0 = empty0 + 8 * S;
+  const uint32_t acce0 = accf0 + 16;
+  const uint32_t drain = acce0 + 16;
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
+  int* pre_gu = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
+  int* pre_dn = pre_gu + (kMaxE + 1);
+  int* soff = pre_dn + (kMaxE + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(full0 + 8 * s, 1);
+      ptx::mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(accf0 + 8 * a, 1);
+      ptx::mbar_init(acce0 + 8 * a, 128);
+    }
+    ptx::mbar_init(drain, 1);
+    misc[1] = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmX);
+    ptx::prefetch_tmap(&tmH);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(&misc[0])), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) soff[i] = min(max(p.offsets[i], 0), p.R);
+  __syncthreads();
+  if (warp == 0) {
+    int run_gu = 0, run_dn = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      int n = 0;
+      if (e < E) n = max(soff[e + 1] - soff[e], 0);
+      const int chunks = (n + NMAX - 1) / NMAX;
+      int a = chunks * p.mb_gu, b = chunks * p.mb_dn;
+      int ia = a, ib = b;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int ya = __shfl_up_sync(0xffffffffu, ia, d);
+        const int yb = __shfl_up_sync(0xffffffffu, ib, d);
+        if (lane >= d) {
+          ia += ya;
+          ib += yb;
+        }
+      }
+      if (e < E) {
+        pre_gu[e] = run_gu + ia - a;
+        pre_dn[e] = run_dn + ib - b;
+      }
+      run_gu += __shfl_sync(0xffffffffu, ia, 31);
+      run_dn += __shfl_sync(0xffffffffu, ib, 31);
+    }
+    if (lane == 0) {
+      pre_gu[E] = run_gu;
+      pre_dn[E] = run_dn;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const int total_gu = pre_gu[E];
+  const int total = total_gu + pre_dn[E];
+
+  auto tile_of = [&](int t) {
+    FTile tl;
+    tl.kind = t >= total_gu;
+    const int* pre = tl.kind ? pre_dn : pre_gu;
+    const int tt = tl.kind ? t - total_gu : t;
+    const int mbk = tl.kind ? p.mb_dn : p.mb_gu;
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid] <= tt) lo = mid; else hi = mid;
+    }
+    const int local = tt - pre[lo];
+    const int chunk = local / mbk;
+    const int start = soff[lo];
+    const int len = max(soff[lo + 1] - start, 0);
+    tl.e = lo;
+    tl.mb = local - chunk * mbk;
+    tl.row0 = start + chunk * NMAX;
+    tl.nrows = min(NMAX, len - chunk * NMAX);
+    return tl;
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_w = ptx::policy_evict_first();
+    const uint64_t pol_x = ptx::policy_evict_last();
+    int armed[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) armed[s] = -1;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    int ready_e = -1;  // expert whose h rows are known to be complete
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const FTile tl = tile_of(t);
+      const int nblk = (tl.nrows + kBoxRows - 1) / kBoxRows;
+      const int KS = tl.kind ? p.ks_dn : p.ks_gu;
+      const uint8_t* wt = tl.kind ? p.tiles_dn : p.tiles_gu;
+      const CUtensorMap* tb = tl.kind ? &tmH : &tmX;
+      if (tl.kind && tl.e != ready_e) {
+        // wait until every gate/up tile of expert e has stored its h rows
+        // (each tile's four epilogue warps arrive once)
+        const int target = 4 * (pre_gu[tl.e + 1] - pre_gu[tl.e]);
+        uint64_t t0 = 0;
+        for (uint32_t it = 0; ld_acquire_gpu(p.ready + tl.e) < target; ++it) {
+          __nanosleep(64);
+          if ((it & 1023u) == 1023u) {
+            if (misc[1]) {
+              ok = false;
+              break;
+            }
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+              t0 = now;
+            } else if (now - t0 > kWaitNs) {
+              misc[1] = 1;
+              set_status(p.status, MOE_DEV_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (!ok) break;
+        fence_proxy_async_global();
+        ready_e = tl.e;
+      }
+      const size_t chunk0 = (static_cast<size_t>(tl.e) * (tl.kind ? p.mb_dn : p.mb_gu) + tl.mb) * KS;
+      for (int ks = 0; ks < KS; ks += G) {
+        if (!wait_bounded<kSpin>(empty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full0 + 8 * s;
+        ptx::mbar_arrive_expect_tx(fb, G * (kABytes + nblk * kBBoxBytes));
+        armed[s] = static_cast<int>(ph);
+        const uint32_t a_dst = ptx::smem_u32(sA + s * G * kABytes);
+        const uint32_t b_dst = ptx::smem_u32(sB + s * G * C::kBBytes);
+        ptx::bulk_load(a_dst, wt + (chunk0 + ks) * kABytes, G * kABytes, fb, pol_w);
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+          for (int b = 0; b < nblk; ++b)
+            ptx::tma_load_2d(b_dst + j * C::kBBytes + b * kBBoxBytes, tb, fb, (ks + j) * kBK, tl.row0 + b * kBoxRows,
+                             pol_x);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (!ok || misc[1]) {
+#pragma unroll
+      for (int q = 0; q < S; ++q)
+        if (armed[q] >= 0) wait_drain(full0 + 8 * q, static_cast<uint32_t>(armed[q]));
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    int s = 0;
+    uint32_t ph = 0;
+    int acc = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    bool issued = false;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const FTile tl = tile_of(t);
+      const int KS = tl.kind ? p.ks_dn : p.ks_gu;
+      const uint32_t idesc = ptx::idesc_bf16_f32(kBM, static_cast<uint32_t>((tl.nrows + 15) & ~15));
+      if (!wait_bounded<kSpin>(acce0 + 8 * acc, aph ^ 1u, misc + 1, p.status)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NMAX);
+      for (int ks = 0; ks < KS; ks += G) {
+        if (!wait_bounded<kSpin>(full0 + 8 * s, ph, misc + 1, p.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+          issue_k_step(d_tmem, ptx::smem_u32(sA + (s * G + j) * kABytes), ptx::smem_u32(sB + (s * G + j) * C::kBBytes),
+                       idesc, ks + j);
+        issued = true;
+        ptx::umma_commit(empty0 + 8 * s);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      ptx::umma_commit(accf0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        aph ^= 1u;
+      }
+    }
+    if ((!ok || misc[1]) && issued) {
+      ptx::umma_commit(drain);
+      wait_drain(drain, 0);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const FTile tl = tile_of(t);
+      const bool ok = wait_bounded<kSleepEpi>(accf0 + 8 * acc, aph, misc + 1, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * NMAX);
+      if (tl.kind == 0) {
+        const bool up_lane = lane >= 16;
+        const int i = tl.mb * 64 + q * 16 + (lane & 15);
+        for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
+          float v[16];
+          ptx::tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+          float recv[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const float send = up_lane ? v[jj] : v[8 + jj];
+            recv[jj] = __shfl_xor_sync(0xffffffffu, send, 16);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int col = c0 + (up_lane ? 8 : 0) + jj;
+            const float g = up_lane ? recv[jj] : v[jj];
+            const float u = up_lane ? v[8 + jj] : recv[jj];
+            if (col < tl.nrows)
+              p.h[static_cast<size_t>(tl.row0 + col) * p.I + i] = f32_to_bf16(g / (1.0f + expf(-g)) * u);
+          }
+        }
+        // publish this warp's h rows to TMA loads in other CTAs: each lane
+        // fences its own stores, then one arrival per warp (4 per tile)
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.ready + tl.e, 1);
+      } else {
+        const int j = tl.mb * kBM + row_in_tile;
+        for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
+          float v[16];
+          ptx::tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int col = c0 + jj;
+            if (col < tl.nrows) p.y[static_cast<size_t>(tl.row0 + col) * p.H + j] = v[jj];
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(acce0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        aph ^= 1u;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    // the last CTA out resets the readiness counters for the next call
+    __threadfence();
+    if (atomicAdd(p.ready + E, 1) == static_cast<int>(gridDim.x) - 1) {
+      for (int e = 0; e < E; ++e) p.ready[e] = 0;
+      p.ready[E] = 0;
+      __threadfence();
+    }
+  }
+}
+
 // ============================================================== int4 kernel
 template <int NMAX, int KIND>
 __global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
@@ -863,7 +1220,56 @@ int pick_nmax(int rows_hint) {
   return 128;
 }
 
+template <int NMAX, int GG>
+cudaError_t run_fused(const CUtensorMap& mx, const CUtensorMap& mh, const FusedArgs& args, cudaStream_t st) {
+  using C = CfgF<NMAX, GG>;
+  auto kern = grouped_swiglu_fused_kernel<NMAX, GG>;
+  cudaError_t e = ensure_smem(kern, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = sm_count();
+  if (grid <= 0) return cudaErrorNoDevice;
+  return launch_pdl(kern, dim3(grid), dim3(kCoreThreads), C::kSmemBytes, st, mx, mh, args);
+}
+
 }  // namespace
+
+cudaError_t launch_swiglu_fused(const uint16_t* x_perm, const int32_t* offsets, int E, int R, int H, int I,
+                                const void* w_gateup, const void* w_down, uint16_t* h, float* y, int32_t* ready,
+                                int32_t* st_word, cudaStream_t st) {
+  CUtensorMap mx, mh;
+  if (!make_rows_map(&mx, x_perm, H, R, kBoxRows)) return cudaErrorInvalidValue;
+  if (!make_rows_map(&mh, h, I, R, kBoxRows)) return cudaErrorInvalidValue;
+  FusedArgs a{};
+  a.offsets = offsets;
+  a.E = E;
+  a.R = R;
+  a.tiles_gu = static_cast<const uint8_t*>(w_gateup);
+  a.tiles_dn = static_cast<const uint8_t*>(w_down);
+  a.ks_gu = H / kBK;
+  a.ks_dn = I / kBK;
+  a.mb_gu = I / 64;
+  a.mb_dn = H / kBM;
+  a.h = h;
+  a.y = y;
+  a.I = I;
+  a.H = H;
+  a.ready = ready;
+  a.status = st_word;
+  if (a.ks_gu % 2 == 0 && a.ks_dn % 2 == 0) {
+    switch (pick_nmax(R)) {
+      case 16: return run_fused<16, 2>(mx, mh, a, st);
+      case 32: return run_fused<32, 2>(mx, mh, a, st);
+      case 64: return run_fused<64, 2>(mx, mh, a, st);
+      default: return run_fused<128, 2>(mx, mh, a, st);
+    }
+  }
+  switch (pick_nmax(R)) {
+    case 16: return run_fused<16, 1>(mx, mh, a, st);
+    case 32: return run_fused<32, 1>(mx, mh, a, st);
+    case 64: return run_fused<64, 1>(mx, mh, a, st);
+    default: return run_fused<128, 1>(mx, mh, a, st);
+  }
+}
 
 cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uint16_t* scales, const uint16_t* b_rows,
                                 const int32_t* offsets, int E, int R, int H, int I, int router_E, void* out,

@@ -61,6 +61,8 @@ class MoELayer:
         self.y_perm = torch.empty((R, H), dtype=torch.float32, device=dev)
         self.out = torch.empty((T_max, H), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self.sync_ws = torch.zeros((E + 1,), dtype=torch.int32, device=dev)
+        self.fused = (fmt == _lib.MOE_W_BF16_TILED)
         self._bound = {}
 
     # -- the five boundary calls, bound once per (T, x, out, stream) ---------
@@ -100,12 +102,21 @@ class MoELayer:
             ("moe_permute", lib.moe_permute,
              (P(self.ids), T, k, E, P(x), H, P(self.counts), P(self.offsets), P(self.perm), P(self.inv),
               P(self.x_perm), P(self.status), st)),
-            ("moe_expert_gateup", lib.moe_expert_gateup,
-             (P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt, P(self.w_gateup), None, P(self.h),
-              P(self.status), st)),
-            ("moe_expert_down", lib.moe_expert_down,
-             (P(self.h), P(self.offsets), R, E, H, I, self.fmt, P(self.w_down), None, P(self.y_perm),
-              P(self.status), st)),
+        ]
+        if self.fused:
+            calls.append(("moe_expert_swiglu_fused", lib.moe_expert_swiglu_fused,
+                          (P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt, P(self.w_gateup), P(self.w_down),
+                           P(self.h), P(self.y_perm), P(self.sync_ws), P(self.status), st)))
+        else:
+            calls += [
+                ("moe_expert_gateup", lib.moe_expert_gateup,
+                 (P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt, P(self.w_gateup), None, P(self.h),
+                  P(self.status), st)),
+                ("moe_expert_down", lib.moe_expert_down,
+                 (P(self.h), P(self.offsets), R, E, H, I, self.fmt, P(self.w_down), None, P(self.y_perm),
+                  P(self.status), st)),
+            ]
+        calls += [
             ("moe_combine", lib.moe_combine,
              (P(self.y_perm), P(self.inv), P(self.w), T, k, H, P(residual), P(out), P(out_f32), P(self.status), st)),
         ]

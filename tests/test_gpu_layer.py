@@ -304,7 +304,11 @@ def test_layer_deterministic():
     b = layer.forward(d["x"]).clone()
     tl, _ = run_layer(cfg, d, tiled=True)
     c = tl.forward(d["x"]).clone()
+    c2 = tl.forward(d["x"]).clone()
     torch.cuda.synchronize()
+    # the fused contraction leaves its readiness counters zeroed for the next call
+    assert int(tl.sync_ws.abs().sum().item()) == 0
+    assert torch.equal(c.view(torch.int16), c2.view(torch.int16))
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     # packing changes where weights live, not the arithmetic: identical bits
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))
