@@ -301,8 +301,11 @@ def main():
         return u * gu_w_bytes + R * H * 2 + R * I * 2
 
     def fused_bytes(u):
-        # both components of the distinct experts + token rows + h out and back + y out
-        return u * (gu_w_bytes + dn_w_bytes) + R * H * 2 + 2 * R * I * 2 + R * H * 4
+        # both components of the distinct experts + token rows + h out and back
+        # + y out (+ the row gather's token reads and row writes when the
+        # launch gathers)
+        b = u * (gu_w_bytes + dn_w_bytes) + R * H * 2 + 2 * R * I * 2 + R * H * 4
+        return b + (cfg.T * H * 2 + R * H * 2 if gather_in_fused else 0)
 
     def layer_bytes(u):
         # distinct experts' weights + router + x in + out + route labels
@@ -328,6 +331,7 @@ def main():
     bound = [layers[l].bound_calls(xs[l], cfg.T, stream=st) for l in range(NL)]
     names = [c[0] for c in bound[0]]
     fused = "moe_expert_swiglu_fused" in names
+    gather_in_fused = fused and R <= MoELayer.GATHER_IN_FUSED_MAX_ROWS
     # the dominant kernel(s): the fused contraction, or gate/up then down
     i_main = names.index("moe_expert_swiglu_fused" if fused else "moe_expert_gateup")
     issue = MoELayer.issue
@@ -428,7 +432,8 @@ def main():
                          f"({NL * (E * 3 * H * I * 2 + router_bytes) / 1e9:.1f} GB)",
                    "parallelism": f"replicas x{world}", "unique_experts_per_step": U},
         "roofline": {"bound": "hbm",
-                     "kernel": "grouped_swiglu_fused_kernel (moe_expert_swiglu_fused: gate/up + SwiGLU + down)"
+                     "kernel": "grouped_swiglu_fused_kernel (moe_expert_swiglu_fused: "
+                               + ("row gather, " if gather_in_fused else "") + "gate/up + SwiGLU, down)"
                      if fused else "grouped_gemm_kernel (moe_expert_gateup)",
                      "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
@@ -440,11 +445,13 @@ def main():
                            "frac_hbm": layer_bytes_avg / (step_ms / 1e3) / 1e9 / pk["hbm_gbs"],
                            "tflops": flops_step / (step_ms / 1e3) / 1e12,
                            "frac_tensor": flops_step / (step_ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
-                           "down_avg_us": dn_avg * 1e3},
+                           **({} if fused else {"down_avg_us": dn_avg * 1e3})},
         "host_issue_us_per_step": 1e6 * (t_issue1 - t_issue0) / K,
         "events_every": EV_EVERY,
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": (6 if fused else 7) * K,
+        # route: logits + selection; permute (+ row gather unless the fused
+        # launch gathers); experts (fused: one launch; else gate/up, down, combine)
+        "gpu_launches": (5 if gather_in_fused else 6 if fused else 7) * K,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

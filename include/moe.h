@@ -203,15 +203,26 @@ MOE_API moe_status moe_grouped_swiglu(const uint16_t *x_perm, const int32_t *off
  * tile-packed bf16 records (fmt = MOE_W_BF16_TILED): the down tiles of an
  * expert start as soon as that expert's gate/up tiles have stored h, so the
  * two contractions share the GPU instead of meeting at a kernel boundary.
- * Same inputs and outputs as moe_grouped_swiglu, plus
- *   sync_ws  [E+1] int32 scratch, zero-filled before its first use; every
- *            call that completes leaves it zero-filled again.  Calls that share
- *            one sync_ws must not overlap on the GPU.
+ * Optionally the launch also does moe_permute's row gather first.
+ *
+ * Same arithmetic and outputs (h, y_perm) as moe_grouped_swiglu, plus
+ *   x        [R/k, H] bf16 or NULL.  If given, the launch first writes
+ *            x_perm[s,:] = x[perm[s] / k, :] for every slot (perm [R] int32
+ *            from moe_permute, k the routes per token, R % k == 0), exactly
+ *            what moe_permute's gather writes; if NULL, x_perm is an input
+ *            holding those rows and k, perm are ignored.
+ *   sync_ws  [E+2] int32 scratch, zero-filled before its first use; a call
+ *            that completes leaves it zero-filled again.  After a call whose
+ *            dev_status shows MOE_DEV_TIMEOUT, zero it again.  Calls that
+ *            share one sync_ws must not overlap on the GPU.
+ * The launch is persistent (one CTA per SM) and its CTAs wait on one another
+ * (bounded): do not run it beside work that could keep some of its CTAs from
+ * becoming resident.
  * ------------------------------------------------------------------------- */
-MOE_API moe_status moe_expert_swiglu_fused(const uint16_t *x_perm, const int32_t *offsets, int R, int E, int H,
-                                           int I, int fmt, const void *w_gateup, const void *w_down,
-                                           uint16_t *h, float *y_perm, int32_t *sync_ws, int32_t *dev_status,
-                                           void *stream);
+MOE_API moe_status moe_expert_swiglu_fused(const uint16_t *x, int k, const int32_t *perm, uint16_t *x_perm,
+                                           const int32_t *offsets, int R, int E, int H, int I, int fmt,
+                                           const void *w_gateup, const void *w_down, uint16_t *h, float *y_perm,
+                                           int32_t *sync_ws, int32_t *dev_status, void *stream);
 
 /* ---------------------------------------------------------------------------
  * moe_pack_experts -- reorder one component of every expert record into the

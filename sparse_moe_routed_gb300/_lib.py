@@ -60,7 +60,7 @@ def load(path: str | None = None):
             "moe_expert_gateup": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
             "moe_expert_down": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
             "moe_grouped_swiglu": ([p, p, i, i, i, i, i, p, p, p, p, p, p, p, p], i),
-            "moe_expert_swiglu_fused": ([p, p, i, i, i, i, i, p, p, p, p, p, p, p], i),
+            "moe_expert_swiglu_fused": ([p, i, p, p, p, i, i, i, i, i, p, p, p, p, p, p, p], i),
             "moe_combine": ([p, p, p, i, i, i, p, p, p, p, p], i),
             "route_block_dedup": ([p, i, i, i, i, i, i, i, p, p, p, p, p, p], i),
             "moe_rmsnorm": ([p, p, f, i, i, p, p, p], i),
@@ -161,10 +161,13 @@ def moe_grouped_swiglu(x_perm, offsets, E, H, I, w_gateup, w_down, h, y_perm, de
 
 
 def moe_expert_swiglu_fused(x_perm, offsets, E, H, I, w_gateup, w_down, h, y_perm, sync_ws, dev_status,
-                            fmt=MOE_W_BF16_TILED, stream=None):
+                            fmt=MOE_W_BF16_TILED, x=None, perm=None, k=0, stream=None):
+    """Gate/up + SwiGLU + down in one launch; with x (and perm, k) it also
+    gathers x_perm from x first."""
     R = x_perm.shape[0]
-    st = load().moe_expert_swiglu_fused(_ptr(x_perm), _ptr(offsets), R, E, H, I, fmt, _ptr(w_gateup), _ptr(w_down),
-                                        _ptr(h), _ptr(y_perm), _ptr(sync_ws), _ptr(dev_status), _stream(stream))
+    st = load().moe_expert_swiglu_fused(_ptr(x), k, _ptr(perm), _ptr(x_perm), _ptr(offsets), R, E, H, I, fmt,
+                                        _ptr(w_gateup), _ptr(w_down), _ptr(h), _ptr(y_perm), _ptr(sync_ws),
+                                        _ptr(dev_status), _stream(stream))
     _check("moe_expert_swiglu_fused", st)
 
 

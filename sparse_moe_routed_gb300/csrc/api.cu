@@ -207,9 +207,10 @@ moe_status moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets, in
   return moe_expert_down(h, offsets, R, E, H, I, fmt, w_down, s_down, y_perm, dev_status, stream);
 }
 
-moe_status moe_expert_swiglu_fused(const uint16_t* x_perm, const int32_t* offsets, int R, int E, int H, int I,
-                                   int fmt, const void* w_gateup, const void* w_down, uint16_t* h, float* y_perm,
-                                   int32_t* sync_ws, int32_t* dev_status, void* stream) {
+moe_status moe_expert_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
+                                   const int32_t* offsets, int R, int E, int H, int I, int fmt, const void* w_gateup,
+                                   const void* w_down, uint16_t* h, float* y_perm, int32_t* sync_ws,
+                                   int32_t* dev_status, void* stream) {
   moe_status c = check_expert_args(R, E, H, I, fmt);
   if (c != MOE_OK) return c;
   if (fmt != MOE_W_BF16_TILED) return MOE_ENOTSUP;
@@ -218,9 +219,14 @@ moe_status moe_expert_swiglu_fused(const uint16_t* x_perm, const int32_t* offset
   if (!a16(x_perm) || !a16(w_gateup) || !a16(w_down) || !a16(h) || !a16(y_perm) || !a4(offsets) ||
       !a4(dev_status) || !a4(sync_ws))
     return MOE_EINVAL;
+  if (x) {  // gather in the same launch
+    if (k <= 0 || R % k != 0) return MOE_ESHAPE;
+    if (k > moe::kMaxK) return MOE_ENOTSUP;
+    if (!perm || !a16(x) || !a4(perm)) return MOE_EINVAL;
+  }
   if (R == 0) return MOE_OK;
-  return cuda_status(moe::launch_swiglu_fused(x_perm, offsets, E, R, H, I, w_gateup, w_down, h, y_perm, sync_ws,
-                                              dev_status, static_cast<cudaStream_t>(stream)));
+  return cuda_status(moe::launch_swiglu_fused(x, k, perm, x_perm, offsets, E, R, H, I, w_gateup, w_down, h, y_perm,
+                                              sync_ws, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_pack_size(int fmt_in, int E, int H, int I, int which) {

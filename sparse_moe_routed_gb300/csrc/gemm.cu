@@ -515,8 +515,15 @@ struct FusedArgs {
   uint16_t* h;              // [R, I]
   float* y;                 // [R, H]
   int I, H;
-  int* ready;               // [E+1]
+  int* ready;               // sync words: [E] per-expert h readiness, then exit and gather counters
   int32_t* status;
+  // Row gather (x != nullptr): every CTA first copies its share of the rows
+  // x_perm[s] = x[perm[s] / k]; the gate/up producers start their token-row
+  // loads once all CTAs have done so.
+  const uint16_t* x;
+  uint16_t* x_perm;
+  const int32_t* perm;
+  int k;
 };
 
 template <int NMAX, int GG>
@@ -546,6 +553,37 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 struct FTile {
   int kind;  // 0 gate/up, 1 down
   int e, mb, row0, nrows;
+};
+
+// The tiles one CTA runs, in order: its round-robin share of the gate/up
+// tiles, then down tiles.  A gate/up tile costs wg K steps and a down tile wd;
+// the CTAs left one gate/up tile short first take wg / wd down tiles each
+// (the earliest experts' down tiles), and the rest of the down tiles go round
+// robin from the first such CTA.  This levels the CTAs' total K steps to
+// within one down tile, where plain round robin over the whole list can leave
+// a CTA a gate/up tile plus a down tile above the mean.  Every role of the
+// CTA walks the same sequence, and every tile is in exactly one CTA's.
+struct FSeq {
+  int b, P, tgu, tdn, g_b, li, fill, nfill, F, rr0;
+  __device__ FSeq(int b_, int P_, int tgu_, int tdn_, int wg, int wd) : b(b_), P(P_), tgu(tgu_), tdn(tdn_) {
+    g_b = tgu > b ? (tgu - 1 - b) / P + 1 : 0;
+    const int r = tgu % P;
+    const bool low = r != 0 && b >= r;
+    fill = (r != 0 && wd > 0) ? max(wg / wd, 1) : 0;
+    F = min((r != 0 ? P - r : 0) * fill, tdn);
+    li = b - r;
+    nfill = low ? min(max(F - li * fill, 0), fill) : 0;
+    rr0 = ((b - r) % P + P) % P;
+  }
+  // Index (gate/up tiles first, then down tiles) of the n-th tile, or -1.
+  __device__ int tile(int n) const {
+    if (n < g_b) return b + n * P;
+    n -= g_b;
+    if (n < nfill) return tgu + li * fill + n;
+    n -= nfill;
+    const int d = F + rr0 + n * P;
+    return d < tdn ? tgu + d : -1;
+  }
 };
 
 template <int NMAX, int GG>
@@ -596,6 +634,42 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
   pdl_wait();
   pdl_trigger();
   for (int i = threadIdx.x; i <= E; i += blockDim.x) soff[i] = min(max(p.offsets[i], 0), p.R);
+  if (p.x != nullptr) {
+    // this CTA's contiguous share of the permuted token rows, eight 16-byte
+    // loads in flight per thread
+    const int s0 = static_cast<int>(static_cast<long long>(p.R) * blockIdx.x / gridDim.x);
+    const int s1 = static_cast<int>(static_cast<long long>(p.R) * (blockIdx.x + 1) / gridDim.x);
+    const int vpr = p.H / 8;
+    const int n = (s1 - s0) * vpr;
+    constexpr int U = 8;
+    for (int i0 = threadIdx.x; i0 < n; i0 += U * kCoreThreads) {
+      uint4 v[U];
+      int dst[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * kCoreThreads;
+        dst[u] = -1;
+        if (i < n) {
+          const int sl = s0 + i / vpr;
+          const int c = i - (sl - s0) * vpr;
+          const int r = p.perm[sl];
+          if (r >= 0 && r < p.R) {
+            v[u] = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(r / p.k) * p.H)[c];
+            dst[u] = sl * vpr + c;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (dst[u] >= 0) reinterpret_cast<uint4*>(p.x_perm)[dst[u]] = v[u];
+    }
+    // publish to the TMA loads of every CTA: fence for the async proxy, then
+    // one arrival per CTA
+    fence_proxy_async_global();
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(p.ready + E + 1, 1);
+  }
   __syncthreads();
   if (warp == 0) {
     int run_gu = 0, run_dn = 0;
@@ -632,7 +706,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const int total_gu = pre_gu[E];
-  const int total = total_gu + pre_dn[E];
+  const FSeq seq(blockIdx.x, gridDim.x, total_gu, pre_dn[E], p.ks_gu, p.ks_dn);
 
   auto tile_of = [&](int t) {
     FTile tl;
@@ -667,12 +741,50 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     uint32_t ph = 0;
     bool ok = true;
     int ready_e = -1;  // expert whose h rows are known to be complete
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    // Until every CTA has gathered its token rows, stages get their weight
+    // chunk at once and their token rows later (at most S stages deferred).
+    bool gathered = p.x == nullptr;
+    int npend = 0;
+    uint32_t pend_dst[S], pend_bar[S];
+    int pend_ks[S], pend_row[S], pend_nblk[S];
+    auto flush_pending = [&]() -> bool {
+      if (!gathered) {
+        uint64_t t0 = 0;
+        for (uint32_t it = 0; ld_acquire_gpu(p.ready + E + 1) < static_cast<int>(gridDim.x); ++it) {
+          __nanosleep(32);
+          if ((it & 1023u) == 1023u) {
+            if (misc[1]) return false;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+              t0 = now;
+            } else if (now - t0 > kWaitNs) {
+              misc[1] = 1;
+              set_status(p.status, MOE_DEV_TIMEOUT);
+              return false;
+            }
+          }
+        }
+        fence_proxy_async_global();
+        gathered = true;
+      }
+      for (int q = 0; q < npend; ++q)
+        for (int j = 0; j < G; ++j)
+          for (int b = 0; b < pend_nblk[q]; ++b)
+            ptx::tma_load_2d(pend_dst[q] + j * C::kBBytes + b * kBBoxBytes, &tmX, pend_bar[q], (pend_ks[q] + j) * kBK,
+                             pend_row[q] + b * kBoxRows, pol_x);
+      npend = 0;
+      return true;
+    };
+    for (int n = 0, t; ok && (t = seq.tile(n)) >= 0; ++n) {
       const FTile tl = tile_of(t);
       const int nblk = (tl.nrows + kBoxRows - 1) / kBoxRows;
       const int KS = tl.kind ? p.ks_dn : p.ks_gu;
       const uint8_t* wt = tl.kind ? p.tiles_dn : p.tiles_gu;
       const CUtensorMap* tb = tl.kind ? &tmH : &tmX;
+      if (tl.kind && (npend > 0 || !gathered) && !flush_pending()) {
+        ok = false;
+        break;
+      }
       if (tl.kind && tl.e != ready_e) {
         // wait until every gate/up tile of expert e has stored its h rows
         // (each tile's four epilogue warps arrive once)
@@ -712,16 +824,29 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         const uint32_t a_dst = ptx::smem_u32(sA + s * G * kABytes);
         const uint32_t b_dst = ptx::smem_u32(sB + s * G * C::kBBytes);
         ptx::bulk_load(a_dst, wt + (chunk0 + ks) * kABytes, G * kABytes, fb, pol_w);
+        if (!gathered) {
+          pend_dst[npend] = b_dst;
+          pend_bar[npend] = fb;
+          pend_ks[npend] = ks;
+          pend_row[npend] = tl.row0;
+          pend_nblk[npend] = nblk;
+          if (++npend == S && !flush_pending()) {
+            ok = false;
+            break;
+          }
+        } else {
 #pragma unroll
-        for (int j = 0; j < G; ++j)
-          for (int b = 0; b < nblk; ++b)
-            ptx::tma_load_2d(b_dst + j * C::kBBytes + b * kBBoxBytes, tb, fb, (ks + j) * kBK, tl.row0 + b * kBoxRows,
-                             pol_x);
+          for (int j = 0; j < G; ++j)
+            for (int b = 0; b < nblk; ++b)
+              ptx::tma_load_2d(b_dst + j * C::kBBytes + b * kBBoxBytes, tb, fb, (ks + j) * kBK,
+                               tl.row0 + b * kBoxRows, pol_x);
+        }
         if (++s == S) {
           s = 0;
           ph ^= 1u;
         }
       }
+      if (ok && npend > 0 && !flush_pending()) ok = false;
     }
     if (!ok || misc[1]) {
 #pragma unroll
@@ -736,7 +861,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     uint32_t aph = 0;
     bool ok = true;
     bool issued = false;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int n = 0, t; ok && (t = seq.tile(n)) >= 0; ++n) {
       const FTile tl = tile_of(t);
       const int KS = tl.kind ? p.ks_dn : p.ks_gu;
       const uint32_t idesc = ptx::idesc_bf16_f32(kBM, static_cast<uint32_t>((tl.nrows + 15) & ~15));
@@ -780,7 +905,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int n = 0, t; (t = seq.tile(n)) >= 0; ++n) {
       const FTile tl = tile_of(t);
       const bool ok = wait_bounded<kSleepEpi>(accf0 + 8 * acc, aph, misc + 1, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -840,14 +965,16 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
+  // The last CTA out resets the sync words for the next call.
   if (threadIdx.x == 0) {
-    // the last CTA out resets the readiness counters for the next call
     __threadfence();
-    if (atomicAdd(p.ready + E, 1) == static_cast<int>(gridDim.x) - 1) {
-      for (int e = 0; e < E; ++e) p.ready[e] = 0;
-      p.ready[E] = 0;
-      __threadfence();
-    }
+    misc[2] = atomicAdd(p.ready + E, 1) == static_cast<int>(gridDim.x) - 1;
+  }
+  __syncthreads();
+  if (misc[2]) {
+    __threadfence();
+    for (int e = threadIdx.x; e < E + 2; e += blockDim.x) p.ready[e] = 0;
+    __threadfence();
   }
 }
 
@@ -1233,9 +1360,10 @@ cudaError_t run_fused(const CUtensorMap& mx, const CUtensorMap& mh, const FusedA
 
 }  // namespace
 
-cudaError_t launch_swiglu_fused(const uint16_t* x_perm, const int32_t* offsets, int E, int R, int H, int I,
-                                const void* w_gateup, const void* w_down, uint16_t* h, float* y, int32_t* ready,
-                                int32_t* st_word, cudaStream_t st) {
+cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
+                                const int32_t* offsets, int E, int R, int H, int I, const void* w_gateup,
+                                const void* w_down, uint16_t* h, float* y, int32_t* ready, int32_t* st_word,
+                                cudaStream_t st) {
   CUtensorMap mx, mh;
   if (!make_rows_map(&mx, x_perm, H, R, kBoxRows)) return cudaErrorInvalidValue;
   if (!make_rows_map(&mh, h, I, R, kBoxRows)) return cudaErrorInvalidValue;
@@ -1255,6 +1383,10 @@ cudaError_t launch_swiglu_fused(const uint16_t* x_perm, const int32_t* offsets, 
   a.H = H;
   a.ready = ready;
   a.status = st_word;
+  a.x = x;
+  a.x_perm = x_perm;
+  a.perm = perm;
+  a.k = k > 0 ? k : 1;
   if (a.ks_gu % 2 == 0 && a.ks_dn % 2 == 0) {
     switch (pick_nmax(R)) {
       case 16: return run_fused<16, 2>(mx, mh, a, st);

@@ -64,9 +64,11 @@ cudaError_t launch_pack(int fmt_in, const void* w, const uint16_t* s, int E, int
                         cudaStream_t st);
 
 // Gate/up + SwiGLU + down in one persistent launch (tile-packed bf16).
-cudaError_t launch_swiglu_fused(const uint16_t* x_perm, const int32_t* offsets, int E, int R, int H, int I,
-                                const void* w_gateup, const void* w_down, uint16_t* h, float* y, int32_t* ready,
-                                int32_t* st_word, cudaStream_t st);
+// With x set, the launch first gathers x_perm[s] = x[perm[s] / k] itself.
+cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
+                                const int32_t* offsets, int E, int R, int H, int I, const void* w_gateup,
+                                const void* w_down, uint16_t* h, float* y, int32_t* ready, int32_t* st_word,
+                                cudaStream_t st);
 
 // combine.cu
 cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int k, int H,

@@ -1,11 +1,17 @@
 """One routed-expert MoE layer driven through the C ABI.
 
 ``MoELayer`` owns the device buffers a layer call needs (allocated once with
-torch, sized for ``T_max`` tokens) and issues the five boundary calls on one
-stream:
+torch, sized for ``T_max`` tokens) and issues the boundary calls on one
+stream.  With plain or int4 records:
 
     moe_route -> moe_permute (+ row gather) -> moe_expert_gateup ->
     moe_expert_down -> moe_combine
+
+With tile-packed bf16 records gate/up and down run as one persistent launch,
+which for a decode-sized block also gathers the token rows itself:
+
+    moe_route -> moe_permute (+ row gather unless few rows) ->
+    moe_expert_swiglu_fused -> moe_combine
 
 Every step runs in the CUDA library; this class only owns memory.
 """
@@ -25,6 +31,8 @@ class MoELayer:
     packed weights (fmt=MOE_W_BF16_TILED or MOE_W_INT4_G64_TILED): the uint8
     buffers moe_pack_experts wrote for the gate/up and down components (pass I).
     """
+
+    GATHER_IN_FUSED_MAX_ROWS = 4096
 
     def __init__(self, w_router, bias, w_gateup, w_down, k: int, T_max: int, fmt: int = _lib.MOE_W_BF16,
                  I: int = None):
@@ -61,8 +69,8 @@ class MoELayer:
         self.y_perm = torch.empty((R, H), dtype=torch.float32, device=dev)
         self.out = torch.empty((T_max, H), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
-        self.sync_ws = torch.zeros((E + 1,), dtype=torch.int32, device=dev)
         self.fused = (fmt == _lib.MOE_W_BF16_TILED)
+        self.sync_ws = torch.zeros((E + 2,), dtype=torch.int32, device=dev)
         self._bound = {}
 
     # -- the five boundary calls, bound once per (T, x, out, stream) ---------
@@ -98,15 +106,20 @@ class MoELayer:
             calls.append(("moe_route", lib.moe_route,
                           (P(x), P(self.w_router), P(self.bias), T, H, E, k, P(self.ids), P(self.w), P(self.gap),
                            P(self.ws), ws_bytes, st)))
+        # the fused launch gathers the token rows itself when there are few
+        # (a decode block); for many rows moe_permute's gather runs at full
+        # occupancy instead
+        gather_in_fused = self.fused and R <= self.GATHER_IN_FUSED_MAX_ROWS
         calls += [
             ("moe_permute", lib.moe_permute,
-             (P(self.ids), T, k, E, P(x), H, P(self.counts), P(self.offsets), P(self.perm), P(self.inv),
-              P(self.x_perm), P(self.status), st)),
+             (P(self.ids), T, k, E, None if gather_in_fused else P(x), H, P(self.counts), P(self.offsets),
+              P(self.perm), P(self.inv), None if gather_in_fused else P(self.x_perm), P(self.status), st)),
         ]
         if self.fused:
             calls.append(("moe_expert_swiglu_fused", lib.moe_expert_swiglu_fused,
-                          (P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt, P(self.w_gateup), P(self.w_down),
-                           P(self.h), P(self.y_perm), P(self.sync_ws), P(self.status), st)))
+                          (P(x) if gather_in_fused else None, k, P(self.perm), P(self.x_perm), P(self.offsets), R,
+                           E, H, I, self.fmt, P(self.w_gateup), P(self.w_down), P(self.h), P(self.y_perm),
+                           P(self.sync_ws), P(self.status), st)))
         else:
             calls += [
                 ("moe_expert_gateup", lib.moe_expert_gateup,
@@ -165,7 +178,10 @@ class MoELayer:
         return int(self.status.item())
 
     def clear_status(self):
+        """Zero the device status word (and the fused launch's sync words,
+        which a launch that gave up on a wait may have left non-zero)."""
         self.status.zero_()
+        self.sync_ws.zero_()
 
 
 class MoEStack:

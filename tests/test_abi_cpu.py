@@ -2,9 +2,8 @@
 
 The library must load, export every function include/moe.h declares, and
 reject bad arguments on the host before anything is enqueued.  The rejection
-cases here use placeholder addresses and every one of them must be refused by
-host admission; with a GPU present these run in test_gpu_negative.py instead,
-on real buffers.
+cases here use placeholder addresses, so every one of them must be refused by
+host admission before any device work; they run only where no GPU is visible.
 """
 import ctypes as C
 
@@ -179,3 +178,33 @@ def test_pack_rejections_and_sizes():
     assert L.moe_pack_experts(0, P, NUL, 64, 250, 64, 0, P, n, NUL) == _lib.MOE_ENOTSUP
     assert _gateup(fmt=1) == _lib.MOE_ENOTSUP  # plain int4 must be packed first
 
+
+
+def test_swiglu_fused_rejections():
+    L = lib()
+    # x, k, perm, x_perm, offsets, R, E, H, I, fmt, w_gateup, w_down, h, y_perm, sync_ws, dev_status, stream
+    base = [NUL, 0, NUL, P, P, 160, 512, 2560, 640, _lib.MOE_W_BF16_TILED, P, P, P, P, P, P, NUL]
+
+    def call(**kw):
+        a = list(base)
+        names = ["x", "k", "perm", "xp", "off", "R", "E", "H", "I", "fmt", "wgu", "wd", "h", "y", "sync", "st"]
+        for n, v in kw.items():
+            a[names.index(n)] = v
+        return L.moe_expert_swiglu_fused(*a)
+
+    assert call(fmt=_lib.MOE_W_BF16) == _lib.MOE_ENOTSUP          # packed bf16 records only
+    assert call(fmt=_lib.MOE_W_INT4_G64_TILED) == _lib.MOE_ENOTSUP
+    assert call(sync=NUL) == _lib.MOE_EWORKSPACE
+    assert call(xp=NUL) == _lib.MOE_EINVAL
+    assert call(st=NUL) == _lib.MOE_EINVAL
+    assert call(y=PM) == _lib.MOE_EINVAL
+    assert call(I=600) == _lib.MOE_ENOTSUP
+    assert call(R=-1) == _lib.MOE_ESHAPE
+    # with the gather: perm and a k that divides R are required
+    assert call(x=P, k=10, perm=NUL) == _lib.MOE_EINVAL
+    assert call(x=P, k=0, perm=P) == _lib.MOE_ESHAPE
+    assert call(x=P, k=7, perm=P) == _lib.MOE_ESHAPE             # 160 % 7 != 0
+    assert call(x=P, k=40, perm=P) == _lib.MOE_ENOTSUP
+    assert call(x=PM, k=10, perm=P) == _lib.MOE_EINVAL
+    assert call(R=0) == _lib.MOE_OK
+    assert call(R=0, x=P, k=10, perm=P) == _lib.MOE_OK

@@ -267,6 +267,7 @@ def test_combine_nonfinite_flag():
 @pytest.mark.parametrize("name,T,nsample,tiled", [("tiny", None, 16, False), ("decode", None, 16, False),
                                                   ("decode", 37, 37, False), ("prefill", None, 24, False),
                                                   ("tiny", None, 16, True), ("decode", None, 16, True),
+                                                  ("decode", 37, 37, True), ("decode", 1, 1, True),
                                                   ("prefill", None, 24, True)])
 def test_layer_parity(name, T, nsample, tiled):
     cfg, d, host = case(name, T)
@@ -314,14 +315,21 @@ def test_layer_deterministic():
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))
 
 
-def test_layer_single_token_and_empty():
+@pytest.mark.parametrize("tiled", [False, True])
+def test_layer_single_token_and_empty(tiled):
     cfg, d, host = case("tiny")
-    layer = MoELayer(d["w_router"], d["bias"], d["w_gateup"], d["w_down"], cfg.k, cfg.T)
+    if tiled:
+        gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, cfg.E, cfg.H, cfg.I)
+        layer = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, cfg.T, fmt=_lib.MOE_W_BF16_TILED, I=cfg.I)
+    else:
+        layer = MoELayer(d["w_router"], d["bias"], d["w_gateup"], d["w_down"], cfg.k, cfg.T)
     x1 = d["x"][3:4].contiguous()
     out1 = layer.forward(x1).clone()
     empty = layer.forward(d["x"][:0])
     torch.cuda.synchronize()
     assert empty.shape[0] == 0
+    if tiled:
+        assert int(layer.sync_ws.abs().sum().item()) == 0
     ids_r, w_r, _, _ = oracle.route(host["x"][3:4], host["wr"], None, cfg.k)
     ref = oracle.experts_combine(f32_of_bits(host["x"][3:4]), ids_r, w_r, cfg.H, cfg.I, wgu_bits=host["wgu"],
                                  wd_bits=host["wd"])
