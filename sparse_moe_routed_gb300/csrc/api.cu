@@ -112,7 +112,7 @@ moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* b
     e = moe::launch_grouped_gemm(moe::GemmKind::kRouter, MOE_W_BF16, w_router, nullptr, x, nullptr, 1, T, H, 0, E,
                                  logits, nullptr, st);
   else
-    e = moe::launch_router_logits_simt(x, w_router, T, H, E, logits, st);
+    e = moe::launch_router_logits_small(x, w_router, T, H, E, logits, st);
   if (e != cudaSuccess) return MOE_ECUDA;
   return cuda_status(moe::launch_topk(logits, bias, T, E, k, topk_ids, topk_w, gap, st));
 }

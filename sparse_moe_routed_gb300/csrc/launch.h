@@ -35,11 +35,32 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// launch_pdl for a grid of thread-block clusters of the given shape.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, dim3 cluster, size_t smem,
+                               cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster.x;
+  attr[1].val.clusterDim.y = cluster.y;
+  attr[1].val.clusterDim.z = cluster.z;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // route.cu
-cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* wr, int T, int H, int E,
-                                      float* logits, cudaStream_t st);
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
-                        float* w, float* gap, cudaStream_t st);
+cudaError_t launch_router_logits_small(const uint16_t* x, const uint16_t* wr, int T, int H, int E, float* logits,
+                                       cudaStream_t st);
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids, float* w,
+                        float* gap, cudaStream_t st);
 
 // permute.cu
 cudaError_t launch_permute(const int32_t* ids, int R, int k, int E, int32_t* counts,

@@ -7,115 +7,156 @@
 // order are the label, so selection is exact on the fp32 logits with a fixed
 // tie rule (lower expert ID first), not on rounded probabilities.
 //
-// Small token counts (decode blocks) use CUDA cores: two warps per expert row,
-// all router-row loads in flight at once, the block's token rows staged once
-// in shared memory.  Large token counts use the tcgen05 grouped kernel in its
-// dense router mode (gemm.cu).  Selection is one warp per token: each lane
-// keeps ceil(E/32) logits in registers and k+1 rounds of warp-wide max/min
-// reductions pick the route and the next logit (for the decision gap).
+// Small token counts (decode blocks) use warp-level MMA on the tensor cores
+// with a K split over the warps of a CTA; large token counts use the tcgen05
+// grouped kernel in its dense router mode (gemm.cu).  Selection is one warp
+// per token: each lane keeps ceil(E/32) logits in registers, sorted once, and
+// k+1 rounds of warp-wide reductions pick the route and the next logit (for
+// the decision gap).
 #include <math.h>
 
 #include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace moe {
 
 namespace {
 
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+// Small-T logits on the tensor cores with warp-level MMA (m16n8k16, bf16 in,
+// fp32 accumulate).  A cluster of four CTAs covers 16 tokens x 8 experts;
+// CTA r of the cluster takes the r-th quarter of K and divides it among its
+// 8 warps, each of which chains its MMAs in ascending K.  The CTA sums its
+// warps' tiles in warp order in shared memory, and CTA 0 of the cluster adds
+// the four CTA tiles in rank order over distributed shared memory, so every
+// logit is summed in one fixed order on every call.  The router rows are
+// constant: their fragments are loaded before the wait on the upstream
+// kernel; the token fragments come straight from global memory.  At decode
+// sizes the contraction is ~42 MFLOP over 256 CTAs: the latency of a global
+// round trip, not MMA throughput, sets its time.
+constexpr int kLogitThreads = 256;
+constexpr int kLogitWarps = kLogitThreads / 32;
+constexpr int kLogitTok = 16;    // tokens per CTA (MMA M)
+constexpr int kLogitExp = 8;     // experts per CTA (MMA N)
+constexpr int kLogitSplit = 4;   // CTAs per cluster, one K quarter each
+constexpr int kLogitChunk = 8;   // k16 steps per register batch
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// One CTA = 8 warps = 4 experts x 2 halves of K.  The router rows are
-// constant, so each lane issues all of its (up to 8 x 16-byte) weight loads
-// before waiting on the upstream kernel; the token tile is then staged once
-// in shared memory and every lane runs TT dot products over its K range.
-constexpr int kLogitThreads = 256;
-constexpr int kLogitExperts = 4;
-constexpr int kWChunk = 8;  // 16-byte weight vectors a lane keeps in flight
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
 
-template <int TT>
-__global__ void __launch_bounds__(kLogitThreads) router_logits_simt_kernel(const uint16_t* __restrict__ x,
-                                                                           const uint16_t* __restrict__ wr,
-                                                                           int T, int H, int E,
-                                                                           float* __restrict__ logits) {
-  extern __shared__ uint4 xs[];  // [TT][H/8]
-  __shared__ float part[kLogitExperts][TT];
-  const int vpr = H / 8;
-  const int hv = vpr / 2;  // 16-byte vectors per K half
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Load of the same shared-memory word in CTA `rank` of the cluster (volatile
+// so that it stays between the cluster barriers; loads issued back to back
+// are still in flight together).
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ptx::smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kLogitThreads) router_logits_mma_kernel(const uint16_t* __restrict__ x,
+                                                                          const uint16_t* __restrict__ wr, int T,
+                                                                          int H, int E, float* __restrict__ logits) {
+  __shared__ float red[kLogitWarps][kLogitTok][kLogitExp];
+  __shared__ float tile[kLogitTok][kLogitExp];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kLogitExperts + (warp >> 1);
-  const int half = warp & 1;
-  const int t0 = blockIdx.y * TT;
-  const int nt = min(TT, T - t0);
-  const bool active = e < E;
-  const uint4* wrow = reinterpret_cast<const uint4*>(wr + static_cast<size_t>(active ? e : 0) * H) + half * hv;
+  const int g = lane >> 2;  // fragment row group
+  const int q = lane & 3;   // thread in group
+  const uint32_t rank = cluster_ctarank();
+  const int e0 = blockIdx.x * kLogitExp;
+  const int t0 = blockIdx.y * kLogitTok;
+  // k16 steps of this warp: worker rank * 8 + warp of 32
+  const int steps_all = H / 16;
+  constexpr int kWorkers = kLogitSplit * kLogitWarps;
+  const int per = (steps_all + kWorkers - 1) / kWorkers;
+  const int s_begin = min(steps_all, (static_cast<int>(rank) * kLogitWarps + warp) * per);
+  const int steps = min(steps_all, s_begin + per) - s_begin;
+  const int kbase = s_begin * 16;
+  // B fragment: expert e0 + g, K pairs (q*2, q*2+1) and (q*2+8, q*2+9)
+  const bool e_ok = e0 + g < E;
+  const uint32_t* wrow = reinterpret_cast<const uint32_t*>(wr + static_cast<size_t>(e_ok ? e0 + g : 0) * H + kbase);
+  // A fragment rows: tokens t0 + g and t0 + g + 8
+  const bool ta = t0 + g < T, tb = t0 + g + 8 < T;
+  const uint32_t* xa = reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(ta ? t0 + g : 0) * H + kbase);
+  const uint32_t* xb = reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(tb ? t0 + g + 8 : 0) * H + kbase);
 
-  uint4 wv[kWChunk];
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t bw[kLogitChunk][2];
 #pragma unroll
-  for (int j = 0; j < kWChunk; ++j) {
-    const int c = lane + 32 * j;
-    wv[j] = (active && c < hv) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+  for (int s = 0; s < kLogitChunk; ++s) {
+    const bool in = e_ok && s < steps;
+    bw[s][0] = in ? __ldg(wrow + s * 8 + q) : 0u;
+    bw[s][1] = in ? __ldg(wrow + s * 8 + 4 + q) : 0u;
   }
-
   pdl_wait();
   pdl_trigger();
-  for (int idx = threadIdx.x; idx < TT * vpr; idx += kLogitThreads) {
-    const int r = idx / vpr;
-    const int c = idx - r * vpr;
-    xs[idx] = (r < nt) ? reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + r) * H)[c]
-                       : make_uint4(0, 0, 0, 0);
-  }
-  __syncthreads();
-
-  float acc[TT];
-#pragma unroll
-  for (int t = 0; t < TT; ++t) acc[t] = 0.f;
-  for (int c0 = 0; c0 < hv; c0 += 32 * kWChunk) {
+  for (int c0 = 0; c0 < steps; c0 += kLogitChunk) {
     if (c0 > 0) {
 #pragma unroll
-      for (int j = 0; j < kWChunk; ++j) {
-        const int c = c0 + lane + 32 * j;
-        wv[j] = (active && c < hv) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+      for (int s = 0; s < kLogitChunk; ++s) {
+        const bool in = e_ok && c0 + s < steps;
+        bw[s][0] = in ? __ldg(wrow + (c0 + s) * 8 + q) : 0u;
+        bw[s][1] = in ? __ldg(wrow + (c0 + s) * 8 + 4 + q) : 0u;
       }
     }
+    uint32_t af[kLogitChunk][4];
 #pragma unroll
-    for (int j = 0; j < kWChunk; ++j) {
-      const int c = c0 + lane + 32 * j;
-      if (c < hv) {
-        float wf[8];
-        unpack8(wv[j], wf);
-#pragma unroll
-        for (int t = 0; t < TT; ++t) {
-          float xf[8];
-          unpack8(xs[t * vpr + half * hv + c], xf);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
-        }
-      }
+    for (int s = 0; s < kLogitChunk; ++s) {
+      const bool in = c0 + s < steps;
+      const int o = (c0 + s) * 8 + q;
+      af[s][0] = (in && ta) ? xa[o] : 0u;
+      af[s][1] = (in && tb) ? xb[o] : 0u;
+      af[s][2] = (in && ta) ? xa[o + 4] : 0u;
+      af[s][3] = (in && tb) ? xb[o + 4] : 0u;
     }
+#pragma unroll
+    for (int s = 0; s < kLogitChunk; ++s)
+      if (c0 + s < steps) mma_bf16_16816(acc, af[s], bw[s]);
   }
-#pragma unroll
-  for (int t = 0; t < TT; ++t) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
-  }
-  float mine = 0.f;
-#pragma unroll
-  for (int t = 0; t < TT; ++t)
-    if (lane == t) mine = acc[t];
-  if (half == 1 && lane < TT) part[warp >> 1][lane] = mine;
+  red[warp][g][2 * q] = acc[0];
+  red[warp][g][2 * q + 1] = acc[1];
+  red[warp][g + 8][2 * q] = acc[2];
+  red[warp][g + 8][2 * q + 1] = acc[3];
   __syncthreads();
-  if (half == 0 && active && lane < nt)
-    logits[static_cast<size_t>(t0 + lane) * E + e] = mine + part[warp >> 1][lane];
+  const int t = threadIdx.x / kLogitExp;
+  const int e = threadIdx.x % kLogitExp;
+  if (threadIdx.x < kLogitTok * kLogitExp) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kLogitWarps; ++w) sum += red[w][t][e];
+    tile[t][e] = sum;
+  }
+  cluster_sync_all();  // every CTA's tile is complete and visible to the cluster
+  if (rank == 0 && threadIdx.x < kLogitTok * kLogitExp) {
+    float part[kLogitSplit];
+    part[0] = tile[t][e];
+#pragma unroll
+    for (int r = 1; r < kLogitSplit; ++r) part[r] = ld_cluster_f32(&tile[t][e], r);
+    float sum = part[0];
+#pragma unroll
+    for (int r = 1; r < kLogitSplit; ++r) sum += part[r];
+    if (t0 + t < T && e0 + e < E) logits[static_cast<size_t>(t0 + t) * E + e0 + e] = sum;
+  }
+  cluster_sync_all();  // keep every tile alive until CTA 0 has read it
 }
 
 // Order-preserving map of a float to an unsigned key (NaN mapped to -inf by
@@ -130,66 +171,131 @@ __device__ __forceinline__ float key2f(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// One warp per token.  Lane l holds the logits of experts l, l+32, ...; each
-// round one __reduce_max_sync finds the largest remaining logit and one
-// __reduce_min_sync the lowest expert ID holding it; only the winning lane
-// rescans its own EPL values.
+// Descending bitonic sort of N (a power of two) values held in registers.
+template <int N>
+__device__ __forceinline__ void sort_desc(uint64_t (&v)[N]) {
+#pragma unroll
+  for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint64_t a = v[i], b = v[l];
+          const bool swap = ((i & k) == 0) ? (a < b) : (a > b);
+          v[i] = swap ? b : a;
+          v[l] = swap ? a : b;
+        }
+      }
+    }
+  }
+}
+
+// Descending bitonic sort of one value per lane across the warp (lane r ends
+// with the r-th largest).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
+      v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  }
+  return v;
+}
+
+// One warp per token.  Lane l holds the logits of experts l, l+32, ... as
+// 64-bit keys (order key of the logit, then the bitwise complement of the
+// expert ID), so the largest key is the largest logit and, among equal
+// logits, the lowest expert ID; every key is distinct.  Let n = min(k+1, E)
+// (the k routes and the next logit, for the decision gap).  The n-th largest
+// of the 32 lane maxima is a threshold that at least n keys reach (those
+// lanes' maxima), so the n largest keys are all at or above it.  The keys at
+// or above it -- rarely more than a few beyond n -- are compacted and sorted
+// across the warp in one bitonic pass, and lane r then holds rank r.  If
+// more than 32 keys reach the threshold (or n > 32), each lane sorts its own
+// keys and n rounds of warp-wide max reductions take the largest head.
 template <int EPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                                                    int T, int E, int k, int32_t* __restrict__ ids,
                                                    float* __restrict__ w, float* __restrict__ gap) {
+  __shared__ uint64_t cand[8][32];
   pdl_wait();
   pdl_trigger();
+  const int warp = threadIdx.x >> 5;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  uint32_t key[EPL];
-  uint32_t taken = 0;
+  // all loads first, then the keys
+  float lv[EPL], bv[EPL];
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int e = j * 32 + lane;
+    lv[j] = e < E ? logits[static_cast<size_t>(t) * E + e] : 0.f;
+    bv[j] = (bias && e < E) ? bias[e] : 0.f;
+  }
+  uint64_t v[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const int e = j * 32 + lane;
+    v[j] = 0;  // below every valid key (f2key(-inf) > 0)
     if (e < E) {
-      float l = logits[static_cast<size_t>(t) * E + e];
-      if (bias) l += bias[e];
+      float l = lv[j];
+      if (bias) l += bv[j];
       if (isnan(l)) l = -INFINITY;
       if (l == 0.0f) l = 0.0f;
-      key[j] = f2key(l);
-    } else {
-      key[j] = 0u;
-      taken |= 1u << j;
+      v[j] = (static_cast<uint64_t>(f2key(l)) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
     }
   }
-  auto local_best = [&](uint32_t& bk, int& be) {
-    bk = 0u;
-    be = 0x7fffffff;
+  const int n = min(k + 1, E);
+  uint64_t mine = 0;  // lane r: the key of rank r (r < n)
+  bool done = false;
+  if (n <= 32) {
+    uint64_t m = v[0];
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-      if (!((taken >> j) & 1u) && (be == 0x7fffffff || key[j] > bk)) {
-        bk = key[j];
-        be = j * 32 + lane;
-      }
+    for (int j = 1; j < EPL; ++j) m = v[j] > m ? v[j] : m;
+    const uint64_t thr = __shfl_sync(0xffffffffu, warp_sort_desc(m, lane), n - 1);
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) c += v[j] >= thr ? 1 : 0;
+    int incl = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
     }
-  };
-  uint32_t bk;
-  int be;
-  local_best(bk, be);
-  uint32_t my_key = 0u, next_key = 0u;
-  int my_e = 0;
-  const int rounds = min(k + 1, E);
-  for (int r = 0; r < rounds; ++r) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-    const int cand = (be != 0x7fffffff && bk == m) ? be : 0x7fffffff;
-    const int emin = __reduce_min_sync(0xffffffffu, cand);
-    if ((emin & 31) == lane) {
-      taken |= 1u << (emin >> 5);
-      local_best(bk, be);
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total <= 32) {
+      int pos = incl - c;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (v[j] >= thr) cand[warp][pos++] = v[j];
+      __syncwarp();
+      mine = warp_sort_desc(lane < total ? cand[warp][lane] : 0, lane);
+      done = true;
     }
-    if (r < k && lane == r) {
-      my_key = m;
-      my_e = emin;
-    }
-    if (r == k) next_key = m;
   }
+  if (!done) {
+    sort_desc<EPL>(v);
+    for (int r = 0; r < n; ++r) {
+      const uint32_t hi = static_cast<uint32_t>(v[0] >> 32);
+      const uint32_t lo = static_cast<uint32_t>(v[0]);
+      const uint32_t m_hi = __reduce_max_sync(0xffffffffu, hi);
+      const uint32_t m_lo = __reduce_max_sync(0xffffffffu, hi == m_hi ? lo : 0u);
+      if (hi == m_hi && lo == m_lo) {
+#pragma unroll
+        for (int j = 0; j + 1 < EPL; ++j) v[j] = v[j + 1];
+        v[EPL - 1] = 0;
+      }
+      if (lane == r) mine = (static_cast<uint64_t>(m_hi) << 32) | m_lo;
+    }
+  }
+  const uint32_t my_key = static_cast<uint32_t>(mine >> 32);
+  const int my_e = static_cast<int>(~static_cast<uint32_t>(mine));
+  const uint32_t next_key = static_cast<uint32_t>(__shfl_sync(0xffffffffu, mine, k & 31) >> 32);
   const float my_v = key2f(my_key);
   const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
   const float ex = (lane < k) ? expf(my_v - v0) : 0.f;
@@ -213,23 +319,11 @@ cudaError_t run_topk(const float* logits, const float* bias, int T, int E, int k
 
 }  // namespace
 
-cudaError_t launch_router_logits_simt(const uint16_t* x, const uint16_t* wr, int T, int H, int E, float* logits,
-                                      cudaStream_t st) {
-  const dim3 grid((E + kLogitExperts - 1) / kLogitExperts, 1);
-  if (H <= 6144) {
-    constexpr int TT = 16;
-    const size_t smem = static_cast<size_t>(TT) * H * 2;
-    cudaError_t e = ensure_smem(router_logits_simt_kernel<TT>, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    return launch_pdl(router_logits_simt_kernel<TT>, dim3(grid.x, (T + TT - 1) / TT), dim3(kLogitThreads), smem,
-                      st, x, wr, T, H, E, logits);
-  }
-  constexpr int TT = 8;
-  const size_t smem = static_cast<size_t>(TT) * H * 2;
-  cudaError_t e = ensure_smem(router_logits_simt_kernel<TT>, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  return launch_pdl(router_logits_simt_kernel<TT>, dim3(grid.x, (T + TT - 1) / TT), dim3(kLogitThreads), smem, st,
-                    x, wr, T, H, E, logits);
+cudaError_t launch_router_logits_small(const uint16_t* x, const uint16_t* wr, int T, int H, int E, float* logits,
+                                       cudaStream_t st) {
+  const dim3 grid((E + kLogitExp - 1) / kLogitExp, (T + kLogitTok - 1) / kLogitTok, kLogitSplit);
+  return launch_pdl_cluster(router_logits_mma_kernel, grid, dim3(kLogitThreads), dim3(1, 1, kLogitSplit), 0, st, x,
+                            wr, T, H, E, logits);
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids, float* w,
@@ -304,7 +398,7 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, const uint16_t* w_rou
   float* logits = noalloc_scratch_for_current_device();
   if (!logits) return MOE_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (moe::launch_router_logits_simt(x, w_router, T, H, E, logits, st) != cudaSuccess) return MOE_ECUDA;
+  if (moe::launch_router_logits_small(x, w_router, T, H, E, logits, st) != cudaSuccess) return MOE_ECUDA;
   if (moe::launch_topk(logits, bias, T, E, k, topk_ids, topk_w, gap, st) != cudaSuccess) return MOE_ECUDA;
   return MOE_OK;
 }
