@@ -567,18 +567,25 @@ def run_stack(args, rank, world, local, dev):
     gu = [g0[j].elapsed_time(g1[j]) for j in range(KE)]
     gu_avg = sum(gu) / KE
     R = T * cfg.k
+    # decode-sized blocks (routes <= 320, K <= 2560) run on the CUDA-core int4 kernel
+    cuda_core_int4 = R <= 320 and cfg.H <= 2560
     gu_bytes = sum((Ul[(j * EV) % L] * (2 * cfg.I * cfg.H // 2 + 2 * cfg.I * cfg.H // 64 * 2) + R * cfg.H * 2 +
                     R * cfg.I * 2) for j in range(KE)) / KE
     step_ms = total_ms / K
     line = {"metric": METRIC, "value": T * K * world / (total_ms / 1e3), "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int4 g64 experts (bf16 tensor-core operands), bf16 router, fp32 residual",
+            "vs_baseline": None,
+            "dtype": ("int4 g64 experts (dequantised to fp32 in registers, fp32 FMA), bf16 router, fp32 residual"
+                      if cuda_core_int4 else
+                      "int4 g64 experts (bf16 tensor-core operands), bf16 router, fp32 residual"),
             "data": "synthetic (seeded)",
             "config": {"workload": f"stack48_int4g64_L{L}_T{T}_blocks{NB}", "layers": L, "T": T, "blocks": NB,
                        "unique_experts_per_layer_block0": Ul,
                        "l2": f"inputs larger than L2: {L} layers of int4 experts "
                              f"({L * (cfg.E * rec_bytes + router_bytes) / 1e9:.1f} GB) streamed per block"},
-            "roofline": {"bound": "hbm", "kernel": "grouped_gemm_kernel int4 (moe_expert_gateup)",
+            "roofline": {"bound": "hbm",
+                         "kernel": "gemv_q4_kernel (moe_expert_gateup, CUDA cores)" if cuda_core_int4 else
+                                   "grouped_gemm_q4_kernel (moe_expert_gateup, tcgen05)",
                          "achieved": gu_bytes / (gu_avg / 1e3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": gu_bytes / (gu_avg / 1e3) / 1e9 / pk["hbm_gbs"], "traffic": None,
                          "bytes_per_launch": gu_bytes, "avg_launch_us": gu_avg * 1e3},

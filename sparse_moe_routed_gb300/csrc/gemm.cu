@@ -94,18 +94,30 @@ struct CfgB {
 // once.
 template <int NMAX>
 struct CfgQ {
-  static constexpr int kDqWarps = NMAX <= 64 ? 8 : 4;
+  // The dequantised operand never touches shared memory: dequantiser warps
+  // write it to tensor memory (tcgen05.st) and the MMA reads A from there.
+  // TMEM lane quarters bind warps to rows: warp w may access lanes
+  // 32 (w % 4) .. +31, so dequantiser warps come in groups of four (one per
+  // quarter) and the groups take turns over the K steps.  Shared memory
+  // holds only the packed chunk ring (which covers HBM latency) and the
+  // token-row ring.
+  static constexpr int kDqGroups = 2;
+  static constexpr int kDqWarps = 4 * kDqGroups;
   static constexpr int kDqWarp0 = 7;  // warp 6 produces token rows
   static constexpr int kThreads = 32 * (kDqWarp0 + kDqWarps);
   static constexpr int kBBytes = NMAX * kBK * 2;
-  static constexpr int SA = kDqWarps;
-  static constexpr int SQmax = NMAX <= 16 ? 16 : 8;  // ring capacity in single-step chunks
+  static constexpr int kTmemCols = 512;               // accumulators first, then the operand ring
+  static constexpr int kTmemA = 2 * NMAX < 32 ? 32 : 2 * NMAX;
+  static constexpr int SA = (kTmemCols - kTmemA) / 32 > 12 ? 12 : (kTmemCols - kTmemA) / 32;  // 32 columns each
+  // token rows: one small stage per K step, so a deep ring for small NMAX
+  static constexpr int SB = NMAX <= 16 ? 24 : (NMAX <= 32 ? 12 : (NMAX <= 64 ? 6 : 4));
+  static constexpr int SQmax = NMAX <= 16 ? 32 : (NMAX <= 32 ? 24 : (NMAX <= 64 ? 24 : 16));  // chunks
   static constexpr int kQRingBytes = SQmax * kQChunk;
-  static constexpr int SB = NMAX <= 32 ? 8 : (NMAX <= 64 ? 6 : 4);
-  static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
   static constexpr int kNumBars = 2 * (SQmax + SA + SB) + 5;
-  static constexpr int kSmemBytes = 1024 + SA * kABytes + SB * kBBytes + kQRingBytes + kNumBars * 8 + kSmemTail;
+  static constexpr int kSmemBytes = 1024 + SB * kBBytes + kQRingBytes + kNumBars * 8 + kSmemTail;
   static_assert(kBBytes % 1024 == 0, "B stage must keep 1024-byte alignment");
+  static_assert(2 * NMAX <= kTmemA, "accumulators below the operand ring");
+  static_assert(kTmemA + SA * 32 <= kTmemCols, "operand ring inside the allocation");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -118,6 +130,7 @@ struct GemmArgs {
   int seg_rows;            // weight rows per segment in the A map (down: H)
   const uint8_t* tiles;    // tile-packed weights (bulk-copy modes), chunk per (e, mb, ks)
   int qgroup;              // int4: K steps per bulk copy (divides ksteps)
+  const uint16_t* brows;   // int4 GEMV: the token rows [R][K] bf16 (staged per tile by bulk copies)
   void* out;
   int ldo;                 // leading dimension of out (elements)
   int32_t* status;
@@ -150,7 +163,6 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 }
 
 constexpr uint32_t kSpin = 0;         // producer / MMA threads
-constexpr uint32_t kSleepQuant = 32;  // dequantiser warps
 constexpr uint32_t kSleepEpi = 256;   // epilogue warps (one wait per tile)
 
 // Drain wait used during teardown after an abort: ignores the abort flag.
@@ -162,9 +174,6 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // One packed 32-bit word of eight int4 g64 codes -> eight bf16 (16 bytes).
 // The packer stores each code offset by +8 and orders a word's nibbles as
@@ -979,23 +988,25 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
 }
 
 // ============================================================== int4 kernel
-template <int NMAX, int KIND>
+// QG (packed chunks per bulk copy) is a template parameter so that the ring
+// positions of a K step are shifts and masks, not divisions: the per-step
+// bookkeeping runs once per 4.3 KB of weights and must stay cheap.
+template <int NMAX, int KIND, int QG>
 __global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
     grouped_gemm_q4_kernel(const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
   using C = CfgQ<NMAX>;
   constexpr int SA = C::SA, SB = C::SB;
-  const int QG = p.qgroup;
-  const int SQ = C::SQmax / QG;  // logical slots of QG chunks each
+  constexpr int SQ = C::SQmax / QG;  // logical slots of QG chunks each
+  static_assert(C::SQmax % QG == 0, "ring holds whole groups");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = base;               // [SA][16 KB] dequantised operand tiles (swizzled)
-  uint8_t* sB = sA + SA * kABytes;  // [SB][NMAX x 128 B] token rows (swizzled)
+  uint8_t* sB = base;                  // [SB][NMAX x 128 B] token rows (swizzled)
   uint8_t* sQ = sB + SB * C::kBBytes;  // [SQ][QG x 4,352 B] packed codes + scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(sQ + C::kQRingBytes);
   const uint32_t qfull0 = ptx::smem_u32(bars);      // packed chunks landed
   const uint32_t qempty0 = qfull0 + 8 * C::SQmax;   // dequantisers done reading them
-  const uint32_t afull0 = qempty0 + 8 * C::SQmax;   // operand tile written
-  const uint32_t aempty0 = afull0 + 8 * SA;     // MMA done with the tile
+  const uint32_t afull0 = qempty0 + 8 * C::SQmax;   // operand slot written (TMEM)
+  const uint32_t aempty0 = afull0 + 8 * SA;     // MMA done with the slot
   const uint32_t bfull0 = aempty0 + 8 * SA;     // token rows landed
   const uint32_t bempty0 = bfull0 + 8 * SB;     // MMA done with the rows
   const uint32_t accf0 = bempty0 + 8 * SB;
@@ -1012,10 +1023,10 @@ __global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < SQ; ++s) {
       ptx::mbar_init(qfull0 + 8 * s, 1);
-      ptx::mbar_init(qempty0 + 8 * s, QG);
+      ptx::mbar_init(qempty0 + 8 * s, QG * 4);  // each chunk is read by the four warps of one group
     }
     for (int s = 0; s < SA; ++s) {
-      ptx::mbar_init(afull0 + 8 * s, 1);
+      ptx::mbar_init(afull0 + 8 * s, 4);
       ptx::mbar_init(aempty0 + 8 * s, 1);
     }
     for (int s = 0; s < SB; ++s) {
@@ -1109,7 +1120,12 @@ __global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        issue_k_step(d_tmem, ptx::smem_u32(sA + sa * kABytes), ptx::smem_u32(sB + sb * C::kBBytes), idesc, ks);
+        const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(C::kTmemA + sa * 32);
+        const uint32_t b0 = ptx::smem_u32(sB + sb * C::kBBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBK / kUK; ++kk)
+          ptx::umma_bf16_ts(d_tmem, a_tmem + static_cast<uint32_t>(kk * kUK / 2), ptx::sdesc_k_sw128(b0 + kk * kUK * 2),
+                            idesc, (ks | kk) != 0 ? 1u : 0u);
         issued = true;
         ptx::umma_commit(aempty0 + 8 * sa);
         ptx::umma_commit(bempty0 + 8 * sb);
@@ -1137,62 +1153,75 @@ __global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
     epilogue_role<NMAX, KIND>(p, sc, total, tmem_base, accf0, acce0, misc + 1);
   } else if (warp >= C::kDqWarp0) {
     // ------------------------------------------------------------ dequantisers
-    // Warp w takes K steps g = w, w + SA, w + 2 SA, ... of this CTA's stream
-    // and always writes operand slot w.  Each lane handles rows lane,
-    // lane + 32, lane + 64, lane + 96: it reads their codes and scales, frees
-    // the packed chunk, then writes 4 x 8 swizzled 16-byte pieces.
+    // Group j of four warps takes K steps g = j, j + kDqGroups, ... of this
+    // CTA's stream; lane l of the group's warp for lane quarter q converts
+    // row 32 q + l (64 inputs) into 32 TMEM columns of operand slot g % SA.
+    // A warp's TMEM store of one step completes while it loads and converts
+    // its next step; only then does it mark the slot full.  Each warp frees
+    // the packed chunk as soon as its codes are read.
     const int dw = warp - C::kDqWarp0;
+    const int grp = dw / 4;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(C::kTmemA);
     uint32_t g = 0;  // this CTA's running K-step index
     bool ok = true;
+    int pending = -1;  // slot whose store is in flight
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       for (int ks = 0; ks < p.ksteps; ++ks, ++g) {
-        if (static_cast<int>(g % SA) != dw) continue;
+        if (static_cast<int>(g % C::kDqGroups) != grp) continue;
         const uint32_t gg = g / QG;  // ring group (QG consecutive K steps)
         const uint32_t sq = gg % SQ;
         const uint32_t phq = (gg / SQ) & 1u;
+        const uint32_t sa = g % SA;
         const uint32_t pha = (g / SA) & 1u;
-        bool got = wait_bounded<kSleepQuant>(qfull0 + 8 * sq, phq, misc + 1, p.status);
+        bool got = wait_bounded<kSpin>(qfull0 + 8 * sq, phq, misc + 1, p.status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         const uint8_t* chunk = sQ + (sq * QG + (g - gg * QG)) * kQChunk;
-        uint4 pk[4][2];
-        uint16_t sbits[4];
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          const int row = lane + 32 * rr;
-          pk[rr][0] = reinterpret_cast<const uint4*>(chunk + row * 32)[0];
-          pk[rr][1] = reinterpret_cast<const uint4*>(chunk + row * 32)[1];
-          sbits[rr] = reinterpret_cast<const uint16_t*>(chunk + kQBytes)[row];
-        }
+        const uint4 qa = reinterpret_cast<const uint4*>(chunk + row * 32)[0];
+        const uint4 qb = reinterpret_cast<const uint4*>(chunk + row * 32)[1];
+        const uint16_t sbits = reinterpret_cast<const uint16_t*>(chunk + kQBytes)[row];
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(qempty0 + 8 * sq);
-        got = wait_bounded<kSleepQuant>(aempty0 + 8 * dw, pha ^ 1u, misc + 1, p.status);
+        __nv_bfloat16 scv;
+        std::memcpy(&scv, &sbits, 2);
+        const __nv_bfloat162 sc2 = __halves2bfloat162(scv, scv);
+        uint32_t cols[32];
+        const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const uint4 d = dequant8(words[w], sc2);  // inputs 8w .. 8w + 7 as four bf16 pairs
+          cols[4 * w] = d.x;
+          cols[4 * w + 1] = d.y;
+          cols[4 * w + 2] = d.z;
+          cols[4 * w + 3] = d.w;
+        }
+        if (pending >= 0) {  // the previous step's columns are in TMEM: publish them
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(afull0 + 8 * pending);
+          pending = -1;
+        }
+        got = wait_bounded<kSpin>(aempty0 + 8 * sa, pha ^ 1u, misc + 1, p.status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        uint8_t* atile = sA + dw * kABytes;
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          const int row = lane + 32 * rr;
-          __nv_bfloat16 scv;
-          std::memcpy(&scv, &sbits[rr], 2);
-          const __nv_bfloat162 sc2 = __halves2bfloat162(scv, scv);
-          uint8_t* arow = atile + row * 128;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t words[4] = {pk[rr][half].x, pk[rr][half].y, pk[rr][half].z, pk[rr][half].w};
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-              *reinterpret_cast<uint4*>(arow + (((4 * half + w) ^ (row & 7)) * 16)) = dequant8(words[w], sc2);
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(afull0 + 8 * dw);
+        ptx::tc_fence_after();
+        ptx::tmem_st32(lane_base + sa * 32, cols);
+        pending = static_cast<int>(sa);
       }
+    }
+    ptx::tmem_wait_st();
+    if (pending >= 0 && ok) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(afull0 + 8 * pending);
     }
   }
 
@@ -1202,6 +1231,300 @@ __global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
+}
+
+// ============================================================ int4 GEMV
+// Decode-sized int4 tiles on the CUDA cores.  With about one token row per
+// expert, a tile is a matrix-vector product: each weight is used once or
+// twice, so expanding the codes into a 16 KB bf16 operand per K step for the
+// tensor core costs more on-chip traffic than the 4.3 KB the step moves from
+// HBM.  Here the codes are turned into fp32 pairs in registers and used at
+// once by packed fp32x2 FMAs.
+//
+// Warps: 0 streams packed chunks (bulk copies, deep ring), 1 stages each
+// tile's token rows (one bulk copy per row, double-buffered), the rest
+// compute.  The compute warps form kGvGroups groups of four that take K steps
+// in turn (more warps in flight hide the latency of each step); in a group,
+// thread t owns the row pair (r, r + 16) -- a gate row and its up row -- for
+// one half of the step's 64 inputs.  Per K step and token row a thread forms
+// the group-64 partial sums of its two rows from the unscaled codes
+// (code - 8, exact) and adds scale x partial to its accumulators.  At the end
+// of a tile the partial sets (groups x halves) meet in shared memory and are
+// added in a fixed order, so results are the same on every call.
+constexpr int kGvRows = 4;                     // token rows per tile
+constexpr int kGvGroups = 3;                   // compute groups of four warps, alternating K steps
+constexpr int kGvWarps = 2 + 4 * kGvGroups;
+constexpr int kGvThreads = 32 * kGvWarps;
+constexpr int kGvMaxK = 2560;                  // inputs per row the token-row stage holds
+
+struct CfgV {
+  static constexpr int SQmax = 32;  // packed chunks in flight
+  static constexpr int kXBytes = kGvRows * kGvMaxK * 2;  // one tile's token rows: 20 KB
+  static constexpr int kParts = 2 * kGvGroups;           // partial sets: groups x K halves
+  static constexpr int kRedFloats = kParts * kBM * kGvRows;
+  static constexpr int kNumBars = 2 * SQmax + 8;
+  static constexpr int kSmemBytes =
+      1024 + SQmax * kQChunk + 2 * kXBytes + 2 * kRedFloats * 4 + kNumBars * 8 + kSmemTail;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// bf16 pair (lower element in the low half) -> fp32 pair (lower in .x)
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t u) {
+  return static_cast<uint64_t>(u << 16) | (static_cast<uint64_t>(u & 0xffff0000u) << 32);
+}
+
+// Codes of inputs 2p, 2p+1 of a packed word -> fp32 pair (code - 8), exact.
+__device__ __forceinline__ uint64_t code_pair_f32x2(uint32_t word, int p) {
+  const uint32_t bits = ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;  // bf16 128 + code
+  __nv_bfloat162 b;
+  std::memcpy(&b, &bits, 4);
+  const __nv_bfloat162 v = __hsub2(b, __floats2bfloat162_rn(136.0f, 136.0f));
+  uint32_t u;
+  std::memcpy(&u, &v, 4);
+  return bf16x2_to_f32x2(u);
+}
+
+__device__ __forceinline__ float f32x2_sum(uint64_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v)) + __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+
+template <int KIND, int QG>
+__global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
+  using C = CfgV;
+  constexpr int SQ = C::SQmax / QG;  // ring slots of QG chunks each
+  static_assert(C::SQmax % QG == 0, "ring holds whole groups");
+  const int K = p.ksteps * kBK;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;                                  // [SQ][QG x 4,352 B] packed codes + scales
+  uint8_t* sX = sQ + C::SQmax * kQChunk;               // [2][8 rows][K] bf16 token rows of a tile
+  float* sRed = reinterpret_cast<float*>(sX + 2 * C::kXBytes);  // [2][parts][128][rows]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRed + 2 * C::kRedFloats);
+  const uint32_t qfull0 = ptx::smem_u32(bars);
+  const uint32_t qempty0 = qfull0 + 8 * C::SQmax;
+  const uint32_t xfull0 = qempty0 + 8 * C::SQmax;  // token rows of a tile staged (2 buffers)
+  const uint32_t xempty0 = xfull0 + 16;            // every compute warp done with them
+  const uint32_t redf0 = xempty0 + 16;             // partial sums written (2 buffers)
+  const uint32_t rede0 = redf0 + 16;               // partial sums consumed (2 buffers)
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
+  int* prefix = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
+  int* soff = prefix + (kMaxE + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SQ; ++s) {
+      ptx::mbar_init(qfull0 + 8 * s, 1);
+      ptx::mbar_init(qempty0 + 8 * s, QG * 4);  // each chunk is read by the four warps of one group
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(xfull0 + 8 * b, 1);
+      ptx::mbar_init(xempty0 + 8 * b, 4 * kGvGroups);
+      ptx::mbar_init(redf0 + 8 * b, 4 * kGvGroups);  // every compute warp
+      ptx::mbar_init(rede0 + 8 * b, 2);  // the two summing warps
+    }
+    misc[1] = 0;
+    ptx::fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_trigger();
+  const int total = build_schedule<kGvRows>(p, false, E, prefix, soff);
+  const Sched sc{prefix, soff, E, p.mblocks, kGvRows};
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ packed chunk producer
+    const uint64_t pol = ptx::policy_evict_first();
+    uint32_t armed_mask = 0, armed_ph = 0;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = sc.tile(t);
+      for (int ks = 0; ks < p.ksteps; ks += QG) {
+        if (!wait_bounded<kSpin>(qempty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = qfull0 + 8 * s;
+        armed_mask |= 1u << s;
+        armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+        ptx::mbar_arrive_expect_tx(fb, QG * kQChunk);
+        const size_t chunk = (static_cast<size_t>(tl.e) * p.mblocks + tl.mb) * p.ksteps + ks;
+        ptx::bulk_load(ptx::smem_u32(sQ + s * QG * kQChunk), p.tiles + chunk * kQChunk, QG * kQChunk, fb, pol);
+        if (++s == SQ) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (!ok || misc[1]) {
+      for (int q = 0; q < SQ; ++q)
+        if ((armed_mask >> q) & 1u) wait_drain(qfull0 + 8 * q, (armed_ph >> q) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ token-row producer
+    const uint64_t pol = ptx::policy_evict_last();
+    uint32_t armed_mask = 0, armed_ph = 0;
+    bool ok = true;
+    int ntile = 0;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++ntile) {
+      const Tile tl = sc.tile(t);
+      const int b = ntile & 1;
+      const uint32_t use = static_cast<uint32_t>(ntile >> 1) & 1u;
+      if (!wait_bounded<kSpin>(xempty0 + 8 * b, use ^ 1u, misc + 1, p.status)) {
+        ok = false;
+        break;
+      }
+      const int n = min(tl.nrows, kGvRows);
+      const uint32_t fb = xfull0 + 8 * b;
+      armed_mask |= 1u << b;
+      armed_ph = (armed_ph & ~(1u << b)) | (use << b);
+      ptx::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(n * K * 2));
+      for (int j = 0; j < n; ++j)
+        ptx::bulk_load(ptx::smem_u32(sX + b * C::kXBytes + j * K * 2), p.brows + static_cast<size_t>(tl.row0 + j) * K,
+                       static_cast<uint32_t>(K * 2), fb, pol);
+    }
+    if (!ok || misc[1]) {
+      for (int q = 0; q < 2; ++q)
+        if ((armed_mask >> q) & 1u) wait_drain(xfull0 + 8 * q, (armed_ph >> q) & 1u);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------- compute
+    const int cw = warp - 2;
+    const int grp = cw / 4;                 // takes the K steps g with g % kGvGroups == grp
+    const int tt = (cw % 4) * 32 + lane;    // 0..127 within the group
+    const int khalf = tt / 64;              // inputs 32 khalf .. +31 of each step
+    const int pi = tt % 64;
+    const int q = pi / 16, i = pi % 16;
+    const int r0 = q * 32 + i, r1 = r0 + 16;  // gate row and its up row (down: two output rows)
+    const int part = grp * 2 + khalf;
+    const bool summer = (grp == 0 && khalf == 0);  // warps 2 and 3 finish each tile
+    uint32_t g = 0;   // running K step of this CTA
+    int ntile = 0;    // tiles finished by this CTA
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++ntile) {
+      const Tile tl = sc.tile(t);
+      const int b = ntile & 1;
+      const uint32_t use = static_cast<uint32_t>(ntile >> 1) & 1u;
+      bool got = wait_bounded<kSpin>(xfull0 + 8 * b, use, misc + 1, p.status);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* xs = sX + b * C::kXBytes;
+      uint64_t acc0[kGvRows], acc1[kGvRows];
+#pragma unroll
+      for (int j = 0; j < kGvRows; ++j) acc0[j] = acc1[j] = 0;
+      for (int ks = 0; ks < p.ksteps; ++ks, ++g) {
+        if (static_cast<int>(g % kGvGroups) != grp) continue;
+        const uint32_t gg = g / QG;
+        const uint32_t sq = gg % SQ;
+        const uint32_t phq = (gg / SQ) & 1u;
+        got = wait_bounded<kSpin>(qfull0 + 8 * sq, phq, misc + 1, p.status);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* chunk = sQ + (sq * QG + (g - gg * QG)) * kQChunk;
+        const uint4 c0 = reinterpret_cast<const uint4*>(chunk + r0 * 32)[khalf];
+        const uint4 c1 = reinterpret_cast<const uint4*>(chunk + r1 * 32)[khalf];
+        const uint16_t* scl = reinterpret_cast<const uint16_t*>(chunk + kQBytes);
+        const float s0 = bf16_to_f32(scl[r0]), s1 = bf16_to_f32(scl[r1]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(qempty0 + 8 * sq);
+        uint64_t w0[16], w1[16];
+        const uint32_t wd0[4] = {c0.x, c0.y, c0.z, c0.w};
+        const uint32_t wd1[4] = {c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            w0[4 * w + pp] = code_pair_f32x2(wd0[w], pp);
+            w1[4 * w + pp] = code_pair_f32x2(wd1[w], pp);
+          }
+        }
+        const uint64_t s0x2 = static_cast<uint64_t>(__float_as_uint(s0)) * 0x100000001ull;
+        const uint64_t s1x2 = static_cast<uint64_t>(__float_as_uint(s1)) * 0x100000001ull;
+        const uint8_t* xk = xs + (ks * kBK + khalf * 32) * 2;
+#pragma unroll
+        for (int j = 0; j < kGvRows; ++j) {
+          if (j >= tl.nrows) break;
+          uint32_t xw[16];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 xv = reinterpret_cast<const uint4*>(xk + j * K * 2)[v];
+            xw[4 * v] = xv.x;
+            xw[4 * v + 1] = xv.y;
+            xw[4 * v + 2] = xv.z;
+            xw[4 * v + 3] = xv.w;
+          }
+          uint64_t p0a = 0, p0b = 0, p1a = 0, p1b = 0;
+#pragma unroll
+          for (int m = 0; m < 16; m += 2) {
+            const uint64_t xa = bf16x2_to_f32x2(xw[m]), xb = bf16x2_to_f32x2(xw[m + 1]);
+            p0a = fma_f32x2(w0[m], xa, p0a);
+            p1a = fma_f32x2(w1[m], xa, p1a);
+            p0b = fma_f32x2(w0[m + 1], xb, p0b);
+            p1b = fma_f32x2(w1[m + 1], xb, p1b);
+          }
+          // acc += scale * (partial over this half of the group), pairwise
+          acc0[j] = fma_f32x2(s0x2, p0b, fma_f32x2(s0x2, p0a, acc0[j]));
+          acc1[j] = fma_f32x2(s1x2, p1b, fma_f32x2(s1x2, p1a, acc1[j]));
+        }
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(xempty0 + 8 * b);
+      // -------- tile end: the four partial sets meet in shared memory
+      got = wait_bounded<kSleepEpi>(rede0 + 8 * b, use ^ 1u, misc + 1, p.status);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      float* red = sRed + b * C::kRedFloats + part * (kBM * kGvRows);
+#pragma unroll
+      for (int j = 0; j < kGvRows; ++j) {
+        red[r0 * kGvRows + j] = f32x2_sum(acc0[j]);
+        red[r1 * kGvRows + j] = f32x2_sum(acc1[j]);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(redf0 + 8 * b);
+      if (summer) {
+        got = wait_bounded<kSpin>(redf0 + 8 * b, use, misc + 1, p.status);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const float* rb = sRed + b * C::kRedFloats;
+        for (int j = 0; j < tl.nrows && j < kGvRows; ++j) {
+          float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+          for (int pp = 0; pp < C::kParts; ++pp) {
+            v0 += rb[pp * (kBM * kGvRows) + r0 * kGvRows + j];
+            v1 += rb[pp * (kBM * kGvRows) + r1 * kGvRows + j];
+          }
+          const size_t orow = static_cast<size_t>(tl.row0 + j) * p.ldo;
+          if (KIND == 0) {
+            reinterpret_cast<uint16_t*>(p.out)[orow + tl.mb * 64 + q * 16 + i] = f32_to_bf16(v0 / (1.0f + expf(-v0)) * v1);
+          } else {
+            reinterpret_cast<float*>(p.out)[orow + tl.mb * kBM + r0] = v0;
+            reinterpret_cast<float*>(p.out)[orow + tl.mb * kBM + r1] = v1;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(rede0 + 8 * b);
+      }
+    }
+  }
+  __syncthreads();
 }
 
 // ------------------------------------------------------------------ host side
@@ -1291,10 +1614,10 @@ cudaError_t run_bf16(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs&
   return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, st, a, b, args);
 }
 
-template <int NMAX, int KIND>
-cudaError_t run_q4(const CUtensorMap& b, const GemmArgs& args, cudaStream_t st) {
+template <int NMAX, int KIND, int QG>
+cudaError_t run_q4_g(const CUtensorMap& b, const GemmArgs& args, cudaStream_t st) {
   using C = CfgQ<NMAX>;
-  auto kern = grouped_gemm_q4_kernel<NMAX, KIND>;
+  auto kern = grouped_gemm_q4_kernel<NMAX, KIND, QG>;
   cudaError_t e = ensure_smem(kern, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = sm_count();
@@ -1302,11 +1625,47 @@ cudaError_t run_q4(const CUtensorMap& b, const GemmArgs& args, cudaStream_t st) 
   return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, st, b, args);
 }
 
+template <int NMAX, int KIND>
+cudaError_t run_q4(const CUtensorMap& b, const GemmArgs& args, cudaStream_t st) {
+  return args.qgroup == 2 ? run_q4_g<NMAX, KIND, 2>(b, args, st) : run_q4_g<NMAX, KIND, 1>(b, args, st);
+}
+
+// Token rows per tile: small when experts see few rows (decode), so the
+// B operand and TMEM footprint stay small and the rings can run deeper.
+int pick_nmax(int rows_hint) {
+  if (rows_hint <= 320) return 16;
+  if (rows_hint <= 1280) return 32;
+  if (rows_hint <= 5120) return 64;
+  return 128;
+}
+
+template <int KIND, int QG>
+cudaError_t run_gemv_q4_g(const GemmArgs& args, cudaStream_t st) {
+  auto kern = gemv_q4_kernel<KIND, QG>;
+  cudaError_t e = ensure_smem(kern, CfgV::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = sm_count();
+  if (grid <= 0) return cudaErrorNoDevice;
+  return launch_pdl(kern, dim3(grid), dim3(kGvThreads), CfgV::kSmemBytes, st, args);
+}
+
+template <int KIND>
+cudaError_t run_gemv_q4(const GemmArgs& args, cudaStream_t st) {
+  return args.qgroup == 2 ? run_gemv_q4_g<KIND, 2>(args, st) : run_gemv_q4_g<KIND, 1>(args, st);
+}
+
+// Decode-sized int4 launches (few rows per expert, K within the token-row
+// stage) go to the CUDA-core kernel.
+bool use_gemv_q4(int fmt, int R, int K) {
+  return fmt == MOE_W_INT4_G64_TILED && pick_nmax(R) == 16 && K <= kGvMaxK;
+}
+
 template <int KIND>
 cudaError_t run_fmt(int fmt, int nmax, const CUtensorMap& a, const CUtensorMap& b, GemmArgs args,
                     cudaStream_t st) {
   if (fmt == MOE_W_INT4_G64_TILED) {
-    args.qgroup = args.ksteps % 4 == 0 ? 4 : (args.ksteps % 2 == 0 ? 2 : 1);
+    args.qgroup = args.ksteps % 2 == 0 ? 2 : 1;  // 8.7 KB bulk copies
+    if (KIND != 2 && use_gemv_q4(fmt, args.R, args.ksteps * kBK)) return run_gemv_q4<KIND>(args, st);
     switch (nmax) {
       case 16: return run_q4<16, KIND>(b, args, st);
       case 32: return run_q4<32, KIND>(b, args, st);
@@ -1338,14 +1697,6 @@ cudaError_t run_fmt(int fmt, int nmax, const CUtensorMap& a, const CUtensorMap& 
   }
 }
 
-// Token rows per tile: small when experts see few rows (decode), so the
-// B operand and TMEM footprint stay small and the rings can run deeper.
-int pick_nmax(int rows_hint) {
-  if (rows_hint <= 320) return 16;
-  if (rows_hint <= 1280) return 32;
-  if (rows_hint <= 5120) return 64;
-  return 128;
-}
 
 template <int NMAX, int GG>
 cudaError_t run_fused(const CUtensorMap& mx, const CUtensorMap& mh, const FusedArgs& args, cudaStream_t st) {
@@ -1415,6 +1766,7 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uin
   args.status = st_word;
   args.out = out;
   args.tiles = static_cast<const uint8_t*>(w);
+  args.brows = b_rows;
   args.qgroup = 1;
   const bool plain = (fmt == MOE_W_BF16);
   if (!plain && fmt != MOE_W_BF16_TILED && fmt != MOE_W_INT4_G64_TILED) return cudaErrorInvalidValue;
