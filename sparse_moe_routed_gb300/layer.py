@@ -169,6 +169,41 @@ class MoELayer:
         s.synchronize()
         return out_host
 
+    def forward_host_graph(self, x_host, out_host):
+        """forward_host replayed from a CUDA graph.
+
+        The host-to-device copy of x, the layer's launches and the copy of the
+        result back are captured once per (x_host, out_host) pair and then
+        replayed: one graph launch per call instead of seven API calls.  The
+        graph reads x_host and writes out_host by address, so the caller
+        refills the same pinned buffers between calls.  Returns after the
+        result is in out_host.
+        """
+        key = (x_host.data_ptr(), out_host.data_ptr(), x_host.shape[0])
+        graphs = self.__dict__.setdefault("_graphs", {})
+        graph = graphs.get(key)
+        if graph is None:
+            T = x_host.shape[0]
+            xd = self.x_dev_buf(T)
+            s = torch.cuda.Stream(device=xd.device)
+            s.wait_stream(torch.cuda.current_stream())
+
+            def body():
+                xd.copy_(x_host, non_blocking=True)
+                out = self.forward(xd, stream=s)
+                out_host.copy_(out, non_blocking=True)
+
+            with torch.cuda.stream(s):  # one eager pass: first-call set-up stays out of the capture
+                body()
+            s.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                body()
+            graphs[key] = graph
+        graph.replay()
+        torch.cuda.current_stream().synchronize()
+        return out_host
+
     def x_dev_buf(self, T):
         if not hasattr(self, "_xdev") or self._xdev.shape[0] < T:
             self._xdev = torch.empty((self.T_max, self.H), dtype=torch.bfloat16, device=self.w_router.device)

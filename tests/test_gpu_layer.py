@@ -315,6 +315,25 @@ def test_layer_deterministic():
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))
 
 
+def test_forward_host_graph_matches_eager():
+    """The graph-replayed host round trip gives the eager layer's bits, call
+    after call, with new inputs written into the same pinned buffer."""
+    cfg, d, _ = case("decode")
+    gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, cfg.E, cfg.H, cfg.I)
+    layer = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, cfg.T, fmt=_lib.MOE_W_BF16_TILED, I=cfg.I)
+    x_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    out_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    for i in range(3):
+        xi = wl.token_batch(cfg, DEV, index=40 + i)
+        ref = layer.forward(xi).clone()
+        torch.cuda.synchronize()
+        x_host.copy_(xi.cpu())
+        got = layer.forward_host_graph(x_host, out_host)
+        assert torch.equal(got.view(torch.int16), ref.cpu().view(torch.int16)), i
+    assert layer.read_status() == 0
+    assert int(layer.sync_ws.abs().sum().item()) == 0
+
+
 @pytest.mark.parametrize("tiled", [False, True])
 def test_layer_single_token_and_empty(tiled):
     cfg, d, host = case("tiny")
