@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--config", default="decode", choices=["decode", "prefill", "stack48", "sweep"])
     ap.add_argument("--layers", type=int, default=0, help="distinct layer weight sets rotated (0 = auto)")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (small profiling case)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the tokens per call of decode/prefill (e.g. 32768: the compute-bound regime)")
     ap.add_argument("--plain", action="store_true",
                     help="stream bf16 weights from the plain record layout through TMA tensor maps "
                          "instead of the tile-packed records")
@@ -256,6 +258,8 @@ def main():
     if args.experts:
         from dataclasses import replace
         cfg = replace(cfg, E=args.experts)
+    if args.tokens:
+        cfg = wl.with_tokens(cfg, args.tokens)
     NL = args.layers or (8 if args.config == "decode" else 1)
     layers, xs, host_w = [], [], None
     for l in range(NL):
@@ -383,6 +387,10 @@ def main():
     gu_bytes_avg = sum(main_bytes(U[(j * EV_EVERY) % NL]) for j in range(KE)) / KE
     layer_bytes_avg = sum(layer_bytes(u) for u in U_steps) / K
     achieved = gu_bytes_avg / (gu_avg / 1e3) / 1e9
+    # the dominant launch's dense FLOPs (padding rows excluded): gate/up, and
+    # down when the launch is fused
+    main_flops = 2 * R * 2 * I * H + (2 * R * H * I if fused else 0)
+    main_tflops = main_flops / (gu_avg / 1e3) / 1e12
     step_ms = total_ms / K
     flops_step = 2 * R * 3 * H * I + 2 * cfg.T * H * E
 
@@ -422,6 +430,26 @@ def main():
     wl_name = workload_name(cfg)
     U_ev = sum(U[(j * EV_EVERY) % NL] for j in range(KE)) / KE
     traffic = recorded_traffic("fused" if fused else "gateup", wl_name, U_ev)
+    main_kernel = ("grouped_swiglu_fused_kernel (moe_expert_swiglu_fused: " +
+                   ("row gather, " if gather_in_fused else "") + "gate/up + SwiGLU, down)"
+                   if fused else "grouped_gemm_kernel (moe_expert_gateup)")
+    roof_hbm = {"bound": "hbm", "kernel": main_kernel,
+                "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                "peak_source": pk["source"] + " hbm_gbs",
+                "bytes_per_launch": gu_bytes_avg, "avg_launch_us": gu_avg * 1e3, "timed_launches": KE}
+    # a launch of several ms inside the step: the sustained bf16 figure
+    roof_tensor = {"bound": "tensor", "kernel": main_kernel,
+                   "achieved": main_tflops, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                   "frac": main_tflops / pk["bf16_tflops_sustained"], "traffic": traffic,
+                   "peak_source": pk["source"] + " bf16_tflops_sustained",
+                   "flops_per_launch": main_flops, "avg_launch_us": gu_avg * 1e3, "timed_launches": KE}
+    # the bound is whichever the launch's arithmetic intensity puts it under
+    intensity = main_flops / gu_bytes_avg
+    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    roof_main, roof_other = (roof_tensor, roof_hbm) if intensity > ridge else (roof_hbm, roof_tensor)
+    roof_main["flop_per_byte"] = intensity
+    roof_main["ridge_flop_per_byte"] = ridge
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -433,15 +461,7 @@ def main():
                    "l2": f"inputs larger than L2: {NL} distinct layer weight sets rotated "
                          f"({NL * (E * 3 * H * I * 2 + router_bytes) / 1e9:.1f} GB)",
                    "parallelism": f"replicas x{world}", "unique_experts_per_step": U},
-        "roofline": {"bound": "hbm",
-                     "kernel": "grouped_swiglu_fused_kernel (moe_expert_swiglu_fused: "
-                               + ("row gather, " if gather_in_fused else "") + "gate/up + SwiGLU, down)"
-                     if fused else "grouped_gemm_kernel (moe_expert_gateup)",
-                     "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                     "peak_source": pk["source"] + " hbm_gbs",
-                     "bytes_per_launch": gu_bytes_avg, "avg_launch_us": gu_avg * 1e3,
-                     "timed_launches": KE},
+        "roofline": roof_main, "roofline_other": roof_other,
         "layer_roofline": {"bytes_per_step": layer_bytes_avg,
                            "achieved_gbs": layer_bytes_avg / (step_ms / 1e3) / 1e9,
                            "frac_hbm": layer_bytes_avg / (step_ms / 1e3) / 1e9 / pk["hbm_gbs"],
