@@ -112,6 +112,56 @@ def test_int4_expert_stage_tiny_geometry():
     assert_output_close(y.cpu().numpy(), ref, what="int4 expert outputs (tiny)")
 
 
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_int4_skewed_routes_split_tiles(name):
+    """Decode-sized int4 launches run on the CUDA-core kernel, which splits an
+    expert's rows into tiles of 4: routes skewed so that one expert gets 9
+    rows (three tiles), others 1-5, graded row by row against the oracle."""
+    cfg = wl.CONFIGS[name]
+    T, k, E = 16, cfg.k, cfg.E
+    d = wl.layer_inputs(cfg, DEV)
+    q_gu, s_gu = wl.quantize_int4_g64(d["w_gateup"])
+    q_d, s_d = wl.quantize_int4_g64(d["w_down"])
+    rng = np.random.default_rng(17)
+    ids_np = np.empty((T, k), np.int32)
+    for t in range(T):
+        pool = rng.permutation(np.arange(4, E))[:k].astype(np.int32)
+        if t < 9:
+            pool[0] = 1                       # expert 1: 9 rows
+        if t % 3 == 0:
+            pool[1] = 2                       # expert 2: 6 rows
+        if t in (4, 5, 6, 7, 8):
+            pool[2] = 3                       # expert 3: 5 rows
+        ids_np[t] = pool
+    assert all(len(set(r)) == k for r in ids_np)
+    R = T * k
+    assert R <= 320  # the CUDA-core path
+    _, offsets_r, perm_r, _ = oracle.permute(ids_np, E)
+    ids = torch.from_numpy(ids_np).to(DEV)
+    counts = torch.empty((E,), dtype=torch.int32, device=DEV)
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device=DEV)
+    perm = torch.empty((R,), dtype=torch.int32, device=DEV)
+    inv = torch.empty((R,), dtype=torch.int32, device=DEV)
+    x = wl.token_batch(cfg, DEV, index=23, T=T)
+    xp = torch.empty((R, cfg.H), dtype=torch.bfloat16, device=DEV)
+    h = torch.empty((R, cfg.I), dtype=torch.bfloat16, device=DEV)
+    y = torch.full((R, cfg.H), float("nan"), dtype=torch.float32, device=DEV)
+    st = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    _lib.moe_permute(ids, E, x, counts, offsets, perm, inv, xp, st)
+    gu, dn = pack_layer_experts(q_gu, q_d, _lib.MOE_W_INT4_G64, E, cfg.H, cfg.I, s_gateup=s_gu, s_down=s_d)
+    _lib.moe_grouped_swiglu(xp, offsets, E, cfg.H, cfg.I, gu, dn, h, y, st, fmt=_lib.MOE_W_INT4_G64_TILED)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert int(counts[1].item()) == 9 and int(counts[2].item()) == 6 and int(counts[3].item()) == 5
+    xin = oracle.bits_to_f32(oracle.bf16_bits(x))
+    seg_e = np.searchsorted(offsets_r, np.arange(R), side="right") - 1
+    tok = perm_r // k
+    ref = oracle.experts_combine(xin[tok], seg_e.reshape(R, 1).astype(np.int32), np.ones((R, 1), np.float32),
+                                 cfg.H, cfg.I, wgu_q=q_gu.cpu().numpy(), sgu_bits=oracle.bf16_bits(s_gu),
+                                 wd_q=q_d.cpu().numpy(), sd_bits=oracle.bf16_bits(s_d))
+    assert_output_close(y.cpu().numpy(), ref, what=f"int4 expert outputs, skewed routes ({name})")
+
+
 def test_int4_stack_forced_routes_six_layers():
     """Six layers free-running with the oracle's routes imposed on the GPU:
     the residual streams must agree to the stated tolerance."""
