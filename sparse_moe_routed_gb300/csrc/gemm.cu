@@ -1234,64 +1234,63 @@ __global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
 }
 
 // ============================================================ int4 GEMV
-// Decode-sized int4 tiles on the CUDA cores.  With about one token row per
-// expert, a tile is a matrix-vector product: each weight is used once or
-// twice, so expanding the codes into a 16 KB bf16 operand per K step for the
-// tensor core costs more on-chip traffic than the 4.3 KB the step moves from
-// HBM.  Here the codes are turned into fp32 pairs in registers and used at
-// once by packed fp32x2 FMAs.
+// Decode-sized int4 tiles.  With about one token row per expert a tile is a
+// matrix-vector product, and what limits it is instructions per weight, not
+// MMA throughput: a tcgen05 MMA must read its operands from shared or tensor
+// memory, so the codes of each K step would be expanded into a 16 KB bf16
+// tile and read back (measured: ~0.35 us per 4.3 KB step), while a CUDA-core
+// dot product spends ~6 instructions per weight.  Here the weights go from
+// registers straight into warp-level MMAs (mma.sync m16n8k16, bf16 in, fp32
+// accumulate): each code pair becomes an exact bf16 pair (code - 8) in three
+// instructions, token values enter as bf16 with no conversion, and one MMA
+// instruction consumes 256 weights against up to 8 token rows.
 //
 // Warps: 0 streams packed chunks (bulk copies, deep ring), 1 stages each
 // tile's token rows (one bulk copy per row, double-buffered), the rest
-// compute.  The compute warps form kGvGroups groups of four that take K steps
-// in turn (more warps in flight hide the latency of each step); in a group,
-// thread t owns the row pair (r, r + 16) -- a gate row and its up row -- for
-// one half of the step's 64 inputs.  Per K step and token row a thread forms
-// the group-64 partial sums of its two rows from the unscaled codes
-// (code - 8, exact) and adds scale x partial to its accumulators.  At the end
-// of a tile the partial sets (groups x halves) meet in shared memory and are
-// added in a fixed order, so results are the same on every call.
+// compute in kGvGroups groups of eight.  The groups take K steps in turn, so
+// each warp has several steps' time for the latency chain of one (wait,
+// loads, dequantise, four dependent MMAs).  Warp w of a group owns tile rows
+// 16w .. 16w + 15: per K step (one scale group of 64 inputs) it runs four
+// MMAs from zero and adds scale x partial to its fp32 accumulators.  At the
+// end of a tile groups 1.. hand their sums to group 0 through shared memory,
+// which adds them in group order (a fixed order: same bits every call); down
+// tiles are then stored from group 0's registers, and for gate/up tiles its
+// up-row warps hand their values to its gate-row warps for SwiGLU.
 constexpr int kGvRows = 4;                     // token rows per tile
-constexpr int kGvGroups = 3;                   // compute groups of four warps, alternating K steps
-constexpr int kGvWarps = 2 + 4 * kGvGroups;
+constexpr int kGvN = 8;                        // MMA N: token columns (those past kGvRows are zero)
+constexpr int kGvGroups = 3;
+constexpr int kGvWarps = 2 + 8 * kGvGroups;
 constexpr int kGvThreads = 32 * kGvWarps;
 constexpr int kGvMaxK = 2560;                  // inputs per row the token-row stage holds
 
 struct CfgV {
-  static constexpr int SQmax = 32;  // packed chunks in flight
+  static constexpr int SQmax = 36;  // packed chunks in flight
   static constexpr int kXBytes = kGvRows * kGvMaxK * 2;  // one tile's token rows: 20 KB
-  static constexpr int kParts = 2 * kGvGroups;           // partial sets: groups x K halves
-  static constexpr int kRedFloats = kParts * kBM * kGvRows;
-  static constexpr int kNumBars = 2 * SQmax + 8;
-  static constexpr int kSmemBytes =
-      1024 + SQmax * kQChunk + 2 * kXBytes + 2 * kRedFloats * 4 + kNumBars * 8 + kSmemTail;
+  static constexpr int kUpFloats = 4 * 16 * kGvN;     // up rows of a gate/up tile: [4][16][8]
+  static constexpr int kRedFloats = (kGvGroups - 1) * kBM * kGvN;  // other groups' sums: [G-1][128][8]
+  static constexpr int kNumBars = 2 * SQmax + 12;
+  static constexpr int kSmemBytes = 1024 + SQmax * kQChunk + 2 * kXBytes + 2 * kUpFloats * 4 +
+                                    2 * kRedFloats * 4 + kNumBars * 8 + kSmemTail;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// bf16 pair (lower element in the low half) -> fp32 pair (lower in .x)
-__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t u) {
-  return static_cast<uint64_t>(u << 16) | (static_cast<uint64_t>(u & 0xffff0000u) << 32);
-}
-
-// Codes of inputs 2p, 2p+1 of a packed word -> fp32 pair (code - 8), exact.
-__device__ __forceinline__ uint64_t code_pair_f32x2(uint32_t word, int p) {
+// Codes of inputs 2p, 2p+1 of a packed word -> bf16 pair (code - 8), exact.
+__device__ __forceinline__ uint32_t code_pair_bf16x2(uint32_t word, int p) {
   const uint32_t bits = ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;  // bf16 128 + code
   __nv_bfloat162 b;
   std::memcpy(&b, &bits, 4);
   const __nv_bfloat162 v = __hsub2(b, __floats2bfloat162_rn(136.0f, 136.0f));
   uint32_t u;
   std::memcpy(&u, &v, 4);
-  return bf16x2_to_f32x2(u);
-}
-
-__device__ __forceinline__ float f32x2_sum(uint64_t v) {
-  return __uint_as_float(static_cast<uint32_t>(v)) + __uint_as_float(static_cast<uint32_t>(v >> 32));
+  return u;
 }
 
 template <int KIND, int QG>
@@ -1304,14 +1303,17 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;                                  // [SQ][QG x 4,352 B] packed codes + scales
   uint8_t* sX = sQ + C::SQmax * kQChunk;               // [2][8 rows][K] bf16 token rows of a tile
-  float* sRed = reinterpret_cast<float*>(sX + 2 * C::kXBytes);  // [2][parts][128][rows]
+  float* sUp = reinterpret_cast<float*>(sX + 2 * C::kXBytes);  // [2][4][16][8] up rows (gate/up tiles)
+  float* sRed = sUp + 2 * C::kUpFloats;                          // [2][G-1][128][8] other groups' sums
   uint64_t* bars = reinterpret_cast<uint64_t*>(sRed + 2 * C::kRedFloats);
   const uint32_t qfull0 = ptx::smem_u32(bars);
   const uint32_t qempty0 = qfull0 + 8 * C::SQmax;
   const uint32_t xfull0 = qempty0 + 8 * C::SQmax;  // token rows of a tile staged (2 buffers)
   const uint32_t xempty0 = xfull0 + 16;            // every compute warp done with them
-  const uint32_t redf0 = xempty0 + 16;             // partial sums written (2 buffers)
-  const uint32_t rede0 = redf0 + 16;               // partial sums consumed (2 buffers)
+  const uint32_t upf0 = xempty0 + 16;              // up rows written (2 buffers)
+  const uint32_t upe0 = upf0 + 16;                 // up rows consumed (2 buffers)
+  const uint32_t redf0 = upe0 + 16;                // other groups' sums written (2 buffers)
+  const uint32_t rede0 = redf0 + 16;               // group 0 done with them (2 buffers)
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
   int* prefix = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
   int* soff = prefix + (kMaxE + 1);
@@ -1323,13 +1325,15 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < SQ; ++s) {
       ptx::mbar_init(qfull0 + 8 * s, 1);
-      ptx::mbar_init(qempty0 + 8 * s, QG * 4);  // each chunk is read by the four warps of one group
+      ptx::mbar_init(qempty0 + 8 * s, QG * 8);  // every chunk is read by the eight warps of one group
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(xfull0 + 8 * b, 1);
-      ptx::mbar_init(xempty0 + 8 * b, 4 * kGvGroups);
-      ptx::mbar_init(redf0 + 8 * b, 4 * kGvGroups);  // every compute warp
-      ptx::mbar_init(rede0 + 8 * b, 2);  // the two summing warps
+      ptx::mbar_init(xempty0 + 8 * b, 8 * kGvGroups);
+      ptx::mbar_init(upf0 + 8 * b, 4);  // group 0's four up-row warps
+      ptx::mbar_init(upe0 + 8 * b, 4);  // group 0's four gate-row warps
+      ptx::mbar_init(redf0 + 8 * b, 8 * (kGvGroups - 1));
+      ptx::mbar_init(rede0 + 8 * b, 8);
     }
     misc[1] = 0;
     ptx::fence_mbar_init();
@@ -1398,17 +1402,13 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------- compute
-    const int cw = warp - 2;
-    const int grp = cw / 4;                 // takes the K steps g with g % kGvGroups == grp
-    const int tt = (cw % 4) * 32 + lane;    // 0..127 within the group
-    const int khalf = tt / 64;              // inputs 32 khalf .. +31 of each step
-    const int pi = tt % 64;
-    const int q = pi / 16, i = pi % 16;
-    const int r0 = q * 32 + i, r1 = r0 + 16;  // gate row and its up row (down: two output rows)
-    const int part = grp * 2 + khalf;
-    const bool summer = (grp == 0 && khalf == 0);  // warps 2 and 3 finish each tile
-    uint32_t g = 0;   // running K step of this CTA
-    int ntile = 0;    // tiles finished by this CTA
+    const int grp = (warp - 2) / 8;    // takes the K steps g with g % kGvGroups == grp
+    const int cw = (warp - 2) % 8;     // owns tile rows 16 cw .. 16 cw + 15
+    const int g = lane >> 2;           // MMA fragment row group / token column
+    const int q = lane & 3;            // thread in group
+    const int ra = 16 * cw + g, rb = ra + 8;
+    uint32_t gk = 0;   // running K step of this CTA
+    int ntile = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++ntile) {
       const Tile tl = sc.tile(t);
@@ -1419,13 +1419,13 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
         ok = false;
         break;
       }
-      const uint8_t* xs = sX + b * C::kXBytes;
-      uint64_t acc0[kGvRows], acc1[kGvRows];
-#pragma unroll
-      for (int j = 0; j < kGvRows; ++j) acc0[j] = acc1[j] = 0;
-      for (int ks = 0; ks < p.ksteps; ++ks, ++g) {
-        if (static_cast<int>(g % kGvGroups) != grp) continue;
-        const uint32_t gg = g / QG;
+      // B fragments read token row g of the stage (zero past the tile's rows)
+      const bool tok_ok = g < tl.nrows;
+      const uint32_t* xrow = reinterpret_cast<const uint32_t*>(sX + b * C::kXBytes + (tok_ok ? g : 0) * K * 2);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int ks = 0; ks < p.ksteps; ++ks, ++gk) {
+        if (static_cast<int>(gk % kGvGroups) != grp) continue;
+        const uint32_t gg = gk / QG;
         const uint32_t sq = gg % SQ;
         const uint32_t phq = (gg / SQ) & 1u;
         got = wait_bounded<kSpin>(qfull0 + 8 * sq, phq, misc + 1, p.status);
@@ -1433,94 +1433,122 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
           ok = false;
           break;
         }
-        const uint8_t* chunk = sQ + (sq * QG + (g - gg * QG)) * kQChunk;
-        const uint4 c0 = reinterpret_cast<const uint4*>(chunk + r0 * 32)[khalf];
-        const uint4 c1 = reinterpret_cast<const uint4*>(chunk + r1 * 32)[khalf];
+        const uint8_t* chunk = sQ + (sq * QG + (gk - gg * QG)) * kQChunk;
+        const uint4 ca0 = reinterpret_cast<const uint4*>(chunk + ra * 32)[0];
+        const uint4 ca1 = reinterpret_cast<const uint4*>(chunk + ra * 32)[1];
+        const uint4 cb0 = reinterpret_cast<const uint4*>(chunk + rb * 32)[0];
+        const uint4 cb1 = reinterpret_cast<const uint4*>(chunk + rb * 32)[1];
         const uint16_t* scl = reinterpret_cast<const uint16_t*>(chunk + kQBytes);
-        const float s0 = bf16_to_f32(scl[r0]), s1 = bf16_to_f32(scl[r1]);
+        const float sa = bf16_to_f32(scl[ra]), sb = bf16_to_f32(scl[rb]);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(qempty0 + 8 * sq);
-        uint64_t w0[16], w1[16];
-        const uint32_t wd0[4] = {c0.x, c0.y, c0.z, c0.w};
-        const uint32_t wd1[4] = {c1.x, c1.y, c1.z, c1.w};
+        const uint32_t wa[8] = {ca0.x, ca0.y, ca0.z, ca0.w, ca1.x, ca1.y, ca1.z, ca1.w};
+        const uint32_t wb[8] = {cb0.x, cb0.y, cb0.z, cb0.w, cb1.x, cb1.y, cb1.z, cb1.w};
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-#pragma unroll
-          for (int pp = 0; pp < 4; ++pp) {
-            w0[4 * w + pp] = code_pair_f32x2(wd0[w], pp);
-            w1[4 * w + pp] = code_pair_f32x2(wd1[w], pp);
-          }
+        for (int j = 0; j < 4; ++j) {  // k16 block j: inputs 16 j .. 16 j + 15 of the step
+          uint32_t a[4];
+          a[0] = code_pair_bf16x2(wa[2 * j], q);      // row ra, inputs 16j + 2q, +1
+          a[1] = code_pair_bf16x2(wb[2 * j], q);      // row rb
+          a[2] = code_pair_bf16x2(wa[2 * j + 1], q);  // row ra, inputs 16j + 8 + 2q, +1
+          a[3] = code_pair_bf16x2(wb[2 * j + 1], q);  // row rb
+          const int kx = (ks * kBK + 16 * j + 2 * q) >> 1;  // 32-bit word of the token row
+          const uint32_t b0 = tok_ok ? xrow[kx] : 0u;
+          const uint32_t b1 = tok_ok ? xrow[kx + 4] : 0u;
+          mma_16816_bf16(d, a, b0, b1);
         }
-        const uint64_t s0x2 = static_cast<uint64_t>(__float_as_uint(s0)) * 0x100000001ull;
-        const uint64_t s1x2 = static_cast<uint64_t>(__float_as_uint(s1)) * 0x100000001ull;
-        const uint8_t* xk = xs + (ks * kBK + khalf * 32) * 2;
-#pragma unroll
-        for (int j = 0; j < kGvRows; ++j) {
-          if (j >= tl.nrows) break;
-          uint32_t xw[16];
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint4 xv = reinterpret_cast<const uint4*>(xk + j * K * 2)[v];
-            xw[4 * v] = xv.x;
-            xw[4 * v + 1] = xv.y;
-            xw[4 * v + 2] = xv.z;
-            xw[4 * v + 3] = xv.w;
-          }
-          uint64_t p0a = 0, p0b = 0, p1a = 0, p1b = 0;
-#pragma unroll
-          for (int m = 0; m < 16; m += 2) {
-            const uint64_t xa = bf16x2_to_f32x2(xw[m]), xb = bf16x2_to_f32x2(xw[m + 1]);
-            p0a = fma_f32x2(w0[m], xa, p0a);
-            p1a = fma_f32x2(w1[m], xa, p1a);
-            p0b = fma_f32x2(w0[m + 1], xb, p0b);
-            p1b = fma_f32x2(w1[m + 1], xb, p1b);
-          }
-          // acc += scale * (partial over this half of the group), pairwise
-          acc0[j] = fma_f32x2(s0x2, p0b, fma_f32x2(s0x2, p0a, acc0[j]));
-          acc1[j] = fma_f32x2(s1x2, p1b, fma_f32x2(s1x2, p1a, acc1[j]));
-        }
+        acc[0] = fmaf(sa, d[0], acc[0]);  // row ra, token 2q
+        acc[1] = fmaf(sa, d[1], acc[1]);  // row ra, token 2q + 1
+        acc[2] = fmaf(sb, d[2], acc[2]);  // row rb, token 2q
+        acc[3] = fmaf(sb, d[3], acc[3]);  // row rb, token 2q + 1
       }
       if (!ok) break;
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(xempty0 + 8 * b);
-      // -------- tile end: the four partial sets meet in shared memory
-      got = wait_bounded<kSleepEpi>(rede0 + 8 * b, use ^ 1u, misc + 1, p.status);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      float* red = sRed + b * C::kRedFloats + part * (kBM * kGvRows);
-#pragma unroll
-      for (int j = 0; j < kGvRows; ++j) {
-        red[r0 * kGvRows + j] = f32x2_sum(acc0[j]);
-        red[r1 * kGvRows + j] = f32x2_sum(acc1[j]);
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(redf0 + 8 * b);
-      if (summer) {
-        got = wait_bounded<kSpin>(redf0 + 8 * b, use, misc + 1, p.status);
+      // groups 1.. hand their sums to group 0, which adds them in group order
+      if (grp > 0) {
+        got = wait_bounded<kSleepEpi>(rede0 + 8 * b, use ^ 1u, misc + 1, p.status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        const float* rb = sRed + b * C::kRedFloats;
-        for (int j = 0; j < tl.nrows && j < kGvRows; ++j) {
-          float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-          for (int pp = 0; pp < C::kParts; ++pp) {
-            v0 += rb[pp * (kBM * kGvRows) + r0 * kGvRows + j];
-            v1 += rb[pp * (kBM * kGvRows) + r1 * kGvRows + j];
-          }
-          const size_t orow = static_cast<size_t>(tl.row0 + j) * p.ldo;
-          if (KIND == 0) {
-            reinterpret_cast<uint16_t*>(p.out)[orow + tl.mb * 64 + q * 16 + i] = f32_to_bf16(v0 / (1.0f + expf(-v0)) * v1);
-          } else {
-            reinterpret_cast<float*>(p.out)[orow + tl.mb * kBM + r0] = v0;
-            reinterpret_cast<float*>(p.out)[orow + tl.mb * kBM + r1] = v1;
-          }
-        }
+        float* red = sRed + b * C::kRedFloats + (grp - 1) * (kBM * kGvN);
+        red[ra * kGvN + 2 * q] = acc[0];
+        red[ra * kGvN + 2 * q + 1] = acc[1];
+        red[rb * kGvN + 2 * q] = acc[2];
+        red[rb * kGvN + 2 * q + 1] = acc[3];
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(rede0 + 8 * b);
+        if (lane == 0) ptx::mbar_arrive(redf0 + 8 * b);
+        continue;
+      }
+      got = wait_bounded<kSpin>(redf0 + 8 * b, use, misc + 1, p.status);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int gi = 0; gi < kGvGroups - 1; ++gi) {
+        const float* red = sRed + b * C::kRedFloats + gi * (kBM * kGvN);
+        acc[0] += red[ra * kGvN + 2 * q];
+        acc[1] += red[ra * kGvN + 2 * q + 1];
+        acc[2] += red[rb * kGvN + 2 * q];
+        acc[3] += red[rb * kGvN + 2 * q + 1];
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(rede0 + 8 * b);
+      const int t0 = 2 * q, t1 = 2 * q + 1;
+      if (KIND == 1) {
+        float* y = reinterpret_cast<float*>(p.out);
+        const int col = tl.mb * kBM;
+        if (t0 < tl.nrows) {
+          y[static_cast<size_t>(tl.row0 + t0) * p.ldo + col + ra] = acc[0];
+          y[static_cast<size_t>(tl.row0 + t0) * p.ldo + col + rb] = acc[2];
+        }
+        if (t1 < tl.nrows) {
+          y[static_cast<size_t>(tl.row0 + t1) * p.ldo + col + ra] = acc[1];
+          y[static_cast<size_t>(tl.row0 + t1) * p.ldo + col + rb] = acc[3];
+        }
+        continue;
+      }
+      // gate/up tile: rows 32m .. 32m + 15 are gate (warp 2m), 32m + 16 .. + 31
+      // up (warp 2m + 1); the up warp hands its values to the gate warp
+      const int m = cw >> 1;
+      float* up = sUp + b * C::kUpFloats + m * (16 * kGvN);
+      if (cw & 1) {
+        got = wait_bounded<kSleepEpi>(upe0 + 8 * b, use ^ 1u, misc + 1, p.status);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        up[g * kGvN + t0] = acc[0];
+        up[g * kGvN + t1] = acc[1];
+        up[(g + 8) * kGvN + t0] = acc[2];
+        up[(g + 8) * kGvN + t1] = acc[3];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(upf0 + 8 * b);
+      } else {
+        got = wait_bounded<kSpin>(upf0 + 8 * b, use, misc + 1, p.status);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        uint16_t* h = reinterpret_cast<uint16_t*>(p.out);
+        // gate row 32m + r (r = g or g + 8) pairs with up row 32m + 16 + r: h index 16m + r
+        const int colA = tl.mb * 64 + 16 * m + g, colB = colA + 8;
+        const float uA0 = up[g * kGvN + t0], uA1 = up[g * kGvN + t1];
+        const float uB0 = up[(g + 8) * kGvN + t0], uB1 = up[(g + 8) * kGvN + t1];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(upe0 + 8 * b);
+        if (t0 < tl.nrows) {
+          const size_t o = static_cast<size_t>(tl.row0 + t0) * p.ldo;
+          h[o + colA] = f32_to_bf16(acc[0] / (1.0f + expf(-acc[0])) * uA0);
+          h[o + colB] = f32_to_bf16(acc[2] / (1.0f + expf(-acc[2])) * uB0);
+        }
+        if (t1 < tl.nrows) {
+          const size_t o = static_cast<size_t>(tl.row0 + t1) * p.ldo;
+          h[o + colA] = f32_to_bf16(acc[1] / (1.0f + expf(-acc[1])) * uA1);
+          h[o + colB] = f32_to_bf16(acc[3] / (1.0f + expf(-acc[3])) * uB1);
+        }
       }
     }
   }
