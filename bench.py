@@ -335,6 +335,11 @@ def main():
     bound = [layers[l].bound_calls(xs[l], cfg.T, stream=st) for l in range(NL)]
     names = [c[0] for c in bound[0]]
     fused = "moe_expert_swiglu_fused" in names
+    # kernels each boundary call launches in this configuration
+    per_call = {"moe_route": 2, "moe_route_permute": 1, "moe_permute": 1 if R <= MoELayer.GATHER_IN_FUSED_MAX_ROWS
+                and fused else 2, "moe_permute_gather": 2, "moe_expert_swiglu_fused": 1, "moe_expert_gateup": 1,
+                "moe_expert_down": 1, "moe_combine": 1}
+    launches_per_step = sum(per_call[n] for n in names)
     gather_in_fused = fused and R <= MoELayer.GATHER_IN_FUSED_MAX_ROWS
     # the dominant kernel(s): the fused contraction, or gate/up then down
     i_main = names.index("moe_expert_swiglu_fused" if fused else "moe_expert_gateup")
@@ -473,7 +478,7 @@ def main():
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         # route: logits + selection; permute (+ row gather unless the fused
         # launch gathers); experts (fused: one launch; else gate/up, down, combine)
-        "gpu_launches": (5 if gather_in_fused else 6 if fused else 7) * K,
+        "gpu_launches": launches_per_step * K,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

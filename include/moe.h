@@ -149,6 +149,27 @@ MOE_API moe_status moe_permute(const int32_t *topk_ids, int T, int k, int E, con
                        uint16_t *x_perm, int32_t *dev_status, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_route_permute -- moe_route followed by moe_permute (without the row
+ * gather) for a decode block of T <= 16 tokens, in one launch.
+ *
+ * Sources: as moe_route and moe_permute.  Outputs: topk_ids, topk_w, gap as
+ * moe_route; counts, offsets, perm, inv_perm as moe_permute.  The selection
+ * rule and the grouping are the same; the logits are summed in a different
+ * (fixed) order than moe_route's, so a route whose 10th and 11th logits are
+ * within rounding of each other may differ between the two entry points.
+ * Runs as one 16-CTA thread-block cluster; returns MOE_ENOTSUP for T > 16 or
+ * on a device that cannot run such a cluster (use moe_route + moe_permute).
+ * On GB300 it is slower than moe_route + moe_permute issued back to back with
+ * programmatic launch (16 SMs pull the whole router matrix); it serves callers
+ * that want a single launch.
+ * No workspace.  dev_status (required) gets MOE_DEV_BAD_EXPERT as moe_permute.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_route_permute(const uint16_t *x, const uint16_t *w_router, const float *bias, int T, int H,
+                                     int E, int k, int32_t *topk_ids, float *topk_w, float *gap, int32_t *counts,
+                                     int32_t *offsets, int32_t *perm, int32_t *inv_perm, int32_t *dev_status,
+                                     void *stream);
+
+/* ---------------------------------------------------------------------------
  * Expert contractions (tensor cores: tcgen05 MMA, TMEM accumulators, TMA).
  *
  * Source: AFN-019, section "Why overlap alone cannot defeat the byte roofline"

@@ -61,6 +61,7 @@ def load(path: str | None = None):
             "moe_expert_down": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
             "moe_grouped_swiglu": ([p, p, i, i, i, i, i, p, p, p, p, p, p, p, p], i),
             "moe_expert_swiglu_fused": ([p, i, p, p, p, i, i, i, i, i, p, p, p, p, p, p, p], i),
+            "moe_route_permute": ([p, p, p, i, i, i, i, p, p, p, p, p, p, p, p, p], i),
             "moe_combine": ([p, p, p, i, i, i, p, p, p, p, p], i),
             "route_block_dedup": ([p, i, i, i, i, i, i, i, p, p, p, p, p, p], i),
             "moe_rmsnorm": ([p, p, f, i, i, p, p, p], i),
@@ -169,6 +170,16 @@ def moe_expert_swiglu_fused(x_perm, offsets, E, H, I, w_gateup, w_down, h, y_per
                                         _ptr(w_gateup), _ptr(w_down), _ptr(h), _ptr(y_perm), _ptr(sync_ws),
                                         _ptr(dev_status), _stream(stream))
     _check("moe_expert_swiglu_fused", st)
+
+
+def moe_route_permute(x, w_router, bias, k, topk_ids, topk_w, gap, counts, offsets, perm, inv_perm, dev_status,
+                      stream=None):
+    T, H = x.shape
+    E = w_router.shape[0]
+    st = load().moe_route_permute(_ptr(x), _ptr(w_router), _ptr(bias), T, H, E, k, _ptr(topk_ids), _ptr(topk_w),
+                                  _ptr(gap), _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv_perm),
+                                  _ptr(dev_status), _stream(stream))
+    _check("moe_route_permute", st)
 
 
 def moe_combine(y_perm, inv_perm, topk_w, residual, out_bf16, out_f32, dev_status, stream=None):

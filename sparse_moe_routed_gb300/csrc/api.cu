@@ -117,6 +117,27 @@ moe_status moe_route(const uint16_t* x, const uint16_t* w_router, const float* b
   return cuda_status(moe::launch_topk(logits, bias, T, E, k, topk_ids, topk_w, gap, st));
 }
 
+moe_status moe_route_permute(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E,
+                             int k, int32_t* topk_ids, float* topk_w, float* gap, int32_t* counts, int32_t* offsets,
+                             int32_t* perm, int32_t* inv_perm, int32_t* dev_status, void* stream) {
+  if (T < 0) return MOE_ESHAPE;
+  moe_status g = check_geometry(H, E, k, 0);
+  if (g != MOE_OK) return g;
+  if (T > 16) return MOE_ENOTSUP;
+  if (!x || !w_router || !topk_ids || !topk_w || !counts || !offsets || !perm || !inv_perm || !dev_status)
+    return MOE_EINVAL;
+  if (!a16(x) || !a16(w_router) || !a4(topk_ids) || !a4(topk_w) || !a4(counts) || !a4(offsets) || !a4(perm) ||
+      !a4(inv_perm) || !a4(dev_status))
+    return MOE_EINVAL;
+  if ((bias && !a4(bias)) || (gap && !a4(gap))) return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  const cudaError_t e = moe::launch_route_permute(x, w_router, bias, T, H, E, k, topk_ids, topk_w, gap, counts,
+                                                  offsets, perm, inv_perm, dev_status,
+                                                  static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return MOE_ENOTSUP;
+  return cuda_status(e);
+}
+
 moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, const uint16_t* x, int H, int32_t* counts,
                        int32_t* offsets, int32_t* perm, int32_t* inv_perm, uint16_t* x_perm, int32_t* dev_status,
                        void* stream) {

@@ -61,6 +61,9 @@ cudaError_t launch_router_logits_small(const uint16_t* x, const uint16_t* wr, in
                                        cudaStream_t st);
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids, float* w,
                         float* gap, cudaStream_t st);
+cudaError_t launch_route_permute(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H, int E, int k,
+                                 int32_t* ids, float* w, float* gap, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                 int32_t* inv, int32_t* st_word, cudaStream_t st);
 
 // permute.cu
 cudaError_t launch_permute(const int32_t* ids, int R, int k, int E, int32_t* counts,

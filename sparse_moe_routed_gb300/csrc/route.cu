@@ -72,6 +72,13 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t ran
   return v;
 }
 
+// Store to the same shared-memory word in CTA `rank` of the cluster.
+__device__ __forceinline__ void st_cluster_s32(int* local, uint32_t rank, int v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ptx::smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+
 __global__ void __launch_bounds__(kLogitThreads) router_logits_mma_kernel(const uint16_t* __restrict__ x,
                                                                           const uint16_t* __restrict__ wr, int T,
                                                                           int H, int E, float* __restrict__ logits) {
@@ -218,25 +225,13 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
 // across the warp in one bitonic pass, and lane r then holds rank r.  If
 // more than 32 keys reach the threshold (or n > 32), each lane sorts its own
 // keys and n rounds of warp-wide max reductions take the largest head.
+// Top-k of one token by one warp: lv/bv hold the logits and bias of experts
+// lane, lane + 32, ... (bias ignored if has_bias is false).  Writes the
+// token's ids/w row and gap; returns on lane r < k the expert of rank r.
 template <int EPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
-                                                   int T, int E, int k, int32_t* __restrict__ ids,
-                                                   float* __restrict__ w, float* __restrict__ gap) {
-  __shared__ uint64_t cand[8][32];
-  pdl_wait();
-  pdl_trigger();
-  const int warp = threadIdx.x >> 5;
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  // all loads first, then the keys
-  float lv[EPL], bv[EPL];
-#pragma unroll
-  for (int j = 0; j < EPL; ++j) {
-    const int e = j * 32 + lane;
-    lv[j] = e < E ? logits[static_cast<size_t>(t) * E + e] : 0.f;
-    bv[j] = (bias && e < E) ? bias[e] : 0.f;
-  }
+__device__ __forceinline__ int select_topk(const float (&lv)[EPL], const float (&bv)[EPL], bool has_bias, int E,
+                                           int k, int lane, uint64_t* cand, int32_t* ids_row, float* w_row,
+                                           float* gap_t) {
   uint64_t v[EPL];
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
@@ -244,7 +239,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     v[j] = 0;  // below every valid key (f2key(-inf) > 0)
     if (e < E) {
       float l = lv[j];
-      if (bias) l += bv[j];
+      if (has_bias) l += bv[j];
       if (isnan(l)) l = -INFINITY;
       if (l == 0.0f) l = 0.0f;
       v[j] = (static_cast<uint64_t>(f2key(l)) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
@@ -272,9 +267,9 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
       int pos = incl - c;
 #pragma unroll
       for (int j = 0; j < EPL; ++j)
-        if (v[j] >= thr) cand[warp][pos++] = v[j];
+        if (v[j] >= thr) cand[pos++] = v[j];
       __syncwarp();
-      mine = warp_sort_desc(lane < total ? cand[warp][lane] : 0, lane);
+      mine = warp_sort_desc(lane < total ? cand[lane] : 0, lane);
       done = true;
     }
   }
@@ -304,10 +299,198 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
   const float vk1 = __shfl_sync(0xffffffffu, my_v, k - 1);
   if (lane < k) {
-    ids[static_cast<size_t>(t) * k + lane] = my_e;
-    w[static_cast<size_t>(t) * k + lane] = ex / sum;
+    ids_row[lane] = my_e;
+    w_row[lane] = ex / sum;
   }
-  if (gap && lane == 0) gap[t] = (k < E) ? (vk1 - key2f(next_key)) : INFINITY;
+  if (gap_t && lane == 0) *gap_t = (k < E) ? (vk1 - key2f(next_key)) : INFINITY;
+  return my_e;
+}
+
+// One warp per token; see select_topk.
+template <int EPL>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                                                   int T, int E, int k, int32_t* __restrict__ ids,
+                                                   float* __restrict__ w, float* __restrict__ gap) {
+  __shared__ uint64_t cand[8][32];
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  // all loads first, then the keys
+  float lv[EPL], bv[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const int e = j * 32 + lane;
+    lv[j] = e < E ? logits[static_cast<size_t>(t) * E + e] : 0.f;
+    bv[j] = (bias && e < E) ? bias[e] : 0.f;
+  }
+  select_topk<EPL>(lv, bv, bias != nullptr, E, k, lane, cand[warp], ids + static_cast<size_t>(t) * k,
+                   w + static_cast<size_t>(t) * k, gap ? gap + t : nullptr);
+}
+
+// ---------------------------------------------------------------------------
+// Decode block (T <= 16): router logits, top-k and the expert grouping in one
+// launch of one 16-CTA thread-block cluster, so the three steps meet at no
+// kernel boundary.  CTA c computes the logits of experts [c*epc, c*epc + epc)
+// for the block's tokens with warp-level MMA (the 8 warps split K and are
+// summed in warp order), keeping its [16][epc] tile in shared memory.  After a
+// cluster barrier, CTA t < T selects token t's route: lane l reads the logits
+// of experts l, l + 32, ... from their owner CTAs over distributed shared
+// memory, then select_topk; each route is also written into CTA 0's shared
+// memory.  After a second barrier CTA 0 groups the T*k routes by expert:
+// counts, exclusive offsets, and the stable slot order (ascending flat route
+// index inside each expert), exactly what permute_kernel writes.
+constexpr int kRpCtas = 16;
+constexpr int kRpThreads = 256;
+constexpr int kRpWarps = kRpThreads / 32;
+constexpr int kRpChunk = 8;   // k16 steps per register batch
+constexpr int kRpMaxNt = 8;   // n8 tiles per CTA (epc <= 64: E <= 1024)
+
+template <int NT, int EPL>
+__global__ void __launch_bounds__(kRpThreads) route_permute_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr, const float* __restrict__ bias, int T, int H,
+    int E, int k, int32_t* __restrict__ ids, float* __restrict__ w, float* __restrict__ gap,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, int32_t* status) {
+  constexpr int epc = 8 * NT;  // experts per CTA
+  __shared__ float red[kRpWarps][kLogitTok][epc];
+  __shared__ float tile[kLogitTok][epc];
+  __shared__ uint64_t cand[32];
+  __shared__ int s_ids[kLogitTok * kMaxK];  // CTA 0: the block's routes
+  __shared__ int s_cnt[kMaxE + 1];
+  __shared__ int s_bad;
+  __shared__ int s_wsum[kRpWarps];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const uint32_t rank = cluster_ctarank();
+  const int e_base = static_cast<int>(rank) * epc;
+  // ------------------------------------------------------------ logits
+  const int kw = H / kRpWarps;  // K per warp (a multiple of 16: H % 128 == 0)
+  const int steps = kw / 16;
+  const int kbase = warp * kw;
+  const bool ta = g < T, tb = g + 8 < T;
+  const uint32_t* xa = reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(ta ? g : 0) * H + kbase);
+  const uint32_t* xb = reinterpret_cast<const uint32_t*>(x + static_cast<size_t>(tb ? g + 8 : 0) * H + kbase);
+  const uint32_t* wrow[NT];
+  bool e_ok[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int e = e_base + nt * 8 + g;
+    e_ok[nt] = e < E;
+    wrow[nt] = reinterpret_cast<const uint32_t*>(wr + static_cast<size_t>(e_ok[nt] ? e : 0) * H + kbase);
+  }
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  if (threadIdx.x == 0) s_bad = 0;
+  pdl_wait();
+  pdl_trigger();
+  for (int c0 = 0; c0 < steps; c0 += kRpChunk) {
+    uint32_t af[kRpChunk][4];
+    uint32_t bw[kRpChunk][NT][2];
+#pragma unroll
+    for (int s2 = 0; s2 < kRpChunk; ++s2) {
+      const bool in = c0 + s2 < steps;
+      const int o = (c0 + s2) * 8 + q;
+      af[s2][0] = (in && ta) ? xa[o] : 0u;
+      af[s2][1] = (in && tb) ? xb[o] : 0u;
+      af[s2][2] = (in && ta) ? xa[o + 4] : 0u;
+      af[s2][3] = (in && tb) ? xb[o + 4] : 0u;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        bw[s2][nt][0] = (in && e_ok[nt]) ? __ldg(wrow[nt] + o) : 0u;
+        bw[s2][nt][1] = (in && e_ok[nt]) ? __ldg(wrow[nt] + o + 4) : 0u;
+      }
+    }
+#pragma unroll
+    for (int s2 = 0; s2 < kRpChunk; ++s2)
+      if (c0 + s2 < steps) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[nt], af[s2], bw[s2][nt]);
+      }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    red[warp][g][nt * 8 + 2 * q] = acc[nt][0];
+    red[warp][g][nt * 8 + 2 * q + 1] = acc[nt][1];
+    red[warp][g + 8][nt * 8 + 2 * q] = acc[nt][2];
+    red[warp][g + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kLogitTok * epc; i += kRpThreads) {
+    const int t = i / epc, e = i % epc;
+    float sum = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < kRpWarps; ++ww) sum += red[ww][t][e];
+    tile[t][e] = sum;
+  }
+  cluster_sync_all();  // every CTA's logit tile is complete
+  // ------------------------------------------------------------ top-k
+  if (static_cast<int>(rank) < T && warp == 0) {
+    const int t = static_cast<int>(rank);
+    float lv[EPL], bv[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      const int e = j * 32 + lane;
+      lv[j] = e < E ? ld_cluster_f32(&tile[t][e % epc], static_cast<uint32_t>(e / epc)) : 0.f;
+      bv[j] = (bias && e < E) ? bias[e] : 0.f;
+    }
+    const int my_e = select_topk<EPL>(lv, bv, bias != nullptr, E, k, lane, cand, ids + static_cast<size_t>(t) * k,
+                                      w + static_cast<size_t>(t) * k, gap ? gap + t : nullptr);
+    if (lane < k) st_cluster_s32(&s_ids[t * k + lane], 0u, my_e);
+  }
+  cluster_sync_all();  // every route is in CTA 0
+  if (rank != 0) return;
+  // ------------------------------------------------------------ grouping
+  const int R = T * k;
+  for (int e = threadIdx.x; e <= E; e += kRpThreads) s_cnt[e] = 0;
+  __syncthreads();
+  for (int r = threadIdx.x; r < R; r += kRpThreads) {
+    const int e = s_ids[r];
+    if (e < 0 || e >= E) s_bad = 1;
+    else atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) set_status(status, MOE_DEV_BAD_EXPERT);
+    return;
+  }
+  // exclusive scan of s_cnt over E experts: each thread a contiguous run
+  const int per = (E + kRpThreads - 1) / kRpThreads;
+  const int e0 = min(E, threadIdx.x * per), e1 = min(E, e0 + per);
+  int run = 0;
+  for (int e = e0; e < e1; ++e) run += s_cnt[e];
+  int incl = run;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int ww = 0; ww < warp; ++ww) before += s_wsum[ww];
+  int off = before + incl - run;
+  for (int e = e0; e < e1; ++e) {
+    const int c = s_cnt[e];
+    counts[e] = c;
+    offsets[e] = off;
+    s_cnt[e] = off;  // now the segment start
+    off += c;
+  }
+  if (threadIdx.x == 0) offsets[E] = R;
+  __syncthreads();
+  for (int r = threadIdx.x; r < R; r += kRpThreads) {
+    const int e = s_ids[r];
+    int before_r = 0;  // earlier routes of the same expert: stable order
+    for (int r2 = 0; r2 < r; ++r2) before_r += (s_ids[r2] == e) ? 1 : 0;
+    const int slot = s_cnt[e] + before_r;
+    perm[slot] = r;
+    inv[r] = slot;
+  }
 }
 
 template <int EPL>
@@ -326,6 +509,41 @@ cudaError_t launch_router_logits_small(const uint16_t* x, const uint16_t* wr, in
                             wr, T, H, E, logits);
 }
 
+template <int NT, int EPL>
+cudaError_t run_route_permute(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H, int E, int k,
+                              int32_t* ids, float* w, float* gap, int32_t* counts, int32_t* offsets, int32_t* perm,
+                              int32_t* inv, int32_t* st_word, cudaStream_t st) {
+  auto kern = route_permute_kernel<NT, EPL>;
+  static std::mutex mu;
+  static int ready[64] = {0};  // per device: 1 usable, -1 not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (ready[dev] == 0) {
+      ready[dev] = -1;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kRpCtas);
+        cfg.blockDim = dim3(kRpThreads);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kRpCtas;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0) ready[dev] = 1;
+      }
+      cudaGetLastError();
+    }
+    if (ready[dev] < 0) return cudaErrorNotSupported;
+  }
+  return launch_pdl_cluster(kern, dim3(kRpCtas), dim3(kRpThreads), dim3(kRpCtas, 1, 1), 0, st, x, wr, bias, T, H, E,
+                            k, ids, w, gap, counts, offsets, perm, inv, st_word);
+}
+
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids, float* w,
                         float* gap, cudaStream_t st) {
   const int epl = (E + 31) / 32;
@@ -335,6 +553,22 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
   if (epl <= 8) return run_topk<8>(logits, bias, T, E, k, ids, w, gap, st);
   if (epl <= 16) return run_topk<16>(logits, bias, T, E, k, ids, w, gap, st);
   return run_topk<32>(logits, bias, T, E, k, ids, w, gap, st);
+}
+
+// One-launch route + grouping for a decode block (T <= 16); cudaErrorNotSupported
+// if this device cannot run a 16-CTA cluster.
+cudaError_t launch_route_permute(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H, int E, int k,
+                                 int32_t* ids, float* w, float* gap, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                 int32_t* inv, int32_t* st_word, cudaStream_t st) {
+  const int nt = ((E + kRpCtas - 1) / kRpCtas + 7) / 8;  // n8 tiles per CTA
+  const int epl = (E + 31) / 32;
+  if (nt <= 1 && epl <= 2)
+    return run_route_permute<1, 2>(x, wr, bias, T, H, E, k, ids, w, gap, counts, offsets, perm, inv, st_word, st);
+  if (nt <= 2 && epl <= 8)
+    return run_route_permute<2, 8>(x, wr, bias, T, H, E, k, ids, w, gap, counts, offsets, perm, inv, st_word, st);
+  if (nt <= 4 && epl <= 16)
+    return run_route_permute<4, 16>(x, wr, bias, T, H, E, k, ids, w, gap, counts, offsets, perm, inv, st_word, st);
+  return run_route_permute<8, 32>(x, wr, bias, T, H, E, k, ids, w, gap, counts, offsets, perm, inv, st_word, st);
 }
 
 }  // namespace moe

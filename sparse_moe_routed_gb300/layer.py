@@ -13,6 +13,9 @@ which for a decode-sized block also gathers the token rows itself:
     moe_route -> moe_permute (+ row gather unless few rows) ->
     moe_expert_swiglu_fused -> moe_combine
 
+(`ROUTE_PERMUTE_ONE_LAUNCH` switches a decode block to moe_route_permute,
+which routes and groups in one launch.)
+
 Every step runs in the CUDA library; this class only owns memory.
 """
 from __future__ import annotations
@@ -33,6 +36,7 @@ class MoELayer:
     """
 
     GATHER_IN_FUSED_MAX_ROWS = 4096
+    ROUTE_PERMUTE_ONE_LAUNCH = False
 
     def __init__(self, w_router, bias, w_gateup, w_down, k: int, T_max: int, fmt: int = _lib.MOE_W_BF16,
                  I: int = None):
@@ -102,7 +106,15 @@ class MoELayer:
         E, H, I, k = self.E, self.H, self.I, self.k
         ws_bytes = self.ws.numel()
         calls = []
-        if route:
+        # moe_route_permute (route + grouping in one 16-CTA cluster launch) is
+        # slower on GB300 than the logits -> top-k -> grouping chain here: a
+        # single cluster pulls the router matrix through 16 SMs.  Kept off.
+        route_and_group = route and T <= 16 and self.ROUTE_PERMUTE_ONE_LAUNCH
+        if route_and_group:
+            calls.append(("moe_route_permute", lib.moe_route_permute,
+                          (P(x), P(self.w_router), P(self.bias), T, H, E, k, P(self.ids), P(self.w), P(self.gap),
+                           P(self.counts), P(self.offsets), P(self.perm), P(self.inv), P(self.status), st)))
+        elif route:
             calls.append(("moe_route", lib.moe_route,
                           (P(x), P(self.w_router), P(self.bias), T, H, E, k, P(self.ids), P(self.w), P(self.gap),
                            P(self.ws), ws_bytes, st)))
@@ -110,11 +122,16 @@ class MoELayer:
         # (a decode block); for many rows moe_permute's gather runs at full
         # occupancy instead
         gather_in_fused = self.fused and R <= self.GATHER_IN_FUSED_MAX_ROWS
-        calls += [
-            ("moe_permute", lib.moe_permute,
-             (P(self.ids), T, k, E, None if gather_in_fused else P(x), H, P(self.counts), P(self.offsets),
-              P(self.perm), P(self.inv), None if gather_in_fused else P(self.x_perm), P(self.status), st)),
-        ]
+        if not route_and_group:
+            calls.append(("moe_permute", lib.moe_permute,
+                          (P(self.ids), T, k, E, None if gather_in_fused else P(x), H, P(self.counts),
+                           P(self.offsets), P(self.perm), P(self.inv),
+                           None if gather_in_fused else P(self.x_perm), P(self.status), st)))
+        elif not gather_in_fused:
+            # grouped already; gather the rows separately
+            calls.append(("moe_permute_gather", lib.moe_permute,
+                          (P(self.ids), T, k, E, P(x), H, P(self.counts), P(self.offsets), P(self.perm),
+                           P(self.inv), P(self.x_perm), P(self.status), st)))
         if self.fused:
             calls.append(("moe_expert_swiglu_fused", lib.moe_expert_swiglu_fused,
                           (P(x) if gather_in_fused else None, k, P(self.perm), P(self.x_perm), P(self.offsets), R,

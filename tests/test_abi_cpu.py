@@ -26,7 +26,7 @@ def lib():
 def test_library_loads_and_exports_every_declared_symbol():
     L = lib()
     names = _lib.declared_functions()
-    assert len(names) == 17
+    assert len(names) == 18
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 100
@@ -208,3 +208,23 @@ def test_swiglu_fused_rejections():
     assert call(x=PM, k=10, perm=P) == _lib.MOE_EINVAL
     assert call(R=0) == _lib.MOE_OK
     assert call(R=0, x=P, k=10, perm=P) == _lib.MOE_OK
+
+
+def test_route_permute_rejections():
+    L = lib()
+    # x, wr, bias, T, H, E, k, ids, w, gap, counts, offsets, perm, inv, status, stream
+    base = [P, P, NUL, 16, 2560, 512, 10, P, P, NUL, P, P, P, P, P, NUL]
+
+    def call(i, v):
+        a = list(base)
+        a[i] = v
+        return L.moe_route_permute(*a)
+
+    assert call(3, 17) == _lib.MOE_ENOTSUP        # one cluster holds at most 16 tokens
+    assert call(3, -1) == _lib.MOE_ESHAPE
+    assert call(3, 0) == _lib.MOE_OK
+    assert call(0, NUL) == _lib.MOE_EINVAL
+    assert call(14, NUL) == _lib.MOE_EINVAL       # status word required
+    assert call(0, PM) == _lib.MOE_EINVAL
+    assert call(6, 40) == _lib.MOE_ENOTSUP        # k > 32
+    assert call(4, 2500) == _lib.MOE_ENOTSUP      # H % 128

@@ -91,6 +91,38 @@ def test_route_parity(name, T, nsample):
           f"rank swaps {rep['rank_swaps']}")
 
 
+@pytest.mark.parametrize("name,T", [("tiny", None), ("decode", None), ("decode", 1), ("decode", 5), ("tiny", 16)])
+def test_route_permute_one_launch(name, T):
+    """moe_route_permute (one cluster launch for a decode block): routes graded
+    against the oracle like moe_route's, and its grouping bit-exact against the
+    oracle's stable counting sort of the routes it chose."""
+    cfg, d, host = case(name, T)
+    E, k, Tn = cfg.E, cfg.k, cfg.T
+    R = Tn * k
+    ids = torch.full((Tn, k), -1, dtype=torch.int32, device=DEV)
+    w = torch.full((Tn, k), float("nan"), dtype=torch.float32, device=DEV)
+    gap = torch.full((Tn,), float("nan"), dtype=torch.float32, device=DEV)
+    counts = torch.full((E,), -7, dtype=torch.int32, device=DEV)
+    offsets = torch.full((E + 1,), -7, dtype=torch.int32, device=DEV)
+    perm = torch.full((R,), -7, dtype=torch.int32, device=DEV)
+    inv = torch.full((R,), -7, dtype=torch.int32, device=DEV)
+    st = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    for _ in range(2):  # twice in a row: nothing carries over between calls
+        _lib.moe_route_permute(d["x"], d["w_router"], d["bias"], k, ids, w, gap, counts, offsets, perm, inv, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ids_np, w_np, gap_np = ids.cpu().numpy(), w.cpu().numpy(), gap.cpu().numpy()
+    ids_r, w_r, gap_r, L_r = oracle.route(host["x"], host["wr"], host["bias"], k)
+    rep = compare_routes(ids_np, w_np, ids_r, w_r, gap_r, L_r)
+    assert np.allclose(gap_np, gap_r, atol=5e-5)
+    assert rep["near_tie"] <= max(2, Tn // 10), rep
+    counts_r, offsets_r, perm_r, inv_r = oracle.permute(ids_np, E)
+    assert np.array_equal(counts.cpu().numpy(), counts_r)
+    assert np.array_equal(offsets.cpu().numpy(), offsets_r)
+    assert np.array_equal(perm.cpu().numpy(), perm_r)
+    assert np.array_equal(inv.cpu().numpy(), inv_r)
+
+
 def test_route_tie_contract_on_gpu():
     """All-zero router weights: every logit equals its bias; ties go to lower IDs."""
     E, H, k, T = 64, 256, 4, 3
@@ -286,6 +318,26 @@ def test_layer_parity(name, T, nsample, tiled):
     rel_max, mean_rel = assert_output_close(got, ref[keep], what=f"{name} layer output")
     print(f"{name} T={cfg.T} tiled={tiled}: {keep.sum()}/{len(toks)} tokens graded, max err {rel_max:.2e} "
           f"of max|ref|, mean rel {mean_rel:.2e}")
+
+
+def test_layer_with_one_launch_routing():
+    """The layer with routing and grouping in one launch (moe_route_permute)
+    against the oracle, as test_layer_parity grades the default chain."""
+    cfg, d, host = case("decode")
+    gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, cfg.E, cfg.H, cfg.I)
+    layer = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, cfg.T, fmt=_lib.MOE_W_BF16_TILED, I=cfg.I)
+    layer.ROUTE_PERMUTE_ONE_LAUNCH = True
+    assert [c[0] for c in layer.bound_calls(d["x"])][0] == "moe_route_permute"
+    out = layer.forward(d["x"]).clone()
+    torch.cuda.synchronize()
+    assert layer.read_status() == 0
+    ids = layer.ids[:cfg.T].cpu().numpy()
+    ids_r, w_r, gap_r, L_r = oracle.route(host["x"], host["wr"], host["bias"], cfg.k)
+    ref = oracle.experts_combine(f32_of_bits(host["x"]), ids_r, w_r, cfg.H, cfg.I, wgu_bits=host["wgu"],
+                                 wd_bits=host["wd"])
+    same = np.array([np.array_equal(ids[t], ids_r[t]) for t in range(cfg.T)])
+    assert same.sum() >= 0.9 * cfg.T
+    assert_output_close(out.float().cpu().numpy()[same], ref[same], what="decode layer, one-launch routing")
 
 
 def _adjacent_swap_ok(ids_gpu, ids_ref, L_ref):
