@@ -10,6 +10,9 @@ weight sets (8 x 5.03 GB) and as many token batches, so the working set is far
 larger than L2 and every step streams its experts' weights from HBM.
 
 --config prefill runs the T=4096 uniform-router layer instead.
+--config offload keeps the decode layer's expert records in pinned host
+memory behind an HBM slot cache and reports tokens/s, hit rate, bytes fetched
+per token and the hidden fraction of the fetch for several wave widths.
 --impl reference times the CPU oracle (the reference arm) on the same workload.
 
 Multi-GPU: one process per GPU under torchrun; every rank runs independent
@@ -44,7 +47,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="decode", choices=["decode", "prefill", "stack48", "sweep"])
+    ap.add_argument("--config", default="decode", choices=["decode", "prefill", "stack48", "sweep", "offload"])
+    ap.add_argument("--slots", default="160,192,256", help="offload: HBM expert slot counts")
+    ap.add_argument("--waves", default="1,2,4,0", help="offload: wave widths to time (0 = all misses)")
     ap.add_argument("--layers", type=int, default=0, help="distinct layer weight sets rotated (0 = auto)")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (small profiling case)")
     ap.add_argument("--tokens", type=int, default=0,
@@ -254,6 +259,8 @@ def main():
 
     if args.config in ("stack48", "sweep"):
         return run_stack(args, rank, world, local, dev)
+    if args.config == "offload":
+        return run_offload(args, rank, world, local, dev)
     cfg = wl.CONFIGS[args.config]
     if args.experts:
         from dataclasses import replace
@@ -602,8 +609,8 @@ def run_stack(args, rank, world, local, dev):
     line = {"metric": METRIC, "value": T * K * world / (total_ms / 1e3), "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": ("int4 g64 experts (dequantised to fp32 in registers, fp32 FMA), bf16 router, fp32 residual"
-                      if cuda_core_int4 else
+            "dtype": ("int4 g64 experts (codes expanded to bf16 pairs in registers, warp-level bf16 MMA, fp32 "
+                      "accumulation), bf16 router, fp32 residual" if cuda_core_int4 else
                       "int4 g64 experts (bf16 tensor-core operands), bf16 router, fp32 residual"),
             "data": "synthetic (seeded)",
             "config": {"workload": f"stack48_int4g64_L{L}_T{T}_blocks{NB}", "layers": L, "T": T, "blocks": NB,
@@ -611,7 +618,7 @@ def run_stack(args, rank, world, local, dev):
                        "l2": f"inputs larger than L2: {L} layers of int4 experts "
                              f"({L * (cfg.E * rec_bytes + router_bytes) / 1e9:.1f} GB) streamed per block"},
             "roofline": {"bound": "hbm",
-                         "kernel": "gemv_q4_kernel (moe_expert_gateup, CUDA cores)" if cuda_core_int4 else
+                         "kernel": "gemv_q4_kernel (moe_expert_gateup, warp-level MMA)" if cuda_core_int4 else
                                    "grouped_gemm_q4_kernel (moe_expert_gateup, tcgen05)",
                          "achieved": gu_bytes / (gu_avg / 1e3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": gu_bytes / (gu_avg / 1e3) / 1e9 / pk["hbm_gbs"], "traffic": None,
@@ -625,6 +632,161 @@ def run_stack(args, rank, world, local, dev):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+    return 0
+
+
+def run_offload(args, rank, world, local, dev):
+    """Decode blocks with the expert records in host memory behind S HBM slots.
+
+    Every pass runs the same sequence of token blocks from the same cache
+    state, so the cached passes see the same hits and misses:
+      resident    MoELayer with the records in HBM;
+      all-hit     the cached layer with every expert already in a slot (its
+                  compute-only time, cache bookkeeping included);
+    and for each slot count S, from an empty cache:
+      copy-first  moe_cache_fetch timed on its own (the I/O wall time of the
+                  misses), then the contraction;
+      wave W      the in-launch fetch with wave width W.
+    hidden fraction = 1 - (wave step time - all-hit step time) / fetch time:
+    the exposed part of the I/O is what the wave path takes beyond compute.
+    """
+    import torch
+    import workloads as wl
+    from sparse_moe_routed_gb300 import CachedMoELayer, MoELayer, _lib, pack_layer_experts
+
+    cfg = wl.DECODE
+    if args.experts:
+        from dataclasses import replace
+        cfg = replace(cfg, E=args.experts)
+    E, H, I, T = cfg.E, cfg.H, cfg.I, cfg.T
+    slots = [int(v) for v in str(args.slots).split(",")]
+    d = wl.layer_inputs(cfg, dev, with_x=False)
+    gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, E, H, I)
+    del d["w_gateup"], d["w_down"]
+    hgu = torch.empty(gu.shape, dtype=torch.uint8, pin_memory=True)
+    hdn = torch.empty(dn.shape, dtype=torch.uint8, pin_memory=True)
+    hgu.copy_(gu)
+    hdn.copy_(dn)
+    torch.cuda.synchronize()
+    rg, rd = hgu.numel() // E, hdn.numel() // E
+    rec = rg + rd
+    NB = 64
+    xs = [wl.token_batch(cfg, dev, index=b, T=T) for b in range(NB)]
+    st = torch.cuda.current_stream()
+    K = max(args.steps, 16) if args.steps < 20000 else 256
+    W0 = max(args.warmup, 3)
+    resident = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, T, fmt=_lib.MOE_W_BF16_TILED, I=I)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    # link bandwidth: a copy-engine copy of 1 GiB pinned -> device, and the
+    # fetch kernel copying whole records alone
+    nb = min(hgu.numel(), 1 << 30)
+    dst = torch.empty((nb,), dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        dst.copy_(hgu[:nb], non_blocking=True)
+    e0.record(st)
+    for _ in range(5):
+        dst.copy_(hgu[:nb], non_blocking=True)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ce_gbs = 5 * nb / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del dst
+
+    # the all-hit layer: S = E slots, every expert in slot e
+    full = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=E)
+    ar = torch.arange(E, dtype=torch.int32, device=dev)
+    stt = torch.tensor([0, E, 0, 0], dtype=torch.int32, device=dev)
+    _lib.moe_cache_fetch(hgu, hdn, rg, rd, ar, ar, stt, full.pool_gu, full.pool_dn)
+    nf = min(E, 96)
+    stt[1] = nf
+    e0.record(st)
+    for _ in range(5):
+        _lib.moe_cache_fetch(hgu, hdn, rg, rd, ar, ar, stt, full.pool_gu, full.pool_dn)
+    e1.record(st)
+    full.slot_of.copy_(ar)
+    full.expert_of.copy_(ar)
+    torch.cuda.synchronize()
+    fetch_gbs = 5 * nf * rec / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+    def timed(layer, fetch_events=False):
+        for i in range(W0):
+            layer.forward(xs[i % NB])
+        torch.cuda.synchronize()
+        if isinstance(layer, CachedMoELayer):
+            layer.stats[2:].zero_()
+        f0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        f1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for i in range(K):
+            for c in layer.bound_calls(xs[(W0 + i) % NB], T, stream=st):
+                if fetch_events and c[0] == "moe_cache_fetch":
+                    f0[i].record(st)
+                    MoELayer.issue(c)
+                    f1[i].record(st)
+                else:
+                    MoELayer.issue(c)
+        b.record(st)
+        torch.cuda.synchronize()
+        assert layer.read_status() == 0, f"device status {layer.read_status():#x}"
+        io = sum(f0[i].elapsed_time(f1[i]) for i in range(K)) / K if fetch_events else None
+        return a.elapsed_time(b) / K, io
+
+    sampler = ClockSampler(gpu_uuid(local))
+    time.sleep(0.3)
+    tw0 = time.time()
+    res_ms, _ = timed(resident)
+    hit_ms, _ = timed(full)
+    assert int(full.stats[3].item()) == 0
+    del full
+    by_slots = {}
+    for S in slots:
+        bar = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=S, fetch="barrier")
+        bar_ms, io_ms = timed(bar, fetch_events=True)
+        hits, misses = [int(v) for v in bar.stats[2:].cpu().tolist()]
+        del bar
+        waves = {}
+        for w in [int(v) for v in args.waves.split(",")]:
+            lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=S,
+                                 wave=w if w > 0 else 1 << 20)
+            ms_w, _ = timed(lay)
+            assert tuple(int(v) for v in lay.stats[2:].cpu().tolist()) == (hits, misses), "passes differ"
+            del lay
+            waves["all" if w <= 0 else str(w)] = {
+                "tokens_per_s": T / (ms_w / 1e3), "ms_per_step": ms_w,
+                "hidden_fraction": (1.0 - (ms_w - hit_ms) / io_ms) if io_ms > 0 else None}
+        fetched = misses * rec / K
+        best = max(waves.values(), key=lambda v: v["tokens_per_s"])
+        by_slots[str(S)] = {
+            "hit_rate": hits / max(hits + misses, 1), "misses_per_step": misses / K,
+            "fetched_bytes_per_token": fetched / T,
+            "copy_first": {"ms_per_step": bar_ms, "tokens_per_s": T / (bar_ms / 1e3), "fetch_ms_per_step": io_ms,
+                           "fetch_gbs": fetched / (io_ms / 1e3) / 1e9 if io_ms else None},
+            "waves": waves, "best_tokens_per_s": best["tokens_per_s"],
+            "link_gbs_during_best": fetched / (best["ms_per_step"] / 1e3) / 1e9}
+    tw1 = time.time()
+    sampler.stop()
+    head = by_slots[str(slots[0])]
+    line = {
+        "metric": METRIC, "value": head["best_tokens_per_s"], "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W0, "ms_per_step": T / head["best_tokens_per_s"] * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; 64 independent token blocks in turn)",
+        "config": {"workload": f"offload_{workload_name(cfg)}_S{slots[0]}", "slots": slots, "T": T, "E": E,
+                   "records": "tile-packed bf16 in pinned host memory; HBM slot cache, FIFO replacement",
+                   "record_bytes": rec},
+        "resident": {"ms_per_step": res_ms, "tokens_per_s": T / (res_ms / 1e3)},
+        "all_hit": {"ms_per_step": hit_ms, "tokens_per_s": T / (hit_ms / 1e3)},
+        "by_slots": by_slots,
+        "link": {"copy_engine_h2d_gbs": ce_gbs, "fetch_kernel_gbs": fetch_gbs,
+                 "fetch_kernel_sample": f"{nf} experts' records, kernel alone"},
+        "roofline": {"bound": "link", "kernel": "moe_cache_fetch (cache_fetch_kernel), alone",
+                     "achieved": fetch_gbs, "peak": ce_gbs, "unit": "GB/s", "frac": fetch_gbs / ce_gbs,
+                     "traffic": None, "peak_source": "copy-engine host-to-device copy measured in this run"},
+        "clocks": sampler.summary(tw0, tw1),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     return 0
 
 

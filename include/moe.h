@@ -60,6 +60,7 @@ typedef enum moe_status {
 #define MOE_DEV_BAD_EXPERT 0x1 /* an expert ID outside [0, E) was seen       */
 #define MOE_DEV_NONFINITE 0x2  /* a layer output was NaN or infinite         */
 #define MOE_DEV_TIMEOUT 0x4    /* a bounded pipeline wait ran out            */
+#define MOE_DEV_CACHE_FULL 0x8 /* routed experts did not fit the expert cache */
 
 typedef enum moe_wfmt {
   MOE_W_BF16 = 0,          /* bf16 weights, plain record layout                  */
@@ -244,6 +245,69 @@ MOE_API moe_status moe_expert_swiglu_fused(const uint16_t *x, int k, const int32
                                            const int32_t *offsets, int R, int E, int H, int I, int fmt,
                                            const void *w_gateup, const void *w_down, uint16_t *h, float *y_perm,
                                            int32_t *sync_ws, int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Expert records in host memory, served through an HBM slot cache.
+ *
+ * Source: AFN-019 "Hide SSD misses before the router knows they exist",
+ * sections "Why overlap alone cannot defeat the byte roofline" (the routed
+ * records fetched from the slower tier are the first-order cost) and
+ * "Hypothesis H4" (gate/up and down records of one expert, fetched whole).
+ * On GB300 the slower tier is Grace memory behind NVLink-C2C: the packed
+ * records (moe_pack_experts output) of all E experts live in pinned host
+ * memory that the GPU reads directly; S slots of HBM hold recent experts.
+ *
+ * moe_cache_plan -- one CTA.  State (device, caller-owned, persistent across
+ *   calls): slot_of [E] int32 (slot of each expert or -1), expert_of [S]
+ *   int32 (expert in each slot or -1), hand [1] int32; initialise to -1, -1,
+ *   0.  From counts [E] (moe_permute): routed experts with a slot are hits;
+ *   the others are misses, in expert order, and take the next slots in
+ *   rotation from the hand that hold no expert routed in this call (FIFO
+ *   replacement).  Writes miss_list [S] (experts to fetch), miss_slot [S]
+ *   (their slots), stats[0..1] = {hits, misses} of this call, adds them to
+ *   the running totals stats[2..3] (the caller zeroes those), and updates the
+ *   state.  If the misses do not fit (more routed experts than S), sets
+ *   MOE_DEV_CACHE_FULL, counts the call as {hits, 0}, and changes nothing
+ *   else.  S <= 1024, E <= 1024.
+ * moe_cache_fetch -- copies the planned misses' records from host memory
+ *   (host_gateup / host_down, E records of rec_* bytes, 16-byte aligned) into
+ *   the pools (S records each); reads the miss count from stats on the
+ *   device, so the plan and the fetch need no host round trip.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_cache_plan(const int32_t *counts, int E, int32_t *slot_of, int32_t *expert_of, int S,
+                                  int32_t *hand, int32_t *miss_list, int32_t *miss_slot, int32_t *stats,
+                                  int32_t *dev_status, void *stream);
+MOE_API moe_status moe_cache_fetch(const void *host_gateup, const void *host_down, size_t rec_gateup,
+                                   size_t rec_down, const int32_t *miss_list, const int32_t *miss_slot,
+                                   const int32_t *stats, void *pool_gateup, void *pool_down, void *stream);
+
+/* moe_expert_swiglu_cached -- moe_expert_swiglu_fused over slot pools:
+ *   pool_gateup / pool_down hold S tile-packed bf16 records (MOE_W_BF16_TILED
+ *   layout, one expert each) and expert e's records are record slot_of[e].
+ *   A routed expert whose slot_of entry is outside [0, S) is read from slot 0
+ *   and flags MOE_DEV_CACHE_FULL.
+ *   host_gateup == NULL: the slots are already filled (moe_cache_fetch).
+ *   host_gateup != NULL: the launch fetches the plan of moe_cache_plan itself
+ *   (miss_list, miss_slot, stats) from the host records (host_gateup /
+ *   host_down, E records each, pinned host memory the device can read, 16-byte
+ *   aligned): extra warps copy the records over the CPU-GPU link in 32 KiB
+ *   pieces while the experts already resident compute, and the tiles of each
+ *   missing expert start once its record has landed.  Order of the copies: the
+ *   wave order of AFN-019 "Hypothesis H4" with `wave` experts per wave (gate/up
+ *   of wave 0; then per wave w the gate/up records of wave w and the down
+ *   records of wave w-1; then the last down records); wave >= the number of
+ *   misses copies every gate/up record before any down record.  The combine
+ *   that follows stays in route-rank order.  Needs H/64 and I/64 even
+ *   (MOE_ENOTSUP otherwise).
+ *   sync_ws: [3E + 3] int32, zero before the first call; every launch leaves
+ *   it zero again. */
+MOE_API moe_status moe_expert_swiglu_cached(const uint16_t *x, int k, const int32_t *perm, uint16_t *x_perm,
+                                            const int32_t *offsets, int R, int E, int H, int I, int fmt,
+                                            void *pool_gateup, void *pool_down, int S, const int32_t *slot_of,
+                                            const void *host_gateup, const void *host_down,
+                                            const int32_t *miss_list, const int32_t *miss_slot,
+                                            const int32_t *stats, int wave, uint16_t *h, float *y_perm,
+                                            int32_t *sync_ws, int32_t *dev_status, void *stream);
 
 /* ---------------------------------------------------------------------------
  * moe_pack_experts -- reorder one component of every expert record into the

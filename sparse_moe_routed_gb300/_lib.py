@@ -17,7 +17,7 @@ import threading
 from . import build as _build
 
 MOE_OK, MOE_EINVAL, MOE_ESHAPE, MOE_ERANGE, MOE_ECUDA, MOE_ENOTSUP, MOE_EDEVICE_TIMEOUT, MOE_EWORKSPACE = range(8)
-MOE_DEV_BAD_EXPERT, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT = 0x1, 0x2, 0x4
+MOE_DEV_BAD_EXPERT, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT, MOE_DEV_CACHE_FULL = 0x1, 0x2, 0x4, 0x8
 MOE_W_BF16, MOE_W_INT4_G64, MOE_W_BF16_TILED, MOE_W_INT4_G64_TILED = 0, 1, 2, 3
 
 HEADER = os.path.join(_build.INCLUDE, "moe.h")
@@ -68,6 +68,10 @@ def load(path: str | None = None):
             "moe_pack_size": ([i, i, i, i, i], sz),
             "moe_pack_experts": ([i, p, p, i, i, i, i, p, sz, p], i),
             "moe_route_recall": ([p, p, i, i, p, p], i),
+            "moe_cache_plan": ([p, i, p, p, i, p, p, p, p, p, p], i),
+            "moe_cache_fetch": ([p, p, sz, sz, p, p, p, p, p, p], i),
+            "moe_expert_swiglu_cached": ([p, i, p, p, p, i, i, i, i, i, p, p, i, p, p, p, p, p, p, i, p, p, p, p, p],
+                                         i),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -170,6 +174,33 @@ def moe_expert_swiglu_fused(x_perm, offsets, E, H, I, w_gateup, w_down, h, y_per
                                         _ptr(w_gateup), _ptr(w_down), _ptr(h), _ptr(y_perm), _ptr(sync_ws),
                                         _ptr(dev_status), _stream(stream))
     _check("moe_expert_swiglu_fused", st)
+
+
+def moe_cache_plan(counts, slot_of, expert_of, hand, miss_list, miss_slot, stats, dev_status, stream=None):
+    E, S = counts.shape[0], expert_of.shape[0]
+    st = load().moe_cache_plan(_ptr(counts), E, _ptr(slot_of), _ptr(expert_of), S, _ptr(hand), _ptr(miss_list),
+                               _ptr(miss_slot), _ptr(stats), _ptr(dev_status), _stream(stream))
+    _check("moe_cache_plan", st)
+
+
+def moe_cache_fetch(host_gateup, host_down, rec_gateup, rec_down, miss_list, miss_slot, stats, pool_gateup,
+                    pool_down, stream=None):
+    st = load().moe_cache_fetch(_ptr(host_gateup), _ptr(host_down), rec_gateup, rec_down, _ptr(miss_list),
+                                _ptr(miss_slot), _ptr(stats), _ptr(pool_gateup), _ptr(pool_down), _stream(stream))
+    _check("moe_cache_fetch", st)
+
+
+def moe_expert_swiglu_cached(x_perm, offsets, E, H, I, pool_gateup, pool_down, S, slot_of, h, y_perm, sync_ws,
+                             dev_status, host_gateup=None, host_down=None, miss_list=None, miss_slot=None,
+                             stats=None, wave=1 << 20, fmt=MOE_W_BF16_TILED, x=None, perm=None, k=0, stream=None):
+    """moe_expert_swiglu_fused over slot pools; with host records it also
+    fetches the planned misses in the same launch."""
+    R = x_perm.shape[0]
+    st = load().moe_expert_swiglu_cached(_ptr(x), k, _ptr(perm), _ptr(x_perm), _ptr(offsets), R, E, H, I, fmt,
+                                         _ptr(pool_gateup), _ptr(pool_down), S, _ptr(slot_of), _ptr(host_gateup),
+                                         _ptr(host_down), _ptr(miss_list), _ptr(miss_slot), _ptr(stats), wave,
+                                         _ptr(h), _ptr(y_perm), _ptr(sync_ws), _ptr(dev_status), _stream(stream))
+    _check("moe_expert_swiglu_cached", st)
 
 
 def moe_route_permute(x, w_router, bias, k, topk_ids, topk_w, gap, counts, offsets, perm, inv_perm, dev_status,

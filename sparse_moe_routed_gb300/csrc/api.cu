@@ -228,10 +228,10 @@ moe_status moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets, in
   return moe_expert_down(h, offsets, R, E, H, I, fmt, w_down, s_down, y_perm, dev_status, stream);
 }
 
-moe_status moe_expert_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
-                                   const int32_t* offsets, int R, int E, int H, int I, int fmt, const void* w_gateup,
-                                   const void* w_down, uint16_t* h, float* y_perm, int32_t* sync_ws,
-                                   int32_t* dev_status, void* stream) {
+static moe_status check_fused(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
+                              const int32_t* offsets, int R, int E, int H, int I, int fmt, const void* w_gateup,
+                              const void* w_down, uint16_t* h, float* y_perm, int32_t* sync_ws,
+                              int32_t* dev_status) {
   moe_status c = check_expert_args(R, E, H, I, fmt);
   if (c != MOE_OK) return c;
   if (fmt != MOE_W_BF16_TILED) return MOE_ENOTSUP;
@@ -245,9 +245,80 @@ moe_status moe_expert_swiglu_fused(const uint16_t* x, int k, const int32_t* perm
     if (k > moe::kMaxK) return MOE_ENOTSUP;
     if (!perm || !a16(x) || !a4(perm)) return MOE_EINVAL;
   }
+  return MOE_OK;
+}
+
+moe_status moe_expert_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
+                                   const int32_t* offsets, int R, int E, int H, int I, int fmt, const void* w_gateup,
+                                   const void* w_down, uint16_t* h, float* y_perm, int32_t* sync_ws,
+                                   int32_t* dev_status, void* stream) {
+  const moe_status c =
+      check_fused(x, k, perm, x_perm, offsets, R, E, H, I, fmt, w_gateup, w_down, h, y_perm, sync_ws, dev_status);
+  if (c != MOE_OK) return c;
   if (R == 0) return MOE_OK;
-  return cuda_status(moe::launch_swiglu_fused(x, k, perm, x_perm, offsets, E, R, H, I, w_gateup, w_down, h, y_perm,
-                                              sync_ws, dev_status, static_cast<cudaStream_t>(stream)));
+  return cuda_status(moe::launch_swiglu_fused(x, k, perm, x_perm, offsets, E, R, H, I, w_gateup, w_down, nullptr, h,
+                                              y_perm, sync_ws, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_swiglu_cached(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
+                                    const int32_t* offsets, int R, int E, int H, int I, int fmt, void* pool_gateup,
+                                    void* pool_down, int S, const int32_t* slot_of, const void* host_gateup,
+                                    const void* host_down, const int32_t* miss_list, const int32_t* miss_slot,
+                                    const int32_t* stats, int wave, uint16_t* h, float* y_perm, int32_t* sync_ws,
+                                    int32_t* dev_status, void* stream) {
+  const moe_status c = check_fused(x, k, perm, x_perm, offsets, R, E, H, I, fmt, pool_gateup, pool_down, h, y_perm,
+                                   sync_ws, dev_status);
+  if (c != MOE_OK) return c;
+  if (S <= 0) return MOE_ESHAPE;
+  if (S > 1024) return MOE_ENOTSUP;
+  if (!slot_of || !a4(slot_of)) return MOE_EINVAL;
+  if ((H / 64) % 2 != 0 || (I / 64) % 2 != 0) return MOE_ENOTSUP;
+  const bool fetch = host_gateup != nullptr;
+  if (fetch) {
+    if (wave <= 0) return MOE_ESHAPE;
+    if (!host_down || !miss_list || !miss_slot || !stats) return MOE_EINVAL;
+    if (!a16(host_gateup) || !a16(host_down) || !a4(miss_list) || !a4(miss_slot) || !a4(stats)) return MOE_EINVAL;
+  }
+  if (R == 0) return MOE_OK;
+  moe::FusedCache fc{};
+  fc.slot_of = slot_of;
+  fc.S = S;
+  if (fetch) {
+    fc.host_gu = host_gateup;
+    fc.host_dn = host_down;
+    fc.miss_list = miss_list;
+    fc.miss_slot = miss_slot;
+    fc.stats = stats;
+    fc.wave = wave;
+  }
+  return cuda_status(moe::launch_swiglu_fused(x, k, perm, x_perm, offsets, E, R, H, I, pool_gateup, pool_down, &fc,
+                                              h, y_perm, sync_ws, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_cache_plan(const int32_t* counts, int E, int32_t* slot_of, int32_t* expert_of, int S, int32_t* hand,
+                          int32_t* miss_list, int32_t* miss_slot, int32_t* stats, int32_t* dev_status, void* stream) {
+  if (E <= 0 || S <= 0) return MOE_ESHAPE;
+  if (E > moe::kMaxE || S > 1024) return MOE_ENOTSUP;
+  if (!counts || !slot_of || !expert_of || !hand || !miss_list || !miss_slot || !stats || !dev_status)
+    return MOE_EINVAL;
+  if (!a4(counts) || !a4(slot_of) || !a4(expert_of) || !a4(hand) || !a4(miss_list) || !a4(miss_slot) || !a4(stats) ||
+      !a4(dev_status))
+    return MOE_EINVAL;
+  return cuda_status(moe::launch_cache_plan(counts, E, slot_of, expert_of, S, hand, miss_list, miss_slot, stats,
+                                            dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_cache_fetch(const void* host_gateup, const void* host_down, size_t rec_gateup, size_t rec_down,
+                           const int32_t* miss_list, const int32_t* miss_slot, const int32_t* stats, void* pool_gateup,
+                           void* pool_down, void* stream) {
+  if (rec_gateup == 0 || rec_down == 0 || rec_gateup % 16 != 0 || rec_down % 16 != 0) return MOE_ESHAPE;
+  if (!host_gateup || !host_down || !miss_list || !miss_slot || !stats || !pool_gateup || !pool_down)
+    return MOE_EINVAL;
+  if (!a16(host_gateup) || !a16(host_down) || !a16(pool_gateup) || !a16(pool_down) || !a4(miss_list) ||
+      !a4(miss_slot) || !a4(stats))
+    return MOE_EINVAL;
+  return cuda_status(moe::launch_cache_fetch(host_gateup, host_down, rec_gateup, rec_down, miss_list, miss_slot,
+                                             stats, pool_gateup, pool_down, static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_pack_size(int fmt_in, int E, int H, int I, int which) {

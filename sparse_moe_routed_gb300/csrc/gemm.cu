@@ -533,9 +533,68 @@ struct FusedArgs {
   uint16_t* x_perm;
   const int32_t* perm;
   int k;
+  // Expert cache (CACHED kernels): expert e's records are record slot_of[e]
+  // of tiles_gu / tiles_dn, pools of S records in HBM.
+  const int32_t* slot_of;
+  int S;
+  // In-launch fetch (CACHED kernels, stats != nullptr): four more warps per
+  // CTA copy the planned misses' records from host memory (host_gu /
+  // host_dn, reached over the CPU-GPU link) into their slots in kFetchChunk
+  // pieces, in wave order, while the other warps compute; the producer of a
+  // missing expert's tile waits until that record has landed.  Sync words:
+  // ready[E + 2] is the fetch queue, ready[E + 3 + 2e + c] counts landed
+  // pieces of expert e's gate/up (c = 0) or down (c = 1) record.
+  const uint8_t* host_gu;
+  const uint8_t* host_dn;
+  uint8_t* pool_gu;
+  uint8_t* pool_dn;
+  size_t rec_gu, rec_dn;  // record bytes
+  int nch_gu, nch_dn;     // pieces per record
+  const int32_t* miss_list;
+  const int32_t* miss_slot;
+  const int32_t* stats;   // [1]: number of misses
+  int wave;               // wave width in experts
 };
 
-template <int NMAX, int GG>
+constexpr int kFetchWarps = 4;
+constexpr int kFetchChunk = 32768;
+
+// The n-th piece of the fetch plan in wave order (wave width W experts, cg /
+// cd pieces per gate/up / down record): the gate/up records of wave 0, then
+// for each later wave w its gate/up records followed by the down records of
+// wave w - 1, then the down records of the last wave.  Gate/up arrive first
+// because down is needed only once the SwiGLU intermediate exists.
+struct FetchItem {
+  int m, comp, c;  // miss index, 0 gate/up or 1 down, piece
+};
+
+__device__ __forceinline__ FetchItem fetch_item(int q, int n, int W, int cg, int cd) {
+  const int nw = (n + W - 1) / W;
+  const int L = n - (nw - 1) * W;  // experts in the last wave
+  if (nw == 1) {
+    if (q < n * cg) return {q / cg, 0, q % cg};
+    q -= n * cg;
+    return {q / cd, 1, q % cd};
+  }
+  if (q < W * cg) return {q / cg, 0, q % cg};
+  q -= W * cg;
+  const int bf = W * (cg + cd), nf = nw - 2;  // full waves 1 .. nw-2
+  if (q < nf * bf) {
+    const int w = 1 + q / bf;
+    int r = q - (w - 1) * bf;
+    if (r < W * cg) return {w * W + r / cg, 0, r % cg};
+    r -= W * cg;
+    return {(w - 1) * W + r / cd, 1, r % cd};
+  }
+  q -= nf * bf;
+  if (q < L * cg) return {(nw - 1) * W + q / cg, 0, q % cg};
+  q -= L * cg;
+  if (q < W * cd) return {(nw - 2) * W + q / cd, 1, q % cd};
+  q -= W * cd;
+  return {(nw - 1) * W + q / cd, 1, q % cd};
+}
+
+template <int NMAX, int GG, bool CACHED>
 struct CfgF {
   static constexpr int G = GG;
   static constexpr int kBBytes = NMAX * kBK * 2;
@@ -544,7 +603,8 @@ struct CfgF {
   static constexpr int kStages = kBudget / kStageBytes < 2 ? 2 : (kBudget / kStageBytes > 10 ? 10 : kBudget / kStageBytes);
   static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
   static constexpr int kNumBars = 2 * kStages + 5;
-  static constexpr int kTail = 16 + 3 * (kMaxE + 1) * 4;
+  // offsets and the two tile prefixes; cached: also slots and the expert order
+  static constexpr int kTail = 16 + (CACHED ? 5 : 3) * (kMaxE + 1) * 4;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + kTail;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -561,7 +621,8 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 
 struct FTile {
   int kind;  // 0 gate/up, 1 down
-  int e, mb, row0, nrows;
+  int j, e;  // position in the expert order, expert
+  int mb, row0, nrows;
 };
 
 // The tiles one CTA runs, in order: its round-robin share of the gate/up
@@ -595,11 +656,12 @@ struct FSeq {
   }
 };
 
-template <int NMAX, int GG>
-__global__ void __launch_bounds__(kCoreThreads, 1)
+template <int NMAX, int GG, bool CACHED>
+__global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0), 1)
     grouped_swiglu_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmH,
                                 FusedArgs p) {
-  using C = CfgF<NMAX, GG>;
+  using C = CfgF<NMAX, GG, CACHED>;
+  constexpr int kThreads = kCoreThreads + (CACHED ? 32 * kFetchWarps : 0);
   constexpr int S = C::kStages;
   constexpr int G = C::G;
   extern __shared__ uint8_t smem_raw[];
@@ -616,6 +678,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
   int* pre_gu = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
   int* pre_dn = pre_gu + (kMaxE + 1);
   int* soff = pre_dn + (kMaxE + 1);
+  int* sslot = soff + (kMaxE + 1);  // cached: slot of each expert
+  int* eord = sslot + (kMaxE + 1);  // cached: expert at each position of the tile order
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -643,6 +707,29 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
   pdl_wait();
   pdl_trigger();
   for (int i = threadIdx.x; i <= E; i += blockDim.x) soff[i] = min(max(p.offsets[i], 0), p.R);
+  int nmiss = 0;
+  if constexpr (CACHED) {
+    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+      int rec = p.slot_of[i];
+      // a routed expert without a slot (the cache could not hold the call):
+      // flag it and read slot 0, so every access stays inside the pool
+      if (rec < 0 || rec >= p.S) {
+        if (p.offsets[i + 1] > p.offsets[i]) set_status(p.status, MOE_DEV_CACHE_FULL);
+        rec = 0;
+      }
+      sslot[i] = rec;
+      eord[i] = i;
+      pre_dn[i] = -1;  // fetch-plan position of each expert until the prefix pass
+    }
+    if (p.stats != nullptr) {
+      nmiss = min(max(p.stats[1], 0), min(E, p.S));
+      __syncthreads();
+      for (int m = threadIdx.x; m < nmiss; m += blockDim.x) {
+        const int e = p.miss_list[m];
+        if (e >= 0 && e < E) pre_dn[e] = m;
+      }
+    }
+  }
   if (p.x != nullptr) {
     // this CTA's contiguous share of the permuted token rows, eight 16-byte
     // loads in flight per thread
@@ -651,12 +738,12 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     const int vpr = p.H / 8;
     const int n = (s1 - s0) * vpr;
     constexpr int U = 8;
-    for (int i0 = threadIdx.x; i0 < n; i0 += U * kCoreThreads) {
+    for (int i0 = threadIdx.x; i0 < n; i0 += U * kThreads) {
       uint4 v[U];
       int dst[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * kCoreThreads;
+        const int i = i0 + u * kThreads;
         dst[u] = -1;
         if (i < n) {
           const int sl = s0 + i / vpr;
@@ -681,11 +768,33 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
   }
   __syncthreads();
   if (warp == 0) {
+    if (CACHED && nmiss > 0) {
+      // tile order: the experts that are resident (ID order), then the ones
+      // being fetched, in fetch-plan order, so resident experts compute while
+      // the records of the others are in flight
+      int run = 0;
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const int mp = e < E ? pre_dn[e] : 0;
+        const bool keep = e < E && mp < 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          eord[run + __popc(bal & ((1u << lane) - 1u))] = e;
+        } else if (e < E) {
+          eord[E - nmiss + mp] = e;
+        }
+        run += __popc(bal);
+      }
+      __syncwarp();
+    }
     int run_gu = 0, run_dn = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
+      const int j = e0 + lane;
       int n = 0;
-      if (e < E) n = max(soff[e + 1] - soff[e], 0);
+      if (j < E) {
+        const int e = CACHED ? eord[j] : j;
+        n = max(soff[e + 1] - soff[e], 0);
+      }
       const int chunks = (n + NMAX - 1) / NMAX;
       int a = chunks * p.mb_gu, b = chunks * p.mb_dn;
       int ia = a, ib = b;
@@ -698,9 +807,10 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
           ib += yb;
         }
       }
-      if (e < E) {
-        pre_gu[e] = run_gu + ia - a;
-        pre_dn[e] = run_dn + ib - b;
+      __syncwarp();
+      if (j < E) {
+        pre_gu[j] = run_gu + ia - a;
+        pre_dn[j] = run_dn + ib - b;
       }
       run_gu += __shfl_sync(0xffffffffu, ia, 31);
       run_dn += __shfl_sync(0xffffffffu, ib, 31);
@@ -730,9 +840,10 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     }
     const int local = tt - pre[lo];
     const int chunk = local / mbk;
-    const int start = soff[lo];
-    const int len = max(soff[lo + 1] - start, 0);
-    tl.e = lo;
+    tl.j = lo;
+    tl.e = CACHED ? eord[lo] : lo;
+    const int start = soff[tl.e];
+    const int len = max(soff[tl.e + 1] - start, 0);
     tl.mb = local - chunk * mbk;
     tl.row0 = start + chunk * NMAX;
     tl.nrows = min(NMAX, len - chunk * NMAX);
@@ -750,6 +861,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     uint32_t ph = 0;
     bool ok = true;
     int ready_e = -1;  // expert whose h rows are known to be complete
+    int landed_e[2] = {-1, -1};  // expert whose fetched gate/up / down record is known to have landed
     // Until every CTA has gathered its token rows, stages get their weight
     // chunk at once and their token rows later (at most S stages deferred).
     bool gathered = p.x == nullptr;
@@ -797,7 +909,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
       if (tl.kind && tl.e != ready_e) {
         // wait until every gate/up tile of expert e has stored its h rows
         // (each tile's four epilogue warps arrive once)
-        const int target = 4 * (pre_gu[tl.e + 1] - pre_gu[tl.e]);
+        const int target = 4 * (pre_gu[tl.j + 1] - pre_gu[tl.j]);
         uint64_t t0 = 0;
         for (uint32_t it = 0; ld_acquire_gpu(p.ready + tl.e) < target; ++it) {
           __nanosleep(64);
@@ -821,7 +933,35 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         fence_proxy_async_global();
         ready_e = tl.e;
       }
-      const size_t chunk0 = (static_cast<size_t>(tl.e) * (tl.kind ? p.mb_dn : p.mb_gu) + tl.mb) * KS;
+      if (CACHED && tl.j >= E - nmiss && landed_e[tl.kind] != tl.e) {
+        // a missing expert: wait until the fetch warps have copied its record
+        const int* word = p.ready + E + 3 + 2 * tl.e + tl.kind;
+        const int target = tl.kind ? p.nch_dn : p.nch_gu;
+        uint64_t t0 = 0;
+        for (uint32_t it = 0; ld_acquire_gpu(word) < target; ++it) {
+          __nanosleep(64);
+          if ((it & 1023u) == 1023u) {
+            if (misc[1]) {
+              ok = false;
+              break;
+            }
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+              t0 = now;
+            } else if (now - t0 > kWaitNs) {
+              misc[1] = 1;
+              set_status(p.status, MOE_DEV_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (!ok) break;
+        fence_proxy_async_global();
+        landed_e[tl.kind] = tl.e;
+      }
+      const int rec = CACHED ? sslot[tl.e] : tl.e;
+      const size_t chunk0 = (static_cast<size_t>(rec) * (tl.kind ? p.mb_dn : p.mb_gu) + tl.mb) * KS;
       for (int ks = 0; ks < KS; ks += G) {
         if (!wait_bounded<kSpin>(empty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
           ok = false;
@@ -908,7 +1048,7 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
       ptx::umma_commit(drain);
       wait_drain(drain, 0);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
@@ -966,6 +1106,48 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
         aph ^= 1u;
       }
     }
+  } else if (CACHED && warp >= 6) {
+    // ------------------------------------------------------------ fetch
+    // Each warp claims the next piece of the plan, copies it host -> slot with
+    // eight 16-byte loads in flight per lane, fences its stores for the TMA
+    // reads of other CTAs, and counts the piece as landed.
+    const int n = nmiss;
+    if (n > 0) {
+      const int W = max(1, min(p.wave, n));
+      const int total = n * (p.nch_gu + p.nch_dn);
+      for (;;) {
+        int q = 0;
+        if (lane == 0) q = atomicAdd(p.ready + E + 2, 1);
+        q = __shfl_sync(0xffffffffu, q, 0);
+        if (q >= total) break;
+        const FetchItem f = fetch_item(q, n, W, p.nch_gu, p.nch_dn);
+        const int e = p.miss_list[f.m], sl = p.miss_slot[f.m];
+        const bool valid = e >= 0 && e < E && sl >= 0 && sl < p.S;
+        if (valid) {
+          const size_t rec = f.comp ? p.rec_dn : p.rec_gu;
+          const size_t off = static_cast<size_t>(f.c) * kFetchChunk;
+          const int nv = static_cast<int>(min(rec - off, static_cast<size_t>(kFetchChunk)) / 16);
+          const uint4* src = reinterpret_cast<const uint4*>((f.comp ? p.host_dn : p.host_gu) + e * rec + off);
+          uint4* dst = reinterpret_cast<uint4*>((f.comp ? p.pool_dn : p.pool_gu) + sl * rec + off);
+          constexpr int U = 8;
+          for (int i0 = lane; i0 < nv; i0 += U * 32) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+              if (i0 + u * 32 < nv) v[u] = src[i0 + u * 32];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+              if (i0 + u * 32 < nv) dst[i0 + u * 32] = v[u];
+          }
+          fence_proxy_async_global();
+        } else if (lane == 0) {
+          set_status(p.status, MOE_DEV_BAD_EXPERT);
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0 && valid) atomicAdd(p.ready + E + 3 + 2 * e + f.comp, 1);
+      }
+    }
   }
 
   ptx::tc_fence_before();
@@ -982,7 +1164,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
   __syncthreads();
   if (misc[2]) {
     __threadfence();
-    for (int e = threadIdx.x; e < E + 2; e += blockDim.x) p.ready[e] = 0;
+    const int nsync = CACHED ? 3 * E + 3 : E + 2;
+    for (int e = threadIdx.x; e < nsync; e += blockDim.x) p.ready[e] = 0;
     __threadfence();
   }
 }
@@ -1726,23 +1909,24 @@ cudaError_t run_fmt(int fmt, int nmax, const CUtensorMap& a, const CUtensorMap& 
 }
 
 
-template <int NMAX, int GG>
+template <int NMAX, int GG, bool CACHED>
 cudaError_t run_fused(const CUtensorMap& mx, const CUtensorMap& mh, const FusedArgs& args, cudaStream_t st) {
-  using C = CfgF<NMAX, GG>;
-  auto kern = grouped_swiglu_fused_kernel<NMAX, GG>;
+  using C = CfgF<NMAX, GG, CACHED>;
+  auto kern = grouped_swiglu_fused_kernel<NMAX, GG, CACHED>;
   cudaError_t e = ensure_smem(kern, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = sm_count();
   if (grid <= 0) return cudaErrorNoDevice;
-  return launch_pdl(kern, dim3(grid), dim3(kCoreThreads), C::kSmemBytes, st, mx, mh, args);
+  return launch_pdl(kern, dim3(grid), dim3(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)), C::kSmemBytes, st, mx,
+                    mh, args);
 }
 
 }  // namespace
 
 cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
                                 const int32_t* offsets, int E, int R, int H, int I, const void* w_gateup,
-                                const void* w_down, uint16_t* h, float* y, int32_t* ready, int32_t* st_word,
-                                cudaStream_t st) {
+                                const void* w_down, const FusedCache* cache, uint16_t* h, float* y, int32_t* ready,
+                                int32_t* st_word, cudaStream_t st) {
   CUtensorMap mx, mh;
   if (!make_rows_map(&mx, x_perm, H, R, kBoxRows)) return cudaErrorInvalidValue;
   if (!make_rows_map(&mh, h, I, R, kBoxRows)) return cudaErrorInvalidValue;
@@ -1766,19 +1950,45 @@ cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, u
   a.x_perm = x_perm;
   a.perm = perm;
   a.k = k > 0 ? k : 1;
+  if (cache != nullptr) {
+    // slot pools; with host records the launch also fetches the planned misses
+    if (a.ks_gu % 2 != 0 || a.ks_dn % 2 != 0) return cudaErrorNotSupported;
+    a.slot_of = cache->slot_of;
+    a.S = cache->S;
+    if (cache->host_gu != nullptr) {
+      a.host_gu = static_cast<const uint8_t*>(cache->host_gu);
+      a.host_dn = static_cast<const uint8_t*>(cache->host_dn);
+      a.pool_gu = static_cast<uint8_t*>(const_cast<void*>(w_gateup));
+      a.pool_dn = static_cast<uint8_t*>(const_cast<void*>(w_down));
+      a.rec_gu = static_cast<size_t>(4) * I * H;
+      a.rec_dn = static_cast<size_t>(2) * I * H;
+      a.nch_gu = static_cast<int>((a.rec_gu + kFetchChunk - 1) / kFetchChunk);
+      a.nch_dn = static_cast<int>((a.rec_dn + kFetchChunk - 1) / kFetchChunk);
+      a.miss_list = cache->miss_list;
+      a.miss_slot = cache->miss_slot;
+      a.stats = cache->stats;
+      a.wave = cache->wave;
+    }
+    switch (pick_nmax(R)) {
+      case 16: return run_fused<16, 2, true>(mx, mh, a, st);
+      case 32: return run_fused<32, 2, true>(mx, mh, a, st);
+      case 64: return run_fused<64, 2, true>(mx, mh, a, st);
+      default: return run_fused<128, 2, true>(mx, mh, a, st);
+    }
+  }
   if (a.ks_gu % 2 == 0 && a.ks_dn % 2 == 0) {
     switch (pick_nmax(R)) {
-      case 16: return run_fused<16, 2>(mx, mh, a, st);
-      case 32: return run_fused<32, 2>(mx, mh, a, st);
-      case 64: return run_fused<64, 2>(mx, mh, a, st);
-      default: return run_fused<128, 2>(mx, mh, a, st);
+      case 16: return run_fused<16, 2, false>(mx, mh, a, st);
+      case 32: return run_fused<32, 2, false>(mx, mh, a, st);
+      case 64: return run_fused<64, 2, false>(mx, mh, a, st);
+      default: return run_fused<128, 2, false>(mx, mh, a, st);
     }
   }
   switch (pick_nmax(R)) {
-    case 16: return run_fused<16, 1>(mx, mh, a, st);
-    case 32: return run_fused<32, 1>(mx, mh, a, st);
-    case 64: return run_fused<64, 1>(mx, mh, a, st);
-    default: return run_fused<128, 1>(mx, mh, a, st);
+    case 16: return run_fused<16, 1, false>(mx, mh, a, st);
+    case 32: return run_fused<32, 1, false>(mx, mh, a, st);
+    case 64: return run_fused<64, 1, false>(mx, mh, a, st);
+    default: return run_fused<128, 1, false>(mx, mh, a, st);
   }
 }
 

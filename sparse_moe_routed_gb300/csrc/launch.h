@@ -65,6 +65,14 @@ cudaError_t launch_route_permute(const uint16_t* x, const uint16_t* wr, const fl
                                  int32_t* ids, float* w, float* gap, int32_t* counts, int32_t* offsets, int32_t* perm,
                                  int32_t* inv, int32_t* st_word, cudaStream_t st);
 
+// cache.cu
+cudaError_t launch_cache_plan(const int32_t* counts, int E, int32_t* slot_of, int32_t* expert_of, int S,
+                              int32_t* hand, int32_t* miss_list, int32_t* miss_slot, int32_t* stats,
+                              int32_t* st_word, cudaStream_t st);
+cudaError_t launch_cache_fetch(const void* host_gu, const void* host_dn, size_t rec_gu, size_t rec_dn,
+                               const int32_t* miss_list, const int32_t* miss_slot, const int32_t* stats,
+                               void* pool_gu, void* pool_dn, cudaStream_t st);
+
 // permute.cu
 cudaError_t launch_permute(const int32_t* ids, int R, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* st_word,
@@ -89,10 +97,22 @@ cudaError_t launch_pack(int fmt_in, const void* w, const uint16_t* s, int E, int
 
 // Gate/up + SwiGLU + down in one persistent launch (tile-packed bf16).
 // With x set, the launch first gathers x_perm[s] = x[perm[s] / k] itself.
+// With cache set, w_gateup / w_down are slot pools read through slot_of;
+// with cache->host_gu also set, the launch fetches the planned misses itself.
+struct FusedCache {
+  const int32_t* slot_of;
+  int S;
+  const void* host_gu;
+  const void* host_dn;
+  const int32_t* miss_list;
+  const int32_t* miss_slot;
+  const int32_t* stats;
+  int wave;
+};
 cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
                                 const int32_t* offsets, int E, int R, int H, int I, const void* w_gateup,
-                                const void* w_down, uint16_t* h, float* y, int32_t* ready, int32_t* st_word,
-                                cudaStream_t st);
+                                const void* w_down, const FusedCache* cache, uint16_t* h, float* y, int32_t* ready,
+                                int32_t* st_word, cudaStream_t st);
 
 // combine.cu
 cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int k, int H,

@@ -16,6 +16,10 @@ which for a decode-sized block also gathers the token rows itself:
 (`ROUTE_PERMUTE_ONE_LAUNCH` switches a decode block to moe_route_permute,
 which routes and groups in one launch.)
 
+``CachedMoELayer`` keeps the expert records in pinned host memory behind an
+HBM slot cache and adds moe_cache_plan (and, copy-first, moe_cache_fetch)
+before moe_expert_swiglu_cached.
+
 Every step runs in the CUDA library; this class only owns memory.
 """
 from __future__ import annotations
@@ -133,10 +137,7 @@ class MoELayer:
                           (P(self.ids), T, k, E, P(x), H, P(self.counts), P(self.offsets), P(self.perm),
                            P(self.inv), P(self.x_perm), P(self.status), st)))
         if self.fused:
-            calls.append(("moe_expert_swiglu_fused", lib.moe_expert_swiglu_fused,
-                          (P(x) if gather_in_fused else None, k, P(self.perm), P(self.x_perm), P(self.offsets), R,
-                           E, H, I, self.fmt, P(self.w_gateup), P(self.w_down), P(self.h), P(self.y_perm),
-                           P(self.sync_ws), P(self.status), st)))
+            calls += self._expert_calls(lib, P, x if gather_in_fused else None, R, st)
         else:
             calls += [
                 ("moe_expert_gateup", lib.moe_expert_gateup,
@@ -152,6 +153,12 @@ class MoELayer:
         ]
         self._bound[key] = calls
         return calls
+
+    def _expert_calls(self, lib, P, x_gather, R, st):
+        return [("moe_expert_swiglu_fused", lib.moe_expert_swiglu_fused,
+                 (P(x_gather), self.k, P(self.perm), P(self.x_perm), P(self.offsets), R, self.E, self.H, self.I,
+                  self.fmt, P(self.w_gateup), P(self.w_down), P(self.h), P(self.y_perm), P(self.sync_ws),
+                  P(self.status), st))]
 
     @staticmethod
     def issue(call):
@@ -234,6 +241,72 @@ class MoELayer:
         which a launch that gave up on a wait may have left non-zero)."""
         self.status.zero_()
         self.sync_ws.zero_()
+
+
+class CachedMoELayer(MoELayer):
+    """A layer whose expert records live in host memory behind an HBM cache.
+
+    host_gateup / host_down: the tile-packed bf16 records (moe_pack_experts
+    output, MOE_W_BF16_TILED) of all E experts in pinned host memory, which
+    the GPU reads directly over the CPU-GPU link.  S slots of HBM hold recently
+    used experts.  Each call plans hits and misses on the device
+    (moe_cache_plan) and then either fetches the misses in the expert launch
+    itself, in waves of `wave` experts while the resident experts compute
+    (fetch="wave"), or copies them first with moe_cache_fetch and computes
+    after (fetch="barrier").  Outputs are bit-identical to MoELayer over the
+    same records in HBM.
+
+        moe_route -> moe_permute -> moe_cache_plan [-> moe_cache_fetch] ->
+        moe_expert_swiglu_cached -> moe_combine
+
+    stats [4] int32 on the device: {hits, misses} of the last call and their
+    running totals.
+    """
+
+    def __init__(self, w_router, bias, host_gateup, host_down, k: int, T_max: int, I: int, S: int,
+                 wave: int = 1 << 20, fetch: str = "wave"):
+        assert not host_gateup.is_cuda and host_gateup.is_pinned() and host_down.is_pinned()
+        assert fetch in ("wave", "barrier")
+        super().__init__(w_router, bias, host_gateup, host_down, k, T_max, fmt=_lib.MOE_W_BF16_TILED, I=I)
+        E, H = self.E, self.H
+        dev = w_router.device
+        self.S, self.wave, self.fetch = S, wave, fetch
+        self.rec_gu = host_gateup.numel() * host_gateup.element_size() // E
+        self.rec_dn = host_down.numel() * host_down.element_size() // E
+        self.pool_gu = torch.empty((S * self.rec_gu,), dtype=torch.uint8, device=dev)
+        self.pool_dn = torch.empty((S * self.rec_dn,), dtype=torch.uint8, device=dev)
+        self.slot_of = torch.full((E,), -1, dtype=torch.int32, device=dev)
+        self.expert_of = torch.full((S,), -1, dtype=torch.int32, device=dev)
+        self.hand = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self.miss_list = torch.zeros((S,), dtype=torch.int32, device=dev)
+        self.miss_slot = torch.zeros((S,), dtype=torch.int32, device=dev)
+        self.stats = torch.zeros((4,), dtype=torch.int32, device=dev)
+        self.sync_ws = torch.zeros((3 * E + 3,), dtype=torch.int32, device=dev)
+
+    def reset_cache(self):
+        """Empty the cache and zero the running totals."""
+        self.slot_of.fill_(-1)
+        self.expert_of.fill_(-1)
+        self.hand.zero_()
+        self.stats.zero_()
+
+    def _expert_calls(self, lib, P, x_gather, R, st):
+        E, H, I, S = self.E, self.H, self.I, self.S
+        calls = [("moe_cache_plan", lib.moe_cache_plan,
+                  (P(self.counts), E, P(self.slot_of), P(self.expert_of), S, P(self.hand), P(self.miss_list),
+                   P(self.miss_slot), P(self.stats), P(self.status), st))]
+        wave = self.fetch == "wave"
+        if not wave:
+            calls.append(("moe_cache_fetch", lib.moe_cache_fetch,
+                          (P(self.w_gateup), P(self.w_down), self.rec_gu, self.rec_dn, P(self.miss_list),
+                           P(self.miss_slot), P(self.stats), P(self.pool_gu), P(self.pool_dn), st)))
+        calls.append(("moe_expert_swiglu_cached", lib.moe_expert_swiglu_cached,
+                      (P(x_gather), self.k, P(self.perm), P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt,
+                       P(self.pool_gu), P(self.pool_dn), S, P(self.slot_of),
+                       P(self.w_gateup) if wave else None, P(self.w_down) if wave else None,
+                       P(self.miss_list), P(self.miss_slot), P(self.stats), self.wave, P(self.h), P(self.y_perm),
+                       P(self.sync_ws), P(self.status), st)))
+        return calls
 
 
 class MoEStack:

@@ -26,7 +26,7 @@ def lib():
 def test_library_loads_and_exports_every_declared_symbol():
     L = lib()
     names = _lib.declared_functions()
-    assert len(names) == 18
+    assert len(names) == 21
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 100
@@ -228,3 +228,66 @@ def test_route_permute_rejections():
     assert call(0, PM) == _lib.MOE_EINVAL
     assert call(6, 40) == _lib.MOE_ENOTSUP        # k > 32
     assert call(4, 2500) == _lib.MOE_ENOTSUP      # H % 128
+
+
+def test_cache_plan_and_fetch_rejections():
+    L = lib()
+    # counts, E, slot_of, expert_of, S, hand, miss_list, miss_slot, stats, status, stream
+    base = [P, 512, P, P, 256, P, P, P, P, P, NUL]
+
+    def plan(i, v):
+        a = list(base)
+        a[i] = v
+        return L.moe_cache_plan(*a)
+
+    assert plan(4, 0) == _lib.MOE_ESHAPE
+    assert plan(1, 0) == _lib.MOE_ESHAPE
+    assert plan(4, 1025) == _lib.MOE_ENOTSUP     # one CTA plans at most 1024 slots
+    assert plan(1, 1025) == _lib.MOE_ENOTSUP
+    for i in (0, 2, 3, 5, 6, 7, 8, 9):
+        assert plan(i, NUL) == _lib.MOE_EINVAL, i
+    assert plan(2, PM) == _lib.MOE_EINVAL
+    assert plan(4, 256) == _lib.MOE_ECUDA         # admitted; no device here
+
+    # host_gu, host_dn, rec_gu, rec_dn, miss_list, miss_slot, stats, pool_gu, pool_dn, stream
+    fbase = [P, P, 6553600, 3276800, P, P, P, P, P, NUL]
+
+    def fetch(i, v):
+        a = list(fbase)
+        a[i] = v
+        return L.moe_cache_fetch(*a)
+
+    assert fetch(2, 0) == _lib.MOE_ESHAPE
+    assert fetch(3, 8) == _lib.MOE_ESHAPE           # records are whole 16-byte units
+    for i in (0, 1, 4, 5, 6, 7, 8):
+        assert fetch(i, NUL) == _lib.MOE_EINVAL, i
+    assert fetch(0, PM) == _lib.MOE_EINVAL
+
+
+def test_swiglu_cached_rejections():
+    L = lib()
+    names = ["x", "k", "perm", "xp", "off", "R", "E", "H", "I", "fmt", "pgu", "pdn", "S", "slot", "hgu", "hdn",
+             "ml", "ms", "stats", "wave", "h", "y", "sync", "st"]
+    base = [NUL, 0, NUL, P, P, 160, 512, 2560, 640, _lib.MOE_W_BF16_TILED, P, P, 256, P, P, P, P, P, P, 4, P, P,
+            P, P, NUL]
+
+    def call(**kw):
+        a = list(base)
+        for n, v in kw.items():
+            a[names.index(n)] = v
+        return L.moe_expert_swiglu_cached(*a)
+
+    assert call(fmt=_lib.MOE_W_INT4_G64_TILED) == _lib.MOE_ENOTSUP
+    assert call(S=0) == _lib.MOE_ESHAPE
+    assert call(S=2000) == _lib.MOE_ENOTSUP
+    assert call(slot=NUL) == _lib.MOE_EINVAL
+    assert call(slot=PM) == _lib.MOE_EINVAL
+    assert call(wave=0) == _lib.MOE_ESHAPE
+    assert call(hgu=NUL, wave=0) == _lib.MOE_ECUDA   # no fetch: wave unused; admitted
+    for n in ("hdn", "ml", "ms", "stats"):
+        assert call(**{n: NUL}) == _lib.MOE_EINVAL, n
+    assert call(hgu=PM) == _lib.MOE_EINVAL
+    assert call(I=704) == _lib.MOE_ENOTSUP          # I/64 odd: the cached kernel steps K in pairs
+    assert call(hgu=NUL, I=704) == _lib.MOE_ENOTSUP
+    assert call(sync=NUL) == _lib.MOE_EWORKSPACE
+    assert call(R=0) == _lib.MOE_OK

@@ -1,0 +1,209 @@
+"""GPU checks of the expert cache: moe_cache_plan, moe_cache_fetch,
+moe_expert_swiglu_cached and CachedMoELayer.
+
+Every expert's tile-packed records sit in pinned host memory and S slots of
+HBM cache them.  Moving records is byte work and each tile's arithmetic is
+unchanged, so a cached layer must return, bit for bit, what MoELayer returns
+over the same records resident in HBM -- call after call, as experts hit,
+miss and are evicted, for every wave width of the in-launch fetch and for the
+copy-first path.  The plan itself is integer work and is compared exactly
+with a plain host model of the same replacement rule (FIFO over the slots
+not pinned by the call's routes).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from sparse_moe_routed_gb300 import CachedMoELayer, MoELayer, _lib, pack_layer_experts
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+# I/64 even: the in-launch fetch runs on the paired-K-step contraction
+SMALL = wl.LayerConfig("cache_small", T=8, H=256, E=64, k=4, I=128, bias=None, seed=21)
+WIDE = wl.LayerConfig("cache_wide", T=16, H=256, E=512, k=10, I=128, bias=None, seed=22)
+QWEN64 = wl.LayerConfig("cache_qwen64", T=4, H=2560, E=64, k=10, I=640, bias=None, seed=23)
+
+
+# ----------------------------------------------------------------- plan
+def plan_model(counts, slot_of, expert_of, hand, S):
+    """The replacement rule, written out on the host."""
+    E = len(counts)
+    routed = [e for e in range(E) if counts[e] > 0]
+    hits = [e for e in routed if slot_of[e] >= 0]
+    misses = [e for e in routed if slot_of[e] < 0]
+    order = [(hand + i) % S for i in range(S)]
+    free = [s for s in order if not (expert_of[s] >= 0 and counts[expert_of[s]] > 0)]
+    if len(misses) > len(free):
+        return True, [], [], hand, (len(hits), 0)
+    victims = free[:len(misses)]
+    for e, v in zip(misses, victims):
+        if expert_of[v] >= 0:
+            slot_of[expert_of[v]] = -1
+    for e, v in zip(misses, victims):
+        slot_of[e] = v
+        expert_of[v] = e
+    if misses:
+        hand = (victims[-1] + 1) % S
+    return False, misses, victims, hand, (len(hits), len(misses))
+
+
+@pytest.mark.parametrize("E,S,T,k", [(64, 24, 4, 4), (512, 200, 16, 10), (1024, 1024, 64, 10), (64, 1, 1, 1)])
+def test_plan_matches_host_model(E, S, T, k):
+    rng = np.random.default_rng(E + S)
+    slot_of = torch.full((E,), -1, dtype=torch.int32, device=DEV)
+    expert_of = torch.full((S,), -1, dtype=torch.int32, device=DEV)
+    hand = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    ml = torch.zeros((S,), dtype=torch.int32, device=DEV)
+    ms = torch.zeros((S,), dtype=torch.int32, device=DEV)
+    stats = torch.zeros((4,), dtype=torch.int32, device=DEV)
+    m_slot, m_exp, m_hand = [-1] * E, [-1] * S, 0
+    tot = [0, 0]
+    saw_full = saw_evict = False
+    for call in range(40):
+        st = torch.zeros((1,), dtype=torch.int32, device=DEV)
+        # a hot set of experts makes hits; now and then a call routes more
+        # experts than the cache holds
+        Tc = T * 8 if call % 13 == 12 else T
+        hot = rng.choice(E, size=max(2 * k, E // 8), replace=False)
+        cnt = np.zeros(E, dtype=np.int32)
+        for _ in range(Tc):
+            pool = hot if rng.random() < 0.6 else np.arange(E)
+            for e in rng.choice(pool, size=min(k, len(pool)), replace=False):
+                cnt[e] += 1
+        counts = torch.from_numpy(cnt).to(DEV)
+        _lib.moe_cache_plan(counts, slot_of, expert_of, hand, ml, ms, stats, st)
+        torch.cuda.synchronize()
+        before_exp = list(m_exp)
+        full, misses, victims, m_hand, (nh, nm) = plan_model(cnt.tolist(), m_slot, m_exp, m_hand, S)
+        tot[0] += nh
+        tot[1] += nm
+        saw_full |= full
+        saw_evict |= any(before_exp[v] >= 0 for v in victims)
+        assert int(st.item()) == (_lib.MOE_DEV_CACHE_FULL if full else 0), call
+        s = stats.cpu().tolist()
+        assert s == [nh, nm, tot[0], tot[1]], call
+        assert slot_of.cpu().tolist() == m_slot, call
+        assert expert_of.cpu().tolist() == m_exp, call
+        assert int(hand.item()) == m_hand, call
+        assert ml[:nm].cpu().tolist() == misses, call
+        assert ms[:nm].cpu().tolist() == victims, call
+        # invariants: a bijection between cached experts and filled slots;
+        # after a call that fit, every routed expert has a slot
+        for e, v in enumerate(m_slot):
+            if v >= 0:
+                assert m_exp[v] == e
+        if not full:
+            assert all(m_slot[e] >= 0 for e in np.nonzero(cnt)[0])
+    if S < E and S > k:
+        assert saw_evict and saw_full
+
+
+# ----------------------------------------------------------------- layer
+_L = {}
+
+
+def layers(cfg):
+    """(resident MoELayer, packed host records) for cfg."""
+    if cfg.name not in _L:
+        d = wl.layer_inputs(cfg, DEV, with_x=False)
+        gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, cfg.E, cfg.H, cfg.I)
+        torch.cuda.synchronize()
+        ref = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, cfg.T, fmt=_lib.MOE_W_BF16_TILED, I=cfg.I)
+        _L[cfg.name] = (ref, gu.cpu().pin_memory(), dn.cpu().pin_memory(), d)
+    return _L[cfg.name]
+
+
+def run_sequence(cfg, S, wave, fetch, calls=12):
+    ref, hgu, hdn, d = layers(cfg)
+    lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, cfg.T, I=cfg.I, S=S, wave=wave, fetch=fetch)
+    uniq = 0
+    for i in range(calls):
+        # repeat a few batches so that some calls hit what earlier ones loaded
+        x = wl.token_batch(cfg, DEV, index=[0, 1, 0, 2, 3, 1, 4, 0, 5, 2, 6, 0][i % 12], T=cfg.T)
+        want = ref.forward(x).clone()
+        got = lay.forward(x).clone()
+        torch.cuda.synchronize()
+        assert lay.read_status() == 0 and ref.read_status() == 0
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"call {i}"
+        uniq += int((lay.counts > 0).sum().item())
+    s = lay.stats.cpu().tolist()
+    assert s[2] + s[3] == uniq
+    return lay, s
+
+
+@pytest.mark.parametrize("wave", [1, 2, 3, 4, 1 << 20])
+def test_cached_layer_bitwise_small(wave):
+    lay, s = run_sequence(SMALL, S=40, wave=wave, fetch="wave")
+    assert s[2] > 0 and s[3] > 40          # hits, and misses beyond the first fill (evictions)
+    assert int(lay.sync_ws.abs().sum().item()) == 0  # sync words left zero
+
+
+def test_cached_layer_copy_first_small():
+    _, s = run_sequence(SMALL, S=40, wave=1, fetch="barrier")
+    assert s[2] > 0 and s[3] > 40
+
+
+@pytest.mark.parametrize("wave", [2, 1 << 20])
+def test_cached_layer_bitwise_512_experts(wave):
+    _, s = run_sequence(WIDE, S=200, wave=wave, fetch="wave", calls=8)
+    assert s[2] > 0 and s[3] > 200
+
+
+@pytest.mark.parametrize("wave,fetch", [(1, "wave"), (4, "wave"), (1 << 20, "wave"), (1, "barrier")])
+def test_cached_layer_bitwise_qwen_geometry(wave, fetch):
+    """Qwen4Exp expert shape (H 2560, I 640) over 64 experts, 40 slots."""
+    _, s = run_sequence(QWEN64, S=40, wave=wave, fetch=fetch, calls=8)
+    assert s[2] > 0 and s[3] > 40
+
+
+def test_cached_layer_host_graph():
+    """The cached layer replays from a CUDA graph like the resident one."""
+    ref, hgu, hdn, d = layers(SMALL)
+    lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, SMALL.k, SMALL.T, I=SMALL.I, S=40, wave=2)
+    xh = torch.empty((SMALL.T, SMALL.H), dtype=torch.bfloat16).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    for i in range(5):
+        x = wl.token_batch(SMALL, DEV, index=i % 3, T=SMALL.T)
+        xh.copy_(x.cpu())
+        lay.forward_host_graph(xh, oh)
+        want = ref.forward(x).cpu()
+        assert torch.equal(oh.view(torch.int16), want.view(torch.int16)), i
+    assert lay.read_status() == 0
+
+
+def test_cache_full_is_flagged_and_changes_nothing():
+    ref, hgu, hdn, d = layers(SMALL)
+    S = 4
+    lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, SMALL.k, SMALL.T, I=SMALL.I, S=S, wave=2)
+    x = wl.token_batch(SMALL, DEV, index=9, T=SMALL.T)   # 8 tokens x 4 routes: more than 4 experts
+    lay.forward(x)
+    torch.cuda.synchronize()
+    assert lay.read_status() & _lib.MOE_DEV_CACHE_FULL
+    assert lay.slot_of.eq(-1).all() and lay.expert_of.eq(-1).all() and int(lay.hand.item()) == 0
+    assert lay.stats[1].item() == 0
+    assert int(lay.sync_ws.abs().sum().item()) == 0
+
+
+def test_fetch_only_kernel_copies_records():
+    """moe_cache_fetch alone: slots receive exactly the planned records."""
+    cfg = SMALL
+    ref, hgu, hdn, d = layers(cfg)
+    S, E = 16, cfg.E
+    rg, rd = hgu.numel() // E, hdn.numel() // E
+    pgu = torch.zeros((S * rg,), dtype=torch.uint8, device=DEV)
+    pdn = torch.zeros((S * rd,), dtype=torch.uint8, device=DEV)
+    ml = torch.tensor([5, 63, 0, 17] + [0] * (S - 4), dtype=torch.int32, device=DEV)
+    ms = torch.tensor([3, 0, 15, 7] + [0] * (S - 4), dtype=torch.int32, device=DEV)
+    stats = torch.tensor([0, 4, 0, 0], dtype=torch.int32, device=DEV)
+    _lib.moe_cache_fetch(hgu, hdn, rg, rd, ml, ms, stats, pgu, pdn)
+    torch.cuda.synchronize()
+    gu_d, dn_d = pgu.cpu(), pdn.cpu()
+    for e, sl in zip([5, 63, 0, 17], [3, 0, 15, 7]):
+        assert torch.equal(gu_d[sl * rg:(sl + 1) * rg], hgu[e * rg:(e + 1) * rg])
+        assert torch.equal(dn_d[sl * rd:(sl + 1) * rd], hdn[e * rd:(e + 1) * rd])
+    untouched = [s for s in range(S) if s not in (3, 0, 15, 7)]
+    for sl in untouched:
+        assert int(gu_d[sl * rg:(sl + 1) * rg].sum()) == 0
