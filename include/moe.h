@@ -299,8 +299,9 @@ MOE_API moe_status moe_cache_fetch(const void *host_gateup, const void *host_dow
  *   misses copies every gate/up record before any down record.  The combine
  *   that follows stays in route-rank order.  Needs H/64 and I/64 even
  *   (MOE_ENOTSUP otherwise).
- *   sync_ws: [3E + 3] int32, zero before the first call; every launch leaves
- *   it zero again. */
+ *   sync_ws: [E * (1 + I/64 + H/128) + 3] int32 (per-expert readiness, and a
+ *   landed-piece counter per weight block), zero before the first call;
+ *   every launch leaves it zero again. */
 MOE_API moe_status moe_expert_swiglu_cached(const uint16_t *x, int k, const int32_t *perm, uint16_t *x_perm,
                                             const int32_t *offsets, int R, int E, int H, int I, int fmt,
                                             void *pool_gateup, void *pool_down, int S, const int32_t *slot_of,

@@ -541,9 +541,10 @@ struct FusedArgs {
   // CTA copy the planned misses' records from host memory (host_gu /
   // host_dn, reached over the CPU-GPU link) into their slots in kFetchChunk
   // pieces, in wave order, while the other warps compute; the producer of a
-  // missing expert's tile waits until that record has landed.  Sync words:
-  // ready[E + 2] is the fetch queue, ready[E + 3 + 2e + c] counts landed
-  // pieces of expert e's gate/up (c = 0) or down (c = 1) record.
+  // missing expert's tile waits until its weight block has landed.  Sync
+  // words: ready[E + 2] is the fetch queue, ready[E + 3 + e * (mb_gu + mb_dn)
+  // + b] counts the landed pieces of expert e's weight block b (gate/up
+  // blocks first, then down blocks).
   const uint8_t* host_gu;
   const uint8_t* host_dn;
   uint8_t* pool_gu;
@@ -654,14 +655,102 @@ struct FSeq {
     const int d = F + rr0 + n * P;
     return d < tdn ? tgu + d : -1;
   }
+  __device__ int count() const {
+    const int rest = tdn - F - rr0;
+    return g_b + nfill + (rest > 0 ? (rest - 1) / P + 1 : 0);
+  }
 };
+
+// With an expert cache: the tiles of the experts already resident (phase A:
+// their gate/up, then their down tiles) come before those of the experts
+// being fetched (phase B), so no CTA holds resident work behind a tile that
+// waits for the link.  Phase A is levelled as FSeq levels the whole list;
+// phase B, whose tiles wait for the link rather than for compute, gives the
+// CTAs after its gate/up tiles one down tile each before any CTA gets two.
+// Returns the index in the combined list (all gate/up tiles by position in
+// the expert order, then all down tiles), or -1.
+struct FOrder {
+  FSeq a, b;
+  int na, tguA, tdnA, tguB, total_gu;
+  __device__ FOrder(int blk, int P, int tguA_, int tdnA_, int tguB_, int tdnB_, int wg, int wd)
+      : a(blk, P, tguA_, tdnA_, wg, wd),
+        b(blk, P, tguB_, tdnB_, 1, 1),
+        na(a.count()),
+        tguA(tguA_),
+        tdnA(tdnA_),
+        tguB(tguB_),
+        total_gu(tguA_ + tguB_) {}
+  __device__ int tile(int n) const {
+    if (n < na) {
+      const int t = a.tile(n);
+      return t < tguA ? t : total_gu + (t - tguA);
+    }
+    const int t = b.tile(n - na);
+    if (t < 0) return -1;
+    return t < tguB ? tguA + t : total_gu + tdnA + (t - tguB);
+  }
+};
+
+// The fetch warps of a cached launch: each warp claims the next piece of the
+// plan, copies it host -> slot with eight 16-byte loads in flight per lane,
+// fences its stores for the TMA reads of other CTAs, and counts the piece as
+// landed in its weight block's word.
+__device__ __forceinline__ void fetch_records(const FusedArgs& p, int E, int n, int lane) {
+  if (n <= 0) return;
+  const int W = max(1, min(p.wave, n));
+  const int total = n * (p.nch_gu + p.nch_dn);
+  for (;;) {
+    int q = 0;
+    if (lane == 0) q = atomicAdd(p.ready + E + 2, 1);
+    q = __shfl_sync(0xffffffffu, q, 0);
+    if (q >= total) break;
+    const FetchItem f = fetch_item(q, n, W, p.nch_gu, p.nch_dn);
+    const int e = p.miss_list[f.m], sl = p.miss_slot[f.m];
+    const bool valid = e >= 0 && e < E && sl >= 0 && sl < p.S;
+    if (valid) {
+      const size_t rec = f.comp ? p.rec_dn : p.rec_gu;
+      const size_t off = static_cast<size_t>(f.c) * kFetchChunk;
+      const int nv = static_cast<int>(min(rec - off, static_cast<size_t>(kFetchChunk)) / 16);
+      const uint4* src = reinterpret_cast<const uint4*>((f.comp ? p.host_dn : p.host_gu) + e * rec + off);
+      uint4* dst = reinterpret_cast<uint4*>((f.comp ? p.pool_dn : p.pool_gu) + sl * rec + off);
+      constexpr int U = 8;
+      for (int i0 = lane; i0 < nv; i0 += U * 32) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (i0 + u * 32 < nv) v[u] = src[i0 + u * 32];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (i0 + u * 32 < nv) dst[i0 + u * 32] = v[u];
+      }
+      fence_proxy_async_global();
+    } else if (lane == 0) {
+      set_status(p.status, MOE_DEV_BAD_EXPERT);
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0 && valid) {
+      // pieces never straddle a weight block: a block is ks / 2 pieces
+      const int blk = f.comp ? p.mb_gu + f.c / (p.ks_dn / 2) : f.c / (p.ks_gu / 2);
+      atomicAdd(p.ready + E + 3 + e * (p.mb_gu + p.mb_dn) + blk, 1);
+    }
+  }
+}
 
 template <int NMAX, int GG, bool CACHED>
 __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0), 1)
     grouped_swiglu_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmH,
                                 FusedArgs p) {
   using C = CfgF<NMAX, GG, CACHED>;
-  constexpr int kThreads = kCoreThreads + (CACHED ? 32 * kFetchWarps : 0);
+  // the compute warps' barrier: all threads, or, with fetch warps that run
+  // on their own, a named barrier of the first kCoreThreads
+  auto compute_sync = [] {
+    if constexpr (CACHED) {
+      asm volatile("bar.sync 1, %0;" ::"n"(kCoreThreads) : "memory");
+    } else {
+      __syncthreads();
+    }
+  };
   constexpr int S = C::kStages;
   constexpr int G = C::G;
   extern __shared__ uint8_t smem_raw[];
@@ -706,10 +795,16 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
   }
   pdl_wait();
   pdl_trigger();
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) soff[i] = min(max(p.offsets[i], 0), p.R);
-  int nmiss = 0;
+  const int nmiss = (CACHED && p.stats != nullptr) ? min(max(p.stats[1], 0), min(E, p.S)) : 0;
+  if (CACHED && warp >= 6) {
+    // ------------------------------------------------------------ fetch
+    // The fetch warps start at once; the compute warps' set-up below syncs
+    // on a named barrier of their own.
+    fetch_records(p, E, nmiss, lane);
+  } else {
+  for (int i = threadIdx.x; i <= E; i += kCoreThreads) soff[i] = min(max(p.offsets[i], 0), p.R);
   if constexpr (CACHED) {
-    for (int i = threadIdx.x; i < E; i += blockDim.x) {
+    for (int i = threadIdx.x; i < E; i += kCoreThreads) {
       int rec = p.slot_of[i];
       // a routed expert without a slot (the cache could not hold the call):
       // flag it and read slot 0, so every access stays inside the pool
@@ -721,10 +816,9 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       eord[i] = i;
       pre_dn[i] = -1;  // fetch-plan position of each expert until the prefix pass
     }
-    if (p.stats != nullptr) {
-      nmiss = min(max(p.stats[1], 0), min(E, p.S));
-      __syncthreads();
-      for (int m = threadIdx.x; m < nmiss; m += blockDim.x) {
+    if (nmiss > 0) {
+      compute_sync();
+      for (int m = threadIdx.x; m < nmiss; m += kCoreThreads) {
         const int e = p.miss_list[m];
         if (e >= 0 && e < E) pre_dn[e] = m;
       }
@@ -738,12 +832,12 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     const int vpr = p.H / 8;
     const int n = (s1 - s0) * vpr;
     constexpr int U = 8;
-    for (int i0 = threadIdx.x; i0 < n; i0 += U * kThreads) {
+    for (int i0 = threadIdx.x; i0 < n; i0 += U * kCoreThreads) {
       uint4 v[U];
       int dst[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * kThreads;
+        const int i = i0 + u * kCoreThreads;
         dst[u] = -1;
         if (i < n) {
           const int sl = s0 + i / vpr;
@@ -763,10 +857,10 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     // one arrival per CTA
     fence_proxy_async_global();
     __threadfence();
-    __syncthreads();
+    compute_sync();
     if (threadIdx.x == 0) atomicAdd(p.ready + E + 1, 1);
   }
-  __syncthreads();
+  compute_sync();
   if (warp == 0) {
     if (CACHED && nmiss > 0) {
       // tile order: the experts that are resident (ID order), then the ones
@@ -821,11 +915,15 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  compute_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const int total_gu = pre_gu[E];
-  const FSeq seq(blockIdx.x, gridDim.x, total_gu, pre_dn[E], p.ks_gu, p.ks_dn);
+  const FSeq seq1(blockIdx.x, gridDim.x, total_gu, pre_dn[E], p.ks_gu, p.ks_dn);
+  const int jB = E - nmiss;  // first position of a fetched expert
+  const FOrder seq2(blockIdx.x, gridDim.x, pre_gu[jB], pre_dn[jB], total_gu - pre_gu[jB], pre_dn[E] - pre_dn[jB],
+                    p.ks_gu, p.ks_dn);
+  auto next_tile = [&](int n) { return CACHED ? seq2.tile(n) : seq1.tile(n); };
 
   auto tile_of = [&](int t) {
     FTile tl;
@@ -861,7 +959,6 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     uint32_t ph = 0;
     bool ok = true;
     int ready_e = -1;  // expert whose h rows are known to be complete
-    int landed_e[2] = {-1, -1};  // expert whose fetched gate/up / down record is known to have landed
     // Until every CTA has gathered its token rows, stages get their weight
     // chunk at once and their token rows later (at most S stages deferred).
     bool gathered = p.x == nullptr;
@@ -896,7 +993,7 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       npend = 0;
       return true;
     };
-    for (int n = 0, t; ok && (t = seq.tile(n)) >= 0; ++n) {
+    for (int n = 0, t; ok && (t = next_tile(n)) >= 0; ++n) {
       const FTile tl = tile_of(t);
       const int nblk = (tl.nrows + kBoxRows - 1) / kBoxRows;
       const int KS = tl.kind ? p.ks_dn : p.ks_gu;
@@ -933,10 +1030,11 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
         fence_proxy_async_global();
         ready_e = tl.e;
       }
-      if (CACHED && tl.j >= E - nmiss && landed_e[tl.kind] != tl.e) {
-        // a missing expert: wait until the fetch warps have copied its record
-        const int* word = p.ready + E + 3 + 2 * tl.e + tl.kind;
-        const int target = tl.kind ? p.nch_dn : p.nch_gu;
+      if (CACHED && tl.j >= jB) {
+        // a fetched expert: wait until the pieces of this tile's weight block
+        // have landed in its slot
+        const int* word = p.ready + E + 3 + tl.e * (p.mb_gu + p.mb_dn) + (tl.kind ? p.mb_gu : 0) + tl.mb;
+        const int target = (tl.kind ? p.ks_dn : p.ks_gu) / 2;
         uint64_t t0 = 0;
         for (uint32_t it = 0; ld_acquire_gpu(word) < target; ++it) {
           __nanosleep(64);
@@ -958,7 +1056,6 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
         }
         if (!ok) break;
         fence_proxy_async_global();
-        landed_e[tl.kind] = tl.e;
       }
       const int rec = CACHED ? sslot[tl.e] : tl.e;
       const size_t chunk0 = (static_cast<size_t>(rec) * (tl.kind ? p.mb_dn : p.mb_gu) + tl.mb) * KS;
@@ -1010,7 +1107,7 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     uint32_t aph = 0;
     bool ok = true;
     bool issued = false;
-    for (int n = 0, t; ok && (t = seq.tile(n)) >= 0; ++n) {
+    for (int n = 0, t; ok && (t = next_tile(n)) >= 0; ++n) {
       const FTile tl = tile_of(t);
       const int KS = tl.kind ? p.ks_dn : p.ks_gu;
       const uint32_t idesc = ptx::idesc_bf16_f32(kBM, static_cast<uint32_t>((tl.nrows + 15) & ~15));
@@ -1054,7 +1151,7 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
-    for (int n = 0, t; (t = seq.tile(n)) >= 0; ++n) {
+    for (int n = 0, t; (t = next_tile(n)) >= 0; ++n) {
       const FTile tl = tile_of(t);
       const bool ok = wait_bounded<kSleepEpi>(accf0 + 8 * acc, aph, misc + 1, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -1106,55 +1203,14 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
         aph ^= 1u;
       }
     }
-  } else if (CACHED && warp >= 6) {
-    // ------------------------------------------------------------ fetch
-    // Each warp claims the next piece of the plan, copies it host -> slot with
-    // eight 16-byte loads in flight per lane, fences its stores for the TMA
-    // reads of other CTAs, and counts the piece as landed.
-    const int n = nmiss;
-    if (n > 0) {
-      const int W = max(1, min(p.wave, n));
-      const int total = n * (p.nch_gu + p.nch_dn);
-      for (;;) {
-        int q = 0;
-        if (lane == 0) q = atomicAdd(p.ready + E + 2, 1);
-        q = __shfl_sync(0xffffffffu, q, 0);
-        if (q >= total) break;
-        const FetchItem f = fetch_item(q, n, W, p.nch_gu, p.nch_dn);
-        const int e = p.miss_list[f.m], sl = p.miss_slot[f.m];
-        const bool valid = e >= 0 && e < E && sl >= 0 && sl < p.S;
-        if (valid) {
-          const size_t rec = f.comp ? p.rec_dn : p.rec_gu;
-          const size_t off = static_cast<size_t>(f.c) * kFetchChunk;
-          const int nv = static_cast<int>(min(rec - off, static_cast<size_t>(kFetchChunk)) / 16);
-          const uint4* src = reinterpret_cast<const uint4*>((f.comp ? p.host_dn : p.host_gu) + e * rec + off);
-          uint4* dst = reinterpret_cast<uint4*>((f.comp ? p.pool_dn : p.pool_gu) + sl * rec + off);
-          constexpr int U = 8;
-          for (int i0 = lane; i0 < nv; i0 += U * 32) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-              if (i0 + u * 32 < nv) v[u] = src[i0 + u * 32];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-              if (i0 + u * 32 < nv) dst[i0 + u * 32] = v[u];
-          }
-          fence_proxy_async_global();
-        } else if (lane == 0) {
-          set_status(p.status, MOE_DEV_BAD_EXPERT);
-        }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0 && valid) atomicAdd(p.ready + E + 3 + 2 * e + f.comp, 1);
-      }
-    }
   }
+  }  // compute warps
 
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+    ptx::tmem_dealloc(misc[0], C::kTmemCols);
   }
   // The last CTA out resets the sync words for the next call.
   if (threadIdx.x == 0) {
@@ -1164,8 +1220,14 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
   __syncthreads();
   if (misc[2]) {
     __threadfence();
-    const int nsync = CACHED ? 3 * E + 3 : E + 2;
-    for (int e = threadIdx.x; e < nsync; e += blockDim.x) p.ready[e] = 0;
+    for (int e = threadIdx.x; e < (CACHED ? E + 3 : E + 2); e += blockDim.x) p.ready[e] = 0;
+    if (CACHED && nmiss > 0) {
+      const int nb = p.mb_gu + p.mb_dn;
+      for (int i = threadIdx.x; i < nmiss * nb; i += blockDim.x) {
+        const int e = p.miss_list[i / nb];
+        if (e >= 0 && e < E) p.ready[E + 3 + e * nb + i % nb] = 0;
+      }
+    }
     __threadfence();
   }
 }

@@ -281,7 +281,7 @@ class CachedMoELayer(MoELayer):
         self.miss_list = torch.zeros((S,), dtype=torch.int32, device=dev)
         self.miss_slot = torch.zeros((S,), dtype=torch.int32, device=dev)
         self.stats = torch.zeros((4,), dtype=torch.int32, device=dev)
-        self.sync_ws = torch.zeros((3 * E + 3,), dtype=torch.int32, device=dev)
+        self.sync_ws = torch.zeros((E * (1 + self.I // 64 + H // 128) + 3,), dtype=torch.int32, device=dev)
 
     def reset_cache(self):
         """Empty the cache and zero the running totals."""
