@@ -13,6 +13,9 @@ larger than L2 and every step streams its experts' weights from HBM.
 --config offload keeps the decode layer's expert records in pinned host
 memory behind an HBM slot cache and reports tokens/s, hit rate, bytes fetched
 per token and the hidden fraction of the fetch for several wave widths.
+--config trace records synthetic decode routes and replays them through the
+cache plan for each replacement policy and slot count, and times merged
+multi-request calls against one call per request.
 --impl reference times the CPU oracle (the reference arm) on the same workload.
 
 Multi-GPU: one process per GPU under torchrun; every rank runs independent
@@ -47,7 +50,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="decode", choices=["decode", "prefill", "stack48", "sweep", "offload"])
+    ap.add_argument("--config", default="decode",
+                    choices=["decode", "prefill", "stack48", "sweep", "offload", "trace"])
+    ap.add_argument("--policy", default="fifo", choices=["fifo", "lru", "score"],
+                    help="offload: replacement policy of the expert cache")
+    ap.add_argument("--decay", type=float, default=0.9, help="offload/trace: the score policy's use-rate factor")
     ap.add_argument("--slots", default="160,192,256", help="offload: HBM expert slot counts")
     ap.add_argument("--waves", default="1,2,4,0", help="offload: wave widths to time (0 = all misses)")
     ap.add_argument("--layers", type=int, default=0, help="distinct layer weight sets rotated (0 = auto)")
@@ -261,6 +268,8 @@ def main():
         return run_stack(args, rank, world, local, dev)
     if args.config == "offload":
         return run_offload(args, rank, world, local, dev)
+    if args.config == "trace":
+        return run_trace(args, rank, world, local, dev)
     cfg = wl.CONFIGS[args.config]
     if args.experts:
         from dataclasses import replace
@@ -741,14 +750,15 @@ def run_offload(args, rank, world, local, dev):
     del full
     by_slots = {}
     for S in slots:
-        bar = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=S, fetch="barrier")
+        bar = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=S, fetch="barrier",
+                             policy=args.policy, decay=args.decay)
         bar_ms, io_ms = timed(bar, fetch_events=True)
         hits, misses = [int(v) for v in bar.stats[2:].cpu().tolist()]
         del bar
         waves = {}
         for w in [int(v) for v in args.waves.split(",")]:
             lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=S,
-                                 wave=w if w > 0 else 1 << 20)
+                                 wave=w if w > 0 else 1 << 20, policy=args.policy, decay=args.decay)
             ms_w, _ = timed(lay)
             assert tuple(int(v) for v in lay.stats[2:].cpu().tolist()) == (hits, misses), "passes differ"
             del lay
@@ -773,8 +783,8 @@ def run_offload(args, rank, world, local, dev):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; 64 independent token blocks in turn)",
         "config": {"workload": f"offload_{workload_name(cfg)}_S{slots[0]}", "slots": slots, "T": T, "E": E,
-                   "records": "tile-packed bf16 in pinned host memory; HBM slot cache, FIFO replacement",
-                   "record_bytes": rec},
+                   "records": f"tile-packed bf16 in pinned host memory; HBM slot cache, {args.policy} replacement",
+                   "policy": args.policy, "decay": args.decay, "record_bytes": rec},
         "resident": {"ms_per_step": res_ms, "tokens_per_s": T / (res_ms / 1e3)},
         "all_hit": {"ms_per_step": hit_ms, "tokens_per_s": T / (hit_ms / 1e3)},
         "by_slots": by_slots,
@@ -785,6 +795,136 @@ def run_offload(args, rank, world, local, dev):
                      "traffic": None, "peak_source": "copy-engine host-to-device copy measured in this run"},
         "clocks": sampler.summary(tw0, tw1),
     }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_trace(args, rank, world, local, dev):
+    """Route traces through the cache plan, and merged multi-request calls.
+
+    Traces: NB decode blocks (T = 16) of each of 8 seeded layers (their own
+    router weights and Zipf bias), routed by moe_route.  Two token-block
+    recipes: independent blocks (x ~ N(0,1) each), and a random walk
+    x_{b+1} = rho x_b + sqrt(1 - rho^2) z (rho = 0.9) whose neighbouring
+    blocks share experts.  Each (recipe, policy, slot count) replays the
+    blocks in order through moe_cache_plan, one cache per layer, from empty.
+    Merge: R independent requests' blocks grouped into one layer call of
+    16 R tokens, against R calls of 16 tokens (records in HBM).
+    """
+    import torch
+    import workloads as wl
+    from sparse_moe_routed_gb300 import MoELayer, _lib, pack_layer_experts
+
+    cfg = wl.DECODE
+    E, H, I, T, k = cfg.E, cfg.H, cfg.I, cfg.T, cfg.k
+    NL, NB = 8, 256
+    rec = 3 * H * I * 2
+    st = torch.cuda.current_stream()
+    routers = []
+    for l in range(NL):
+        routers.append(wl.router_inputs(cfg, dev, layer=l))
+    g = torch.Generator(device=dev)
+    g.manual_seed(cfg.seed * 1_000_003 + 77)
+
+    def blocks(rho):
+        x = torch.randn((T, H), generator=g, device=dev)
+        out = []
+        for _ in range(NB):
+            out.append(x.to(torch.bfloat16))
+            x = rho * x + (1 - rho * rho) ** 0.5 * torch.randn((T, H), generator=g, device=dev)
+        return out
+
+    ws = torch.empty((_lib.route_workspace_size(T, E),), dtype=torch.uint8, device=dev)
+
+    def trace(xs):
+        cnt = torch.zeros((NL, NB, E), dtype=torch.int32, device=dev)
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        for l, (wr, b) in enumerate(routers):
+            for bi, x in enumerate(xs):
+                _lib.moe_route(x, wr, b, k, ids, w, None, ws)
+                cnt[l, bi].index_add_(0, ids.flatten().long(), torch.ones(T * k, dtype=torch.int32, device=dev))
+        return cnt
+
+    pols = {"fifo": _lib.MOE_CACHE_FIFO, "lru": _lib.MOE_CACHE_LRU, "score": _lib.MOE_CACHE_SCORE}
+    slots = [160, 192, 256, 320]
+    result = {}
+    t0 = time.perf_counter()
+    for recipe, rho in (("independent", 0.0), ("walk_rho0.9", 0.9)):
+        cnt = trace(blocks(rho))
+        routed = (cnt > 0)
+        uniq = routed.sum(-1).float()
+        overlap = (routed[:, 1:] & routed[:, :-1]).sum(-1).float() / uniq[:, 1:]
+        r = {"unique_experts_per_block": float(uniq.mean()), "overlap_with_previous_block": float(overlap.mean())}
+        for pol, pid in pols.items():
+            for S in slots:
+                hits = misses = 0
+                for l in range(NL):
+                    so = torch.full((E,), -1, dtype=torch.int32, device=dev)
+                    eo = torch.full((S,), -1, dtype=torch.int32, device=dev)
+                    hand = torch.zeros((2,), dtype=torch.int32, device=dev)
+                    sc = torch.zeros((E,), dtype=torch.float32, device=dev)
+                    lu = torch.full((S,), -1, dtype=torch.int32, device=dev)
+                    ml = torch.empty((S,), dtype=torch.int32, device=dev)
+                    msl = torch.empty((S,), dtype=torch.int32, device=dev)
+                    stt = torch.zeros((4,), dtype=torch.int32, device=dev)
+                    sw = torch.zeros((1,), dtype=torch.int32, device=dev)
+                    for bi in range(NB):
+                        _lib.moe_cache_plan(cnt[l, bi], so, eo, hand, ml, msl, stt, sw, policy=pid,
+                                            decay=args.decay, score=sc, last_use=lu)
+                    torch.cuda.synchronize()
+                    assert int(sw.item()) == 0
+                    hits += int(stt[2].item())
+                    misses += int(stt[3].item())
+                r[f"{pol}_S{S}"] = {"hit_rate": hits / (hits + misses),
+                                    "fetched_bytes_per_token": misses * rec / (NL * NB * T)}
+        result[recipe] = r
+    sim_s = time.perf_counter() - t0
+
+    # merged multi-request calls vs one call per request (records in HBM)
+    d = wl.layer_inputs(cfg, dev, with_x=False)
+    gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, E, H, I)
+    del d["w_gateup"], d["w_down"]
+    xs = [wl.token_batch(cfg, dev, index=b, T=T) for b in range(64)]
+    merge = {}
+    for R in (1, 2, 4, 8):
+        lay = MoELayer(d["w_router"], d["bias"], gu, dn, k, T * R, fmt=_lib.MOE_W_BF16_TILED, I=I)
+        xm = [torch.cat(xs[i * R:(i + 1) * R]) for i in range(64 // R)]
+        single = MoELayer(d["w_router"], d["bias"], gu, dn, k, T, fmt=_lib.MOE_W_BF16_TILED, I=I)
+        K = 64 // R * 4
+
+        def run(fn, n):
+            for i in range(3):
+                fn(i)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            for i in range(n):
+                fn(i)
+            b.record(st)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / n
+
+        ms_merged = run(lambda i: lay.forward(xm[i % len(xm)]), K)
+        ms_sep = run(lambda i: [single.forward(xs[(i % len(xm)) * R + j]) for j in range(R)], K)
+        u = []
+        for i in range(len(xm)):
+            lay.forward(xm[i])
+            torch.cuda.synchronize()
+            u.append(int((lay.counts > 0).sum().item()))
+        assert lay.read_status() == 0 and single.read_status() == 0
+        merge[str(R)] = {"tokens_per_s_merged": T * R / (ms_merged / 1e3),
+                         "tokens_per_s_separate": T * R / (ms_sep / 1e3),
+                         "unique_experts_per_call": sum(u) / len(u),
+                         "record_bytes_per_token_merged": sum(u) / len(u) * rec / (T * R)}
+    best = max(merge.values(), key=lambda v: v["tokens_per_s_merged"])
+    line = {"metric": METRIC, "value": best["tokens_per_s_merged"], "unit": UNIT, "n_gpus": world,
+            "steps": None, "warmup": 3, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded route traces)",
+            "config": {"workload": f"trace_{workload_name(cfg)}_L{NL}_B{NB}", "layers": NL, "blocks": NB,
+                       "slots": slots, "decay": args.decay, "record_bytes": rec},
+            "cache_simulation": result, "simulation_seconds": sim_s, "merge": merge}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

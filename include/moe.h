@@ -259,24 +259,41 @@ MOE_API moe_status moe_expert_swiglu_fused(const uint16_t *x, int k, const int32
  *
  * moe_cache_plan -- one CTA.  State (device, caller-owned, persistent across
  *   calls): slot_of [E] int32 (slot of each expert or -1), expert_of [S]
- *   int32 (expert in each slot or -1), hand [1] int32; initialise to -1, -1,
- *   0.  From counts [E] (moe_permute): routed experts with a slot are hits;
- *   the others are misses, in expert order, and take the next slots in
- *   rotation from the hand that hold no expert routed in this call (FIFO
- *   replacement).  Writes miss_list [S] (experts to fetch), miss_slot [S]
- *   (their slots), stats[0..1] = {hits, misses} of this call, adds them to
- *   the running totals stats[2..3] (the caller zeroes those), and updates the
- *   state.  If the misses do not fit (more routed experts than S), sets
- *   MOE_DEV_CACHE_FULL, counts the call as {hits, 0}, and changes nothing
- *   else.  S <= 1024, E <= 1024.
+ *   int32 (expert in each slot or -1), hand [2] int32 {FIFO hand, call
+ *   counter}; initialise to -1, -1, {0, 0}.  From counts [E] (moe_permute):
+ *   routed experts with a slot are hits, the others misses (expert order).
+ *   Slots holding an expert routed in this call are pinned; the others are
+ *   victims in the order of `policy`, ties to the lower slot:
+ *     MOE_CACHE_FIFO  rotation order from the hand;
+ *     MOE_CACHE_LRU   empty slots, then least recent use; needs last_use [S]
+ *                     int32 (initialise to -1);
+ *     MOE_CACHE_SCORE empty slots, then lowest score(record) (AFN-019, "Two
+ *                     storage workloads, not one": P(use before eviction) x
+ *                     expected exposed latency avoided / resident bytes;
+ *                     whole records of one size, so the order is that of
+ *                     P(use), estimated per expert as f <- decay * f +
+ *                     [routed in this call], one fp32 fused multiply-add);
+ *                     needs score [E] fp32 (initialise to 0), 0 <= decay < 1
+ *                     (MOE_ERANGE otherwise).
+ *   Miss m takes the m-th victim.  Writes miss_list [S] (experts to fetch),
+ *   miss_slot [S] (their slots), stats[0..1] = {hits, misses} of this call,
+ *   adds them to the running totals stats[2..3] (the caller zeroes those),
+ *   and updates the state.  If the misses do not fit (more routed experts
+ *   than unpinned slots), sets MOE_DEV_CACHE_FULL, counts the call as
+ *   {hits, 0} and leaves the slots unchanged (the call counter and the use
+ *   rates still advance).  S <= 1024, E <= 1024.
  * moe_cache_fetch -- copies the planned misses' records from host memory
  *   (host_gateup / host_down, E records of rec_* bytes, 16-byte aligned) into
  *   the pools (S records each); reads the miss count from stats on the
  *   device, so the plan and the fetch need no host round trip.
  * ------------------------------------------------------------------------- */
+#define MOE_CACHE_FIFO 0
+#define MOE_CACHE_LRU 1
+#define MOE_CACHE_SCORE 2
 MOE_API moe_status moe_cache_plan(const int32_t *counts, int E, int32_t *slot_of, int32_t *expert_of, int S,
-                                  int32_t *hand, int32_t *miss_list, int32_t *miss_slot, int32_t *stats,
-                                  int32_t *dev_status, void *stream);
+                                  int32_t *hand, int policy, float decay, float *score, int32_t *last_use,
+                                  int32_t *miss_list, int32_t *miss_slot, int32_t *stats, int32_t *dev_status,
+                                  void *stream);
 MOE_API moe_status moe_cache_fetch(const void *host_gateup, const void *host_down, size_t rec_gateup,
                                    size_t rec_down, const int32_t *miss_list, const int32_t *miss_slot,
                                    const int32_t *stats, void *pool_gateup, void *pool_down, void *stream);

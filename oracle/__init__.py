@@ -68,6 +68,8 @@ def _load():
         lib.oracle_recall.argtypes = [p, p, i, i, p]
         lib.oracle_dedup.argtypes = [p, i, i, i, i, i, i, i, p, p, p, p]
         lib.oracle_dedup.restype = i
+        lib.oracle_cache_plan.argtypes = [i, C.c_float, p, i, p, p, i, p, p, p, p, p, p]
+        lib.oracle_cache_plan.restype = i
         _lib = lib
     return _lib
 
@@ -232,6 +234,35 @@ def dedup(ids, E, block, H, I):
     if rc != 0:
         raise ValueError("expert id out of range")
     return mask, U, b2, b4
+
+
+POLICIES = {"fifo": 0, "lru": 1, "score": 2}
+
+
+class CachePlan:
+    """State of one expert cache (E experts, S slots) stepped by the oracle."""
+
+    def __init__(self, E, S, policy="fifo", decay=0.9):
+        self.E, self.S = E, S
+        self.policy = POLICIES[policy]
+        self.decay = np.float32(decay)
+        self.slot_of = np.full(E, -1, np.int32)
+        self.expert_of = np.full(S, -1, np.int32)
+        self.hand = np.zeros(2, np.int32)
+        self.score = np.zeros(E, np.float32)
+        self.last_use = np.full(S, -1, np.int32)
+        self.stats = np.zeros(4, np.int32)
+
+    def step(self, counts):
+        """One call; returns (full, miss_list, miss_slot)."""
+        c = _c(counts, np.int32)
+        ml = np.zeros(max(self.S, 1), np.int32)
+        ms = np.zeros(max(self.S, 1), np.int32)
+        full = _load().oracle_cache_plan(self.policy, float(self.decay), _ptr(c), self.E, _ptr(self.slot_of),
+                                         _ptr(self.expert_of), self.S, _ptr(self.hand), _ptr(self.score),
+                                         _ptr(self.last_use), _ptr(ml), _ptr(ms), _ptr(self.stats))
+        n = int(self.stats[1])
+        return bool(full), ml[:n].copy(), ms[:n].copy()
 
 
 def moe_layer(x_bits, wr_bits, bias, wgu_bits, wd_bits, k, I):

@@ -21,6 +21,10 @@
  *    deterministic route-rank order.
  *  - AFN-019, section "Hypothesis H7: DFlash block size must follow I/O
  *    cost": 48 * U_B * record bytes per block, break-even U_B < 10 tau(B).
+ *  - AFN-019, section "Two storage workloads, not one": an expert miss moves
+ *    a whole record; replacement by score(record) = P(use before eviction)
+ *    x expected exposed latency avoided / resident bytes, with plain LRU
+ *    as the control.
  *  - AFN-021 "Replay decode as prefill: a training flywheel for predictive
  *    MoE I/O", section "The key equivalence -- and where it breaks": expert
  *    IDs and their rank order must match exactly; weights within a declared
@@ -141,6 +145,7 @@ void oracle_topk(const float *logits, int T, int E, int k, int32_t *ids, float *
 int oracle_permute(const int32_t *ids, int T, int k, int E, int32_t *counts, int32_t *offsets,
                    int32_t *perm, int32_t *inv) {
   const int R = T * k;
+  if (E <= 0) return -1;
   for (int r = 0; r < R; ++r)
     if (ids[r] < 0 || ids[r] >= E) return -1;
   for (int e = 0; e < E; ++e) counts[e] = 0;
@@ -365,4 +370,115 @@ int oracle_dedup(const int32_t *ids, int L, int Ttot, int k, int E, int B, int H
   }
   free(seen);
   return 0;
+}
+
+/* ---- expert cache plan ---------------------------------------------------
+ * One call of the exact-miss expert cache (S slots over E experts).
+ * State: slot_of [E] (slot or -1), expert_of [S] (expert or -1),
+ * hand [2] = {FIFO hand, call counter}, score [E] (SCORE), last_use [S]
+ * (LRU).  counts [E]: routes per expert in this call.
+ *
+ * Routed experts that hold a slot are hits; the others are misses, taken in
+ * expert order.  A slot whose expert is routed in this call is pinned.  The
+ * other slots are candidate victims, ordered by the policy:
+ *   0 FIFO: rotation order starting at the hand (the oldest fill first);
+ *   1 LRU: empty slots first, then the least recent call that used them;
+ *   2 SCORE: empty slots first, then the lowest
+ *        score(record) = P(use before eviction)
+ *                        * expected exposed latency avoided / resident bytes.
+ *     Readings: every record is a whole gate/up/down record of one size, so
+ *     the latency a hit avoids (bytes / link bandwidth, the same for every
+ *     record) divided by the resident bytes is one constant; P(use before
+ *     eviction) over a common horizon grows with the per-call use rate p,
+ *     estimated as p = (1 - decay) * f with f <- decay * f + [routed] (one
+ *     fp32 fused multiply-add per call, the precision the device keeps).
+ * Ties go to the lower slot.  Miss m takes the m-th candidate.  If there are
+ * more misses than candidates the slots stay unchanged; returns 1 then
+ * (CACHE_FULL), else 0.  The call counter and the use rates advance either
+ * way.  stats = {hits, misses, running hits, running misses}.              */
+typedef struct {
+  double key;
+  int empty;
+  int slot;
+} victim_t;
+
+static int cmp_victim(const void *pa, const void *pb) {
+  const victim_t *a = (const victim_t *)pa, *b = (const victim_t *)pb;
+  if (a->empty != b->empty) return a->empty ? -1 : 1;
+  if (a->key < b->key) return -1;
+  if (a->key > b->key) return 1;
+  return a->slot - b->slot;
+}
+
+int oracle_cache_plan(int policy, float decay, const int32_t *counts, int E, int32_t *slot_of,
+                      int32_t *expert_of, int S, int32_t *hand, float *score, int32_t *last_use,
+                      int32_t *miss_list, int32_t *miss_slot, int32_t *stats) {
+  const int step = hand[1];
+  const double link_bw = 1.0, record_bytes = 1.0; /* one size for every record */
+  if (policy == 2)
+    for (int e = 0; e < E; ++e) score[e] = fmaf(decay, score[e], counts[e] > 0 ? 1.0f : 0.0f);
+  int hits = 0, nmiss = 0;
+  int32_t *misses = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+  for (int e = 0; e < E; ++e) {
+    if (counts[e] <= 0) continue;
+    if (slot_of[e] >= 0)
+      ++hits;
+    else
+      misses[nmiss++] = e;
+  }
+  victim_t *cand = (victim_t *)malloc(sizeof(victim_t) * (size_t)S);
+  int nc = 0;
+  const int h = ((hand[0] % S) + S) % S;
+  for (int s = 0; s < S; ++s) {
+    const int ex = expert_of[s];
+    const int occupied = ex >= 0 && ex < E;
+    if (occupied && counts[ex] > 0) continue; /* pinned by this call */
+    victim_t v;
+    v.slot = s;
+    v.empty = 0;
+    v.key = 0.0;
+    if (policy == 0) {
+      v.key = (double)((s - h + S) % S);
+    } else if (!occupied) {
+      v.empty = 1;
+    } else if (policy == 1) {
+      v.key = (double)last_use[s];
+    } else {
+      const double p_use = (1.0 - (double)decay) * (double)score[ex];
+      v.key = p_use * (record_bytes / link_bw) / record_bytes;
+    }
+    cand[nc++] = v;
+  }
+  int full = 0;
+  if (nmiss > nc) {
+    full = 1;
+    stats[0] = hits;
+    stats[1] = 0;
+    stats[2] += hits;
+  } else {
+    qsort(cand, (size_t)nc, sizeof(victim_t), cmp_victim);
+    for (int m = 0; m < nmiss; ++m) {
+      const int v = cand[m].slot;
+      if (expert_of[v] >= 0 && expert_of[v] < E) slot_of[expert_of[v]] = -1;
+    }
+    for (int m = 0; m < nmiss; ++m) {
+      const int e = misses[m], v = cand[m].slot;
+      slot_of[e] = v;
+      expert_of[v] = e;
+      miss_list[m] = e;
+      miss_slot[m] = v;
+    }
+    if (policy == 1)
+      for (int e = 0; e < E; ++e)
+        if (counts[e] > 0) last_use[slot_of[e]] = step;
+    if (policy == 0 && nmiss > 0) hand[0] = (cand[nmiss - 1].slot + 1) % S;
+    stats[0] = hits;
+    stats[1] = nmiss;
+    stats[2] += hits;
+    stats[3] += nmiss;
+  }
+  hand[1] = step + 1;
+  free(misses);
+  free(cand);
+  return full;
 }

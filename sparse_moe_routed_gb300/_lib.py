@@ -19,6 +19,7 @@ from . import build as _build
 MOE_OK, MOE_EINVAL, MOE_ESHAPE, MOE_ERANGE, MOE_ECUDA, MOE_ENOTSUP, MOE_EDEVICE_TIMEOUT, MOE_EWORKSPACE = range(8)
 MOE_DEV_BAD_EXPERT, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT, MOE_DEV_CACHE_FULL = 0x1, 0x2, 0x4, 0x8
 MOE_W_BF16, MOE_W_INT4_G64, MOE_W_BF16_TILED, MOE_W_INT4_G64_TILED = 0, 1, 2, 3
+MOE_CACHE_FIFO, MOE_CACHE_LRU, MOE_CACHE_SCORE = 0, 1, 2
 
 HEADER = os.path.join(_build.INCLUDE, "moe.h")
 
@@ -68,7 +69,7 @@ def load(path: str | None = None):
             "moe_pack_size": ([i, i, i, i, i], sz),
             "moe_pack_experts": ([i, p, p, i, i, i, i, p, sz, p], i),
             "moe_route_recall": ([p, p, i, i, p, p], i),
-            "moe_cache_plan": ([p, i, p, p, i, p, p, p, p, p, p], i),
+            "moe_cache_plan": ([p, i, p, p, i, p, i, f, p, p, p, p, p, p, p], i),
             "moe_cache_fetch": ([p, p, sz, sz, p, p, p, p, p, p], i),
             "moe_expert_swiglu_cached": ([p, i, p, p, p, i, i, i, i, i, p, p, i, p, p, p, p, p, p, i, p, p, p, p, p],
                                          i),
@@ -176,10 +177,12 @@ def moe_expert_swiglu_fused(x_perm, offsets, E, H, I, w_gateup, w_down, h, y_per
     _check("moe_expert_swiglu_fused", st)
 
 
-def moe_cache_plan(counts, slot_of, expert_of, hand, miss_list, miss_slot, stats, dev_status, stream=None):
+def moe_cache_plan(counts, slot_of, expert_of, hand, miss_list, miss_slot, stats, dev_status,
+                   policy=MOE_CACHE_FIFO, decay=0.9, score=None, last_use=None, stream=None):
     E, S = counts.shape[0], expert_of.shape[0]
-    st = load().moe_cache_plan(_ptr(counts), E, _ptr(slot_of), _ptr(expert_of), S, _ptr(hand), _ptr(miss_list),
-                               _ptr(miss_slot), _ptr(stats), _ptr(dev_status), _stream(stream))
+    st = load().moe_cache_plan(_ptr(counts), E, _ptr(slot_of), _ptr(expert_of), S, _ptr(hand), policy,
+                               C.c_float(decay), _ptr(score), _ptr(last_use), _ptr(miss_list), _ptr(miss_slot),
+                               _ptr(stats), _ptr(dev_status), _stream(stream))
     _check("moe_cache_plan", st)
 
 

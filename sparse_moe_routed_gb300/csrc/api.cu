@@ -296,16 +296,24 @@ moe_status moe_expert_swiglu_cached(const uint16_t* x, int k, const int32_t* per
 }
 
 moe_status moe_cache_plan(const int32_t* counts, int E, int32_t* slot_of, int32_t* expert_of, int S, int32_t* hand,
-                          int32_t* miss_list, int32_t* miss_slot, int32_t* stats, int32_t* dev_status, void* stream) {
+                          int policy, float decay, float* score, int32_t* last_use, int32_t* miss_list,
+                          int32_t* miss_slot, int32_t* stats, int32_t* dev_status, void* stream) {
   if (E <= 0 || S <= 0) return MOE_ESHAPE;
   if (E > moe::kMaxE || S > 1024) return MOE_ENOTSUP;
+  if (policy != MOE_CACHE_FIFO && policy != MOE_CACHE_LRU && policy != MOE_CACHE_SCORE) return MOE_EINVAL;
   if (!counts || !slot_of || !expert_of || !hand || !miss_list || !miss_slot || !stats || !dev_status)
     return MOE_EINVAL;
   if (!a4(counts) || !a4(slot_of) || !a4(expert_of) || !a4(hand) || !a4(miss_list) || !a4(miss_slot) || !a4(stats) ||
       !a4(dev_status))
     return MOE_EINVAL;
-  return cuda_status(moe::launch_cache_plan(counts, E, slot_of, expert_of, S, hand, miss_list, miss_slot, stats,
-                                            dev_status, static_cast<cudaStream_t>(stream)));
+  if (policy == MOE_CACHE_LRU && (!last_use || !a4(last_use))) return MOE_EINVAL;
+  if (policy == MOE_CACHE_SCORE) {
+    if (!score || !a4(score)) return MOE_EINVAL;
+    if (!(decay >= 0.0f && decay < 1.0f)) return MOE_ERANGE;
+  }
+  return cuda_status(moe::launch_cache_plan(counts, E, slot_of, expert_of, S, hand, policy, decay, score, last_use,
+                                            miss_list, miss_slot, stats, dev_status,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_cache_fetch(const void* host_gateup, const void* host_down, size_t rec_gateup, size_t rec_down,

@@ -10,12 +10,22 @@
 //
 // cache_plan_kernel (one CTA, one thread per expert and per slot):
 //   routed experts already resident are hits; the others are misses, ordered
-//   by expert ID.  Victim slots are taken in rotation order from the hand,
-//   skipping slots whose expert is routed in this call (FIFO replacement);
-//   miss m gets the m-th such slot.  The plan is written as (miss_list,
+//   by expert ID.  Slots whose expert is routed in this call are pinned; the
+//   others are eligible victims, taken in the policy's order and given to the
+//   misses in turn:
+//     FIFO  rotation order from the hand (the oldest fill first);
+//     LRU   empty slots first, then least recent use (the control);
+//     SCORE empty slots first, then lowest score(record) (AFN-019, section
+//           "Two storage workloads, not one": P(use before eviction) x
+//           expected exposed latency avoided / resident bytes).  Records are
+//           whole and of one size, so the score orders as P(use), estimated
+//           per expert by an exponentially weighted use rate
+//           f <- decay * f + [routed] (one fused multiply-add in fp32);
+//   ties go to the lower slot.  The plan is written as (miss_list,
 //   miss_slot, counters of this call, running totals) and the slot table is
 //   updated in place; if the misses do not fit in the slots not pinned by
-//   this call's routes, MOE_DEV_CACHE_FULL is set and nothing changes.
+//   this call's routes, MOE_DEV_CACHE_FULL is set and the slots stay as they
+//   were (the call counter and the use rates still advance).
 // cache_fetch_kernel (grid-stride, 16-byte loads from host memory, eight in
 //   flight per thread): copies each missing expert's gate/up and down records
 //   into its slot.
@@ -46,68 +56,106 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums) {
 
 __global__ void __launch_bounds__(kPlanThreads) cache_plan_kernel(const int32_t* __restrict__ counts, int E,
                                                                   int32_t* slot_of, int32_t* expert_of, int S,
-                                                                  int32_t* hand, int32_t* __restrict__ miss_list,
+                                                                  int32_t* hand, int policy, float decay,
+                                                                  float* score, int32_t* last_use,
+                                                                  int32_t* __restrict__ miss_list,
                                                                   int32_t* __restrict__ miss_slot,
                                                                   int32_t* __restrict__ stats, int32_t* status) {
   __shared__ int warp_sums[32];
   __shared__ int s_missexp[kMaxE];
-  __shared__ int s_victim[kMaxE];
-  __shared__ int s_nmiss, s_nelig, s_last;
+  __shared__ unsigned long long s_key[kPlanThreads];
+  __shared__ int s_nmiss, s_nelig;
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x;
-  const int h0 = S > 0 ? ((*hand % S) + S) % S : 0;
-  // experts: hit / miss
+  const int h0 = ((hand[0] % S) + S) % S;
+  const int step = hand[1];
+  // experts: hit / miss; use rates
   bool miss = false, hit = false;
   if (tid < E) {
     const bool routed = counts[tid] > 0;
     hit = routed && slot_of[tid] >= 0;
     miss = routed && !hit;
+    if (policy == MOE_CACHE_SCORE) score[tid] = __fmaf_rn(decay, score[tid], routed ? 1.0f : 0.0f);
   }
   const int midx = block_exclusive_scan(miss ? 1 : 0, warp_sums);
   if (miss) s_missexp[midx] = tid;
   if (tid == E - 1) s_nmiss = midx + (miss ? 1 : 0);
-  const int nhit = __syncthreads_count(hit);
-  // slots in rotation order from the hand: eligible = not holding a routed expert
-  const int s = (h0 + tid) % (S > 0 ? S : 1);
+  const int nhit = __syncthreads_count(hit);  // also publishes the use rates
+  // eligible slots and their order keys: (primary << 32) | slot
   bool elig = false;
+  unsigned long long key = ~0ull;
   if (tid < S) {
-    const int ex = expert_of[s];
-    elig = !(ex >= 0 && ex < E && counts[ex] > 0);
+    const int ex = expert_of[tid];
+    const bool occupied = ex >= 0 && ex < E;
+    elig = !(occupied && counts[ex] > 0);
+    if (elig) {
+      uint32_t primary;
+      if (policy == MOE_CACHE_FIFO) {
+        primary = 1u + static_cast<uint32_t>((tid - h0 + S) % S);
+      } else if (!occupied) {
+        primary = 0u;
+      } else if (policy == MOE_CACHE_LRU) {
+        primary = 1u + static_cast<uint32_t>(max(last_use[tid], 0));
+      } else {
+        primary = 1u + __float_as_uint(score[ex]);
+      }
+      key = (static_cast<unsigned long long>(primary) << 32) | static_cast<unsigned>(tid);
+    }
   }
-  const int vidx = block_exclusive_scan(elig ? 1 : 0, warp_sums);
-  if (tid == S - 1) s_nelig = vidx + (elig ? 1 : 0);
-  __syncthreads();
+  s_key[tid] = key;
+  const int nelig = __syncthreads_count(elig);
   const int nmiss = s_nmiss;
-  if (nmiss > s_nelig) {  // cannot hold this call's experts: change nothing, fetch nothing
+  if (nmiss > nelig) {  // cannot hold this call's experts: no slot changes
     if (tid == 0) {
       set_status(status, MOE_DEV_CACHE_FULL);
       stats[0] = nhit;
       stats[1] = 0;
       stats[2] += nhit;
+      hand[1] = step + 1;
     }
     return;
   }
-  if (tid < S && elig && vidx < nmiss) {
-    s_victim[vidx] = s;
-    if (vidx == nmiss - 1) s_last = s;
+  // bitonic sort of the keys, ascending (ineligible slots sort last)
+  int n2 = 1;
+  while (n2 < S) n2 <<= 1;
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      if (tid < n2) {
+        const int other = tid ^ stride;
+        if (other > tid) {
+          const unsigned long long a = s_key[tid], b = s_key[other];
+          const bool up = (tid & size) == 0;
+          if ((a > b) == up) {
+            s_key[tid] = b;
+            s_key[other] = a;
+          }
+        }
+      }
+    }
   }
   __syncthreads();
+  // miss m takes the m-th victim; evict the victims' experts first (none of
+  // them is routed in this call, so no miss is touched)
   for (int m = tid; m < nmiss; m += kPlanThreads) {
-    const int e = s_missexp[m], v = s_victim[m];
+    const int v = static_cast<int>(s_key[m] & 0xffffffffu);
     const int old = expert_of[v];
-    if (old >= 0 && old < E) slot_of[old] = -1;  // never a routed expert: no other miss touches it
-    miss_list[m] = e;
+    if (old >= 0 && old < E) slot_of[old] = -1;
+    miss_list[m] = s_missexp[m];
     miss_slot[m] = v;
   }
   __syncthreads();
   for (int m = tid; m < nmiss; m += kPlanThreads) {
-    const int e = s_missexp[m], v = s_victim[m];
+    const int e = s_missexp[m], v = static_cast<int>(s_key[m] & 0xffffffffu);
     slot_of[e] = v;
     expert_of[v] = e;
+    if (policy == MOE_CACHE_LRU) last_use[v] = step;
   }
+  if (policy == MOE_CACHE_LRU && hit) last_use[slot_of[tid]] = step;
   if (tid == 0) {
-    if (nmiss > 0) *hand = (s_last + 1) % S;
+    if (policy == MOE_CACHE_FIFO && nmiss > 0) *hand = (static_cast<int>(s_key[nmiss - 1] & 0xffffffffu) + 1) % S;
+    hand[1] = step + 1;
     stats[0] = nhit;
     stats[1] = nmiss;
     stats[2] += nhit;
@@ -154,10 +202,11 @@ __global__ void cache_fetch_kernel(const uint8_t* __restrict__ host_gu, const ui
 }  // namespace
 
 cudaError_t launch_cache_plan(const int32_t* counts, int E, int32_t* slot_of, int32_t* expert_of, int S,
-                              int32_t* hand, int32_t* miss_list, int32_t* miss_slot, int32_t* stats,
-                              int32_t* st_word, cudaStream_t st) {
+                              int32_t* hand, int policy, float decay, float* score, int32_t* last_use,
+                              int32_t* miss_list, int32_t* miss_slot, int32_t* stats, int32_t* st_word,
+                              cudaStream_t st) {
   return launch_pdl(cache_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, counts, E, slot_of, expert_of, S, hand,
-                    miss_list, miss_slot, stats, st_word);
+                    policy, decay, score, last_use, miss_list, miss_slot, stats, st_word);
 }
 
 cudaError_t launch_cache_fetch(const void* host_gu, const void* host_dn, size_t rec_gu, size_t rec_dn,

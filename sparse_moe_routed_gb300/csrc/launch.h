@@ -67,8 +67,9 @@ cudaError_t launch_route_permute(const uint16_t* x, const uint16_t* wr, const fl
 
 // cache.cu
 cudaError_t launch_cache_plan(const int32_t* counts, int E, int32_t* slot_of, int32_t* expert_of, int S,
-                              int32_t* hand, int32_t* miss_list, int32_t* miss_slot, int32_t* stats,
-                              int32_t* st_word, cudaStream_t st);
+                              int32_t* hand, int policy, float decay, float* score, int32_t* last_use,
+                              int32_t* miss_list, int32_t* miss_slot, int32_t* stats, int32_t* st_word,
+                              cudaStream_t st);
 cudaError_t launch_cache_fetch(const void* host_gu, const void* host_dn, size_t rec_gu, size_t rec_dn,
                                const int32_t* miss_list, const int32_t* miss_slot, const int32_t* stats,
                                void* pool_gu, void* pool_dn, cudaStream_t st);

@@ -260,13 +260,17 @@ class CachedMoELayer(MoELayer):
         moe_expert_swiglu_cached -> moe_combine
 
     stats [4] int32 on the device: {hits, misses} of the last call and their
-    running totals.
+    running totals.  policy: "fifo", "lru" or "score" (moe_cache_plan), decay
+    the score policy's use-rate factor.
     """
 
+    POLICIES = {"fifo": _lib.MOE_CACHE_FIFO, "lru": _lib.MOE_CACHE_LRU, "score": _lib.MOE_CACHE_SCORE}
+
     def __init__(self, w_router, bias, host_gateup, host_down, k: int, T_max: int, I: int, S: int,
-                 wave: int = 1 << 20, fetch: str = "wave"):
+                 wave: int = 1 << 20, fetch: str = "wave", policy: str = "fifo", decay: float = 0.9):
         assert not host_gateup.is_cuda and host_gateup.is_pinned() and host_down.is_pinned()
-        assert fetch in ("wave", "barrier")
+        assert fetch in ("wave", "barrier") and policy in self.POLICIES
+        self.policy, self.decay = self.POLICIES[policy], float(decay)
         super().__init__(w_router, bias, host_gateup, host_down, k, T_max, fmt=_lib.MOE_W_BF16_TILED, I=I)
         E, H = self.E, self.H
         dev = w_router.device
@@ -277,7 +281,9 @@ class CachedMoELayer(MoELayer):
         self.pool_dn = torch.empty((S * self.rec_dn,), dtype=torch.uint8, device=dev)
         self.slot_of = torch.full((E,), -1, dtype=torch.int32, device=dev)
         self.expert_of = torch.full((S,), -1, dtype=torch.int32, device=dev)
-        self.hand = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self.hand = torch.zeros((2,), dtype=torch.int32, device=dev)
+        self.score = torch.zeros((E,), dtype=torch.float32, device=dev)
+        self.last_use = torch.full((S,), -1, dtype=torch.int32, device=dev)
         self.miss_list = torch.zeros((S,), dtype=torch.int32, device=dev)
         self.miss_slot = torch.zeros((S,), dtype=torch.int32, device=dev)
         self.stats = torch.zeros((4,), dtype=torch.int32, device=dev)
@@ -288,13 +294,16 @@ class CachedMoELayer(MoELayer):
         self.slot_of.fill_(-1)
         self.expert_of.fill_(-1)
         self.hand.zero_()
+        self.score.zero_()
+        self.last_use.fill_(-1)
         self.stats.zero_()
 
     def _expert_calls(self, lib, P, x_gather, R, st):
         E, H, I, S = self.E, self.H, self.I, self.S
         calls = [("moe_cache_plan", lib.moe_cache_plan,
-                  (P(self.counts), E, P(self.slot_of), P(self.expert_of), S, P(self.hand), P(self.miss_list),
-                   P(self.miss_slot), P(self.stats), P(self.status), st))]
+                  (P(self.counts), E, P(self.slot_of), P(self.expert_of), S, P(self.hand), self.policy,
+                   C.c_float(self.decay), P(self.score), P(self.last_use), P(self.miss_list), P(self.miss_slot),
+                   P(self.stats), P(self.status), st))]
         wave = self.fetch == "wave"
         if not wave:
             calls.append(("moe_cache_fetch", lib.moe_cache_fetch,

@@ -232,8 +232,9 @@ def test_route_permute_rejections():
 
 def test_cache_plan_and_fetch_rejections():
     L = lib()
-    # counts, E, slot_of, expert_of, S, hand, miss_list, miss_slot, stats, status, stream
-    base = [P, 512, P, P, 256, P, P, P, P, P, NUL]
+    # counts, E, slot_of, expert_of, S, hand, policy, decay, score, last_use, miss_list, miss_slot, stats,
+    # status, stream
+    base = [P, 512, P, P, 256, P, 0, C.c_float(0.9), NUL, NUL, P, P, P, P, NUL]
 
     def plan(i, v):
         a = list(base)
@@ -244,9 +245,23 @@ def test_cache_plan_and_fetch_rejections():
     assert plan(1, 0) == _lib.MOE_ESHAPE
     assert plan(4, 1025) == _lib.MOE_ENOTSUP     # one CTA plans at most 1024 slots
     assert plan(1, 1025) == _lib.MOE_ENOTSUP
-    for i in (0, 2, 3, 5, 6, 7, 8, 9):
+    for i in (0, 2, 3, 5, 10, 11, 12, 13):
         assert plan(i, NUL) == _lib.MOE_EINVAL, i
     assert plan(2, PM) == _lib.MOE_EINVAL
+    assert plan(6, 3) == _lib.MOE_EINVAL          # unknown policy
+    assert plan(6, 1) == _lib.MOE_EINVAL          # LRU needs last_use
+    assert plan(6, 2) == _lib.MOE_EINVAL          # SCORE needs score
+    b2 = list(base)
+    b2[6], b2[8] = 2, P
+    b2[7] = C.c_float(1.0)
+    assert L.moe_cache_plan(*b2) == _lib.MOE_ERANGE   # decay must be < 1
+    b2[7] = C.c_float(-0.5)
+    assert L.moe_cache_plan(*b2) == _lib.MOE_ERANGE
+    b2[7] = C.c_float(0.5)
+    assert L.moe_cache_plan(*b2) == _lib.MOE_ECUDA
+    b3 = list(base)
+    b3[6], b3[9] = 1, P
+    assert L.moe_cache_plan(*b3) == _lib.MOE_ECUDA
     assert plan(4, 256) == _lib.MOE_ECUDA         # admitted; no device here
 
     # host_gu, host_dn, rec_gu, rec_dn, miss_list, miss_slot, stats, pool_gu, pool_dn, stream

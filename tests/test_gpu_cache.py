@@ -6,14 +6,15 @@ HBM cache them.  Moving records is byte work and each tile's arithmetic is
 unchanged, so a cached layer must return, bit for bit, what MoELayer returns
 over the same records resident in HBM -- call after call, as experts hit,
 miss and are evicted, for every wave width of the in-launch fetch and for the
-copy-first path.  The plan itself is integer work and is compared exactly
-with a plain host model of the same replacement rule (FIFO over the slots
-not pinned by the call's routes).
+copy-first path.  The plan itself is integer work (plus one fp32 fused multiply-add
+per expert for the score policy's use rates) and is compared bit for bit
+with the oracle's plan for the FIFO, LRU and score policies.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 from sparse_moe_routed_gb300 import CachedMoELayer, MoELayer, _lib, pack_layer_experts
 
@@ -28,39 +29,23 @@ QWEN64 = wl.LayerConfig("cache_qwen64", T=4, H=2560, E=64, k=10, I=640, bias=Non
 
 
 # ----------------------------------------------------------------- plan
-def plan_model(counts, slot_of, expert_of, hand, S):
-    """The replacement rule, written out on the host."""
-    E = len(counts)
-    routed = [e for e in range(E) if counts[e] > 0]
-    hits = [e for e in routed if slot_of[e] >= 0]
-    misses = [e for e in routed if slot_of[e] < 0]
-    order = [(hand + i) % S for i in range(S)]
-    free = [s for s in order if not (expert_of[s] >= 0 and counts[expert_of[s]] > 0)]
-    if len(misses) > len(free):
-        return True, [], [], hand, (len(hits), 0)
-    victims = free[:len(misses)]
-    for e, v in zip(misses, victims):
-        if expert_of[v] >= 0:
-            slot_of[expert_of[v]] = -1
-    for e, v in zip(misses, victims):
-        slot_of[e] = v
-        expert_of[v] = e
-    if misses:
-        hand = (victims[-1] + 1) % S
-    return False, misses, victims, hand, (len(hits), len(misses))
-
-
-@pytest.mark.parametrize("E,S,T,k", [(64, 24, 4, 4), (512, 200, 16, 10), (1024, 1024, 64, 10), (64, 1, 1, 1)])
-def test_plan_matches_host_model(E, S, T, k):
-    rng = np.random.default_rng(E + S)
+@pytest.mark.parametrize("policy", ["fifo", "lru", "score"])
+@pytest.mark.parametrize("E,S,T,k", [(64, 24, 4, 4), (512, 200, 16, 10), (1024, 1024, 64, 10), (64, 1, 1, 1),
+                                     (100, 37, 3, 8)])
+def test_plan_matches_oracle(policy, E, S, T, k):
+    """Every output and every piece of state, bit for bit, call after call."""
+    rng = np.random.default_rng(E + S + len(policy))
+    pol = CachedMoELayer.POLICIES[policy]
+    decay = 0.85
+    ref = oracle.CachePlan(E, S, policy, decay)
     slot_of = torch.full((E,), -1, dtype=torch.int32, device=DEV)
     expert_of = torch.full((S,), -1, dtype=torch.int32, device=DEV)
-    hand = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    hand = torch.zeros((2,), dtype=torch.int32, device=DEV)
+    score = torch.zeros((E,), dtype=torch.float32, device=DEV)
+    last_use = torch.full((S,), -1, dtype=torch.int32, device=DEV)
     ml = torch.zeros((S,), dtype=torch.int32, device=DEV)
     ms = torch.zeros((S,), dtype=torch.int32, device=DEV)
     stats = torch.zeros((4,), dtype=torch.int32, device=DEV)
-    m_slot, m_exp, m_hand = [-1] * E, [-1] * S, 0
-    tot = [0, 0]
     saw_full = saw_evict = False
     for call in range(40):
         st = torch.zeros((1,), dtype=torch.int32, device=DEV)
@@ -73,30 +58,25 @@ def test_plan_matches_host_model(E, S, T, k):
             pool = hot if rng.random() < 0.6 else np.arange(E)
             for e in rng.choice(pool, size=min(k, len(pool)), replace=False):
                 cnt[e] += 1
-        counts = torch.from_numpy(cnt).to(DEV)
-        _lib.moe_cache_plan(counts, slot_of, expert_of, hand, ml, ms, stats, st)
+        before = ref.expert_of.copy()
+        _lib.moe_cache_plan(torch.from_numpy(cnt).to(DEV), slot_of, expert_of, hand, ml, ms, stats, st,
+                            policy=pol, decay=decay, score=score, last_use=last_use)
+        full, misses, victims = ref.step(cnt)
         torch.cuda.synchronize()
-        before_exp = list(m_exp)
-        full, misses, victims, m_hand, (nh, nm) = plan_model(cnt.tolist(), m_slot, m_exp, m_hand, S)
-        tot[0] += nh
-        tot[1] += nm
         saw_full |= full
-        saw_evict |= any(before_exp[v] >= 0 for v in victims)
+        saw_evict |= any(before[v] >= 0 for v in victims)
         assert int(st.item()) == (_lib.MOE_DEV_CACHE_FULL if full else 0), call
-        s = stats.cpu().tolist()
-        assert s == [nh, nm, tot[0], tot[1]], call
-        assert slot_of.cpu().tolist() == m_slot, call
-        assert expert_of.cpu().tolist() == m_exp, call
-        assert int(hand.item()) == m_hand, call
-        assert ml[:nm].cpu().tolist() == misses, call
-        assert ms[:nm].cpu().tolist() == victims, call
-        # invariants: a bijection between cached experts and filled slots;
-        # after a call that fit, every routed expert has a slot
-        for e, v in enumerate(m_slot):
-            if v >= 0:
-                assert m_exp[v] == e
-        if not full:
-            assert all(m_slot[e] >= 0 for e in np.nonzero(cnt)[0])
+        assert stats.cpu().tolist() == ref.stats.tolist(), call
+        assert slot_of.cpu().tolist() == ref.slot_of.tolist(), call
+        assert expert_of.cpu().tolist() == ref.expert_of.tolist(), call
+        assert hand.cpu().tolist() == ref.hand.tolist(), call
+        n = len(misses)
+        assert ml[:n].cpu().tolist() == misses.tolist(), call
+        assert ms[:n].cpu().tolist() == victims.tolist(), call
+        if policy == "lru":
+            assert last_use.cpu().tolist() == ref.last_use.tolist(), call
+        if policy == "score":
+            assert torch.equal(score.cpu().view(torch.int32), torch.from_numpy(ref.score).view(torch.int32)), call
     if S < E and S > k:
         assert saw_evict and saw_full
 
@@ -116,9 +96,10 @@ def layers(cfg):
     return _L[cfg.name]
 
 
-def run_sequence(cfg, S, wave, fetch, calls=12):
+def run_sequence(cfg, S, wave, fetch, calls=12, policy="fifo"):
     ref, hgu, hdn, d = layers(cfg)
-    lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, cfg.T, I=cfg.I, S=S, wave=wave, fetch=fetch)
+    lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, cfg.T, I=cfg.I, S=S, wave=wave, fetch=fetch,
+                         policy=policy)
     uniq = 0
     for i in range(calls):
         # repeat a few batches so that some calls hit what earlier ones loaded
@@ -141,6 +122,12 @@ def test_cached_layer_bitwise_small(wave):
     assert int(lay.sync_ws.abs().sum().item()) == 0  # sync words left zero
 
 
+@pytest.mark.parametrize("policy", ["lru", "score"])
+def test_cached_layer_bitwise_policies(policy):
+    lay, s = run_sequence(SMALL, S=40, wave=2, fetch="wave", policy=policy)
+    assert s[2] > 0 and s[3] > 40
+
+
 def test_cached_layer_copy_first_small():
     _, s = run_sequence(SMALL, S=40, wave=1, fetch="barrier")
     assert s[2] > 0 and s[3] > 40
@@ -152,10 +139,11 @@ def test_cached_layer_bitwise_512_experts(wave):
     assert s[2] > 0 and s[3] > 200
 
 
-@pytest.mark.parametrize("wave,fetch", [(1, "wave"), (4, "wave"), (1 << 20, "wave"), (1, "barrier")])
-def test_cached_layer_bitwise_qwen_geometry(wave, fetch):
+@pytest.mark.parametrize("wave,fetch,policy", [(1, "wave", "fifo"), (4, "wave", "lru"), (1 << 20, "wave", "score"),
+                                               (1, "barrier", "fifo")])
+def test_cached_layer_bitwise_qwen_geometry(wave, fetch, policy):
     """Qwen4Exp expert shape (H 2560, I 640) over 64 experts, 40 slots."""
-    _, s = run_sequence(QWEN64, S=40, wave=wave, fetch=fetch, calls=8)
+    _, s = run_sequence(QWEN64, S=40, wave=wave, fetch=fetch, calls=8, policy=policy)
     assert s[2] > 0 and s[3] > 40
 
 
@@ -182,7 +170,7 @@ def test_cache_full_is_flagged_and_changes_nothing():
     lay.forward(x)
     torch.cuda.synchronize()
     assert lay.read_status() & _lib.MOE_DEV_CACHE_FULL
-    assert lay.slot_of.eq(-1).all() and lay.expert_of.eq(-1).all() and int(lay.hand.item()) == 0
+    assert lay.slot_of.eq(-1).all() and lay.expert_of.eq(-1).all() and lay.hand.cpu().tolist() == [0, 1]
     assert lay.stats[1].item() == 0
     assert int(lay.sync_ws.abs().sum().item()) == 0
 
@@ -207,3 +195,25 @@ def test_fetch_only_kernel_copies_records():
     untouched = [s for s in range(S) if s not in (3, 0, 15, 7)]
     for sl in untouched:
         assert int(gu_d[sl * rg:(sl + 1) * rg].sum()) == 0
+
+
+# ----------------------------------------------------------------- merge
+@pytest.mark.parametrize("name,R", [("decode", 4), ("decode", 2), ("tiny", 3)])
+def test_merged_requests_equal_separate_calls(name, R):
+    """Several requests' decode blocks grouped into one call (routes grouped
+    by expert across the requests) give every token the output its own
+    request's call gives, bit for bit: a row's contraction and its
+    rank-order combine do not depend on the other rows of the call.  Up to
+    64 tokens, where one router kernel serves both call sizes."""
+    cfg = wl.CONFIGS[name]
+    d = wl.layer_inputs(cfg, DEV, with_x=False)
+    gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, cfg.E, cfg.H, cfg.I)
+    T = 16
+    merged = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, T * R, fmt=_lib.MOE_W_BF16_TILED, I=cfg.I)
+    single = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, T, fmt=_lib.MOE_W_BF16_TILED, I=cfg.I)
+    xs = [wl.token_batch(cfg, DEV, index=40 + r, T=T) for r in range(R)]
+    got = merged.forward(torch.cat(xs)).clone()
+    want = torch.cat([single.forward(x).clone() for x in xs])
+    torch.cuda.synchronize()
+    assert merged.read_status() == 0 and single.read_status() == 0
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))

@@ -136,6 +136,14 @@ def layer_inputs(cfg: LayerConfig, device="cpu", layer: int = 0, x_seed_offset: 
     return out
 
 
+def router_inputs(cfg: LayerConfig, device="cpu", layer: int = 0):
+    """(w_router, bias) of layer_inputs(cfg, device, layer) without the experts."""
+    dev = torch.device(device)
+    wr = _normal_bf16((cfg.E, cfg.H), STD_W, _gen(dev, cfg.seed, _S_ROUTER, layer), dev)
+    bias = zipf_bias(cfg.E, cfg.seed, cfg.zipf_s, layer).to(dev) if cfg.bias == "zipf" else None
+    return wr, bias
+
+
 def token_batch(cfg: LayerConfig, device="cpu", index: int = 0, T: Optional[int] = None) -> torch.Tensor:
     """An independent x ~ N(0,1) bf16 batch [T,H] (index selects the draw)."""
     dev = torch.device(device)
@@ -200,7 +208,7 @@ def stack_layer_weights(layer: int, device="cpu", cfg: LayerConfig = STACK48) ->
 
 
 __all__ = [
-    "LayerConfig", "TINY", "DECODE", "PREFILL", "STACK48", "CONFIGS", "STD_W",
+    "LayerConfig", "TINY", "DECODE", "PREFILL", "STACK48", "CONFIGS", "STD_W", "router_inputs",
     "STACK_LAYERS", "STACK_BLOCKS", "SWEEP_BLOCKS", "SWEEP_SEED", "with_tokens",
     "layer_inputs", "token_batch", "zipf_bias", "predictor_weights",
     "quantize_int4_g64", "stack_layer_weights", "INT4_GROUP"
