@@ -16,6 +16,10 @@ per token and the hidden fraction of the fetch for several wave widths.
 --config trace records synthetic decode routes and replays them through the
 cache plan for each replacement policy and slot count, and times merged
 multi-request calls against one call per request.
+--config crossover measures, for token blocks of 16 to 4,096, the time to
+bring the routed records from host memory (selected records) against the
+whole layer, finds the crossover in the unique-record fraction, and times
+macro prefill through the two-layer ring.
 --impl reference times the CPU oracle (the reference arm) on the same workload.
 
 Multi-GPU: one process per GPU under torchrun; every rank runs independent
@@ -51,7 +55,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode",
-                    choices=["decode", "prefill", "stack48", "sweep", "offload", "trace"])
+                    choices=["decode", "prefill", "stack48", "sweep", "offload", "trace", "crossover"])
     ap.add_argument("--policy", default="fifo", choices=["fifo", "lru", "score"],
                     help="offload: replacement policy of the expert cache")
     ap.add_argument("--decay", type=float, default=0.9, help="offload/trace: the score policy's use-rate factor")
@@ -270,6 +274,8 @@ def main():
         return run_offload(args, rank, world, local, dev)
     if args.config == "trace":
         return run_trace(args, rank, world, local, dev)
+    if args.config == "crossover":
+        return run_crossover(args, rank, world, local, dev)
     cfg = wl.CONFIGS[args.config]
     if args.experts:
         from dataclasses import replace
@@ -925,6 +931,117 @@ def run_trace(args, rank, world, local, dev):
             "config": {"workload": f"trace_{workload_name(cfg)}_L{NL}_B{NB}", "layers": NL, "blocks": NB,
                        "slots": slots, "decay": args.decay, "record_bytes": rec},
             "cache_simulation": result, "simulation_seconds": sim_s, "merge": merge}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_crossover(args, rank, world, local, dev):
+    """Selected records against the whole layer, and the two-layer ring.
+
+    For T in 16 .. 4096 tokens of the uniform-router layer: U = distinct
+    routed experts; t_selected = moe_cache_fetch of those U records from
+    pinned host memory (SM copy warps); t_layer = moe_layer_stream of all E
+    records (copy engines); t_compute = the layer with its records in HBM.
+    t_selected is fitted as a + b U; the crossover is where it meets t_layer.
+    Macro prefill: L layers (two host record sets in turn) at T = 4096
+    through PrefillRing, against the same stack resident in HBM.
+    """
+    import numpy as np
+    import torch
+    import workloads as wl
+    from sparse_moe_routed_gb300 import MoELayer, MoEStack, PrefillRing, _lib, pack_layer_experts
+
+    cfg = wl.PREFILL
+    E, H, I, k = cfg.E, cfg.H, cfg.I, cfg.k
+    st = torch.cuda.current_stream()
+    sets = []
+    for l in range(2):
+        d = wl.layer_inputs(cfg, dev, layer=l, with_x=False)
+        gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, E, H, I)
+        del d["w_gateup"], d["w_down"]
+        hgu = torch.empty(gu.shape, dtype=torch.uint8, pin_memory=True)
+        hdn = torch.empty(dn.shape, dtype=torch.uint8, pin_memory=True)
+        hgu.copy_(gu)
+        hdn.copy_(dn)
+        torch.cuda.synchronize()
+        sets.append({"wr": d["w_router"], "bias": d["bias"], "gu": gu, "dn": dn, "hgu": hgu, "hdn": hdn})
+    s0 = sets[0]
+    rg, rd = s0["hgu"].numel() // E, s0["hdn"].numel() // E
+    rec = rg + rd
+    pool_gu = torch.empty_like(s0["gu"])
+    pool_dn = torch.empty_like(s0["dn"])
+    ring_gu = torch.empty_like(s0["gu"])
+    ring_dn = torch.empty_like(s0["dn"])
+
+    def timed(fn, reps=5, warm=2):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(reps):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps * 1e3  # microseconds
+
+    t_layer = timed(lambda: _lib.moe_layer_stream(s0["hgu"], s0["hdn"], ring_gu, ring_dn))
+    points = []
+    for T in (16, 64, 256, 1024, 4096):
+        lay = MoELayer(s0["wr"], s0["bias"], s0["gu"], s0["dn"], k, T, fmt=_lib.MOE_W_BF16_TILED, I=I)
+        x = wl.token_batch(cfg, dev, index=T, T=T)
+        t_comp = timed(lambda: lay.forward(x), reps=10)
+        assert lay.read_status() == 0
+        routed = torch.nonzero(lay.counts > 0).flatten().to(torch.int32)
+        U = int(routed.numel())
+        ms = torch.arange(U, dtype=torch.int32, device=dev)
+        stt = torch.tensor([0, U, 0, 0], dtype=torch.int32, device=dev)
+        t_sel = timed(lambda: _lib.moe_cache_fetch(s0["hgu"], s0["hdn"], rg, rd, routed, ms, stt, pool_gu, pool_dn))
+        points.append({"T": T, "U": U, "unique_fraction": U / E, "t_selected_us": t_sel, "t_layer_us": t_layer,
+                       "t_compute_us": t_comp, "selected_gbs": U * rec / t_sel / 1e3})
+        del lay
+    Us = np.array([p["U"] for p in points], float)
+    ts = np.array([p["t_selected_us"] for p in points], float)
+    b, a = np.polyfit(Us, ts, 1)
+    u_star = (t_layer - a) / b / E
+    sel_gbs = rec / b / 1e3
+    layer_gbs = E * rec / t_layer / 1e3
+    for p in points:
+        p["mode"] = ["selected", "layer"][_lib.stream_mode(p["U"], E, rec, sel_gbs, layer_gbs, max(a, 0.0))[0]]
+
+    # macro prefill through the ring, L layers, T = 4096
+    L, T = 8, 4096
+    routers = [(sets[l % 2]["wr"], sets[l % 2]["bias"]) for l in range(L)]
+    host = [(sets[l % 2]["hgu"], sets[l % 2]["hdn"]) for l in range(L)]
+    ring = PrefillRing(routers, host, k, T, I)
+    res = MoEStack([MoELayer(sets[l % 2]["wr"], sets[l % 2]["bias"], sets[l % 2]["gu"], sets[l % 2]["dn"], k, T,
+                             fmt=_lib.MOE_W_BF16_TILED, I=I) for l in range(L)], T)
+    x0 = wl.token_batch(cfg, dev, index=7, T=T).float()
+    xr = x0.clone()
+    xs_ = x0.clone()
+    sampler = ClockSampler(gpu_uuid(local))
+    time.sleep(0.3)
+    tw0 = time.time()
+    t_ring = timed(lambda: ring.forward(xr), reps=3, warm=1)
+    t_res = timed(lambda: res.forward(xs_), reps=3, warm=1)
+    tw1 = time.time()
+    sampler.stop()
+    for ml in ring.stack.layers + res.layers:
+        assert ml.read_status() == 0
+    io = L * t_layer
+    line = {"metric": METRIC, "value": T / (t_ring / 1e6), "unit": UNIT, "n_gpus": world, "steps": 3, "warmup": 1,
+            "ms_per_step": t_ring / 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded; uniform router)",
+            "config": {"workload": f"crossover_{workload_name(cfg)}", "record_bytes": rec,
+                       "ring": f"{L} layers x {T} tokens, records in pinned host memory, two-layer HBM ring"},
+            "points": points,
+            "fit": {"selected_overhead_us": a, "selected_us_per_record": b, "selected_gbs": sel_gbs,
+                    "layer_gbs": layer_gbs, "crossover_unique_fraction": u_star},
+            "ring": {"layers": L, "T": T, "t_ring_ms": t_ring / 1e3, "t_resident_ms": t_res / 1e3,
+                     "t_io_ms": io / 1e3, "hidden_fraction": 1.0 - (t_ring - t_res) / io,
+                     "tokens_per_s_ring": T / (t_ring / 1e6), "tokens_per_s_resident": T / (t_res / 1e6)},
+            "clocks": sampler.summary(tw0, tw1)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

@@ -298,6 +298,35 @@ MOE_API moe_status moe_cache_fetch(const void *host_gateup, const void *host_dow
                                    size_t rec_down, const int32_t *miss_list, const int32_t *miss_slot,
                                    const int32_t *stats, void *pool_gateup, void *pool_down, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Selected records or the whole layer.
+ *
+ * Source: AFN-019, section "Hypothesis H5: prefill and decode need different
+ * streaming modes": decode and small blocks read the selected records; a
+ * large prefill tile routes to most experts, where one sequential layer
+ * extent may cost less than sparse reads; macro prefill streams layer l+1
+ * into a two-layer ring while layer l computes; the crossover is measured
+ * from the unique-record fraction and sustained bandwidth, not guessed from
+ * the prompt length.
+ *
+ * moe_layer_stream -- host -> device copy of a whole layer's packed records
+ *   (bytes_* each a multiple of 16, 16-byte aligned), one copy-engine copy
+ *   per component on `stream`: the ring fill of macro prefill.
+ * moe_stream_mode -- host only: the cheaper way to bring a call's U distinct
+ *   records (of E, record_bytes each) to the device, from measured rates:
+ *   t_selected = overhead + U * record_bytes / selected_gbs (0 when U = 0),
+ *   t_layer = E * record_bytes / layer_gbs (times in microseconds, rates in
+ *   GB/s).  Returns MOE_STREAM_LAYER if t_layer < t_selected, else
+ *   MOE_STREAM_SELECTED; -1 on an argument out of range.  Writes the two
+ *   times when the pointers are not NULL.
+ * ------------------------------------------------------------------------- */
+#define MOE_STREAM_SELECTED 0
+#define MOE_STREAM_LAYER 1
+MOE_API moe_status moe_layer_stream(const void *host_gateup, const void *host_down, size_t bytes_gateup,
+                                    size_t bytes_down, void *dev_gateup, void *dev_down, void *stream);
+MOE_API int moe_stream_mode(int U, int E, double record_bytes, double selected_gbs, double layer_gbs,
+                            double selected_overhead_us, double *t_selected_us, double *t_layer_us);
+
 /* moe_expert_swiglu_cached -- moe_expert_swiglu_fused over slot pools:
  *   pool_gateup / pool_down hold S tile-packed bf16 records (MOE_W_BF16_TILED
  *   layout, one expert each) and expert e's records are record slot_of[e].

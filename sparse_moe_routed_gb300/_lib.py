@@ -71,6 +71,8 @@ def load(path: str | None = None):
             "moe_route_recall": ([p, p, i, i, p, p], i),
             "moe_cache_plan": ([p, i, p, p, i, p, i, f, p, p, p, p, p, p, p], i),
             "moe_cache_fetch": ([p, p, sz, sz, p, p, p, p, p, p], i),
+            "moe_layer_stream": ([p, p, sz, sz, p, p, p], i),
+            "moe_stream_mode": ([i, i, C.c_double, C.c_double, C.c_double, C.c_double, p, p], i),
             "moe_expert_swiglu_cached": ([p, i, p, p, p, i, i, i, i, i, p, p, i, p, p, p, p, p, p, i, p, p, p, p, p],
                                          i),
         }
@@ -191,6 +193,28 @@ def moe_cache_fetch(host_gateup, host_down, rec_gateup, rec_down, miss_list, mis
     st = load().moe_cache_fetch(_ptr(host_gateup), _ptr(host_down), rec_gateup, rec_down, _ptr(miss_list),
                                 _ptr(miss_slot), _ptr(stats), _ptr(pool_gateup), _ptr(pool_down), _stream(stream))
     _check("moe_cache_fetch", st)
+
+
+MOE_STREAM_SELECTED, MOE_STREAM_LAYER = 0, 1
+
+
+def moe_layer_stream(host_gateup, host_down, dev_gateup, dev_down, stream=None):
+    """Copy a whole layer's packed records host -> device (copy engines)."""
+    bg = host_gateup.numel() * host_gateup.element_size()
+    bd = host_down.numel() * host_down.element_size()
+    st = load().moe_layer_stream(_ptr(host_gateup), _ptr(host_down), bg, bd, _ptr(dev_gateup), _ptr(dev_down),
+                                 _stream(stream))
+    _check("moe_layer_stream", st)
+
+
+def stream_mode(U, E, record_bytes, selected_gbs, layer_gbs, selected_overhead_us=0.0):
+    """(mode, t_selected_us, t_layer_us) from moe_stream_mode."""
+    ts, tl = C.c_double(), C.c_double()
+    m = load().moe_stream_mode(U, E, float(record_bytes), float(selected_gbs), float(layer_gbs),
+                               float(selected_overhead_us), C.byref(ts), C.byref(tl))
+    if m < 0:
+        raise ValueError("moe_stream_mode: argument out of range")
+    return m, ts.value, tl.value
 
 
 def moe_expert_swiglu_cached(x_perm, offsets, E, H, I, pool_gateup, pool_down, S, slot_of, h, y_perm, sync_ws,

@@ -329,6 +329,38 @@ moe_status moe_cache_fetch(const void* host_gateup, const void* host_down, size_
                                              stats, pool_gateup, pool_down, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_layer_stream(const void* host_gateup, const void* host_down, size_t bytes_gateup, size_t bytes_down,
+                            void* dev_gateup, void* dev_down, void* stream) {
+  if (bytes_gateup == 0 && bytes_down == 0) return MOE_OK;
+  if (bytes_gateup % 16 != 0 || bytes_down % 16 != 0) return MOE_ESHAPE;
+  if ((bytes_gateup && (!host_gateup || !dev_gateup)) || (bytes_down && (!host_down || !dev_down))) return MOE_EINVAL;
+  if (!a16(host_gateup) || !a16(host_down) || !a16(dev_gateup) || !a16(dev_down)) return MOE_EINVAL;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // one copy per component, on the copy engines: no SM time taken from the
+  // contraction that runs meanwhile
+  if (bytes_gateup) {
+    const cudaError_t e = cudaMemcpyAsync(dev_gateup, host_gateup, bytes_gateup, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return MOE_ECUDA;
+  }
+  if (bytes_down) {
+    const cudaError_t e = cudaMemcpyAsync(dev_down, host_down, bytes_down, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return MOE_ECUDA;
+  }
+  return MOE_OK;
+}
+
+int moe_stream_mode(int U, int E, double record_bytes, double selected_gbs, double layer_gbs,
+                    double selected_overhead_us, double* t_selected_us, double* t_layer_us) {
+  if (U < 0 || E <= 0 || U > E || !(record_bytes > 0.0) || !(selected_gbs > 0.0) || !(layer_gbs > 0.0) ||
+      !(selected_overhead_us >= 0.0))
+    return -1;
+  const double ts = U > 0 ? selected_overhead_us + U * record_bytes / (selected_gbs * 1e3) : 0.0;
+  const double tl = E * record_bytes / (layer_gbs * 1e3);
+  if (t_selected_us) *t_selected_us = ts;
+  if (t_layer_us) *t_layer_us = tl;
+  return tl < ts ? MOE_STREAM_LAYER : MOE_STREAM_SELECTED;
+}
+
 size_t moe_pack_size(int fmt_in, int E, int H, int I, int which) {
   if (E <= 0 || H <= 0 || I <= 0 || (which != 0 && which != 1)) return 0;
   if (H % 128 != 0 || I % 64 != 0) return 0;

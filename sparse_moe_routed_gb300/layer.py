@@ -369,6 +369,65 @@ class MoEStack:
         return x
 
 
+class PrefillRing:
+    """Macro prefill with every layer's records in host memory.
+
+    A prefill tile routes to most experts of a layer, so the layer's records
+    are streamed whole (moe_layer_stream, copy engines) into a two-layer HBM
+    ring: layer l + 1 lands in one ring slot while layer l computes from the
+    other, and the copy into a slot waits until the layer that last used it
+    is done (AFN-019, section "Hypothesis H5: prefill and decode need
+    different streaming modes").  The residual stack is MoEStack's:
+    x <- x + MoE_l(RMSNorm(x)); the output is bit-identical to MoEStack over
+    the same records resident in HBM.
+
+    routers: [(w_router [E,H] bf16, bias or None)] per layer (device);
+    host_records: [(gate/up, down)] per layer, the pinned uint8 buffers of
+    moe_pack_experts (MOE_W_BF16_TILED layout), same sizes for all layers.
+    """
+
+    def __init__(self, routers, host_records, k: int, T_max: int, I: int, eps: float = 1e-6, gammas=None):
+        assert len(routers) == len(host_records) >= 1
+        dev = routers[0][0].device
+        gu0, dn0 = host_records[0]
+        for gu, dn in host_records:
+            assert gu.is_pinned() and dn.is_pinned() and gu.numel() == gu0.numel() and dn.numel() == dn0.numel()
+        self.ring = [(torch.empty(gu0.shape, dtype=torch.uint8, device=dev),
+                      torch.empty(dn0.shape, dtype=torch.uint8, device=dev)) for _ in range(2)]
+        layers = [MoELayer(wr, b, *self.ring[l % 2], k, T_max, fmt=_lib.MOE_W_BF16_TILED, I=I)
+                  for l, (wr, b) in enumerate(routers)]
+        self.stack = MoEStack(layers, T_max, eps, gammas)
+        self.host = list(host_records)
+        self.copy_stream = torch.cuda.Stream(device=dev)
+
+    def forward(self, x, stream=None):
+        """x [T,H] fp32 residual stream on the GPU, updated in place."""
+        s = torch.cuda.current_stream() if stream is None else stream
+        cs = self.copy_stream
+        L = len(self.host)
+        copied = [torch.cuda.Event() for _ in range(L)]
+        done = [torch.cuda.Event() for _ in range(L)]
+        cs.wait_stream(s)  # the ring is free once earlier work on s is done
+
+        def fill(l):
+            if l >= 2:
+                cs.wait_event(done[l - 2])
+            _lib.moe_layer_stream(*self.host[l], *self.ring[l % 2], stream=cs)
+            copied[l].record(cs)
+
+        fill(0)
+        if L > 1:
+            fill(1)
+        for l in range(L):
+            s.wait_event(copied[l])
+            for call in self.stack.layer_calls(x, l, stream=s):
+                MoELayer.issue(call)
+            done[l].record(s)
+            if l + 2 < L:
+                fill(l + 2)
+        return x
+
+
 def pack_layer_experts(w_gateup, w_down, fmt_in, E, H, I, s_gateup=None, s_down=None, stream=None):
     """(packed gate/up, packed down) uint8 device tensors for MoELayer."""
     gu = _lib.moe_pack_experts(fmt_in, w_gateup, s_gateup, E, H, I, 0, stream=stream)

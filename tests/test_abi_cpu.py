@@ -26,7 +26,7 @@ def lib():
 def test_library_loads_and_exports_every_declared_symbol():
     L = lib()
     names = _lib.declared_functions()
-    assert len(names) == 21
+    assert len(names) == 23
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 100
@@ -306,3 +306,37 @@ def test_swiglu_cached_rejections():
     assert call(hgu=NUL, I=704) == _lib.MOE_ENOTSUP
     assert call(sync=NUL) == _lib.MOE_EWORKSPACE
     assert call(R=0) == _lib.MOE_OK
+
+
+def test_layer_stream_rejections():
+    L = lib()
+    # host_gu, host_dn, bytes_gu, bytes_dn, dev_gu, dev_dn, stream
+    assert L.moe_layer_stream(NUL, NUL, 0, 0, NUL, NUL, NUL) == _lib.MOE_OK       # nothing to copy
+    assert L.moe_layer_stream(P, P, 8, 16, P, P, NUL) == _lib.MOE_ESHAPE
+    assert L.moe_layer_stream(NUL, P, 16, 16, P, P, NUL) == _lib.MOE_EINVAL
+    assert L.moe_layer_stream(P, P, 16, 16, P, NUL, NUL) == _lib.MOE_EINVAL
+    assert L.moe_layer_stream(PM, P, 16, 16, P, P, NUL) == _lib.MOE_EINVAL
+    assert L.moe_layer_stream(P, P, 16, 16, P, P, NUL) == _lib.MOE_ECUDA         # admitted; no device here
+
+
+def test_stream_mode_crossover():
+    """Selected records win for few distinct records, the whole layer once
+    the unique-record fraction passes the measured crossover; the switch
+    happens once as U grows, where the two times cross."""
+    E, rec = 512, 9830400.0
+    modes = [_lib.stream_mode(U, E, rec, 200.0, 211.0, 10.0) for U in range(E + 1)]
+    m = [x[0] for x in modes]
+    assert m[0] == _lib.MOE_STREAM_SELECTED and modes[0][1] == 0.0
+    assert m[16] == _lib.MOE_STREAM_SELECTED and m[E] == _lib.MOE_STREAM_LAYER
+    flip = m.index(_lib.MOE_STREAM_LAYER)
+    assert all(v == _lib.MOE_STREAM_LAYER for v in m[flip:])
+    ts_flip, tl = modes[flip][1], modes[flip][2]
+    assert modes[flip - 1][1] <= tl < ts_flip
+    # t_layer = E * rec / 211 GB/s, in microseconds
+    assert abs(tl - E * rec / 211e3) < 1e-6 * tl
+    # equal rates and no overhead: selected never loses
+    assert all(_lib.stream_mode(U, E, rec, 211.0, 211.0, 0.0)[0] == _lib.MOE_STREAM_SELECTED for U in (1, 256, 512))
+    with pytest.raises(ValueError):
+        _lib.stream_mode(E + 1, E, rec, 200.0, 211.0)
+    with pytest.raises(ValueError):
+        _lib.stream_mode(4, E, rec, 0.0, 211.0)
