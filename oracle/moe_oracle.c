@@ -23,8 +23,8 @@
  *    cost": 48 * U_B * record bytes per block, break-even U_B < 10 tau(B).
  *  - AFN-019, section "Two storage workloads, not one": an expert miss moves
  *    a whole record; replacement by score(record) = P(use before eviction)
- *    x expected exposed latency avoided / resident bytes, with plain LRU
- *    as the control.
+ *    x expected exposed latency avoided / resident bytes, measured against
+ *    least-recently-used replacement as the baseline.
  *  - AFN-021 "Replay decode as prefill: a training flywheel for predictive
  *    MoE I/O", section "The key equivalence -- and where it breaks": expert
  *    IDs and their rank order must match exactly; weights within a declared

@@ -3,7 +3,7 @@
 The plan is the exact-miss expert cache of AFN-019 "Hide SSD misses before
 the router knows they exist", section "Two storage workloads, not one"
 (whole records; score(record) = P(use before eviction) x expected exposed
-latency avoided / resident bytes; plain LRU as the control).  With one expert
+latency avoided / resident bytes; LRU as the comparison baseline).  With one expert
 routed per call it is textbook demand paging, so the classic worked examples
 of page replacement fix FIFO and LRU; LRU's inclusion property (a stack
 algorithm never faults more with more frames) must hold on any trace; the
