@@ -20,6 +20,8 @@ multi-request calls against one call per request.
 bring the routed records from host memory (selected records) against the
 whole layer, finds the crossover in the unique-record fraction, and times
 macro prefill through the two-layer ring.
+--config sidecar times the route-sidecar forward pass (trunk 2560 -> 256,
+48 layer embeddings, 512 expert heads, 16 ranked candidates per layer).
 --impl reference times the CPU oracle (the reference arm) on the same workload.
 
 Multi-GPU: one process per GPU under torchrun; every rank runs independent
@@ -55,7 +57,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode",
-                    choices=["decode", "prefill", "stack48", "sweep", "offload", "trace", "crossover"])
+                    choices=["decode", "prefill", "stack48", "sweep", "offload", "trace", "crossover", "sidecar"])
     ap.add_argument("--policy", default="fifo", choices=["fifo", "lru", "score"],
                     help="offload: replacement policy of the expert cache")
     ap.add_argument("--decay", type=float, default=0.9, help="offload/trace: the score policy's use-rate factor")
@@ -276,6 +278,8 @@ def main():
         return run_trace(args, rank, world, local, dev)
     if args.config == "crossover":
         return run_crossover(args, rank, world, local, dev)
+    if args.config == "sidecar":
+        return run_sidecar(args, rank, world, local, dev)
     cfg = wl.CONFIGS[args.config]
     if args.experts:
         from dataclasses import replace
@@ -1042,6 +1046,60 @@ def run_crossover(args, rank, world, local, dev):
                      "t_io_ms": io / 1e3, "hidden_fraction": 1.0 - (t_ring - t_res) / io,
                      "tokens_per_s_ring": T / (t_ring / 1e6), "tokens_per_s_resident": T / (t_res / 1e6)},
             "clocks": sampler.summary(tw0, tw1)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_sidecar(args, rank, world, local, dev):
+    """Route-sidecar forward pass: T positions -> 48 layers x N candidates."""
+    import torch
+    import workloads as wl
+    from sparse_moe_routed_gb300 import _lib
+
+    F, r, E, L, N = 2560, 256, 512, 48, 16
+    w = wl.sidecar_weights(F, r, E, L, dev)
+    hb = torch.empty((L, E), dtype=torch.float32, device=dev)
+    _lib.moe_sidecar_prepare(w["w_head"], w["layer_emb"], hb)
+    st = torch.cuda.current_stream()
+    pk = peaks()
+    res = {}
+    for T in (1, 16, 64, 256):
+        NB = 64
+        feats = [wl.token_batch(wl.DECODE, dev, index=b, T=T) for b in range(NB)]
+        z = torch.empty((T, r), dtype=torch.float32, device=dev)
+        cand = torch.empty((T, L, N), dtype=torch.int32, device=dev)
+        cs = torch.empty((T, L, N), dtype=torch.float32, device=dev)
+        sw = torch.zeros((1,), dtype=torch.int32, device=dev)
+        K = max(args.steps, 16) if args.steps < 20000 else 2000
+        for i in range(max(args.warmup, 3)):
+            _lib.moe_sidecar_forward(feats[i % NB], w["w_trunk"], w["w_head"], hb, N, z, cand, cs, sw)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for i in range(K):
+            _lib.moe_sidecar_forward(feats[i % NB], w["w_trunk"], w["w_head"], hb, N, z, cand, cs, sw)
+        b.record(st)
+        torch.cuda.synchronize()
+        assert int(sw.item()) == 0
+        us = a.elapsed_time(b) / K * 1e3
+        byts = r * F * 2 + E * r * 2 + L * E * 4 + T * F * 2 + T * L * N * 8
+        flops = 2 * T * (r * F + E * r) + T * L * E
+        res[str(T)] = {"us_per_call": us, "positions_per_s": T / (us / 1e6),
+                       "achieved_gbs": byts / (us / 1e6) / 1e9, "frac_hbm": byts / (us / 1e6) / 1e9 / pk["hbm_gbs"],
+                       "tflops": flops / (us / 1e6) / 1e12, "bytes_per_call": byts}
+    line = {"metric": METRIC, "value": res["16"]["positions_per_s"], "unit": "positions/s", "n_gpus": world,
+            "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": res["16"]["us_per_call"] / 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 weights, fp32",
+            "data": "synthetic (seeded random sidecar weights)",
+            "config": {"workload": f"sidecar_F{F}_r{r}_E{E}_L{L}_N{N}", "F": F, "r": r, "E": E, "L": L, "N": N},
+            "by_positions": res,
+            "roofline": {"bound": "hbm", "kernel": "router_logits_mma_kernel (trunk) + sidecar_head_kernel",
+                         "achieved": res["16"]["achieved_gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": res["16"]["frac_hbm"], "traffic": None,
+                         "peak_source": pk["source"] + " hbm_gbs",
+                         "note": "1.7 MB of weights per call: launch and round-trip latency bound"},
+            "gpu_launches": 2 * K}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

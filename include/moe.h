@@ -299,6 +299,33 @@ MOE_API moe_status moe_cache_fetch(const void *host_gateup, const void *host_dow
                                    const int32_t *stats, void *pool_gateup, void *pool_down, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Route sidecar forward pass.
+ *
+ * Source: AFN-021 "Replay decode as prefill: a training flywheel for
+ * predictive MoE I/O", section "What feature should the sidecar see?": an
+ * opaque feature vector goes through a low-rank trunk shared by all layers,
+ * the target layer's embedding is added, scores against expert-head
+ * embeddings shared by all layers give one score per expert, and the ranked
+ * experts are the prefetch candidates.  Readings: no nonlinearity (the
+ * pages name none), bf16 weights, fp32 arithmetic.
+ *
+ * moe_sidecar_prepare -- head_bias [L, E] fp32 = w_head [E, r] bf16 .
+ *   layer_emb [L, r] bf16, once per weight set.
+ * moe_sidecar_forward -- for feat [T, F] bf16 (the feature of each
+ *   position): z [T, r] fp32 = feat . w_trunk^T (w_trunk [r, F] bf16), then
+ *   for every layer l the scores w_head (z + layer_emb[l]), computed as
+ *   w_head z + head_bias[l], and the N best experts in rank order
+ *   (ties to the lower expert ID): cand [T, L, N] int32, cand_score [T, L, N]
+ *   fp32.  F % 128 == 0, r % 8 == 0, r <= 1024, E <= 1024, N <= 32, N <= E.
+ *   A non-finite score sets MOE_DEV_NONFINITE.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_sidecar_prepare(const uint16_t *w_head, const uint16_t *layer_emb, int E, int r, int L,
+                                       float *head_bias, void *stream);
+MOE_API moe_status moe_sidecar_forward(const uint16_t *feat, const uint16_t *w_trunk, const uint16_t *w_head,
+                                       const float *head_bias, int T, int F, int r, int E, int L, int N, float *z,
+                                       int32_t *cand, float *cand_score, int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Selected records or the whole layer.
  *
  * Source: AFN-019, section "Hypothesis H5: prefill and decode need different

@@ -70,6 +70,7 @@ def _load():
         lib.oracle_dedup.restype = i
         lib.oracle_cache_plan.argtypes = [i, C.c_float, p, i, p, p, i, p, p, p, p, p, p]
         lib.oracle_cache_plan.restype = i
+        lib.oracle_sidecar.argtypes = [p, p, p, p, i, i, i, i, i, i, p, p, p]
         _lib = lib
     return _lib
 
@@ -263,6 +264,26 @@ class CachePlan:
                                          _ptr(self.last_use), _ptr(ml), _ptr(ms), _ptr(self.stats))
         n = int(self.stats[1])
         return bool(full), ml[:n].copy(), ms[:n].copy()
+
+
+def sidecar(feat_bits, trunk_bits, emb_bits, head_bits, N, want_scores=False):
+    """Route sidecar: (cand [T,L,N] int32, cand_score [T,L,N] f32, scores
+    [T,L,E] f64 or None) for bf16 bit arrays feat [T,F], trunk [r,F],
+    emb [L,r], head [E,r]."""
+    f = _c(feat_bits, np.uint16)
+    wt = _c(trunk_bits, np.uint16)
+    em = _c(emb_bits, np.uint16)
+    wh = _c(head_bits, np.uint16)
+    T, F = f.shape
+    r = wt.shape[0]
+    L = em.shape[0]
+    E = wh.shape[0]
+    cand = np.empty((T, L, N), np.int32)
+    cs = np.empty((T, L, N), np.float32)
+    sc = np.empty((T, L, E), np.float64) if want_scores else None
+    _load().oracle_sidecar(_ptr(f), _ptr(wt), _ptr(em), _ptr(wh), T, F, r, E, L, N, _ptr(cand), _ptr(cs),
+                           _ptr(sc) if sc is not None else None)
+    return cand, cs, sc
 
 
 def moe_layer(x_bits, wr_bits, bias, wgu_bits, wd_bits, k, I):

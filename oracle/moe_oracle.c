@@ -26,6 +26,10 @@
  *    x expected exposed latency avoided / resident bytes, measured against
  *    least-recently-used replacement as the baseline.
  *  - AFN-021 "Replay decode as prefill: a training flywheel for predictive
+ *    MoE I/O", section "What feature should the sidecar see?": feature ->
+ *    shared low-rank trunk -> plus target-layer embedding -> shared
+ *    expert-head embeddings -> one score per expert -> ranked candidates.
+ *  - AFN-021 "Replay decode as prefill: a training flywheel for predictive
  *    MoE I/O", section "The key equivalence -- and where it breaks": expert
  *    IDs and their rank order must match exactly; weights within a declared
  *    tolerance.
@@ -481,4 +485,61 @@ int oracle_cache_plan(int policy, float decay, const int32_t *counts, int E, int
   free(misses);
   free(cand);
   return full;
+}
+
+/* ---- route sidecar forward pass ------------------------------------------
+ * feat [T,F], w_trunk [r,F], layer_emb [L,r], w_head [E,r], all bf16.
+ * For position t and layer l:
+ *   z      = w_trunk . feat[t]                 (the shared low-rank trunk)
+ *   z_l    = z + layer_emb[l]                  (the target-layer embedding)
+ *   s[e]   = w_head[e] . z_l                   (shared expert-head embeddings)
+ * and the N experts with the largest s in rank order (ties to the lower ID).
+ * Reading: no nonlinearity anywhere (the pages name none).  Everything in
+ * fp64; scores [T,L,E] (optional) and cand_score are the fp64 values
+ * (cand_score rounded to fp32).                                              */
+static const double *sidecar_scores_for_sort;
+
+static int cmp_sidecar(const void *pa, const void *pb) {
+  const int a = *(const int *)pa, b = *(const int *)pb;
+  const double sa = sidecar_scores_for_sort[a], sb = sidecar_scores_for_sort[b];
+  if (sa > sb) return -1;
+  if (sa < sb) return 1;
+  return a - b;
+}
+
+void oracle_sidecar(const uint16_t *feat, const uint16_t *w_trunk, const uint16_t *layer_emb,
+                    const uint16_t *w_head, int T, int F, int r, int E, int L, int N, int32_t *cand,
+                    float *cand_score, double *scores) {
+  double *z = (double *)malloc(sizeof(double) * (size_t)r);
+  double *zl = (double *)malloc(sizeof(double) * (size_t)r);
+  double *s = (double *)malloc(sizeof(double) * (size_t)E);
+  int *order = (int *)malloc(sizeof(int) * (size_t)E);
+  for (int t = 0; t < T; ++t) {
+    for (int j = 0; j < r; ++j) {
+      double acc = 0.0;
+      for (int f = 0; f < F; ++f)
+        acc += bf16_bits_to_f64(w_trunk[(size_t)j * F + f]) * bf16_bits_to_f64(feat[(size_t)t * F + f]);
+      z[j] = acc;
+    }
+    for (int l = 0; l < L; ++l) {
+      for (int j = 0; j < r; ++j) zl[j] = z[j] + bf16_bits_to_f64(layer_emb[(size_t)l * r + j]);
+      for (int e = 0; e < E; ++e) {
+        double acc = 0.0;
+        for (int j = 0; j < r; ++j) acc += bf16_bits_to_f64(w_head[(size_t)e * r + j]) * zl[j];
+        s[e] = acc;
+        order[e] = e;
+        if (scores) scores[((size_t)t * L + l) * E + e] = acc;
+      }
+      sidecar_scores_for_sort = s;
+      qsort(order, (size_t)E, sizeof(int), cmp_sidecar);
+      for (int n = 0; n < N; ++n) {
+        cand[((size_t)t * L + l) * N + n] = order[n];
+        cand_score[((size_t)t * L + l) * N + n] = (float)s[order[n]];
+      }
+    }
+  }
+  free(z);
+  free(zl);
+  free(s);
+  free(order);
 }

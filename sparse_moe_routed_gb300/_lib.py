@@ -72,6 +72,8 @@ def load(path: str | None = None):
             "moe_cache_plan": ([p, i, p, p, i, p, i, f, p, p, p, p, p, p, p], i),
             "moe_cache_fetch": ([p, p, sz, sz, p, p, p, p, p, p], i),
             "moe_layer_stream": ([p, p, sz, sz, p, p, p], i),
+            "moe_sidecar_prepare": ([p, p, i, i, i, p, p], i),
+            "moe_sidecar_forward": ([p, p, p, p, i, i, i, i, i, i, p, p, p, p, p], i),
             "moe_stream_mode": ([i, i, C.c_double, C.c_double, C.c_double, C.c_double, p, p], i),
             "moe_expert_swiglu_cached": ([p, i, p, p, p, i, i, i, i, i, p, p, i, p, p, p, p, p, p, i, p, p, p, p, p],
                                          i),
@@ -193,6 +195,22 @@ def moe_cache_fetch(host_gateup, host_down, rec_gateup, rec_down, miss_list, mis
     st = load().moe_cache_fetch(_ptr(host_gateup), _ptr(host_down), rec_gateup, rec_down, _ptr(miss_list),
                                 _ptr(miss_slot), _ptr(stats), _ptr(pool_gateup), _ptr(pool_down), _stream(stream))
     _check("moe_cache_fetch", st)
+
+
+def moe_sidecar_prepare(w_head, layer_emb, head_bias, stream=None):
+    E, r = w_head.shape
+    L = layer_emb.shape[0]
+    st = load().moe_sidecar_prepare(_ptr(w_head), _ptr(layer_emb), E, r, L, _ptr(head_bias), _stream(stream))
+    _check("moe_sidecar_prepare", st)
+
+
+def moe_sidecar_forward(feat, w_trunk, w_head, head_bias, N, z, cand, cand_score, dev_status, stream=None):
+    T, F = feat.shape
+    r = w_trunk.shape[0]
+    L, E = head_bias.shape
+    st = load().moe_sidecar_forward(_ptr(feat), _ptr(w_trunk), _ptr(w_head), _ptr(head_bias), T, F, r, E, L, N,
+                                    _ptr(z), _ptr(cand), _ptr(cand_score), _ptr(dev_status), _stream(stream))
+    _check("moe_sidecar_forward", st)
 
 
 MOE_STREAM_SELECTED, MOE_STREAM_LAYER = 0, 1

@@ -361,6 +361,31 @@ int moe_stream_mode(int U, int E, double record_bytes, double selected_gbs, doub
   return tl < ts ? MOE_STREAM_LAYER : MOE_STREAM_SELECTED;
 }
 
+moe_status moe_sidecar_prepare(const uint16_t* w_head, const uint16_t* layer_emb, int E, int r, int L,
+                               float* head_bias, void* stream) {
+  if (E <= 0 || r <= 0 || L <= 0) return MOE_ESHAPE;
+  if (E > 1024 || r > 1024 || r % 8 != 0 || L > 65535) return MOE_ENOTSUP;
+  if (!w_head || !layer_emb || !head_bias) return MOE_EINVAL;
+  if (!a16(w_head) || !a4(head_bias) || (reinterpret_cast<uintptr_t>(layer_emb) & 1u)) return MOE_EINVAL;
+  return cuda_status(moe::launch_sidecar_prepare(w_head, layer_emb, E, r, L, head_bias,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_sidecar_forward(const uint16_t* feat, const uint16_t* w_trunk, const uint16_t* w_head,
+                               const float* head_bias, int T, int F, int r, int E, int L, int N, float* z,
+                               int32_t* cand, float* cand_score, int32_t* dev_status, void* stream) {
+  if (T < 0 || F <= 0 || r <= 0 || E <= 0 || L <= 0 || N <= 0) return MOE_ESHAPE;
+  if (F % 128 != 0 || F > 16384 || r % 8 != 0 || r > 1024 || E > 1024 || L > 65535 || N > 32 || N > E)
+    return MOE_ENOTSUP;
+  if (!feat || !w_trunk || !w_head || !head_bias || !z || !cand || !cand_score || !dev_status) return MOE_EINVAL;
+  if (!a16(feat) || !a16(w_trunk) || !a16(w_head) || !a4(head_bias) || !a4(z) || !a4(cand) || !a4(cand_score) ||
+      !a4(dev_status))
+    return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  return cuda_status(moe::launch_sidecar_forward(feat, w_trunk, w_head, head_bias, T, F, r, E, L, N, z, cand,
+                                                 cand_score, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_pack_size(int fmt_in, int E, int H, int I, int which) {
   if (E <= 0 || H <= 0 || I <= 0 || (which != 0 && which != 1)) return 0;
   if (H % 128 != 0 || I % 64 != 0) return 0;

@@ -65,6 +65,13 @@ cudaError_t launch_route_permute(const uint16_t* x, const uint16_t* wr, const fl
                                  int32_t* ids, float* w, float* gap, int32_t* counts, int32_t* offsets, int32_t* perm,
                                  int32_t* inv, int32_t* st_word, cudaStream_t st);
 
+// route.cu: route sidecar
+cudaError_t launch_sidecar_prepare(const uint16_t* w_head, const uint16_t* emb, int E, int r, int L, float* c,
+                                   cudaStream_t st);
+cudaError_t launch_sidecar_forward(const uint16_t* feat, const uint16_t* w_trunk, const uint16_t* w_head,
+                                   const float* c, int T, int F, int r, int E, int L, int N, float* z, int32_t* cand,
+                                   float* score, int32_t* st_word, cudaStream_t st);
+
 // cache.cu
 cudaError_t launch_cache_plan(const int32_t* counts, int E, int32_t* slot_of, int32_t* expert_of, int S,
                               int32_t* hand, int policy, float decay, float* score, int32_t* last_use,

@@ -493,6 +493,145 @@ __global__ void __launch_bounds__(kRpThreads) route_permute_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Route sidecar forward pass (AFN-021 "Replay decode as prefill: a training
+// flywheel for predictive MoE I/O", section "What feature should the sidecar
+// see?"): a feature vector f -> shared low-rank trunk z = Wt f -> plus the
+// target layer's embedding e_l -> scores against the shared expert-head
+// embeddings, s_l = Wh (z + e_l) -> the N highest-scoring experts of every
+// layer, ranked (ties to the lower expert ID).  s_l is computed as
+// Wh z + Wh e_l: the [L, E] table Wh e_l depends on the weights only and is
+// prepared once (sidecar_prepare_kernel); per call the trunk runs on the
+// router's small-T logits kernel (trunk rows in place of router rows) and
+// sidecar_head_kernel forms Wh z once per position and selects every layer's
+// candidates from Wh z + Wh e_l.
+constexpr int kSideThreads = 512;
+constexpr int kSideWarps = kSideThreads / 32;
+constexpr int kSideMaxR = 1024;
+
+// One warp: dots of kSideBatch bf16 rows w[e0 + b][0, r) (rows of r inputs,
+// rows past E read as zero) with the fp32 vector v[0, r) in shared memory;
+// lane l takes inputs 8l .. 8l+7 of every 256-wide chunk, one 16-byte load
+// per row in flight at once, then a butterfly sum per row.  r % 8 == 0, w
+// 16-byte aligned.  Every lane returns the kSideBatch dots.
+constexpr int kSideBatch = 16;
+
+__device__ __forceinline__ void warp_dots_bf16(const uint16_t* __restrict__ w, int e0, int E, int r, const float* v,
+                                               int lane, float (&out)[kSideBatch]) {
+  float acc[kSideBatch];
+#pragma unroll
+  for (int b = 0; b < kSideBatch; ++b) acc[b] = 0.f;
+  for (int j0 = lane * 8; j0 < r; j0 += 256) {
+    uint4 q[kSideBatch];
+#pragma unroll
+    for (int b = 0; b < kSideBatch; ++b)
+      q[b] = e0 + b < E ? __ldg(reinterpret_cast<const uint4*>(w + static_cast<size_t>(e0 + b) * r + j0))
+                        : make_uint4(0u, 0u, 0u, 0u);
+    const float4 va = *reinterpret_cast<const float4*>(v + j0);
+    const float4 vb = *reinterpret_cast<const float4*>(v + j0 + 4);
+    const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int b = 0; b < kSideBatch; ++b) {
+      const uint32_t u[4] = {q[b].x, q[b].y, q[b].z, q[b].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[b] = fmaf(__uint_as_float(u[i] << 16), vv[2 * i], acc[b]);
+        acc[b] = fmaf(__uint_as_float(u[i] & 0xffff0000u), vv[2 * i + 1], acc[b]);
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < kSideBatch; ++b) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], off);
+    out[b] = acc[b];
+  }
+}
+
+// c[l, e] = Wh[e, :] . emb[l, :]; one CTA per layer.
+__global__ void __launch_bounds__(kSideThreads) sidecar_prepare_kernel(const uint16_t* __restrict__ w_head,
+                                                                       const uint16_t* __restrict__ emb, int E,
+                                                                       int r, float* __restrict__ c) {
+  __shared__ __align__(16) float v[kSideMaxR];
+  const int l = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
+  for (int j = threadIdx.x; j < r; j += kSideThreads)
+    v[j] = __uint_as_float(static_cast<uint32_t>(emb[static_cast<size_t>(l) * r + j]) << 16);
+  __syncthreads();
+  for (int e0 = warp * kSideBatch; e0 < E; e0 += kSideWarps * kSideBatch) {
+    float d[kSideBatch];
+    warp_dots_bf16(w_head, e0, E, r, v, lane, d);
+#pragma unroll
+    for (int b = 0; b < kSideBatch; ++b)
+      if (lane == b && e0 + b < E) c[static_cast<size_t>(l) * E + e0 + b] = d[b];
+  }
+}
+
+// CTA (t, y): u = Wh z[t] into shared memory, then the warps rank the
+// layers [y per, (y + 1) per), per = ceil(L / gridDim.y), layer y per + w,
+// + 16, ... by warp w: scores u + c[l] through select_topk.  For a few
+// positions the CTAs of one position each form u (W_h comes from L2) so that
+// every warp ranks one layer; for many, one CTA per position ranks them all.
+template <int EPL>
+__global__ void __launch_bounds__(kSideThreads) sidecar_head_kernel(const float* __restrict__ z,
+                                                                    const uint16_t* __restrict__ w_head,
+                                                                    const float* __restrict__ c, int r, int E, int L,
+                                                                    int N, int32_t* __restrict__ cand,
+                                                                    float* __restrict__ score, int32_t* status) {
+  __shared__ __align__(16) float zs[kSideMaxR];
+  __shared__ float u[32 * EPL];
+  __shared__ uint64_t keys[kSideWarps][32];
+  __shared__ float wscr[kSideWarps][32];
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
+  const int per = (L + gridDim.y - 1) / gridDim.y;
+  const int l0 = blockIdx.y * per, l1 = min(L, l0 + per);
+  if (l0 >= l1) return;
+  for (int j = threadIdx.x; j < r; j += kSideThreads) zs[j] = z[static_cast<size_t>(t) * r + j];
+  __syncthreads();
+  bool bad = false;
+  for (int e0 = warp * kSideBatch; e0 < E; e0 += kSideWarps * kSideBatch) {
+    float d[kSideBatch];
+    warp_dots_bf16(w_head, e0, E, r, zs, lane, d);
+#pragma unroll
+    for (int b = 0; b < kSideBatch; ++b)
+      if (lane == b && e0 + b < E) {
+        u[e0 + b] = d[b];
+        bad |= !isfinite(d[b]);
+      }
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0 && blockIdx.y == 0) set_status(status, MOE_DEV_NONFINITE);
+  for (int l = l0 + warp; l < l1; l += kSideWarps) {
+    float lv[EPL], bv[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      const int e = j * 32 + lane;
+      lv[j] = e < E ? u[e] : 0.f;
+      bv[j] = e < E ? c[static_cast<size_t>(l) * E + e] : 0.f;
+    }
+    const size_t row = (static_cast<size_t>(t) * L + l) * N;
+    const int my_e = select_topk<EPL>(lv, bv, true, E, N, lane, keys[warp], cand + row, wscr[warp], nullptr);
+    if (lane < N) {
+      float sc = u[my_e];
+      sc += c[static_cast<size_t>(l) * E + my_e];
+      score[row + lane] = sc;
+    }
+    __syncwarp();
+  }
+}
+
+template <int EPL>
+cudaError_t run_sidecar_head(const float* z, const uint16_t* w_head, const float* c, int T, int r, int E, int L,
+                             int N, int32_t* cand, float* score, int32_t* st_word, cudaStream_t st) {
+  const int ysplit = T <= 32 ? (L + kSideWarps - 1) / kSideWarps : 1;
+  return launch_pdl(sidecar_head_kernel<EPL>, dim3(T, ysplit), dim3(kSideThreads), 0, st, z, w_head, c, r, E, L, N,
+                    cand, score, st_word);
+}
+
 template <int EPL>
 cudaError_t run_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids, float* w, float* gap,
                      cudaStream_t st) {
@@ -553,6 +692,26 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
   if (epl <= 8) return run_topk<8>(logits, bias, T, E, k, ids, w, gap, st);
   if (epl <= 16) return run_topk<16>(logits, bias, T, E, k, ids, w, gap, st);
   return run_topk<32>(logits, bias, T, E, k, ids, w, gap, st);
+}
+
+cudaError_t launch_sidecar_prepare(const uint16_t* w_head, const uint16_t* emb, int E, int r, int L, float* c,
+                                   cudaStream_t st) {
+  return launch_pdl(sidecar_prepare_kernel, dim3(L), dim3(kSideThreads), 0, st, w_head, emb, E, r, c);
+}
+
+cudaError_t launch_sidecar_forward(const uint16_t* feat, const uint16_t* w_trunk, const uint16_t* w_head,
+                                   const float* c, int T, int F, int r, int E, int L, int N, float* z, int32_t* cand,
+                                   float* score, int32_t* st_word, cudaStream_t st) {
+  if (r > kSideMaxR || E > 1024) return cudaErrorInvalidValue;
+  cudaError_t e = launch_router_logits_small(feat, w_trunk, T, F, r, z, st);
+  if (e != cudaSuccess) return e;
+  const int epl = (E + 31) / 32;
+  if (epl <= 1) return run_sidecar_head<1>(z, w_head, c, T, r, E, L, N, cand, score, st_word, st);
+  if (epl <= 2) return run_sidecar_head<2>(z, w_head, c, T, r, E, L, N, cand, score, st_word, st);
+  if (epl <= 4) return run_sidecar_head<4>(z, w_head, c, T, r, E, L, N, cand, score, st_word, st);
+  if (epl <= 8) return run_sidecar_head<8>(z, w_head, c, T, r, E, L, N, cand, score, st_word, st);
+  if (epl <= 16) return run_sidecar_head<16>(z, w_head, c, T, r, E, L, N, cand, score, st_word, st);
+  return run_sidecar_head<32>(z, w_head, c, T, r, E, L, N, cand, score, st_word, st);
 }
 
 // One-launch route + grouping for a decode block (T <= 16); cudaErrorNotSupported

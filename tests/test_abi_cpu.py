@@ -26,7 +26,7 @@ def lib():
 def test_library_loads_and_exports_every_declared_symbol():
     L = lib()
     names = _lib.declared_functions()
-    assert len(names) == 23
+    assert len(names) == 25
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 100
@@ -340,3 +340,32 @@ def test_stream_mode_crossover():
         _lib.stream_mode(E + 1, E, rec, 200.0, 211.0)
     with pytest.raises(ValueError):
         _lib.stream_mode(4, E, rec, 0.0, 211.0)
+
+
+def test_sidecar_rejections():
+    L = lib()
+    # w_head, emb, E, r, L, head_bias, stream
+    assert L.moe_sidecar_prepare(P, P, 512, 256, 48, P, NUL) == _lib.MOE_ECUDA
+    assert L.moe_sidecar_prepare(P, P, 512, 250, 48, P, NUL) == _lib.MOE_ENOTSUP   # r % 8
+    assert L.moe_sidecar_prepare(P, P, 2048, 256, 48, P, NUL) == _lib.MOE_ENOTSUP
+    assert L.moe_sidecar_prepare(P, P, 0, 256, 48, P, NUL) == _lib.MOE_ESHAPE
+    assert L.moe_sidecar_prepare(NUL, P, 512, 256, 48, P, NUL) == _lib.MOE_EINVAL
+    assert L.moe_sidecar_prepare(PM, P, 512, 256, 48, P, NUL) == _lib.MOE_EINVAL
+    # feat, trunk, head, head_bias, T, F, r, E, L, N, z, cand, score, status, stream
+    base = [P, P, P, P, 16, 2560, 256, 512, 48, 16, P, P, P, P, NUL]
+
+    def fwd(i, v):
+        a = list(base)
+        a[i] = v
+        return L.moe_sidecar_forward(*a)
+
+    assert fwd(4, 0) == _lib.MOE_OK
+    assert fwd(4, -1) == _lib.MOE_ESHAPE
+    assert fwd(5, 2500) == _lib.MOE_ENOTSUP      # F % 128
+    assert fwd(9, 33) == _lib.MOE_ENOTSUP        # N <= 32
+    assert fwd(7, 8) == _lib.MOE_ENOTSUP         # N <= E
+    assert fwd(6, 1032) == _lib.MOE_ENOTSUP      # r <= 1024
+    for i in (0, 1, 2, 3, 10, 11, 12, 13):
+        assert fwd(i, NUL) == _lib.MOE_EINVAL, i
+    assert fwd(0, PM) == _lib.MOE_EINVAL
+    assert fwd(4, 16) == _lib.MOE_ECUDA

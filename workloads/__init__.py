@@ -144,6 +144,20 @@ def router_inputs(cfg: LayerConfig, device="cpu", layer: int = 0):
     return wr, bias
 
 
+SIDECAR_SEED = 5
+
+
+def sidecar_weights(F: int, r: int, E: int, L: int, device="cpu", seed: int = SIDECAR_SEED) -> dict:
+    """Random route-sidecar weights (bf16): trunk [r,F] ~ N(0, 1/F), layer
+    embeddings [L,r] ~ N(0, 1), expert heads [E,r] ~ N(0, 1/r); the trunk
+    output and the layer embeddings are then of one scale, so the layer
+    changes the ranking."""
+    dev = torch.device(device)
+    return {"w_trunk": _normal_bf16((r, F), F ** -0.5, _gen(dev, seed, _S_PRED, 1), dev),
+            "layer_emb": _normal_bf16((L, r), 1.0, _gen(dev, seed, _S_PRED, 2), dev),
+            "w_head": _normal_bf16((E, r), r ** -0.5, _gen(dev, seed, _S_PRED, 3), dev)}
+
+
 def token_batch(cfg: LayerConfig, device="cpu", index: int = 0, T: Optional[int] = None) -> torch.Tensor:
     """An independent x ~ N(0,1) bf16 batch [T,H] (index selects the draw)."""
     dev = torch.device(device)
@@ -208,7 +222,7 @@ def stack_layer_weights(layer: int, device="cpu", cfg: LayerConfig = STACK48) ->
 
 
 __all__ = [
-    "LayerConfig", "TINY", "DECODE", "PREFILL", "STACK48", "CONFIGS", "STD_W", "router_inputs",
+    "LayerConfig", "TINY", "DECODE", "PREFILL", "STACK48", "CONFIGS", "STD_W", "router_inputs", "sidecar_weights",
     "STACK_LAYERS", "STACK_BLOCKS", "SWEEP_BLOCKS", "SWEEP_SEED", "with_tokens",
     "layer_inputs", "token_batch", "zipf_bias", "predictor_weights",
     "quantize_int4_g64", "stack_layer_weights", "INT4_GROUP"
