@@ -1492,27 +1492,32 @@ __global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
 //
 // Warps: 0 streams packed chunks (bulk copies, deep ring), 1 stages each
 // tile's token rows (one bulk copy per row, double-buffered), the rest
-// compute in kGvGroups groups of eight.  The groups take K steps in turn, so
+// compute in kGvGroups groups of four.  The groups take K steps in turn, so
 // each warp has several steps' time for the latency chain of one (wait,
-// loads, dequantise, four dependent MMAs).  Warp w of a group owns tile rows
-// 16w .. 16w + 15: per K step (one scale group of 64 inputs) it runs four
-// MMAs from zero and adds scale x partial to its fp32 accumulators.  At the
-// end of a tile groups 1.. hand their sums to group 0 through shared memory,
-// which adds them in group order (a fixed order: same bits every call); down
-// tiles are then stored from group 0's registers, and for gate/up tiles its
-// up-row warps hand their values to its gate-row warps for SwiGLU.
+// loads, dequantise, MMAs).  Warp w of a group owns tile rows 32w .. 32w + 31
+// as two MMA row tiles that share the token fragments: per K step (one scale
+// group of 64 inputs) it runs eight MMAs from zero and adds scale x partial
+// to its fp32 accumulators.  In a gate/up record rows 32w .. 32w + 15 are gate
+// and 32w + 16 .. 32w + 31 the up rows of the same h columns, so each lane
+// ends a tile holding gate and up of the same outputs.  At the end of a tile
+// groups 1.. hand their sums (valid token columns only) to group 0 through
+// shared memory, which adds them in group order (a fixed order: same bits
+// every call) and stores y, or h = silu(gate) * up.  Token columns past the
+// tile's rows read stale staged rows and are never stored (an MMA column
+// depends on its own B column only).
 constexpr int kGvRows = 4;                     // token rows per tile
-constexpr int kGvN = 8;                        // MMA N: token columns (those past kGvRows are zero)
-constexpr int kGvGroups = 3;
-constexpr int kGvWarps = 2 + 8 * kGvGroups;
+constexpr int kGvN = 8;                        // MMA N: token columns (those past kGvRows are never stored)
+constexpr int kGvGroups = 4;
+constexpr int kGvWpg = 4;                      // compute warps per group, 32 rows each
+constexpr int kGvWarps = 2 + kGvWpg * kGvGroups;
 constexpr int kGvThreads = 32 * kGvWarps;
 constexpr int kGvMaxK = 2560;                  // inputs per row the token-row stage holds
 
 struct CfgV {
   static constexpr int SQmax = 36;  // packed chunks in flight
   static constexpr int kXBytes = kGvRows * kGvMaxK * 2;  // one tile's token rows: 20 KB
-  static constexpr int kUpFloats = 4 * 16 * kGvN;     // up rows of a gate/up tile: [4][16][8]
-  static constexpr int kRedFloats = (kGvGroups - 1) * kBM * kGvN;  // other groups' sums: [G-1][128][8]
+  static constexpr int kUpFloats = 0;
+  static constexpr int kRedFloats = (kGvGroups - 1) * kBM * kGvRows;  // other groups' sums: [G-1][128][4]
   static constexpr int kNumBars = 2 * SQmax + 12;
   static constexpr int kSmemBytes = 1024 + SQmax * kQChunk + 2 * kXBytes + 2 * kUpFloats * 4 +
                                     2 * kRedFloats * 4 + kNumBars * 8 + kSmemTail;
@@ -1548,16 +1553,13 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;                                  // [SQ][QG x 4,352 B] packed codes + scales
   uint8_t* sX = sQ + C::SQmax * kQChunk;               // [2][8 rows][K] bf16 token rows of a tile
-  float* sUp = reinterpret_cast<float*>(sX + 2 * C::kXBytes);  // [2][4][16][8] up rows (gate/up tiles)
-  float* sRed = sUp + 2 * C::kUpFloats;                          // [2][G-1][128][8] other groups' sums
+  float* sRed = reinterpret_cast<float*>(sX + 2 * C::kXBytes);  // [2][G-1][128][4] other groups' sums
   uint64_t* bars = reinterpret_cast<uint64_t*>(sRed + 2 * C::kRedFloats);
   const uint32_t qfull0 = ptx::smem_u32(bars);
   const uint32_t qempty0 = qfull0 + 8 * C::SQmax;
   const uint32_t xfull0 = qempty0 + 8 * C::SQmax;  // token rows of a tile staged (2 buffers)
   const uint32_t xempty0 = xfull0 + 16;            // every compute warp done with them
-  const uint32_t upf0 = xempty0 + 16;              // up rows written (2 buffers)
-  const uint32_t upe0 = upf0 + 16;                 // up rows consumed (2 buffers)
-  const uint32_t redf0 = upe0 + 16;                // other groups' sums written (2 buffers)
+  const uint32_t redf0 = xempty0 + 16;             // other groups' sums written (2 buffers)
   const uint32_t rede0 = redf0 + 16;               // group 0 done with them (2 buffers)
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
   int* prefix = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
@@ -1570,15 +1572,13 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < SQ; ++s) {
       ptx::mbar_init(qfull0 + 8 * s, 1);
-      ptx::mbar_init(qempty0 + 8 * s, QG * 8);  // every chunk is read by the eight warps of one group
+      ptx::mbar_init(qempty0 + 8 * s, QG * kGvWpg);  // every chunk is read by the warps of one group
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(xfull0 + 8 * b, 1);
-      ptx::mbar_init(xempty0 + 8 * b, 8 * kGvGroups);
-      ptx::mbar_init(upf0 + 8 * b, 4);  // group 0's four up-row warps
-      ptx::mbar_init(upe0 + 8 * b, 4);  // group 0's four gate-row warps
-      ptx::mbar_init(redf0 + 8 * b, 8 * (kGvGroups - 1));
-      ptx::mbar_init(rede0 + 8 * b, 8);
+      ptx::mbar_init(xempty0 + 8 * b, kGvWpg * kGvGroups);
+      ptx::mbar_init(redf0 + 8 * b, kGvWpg * (kGvGroups - 1));
+      ptx::mbar_init(rede0 + 8 * b, kGvWpg);
     }
     misc[1] = 0;
     ptx::fence_mbar_init();
@@ -1647,12 +1647,12 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------- compute
-    const int grp = (warp - 2) / 8;    // takes the K steps g with g % kGvGroups == grp
-    const int cw = (warp - 2) % 8;     // owns tile rows 16 cw .. 16 cw + 15
-    const int g = lane >> 2;           // MMA fragment row group / token column
-    const int q = lane & 3;            // thread in group
-    const int ra = 16 * cw + g, rb = ra + 8;
-    uint32_t gk = 0;   // running K step of this CTA
+    const int grp = (warp - 2) / kGvWpg;  // takes the K steps gk with gk % kGvGroups == grp
+    const int cw = (warp - 2) % kGvWpg;   // owns tile rows 32 cw .. 32 cw + 31
+    const int g = lane >> 2;              // MMA fragment row group / token column
+    const int q = lane & 3;               // thread in group
+    const int r0 = 32 * cw + g;           // rows r0, r0 + 8 (tile 0), r0 + 16, r0 + 24 (tile 1)
+    uint32_t gbase = 0;  // running K step of this CTA at the start of the tile
     int ntile = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++ntile) {
@@ -1664,12 +1664,13 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
         ok = false;
         break;
       }
-      // B fragments read token row g of the stage (zero past the tile's rows)
-      const bool tok_ok = g < tl.nrows;
-      const uint32_t* xrow = reinterpret_cast<const uint32_t*>(sX + b * C::kXBytes + (tok_ok ? g : 0) * K * 2);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int ks = 0; ks < p.ksteps; ++ks, ++gk) {
-        if (static_cast<int>(gk % kGvGroups) != grp) continue;
+      // B fragments read token row g of the stage; columns g >= the tile's
+      // rows read a stale row and are never stored
+      const uint32_t* xrow = reinterpret_cast<const uint32_t*>(sX + b * C::kXBytes + (g & (kGvRows - 1)) * K * 2);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const int ks0 = static_cast<int>((static_cast<uint32_t>(grp) + kGvGroups - gbase % kGvGroups) % kGvGroups);
+      for (int ks = ks0; ks < p.ksteps; ks += kGvGroups) {
+        const uint32_t gk = gbase + ks;
         const uint32_t gg = gk / QG;
         const uint32_t sq = gg % SQ;
         const uint32_t phq = (gg / SQ) & 1u;
@@ -1679,49 +1680,71 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
           break;
         }
         const uint8_t* chunk = sQ + (sq * QG + (gk - gg * QG)) * kQChunk;
-        const uint4 ca0 = reinterpret_cast<const uint4*>(chunk + ra * 32)[0];
-        const uint4 ca1 = reinterpret_cast<const uint4*>(chunk + ra * 32)[1];
-        const uint4 cb0 = reinterpret_cast<const uint4*>(chunk + rb * 32)[0];
-        const uint4 cb1 = reinterpret_cast<const uint4*>(chunk + rb * 32)[1];
+        uint32_t w[4][8];  // codes of rows r0, r0 + 8, r0 + 16, r0 + 24
+        float sc4[4];
         const uint16_t* scl = reinterpret_cast<const uint16_t*>(chunk + kQBytes);
-        const float sa = bf16_to_f32(scl[ra]), sb = bf16_to_f32(scl[rb]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 c0 = reinterpret_cast<const uint4*>(chunk + (r0 + 8 * i) * 32)[0];
+          const uint4 c1 = reinterpret_cast<const uint4*>(chunk + (r0 + 8 * i) * 32)[1];
+          w[i][0] = c0.x;
+          w[i][1] = c0.y;
+          w[i][2] = c0.z;
+          w[i][3] = c0.w;
+          w[i][4] = c1.x;
+          w[i][5] = c1.y;
+          w[i][6] = c1.z;
+          w[i][7] = c1.w;
+          sc4[i] = bf16_to_f32(scl[r0 + 8 * i]);
+        }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(qempty0 + 8 * sq);
-        const uint32_t wa[8] = {ca0.x, ca0.y, ca0.z, ca0.w, ca1.x, ca1.y, ca1.z, ca1.w};
-        const uint32_t wb[8] = {cb0.x, cb0.y, cb0.z, cb0.w, cb1.x, cb1.y, cb1.z, cb1.w};
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t* xk = xrow + ks * (kBK / 2) + q;  // token row words of this K step
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // k16 block j: inputs 16 j .. 16 j + 15 of the step
+          const uint32_t b0 = xk[8 * j], b1 = xk[8 * j + 4];
           uint32_t a[4];
-          a[0] = code_pair_bf16x2(wa[2 * j], q);      // row ra, inputs 16j + 2q, +1
-          a[1] = code_pair_bf16x2(wb[2 * j], q);      // row rb
-          a[2] = code_pair_bf16x2(wa[2 * j + 1], q);  // row ra, inputs 16j + 8 + 2q, +1
-          a[3] = code_pair_bf16x2(wb[2 * j + 1], q);  // row rb
-          const int kx = (ks * kBK + 16 * j + 2 * q) >> 1;  // 32-bit word of the token row
-          const uint32_t b0 = tok_ok ? xrow[kx] : 0u;
-          const uint32_t b1 = tok_ok ? xrow[kx + 4] : 0u;
-          mma_16816_bf16(d, a, b0, b1);
+          a[0] = code_pair_bf16x2(w[0][2 * j], q);      // row r0, inputs 16j + 2q, +1
+          a[1] = code_pair_bf16x2(w[1][2 * j], q);      // row r0 + 8
+          a[2] = code_pair_bf16x2(w[0][2 * j + 1], q);  // row r0, inputs 16j + 8 + 2q, +1
+          a[3] = code_pair_bf16x2(w[1][2 * j + 1], q);  // row r0 + 8
+          mma_16816_bf16(d0, a, b0, b1);
+          a[0] = code_pair_bf16x2(w[2][2 * j], q);      // row r0 + 16
+          a[1] = code_pair_bf16x2(w[3][2 * j], q);      // row r0 + 24
+          a[2] = code_pair_bf16x2(w[2][2 * j + 1], q);
+          a[3] = code_pair_bf16x2(w[3][2 * j + 1], q);
+          mma_16816_bf16(d1, a, b0, b1);
         }
-        acc[0] = fmaf(sa, d[0], acc[0]);  // row ra, token 2q
-        acc[1] = fmaf(sa, d[1], acc[1]);  // row ra, token 2q + 1
-        acc[2] = fmaf(sb, d[2], acc[2]);  // row rb, token 2q
-        acc[3] = fmaf(sb, d[3], acc[3]);  // row rb, token 2q + 1
+        acc[0] = fmaf(sc4[0], d0[0], acc[0]);  // row r0, token 2q
+        acc[1] = fmaf(sc4[0], d0[1], acc[1]);  // row r0, token 2q + 1
+        acc[2] = fmaf(sc4[1], d0[2], acc[2]);  // row r0 + 8
+        acc[3] = fmaf(sc4[1], d0[3], acc[3]);
+        acc[4] = fmaf(sc4[2], d1[0], acc[4]);  // row r0 + 16
+        acc[5] = fmaf(sc4[2], d1[1], acc[5]);
+        acc[6] = fmaf(sc4[3], d1[2], acc[6]);  // row r0 + 24
+        acc[7] = fmaf(sc4[3], d1[3], acc[7]);
       }
       if (!ok) break;
+      gbase += static_cast<uint32_t>(p.ksteps);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(xempty0 + 8 * b);
-      // groups 1.. hand their sums to group 0, which adds them in group order
+      // groups 1.. hand their sums of the valid token columns (lanes q < 2)
+      // to group 0
       if (grp > 0) {
         got = wait_bounded<kSleepEpi>(rede0 + 8 * b, use ^ 1u, misc + 1, p.status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        float* red = sRed + b * C::kRedFloats + (grp - 1) * (kBM * kGvN);
-        red[ra * kGvN + 2 * q] = acc[0];
-        red[ra * kGvN + 2 * q + 1] = acc[1];
-        red[rb * kGvN + 2 * q] = acc[2];
-        red[rb * kGvN + 2 * q + 1] = acc[3];
+        if (q < kGvRows / 2) {
+          float* red = sRed + b * C::kRedFloats + (grp - 1) * (kBM * kGvRows);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            red[(r0 + 8 * i) * kGvRows + 2 * q] = acc[2 * i];
+            red[(r0 + 8 * i) * kGvRows + 2 * q + 1] = acc[2 * i + 1];
+          }
+        }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(redf0 + 8 * b);
         continue;
@@ -1731,13 +1754,16 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
         ok = false;
         break;
       }
+      if (q < kGvRows / 2) {
 #pragma unroll
-      for (int gi = 0; gi < kGvGroups - 1; ++gi) {
-        const float* red = sRed + b * C::kRedFloats + gi * (kBM * kGvN);
-        acc[0] += red[ra * kGvN + 2 * q];
-        acc[1] += red[ra * kGvN + 2 * q + 1];
-        acc[2] += red[rb * kGvN + 2 * q];
-        acc[3] += red[rb * kGvN + 2 * q + 1];
+        for (int gi = 0; gi < kGvGroups - 1; ++gi) {
+          const float* red = sRed + b * C::kRedFloats + gi * (kBM * kGvRows);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += red[(r0 + 8 * i) * kGvRows + 2 * q];
+            acc[2 * i + 1] += red[(r0 + 8 * i) * kGvRows + 2 * q + 1];
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(rede0 + 8 * b);
@@ -1745,55 +1771,26 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       if (KIND == 1) {
         float* y = reinterpret_cast<float*>(p.out);
         const int col = tl.mb * kBM;
-        if (t0 < tl.nrows) {
-          y[static_cast<size_t>(tl.row0 + t0) * p.ldo + col + ra] = acc[0];
-          y[static_cast<size_t>(tl.row0 + t0) * p.ldo + col + rb] = acc[2];
-        }
-        if (t1 < tl.nrows) {
-          y[static_cast<size_t>(tl.row0 + t1) * p.ldo + col + ra] = acc[1];
-          y[static_cast<size_t>(tl.row0 + t1) * p.ldo + col + rb] = acc[3];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (t0 < tl.nrows) y[static_cast<size_t>(tl.row0 + t0) * p.ldo + col + r0 + 8 * i] = acc[2 * i];
+          if (t1 < tl.nrows) y[static_cast<size_t>(tl.row0 + t1) * p.ldo + col + r0 + 8 * i] = acc[2 * i + 1];
         }
         continue;
       }
-      // gate/up tile: rows 32m .. 32m + 15 are gate (warp 2m), 32m + 16 .. + 31
-      // up (warp 2m + 1); the up warp hands its values to the gate warp
-      const int m = cw >> 1;
-      float* up = sUp + b * C::kUpFloats + m * (16 * kGvN);
-      if (cw & 1) {
-        got = wait_bounded<kSleepEpi>(upe0 + 8 * b, use ^ 1u, misc + 1, p.status);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        up[g * kGvN + t0] = acc[0];
-        up[g * kGvN + t1] = acc[1];
-        up[(g + 8) * kGvN + t0] = acc[2];
-        up[(g + 8) * kGvN + t1] = acc[3];
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(upf0 + 8 * b);
-      } else {
-        got = wait_bounded<kSpin>(upf0 + 8 * b, use, misc + 1, p.status);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        uint16_t* h = reinterpret_cast<uint16_t*>(p.out);
-        // gate row 32m + r (r = g or g + 8) pairs with up row 32m + 16 + r: h index 16m + r
-        const int colA = tl.mb * 64 + 16 * m + g, colB = colA + 8;
-        const float uA0 = up[g * kGvN + t0], uA1 = up[g * kGvN + t1];
-        const float uB0 = up[(g + 8) * kGvN + t0], uB1 = up[(g + 8) * kGvN + t1];
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(upe0 + 8 * b);
-        if (t0 < tl.nrows) {
-          const size_t o = static_cast<size_t>(tl.row0 + t0) * p.ldo;
-          h[o + colA] = f32_to_bf16(acc[0] / (1.0f + expf(-acc[0])) * uA0);
-          h[o + colB] = f32_to_bf16(acc[2] / (1.0f + expf(-acc[2])) * uB0);
-        }
-        if (t1 < tl.nrows) {
-          const size_t o = static_cast<size_t>(tl.row0 + t1) * p.ldo;
-          h[o + colA] = f32_to_bf16(acc[1] / (1.0f + expf(-acc[1])) * uA1);
-          h[o + colB] = f32_to_bf16(acc[3] / (1.0f + expf(-acc[3])) * uB1);
-        }
+      // gate/up tile: gate row 32 cw + r (r = g or g + 8) pairs with up row
+      // 32 cw + 16 + r, both in this lane: h index 16 cw + r
+      uint16_t* h = reinterpret_cast<uint16_t*>(p.out);
+      const int colA = tl.mb * 64 + 16 * cw + g, colB = colA + 8;
+      if (t0 < tl.nrows) {
+        const size_t o = static_cast<size_t>(tl.row0 + t0) * p.ldo;
+        h[o + colA] = f32_to_bf16(acc[0] / (1.0f + expf(-acc[0])) * acc[4]);
+        h[o + colB] = f32_to_bf16(acc[2] / (1.0f + expf(-acc[2])) * acc[6]);
+      }
+      if (t1 < tl.nrows) {
+        const size_t o = static_cast<size_t>(tl.row0 + t1) * p.ldo;
+        h[o + colA] = f32_to_bf16(acc[1] / (1.0f + expf(-acc[1])) * acc[5]);
+        h[o + colB] = f32_to_bf16(acc[3] / (1.0f + expf(-acc[3])) * acc[7]);
       }
     }
   }
