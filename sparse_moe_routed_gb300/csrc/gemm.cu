@@ -1515,7 +1515,9 @@ constexpr int kGvMaxK = 2560;                  // inputs per row the token-row s
 
 struct CfgV {
   static constexpr int SQmax = 36;  // packed chunks in flight
-  static constexpr int kXBytes = kGvRows * kGvMaxK * 2;  // one tile's token rows: 20 KB
+  // one tile's token rows, each row padded by 16 bytes so that the four
+  // rows' MMA fragment words fall in different shared-memory banks
+  static constexpr int kXBytes = kGvRows * (kGvMaxK * 2 + 16);
   static constexpr int kUpFloats = 0;
   static constexpr int kRedFloats = (kGvGroups - 1) * kBM * kGvRows;  // other groups' sums: [G-1][128][4]
   static constexpr int kNumBars = 2 * SQmax + 12;
@@ -1530,6 +1532,12 @@ __device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Codes of inputs 2p, 2p+1 of a packed word -> bf16 pair (128 + stored code),
+// exact; the stored code is the weight code + 8, so this is 136 + code.
+__device__ __forceinline__ uint32_t code_pair_biased(uint32_t word, int p) {
+  return ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
 }
 
 // Codes of inputs 2p, 2p+1 of a packed word -> bf16 pair (code - 8), exact.
@@ -1638,7 +1646,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       armed_ph = (armed_ph & ~(1u << b)) | (use << b);
       ptx::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(n * K * 2));
       for (int j = 0; j < n; ++j)
-        ptx::bulk_load(ptx::smem_u32(sX + b * C::kXBytes + j * K * 2), p.brows + static_cast<size_t>(tl.row0 + j) * K,
+        ptx::bulk_load(ptx::smem_u32(sX + b * C::kXBytes + j * (K * 2 + 16)), p.brows + static_cast<size_t>(tl.row0 + j) * K,
                        static_cast<uint32_t>(K * 2), fb, pol);
     }
     if (!ok || misc[1]) {
@@ -1666,7 +1674,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       }
       // B fragments read token row g of the stage; columns g >= the tile's
       // rows read a stale row and are never stored
-      const uint32_t* xrow = reinterpret_cast<const uint32_t*>(sX + b * C::kXBytes + (g & (kGvRows - 1)) * K * 2);
+      const uint32_t* xrow =
+          reinterpret_cast<const uint32_t*>(sX + b * C::kXBytes + (g & (kGvRows - 1)) * (K * 2 + 16));
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       const int ks0 = static_cast<int>((static_cast<uint32_t>(grp) + kGvGroups - gbase % kGvGroups) % kGvGroups);
       for (int ks = ks0; ks < p.ksteps; ks += kGvGroups) {
@@ -1700,30 +1709,35 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(qempty0 + 8 * sq);
         const uint32_t* xk = xrow + ks * (kBK / 2) + q;  // token row words of this K step
-        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        // The MMAs take the codes as exact bf16 (136 + code) pairs, two
+        // instructions a pair; a ninth MMA with all-ones A sums each token's
+        // 64 inputs, and sum((136 + c) x) - 136 sum(x) = sum(c x).
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // k16 block j: inputs 16 j .. 16 j + 15 of the step
           const uint32_t b0 = xk[8 * j], b1 = xk[8 * j + 4];
           uint32_t a[4];
-          a[0] = code_pair_bf16x2(w[0][2 * j], q);      // row r0, inputs 16j + 2q, +1
-          a[1] = code_pair_bf16x2(w[1][2 * j], q);      // row r0 + 8
-          a[2] = code_pair_bf16x2(w[0][2 * j + 1], q);  // row r0, inputs 16j + 8 + 2q, +1
-          a[3] = code_pair_bf16x2(w[1][2 * j + 1], q);  // row r0 + 8
+          a[0] = code_pair_biased(w[0][2 * j], q);      // row r0, inputs 16j + 2q, +1
+          a[1] = code_pair_biased(w[1][2 * j], q);      // row r0 + 8
+          a[2] = code_pair_biased(w[0][2 * j + 1], q);  // row r0, inputs 16j + 8 + 2q, +1
+          a[3] = code_pair_biased(w[1][2 * j + 1], q);  // row r0 + 8
           mma_16816_bf16(d0, a, b0, b1);
-          a[0] = code_pair_bf16x2(w[2][2 * j], q);      // row r0 + 16
-          a[1] = code_pair_bf16x2(w[3][2 * j], q);      // row r0 + 24
-          a[2] = code_pair_bf16x2(w[2][2 * j + 1], q);
-          a[3] = code_pair_bf16x2(w[3][2 * j + 1], q);
+          a[0] = code_pair_biased(w[2][2 * j], q);      // row r0 + 16
+          a[1] = code_pair_biased(w[3][2 * j], q);      // row r0 + 24
+          a[2] = code_pair_biased(w[2][2 * j + 1], q);
+          a[3] = code_pair_biased(w[3][2 * j + 1], q);
           mma_16816_bf16(d1, a, b0, b1);
+          mma_16816_bf16(dx, ones, b0, b1);
         }
-        acc[0] = fmaf(sc4[0], d0[0], acc[0]);  // row r0, token 2q
-        acc[1] = fmaf(sc4[0], d0[1], acc[1]);  // row r0, token 2q + 1
-        acc[2] = fmaf(sc4[1], d0[2], acc[2]);  // row r0 + 8
-        acc[3] = fmaf(sc4[1], d0[3], acc[3]);
-        acc[4] = fmaf(sc4[2], d1[0], acc[4]);  // row r0 + 16
-        acc[5] = fmaf(sc4[2], d1[1], acc[5]);
-        acc[6] = fmaf(sc4[3], d1[2], acc[6]);  // row r0 + 24
-        acc[7] = fmaf(sc4[3], d1[3], acc[7]);
+        acc[0] = fmaf(sc4[0], fmaf(-136.0f, dx[0], d0[0]), acc[0]);  // row r0, token 2q
+        acc[1] = fmaf(sc4[0], fmaf(-136.0f, dx[1], d0[1]), acc[1]);  // row r0, token 2q + 1
+        acc[2] = fmaf(sc4[1], fmaf(-136.0f, dx[0], d0[2]), acc[2]);  // row r0 + 8
+        acc[3] = fmaf(sc4[1], fmaf(-136.0f, dx[1], d0[3]), acc[3]);
+        acc[4] = fmaf(sc4[2], fmaf(-136.0f, dx[0], d1[0]), acc[4]);  // row r0 + 16
+        acc[5] = fmaf(sc4[2], fmaf(-136.0f, dx[1], d1[1]), acc[5]);
+        acc[6] = fmaf(sc4[3], fmaf(-136.0f, dx[0], d1[2]), acc[6]);  // row r0 + 24
+        acc[7] = fmaf(sc4[3], fmaf(-136.0f, dx[1], d1[3]), acc[7]);
       }
       if (!ok) break;
       gbase += static_cast<uint32_t>(p.ksteps);
