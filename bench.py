@@ -83,6 +83,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (the slowest rank's time); x itself on
+    one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, seconds_max: float, world: int) -> float:
+    """Units all ranks processed (each rank the same share: weak scaling)
+    over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -398,11 +416,7 @@ def main():
         dist.barrier()
     sampler.stop()
 
-    total_ms = e_start.elapsed_time(e_end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
     gu_ms = [ev_g0[j].elapsed_time(ev_g1[j]) for j in range(KE)]
     dn_ms = [ev_g1[j].elapsed_time(ev_d1[j]) for j in range(KE)]
     gu_avg = sum(gu_ms) / KE
@@ -410,8 +424,7 @@ def main():
     for L in layers:
         assert L.read_status() == 0, f"device status {L.read_status():#x}"
 
-    tokens = cfg.T * K * world
-    value = tokens / (total_ms / 1e3)
+    value = whole_job_rate(cfg.T * K, total_ms / 1e3, world)
     pk = peaks()
     U_steps = [U[i % NL] for i in range(K)]
     main_bytes = fused_bytes if fused else gateup_bytes
@@ -439,12 +452,8 @@ def main():
         t0 = time.perf_counter()
         for i in range(Ke):
             layers[i % NL].forward_host_graph(x_host[i % NL], out_host)
-        el = time.perf_counter() - t0
-        e2e_val = cfg.T * Ke * world / el
-        if world > 1:
-            t = torch.tensor([el], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_val = cfg.T * Ke * world / float(t.item())
+        el = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e_val = whole_job_rate(cfg.T * Ke, el, world)
         e2e = {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": cfg.T * H * 2,
                "d2h_bytes_per_step": cfg.T * H * 2, "steps": Ke,
                "path": "MoELayer.forward_host_graph: pinned x in, result out, one CUDA graph per layer "
@@ -610,11 +619,7 @@ def run_stack(args, rank, world, local, dev):
     torch.cuda.synchronize()
     tw1 = time.time()
     sampler.stop()
-    total_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     for ml in stack.layers:
         assert ml.read_status() == 0, f"device status {ml.read_status():#x}"
     gu = [g0[j].elapsed_time(g1[j]) for j in range(KE)]
@@ -625,7 +630,8 @@ def run_stack(args, rank, world, local, dev):
     gu_bytes = sum((Ul[(j * EV) % L] * (2 * cfg.I * cfg.H // 2 + 2 * cfg.I * cfg.H // 64 * 2) + R * cfg.H * 2 +
                     R * cfg.I * 2) for j in range(KE)) / KE
     step_ms = total_ms / K
-    line = {"metric": METRIC, "value": T * K * world / (total_ms / 1e3), "unit": UNIT, "n_gpus": world, "steps": K,
+    line = {"metric": METRIC, "value": whole_job_rate(T * K, total_ms / 1e3, world), "unit": UNIT, "n_gpus": world,
+            "steps": K,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
             "dtype": ("int4 g64 experts (codes expanded to bf16 pairs in registers, warp-level bf16 MMA, fp32 "
