@@ -233,7 +233,7 @@ MOE_API moe_status moe_grouped_swiglu(const uint16_t *x_perm, const int32_t *off
  *            from moe_permute, k the routes per token, R % k == 0), exactly
  *            what moe_permute's gather writes; if NULL, x_perm is an input
  *            holding those rows and k, perm are ignored.
- *   sync_ws  [E+2] int32 scratch, zero-filled before its first use; a call
+ *   sync_ws  [E+3] int32 scratch, zero-filled before its first use; a call
  *            that completes leaves it zero-filled again.  After a call whose
  *            dev_status shows MOE_DEV_TIMEOUT, zero it again.  Calls that
  *            share one sync_ws must not overlap on the GPU.
@@ -372,7 +372,7 @@ MOE_API int moe_stream_mode(int U, int E, double record_bytes, double selected_g
  *   misses copies every gate/up record before any down record.  The combine
  *   that follows stays in route-rank order.  Needs H/64 and I/64 even
  *   (MOE_ENOTSUP otherwise).
- *   sync_ws: [E * (1 + I/64 + H/128) + 3] int32 (per-expert readiness, and a
+ *   sync_ws: [E * (1 + I/64 + H/128) + 4] int32 (per-expert readiness, and a
  *   landed-piece counter per weight block), zero before the first call;
  *   every launch leaves it zero again. */
 MOE_API moe_status moe_expert_swiglu_cached(const uint16_t *x, int k, const int32_t *perm, uint16_t *x_perm,

@@ -506,14 +506,16 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
 // ============================================================== fused SwiGLU
 // Gate/up and down of every routed expert in one persistent launch (tile-
 // packed bf16 records).  The tile list is all gate/up tiles (expert-major)
-// followed by all down tiles (expert-major).  A down tile of expert e may
-// start once the gate/up tiles of e have stored their h rows: each of their
-// epilogue warps fences its generic stores for the async proxy and bumps
-// ready[e]; the
-// producer of a down tile polls ready[e] (acquire, bounded) before its TMA
-// loads of h.  Down tiles thus fill the SMs the gate/up tail would leave
-// idle, and there is no kernel boundary between the two contractions.  The
-// last CTA to exit resets ready[0..E] to zero for the next call.
+// followed by all down tiles (expert-major); each CTA's producer claims the
+// next tile from a device-wide queue and hands its index to the CTA's MMA
+// issuer and epilogue through a small ring in shared memory.  A down tile of
+// expert e may start once the gate/up tiles of e have stored their h rows:
+// each of their epilogue warps fences its generic stores for the async proxy
+// and bumps ready[e]; the producer of a down tile polls ready[e] (acquire,
+// bounded) before its TMA loads of h.  Down tiles thus fill the SMs the
+// gate/up tail would leave idle, and there is no kernel boundary between the
+// two contractions.  The last CTA to exit resets the sync words to zero for
+// the next call.
 struct FusedArgs {
   const int32_t* offsets;
   int E, R;
@@ -524,11 +526,13 @@ struct FusedArgs {
   uint16_t* h;              // [R, I]
   float* y;                 // [R, H]
   int I, H;
-  int* ready;               // sync words: [E] per-expert h readiness, then exit and gather counters
+  int* ready;               // sync words: [E] per-expert h readiness, then the exit and gather counters
+                            // and the tile queue
   int32_t* status;
-  // Row gather (x != nullptr): every CTA first copies its share of the rows
-  // x_perm[s] = x[perm[s] / k]; the gate/up producers start their token-row
-  // loads once all CTAs have done so.
+  // Row gather (x != nullptr): the epilogue warps of every CTA copy its share
+  // of the rows x_perm[s] = x[perm[s] / k] at the start of the launch, while
+  // the producer already streams weights; the producers start their
+  // token-row loads once all CTAs have done so.
   const uint16_t* x;
   uint16_t* x_perm;
   const int32_t* perm;
@@ -542,7 +546,7 @@ struct FusedArgs {
   // host_dn, reached over the CPU-GPU link) into their slots in kFetchChunk
   // pieces, in wave order, while the other warps compute; the producer of a
   // missing expert's tile waits until its weight block has landed.  Sync
-  // words: ready[E + 2] is the fetch queue, ready[E + 3 + e * (mb_gu + mb_dn)
+  // words: ready[E + 3] is the fetch queue, ready[E + 4 + e * (mb_gu + mb_dn)
   // + b] counts the landed pieces of expert e's weight block b (gate/up
   // blocks first, then down blocks).
   const uint8_t* host_gu;
@@ -558,6 +562,7 @@ struct FusedArgs {
 };
 
 constexpr int kFetchWarps = 4;
+constexpr int kFusedDynamicRows = 4096;  // launches up to this many rows claim tiles dynamically
 constexpr int kFetchChunk = 32768;
 
 // The n-th piece of the fetch plan in wave order (wave width W experts, cg /
@@ -603,9 +608,11 @@ struct CfgF {
   static constexpr int kBudget = 196 * 1024;
   static constexpr int kStages = kBudget / kStageBytes < 2 ? 2 : (kBudget / kStageBytes > 10 ? 10 : kBudget / kStageBytes);
   static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
-  static constexpr int kNumBars = 2 * kStages + 5;
-  // offsets and the two tile prefixes; cached: also slots and the expert order
-  static constexpr int kTail = 16 + (CACHED ? 5 : 3) * (kMaxE + 1) * 4;
+  static constexpr int kTileRing = 4;  // tile ids the producer publishes ahead
+  static constexpr int kNumBars = 2 * kStages + 5 + 2 * kTileRing;
+  // misc words and the tile-id ring; offsets and the two tile prefixes;
+  // cached: also slots and the expert order
+  static constexpr int kTail = 32 + (CACHED ? 5 : 3) * (kMaxE + 1) * 4;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + kTail;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -691,6 +698,28 @@ struct FOrder {
   }
 };
 
+// Decode-sized launches instead claim tiles from a device-wide queue (one
+// atomic per tile) in a global order: all gate/up tiles, then all down
+// tiles.  A CTA that finishes early takes the next tile, so the CTAs end
+// within about one tile of each other whatever bandwidth each one sees (the
+// static order leaves a spread of several microseconds at the end of a
+// decode launch); on large launches the static order measured faster.  A down tile waits for the gate/up
+// tiles of its expert, which all come earlier in the queue and wait for
+// nothing, so every wait ends.  With an expert cache the order is: the
+// resident experts' gate/up tiles, their down tiles, then the fetched
+// experts' gate/up and down tiles (which also wait for the link), so no
+// resident work queues behind a tile that waits for the link.  Returns the
+// index in the combined list (all gate/up tiles by position in the expert
+// order, then all down tiles).
+__device__ __forceinline__ int fused_tile_at(int g, int tguA, int tdnA, int tguB, int total_gu) {
+  if (g < tguA) return g;
+  g -= tguA;
+  if (g < tdnA) return total_gu + g;
+  g -= tdnA;
+  if (g < tguB) return tguA + g;
+  return total_gu + tdnA + (g - tguB);
+}
+
 // The fetch warps of a cached launch: each warp claims the next piece of the
 // plan, copies it host -> slot with eight 16-byte loads in flight per lane,
 // fences its stores for the TMA reads of other CTAs, and counts the piece as
@@ -701,7 +730,7 @@ __device__ __forceinline__ void fetch_records(const FusedArgs& p, int E, int n, 
   const int total = n * (p.nch_gu + p.nch_dn);
   for (;;) {
     int q = 0;
-    if (lane == 0) q = atomicAdd(p.ready + E + 2, 1);
+    if (lane == 0) q = atomicAdd(p.ready + E + 3, 1);
     q = __shfl_sync(0xffffffffu, q, 0);
     if (q >= total) break;
     const FetchItem f = fetch_item(q, n, W, p.nch_gu, p.nch_dn);
@@ -732,7 +761,7 @@ __device__ __forceinline__ void fetch_records(const FusedArgs& p, int E, int n, 
     if (lane == 0 && valid) {
       // pieces never straddle a weight block: a block is ks / 2 pieces
       const int blk = f.comp ? p.mb_gu + f.c / (p.ks_dn / 2) : f.c / (p.ks_gu / 2);
-      atomicAdd(p.ready + E + 3 + e * (p.mb_gu + p.mb_dn) + blk, 1);
+      atomicAdd(p.ready + E + 4 + e * (p.mb_gu + p.mb_dn) + blk, 1);
     }
   }
 }
@@ -763,8 +792,12 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
   const uint32_t accf0 = empty0 + 8 * S;
   const uint32_t acce0 = accf0 + 16;
   const uint32_t drain = acce0 + 16;
+  constexpr int QR = C::kTileRing;
+  const uint32_t tqf0 = drain + 8;          // tile id published (QR slots)
+  const uint32_t tqe0 = tqf0 + 8 * QR;      // tile id read by the MMA issuer and the 4 epilogue warps
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
-  int* pre_gu = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
+  volatile int* tq = reinterpret_cast<volatile int*>(misc + 4);  // [QR] tile ids
+  int* pre_gu = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 8));
   int* pre_dn = pre_gu + (kMaxE + 1);
   int* soff = pre_dn + (kMaxE + 1);
   int* sslot = soff + (kMaxE + 1);  // cached: slot of each expert
@@ -784,6 +817,10 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       ptx::mbar_init(acce0 + 8 * a, 128);
     }
     ptx::mbar_init(drain, 1);
+    for (int q = 0; q < QR; ++q) {
+      ptx::mbar_init(tqf0 + 8 * q, 1);
+      ptx::mbar_init(tqe0 + 8 * q, 1 + 4);
+    }
     misc[1] = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmX);
@@ -823,42 +860,6 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
         if (e >= 0 && e < E) pre_dn[e] = m;
       }
     }
-  }
-  if (p.x != nullptr) {
-    // this CTA's contiguous share of the permuted token rows, eight 16-byte
-    // loads in flight per thread
-    const int s0 = static_cast<int>(static_cast<long long>(p.R) * blockIdx.x / gridDim.x);
-    const int s1 = static_cast<int>(static_cast<long long>(p.R) * (blockIdx.x + 1) / gridDim.x);
-    const int vpr = p.H / 8;
-    const int n = (s1 - s0) * vpr;
-    constexpr int U = 8;
-    for (int i0 = threadIdx.x; i0 < n; i0 += U * kCoreThreads) {
-      uint4 v[U];
-      int dst[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * kCoreThreads;
-        dst[u] = -1;
-        if (i < n) {
-          const int sl = s0 + i / vpr;
-          const int c = i - (sl - s0) * vpr;
-          const int r = p.perm[sl];
-          if (r >= 0 && r < p.R) {
-            v[u] = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(r / p.k) * p.H)[c];
-            dst[u] = sl * vpr + c;
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (dst[u] >= 0) reinterpret_cast<uint4*>(p.x_perm)[dst[u]] = v[u];
-    }
-    // publish to the TMA loads of every CTA: fence for the async proxy, then
-    // one arrival per CTA
-    fence_proxy_async_global();
-    __threadfence();
-    compute_sync();
-    if (threadIdx.x == 0) atomicAdd(p.ready + E + 1, 1);
   }
   compute_sync();
   if (warp == 0) {
@@ -919,11 +920,19 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
   ptx::tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const int total_gu = pre_gu[E];
-  const FSeq seq1(blockIdx.x, gridDim.x, total_gu, pre_dn[E], p.ks_gu, p.ks_dn);
+  const int total = total_gu + pre_dn[E];
   const int jB = E - nmiss;  // first position of a fetched expert
-  const FOrder seq2(blockIdx.x, gridDim.x, pre_gu[jB], pre_dn[jB], total_gu - pre_gu[jB], pre_dn[E] - pre_dn[jB],
-                    p.ks_gu, p.ks_dn);
-  auto next_tile = [&](int n) { return CACHED ? seq2.tile(n) : seq1.tile(n); };
+  const int tguA = pre_gu[jB], tdnA = pre_dn[jB], tguB = total_gu - tguA;
+  int* const queue = p.ready + E + 2;  // device-wide tile queue
+  const bool dynamic = p.R <= kFusedDynamicRows;
+  const FSeq seq1(blockIdx.x, gridDim.x, total_gu, pre_dn[E], p.ks_gu, p.ks_dn);
+  const FOrder seq2(blockIdx.x, gridDim.x, tguA, tdnA, tguB, pre_dn[E] - tdnA, p.ks_gu, p.ks_dn);
+  // the MMA issuer and the epilogue warps follow the producer's tile ids
+  auto read_tile = [&](int& qs, uint32_t& qph, int* t) -> bool {
+    if (!wait_bounded<kSpin>(tqf0 + 8 * qs, qph, misc + 1, p.status)) return false;
+    *t = tq[qs];
+    return true;
+  };
 
   auto tile_of = [&](int t) {
     FTile tl;
@@ -993,7 +1002,30 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       npend = 0;
       return true;
     };
-    for (int n = 0, t; ok && (t = next_tile(n)) >= 0; ++n) {
+    int qs = 0;
+    uint32_t qph = 0;
+    int next = dynamic ? atomicAdd(queue, 1) : 0;
+    for (int n = 0; ok; ++n) {
+      int t;
+      if (dynamic) {
+        const int g = next;
+        t = g < total ? (CACHED ? fused_tile_at(g, tguA, tdnA, tguB, total_gu) : g) : -1;
+        if (t >= 0) next = atomicAdd(queue, 1);  // the following claim, in flight while this tile's loads go out
+      } else {
+        t = CACHED ? seq2.tile(n) : seq1.tile(n);
+      }
+      // publish the tile id for the MMA issuer and the epilogue
+      if (!wait_bounded<kSpin>(tqe0 + 8 * qs, qph ^ 1u, misc + 1, p.status)) {
+        ok = false;
+        break;
+      }
+      tq[qs] = t;
+      ptx::mbar_arrive(tqf0 + 8 * qs);
+      if (++qs == QR) {
+        qs = 0;
+        qph ^= 1u;
+      }
+      if (t < 0) break;
       const FTile tl = tile_of(t);
       const int nblk = (tl.nrows + kBoxRows - 1) / kBoxRows;
       const int KS = tl.kind ? p.ks_dn : p.ks_gu;
@@ -1033,7 +1065,7 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       if (CACHED && tl.j >= jB) {
         // a fetched expert: wait until the pieces of this tile's weight block
         // have landed in its slot
-        const int* word = p.ready + E + 3 + tl.e * (p.mb_gu + p.mb_dn) + (tl.kind ? p.mb_gu : 0) + tl.mb;
+        const int* word = p.ready + E + 4 + tl.e * (p.mb_gu + p.mb_dn) + (tl.kind ? p.mb_gu : 0) + tl.mb;
         const int target = (tl.kind ? p.ks_dn : p.ks_gu) / 2;
         uint64_t t0 = 0;
         for (uint32_t it = 0; ld_acquire_gpu(word) < target; ++it) {
@@ -1107,7 +1139,20 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     uint32_t aph = 0;
     bool ok = true;
     bool issued = false;
-    for (int n = 0, t; ok && (t = next_tile(n)) >= 0; ++n) {
+    int qs = 0;
+    uint32_t qph = 0;
+    while (ok) {
+      int t = -1;
+      if (!read_tile(qs, qph, &t)) {
+        ok = false;
+        break;
+      }
+      ptx::mbar_arrive(tqe0 + 8 * qs);
+      if (++qs == QR) {
+        qs = 0;
+        qph ^= 1u;
+      }
+      if (t < 0) break;
       const FTile tl = tile_of(t);
       const int KS = tl.kind ? p.ks_dn : p.ks_gu;
       const uint32_t idesc = ptx::idesc_bf16_f32(kBM, static_cast<uint32_t>((tl.nrows + 15) & ~15));
@@ -1147,11 +1192,62 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     }
   } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue
+    if (p.x != nullptr) {
+      // Row gather, done here so that it overlaps the first weight loads:
+      // this CTA's contiguous share of the permuted token rows, eight 16-byte
+      // loads in flight per thread.  The producers start their token-row
+      // loads once every CTA has published its share.
+      constexpr int kEpiThreads = 128;
+      const int et = threadIdx.x - 64;
+      const int s0 = static_cast<int>(static_cast<long long>(p.R) * blockIdx.x / gridDim.x);
+      const int s1 = static_cast<int>(static_cast<long long>(p.R) * (blockIdx.x + 1) / gridDim.x);
+      const int vpr = p.H / 8;
+      const int n = (s1 - s0) * vpr;
+      constexpr int U = 8;
+      for (int i0 = et; i0 < n; i0 += U * kEpiThreads) {
+        uint4 v[U];
+        int dst[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + u * kEpiThreads;
+          dst[u] = -1;
+          if (i < n) {
+            const int sl = s0 + i / vpr;
+            const int c = i - (sl - s0) * vpr;
+            const int r = p.perm[sl];
+            if (r >= 0 && r < p.R) {
+              v[u] = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(r / p.k) * p.H)[c];
+              dst[u] = sl * vpr + c;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (dst[u] >= 0) reinterpret_cast<uint4*>(p.x_perm)[dst[u]] = v[u];
+      }
+      // publish to the TMA loads of every CTA: fence for the async proxy, then
+      // one arrival per CTA
+      fence_proxy_async_global();
+      __threadfence();
+      asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
+      if (et == 0) atomicAdd(p.ready + E + 1, 1);
+    }
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
-    for (int n = 0, t; (t = next_tile(n)) >= 0; ++n) {
+    int qs = 0;
+    uint32_t qph = 0;
+    for (;;) {
+      int t = -1;
+      if (!__all_sync(0xffffffffu, read_tile(qs, qph, &t))) break;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tqe0 + 8 * qs);
+      if (++qs == QR) {
+        qs = 0;
+        qph ^= 1u;
+      }
+      if (t < 0) break;
       const FTile tl = tile_of(t);
       const bool ok = wait_bounded<kSleepEpi>(accf0 + 8 * acc, aph, misc + 1, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -1220,12 +1316,12 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
   __syncthreads();
   if (misc[2]) {
     __threadfence();
-    for (int e = threadIdx.x; e < (CACHED ? E + 3 : E + 2); e += blockDim.x) p.ready[e] = 0;
+    for (int e = threadIdx.x; e < (CACHED ? E + 4 : E + 3); e += blockDim.x) p.ready[e] = 0;
     if (CACHED && nmiss > 0) {
       const int nb = p.mb_gu + p.mb_dn;
       for (int i = threadIdx.x; i < nmiss * nb; i += blockDim.x) {
         const int e = p.miss_list[i / nb];
-        if (e >= 0 && e < E) p.ready[E + 3 + e * nb + i % nb] = 0;
+        if (e >= 0 && e < E) p.ready[E + 4 + e * nb + i % nb] = 0;
       }
     }
     __threadfence();

@@ -78,7 +78,7 @@ class MoELayer:
         self.out = torch.empty((T_max, H), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.fused = (fmt == _lib.MOE_W_BF16_TILED)
-        self.sync_ws = torch.zeros((E + 2,), dtype=torch.int32, device=dev)
+        self.sync_ws = torch.zeros((E + 3,), dtype=torch.int32, device=dev)
         self._bound = {}
 
     # -- the five boundary calls, bound once per (T, x, out, stream) ---------
@@ -287,7 +287,7 @@ class CachedMoELayer(MoELayer):
         self.miss_list = torch.zeros((S,), dtype=torch.int32, device=dev)
         self.miss_slot = torch.zeros((S,), dtype=torch.int32, device=dev)
         self.stats = torch.zeros((4,), dtype=torch.int32, device=dev)
-        self.sync_ws = torch.zeros((E * (1 + self.I // 64 + H // 128) + 3,), dtype=torch.int32, device=dev)
+        self.sync_ws = torch.zeros((E * (1 + self.I // 64 + H // 128) + 4,), dtype=torch.int32, device=dev)
 
     def reset_cache(self):
         """Empty the cache and zero the running totals."""

@@ -46,7 +46,7 @@ def test_bounded_wait_runs_out_and_the_next_call_is_clean():
     miss_list = torch.tensor([E + 5], dtype=torch.int32, device=DEV)  # names no expert
     miss_slot = torch.tensor([0], dtype=torch.int32, device=DEV)
     stats = torch.tensor([0, 1, 0, 0], dtype=torch.int32, device=DEV)
-    sync = torch.zeros(E * (1 + I // 64 + H // 128) + 3, dtype=torch.int32, device=DEV)
+    sync = torch.zeros(E * (1 + I // 64 + H // 128) + 4, dtype=torch.int32, device=DEV)
     h = torch.empty((R, I), dtype=torch.bfloat16, device=DEV)
     y = torch.empty((R, H), dtype=torch.float32, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -68,7 +68,7 @@ def test_bounded_wait_runs_out_and_the_next_call_is_clean():
     h2 = torch.empty_like(h)
     y2 = torch.empty_like(y)
     st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
-    sync2 = torch.zeros(E + 2, dtype=torch.int32, device=DEV)
+    sync2 = torch.zeros(E + 3, dtype=torch.int32, device=DEV)
     _lib.moe_expert_swiglu_fused(x_perm, offsets, E, H, I, gu, dn, h2, y2, sync2, st2)
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and int(st2.item()) == 0

@@ -52,7 +52,7 @@ def run(cfg, gu, dn, b, gather, perm=None, sync=None):
     h = torch.empty((R, I), dtype=torch.bfloat16, device=DEV)
     y = torch.empty((R, H), dtype=torch.float32, device=DEV)
     if sync is None:
-        sync = torch.zeros((E + 2,), dtype=torch.int32, device=DEV)
+        sync = torch.zeros((E + 3,), dtype=torch.int32, device=DEV)
     perm = b["perm"] if perm is None else perm
     if gather:
         _lib.moe_expert_swiglu_fused(xp, b["offsets"], E, H, I, gu, dn, h, y, sync, b["st"], x=b["x"], perm=perm,
@@ -75,7 +75,7 @@ def test_gather_in_launch_bitwise(name, T):
     cfg, gu, dn = weights(name)
     b = permuted(cfg, T, seed=T + 11)
     xp0, h0, y0, _ = run(cfg, gu, dn, b, gather=False)
-    sync = torch.zeros((cfg.E + 2,), dtype=torch.int32, device=DEV)
+    sync = torch.zeros((cfg.E + 3,), dtype=torch.int32, device=DEV)
     for _ in range(2):  # two calls in a row on one sync_ws
         xp1, h1, y1, sync = run(cfg, gu, dn, b, gather=True, sync=sync)
         assert b["st"].item() == 0
