@@ -651,7 +651,9 @@ def run_stack(args, rank, world, local, dev):
             "layer_roofline": {"bytes_per_block": bytes_block,
                                "achieved_gbs": bytes_block / (step_ms / 1e3) / 1e9,
                                "frac_hbm": bytes_block / (step_ms / 1e3) / 1e9 / pk["hbm_gbs"]},
-            "clocks": sampler.summary(tw0, tw1), "gpu_launches": 6 * L * K}
+            # per layer: RMSNorm 1, route 2 (logits, selection), permute 2
+            # (grouping, row gather), gate/up 1, down 1, combine 1
+            "clocks": sampler.summary(tw0, tw1), "gpu_launches": 8 * L * K}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
