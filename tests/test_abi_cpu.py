@@ -76,6 +76,21 @@ def test_route_rejections(kw, code):
     assert _route(**kw) == code
 
 
+@pytest.mark.parametrize("kw", [dict(k=32), dict(E=1024), dict(E=1024, k=32, wsb=16 * 1024 * 4),
+                                dict(E=32, k=32)])
+def test_route_last_accepted_shapes_are_admitted(kw):
+    """The largest accepted k and E pass host admission (and reach the
+    device, absent here)."""
+    if "wsb" not in kw and kw.get("E", 512) * 16 * 4 > 16 * 512 * 4:
+        kw["wsb"] = kw["E"] * 16 * 4
+    assert _route(**kw) == _lib.MOE_ECUDA
+
+
+def test_permute_last_accepted_expert_count_is_admitted():
+    assert _permute(E=1024) == _lib.MOE_ECUDA
+    assert _permute(E=1025) == _lib.MOE_ENOTSUP
+
+
 def test_route_zero_tokens_is_noop():
     assert _route(T=0, ws=NUL, wsb=0) == _lib.MOE_OK
 

@@ -159,6 +159,27 @@ def test_route_k_equals_e_is_full_softmax():
     assert np.all(np.isinf(gap.cpu().numpy()))
 
 
+@pytest.mark.parametrize("T,H", [(5, 2560), (70, 1024)])
+def test_route_at_the_largest_accepted_shape(T, H):
+    """The last accepted expert count and route width (E = 1024, k = 32), on
+    the small-T path (T <= 64) and on the tcgen05 router path (T > 64)."""
+    E, k = 1024, 32
+    g = torch.Generator(device=DEV).manual_seed(T + H)
+    x = torch.randn((T, H), device=DEV, generator=g).to(torch.bfloat16)
+    wr = (0.02 * torch.randn((E, H), device=DEV, generator=g)).to(torch.bfloat16)
+    bias = (0.1 * torch.randn((E,), device=DEV, generator=g)).float()
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    gap = torch.empty((T,), dtype=torch.float32, device=DEV)
+    ws = torch.empty((_lib.route_workspace_size(T, E),), dtype=torch.uint8, device=DEV)
+    _lib.moe_route(x, wr, bias, k, ids, w, gap, ws)
+    torch.cuda.synchronize()
+    ids_r, w_r, gap_r, L_r = oracle.route(bits(x), bits(wr), bias.cpu().numpy(), k)
+    rep = compare_routes(ids.cpu().numpy(), w.cpu().numpy(), ids_r, w_r, gap_r, L_r)
+    assert rep["near_tie"] <= max(2, T // 10), rep
+    assert np.allclose(gap.cpu().numpy(), gap_r, atol=5e-5)
+
+
 # --------------------------------------------------------------------------
 # Grouping by expert (integer: bit-exact)
 # --------------------------------------------------------------------------
