@@ -112,21 +112,30 @@ def peaks():
             "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def gemm_source_sha():
-    src = os.path.join(ROOT, "sparse_moe_routed_gb300", "csrc", "gemm.cu")
-    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+# the files whose text a recorded DRAM-traffic figure depends on
+KERNEL_SOURCES = {
+    "fused": ["fused.cu", "gemm_common.cuh", "ptx.cuh", "common.cuh"],
+    "gateup": ["gemm.cu", "gemm_common.cuh", "ptx.cuh", "common.cuh"],
+}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "sparse_moe_routed_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, workload: str, units: float):
     """DRAM bytes per launch from a committed ncu summary (per distinct expert,
-    scaled by the launch's units), if the kernel source is unchanged."""
+    scaled by the launch's units), if the kernel's sources are unchanged."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
         ent = d.get(kernel, {}).get(workload)
-        if ent and ent.get("gemm_src_sha") == gemm_source_sha():
+        if ent and ent.get("src_sha") == kernel_source_sha(kernel):
             return ent["dram_bytes_per_unit"] * units
     except Exception:
         return None

@@ -1,0 +1,381 @@
+// int4 g64 matrix-vector contraction for decode-sized launches (a few token
+// rows per expert): codes from tile-packed records become bf16 MMA operands in
+// registers.  AFN-001 "Porting Qwen3.8-Flash-Next to Hebrus", section
+// "Phase 2": affine4 with group size 64, read as symmetric codes with one
+// bf16 scale per group.  Shared tile machinery: gemm_common.cuh.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "gemm_common.cuh"
+
+namespace moe {
+
+using namespace gk;
+
+namespace {
+
+// ============================================================ int4 GEMV
+// Decode-sized int4 tiles.  With about one token row per expert a tile is a
+// matrix-vector product, and what limits it is instructions per weight, not
+// MMA throughput: a tcgen05 MMA must read its operands from shared or tensor
+// memory, so the codes of each K step would be expanded into a 16 KB bf16
+// tile and read back (measured: ~0.35 us per 4.3 KB step), while a CUDA-core
+// dot product spends ~6 instructions per weight.  Here the weights go from
+// registers straight into warp-level MMAs (mma.sync m16n8k16, bf16 in, fp32
+// accumulate): each code pair becomes an exact bf16 pair (code - 8) in three
+// instructions, token values enter as bf16 with no conversion, and one MMA
+// instruction consumes 256 weights against up to 8 token rows.
+//
+// Warps: 0 streams packed chunks (bulk copies, deep ring), 1 stages each
+// tile's token rows (one bulk copy per row, double-buffered), the rest
+// compute in kGvGroups groups of four.  The groups take K steps in turn, so
+// each warp has several steps' time for the latency chain of one (wait,
+// loads, dequantise, MMAs).  Warp w of a group owns tile rows 32w .. 32w + 31
+// as two MMA row tiles that share the token fragments: per K step (one scale
+// group of 64 inputs) it runs eight MMAs from zero and adds scale x partial
+// to its fp32 accumulators.  In a gate/up record rows 32w .. 32w + 15 are gate
+// and 32w + 16 .. 32w + 31 the up rows of the same h columns, so each lane
+// ends a tile holding gate and up of the same outputs.  At the end of a tile
+// groups 1.. hand their sums (valid token columns only) to group 0 through
+// shared memory, which adds them in group order (a fixed order: same bits
+// every call) and stores y, or h = silu(gate) * up.  Token columns past the
+// tile's rows read stale staged rows and are never stored (an MMA column
+// depends on its own B column only).
+constexpr int kGvRows = 4;                     // token rows per tile
+constexpr int kGvN = 8;                        // MMA N: token columns (those past kGvRows are never stored)
+constexpr int kGvGroups = 4;
+constexpr int kGvWpg = 4;                      // compute warps per group, 32 rows each
+constexpr int kGvWarps = 2 + kGvWpg * kGvGroups;
+constexpr int kGvThreads = 32 * kGvWarps;
+constexpr int kGvMaxK = 2560;                  // inputs per row the token-row stage holds
+
+struct CfgV {
+  static constexpr int SQmax = 36;  // packed chunks in flight
+  // one tile's token rows, each row padded by 16 bytes so that the four
+  // rows' MMA fragment words fall in different shared-memory banks
+  static constexpr int kXBytes = kGvRows * (kGvMaxK * 2 + 16);
+  static constexpr int kUpFloats = 0;
+  static constexpr int kRedFloats = (kGvGroups - 1) * kBM * kGvRows;  // other groups' sums: [G-1][128][4]
+  static constexpr int kNumBars = 2 * SQmax + 12;
+  static constexpr int kSmemBytes = 1024 + SQmax * kQChunk + 2 * kXBytes + 2 * kUpFloats * 4 +
+                                    2 * kRedFloats * 4 + kNumBars * 8 + kSmemTail;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Codes of inputs 2p, 2p+1 of a packed word -> bf16 pair (128 + stored code),
+// exact; the stored code is the weight code + 8, so this is 136 + code.
+__device__ __forceinline__ uint32_t code_pair_biased(uint32_t word, int p) {
+  return ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+}
+
+// Codes of inputs 2p, 2p+1 of a packed word -> bf16 pair (code - 8), exact.
+__device__ __forceinline__ uint32_t code_pair_bf16x2(uint32_t word, int p) {
+  const uint32_t bits = ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;  // bf16 128 + code
+  __nv_bfloat162 b;
+  std::memcpy(&b, &bits, 4);
+  const __nv_bfloat162 v = __hsub2(b, __floats2bfloat162_rn(136.0f, 136.0f));
+  uint32_t u;
+  std::memcpy(&u, &v, 4);
+  return u;
+}
+
+template <int KIND, int QG>
+__global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
+  using C = CfgV;
+  constexpr int SQ = C::SQmax / QG;  // ring slots of QG chunks each
+  static_assert(C::SQmax % QG == 0, "ring holds whole groups");
+  const int K = p.ksteps * kBK;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;                                  // [SQ][QG x 4,352 B] packed codes + scales
+  uint8_t* sX = sQ + C::SQmax * kQChunk;               // [2][8 rows][K] bf16 token rows of a tile
+  float* sRed = reinterpret_cast<float*>(sX + 2 * C::kXBytes);  // [2][G-1][128][4] other groups' sums
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRed + 2 * C::kRedFloats);
+  const uint32_t qfull0 = ptx::smem_u32(bars);
+  const uint32_t qempty0 = qfull0 + 8 * C::SQmax;
+  const uint32_t xfull0 = qempty0 + 8 * C::SQmax;  // token rows of a tile staged (2 buffers)
+  const uint32_t xempty0 = xfull0 + 16;            // every compute warp done with them
+  const uint32_t redf0 = xempty0 + 16;             // other groups' sums written (2 buffers)
+  const uint32_t rede0 = redf0 + 16;               // group 0 done with them (2 buffers)
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
+  int* prefix = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
+  int* soff = prefix + (kMaxE + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SQ; ++s) {
+      ptx::mbar_init(qfull0 + 8 * s, 1);
+      ptx::mbar_init(qempty0 + 8 * s, QG * kGvWpg);  // every chunk is read by the warps of one group
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(xfull0 + 8 * b, 1);
+      ptx::mbar_init(xempty0 + 8 * b, kGvWpg * kGvGroups);
+      ptx::mbar_init(redf0 + 8 * b, kGvWpg * (kGvGroups - 1));
+      ptx::mbar_init(rede0 + 8 * b, kGvWpg);
+    }
+    misc[1] = 0;
+    ptx::fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_trigger();
+  const int total = build_schedule<kGvRows>(p, false, E, prefix, soff);
+  const Sched sc{prefix, soff, E, p.mblocks, kGvRows};
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ packed chunk producer
+    const uint64_t pol = ptx::policy_evict_first();
+    uint32_t armed_mask = 0, armed_ph = 0;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = sc.tile(t);
+      for (int ks = 0; ks < p.ksteps; ks += QG) {
+        if (!wait_bounded<kSpin>(qempty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = qfull0 + 8 * s;
+        armed_mask |= 1u << s;
+        armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+        ptx::mbar_arrive_expect_tx(fb, QG * kQChunk);
+        const size_t chunk = (static_cast<size_t>(tl.e) * p.mblocks + tl.mb) * p.ksteps + ks;
+        ptx::bulk_load(ptx::smem_u32(sQ + s * QG * kQChunk), p.tiles + chunk * kQChunk, QG * kQChunk, fb, pol);
+        if (++s == SQ) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (!ok || misc[1]) {
+      for (int q = 0; q < SQ; ++q)
+        if ((armed_mask >> q) & 1u) wait_drain(qfull0 + 8 * q, (armed_ph >> q) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------ token-row producer
+    const uint64_t pol = ptx::policy_evict_last();
+    uint32_t armed_mask = 0, armed_ph = 0;
+    bool ok = true;
+    int ntile = 0;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++ntile) {
+      const Tile tl = sc.tile(t);
+      const int b = ntile & 1;
+      const uint32_t use = static_cast<uint32_t>(ntile >> 1) & 1u;
+      if (!wait_bounded<kSpin>(xempty0 + 8 * b, use ^ 1u, misc + 1, p.status)) {
+        ok = false;
+        break;
+      }
+      const int n = min(tl.nrows, kGvRows);
+      const uint32_t fb = xfull0 + 8 * b;
+      armed_mask |= 1u << b;
+      armed_ph = (armed_ph & ~(1u << b)) | (use << b);
+      ptx::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(n * K * 2));
+      for (int j = 0; j < n; ++j)
+        ptx::bulk_load(ptx::smem_u32(sX + b * C::kXBytes + j * (K * 2 + 16)), p.brows + static_cast<size_t>(tl.row0 + j) * K,
+                       static_cast<uint32_t>(K * 2), fb, pol);
+    }
+    if (!ok || misc[1]) {
+      for (int q = 0; q < 2; ++q)
+        if ((armed_mask >> q) & 1u) wait_drain(xfull0 + 8 * q, (armed_ph >> q) & 1u);
+    }
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------- compute
+    const int grp = (warp - 2) / kGvWpg;  // takes the K steps gk with gk % kGvGroups == grp
+    const int cw = (warp - 2) % kGvWpg;   // owns tile rows 32 cw .. 32 cw + 31
+    const int g = lane >> 2;              // MMA fragment row group / token column
+    const int q = lane & 3;               // thread in group
+    const int r0 = 32 * cw + g;           // rows r0, r0 + 8 (tile 0), r0 + 16, r0 + 24 (tile 1)
+    uint32_t gbase = 0;  // running K step of this CTA at the start of the tile
+    int ntile = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++ntile) {
+      const Tile tl = sc.tile(t);
+      const int b = ntile & 1;
+      const uint32_t use = static_cast<uint32_t>(ntile >> 1) & 1u;
+      bool got = wait_bounded<kSpin>(xfull0 + 8 * b, use, misc + 1, p.status);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      // B fragments read token row g of the stage; columns g >= the tile's
+      // rows read a stale row and are never stored
+      const uint32_t* xrow =
+          reinterpret_cast<const uint32_t*>(sX + b * C::kXBytes + (g & (kGvRows - 1)) * (K * 2 + 16));
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const int ks0 = static_cast<int>((static_cast<uint32_t>(grp) + kGvGroups - gbase % kGvGroups) % kGvGroups);
+      for (int ks = ks0; ks < p.ksteps; ks += kGvGroups) {
+        const uint32_t gk = gbase + ks;
+        const uint32_t gg = gk / QG;
+        const uint32_t sq = gg % SQ;
+        const uint32_t phq = (gg / SQ) & 1u;
+        got = wait_bounded<kSpin>(qfull0 + 8 * sq, phq, misc + 1, p.status);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* chunk = sQ + (sq * QG + (gk - gg * QG)) * kQChunk;
+        uint32_t w[4][8];  // codes of rows r0, r0 + 8, r0 + 16, r0 + 24
+        float sc4[4];
+        const uint16_t* scl = reinterpret_cast<const uint16_t*>(chunk + kQBytes);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 c0 = reinterpret_cast<const uint4*>(chunk + (r0 + 8 * i) * 32)[0];
+          const uint4 c1 = reinterpret_cast<const uint4*>(chunk + (r0 + 8 * i) * 32)[1];
+          w[i][0] = c0.x;
+          w[i][1] = c0.y;
+          w[i][2] = c0.z;
+          w[i][3] = c0.w;
+          w[i][4] = c1.x;
+          w[i][5] = c1.y;
+          w[i][6] = c1.z;
+          w[i][7] = c1.w;
+          sc4[i] = bf16_to_f32(scl[r0 + 8 * i]);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(qempty0 + 8 * sq);
+        const uint32_t* xk = xrow + ks * (kBK / 2) + q;  // token row words of this K step
+        // The MMAs take the codes as exact bf16 (136 + code) pairs, two
+        // instructions a pair; a ninth MMA with all-ones A sums each token's
+        // 64 inputs, and sum((136 + c) x) - 136 sum(x) = sum(c x).
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // k16 block j: inputs 16 j .. 16 j + 15 of the step
+          const uint32_t b0 = xk[8 * j], b1 = xk[8 * j + 4];
+          uint32_t a[4];
+          a[0] = code_pair_biased(w[0][2 * j], q);      // row r0, inputs 16j + 2q, +1
+          a[1] = code_pair_biased(w[1][2 * j], q);      // row r0 + 8
+          a[2] = code_pair_biased(w[0][2 * j + 1], q);  // row r0, inputs 16j + 8 + 2q, +1
+          a[3] = code_pair_biased(w[1][2 * j + 1], q);  // row r0 + 8
+          mma_16816_bf16(d0, a, b0, b1);
+          a[0] = code_pair_biased(w[2][2 * j], q);      // row r0 + 16
+          a[1] = code_pair_biased(w[3][2 * j], q);      // row r0 + 24
+          a[2] = code_pair_biased(w[2][2 * j + 1], q);
+          a[3] = code_pair_biased(w[3][2 * j + 1], q);
+          mma_16816_bf16(d1, a, b0, b1);
+          mma_16816_bf16(dx, ones, b0, b1);
+        }
+        acc[0] = fmaf(sc4[0], fmaf(-136.0f, dx[0], d0[0]), acc[0]);  // row r0, token 2q
+        acc[1] = fmaf(sc4[0], fmaf(-136.0f, dx[1], d0[1]), acc[1]);  // row r0, token 2q + 1
+        acc[2] = fmaf(sc4[1], fmaf(-136.0f, dx[0], d0[2]), acc[2]);  // row r0 + 8
+        acc[3] = fmaf(sc4[1], fmaf(-136.0f, dx[1], d0[3]), acc[3]);
+        acc[4] = fmaf(sc4[2], fmaf(-136.0f, dx[0], d1[0]), acc[4]);  // row r0 + 16
+        acc[5] = fmaf(sc4[2], fmaf(-136.0f, dx[1], d1[1]), acc[5]);
+        acc[6] = fmaf(sc4[3], fmaf(-136.0f, dx[0], d1[2]), acc[6]);  // row r0 + 24
+        acc[7] = fmaf(sc4[3], fmaf(-136.0f, dx[1], d1[3]), acc[7]);
+      }
+      if (!ok) break;
+      gbase += static_cast<uint32_t>(p.ksteps);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(xempty0 + 8 * b);
+      // groups 1.. hand their sums of the valid token columns (lanes q < 2)
+      // to group 0
+      if (grp > 0) {
+        got = wait_bounded<kSleepEpi>(rede0 + 8 * b, use ^ 1u, misc + 1, p.status);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        if (q < kGvRows / 2) {
+          float* red = sRed + b * C::kRedFloats + (grp - 1) * (kBM * kGvRows);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            red[(r0 + 8 * i) * kGvRows + 2 * q] = acc[2 * i];
+            red[(r0 + 8 * i) * kGvRows + 2 * q + 1] = acc[2 * i + 1];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(redf0 + 8 * b);
+        continue;
+      }
+      got = wait_bounded<kSpin>(redf0 + 8 * b, use, misc + 1, p.status);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      if (q < kGvRows / 2) {
+#pragma unroll
+        for (int gi = 0; gi < kGvGroups - 1; ++gi) {
+          const float* red = sRed + b * C::kRedFloats + gi * (kBM * kGvRows);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += red[(r0 + 8 * i) * kGvRows + 2 * q];
+            acc[2 * i + 1] += red[(r0 + 8 * i) * kGvRows + 2 * q + 1];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(rede0 + 8 * b);
+      const int t0 = 2 * q, t1 = 2 * q + 1;
+      if (KIND == 1) {
+        float* y = reinterpret_cast<float*>(p.out);
+        const int col = tl.mb * kBM;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (t0 < tl.nrows) y[static_cast<size_t>(tl.row0 + t0) * p.ldo + col + r0 + 8 * i] = acc[2 * i];
+          if (t1 < tl.nrows) y[static_cast<size_t>(tl.row0 + t1) * p.ldo + col + r0 + 8 * i] = acc[2 * i + 1];
+        }
+        continue;
+      }
+      // gate/up tile: gate row 32 cw + r (r = g or g + 8) pairs with up row
+      // 32 cw + 16 + r, both in this lane: h index 16 cw + r
+      uint16_t* h = reinterpret_cast<uint16_t*>(p.out);
+      const int colA = tl.mb * 64 + 16 * cw + g, colB = colA + 8;
+      if (t0 < tl.nrows) {
+        const size_t o = static_cast<size_t>(tl.row0 + t0) * p.ldo;
+        h[o + colA] = f32_to_bf16(acc[0] / (1.0f + expf(-acc[0])) * acc[4]);
+        h[o + colB] = f32_to_bf16(acc[2] / (1.0f + expf(-acc[2])) * acc[6]);
+      }
+      if (t1 < tl.nrows) {
+        const size_t o = static_cast<size_t>(tl.row0 + t1) * p.ldo;
+        h[o + colA] = f32_to_bf16(acc[1] / (1.0f + expf(-acc[1])) * acc[5]);
+        h[o + colB] = f32_to_bf16(acc[3] / (1.0f + expf(-acc[3])) * acc[7]);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+template <int KIND, int QG>
+cudaError_t run_gemv_q4_g(const GemmArgs& args, cudaStream_t st) {
+  auto kern = gemv_q4_kernel<KIND, QG>;
+  cudaError_t e = ensure_smem(kern, CfgV::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = sm_count();
+  if (grid <= 0) return cudaErrorNoDevice;
+  return launch_pdl(kern, dim3(grid), dim3(kGvThreads), CfgV::kSmemBytes, st, args);
+}
+
+template <int KIND>
+cudaError_t run_gemv_q4(const GemmArgs& args, cudaStream_t st) {
+  return args.qgroup == 2 ? run_gemv_q4_g<KIND, 2>(args, st) : run_gemv_q4_g<KIND, 1>(args, st);
+}
+
+}  // namespace
+
+namespace gk {
+
+// Decode-sized int4 launches (few rows per expert, K within the token-row
+// stage) go to the CUDA-core kernel.
+bool use_gemv_q4(int fmt, int R, int K) {
+  return fmt == MOE_W_INT4_G64_TILED && pick_nmax(R) == 16 && K <= kGvMaxK;
+}
+
+cudaError_t launch_gemv_q4(int kind, const GemmArgs& args, cudaStream_t st) {
+  return kind == 1 ? run_gemv_q4<1>(args, st) : run_gemv_q4<0>(args, st);
+}
+
+}  // namespace gk
+
+}  // namespace moe

@@ -273,6 +273,7 @@ __device__ __forceinline__ int select_topk(const float (&lv)[EPL], const float (
       done = true;
     }
   }
+  uint32_t rank32_key = 0;  // with k = 32 the next logit (rank 32) has no lane of its own
   if (!done) {
     sort_desc<EPL>(v);
     for (int r = 0; r < n; ++r) {
@@ -286,11 +287,13 @@ __device__ __forceinline__ int select_topk(const float (&lv)[EPL], const float (
         v[EPL - 1] = 0;
       }
       if (lane == r) mine = (static_cast<uint64_t>(m_hi) << 32) | m_lo;
+      if (r == 32) rank32_key = m_hi;
     }
   }
   const uint32_t my_key = static_cast<uint32_t>(mine >> 32);
   const int my_e = static_cast<int>(~static_cast<uint32_t>(mine));
-  const uint32_t next_key = static_cast<uint32_t>(__shfl_sync(0xffffffffu, mine, k & 31) >> 32);
+  const uint32_t next_key =
+      k < 32 ? static_cast<uint32_t>(__shfl_sync(0xffffffffu, mine, k & 31) >> 32) : rank32_key;
   const float my_v = key2f(my_key);
   const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
   const float ex = (lane < k) ? expf(my_v - v0) : 0.f;
