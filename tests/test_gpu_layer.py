@@ -159,11 +159,12 @@ def test_route_k_equals_e_is_full_softmax():
     assert np.all(np.isinf(gap.cpu().numpy()))
 
 
-@pytest.mark.parametrize("T,H", [(5, 2560), (70, 1024)])
-def test_route_at_the_largest_accepted_shape(T, H):
+@pytest.mark.parametrize("T,H,E,k", [(5, 2560, 1024, 32), (70, 1024, 1024, 32), (3, 256, 100, 7),
+                                     (4, 128, 33, 32), (64, 384, 96, 31)])
+def test_route_at_the_largest_accepted_shape(T, H, E, k):
     """The last accepted expert count and route width (E = 1024, k = 32), on
-    the small-T path (T <= 64) and on the tcgen05 router path (T > 64)."""
-    E, k = 1024, 32
+    the small-T path (T <= 64) and on the tcgen05 router path (T > 64); and
+    odd shapes: E not a multiple of 32, k + 1 = E, k = 31."""
     g = torch.Generator(device=DEV).manual_seed(T + H)
     x = torch.randn((T, H), device=DEV, generator=g).to(torch.bfloat16)
     wr = (0.02 * torch.randn((E, H), device=DEV, generator=g)).to(torch.bfloat16)
@@ -276,7 +277,8 @@ def test_expert_stage_parity(name, T, nslots):
 # --------------------------------------------------------------------------
 # Combine
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("T,k,H,residual", [(16, 10, 2560, False), (5, 4, 256, True), (129, 10, 2560, True)])
+@pytest.mark.parametrize("T,k,H,residual", [(16, 10, 2560, False), (5, 4, 256, True), (129, 10, 2560, True),
+                                             (7, 32, 256, True)])
 def test_combine_parity(T, k, H, residual):
     rng = np.random.default_rng(T + k)
     E = 64 if k <= 10 else 128
@@ -321,7 +323,15 @@ def test_combine_nonfinite_flag():
                                                   ("decode", 37, 37, False), ("prefill", None, 24, False),
                                                   ("tiny", None, 16, True), ("decode", None, 16, True),
                                                   ("decode", 37, 37, True), ("decode", 1, 1, True),
-                                                  ("prefill", None, 24, True)])
+                                                  ("prefill", None, 24, True),
+                                                  # edges of the launch choices: token rows per tile
+                                                  # (R 320 / 330, 1,280 / 1,290), the router's small-T path
+                                                  # (T 64 / 65), the in-launch gather and tile queue
+                                                  # (R 4,090 / 4,100)
+                                                  ("decode", 32, 12, True), ("decode", 33, 12, True),
+                                                  ("decode", 64, 12, True), ("decode", 65, 12, True),
+                                                  ("decode", 128, 12, True), ("decode", 129, 12, True),
+                                                  ("decode", 409, 12, True), ("decode", 410, 12, True)])
 def test_layer_parity(name, T, nsample, tiled):
     cfg, d, host = case(name, T)
     layer, out = run_layer(cfg, d, tiled)
