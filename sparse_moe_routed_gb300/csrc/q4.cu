@@ -22,9 +22,10 @@ namespace {
 // tile and read back (measured: ~0.35 us per 4.3 KB step), while a CUDA-core
 // dot product spends ~6 instructions per weight.  Here the weights go from
 // registers straight into warp-level MMAs (mma.sync m16n8k16, bf16 in, fp32
-// accumulate): each code pair becomes an exact bf16 pair (code - 8) in three
-// instructions, token values enter as bf16 with no conversion, and one MMA
-// instruction consumes 256 weights against up to 8 token rows.
+// accumulate): each code pair becomes an exact bf16 pair (136 + code) in two
+// instructions (an all-ones MMA supplies the 136 x sum(x) correction), token
+// values enter as bf16 with no conversion, and one MMA instruction consumes
+// 256 weights against up to 8 token rows.
 //
 // Warps: 0 streams packed chunks (bulk copies, deep ring), 1 stages each
 // tile's token rows (one bulk copy per row, double-buffered), the rest
@@ -41,6 +42,12 @@ namespace {
 // every call) and stores y, or h = silu(gate) * up.  Token columns past the
 // tile's rows read stale staged rows and are never stored (an MMA column
 // depends on its own B column only).
+//
+// Down tiles (K = I = 640: ten K steps) are short, so the per-tile work of
+// the group split (staging, the hand-over of sums) weighs more: when a
+// record's 128-row blocks pair up, a down tile spans two of them (256 rows)
+// and the compute warps form two groups of eight, each warp owning 32 rows of
+// one block; a ring slot then holds both blocks' chunks of one K step.
 constexpr int kGvRows = 4;                     // token rows per tile
 constexpr int kGvN = 8;                        // MMA N: token columns (those past kGvRows are never stored)
 constexpr int kGvGroups = 4;
@@ -87,11 +94,18 @@ __device__ __forceinline__ uint32_t code_pair_bf16x2(uint32_t word, int p) {
   return u;
 }
 
-template <int KIND, int QG>
+template <int KIND, int QG, bool PAIR>
 __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   using C = CfgV;
-  constexpr int SQ = C::SQmax / QG;  // ring slots of QG chunks each
-  static_assert(C::SQmax % QG == 0, "ring holds whole groups");
+  static_assert(!PAIR || (KIND == 1 && QG == 1), "paired blocks: down tiles, one K step per slot");
+  constexpr int G = PAIR ? 2 : kGvGroups;         // K-step groups
+  constexpr int WPG = PAIR ? 2 * kGvWpg : kGvWpg;  // compute warps per group, 32 rows each
+  constexpr int RT = 32 * WPG;                     // weight rows per tile
+  constexpr int CPS = PAIR ? 2 : QG;               // chunks per ring slot
+  constexpr int SQ = C::SQmax / CPS;               // ring slots
+  static_assert(C::SQmax % CPS == 0, "ring holds whole slots");
+  static_assert(G * WPG == kGvGroups * kGvWpg, "all compute warps");
+  static_assert((G - 1) * RT * kGvRows <= C::kRedFloats, "hand-over buffer");
   const int K = p.ksteps * kBK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -116,21 +130,23 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < SQ; ++s) {
       ptx::mbar_init(qfull0 + 8 * s, 1);
-      ptx::mbar_init(qempty0 + 8 * s, QG * kGvWpg);  // every chunk is read by the warps of one group
+      ptx::mbar_init(qempty0 + 8 * s, PAIR ? WPG : QG * WPG);  // every chunk is read by the warps of one group
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(xfull0 + 8 * b, 1);
-      ptx::mbar_init(xempty0 + 8 * b, kGvWpg * kGvGroups);
-      ptx::mbar_init(redf0 + 8 * b, kGvWpg * (kGvGroups - 1));
-      ptx::mbar_init(rede0 + 8 * b, kGvWpg);
+      ptx::mbar_init(xempty0 + 8 * b, WPG * G);
+      ptx::mbar_init(redf0 + 8 * b, WPG * (G - 1));
+      ptx::mbar_init(rede0 + 8 * b, WPG);
     }
     misc[1] = 0;
     ptx::fence_mbar_init();
   }
   pdl_wait();
   pdl_trigger();
-  const int total = build_schedule<kGvRows>(p, false, E, prefix, soff);
-  const Sched sc{prefix, soff, E, p.mblocks, kGvRows};
+  GemmArgs ps = p;  // the schedule counts tiles of RT rows
+  if (PAIR) ps.mblocks = p.mblocks / 2;
+  const int total = build_schedule<kGvRows>(ps, false, E, prefix, soff);
+  const Sched sc{prefix, soff, E, ps.mblocks, kGvRows};
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ packed chunk producer
@@ -141,7 +157,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = sc.tile(t);
-      for (int ks = 0; ks < p.ksteps; ks += QG) {
+      for (int ks = 0; ks < p.ksteps; ks += PAIR ? 1 : QG) {
         if (!wait_bounded<kSpin>(qempty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
           ok = false;
           break;
@@ -149,9 +165,17 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
         const uint32_t fb = qfull0 + 8 * s;
         armed_mask |= 1u << s;
         armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-        ptx::mbar_arrive_expect_tx(fb, QG * kQChunk);
-        const size_t chunk = (static_cast<size_t>(tl.e) * p.mblocks + tl.mb) * p.ksteps + ks;
-        ptx::bulk_load(ptx::smem_u32(sQ + s * QG * kQChunk), p.tiles + chunk * kQChunk, QG * kQChunk, fb, pol);
+        ptx::mbar_arrive_expect_tx(fb, CPS * kQChunk);
+        if (PAIR) {
+          // K step ks of the tile's two 128-row blocks
+          const size_t c0 = (static_cast<size_t>(tl.e) * p.mblocks + 2 * tl.mb) * p.ksteps + ks;
+          ptx::bulk_load(ptx::smem_u32(sQ + s * CPS * kQChunk), p.tiles + c0 * kQChunk, kQChunk, fb, pol);
+          ptx::bulk_load(ptx::smem_u32(sQ + (s * CPS + 1) * kQChunk), p.tiles + (c0 + p.ksteps) * kQChunk, kQChunk,
+                         fb, pol);
+        } else {
+          const size_t chunk = (static_cast<size_t>(tl.e) * p.mblocks + tl.mb) * p.ksteps + ks;
+          ptx::bulk_load(ptx::smem_u32(sQ + s * QG * kQChunk), p.tiles + chunk * kQChunk, QG * kQChunk, fb, pol);
+        }
         if (++s == SQ) {
           s = 0;
           ph ^= 1u;
@@ -191,8 +215,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------- compute
-    const int grp = (warp - 2) / kGvWpg;  // takes the K steps gk with gk % kGvGroups == grp
-    const int cw = (warp - 2) % kGvWpg;   // owns tile rows 32 cw .. 32 cw + 31
+    const int grp = (warp - 2) / WPG;  // takes the K steps gk with gk % G == grp
+    const int cwg = (warp - 2) % WPG;  // owns tile rows 32 cwg .. 32 cwg + 31
+    const int blk = cwg / kGvWpg;      // the 128-row block (chunk) of those rows
+    const int cw = cwg % kGvWpg;       // rows 32 cw .. 32 cw + 31 of that block
     const int g = lane >> 2;              // MMA fragment row group / token column
     const int q = lane & 3;               // thread in group
     const int r0 = 32 * cw + g;           // rows r0, r0 + 8 (tile 0), r0 + 16, r0 + 24 (tile 1)
@@ -213,10 +239,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       const uint32_t* xrow =
           reinterpret_cast<const uint32_t*>(sX + b * C::kXBytes + (g & (kGvRows - 1)) * (K * 2 + 16));
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      const int ks0 = static_cast<int>((static_cast<uint32_t>(grp) + kGvGroups - gbase % kGvGroups) % kGvGroups);
-      for (int ks = ks0; ks < p.ksteps; ks += kGvGroups) {
+      const int ks0 = static_cast<int>((static_cast<uint32_t>(grp) + G - gbase % G) % G);
+      for (int ks = ks0; ks < p.ksteps; ks += G) {
         const uint32_t gk = gbase + ks;
-        const uint32_t gg = gk / QG;
+        const uint32_t gg = PAIR ? gk : gk / QG;
         const uint32_t sq = gg % SQ;
         const uint32_t phq = (gg / SQ) & 1u;
         got = wait_bounded<kSpin>(qfull0 + 8 * sq, phq, misc + 1, p.status);
@@ -224,7 +250,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
           ok = false;
           break;
         }
-        const uint8_t* chunk = sQ + (sq * QG + (gk - gg * QG)) * kQChunk;
+        const uint8_t* chunk = sQ + (sq * CPS + (PAIR ? static_cast<uint32_t>(blk) : gk - gg * QG)) * kQChunk;
         uint32_t w[4][8];  // codes of rows r0, r0 + 8, r0 + 16, r0 + 24
         float sc4[4];
         const uint16_t* scl = reinterpret_cast<const uint16_t*>(chunk + kQBytes);
@@ -288,7 +314,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
           break;
         }
         if (q < kGvRows / 2) {
-          float* red = sRed + b * C::kRedFloats + (grp - 1) * (kBM * kGvRows);
+          float* red = sRed + b * C::kRedFloats + (grp - 1) * (RT * kGvRows) + blk * (kBM * kGvRows);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             red[(r0 + 8 * i) * kGvRows + 2 * q] = acc[2 * i];
@@ -306,8 +332,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       }
       if (q < kGvRows / 2) {
 #pragma unroll
-        for (int gi = 0; gi < kGvGroups - 1; ++gi) {
-          const float* red = sRed + b * C::kRedFloats + gi * (kBM * kGvRows);
+        for (int gi = 0; gi < G - 1; ++gi) {
+          const float* red = sRed + b * C::kRedFloats + gi * (RT * kGvRows) + blk * (kBM * kGvRows);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             acc[2 * i] += red[(r0 + 8 * i) * kGvRows + 2 * q];
@@ -320,7 +346,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       const int t0 = 2 * q, t1 = 2 * q + 1;
       if (KIND == 1) {
         float* y = reinterpret_cast<float*>(p.out);
-        const int col = tl.mb * kBM;
+        const int col = tl.mb * RT + blk * kBM;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           if (t0 < tl.nrows) y[static_cast<size_t>(tl.row0 + t0) * p.ldo + col + r0 + 8 * i] = acc[2 * i];
@@ -347,9 +373,9 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   __syncthreads();
 }
 
-template <int KIND, int QG>
+template <int KIND, int QG, bool PAIR>
 cudaError_t run_gemv_q4_g(const GemmArgs& args, cudaStream_t st) {
-  auto kern = gemv_q4_kernel<KIND, QG>;
+  auto kern = gemv_q4_kernel<KIND, QG, PAIR>;
   cudaError_t e = ensure_smem(kern, CfgV::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = sm_count();
@@ -359,7 +385,8 @@ cudaError_t run_gemv_q4_g(const GemmArgs& args, cudaStream_t st) {
 
 template <int KIND>
 cudaError_t run_gemv_q4(const GemmArgs& args, cudaStream_t st) {
-  return args.qgroup == 2 ? run_gemv_q4_g<KIND, 2>(args, st) : run_gemv_q4_g<KIND, 1>(args, st);
+  if (KIND == 1 && args.mblocks % 2 == 0) return run_gemv_q4_g<1, 1, true>(args, st);
+  return args.qgroup == 2 ? run_gemv_q4_g<KIND, 2, false>(args, st) : run_gemv_q4_g<KIND, 1, false>(args, st);
 }
 
 }  // namespace

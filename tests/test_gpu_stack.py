@@ -76,7 +76,7 @@ def test_int4_stack_layer_parity(T):
 
 
 def test_int4_expert_stage_tiny_geometry():
-    """int4 contraction on the tiny geometry (one 128-row block, K = 256 / 64)."""
+    """int4 contraction on the tiny geometry (two 128-row down blocks, K = 256 / 64)."""
     cfg = wl.TINY
     d = wl.layer_inputs(cfg, DEV)
     q_gu, s_gu = wl.quantize_int4_g64(d["w_gateup"])
@@ -112,12 +112,19 @@ def test_int4_expert_stage_tiny_geometry():
     assert_output_close(y.cpu().numpy(), ref, what="int4 expert outputs (tiny)")
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode"])
+# an odd number of 128-row blocks on both sides (H = 384, 2I = 384): the down
+# launch cannot pair its blocks into 256-row tiles and takes the four-group split
+ODD = wl.LayerConfig("int4_odd", T=16, H=384, E=64, k=4, I=192, bias=None, seed=19)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "odd"])
 def test_int4_skewed_routes_split_tiles(name):
     """Decode-sized int4 launches run on the CUDA-core kernel, which splits an
     expert's rows into tiles of 4: routes skewed so that one expert gets 9
-    rows (three tiles), others 1-5, graded row by row against the oracle."""
-    cfg = wl.CONFIGS[name]
+    rows (three tiles), others 1-5, graded row by row against the oracle.
+    Down launches with an even block count pair two blocks per tile, odd ones
+    do not: both are covered."""
+    cfg = ODD if name == "odd" else wl.CONFIGS[name]
     T, k, E = 16, cfg.k, cfg.E
     d = wl.layer_inputs(cfg, DEV)
     q_gu, s_gu = wl.quantize_int4_g64(d["w_gateup"])
