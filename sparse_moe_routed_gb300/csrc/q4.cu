@@ -22,8 +22,8 @@ namespace {
 // tile and read back (measured: ~0.35 us per 4.3 KB step), while a CUDA-core
 // dot product spends ~6 instructions per weight.  Here the weights go from
 // registers straight into warp-level MMAs (mma.sync m16n8k16, bf16 in, fp32
-// accumulate): each code pair becomes an exact bf16 pair (136 + code) in two
-// instructions (an all-ones MMA supplies the 136 x sum(x) correction), token
+// accumulate): each code pair becomes an exact bf16 pair (136 + code) in one
+// or two instructions (an all-ones MMA supplies the 136 x sum(x) correction), token
 // values enter as bf16 with no conversion, and one MMA instruction consumes
 // 256 weights against up to 8 token rows.
 //
@@ -34,7 +34,13 @@ namespace {
 // loads, dequantise, MMAs).  Warp w of a group owns tile rows 32w .. 32w + 31
 // as two MMA row tiles that share the token fragments: per K step (one scale
 // group of 64 inputs) it runs eight MMAs from zero and adds scale x partial
-// to its fp32 accumulators.  In a gate/up record rows 32w .. 32w + 15 are gate
+// to its fp32 accumulators.  The MMA's k slots run over the step's inputs in
+// a permuted order (the same for weights and tokens), chosen so that each
+// lane reads 16 consecutive inputs: one 8-byte load per weight row, two
+// 16-byte loads of token values, and every code pair at a fixed nibble
+// position.  A group takes whole ring slots (two K steps for gate/up
+// records), so the wait, the release and the address arithmetic of a slot
+// are shared by two steps' MMAs.  In a gate/up record rows 32w .. 32w + 15 are gate
 // and 32w + 16 .. 32w + 31 the up rows of the same h columns, so each lane
 // ends a tile holding gate and up of the same outputs.  At the end of a tile
 // groups 1.. hand their sums (valid token columns only) to group 0 through
@@ -55,6 +61,7 @@ constexpr int kGvWpg = 4;                      // compute warps per group, 32 ro
 constexpr int kGvWarps = 2 + kGvWpg * kGvGroups;
 constexpr int kGvThreads = 32 * kGvWarps;
 constexpr int kGvMaxK = 2560;                  // inputs per row the token-row stage holds
+static_assert(kGvRows <= kGvN, "a tile's token rows fit the MMA's columns");
 
 struct CfgV {
   static constexpr int SQmax = 36;  // packed chunks in flight
@@ -77,21 +84,19 @@ __device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same MMA with a zero accumulator in.
+__device__ __forceinline__ void mma_16816_bf16_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 // Codes of inputs 2p, 2p+1 of a packed word -> bf16 pair (128 + stored code),
 // exact; the stored code is the weight code + 8, so this is 136 + code.
 __device__ __forceinline__ uint32_t code_pair_biased(uint32_t word, int p) {
   return ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
-}
-
-// Codes of inputs 2p, 2p+1 of a packed word -> bf16 pair (code - 8), exact.
-__device__ __forceinline__ uint32_t code_pair_bf16x2(uint32_t word, int p) {
-  const uint32_t bits = ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;  // bf16 128 + code
-  __nv_bfloat162 b;
-  std::memcpy(&b, &bits, 4);
-  const __nv_bfloat162 v = __hsub2(b, __floats2bfloat162_rn(136.0f, 136.0f));
-  uint32_t u;
-  std::memcpy(&u, &v, 4);
-  return u;
 }
 
 template <int KIND, int QG, bool PAIR>
@@ -103,6 +108,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   constexpr int RT = 32 * WPG;                     // weight rows per tile
   constexpr int CPS = PAIR ? 2 : QG;               // chunks per ring slot
   constexpr int SQ = C::SQmax / CPS;               // ring slots
+  constexpr int S = PAIR ? 1 : QG;                 // K steps per ring slot (one group reads them all)
   static_assert(C::SQmax % CPS == 0, "ring holds whole slots");
   static_assert(G * WPG == kGvGroups * kGvWpg, "all compute warps");
   static_assert((G - 1) * RT * kGvRows <= C::kRedFloats, "hand-over buffer");
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < SQ; ++s) {
       ptx::mbar_init(qfull0 + 8 * s, 1);
-      ptx::mbar_init(qempty0 + 8 * s, PAIR ? WPG : QG * WPG);  // every chunk is read by the warps of one group
+      ptx::mbar_init(qempty0 + 8 * s, WPG);  // a slot is read by the warps of one group
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(xfull0 + 8 * b, 1);
@@ -215,7 +221,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------- compute
-    const int grp = (warp - 2) / WPG;  // takes the K steps gk with gk % G == grp
+    const int grp = (warp - 2) / WPG;  // takes the ring slots gu with gu % G == grp
     const int cwg = (warp - 2) % WPG;  // owns tile rows 32 cwg .. 32 cwg + 31
     const int blk = cwg / kGvWpg;      // the 128-row block (chunk) of those rows
     const int cw = cwg % kGvWpg;       // rows 32 cw .. 32 cw + 31 of that block
@@ -236,70 +242,79 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       }
       // B fragments read token row g of the stage; columns g >= the tile's
       // rows read a stale row and are never stored
-      const uint32_t* xrow =
-          reinterpret_cast<const uint32_t*>(sX + b * C::kXBytes + (g & (kGvRows - 1)) * (K * 2 + 16));
+      const uint32_t kOnes[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // bf16 1.0 pairs
+      const uint8_t* xrow = sX + b * C::kXBytes + (g & (kGvRows - 1)) * (K * 2 + 16) + 32 * q;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      const int ks0 = static_cast<int>((static_cast<uint32_t>(grp) + G - gbase % G) % G);
-      for (int ks = ks0; ks < p.ksteps; ks += G) {
-        const uint32_t gk = gbase + ks;
-        const uint32_t gg = PAIR ? gk : gk / QG;
-        const uint32_t sq = gg % SQ;
-        const uint32_t phq = (gg / SQ) & 1u;
-        got = wait_bounded<kSpin>(qfull0 + 8 * sq, phq, misc + 1, p.status);
+      // The MMA's k slots run over a step's 64 inputs in a permuted order
+      // (the same for weights and tokens, so the products and their sum are
+      // unchanged): in k16 block j, lane q's slots 2q, 2q + 1 take inputs
+      // 16q + 4j, +1 and slots 2q + 8, 2q + 9 take inputs 16q + 4j + 2, +3.
+      // Lane q thus reads inputs 16q .. 16q + 15 only: 8 code bytes per
+      // weight row and 32 bytes of each token row, and every code pair sits
+      // at a fixed nibble position.  A group takes whole ring slots (S
+      // consecutive K steps): one wait and one release per slot.
+      const int nslot = p.ksteps / S;
+      const uint32_t sbase = gbase / S;  // this CTA's running ring-slot index at the tile's start
+      for (int u = static_cast<int>((static_cast<uint32_t>(grp) + G - sbase % G) % G); u < nslot; u += G) {
+        const uint32_t gu = sbase + u;
+        const uint32_t sq = gu % SQ;
+        got = wait_bounded<kSpin>(qfull0 + 8 * sq, (gu / SQ) & 1u, misc + 1, p.status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        const uint8_t* chunk = sQ + (sq * CPS + (PAIR ? static_cast<uint32_t>(blk) : gk - gg * QG)) * kQChunk;
-        uint32_t w[4][8];  // codes of rows r0, r0 + 8, r0 + 16, r0 + 24
-        float sc4[4];
-        const uint16_t* scl = reinterpret_cast<const uint16_t*>(chunk + kQBytes);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 c0 = reinterpret_cast<const uint4*>(chunk + (r0 + 8 * i) * 32)[0];
-          const uint4 c1 = reinterpret_cast<const uint4*>(chunk + (r0 + 8 * i) * 32)[1];
-          w[i][0] = c0.x;
-          w[i][1] = c0.y;
-          w[i][2] = c0.z;
-          w[i][3] = c0.w;
-          w[i][4] = c1.x;
-          w[i][5] = c1.y;
-          w[i][6] = c1.z;
-          w[i][7] = c1.w;
-          sc4[i] = bf16_to_f32(scl[r0 + 8 * i]);
-        }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(qempty0 + 8 * sq);
-        const uint32_t* xk = xrow + ks * (kBK / 2) + q;  // token row words of this K step
-        // The MMAs take the codes as exact bf16 (136 + code) pairs, two
-        // instructions a pair; a ninth MMA with all-ones A sums each token's
-        // 64 inputs, and sum((136 + c) x) - 136 sum(x) = sum(c x).
-        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f}, dx[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+        for (int st = 0; st < S; ++st) {
+          uint2 cw[4];  // code words of rows r0 + 8i, inputs 16q .. 16q + 15 of the step
+          float sc[4];  // their group scales
+          const uint8_t* chunk = sQ + (sq * CPS + (PAIR ? blk : st)) * kQChunk;
+          const uint16_t* scl = reinterpret_cast<const uint16_t*>(chunk + kQBytes);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // k16 block j: inputs 16 j .. 16 j + 15 of the step
-          const uint32_t b0 = xk[8 * j], b1 = xk[8 * j + 4];
-          uint32_t a[4];
-          a[0] = code_pair_biased(w[0][2 * j], q);      // row r0, inputs 16j + 2q, +1
-          a[1] = code_pair_biased(w[1][2 * j], q);      // row r0 + 8
-          a[2] = code_pair_biased(w[0][2 * j + 1], q);  // row r0, inputs 16j + 8 + 2q, +1
-          a[3] = code_pair_biased(w[1][2 * j + 1], q);  // row r0 + 8
-          mma_16816_bf16(d0, a, b0, b1);
-          a[0] = code_pair_biased(w[2][2 * j], q);      // row r0 + 16
-          a[1] = code_pair_biased(w[3][2 * j], q);      // row r0 + 24
-          a[2] = code_pair_biased(w[2][2 * j + 1], q);
-          a[3] = code_pair_biased(w[3][2 * j + 1], q);
-          mma_16816_bf16(d1, a, b0, b1);
-          mma_16816_bf16(dx, ones, b0, b1);
+          for (int i = 0; i < 4; ++i) {
+            cw[i] = *reinterpret_cast<const uint2*>(chunk + (r0 + 8 * i) * 32 + 8 * q);
+            sc[i] = bf16_to_f32(scl[r0 + 8 * i]);
+          }
+          if (st == S - 1) {  // the slot's last reads are done: release it
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(qempty0 + 8 * sq);
+          }
+          const uint4* xk = reinterpret_cast<const uint4*>(xrow + (u * S + st) * (kBK * 2));
+          const uint4 x0 = xk[0], x1 = xk[1];
+          const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          // The MMAs take the codes as exact bf16 (136 + code) pairs; a
+          // ninth MMA with all-ones A sums each token's 64 inputs, and
+          // sum((136 + c) x) - 136 sum(x) = sum(c x).
+          float d0[4], d1[4], dx[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // word j/2 of a row holds inputs 16q + 8(j/2) .. +7; its pair
+            // 2(j%2) is inputs 16q + 4j, +1 and pair 2(j%2) + 1 the next two
+            const int pl = 2 * (j & 1);
+            const uint32_t w0 = (j >> 1) ? cw[0].y : cw[0].x, w1 = (j >> 1) ? cw[1].y : cw[1].x;
+            const uint32_t w2 = (j >> 1) ? cw[2].y : cw[2].x, w3 = (j >> 1) ? cw[3].y : cw[3].x;
+            const uint32_t a0[4] = {code_pair_biased(w0, pl), code_pair_biased(w1, pl), code_pair_biased(w0, pl + 1),
+                                    code_pair_biased(w1, pl + 1)};  // rows r0, r0 + 8
+            const uint32_t a1[4] = {code_pair_biased(w2, pl), code_pair_biased(w3, pl), code_pair_biased(w2, pl + 1),
+                                    code_pair_biased(w3, pl + 1)};  // rows r0 + 16, r0 + 24
+            if (j == 0) {
+              mma_16816_bf16_first(d0, a0, xb[0], xb[1]);
+              mma_16816_bf16_first(d1, a1, xb[0], xb[1]);
+              mma_16816_bf16_first(dx, kOnes, xb[0], xb[1]);
+            } else {
+              mma_16816_bf16(d0, a0, xb[2 * j], xb[2 * j + 1]);
+              mma_16816_bf16(d1, a1, xb[2 * j], xb[2 * j + 1]);
+              mma_16816_bf16(dx, kOnes, xb[2 * j], xb[2 * j + 1]);
+            }
+          }
+          acc[0] = fmaf(sc[0], fmaf(-136.0f, dx[0], d0[0]), acc[0]);  // row r0, token 2q
+          acc[1] = fmaf(sc[0], fmaf(-136.0f, dx[1], d0[1]), acc[1]);  // row r0, token 2q + 1
+          acc[2] = fmaf(sc[1], fmaf(-136.0f, dx[0], d0[2]), acc[2]);  // row r0 + 8
+          acc[3] = fmaf(sc[1], fmaf(-136.0f, dx[1], d0[3]), acc[3]);
+          acc[4] = fmaf(sc[2], fmaf(-136.0f, dx[0], d1[0]), acc[4]);  // row r0 + 16
+          acc[5] = fmaf(sc[2], fmaf(-136.0f, dx[1], d1[1]), acc[5]);
+          acc[6] = fmaf(sc[3], fmaf(-136.0f, dx[0], d1[2]), acc[6]);  // row r0 + 24
+          acc[7] = fmaf(sc[3], fmaf(-136.0f, dx[1], d1[3]), acc[7]);
         }
-        acc[0] = fmaf(sc4[0], fmaf(-136.0f, dx[0], d0[0]), acc[0]);  // row r0, token 2q
-        acc[1] = fmaf(sc4[0], fmaf(-136.0f, dx[1], d0[1]), acc[1]);  // row r0, token 2q + 1
-        acc[2] = fmaf(sc4[1], fmaf(-136.0f, dx[0], d0[2]), acc[2]);  // row r0 + 8
-        acc[3] = fmaf(sc4[1], fmaf(-136.0f, dx[1], d0[3]), acc[3]);
-        acc[4] = fmaf(sc4[2], fmaf(-136.0f, dx[0], d1[0]), acc[4]);  // row r0 + 16
-        acc[5] = fmaf(sc4[2], fmaf(-136.0f, dx[1], d1[1]), acc[5]);
-        acc[6] = fmaf(sc4[3], fmaf(-136.0f, dx[0], d1[2]), acc[6]);  // row r0 + 24
-        acc[7] = fmaf(sc4[3], fmaf(-136.0f, dx[1], d1[3]), acc[7]);
       }
       if (!ok) break;
       gbase += static_cast<uint32_t>(p.ksteps);
