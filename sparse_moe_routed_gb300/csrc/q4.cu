@@ -102,20 +102,20 @@ __device__ __forceinline__ uint32_t code_pair_biased(uint32_t word, int p) {
 template <int KIND, int QG, bool PAIR>
 __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   using C = CfgV;
-  static_assert(!PAIR || (KIND == 1 && QG == 1), "paired blocks: down tiles, one K step per slot");
+  static_assert(!PAIR || KIND == 1, "paired blocks: down tiles");
   constexpr int G = PAIR ? 2 : kGvGroups;         // K-step groups
   constexpr int WPG = PAIR ? 2 * kGvWpg : kGvWpg;  // compute warps per group, 32 rows each
   constexpr int RT = 32 * WPG;                     // weight rows per tile
-  constexpr int CPS = PAIR ? 2 : QG;               // chunks per ring slot
+  constexpr int CPS = PAIR ? 2 * QG : QG;          // chunks per ring slot
   constexpr int SQ = C::SQmax / CPS;               // ring slots
-  constexpr int S = PAIR ? 1 : QG;                 // K steps per ring slot (one group reads them all)
+  constexpr int S = QG;                            // K steps per ring slot (one group reads them all)
   static_assert(C::SQmax % CPS == 0, "ring holds whole slots");
   static_assert(G * WPG == kGvGroups * kGvWpg, "all compute warps");
   static_assert((G - 1) * RT * kGvRows <= C::kRedFloats, "hand-over buffer");
   const int K = p.ksteps * kBK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;                                  // [SQ][QG x 4,352 B] packed codes + scales
+  uint8_t* sQ = base;                                  // [SQ][CPS x 4,352 B] packed codes + scales
   uint8_t* sX = sQ + C::SQmax * kQChunk;               // [2][8 rows][K] bf16 token rows of a tile
   float* sRed = reinterpret_cast<float*>(sX + 2 * C::kXBytes);  // [2][G-1][128][4] other groups' sums
   uint64_t* bars = reinterpret_cast<uint64_t*>(sRed + 2 * C::kRedFloats);
@@ -157,27 +157,28 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ packed chunk producer
     const uint64_t pol = ptx::policy_evict_first();
-    uint32_t armed_mask = 0, armed_ph = 0;
+    static_assert(SQ <= 64, "armed-slot masks");
+    uint64_t armed_mask = 0, armed_ph = 0;  // slots with a copy issued, and the phase it completes
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = sc.tile(t);
-      for (int ks = 0; ks < p.ksteps; ks += PAIR ? 1 : QG) {
+      for (int ks = 0; ks < p.ksteps; ks += QG) {
         if (!wait_bounded<kSpin>(qempty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
           ok = false;
           break;
         }
         const uint32_t fb = qfull0 + 8 * s;
-        armed_mask |= 1u << s;
-        armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+        armed_mask |= 1ull << s;
+        armed_ph = (armed_ph & ~(1ull << s)) | (static_cast<uint64_t>(ph) << s);
         ptx::mbar_arrive_expect_tx(fb, CPS * kQChunk);
         if (PAIR) {
-          // K step ks of the tile's two 128-row blocks
+          // K steps ks .. ks + QG - 1 of the tile's two 128-row blocks
           const size_t c0 = (static_cast<size_t>(tl.e) * p.mblocks + 2 * tl.mb) * p.ksteps + ks;
-          ptx::bulk_load(ptx::smem_u32(sQ + s * CPS * kQChunk), p.tiles + c0 * kQChunk, kQChunk, fb, pol);
-          ptx::bulk_load(ptx::smem_u32(sQ + (s * CPS + 1) * kQChunk), p.tiles + (c0 + p.ksteps) * kQChunk, kQChunk,
-                         fb, pol);
+          ptx::bulk_load(ptx::smem_u32(sQ + s * CPS * kQChunk), p.tiles + c0 * kQChunk, QG * kQChunk, fb, pol);
+          ptx::bulk_load(ptx::smem_u32(sQ + (s * CPS + QG) * kQChunk), p.tiles + (c0 + p.ksteps) * kQChunk,
+                         QG * kQChunk, fb, pol);
         } else {
           const size_t chunk = (static_cast<size_t>(tl.e) * p.mblocks + tl.mb) * p.ksteps + ks;
           ptx::bulk_load(ptx::smem_u32(sQ + s * QG * kQChunk), p.tiles + chunk * kQChunk, QG * kQChunk, fb, pol);
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
     }
     if (!ok || misc[1]) {
       for (int q = 0; q < SQ; ++q)
-        if ((armed_mask >> q) & 1u) wait_drain(qfull0 + 8 * q, (armed_ph >> q) & 1u);
+        if ((armed_mask >> q) & 1u) wait_drain(qfull0 + 8 * q, static_cast<uint32_t>((armed_ph >> q) & 1u));
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------ token-row producer
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
         for (int st = 0; st < S; ++st) {
           uint2 cw[4];  // code words of rows r0 + 8i, inputs 16q .. 16q + 15 of the step
           float sc[4];  // their group scales
-          const uint8_t* chunk = sQ + (sq * CPS + (PAIR ? blk : st)) * kQChunk;
+          const uint8_t* chunk = sQ + (sq * CPS + (PAIR ? blk * S + st : st)) * kQChunk;
           const uint16_t* scl = reinterpret_cast<const uint16_t*>(chunk + kQBytes);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -398,10 +399,15 @@ cudaError_t run_gemv_q4_g(const GemmArgs& args, cudaStream_t st) {
   return launch_pdl(kern, dim3(grid), dim3(kGvThreads), CfgV::kSmemBytes, st, args);
 }
 
+// A ring slot holds as many consecutive K steps as divide the record's
+// (four, two or one); paired down tiles take two steps of both blocks.
 template <int KIND>
 cudaError_t run_gemv_q4(const GemmArgs& args, cudaStream_t st) {
-  if (KIND == 1 && args.mblocks % 2 == 0) return run_gemv_q4_g<1, 1, true>(args, st);
-  return args.qgroup == 2 ? run_gemv_q4_g<KIND, 2, false>(args, st) : run_gemv_q4_g<KIND, 1, false>(args, st);
+  const bool even = args.ksteps % 2 == 0;
+  if (KIND == 1 && args.mblocks % 2 == 0)
+    return even ? run_gemv_q4_g<1, 2, true>(args, st) : run_gemv_q4_g<1, 1, true>(args, st);
+  if (args.ksteps % 4 == 0) return run_gemv_q4_g<KIND, 4, false>(args, st);
+  return even ? run_gemv_q4_g<KIND, 2, false>(args, st) : run_gemv_q4_g<KIND, 1, false>(args, st);
 }
 
 }  // namespace
