@@ -23,12 +23,14 @@ namespace {
 // dot product spends ~6 instructions per weight.  Here the weights go from
 // registers straight into warp-level MMAs (mma.sync m16n8k16, bf16 in, fp32
 // accumulate): each code pair becomes an exact bf16 pair (136 + code) in one
-// or two instructions (an all-ones MMA supplies the 136 x sum(x) correction), token
-// values enter as bf16 with no conversion, and one MMA instruction consumes
-// 256 weights against up to 8 token rows.
+// or two instructions (each token row's sums over the K steps, computed once
+// per tile, supply the 136 x sum(x) correction), token values enter as bf16
+// with no conversion, and one MMA instruction consumes 256 weights against up
+// to 8 token rows.
 //
 // Warps: 0 streams packed chunks (bulk copies, deep ring), 1 stages each
-// tile's token rows (one bulk copy per row, double-buffered), the rest
+// tile's token rows (one bulk copy per row, double-buffered) and their
+// per-step sums, the rest
 // compute in kGvGroups groups of four.  The groups take K steps in turn, so
 // each warp has several steps' time for the latency chain of one (wait,
 // loads, dequantise, MMAs).  Warp w of a group owns tile rows 32w .. 32w + 31
@@ -70,9 +72,10 @@ struct CfgV {
   static constexpr int kXBytes = kGvRows * (kGvMaxK * 2 + 16);
   static constexpr int kUpFloats = 0;
   static constexpr int kRedFloats = (kGvGroups - 1) * kBM * kGvRows;  // other groups' sums: [G-1][128][4]
+  static constexpr int kXsFloats = kGvMaxK / 64 * kGvRows;             // token-row sums: [K steps][4]
   static constexpr int kNumBars = 2 * SQmax + 12;
   static constexpr int kSmemBytes = 1024 + SQmax * kQChunk + 2 * kXBytes + 2 * kUpFloats * 4 +
-                                    2 * kRedFloats * 4 + kNumBars * 8 + kSmemTail;
+                                    2 * kRedFloats * 4 + 2 * kXsFloats * 4 + kNumBars * 8 + kSmemTail;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -95,8 +98,12 @@ __device__ __forceinline__ void mma_16816_bf16_first(float (&d)[4], const uint32
 
 // Codes of inputs 2p, 2p+1 of a packed word -> bf16 pair (128 + stored code),
 // exact; the stored code is the weight code + 8, so this is 136 + code.
-__device__ __forceinline__ uint32_t code_pair_biased(uint32_t word, int p) {
-  return ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+// `magic` is 0x43004300 held in a register: with the mask as the one
+// immediate, the and-or is a single three-input logic instruction.
+__device__ __forceinline__ uint32_t code_pair_biased(uint32_t word, int p, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(word >> (4 * p)), "n"(0x000F000F), "r"(magic));
+  return d;
 }
 
 template <int KIND, int QG, bool PAIR>
@@ -118,13 +125,15 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   uint8_t* sQ = base;                                  // [SQ][CPS x 4,352 B] packed codes + scales
   uint8_t* sX = sQ + C::SQmax * kQChunk;               // [2][8 rows][K] bf16 token rows of a tile
   float* sRed = reinterpret_cast<float*>(sX + 2 * C::kXBytes);  // [2][G-1][128][4] other groups' sums
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sRed + 2 * C::kRedFloats);
+  float* sXs = sRed + 2 * C::kRedFloats;  // [2][K steps][4]: each staged token row's sum over each K step
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sXs + 2 * C::kXsFloats);
   const uint32_t qfull0 = ptx::smem_u32(bars);
   const uint32_t qempty0 = qfull0 + 8 * C::SQmax;
   const uint32_t xfull0 = qempty0 + 8 * C::SQmax;  // token rows of a tile staged (2 buffers)
   const uint32_t xempty0 = xfull0 + 16;            // every compute warp done with them
   const uint32_t redf0 = xempty0 + 16;             // other groups' sums written (2 buffers)
   const uint32_t rede0 = redf0 + 16;               // group 0 done with them (2 buffers)
+  const uint32_t xland0 = rede0 + 16;              // token-row copies landed (2 buffers)
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
   int* prefix = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
   int* soff = prefix + (kMaxE + 1);
@@ -140,6 +149,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(xfull0 + 8 * b, 1);
+      ptx::mbar_init(xland0 + 8 * b, 1);
       ptx::mbar_init(xempty0 + 8 * b, WPG * G);
       ptx::mbar_init(redf0 + 8 * b, WPG * (G - 1));
       ptx::mbar_init(rede0 + 8 * b, WPG);
@@ -193,8 +203,12 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       for (int q = 0; q < SQ; ++q)
         if ((armed_mask >> q) & 1u) wait_drain(qfull0 + 8 * q, static_cast<uint32_t>((armed_ph >> q) & 1u));
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
     // ------------------------------------------------ token-row producer
+    // Lane 0 stages each tile's token rows (one bulk copy per row); once they
+    // have landed the warp sums every row over every 64-input K step (fp32,
+    // in input order) into the tile's table, which supplies the 136 x sum(x)
+    // correction of the biased codes, and then marks the stage full.
     const uint64_t pol = ptx::policy_evict_last();
     uint32_t armed_mask = 0, armed_ph = 0;
     bool ok = true;
@@ -203,22 +217,51 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       const Tile tl = sc.tile(t);
       const int b = ntile & 1;
       const uint32_t use = static_cast<uint32_t>(ntile >> 1) & 1u;
-      if (!wait_bounded<kSpin>(xempty0 + 8 * b, use ^ 1u, misc + 1, p.status)) {
+      const int n = min(tl.nrows, kGvRows);
+      if (lane == 0) {
+        ok = wait_bounded<kSpin>(xempty0 + 8 * b, use ^ 1u, misc + 1, p.status);
+        if (ok) {
+          const uint32_t lb = xland0 + 8 * b;
+          armed_mask |= 1u << b;
+          armed_ph = (armed_ph & ~(1u << b)) | (use << b);
+          ptx::mbar_arrive_expect_tx(lb, static_cast<uint32_t>(n * K * 2));
+          for (int j = 0; j < n; ++j)
+            ptx::bulk_load(ptx::smem_u32(sX + b * C::kXBytes + j * (K * 2 + 16)),
+                           p.brows + static_cast<size_t>(tl.row0 + j) * K, static_cast<uint32_t>(K * 2), lb, pol);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const bool landed = wait_bounded<kSleepEpi>(xland0 + 8 * b, use, misc + 1, p.status);
+      if (!__all_sync(0xffffffffu, landed)) {
         ok = false;
         break;
       }
-      const int n = min(tl.nrows, kGvRows);
-      const uint32_t fb = xfull0 + 8 * b;
-      armed_mask |= 1u << b;
-      armed_ph = (armed_ph & ~(1u << b)) | (use << b);
-      ptx::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(n * K * 2));
-      for (int j = 0; j < n; ++j)
-        ptx::bulk_load(ptx::smem_u32(sX + b * C::kXBytes + j * (K * 2 + 16)), p.brows + static_cast<size_t>(tl.row0 + j) * K,
-                       static_cast<uint32_t>(K * 2), fb, pol);
+      float* xs = sXs + b * C::kXsFloats;
+      for (int it = lane; it < p.ksteps * kGvRows; it += 32) {
+        const int ks = it / kGvRows, j = it % kGvRows;
+        float sum = 0.f;
+        if (j < n) {
+          const uint4* src = reinterpret_cast<const uint4*>(sX + b * C::kXBytes + j * (K * 2 + 16) + ks * (kBK * 2));
+#pragma unroll
+          for (int v = 0; v < kBK / 8; ++v) {
+            const uint4 w = src[v];
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              sum += __uint_as_float(ws[e] << 16);
+              sum += __uint_as_float(ws[e] & 0xFFFF0000u);
+            }
+          }
+        }
+        xs[ks * kGvRows + j] = sum;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(xfull0 + 8 * b);
     }
-    if (!ok || misc[1]) {
+    if (lane == 0 && (!ok || misc[1])) {
       for (int q = 0; q < 2; ++q)
-        if ((armed_mask >> q) & 1u) wait_drain(xfull0 + 8 * q, (armed_ph >> q) & 1u);
+        if ((armed_mask >> q) & 1u) wait_drain(xland0 + 8 * q, (armed_ph >> q) & 1u);
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------- compute
@@ -243,8 +286,12 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       }
       // B fragments read token row g of the stage; columns g >= the tile's
       // rows read a stale row and are never stored
-      const uint32_t kOnes[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // bf16 1.0 pairs
+      // 0x43004300, opaque to the compiler so that it stays in a register
+      const uint32_t magic = 0x43004300u | (static_cast<uint32_t>(p.ksteps) >> 31);
       const uint8_t* xrow = sX + b * C::kXBytes + (g & (kGvRows - 1)) * (K * 2 + 16) + 32 * q;
+      // sums of token columns 2q, 2q + 1 (columns past the tile's rows read
+      // another column's sum and are never stored)
+      const float* xsum = sXs + b * C::kXsFloats + 2 * (q & 1);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       // The MMA's k slots run over a step's 64 inputs in a permuted order
       // (the same for weights and tokens, so the products and their sum are
@@ -264,7 +311,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
           ok = false;
           break;
         }
-#pragma unroll
+#pragma unroll 2  // two steps interleaved: more would spill
         for (int st = 0; st < S; ++st) {
           uint2 cw[4];  // code words of rows r0 + 8i, inputs 16q .. 16q + 15 of the step
           float sc[4];  // their group scales
@@ -282,10 +329,11 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
           const uint4* xk = reinterpret_cast<const uint4*>(xrow + (u * S + st) * (kBK * 2));
           const uint4 x0 = xk[0], x1 = xk[1];
           const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          // The MMAs take the codes as exact bf16 (136 + code) pairs; a
-          // ninth MMA with all-ones A sums each token's 64 inputs, and
-          // sum((136 + c) x) - 136 sum(x) = sum(c x).
-          float d0[4], d1[4], dx[4];
+          // The MMAs take the codes as exact bf16 (136 + code) pairs, and
+          // sum((136 + c) x) - 136 sum(x) = sum(c x) with the token sums of
+          // the step from the table.
+          const float2 xs = *reinterpret_cast<const float2*>(xsum + (u * S + st) * kGvRows);
+          float d0[4], d1[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             // word j/2 of a row holds inputs 16q + 8(j/2) .. +7; its pair
@@ -293,28 +341,28 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
             const int pl = 2 * (j & 1);
             const uint32_t w0 = (j >> 1) ? cw[0].y : cw[0].x, w1 = (j >> 1) ? cw[1].y : cw[1].x;
             const uint32_t w2 = (j >> 1) ? cw[2].y : cw[2].x, w3 = (j >> 1) ? cw[3].y : cw[3].x;
-            const uint32_t a0[4] = {code_pair_biased(w0, pl), code_pair_biased(w1, pl), code_pair_biased(w0, pl + 1),
-                                    code_pair_biased(w1, pl + 1)};  // rows r0, r0 + 8
-            const uint32_t a1[4] = {code_pair_biased(w2, pl), code_pair_biased(w3, pl), code_pair_biased(w2, pl + 1),
-                                    code_pair_biased(w3, pl + 1)};  // rows r0 + 16, r0 + 24
+            const uint32_t a0[4] = {code_pair_biased(w0, pl, magic), code_pair_biased(w1, pl, magic),
+                                    code_pair_biased(w0, pl + 1, magic),
+                                    code_pair_biased(w1, pl + 1, magic)};  // rows r0, r0 + 8
+            const uint32_t a1[4] = {code_pair_biased(w2, pl, magic), code_pair_biased(w3, pl, magic),
+                                    code_pair_biased(w2, pl + 1, magic),
+                                    code_pair_biased(w3, pl + 1, magic)};  // rows r0 + 16, r0 + 24
             if (j == 0) {
               mma_16816_bf16_first(d0, a0, xb[0], xb[1]);
               mma_16816_bf16_first(d1, a1, xb[0], xb[1]);
-              mma_16816_bf16_first(dx, kOnes, xb[0], xb[1]);
             } else {
               mma_16816_bf16(d0, a0, xb[2 * j], xb[2 * j + 1]);
               mma_16816_bf16(d1, a1, xb[2 * j], xb[2 * j + 1]);
-              mma_16816_bf16(dx, kOnes, xb[2 * j], xb[2 * j + 1]);
             }
           }
-          acc[0] = fmaf(sc[0], fmaf(-136.0f, dx[0], d0[0]), acc[0]);  // row r0, token 2q
-          acc[1] = fmaf(sc[0], fmaf(-136.0f, dx[1], d0[1]), acc[1]);  // row r0, token 2q + 1
-          acc[2] = fmaf(sc[1], fmaf(-136.0f, dx[0], d0[2]), acc[2]);  // row r0 + 8
-          acc[3] = fmaf(sc[1], fmaf(-136.0f, dx[1], d0[3]), acc[3]);
-          acc[4] = fmaf(sc[2], fmaf(-136.0f, dx[0], d1[0]), acc[4]);  // row r0 + 16
-          acc[5] = fmaf(sc[2], fmaf(-136.0f, dx[1], d1[1]), acc[5]);
-          acc[6] = fmaf(sc[3], fmaf(-136.0f, dx[0], d1[2]), acc[6]);  // row r0 + 24
-          acc[7] = fmaf(sc[3], fmaf(-136.0f, dx[1], d1[3]), acc[7]);
+          acc[0] = fmaf(sc[0], fmaf(-136.0f, xs.x, d0[0]), acc[0]);  // row r0, token 2q
+          acc[1] = fmaf(sc[0], fmaf(-136.0f, xs.y, d0[1]), acc[1]);  // row r0, token 2q + 1
+          acc[2] = fmaf(sc[1], fmaf(-136.0f, xs.x, d0[2]), acc[2]);  // row r0 + 8
+          acc[3] = fmaf(sc[1], fmaf(-136.0f, xs.y, d0[3]), acc[3]);
+          acc[4] = fmaf(sc[2], fmaf(-136.0f, xs.x, d1[0]), acc[4]);  // row r0 + 16
+          acc[5] = fmaf(sc[2], fmaf(-136.0f, xs.y, d1[1]), acc[5]);
+          acc[6] = fmaf(sc[3], fmaf(-136.0f, xs.x, d1[2]), acc[6]);  // row r0 + 24
+          acc[7] = fmaf(sc[3], fmaf(-136.0f, xs.y, d1[3]), acc[7]);
         }
       }
       if (!ok) break;
