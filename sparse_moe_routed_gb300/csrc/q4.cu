@@ -35,8 +35,9 @@ namespace {
 // each warp has several steps' time for the latency chain of one (wait,
 // loads, dequantise, MMAs).  Warp w of a group owns tile rows 32w .. 32w + 31
 // as two MMA row tiles that share the token fragments: per K step (one scale
-// group of 64 inputs) it runs eight MMAs from zero and adds scale x partial
-// to its fp32 accumulators.  The MMA's k slots run over the step's inputs in
+// group of 64 inputs) it runs eight MMAs, the first of each chain starting
+// from -136 x the step's token sums, and adds scale x partial to its fp32
+// accumulators.  The MMA's k slots run over the step's inputs in
 // a permuted order (the same for weights and tokens), chosen so that each
 // lane reads 16 consecutive inputs: one 8-byte load per weight row, two
 // 16-byte loads of token values, and every code pair at a fixed nibble
@@ -72,7 +73,9 @@ struct CfgV {
   static constexpr int kXBytes = kGvRows * (kGvMaxK * 2 + 16);
   static constexpr int kUpFloats = 0;
   static constexpr int kRedFloats = (kGvGroups - 1) * kBM * kGvRows;  // other groups' sums: [G-1][128][4]
-  static constexpr int kXsFloats = kGvMaxK / 64 * kGvRows;             // token-row sums: [K steps][4]
+  // per K step, -136 x each staged token row's sum in the MMA accumulator
+  // layout of the two lane classes: [K steps][c0, c1, c0, c1, c2, c3, c2, c3]
+  static constexpr int kXsFloats = kGvMaxK / 64 * 8;
   static constexpr int kNumBars = 2 * SQmax + 12;
   static constexpr int kSmemBytes = 1024 + SQmax * kQChunk + 2 * kXBytes + 2 * kUpFloats * 4 +
                                     2 * kRedFloats * 4 + 2 * kXsFloats * 4 + kNumBars * 8 + kSmemTail;
@@ -87,13 +90,14 @@ __device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// The same MMA with a zero accumulator in.
-__device__ __forceinline__ void mma_16816_bf16_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+// The same MMA from the accumulator c (read only) into d.
+__device__ __forceinline__ void mma_16816_bf16_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                                     const float4& c) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%10,%10,%10};"
+      "{%10,%11,%12,%13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y), "f"(c.z), "f"(c.w));
 }
 
 // Codes of inputs 2p, 2p+1 of a packed word -> bf16 pair (128 + stored code),
@@ -125,7 +129,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   uint8_t* sQ = base;                                  // [SQ][CPS x 4,352 B] packed codes + scales
   uint8_t* sX = sQ + C::SQmax * kQChunk;               // [2][8 rows][K] bf16 token rows of a tile
   float* sRed = reinterpret_cast<float*>(sX + 2 * C::kXBytes);  // [2][G-1][128][4] other groups' sums
-  float* sXs = sRed + 2 * C::kRedFloats;  // [2][K steps][4]: each staged token row's sum over each K step
+  float* sXs = sRed + 2 * C::kRedFloats;  // [2][K steps][8]: -136 x each token row's sum over each K step
   uint64_t* bars = reinterpret_cast<uint64_t*>(sXs + 2 * C::kXsFloats);
   const uint32_t qfull0 = ptx::smem_u32(bars);
   const uint32_t qempty0 = qfull0 + 8 * C::SQmax;
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
         break;
       }
       float* xs = sXs + b * C::kXsFloats;
-      for (int it = lane; it < p.ksteps * kGvRows; it += 32) {
+      for (int it = lane; it < p.ksteps * kGvRows; it += 32) {  // item = (K step, token row)
         const int ks = it / kGvRows, j = it % kGvRows;
         float sum = 0.f;
         if (j < n) {
@@ -254,7 +258,9 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
             }
           }
         }
-        xs[ks * kGvRows + j] = sum;
+        const float c = -136.0f * sum;
+        xs[ks * 8 + 4 * (j >> 1) + (j & 1)] = c;
+        xs[ks * 8 + 4 * (j >> 1) + (j & 1) + 2] = c;
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(xfull0 + 8 * b);
@@ -289,9 +295,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       // 0x43004300, opaque to the compiler so that it stays in a register
       const uint32_t magic = 0x43004300u | (static_cast<uint32_t>(p.ksteps) >> 31);
       const uint8_t* xrow = sX + b * C::kXBytes + (g & (kGvRows - 1)) * (K * 2 + 16) + 32 * q;
-      // sums of token columns 2q, 2q + 1 (columns past the tile's rows read
-      // another column's sum and are never stored)
-      const float* xsum = sXs + b * C::kXsFloats + 2 * (q & 1);
+      // -136 x the sums of token columns 2q, 2q + 1 in accumulator order
+      // (columns past the tile's rows read another column's and are never
+      // stored)
+      const float* xsum = sXs + b * C::kXsFloats + 4 * (q & 1);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       // The MMA's k slots run over a step's 64 inputs in a permuted order
       // (the same for weights and tokens, so the products and their sum are
@@ -329,10 +336,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
           const uint4* xk = reinterpret_cast<const uint4*>(xrow + (u * S + st) * (kBK * 2));
           const uint4 x0 = xk[0], x1 = xk[1];
           const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          // The MMAs take the codes as exact bf16 (136 + code) pairs, and
-          // sum((136 + c) x) - 136 sum(x) = sum(c x) with the token sums of
-          // the step from the table.
-          const float2 xs = *reinterpret_cast<const float2*>(xsum + (u * S + st) * kGvRows);
+          // The MMAs take the codes as exact bf16 (136 + code) pairs and
+          // start from -136 sum(x) of the step (from the table), so they end
+          // at sum((136 + c) x) - 136 sum(x) = sum(c x).
+          const float4 xs = *reinterpret_cast<const float4*>(xsum + (u * S + st) * 8);
           float d0[4], d1[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -348,21 +355,21 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
                                     code_pair_biased(w2, pl + 1, magic),
                                     code_pair_biased(w3, pl + 1, magic)};  // rows r0 + 16, r0 + 24
             if (j == 0) {
-              mma_16816_bf16_first(d0, a0, xb[0], xb[1]);
-              mma_16816_bf16_first(d1, a1, xb[0], xb[1]);
+              mma_16816_bf16_first(d0, a0, xb[0], xb[1], xs);
+              mma_16816_bf16_first(d1, a1, xb[0], xb[1], xs);
             } else {
               mma_16816_bf16(d0, a0, xb[2 * j], xb[2 * j + 1]);
               mma_16816_bf16(d1, a1, xb[2 * j], xb[2 * j + 1]);
             }
           }
-          acc[0] = fmaf(sc[0], fmaf(-136.0f, xs.x, d0[0]), acc[0]);  // row r0, token 2q
-          acc[1] = fmaf(sc[0], fmaf(-136.0f, xs.y, d0[1]), acc[1]);  // row r0, token 2q + 1
-          acc[2] = fmaf(sc[1], fmaf(-136.0f, xs.x, d0[2]), acc[2]);  // row r0 + 8
-          acc[3] = fmaf(sc[1], fmaf(-136.0f, xs.y, d0[3]), acc[3]);
-          acc[4] = fmaf(sc[2], fmaf(-136.0f, xs.x, d1[0]), acc[4]);  // row r0 + 16
-          acc[5] = fmaf(sc[2], fmaf(-136.0f, xs.y, d1[1]), acc[5]);
-          acc[6] = fmaf(sc[3], fmaf(-136.0f, xs.x, d1[2]), acc[6]);  // row r0 + 24
-          acc[7] = fmaf(sc[3], fmaf(-136.0f, xs.y, d1[3]), acc[7]);
+          acc[0] = fmaf(sc[0], d0[0], acc[0]);  // row r0, token 2q
+          acc[1] = fmaf(sc[0], d0[1], acc[1]);  // row r0, token 2q + 1
+          acc[2] = fmaf(sc[1], d0[2], acc[2]);  // row r0 + 8
+          acc[3] = fmaf(sc[1], d0[3], acc[3]);
+          acc[4] = fmaf(sc[2], d1[0], acc[4]);  // row r0 + 16
+          acc[5] = fmaf(sc[2], d1[1], acc[5]);
+          acc[6] = fmaf(sc[3], d1[2], acc[6]);  // row r0 + 24
+          acc[7] = fmaf(sc[3], d1[3], acc[7]);
         }
       }
       if (!ok) break;
