@@ -115,16 +115,23 @@ def test_int4_expert_stage_tiny_geometry():
 # an odd number of 128-row blocks on both sides (H = 384, 2I = 384): the down
 # launch cannot pair its blocks into 256-row tiles and takes the four-group split
 ODD = wl.LayerConfig("int4_odd", T=16, H=384, E=64, k=4, I=192, bias=None, seed=19)
+# unpaired down blocks whose record has a multiple of four (I = 256) or of two
+# (I = 128) K steps: a ring slot holds four or two steps of one block
+ODD_K4 = wl.LayerConfig("int4_odd_k4", T=16, H=384, E=64, k=4, I=256, bias=None, seed=29)
+ODD_K2 = wl.LayerConfig("int4_odd_k2", T=16, H=384, E=64, k=4, I=128, bias=None, seed=31)
+GEOM = {"odd": ODD, "odd_k4": ODD_K4, "odd_k2": ODD_K2}
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode", "odd"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "odd", "odd_k4", "odd_k2"])
 def test_int4_skewed_routes_split_tiles(name):
     """Decode-sized int4 launches run on the CUDA-core kernel, which splits an
     expert's rows into tiles of 4: routes skewed so that one expert gets 9
     rows (three tiles), others 1-5, graded row by row against the oracle.
     Down launches with an even block count pair two blocks per tile, odd ones
-    do not: both are covered."""
-    cfg = ODD if name == "odd" else wl.CONFIGS[name]
+    do not; ring slots hold four, two or one K steps: every combination the
+    geometries allow is covered (gate/up 4 and 2 steps; down paired 2 and 1,
+    unpaired 4, 2 and 1)."""
+    cfg = GEOM[name] if name in GEOM else wl.CONFIGS[name]
     T, k, E = 16, cfg.k, cfg.E
     d = wl.layer_inputs(cfg, DEV)
     q_gu, s_gu = wl.quantize_int4_g64(d["w_gateup"])
