@@ -46,9 +46,10 @@ namespace {
 // are shared by two steps' MMAs.  In a gate/up record rows 32w .. 32w + 15 are gate
 // and 32w + 16 .. 32w + 31 the up rows of the same h columns, so each lane
 // ends a tile holding gate and up of the same outputs.  At the end of a tile
-// groups 1.. hand their sums (valid token columns only) to group 0 through
-// shared memory, which adds them in group order (a fixed order: same bits
-// every call) and stores y, or h = silu(gate) * up.  Token columns past the
+// the other groups hand their sums (valid token columns only) through shared
+// memory to the group that took the tile's last ring slot, which adds them in
+// a fixed order (the same bits every call) and stores y, or
+// h = silu(gate) * up.  Token columns past the
 // tile's rows read stale staged rows and are never stored (an MMA column
 // depends on its own B column only).
 //
@@ -376,16 +377,19 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       gbase += static_cast<uint32_t>(p.ksteps);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(xempty0 + 8 * b);
-      // groups 1.. hand their sums of the valid token columns (lanes q < 2)
-      // to group 0
-      if (grp > 0) {
+      // The group that took the tile's last ring slot (it finishes last)
+      // reduces and stores; the others hand it their sums of the valid token
+      // columns (lanes q < 2), slot ri = their distance after it - 1.
+      const int eg = static_cast<int>((sbase + static_cast<uint32_t>(nslot) - 1u) % G);
+      if (grp != eg) {
         got = wait_bounded<kSleepEpi>(rede0 + 8 * b, use ^ 1u, misc + 1, p.status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         if (q < kGvRows / 2) {
-          float* red = sRed + b * C::kRedFloats + (grp - 1) * (RT * kGvRows) + blk * (kBM * kGvRows);
+          const int ri = (grp - eg - 1 + G) % G;
+          float* red = sRed + b * C::kRedFloats + ri * (RT * kGvRows) + blk * (kBM * kGvRows);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             red[(r0 + 8 * i) * kGvRows + 2 * q] = acc[2 * i];
