@@ -54,10 +54,11 @@ namespace {
 // depends on its own B column only).
 //
 // Down tiles (K = I = 640: ten K steps) are short, so the per-tile work of
-// the group split (staging, the hand-over of sums) weighs more: when a
-// record's 128-row blocks pair up, a down tile spans two of them (256 rows)
-// and the compute warps form two groups of eight, each warp owning 32 rows of
-// one block; a ring slot then holds both blocks' chunks of one K step.
+// the group split (staging, the hand-over of sums) weighs more: a down tile
+// spans four of the record's 128-row blocks when their count allows (512
+// rows, one group of all sixteen warps, no hand-over) or two (256 rows, two
+// groups of eight), each warp owning 32 rows of one block; a ring slot then
+// holds the same K steps of every block of the tile.
 constexpr int kGvRows = 4;                     // token rows per tile
 constexpr int kGvN = 8;                        // MMA N: token columns (those past kGvRows are never stored)
 constexpr int kGvGroups = 4;
@@ -111,17 +112,18 @@ __device__ __forceinline__ uint32_t code_pair_biased(uint32_t word, int p, uint3
   return d;
 }
 
-template <int KIND, int QG, bool PAIR>
+template <int KIND, int QG, int BPT>
 __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   using C = CfgV;
-  static_assert(!PAIR || KIND == 1, "paired blocks: down tiles");
-  constexpr int G = PAIR ? 2 : kGvGroups;         // K-step groups
-  constexpr int WPG = PAIR ? 2 * kGvWpg : kGvWpg;  // compute warps per group, 32 rows each
+  static_assert(BPT == 1 || KIND == 1, "tiles of several 128-row blocks: down records");
+  static_assert(kGvGroups % BPT == 0, "groups");
+  constexpr int G = kGvGroups / BPT;               // K-step groups
+  constexpr int WPG = BPT * kGvWpg;                // compute warps per group, 32 rows each
   constexpr int RT = 32 * WPG;                     // weight rows per tile
-  constexpr int CPS = PAIR ? 2 * QG : QG;          // chunks per ring slot
+  constexpr int CPS = BPT * QG;                    // chunks per ring slot
   constexpr int SQ = C::SQmax / CPS;               // ring slots
   constexpr int S = QG;                            // K steps per ring slot (one group reads them all)
-  static_assert(C::SQmax % CPS == 0, "ring holds whole slots");
+  static_assert(SQ >= 2, "ring depth");
   static_assert(G * WPG == kGvGroups * kGvWpg, "all compute warps");
   static_assert((G - 1) * RT * kGvRows <= C::kRedFloats, "hand-over buffer");
   const int K = p.ksteps * kBK;
@@ -156,8 +158,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       ptx::mbar_init(xfull0 + 8 * b, 1);
       ptx::mbar_init(xland0 + 8 * b, 1);
       ptx::mbar_init(xempty0 + 8 * b, WPG * G);
-      ptx::mbar_init(redf0 + 8 * b, WPG * (G - 1));
-      ptx::mbar_init(rede0 + 8 * b, WPG);
+      if (G > 1) {
+        ptx::mbar_init(redf0 + 8 * b, WPG * (G - 1));
+        ptx::mbar_init(rede0 + 8 * b, WPG);
+      }
     }
     misc[1] = 0;
     ptx::fence_mbar_init();
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   pdl_wait();
   pdl_trigger();
   GemmArgs ps = p;  // the schedule counts tiles of RT rows
-  if (PAIR) ps.mblocks = p.mblocks / 2;
+  ps.mblocks = p.mblocks / BPT;
   const int total = build_schedule<kGvRows>(ps, false, E, prefix, soff);
   const Sched sc{prefix, soff, E, ps.mblocks, kGvRows};
 
@@ -188,16 +192,12 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
         armed_mask |= 1ull << s;
         armed_ph = (armed_ph & ~(1ull << s)) | (static_cast<uint64_t>(ph) << s);
         ptx::mbar_arrive_expect_tx(fb, CPS * kQChunk);
-        if (PAIR) {
-          // K steps ks .. ks + QG - 1 of the tile's two 128-row blocks
-          const size_t c0 = (static_cast<size_t>(tl.e) * p.mblocks + 2 * tl.mb) * p.ksteps + ks;
-          ptx::bulk_load(ptx::smem_u32(sQ + s * CPS * kQChunk), p.tiles + c0 * kQChunk, QG * kQChunk, fb, pol);
-          ptx::bulk_load(ptx::smem_u32(sQ + (s * CPS + QG) * kQChunk), p.tiles + (c0 + p.ksteps) * kQChunk,
+        // K steps ks .. ks + QG - 1 of each of the tile's BPT 128-row blocks
+        const size_t c0 = (static_cast<size_t>(tl.e) * p.mblocks + BPT * tl.mb) * p.ksteps + ks;
+#pragma unroll
+        for (int bb = 0; bb < BPT; ++bb)
+          ptx::bulk_load(ptx::smem_u32(sQ + (s * CPS + bb * QG) * kQChunk), p.tiles + (c0 + bb * p.ksteps) * kQChunk,
                          QG * kQChunk, fb, pol);
-        } else {
-          const size_t chunk = (static_cast<size_t>(tl.e) * p.mblocks + tl.mb) * p.ksteps + ks;
-          ptx::bulk_load(ptx::smem_u32(sQ + s * QG * kQChunk), p.tiles + chunk * kQChunk, QG * kQChunk, fb, pol);
-        }
         if (++s == SQ) {
           s = 0;
           ph ^= 1u;
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
         for (int st = 0; st < S; ++st) {
           uint2 cw[4];  // code words of rows r0 + 8i, inputs 16q .. 16q + 15 of the step
           float sc[4];  // their group scales
-          const uint8_t* chunk = sQ + (sq * CPS + (PAIR ? blk * S + st : st)) * kQChunk;
+          const uint8_t* chunk = sQ + (sq * CPS + blk * S + st) * kQChunk;
           const uint16_t* scl = reinterpret_cast<const uint16_t*>(chunk + kQBytes);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -377,47 +377,49 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       gbase += static_cast<uint32_t>(p.ksteps);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(xempty0 + 8 * b);
-      // The group that took the tile's last ring slot (it finishes last)
-      // reduces and stores; the others hand it their sums of the valid token
-      // columns (lanes q < 2), slot ri = their distance after it - 1.
-      const int eg = static_cast<int>((sbase + static_cast<uint32_t>(nslot) - 1u) % G);
-      if (grp != eg) {
-        got = wait_bounded<kSleepEpi>(rede0 + 8 * b, use ^ 1u, misc + 1, p.status);
+      if constexpr (G > 1) {  // (one group: it holds the whole sums)
+        // The group that took the tile's last ring slot (it finishes last)
+        // reduces and stores; the others hand it their sums of the valid token
+        // columns (lanes q < 2), slot ri = their distance after it - 1.
+        const int eg = static_cast<int>((sbase + static_cast<uint32_t>(nslot) - 1u) % G);
+        if (grp != eg) {
+          got = wait_bounded<kSleepEpi>(rede0 + 8 * b, use ^ 1u, misc + 1, p.status);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          if (q < kGvRows / 2) {
+            const int ri = (grp - eg - 1 + G) % G;
+            float* red = sRed + b * C::kRedFloats + ri * (RT * kGvRows) + blk * (kBM * kGvRows);
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              red[(r0 + 8 * i) * kGvRows + 2 * q] = acc[2 * i];
+              red[(r0 + 8 * i) * kGvRows + 2 * q + 1] = acc[2 * i + 1];
+            }
+          }
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(redf0 + 8 * b);
+          continue;
+        }
+        got = wait_bounded<kSpin>(redf0 + 8 * b, use, misc + 1, p.status);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         if (q < kGvRows / 2) {
-          const int ri = (grp - eg - 1 + G) % G;
-          float* red = sRed + b * C::kRedFloats + ri * (RT * kGvRows) + blk * (kBM * kGvRows);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            red[(r0 + 8 * i) * kGvRows + 2 * q] = acc[2 * i];
-            red[(r0 + 8 * i) * kGvRows + 2 * q + 1] = acc[2 * i + 1];
+  #pragma unroll
+          for (int gi = 0; gi < G - 1; ++gi) {
+            const float* red = sRed + b * C::kRedFloats + gi * (RT * kGvRows) + blk * (kBM * kGvRows);
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc[2 * i] += red[(r0 + 8 * i) * kGvRows + 2 * q];
+              acc[2 * i + 1] += red[(r0 + 8 * i) * kGvRows + 2 * q + 1];
+            }
           }
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(redf0 + 8 * b);
-        continue;
+        if (lane == 0) ptx::mbar_arrive(rede0 + 8 * b);
       }
-      got = wait_bounded<kSpin>(redf0 + 8 * b, use, misc + 1, p.status);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      if (q < kGvRows / 2) {
-#pragma unroll
-        for (int gi = 0; gi < G - 1; ++gi) {
-          const float* red = sRed + b * C::kRedFloats + gi * (RT * kGvRows) + blk * (kBM * kGvRows);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc[2 * i] += red[(r0 + 8 * i) * kGvRows + 2 * q];
-            acc[2 * i + 1] += red[(r0 + 8 * i) * kGvRows + 2 * q + 1];
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(rede0 + 8 * b);
       const int t0 = 2 * q, t1 = 2 * q + 1;
       if (KIND == 1) {
         float* y = reinterpret_cast<float*>(p.out);
@@ -448,9 +450,9 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   __syncthreads();
 }
 
-template <int KIND, int QG, bool PAIR>
+template <int KIND, int QG, int BPT>
 cudaError_t run_gemv_q4_g(const GemmArgs& args, cudaStream_t st) {
-  auto kern = gemv_q4_kernel<KIND, QG, PAIR>;
+  auto kern = gemv_q4_kernel<KIND, QG, BPT>;
   cudaError_t e = ensure_smem(kern, CfgV::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = sm_count();
@@ -459,14 +461,18 @@ cudaError_t run_gemv_q4_g(const GemmArgs& args, cudaStream_t st) {
 }
 
 // A ring slot holds as many consecutive K steps as divide the record's
-// (four, two or one); paired down tiles take two steps of both blocks.
+// (four, two or one).  Down tiles span four 128-row blocks (one group of all
+// sixteen warps: no hand-over of sums) or two when the block count allows,
+// and a slot then holds two steps of each block.
 template <int KIND>
 cudaError_t run_gemv_q4(const GemmArgs& args, cudaStream_t st) {
   const bool even = args.ksteps % 2 == 0;
+  if (KIND == 1 && args.mblocks % 4 == 0)
+    return even ? run_gemv_q4_g<1, 2, 4>(args, st) : run_gemv_q4_g<1, 1, 4>(args, st);
   if (KIND == 1 && args.mblocks % 2 == 0)
-    return even ? run_gemv_q4_g<1, 2, true>(args, st) : run_gemv_q4_g<1, 1, true>(args, st);
-  if (args.ksteps % 4 == 0) return run_gemv_q4_g<KIND, 4, false>(args, st);
-  return even ? run_gemv_q4_g<KIND, 2, false>(args, st) : run_gemv_q4_g<KIND, 1, false>(args, st);
+    return even ? run_gemv_q4_g<1, 2, 2>(args, st) : run_gemv_q4_g<1, 1, 2>(args, st);
+  if (args.ksteps % 4 == 0) return run_gemv_q4_g<KIND, 4, 1>(args, st);
+  return even ? run_gemv_q4_g<KIND, 2, 1>(args, st) : run_gemv_q4_g<KIND, 1, 1>(args, st);
 }
 
 }  // namespace

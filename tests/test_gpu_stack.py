@@ -119,18 +119,22 @@ ODD = wl.LayerConfig("int4_odd", T=16, H=384, E=64, k=4, I=192, bias=None, seed=
 # (I = 128) K steps: a ring slot holds four or two steps of one block
 ODD_K4 = wl.LayerConfig("int4_odd_k4", T=16, H=384, E=64, k=4, I=256, bias=None, seed=29)
 ODD_K2 = wl.LayerConfig("int4_odd_k2", T=16, H=384, E=64, k=4, I=128, bias=None, seed=31)
-GEOM = {"odd": ODD, "odd_k4": ODD_K4, "odd_k2": ODD_K2}
+# down tiles of four blocks with one K step per slot (H = 512, I = 192), and
+# of two blocks with two steps per slot (H = 768: six blocks, I = 128)
+QUAD_K1 = wl.LayerConfig("int4_quad_k1", T=16, H=512, E=64, k=4, I=192, bias=None, seed=37)
+PAIR_K2 = wl.LayerConfig("int4_pair_k2", T=16, H=768, E=64, k=4, I=128, bias=None, seed=41)
+GEOM = {"odd": ODD, "odd_k4": ODD_K4, "odd_k2": ODD_K2, "quad_k1": QUAD_K1, "pair_k2": PAIR_K2}
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode", "odd", "odd_k4", "odd_k2"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "odd", "odd_k4", "odd_k2", "quad_k1", "pair_k2"])
 def test_int4_skewed_routes_split_tiles(name):
     """Decode-sized int4 launches run on the CUDA-core kernel, which splits an
     expert's rows into tiles of 4: routes skewed so that one expert gets 9
     rows (three tiles), others 1-5, graded row by row against the oracle.
-    Down launches with an even block count pair two blocks per tile, odd ones
-    do not; ring slots hold four, two or one K steps: every combination the
-    geometries allow is covered (gate/up 4 and 2 steps; down paired 2 and 1,
-    unpaired 4, 2 and 1)."""
+    Down tiles span four, two or one 128-row blocks (by the block count) and
+    ring slots hold four, two or one K steps: every combination the
+    geometries allow is covered (gate/up 4 and 2 steps; down four blocks with
+    2 and 1, two blocks with 2 and 1, one block with 4, 2 and 1)."""
     cfg = GEOM[name] if name in GEOM else wl.CONFIGS[name]
     T, k, E = 16, cfg.k, cfg.E
     d = wl.layer_inputs(cfg, DEV)
