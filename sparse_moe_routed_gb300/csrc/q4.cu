@@ -115,7 +115,6 @@ __device__ __forceinline__ uint32_t code_pair_biased(uint32_t word, int p, uint3
 template <int KIND, int QG, int BPT>
 __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   using C = CfgV;
-  static_assert(BPT == 1 || KIND == 1, "tiles of several 128-row blocks: down records");
   static_assert(kGvGroups % BPT == 0, "groups");
   constexpr int G = kGvGroups / BPT;               // K-step groups
   constexpr int WPG = BPT * kGvWpg;                // compute warps per group, 32 rows each
@@ -434,7 +433,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       // gate/up tile: gate row 32 cw + r (r = g or g + 8) pairs with up row
       // 32 cw + 16 + r, both in this lane: h index 16 cw + r
       uint16_t* h = reinterpret_cast<uint16_t*>(p.out);
-      const int colA = tl.mb * 64 + 16 * cw + g, colB = colA + 8;
+      const int colA = (tl.mb * BPT + blk) * 64 + 16 * cw + g, colB = colA + 8;
       if (t0 < tl.nrows) {
         const size_t o = static_cast<size_t>(tl.row0 + t0) * p.ldo;
         h[o + colA] = f32_to_bf16(acc[0] / (1.0f + expf(-acc[0])) * acc[4]);
@@ -471,6 +470,7 @@ cudaError_t run_gemv_q4(const GemmArgs& args, cudaStream_t st) {
     return even ? run_gemv_q4_g<1, 2, 4>(args, st) : run_gemv_q4_g<1, 1, 4>(args, st);
   if (KIND == 1 && args.mblocks % 2 == 0)
     return even ? run_gemv_q4_g<1, 2, 2>(args, st) : run_gemv_q4_g<1, 1, 2>(args, st);
+  if (KIND == 0 && args.mblocks % 2 == 0 && args.ksteps % 4 == 0) return run_gemv_q4_g<0, 4, 2>(args, st);
   if (args.ksteps % 4 == 0) return run_gemv_q4_g<KIND, 4, 1>(args, st);
   return even ? run_gemv_q4_g<KIND, 2, 1>(args, st) : run_gemv_q4_g<KIND, 1, 1>(args, st);
 }
