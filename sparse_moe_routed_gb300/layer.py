@@ -203,6 +203,16 @@ class MoELayer:
         refills the same pinned buffers between calls.  Returns after the
         result is in out_host.
         """
+        MoELayer.wait(self.forward_host_submit(x_host, out_host))
+        return out_host
+
+    def forward_host_submit(self, x_host, out_host):
+        """forward_host_graph without the wait: enqueues the graph (input copy,
+        the layer's launches, result copy) on the current stream and returns
+        an event that completes once out_host holds the result.  Until then
+        the caller leaves x_host and out_host alone; calls queued on the same
+        stream run in order, so a caller may queue the next call (with other
+        host buffers) before it waits for this one."""
         key = (x_host.data_ptr(), out_host.data_ptr(), x_host.shape[0])
         graphs = self.__dict__.setdefault("_graphs", {})
         graph = graphs.get(key)
@@ -225,8 +235,14 @@ class MoELayer:
                 body()
             graphs[key] = graph
         graph.replay()
-        torch.cuda.current_stream().synchronize()
-        return out_host
+        done = torch.cuda.Event()
+        done.record()
+        return done
+
+    @staticmethod
+    def wait(done):
+        """Block until a call returned by forward_host_submit has finished."""
+        done.synchronize()
 
     def x_dev_buf(self, T):
         if not hasattr(self, "_xdev") or self._xdev.shape[0] < T:
