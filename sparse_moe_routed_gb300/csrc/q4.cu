@@ -5,6 +5,7 @@
 // bf16 scale per group.  Shared tile machinery: gemm_common.cuh.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "gemm_common.cuh"
 
@@ -84,31 +85,36 @@ struct CfgV {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // The same MMA from the accumulator c (read only) into d.
-__device__ __forceinline__ void mma_16816_bf16_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
-                                                     const float4& c) {
+__device__ __forceinline__ void mma_16816_f16_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                                    const float4& c) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%10,%11,%12,%13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y), "f"(c.z), "f"(c.w));
 }
 
-// Codes of inputs 2p, 2p+1 of a packed word -> bf16 pair (128 + stored code),
-// exact; the stored code is the weight code + 8, so this is 136 + code.
-// `magic` is 0x43004300 held in a register: with the mask as the one
-// immediate, the and-or is a single three-input logic instruction.
-__device__ __forceinline__ uint32_t code_pair_biased(uint32_t word, int p, uint32_t magic) {
+// Codes of a packed word as exact fp16 pairs over the exponent of 1024: in
+// v = word (pairs 0, 1) or word >> 8 (pairs 2, 3), the codes in bits 0-3 and
+// 16-19 give (1024 + stored code) x 2 (lo = true) and those in bits 4-7 and
+// 20-23 give (1024 + 16 stored code) x 2 (lo = false): one three-input
+// logic instruction each (mask as the immediate, `magic` = 0x64006400 held
+// in a register).  The stored code is the weight code + 8.
+__device__ __forceinline__ uint32_t code_pair_f16(uint32_t v, bool lo, uint32_t magic) {
   uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(word >> (4 * p)), "n"(0x000F000F), "r"(magic));
+  if (lo)
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(v), "n"(0x000F000F), "r"(magic));
+  else
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(v), "n"(0x00F000F0), "r"(magic));
   return d;
 }
 
@@ -244,24 +250,41 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       float* xs = sXs + b * C::kXsFloats;
       for (int it = lane; it < p.ksteps * kGvRows; it += 32) {  // item = (K step, token row)
         const int ks = it / kGvRows, j = it % kGvRows;
-        float sum = 0.f;
+        // The step's 64 bf16 values become fp16 in place, those at inputs
+        // with bit 1 set (odd pair words) divided by 16 (they meet codes
+        // scaled by 16); both are exact inside fp16's normal range, and
+        // magnitudes of 65,520 and more become infinite.  s1 sums the stored
+        // values, s16 the token values themselves (fp32, input order).
+        float s1 = 0.f, s16 = 0.f;
         if (j < n) {
-          const uint4* src = reinterpret_cast<const uint4*>(sX + b * C::kXBytes + j * (K * 2 + 16) + ks * (kBK * 2));
+          uint4* src = reinterpret_cast<uint4*>(sX + b * C::kXBytes + j * (K * 2 + 16) + ks * (kBK * 2));
 #pragma unroll
           for (int v = 0; v < kBK / 8; ++v) {
             const uint4 w = src[v];
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              sum += __uint_as_float(ws[e] << 16);
-              sum += __uint_as_float(ws[e] & 0xFFFF0000u);
+              const float sc = (e & 1) ? 0.0625f : 1.0f;
+              const __half2 h2 = __floats2half2_rn(__uint_as_float(ws[e] << 16) * sc,
+                                                   __uint_as_float(ws[e] & 0xFFFF0000u) * sc);
+              const float f0 = __low2float(h2), f1 = __high2float(h2);
+              s1 += f0;
+              s1 += f1;
+              s16 += (e & 1) ? 16.0f * (f0 + f1) : (f0 + f1);
+              std::memcpy(&ws[e], &h2, 4);
             }
+            src[v] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
           }
         }
-        const float c = -136.0f * sum;
+        // sum over the step of A x B = 1024 s1 + sum(stored code x x), and
+        // stored code = code + 8: the MMAs start from -(1024 s1 + 8 s16)
+        const float c = -(1024.0f * s1 + 8.0f * s16);
         xs[ks * 8 + 4 * (j >> 1) + (j & 1)] = c;
         xs[ks * 8 + 4 * (j >> 1) + (j & 1) + 2] = c;
       }
+      // the stage was rewritten by ordinary stores; a later bulk copy into it
+      // (async proxy) must be ordered after them
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(xfull0 + 8 * b);
     }
@@ -292,8 +315,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       }
       // B fragments read token row g of the stage; columns g >= the tile's
       // rows read a stale row and are never stored
-      // 0x43004300, opaque to the compiler so that it stays in a register
-      const uint32_t magic = 0x43004300u | (static_cast<uint32_t>(p.ksteps) >> 31);
+      // 0x64006400 (fp16 1024 pair), opaque to the compiler so that it stays in a register
+      const uint32_t magic = 0x64006400u | (static_cast<uint32_t>(p.ksteps) >> 31);
       const uint8_t* xrow = sX + b * C::kXBytes + (g & (kGvRows - 1)) * (K * 2 + 16) + 32 * q;
       // -136 x the sums of token columns 2q, 2q + 1 in accumulator order
       // (columns past the tile's rows read another column's and are never
@@ -336,30 +359,31 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
           const uint4* xk = reinterpret_cast<const uint4*>(xrow + (u * S + st) * (kBK * 2));
           const uint4 x0 = xk[0], x1 = xk[1];
           const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          // The MMAs take the codes as exact bf16 (136 + code) pairs and
-          // start from -136 sum(x) of the step (from the table), so they end
-          // at sum((136 + c) x) - 136 sum(x) = sum(c x).
+          // The MMAs take the codes as exact fp16 pairs (1024 + stored code
+          // against the token value, 1024 + 16 stored code against a sixteenth
+          // of it) and start from the step's correction in the table, so
+          // they end at sum(code x).
           const float4 xs = *reinterpret_cast<const float4*>(xsum + (u * S + st) * 8);
           float d0[4], d1[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             // word j/2 of a row holds inputs 16q + 8(j/2) .. +7; its pair
             // 2(j%2) is inputs 16q + 4j, +1 and pair 2(j%2) + 1 the next two
-            const int pl = 2 * (j & 1);
-            const uint32_t w0 = (j >> 1) ? cw[0].y : cw[0].x, w1 = (j >> 1) ? cw[1].y : cw[1].x;
-            const uint32_t w2 = (j >> 1) ? cw[2].y : cw[2].x, w3 = (j >> 1) ? cw[3].y : cw[3].x;
-            const uint32_t a0[4] = {code_pair_biased(w0, pl, magic), code_pair_biased(w1, pl, magic),
-                                    code_pair_biased(w0, pl + 1, magic),
-                                    code_pair_biased(w1, pl + 1, magic)};  // rows r0, r0 + 8
-            const uint32_t a1[4] = {code_pair_biased(w2, pl, magic), code_pair_biased(w3, pl, magic),
-                                    code_pair_biased(w2, pl + 1, magic),
-                                    code_pair_biased(w3, pl + 1, magic)};  // rows r0 + 16, r0 + 24
+            const uint32_t sh = (j & 1) ? 8u : 0u;  // pairs 2(j%2), 2(j%2) + 1 sit 8 bits up for odd j
+            const uint32_t v0 = ((j >> 1) ? cw[0].y : cw[0].x) >> sh, v1 = ((j >> 1) ? cw[1].y : cw[1].x) >> sh;
+            const uint32_t v2 = ((j >> 1) ? cw[2].y : cw[2].x) >> sh, v3 = ((j >> 1) ? cw[3].y : cw[3].x) >> sh;
+            const uint32_t a0[4] = {code_pair_f16(v0, true, magic), code_pair_f16(v1, true, magic),
+                                    code_pair_f16(v0, false, magic),
+                                    code_pair_f16(v1, false, magic)};  // rows r0, r0 + 8
+            const uint32_t a1[4] = {code_pair_f16(v2, true, magic), code_pair_f16(v3, true, magic),
+                                    code_pair_f16(v2, false, magic),
+                                    code_pair_f16(v3, false, magic)};  // rows r0 + 16, r0 + 24
             if (j == 0) {
-              mma_16816_bf16_first(d0, a0, xb[0], xb[1], xs);
-              mma_16816_bf16_first(d1, a1, xb[0], xb[1], xs);
+              mma_16816_f16_first(d0, a0, xb[0], xb[1], xs);
+              mma_16816_f16_first(d1, a1, xb[0], xb[1], xs);
             } else {
-              mma_16816_bf16(d0, a0, xb[2 * j], xb[2 * j + 1]);
-              mma_16816_bf16(d1, a1, xb[2 * j], xb[2 * j + 1]);
+              mma_16816_f16(d0, a0, xb[2 * j], xb[2 * j + 1]);
+              mma_16816_f16(d1, a1, xb[2 * j], xb[2 * j + 1]);
             }
           }
           acc[0] = fmaf(sc[0], d0[0], acc[0]);  // row r0, token 2q
