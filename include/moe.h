@@ -191,8 +191,12 @@ MOE_API moe_status moe_route_permute(const uint16_t *x, const uint16_t *w_router
  *                   and s_down [E, H, I/64] bf16, one scale per 64 consecutive
  *                   inputs of a row; w = scale * code.  (AFN-001, section
  *                   "Phase 2": affine4 with group size 64, read as symmetric
- *                   codes with one bf16 scale per group.)  The tensor cores
- *                   see w = bf16(scale * code).
+ *                   codes with one bf16 scale per group.)  Decode-sized
+ *                   launches (up to 320 slots, K <= 2560) multiply the exact
+ *                   codes with the token values rounded to fp16 (exact inside
+ *                   fp16's normal range; magnitudes of 65,520 and more become
+ *                   infinite) and apply the scale in fp32; larger launches
+ *                   give the tensor cores w = bf16(scale * code).
  *
  * moe_expert_gateup:  for every slot s of expert e (offsets from moe_permute)
  *     g = Wgate_e . x_perm[s],  u = Wup_e . x_perm[s]      (fp32 accumulate)
