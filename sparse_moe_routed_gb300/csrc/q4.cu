@@ -22,44 +22,42 @@ namespace {
 // memory, so the codes of each K step would be expanded into a 16 KB bf16
 // tile and read back (measured: ~0.35 us per 4.3 KB step), while a CUDA-core
 // dot product spends ~6 instructions per weight.  Here the weights go from
-// registers straight into warp-level MMAs (mma.sync m16n8k16, bf16 in, fp32
-// accumulate): each code pair becomes an exact bf16 pair (136 + code) in one
-// or two instructions (each token row's sums over the K steps, computed once
-// per tile, supply the 136 x sum(x) correction), token values enter as bf16
-// with no conversion, and one MMA instruction consumes 256 weights against up
-// to 8 token rows.
+// registers straight into warp-level MMAs (mma.sync m16n8k16, fp16 in, fp32
+// accumulate): the codes of a packed word become exact fp16 pairs over the
+// exponent of 1024 (1024 + c, or 1024 + 16c for the codes in bits 4-7 of a
+// half-word), four logic instructions and one shift per word; the token
+// values that meet the 16c codes are staged divided by 16 (exact in fp16), and
+// one MMA instruction consumes 256 weights against up to 8 token rows.
 //
-// Warps: 0 streams packed chunks (bulk copies, deep ring), 1 stages each
-// tile's token rows (one bulk copy per row, double-buffered) and their
-// per-step sums, the rest
-// compute in kGvGroups groups of four.  The groups take K steps in turn, so
-// each warp has several steps' time for the latency chain of one (wait,
-// loads, dequantise, MMAs).  Warp w of a group owns tile rows 32w .. 32w + 31
-// as two MMA row tiles that share the token fragments: per K step (one scale
-// group of 64 inputs) it runs eight MMAs, the first of each chain starting
-// from -136 x the step's token sums, and adds scale x partial to its fp32
-// accumulators.  The MMA's k slots run over the step's inputs in
-// a permuted order (the same for weights and tokens), chosen so that each
-// lane reads 16 consecutive inputs: one 8-byte load per weight row, two
-// 16-byte loads of token values, and every code pair at a fixed nibble
-// position.  A group takes whole ring slots (two K steps for gate/up
-// records), so the wait, the release and the address arithmetic of a slot
-// are shared by two steps' MMAs.  In a gate/up record rows 32w .. 32w + 15 are gate
-// and 32w + 16 .. 32w + 31 the up rows of the same h columns, so each lane
-// ends a tile holding gate and up of the same outputs.  At the end of a tile
-// the other groups hand their sums (valid token columns only) through shared
-// memory to the group that took the tile's last ring slot, which adds them in
-// a fixed order (the same bits every call) and stores y, or
-// h = silu(gate) * up.  Token columns past the
-// tile's rows read stale staged rows and are never stored (an MMA column
-// depends on its own B column only).
+// Warps: 0 streams packed chunks (bulk copies, deep ring); 1 stages each
+// tile's token rows (one bulk copy per row, double-buffered), converts them
+// to fp16 in place and writes each step's bias correction (from the row sums)
+// into a table; the rest compute in groups.  The groups take ring slots (a
+// slot holds four K steps, or two of each block of a multi-block tile) in
+// turn, so each warp has several steps' time for the latency chain of one
+// (wait, loads, conversion, MMAs); one wait and one release per slot.  Warp w
+// of a group owns tile rows 32w .. 32w + 31 of one 128-row block as two MMA
+// row tiles that share the token fragments: per K step (one scale group of
+// 64 inputs) it runs eight MMAs, the first of each chain starting from the
+// step's correction, and adds scale x partial to its fp32 accumulators.  The
+// MMA's k slots run over the step's inputs in a permuted order (the same for
+// weights and tokens), chosen so that each lane reads 16 consecutive inputs:
+// one 8-byte load per weight row, two 16-byte loads of token values, and
+// every code pair at a fixed nibble position.  In a gate/up record rows
+// 32w .. 32w + 15 are gate and 32w + 16 .. 32w + 31 the up rows of the same h
+// columns, so each lane ends a tile holding gate and up of the same outputs.
+// At the end of a tile the other groups hand their sums (valid token columns
+// only) through shared memory to the group that took the tile's last ring
+// slot, which adds them in a fixed order (the same bits every call) and
+// stores y, or h = silu(gate) * up.  Token columns past the tile's rows read
+// stale staged rows and are never stored (an MMA column depends on its own B
+// column only).
 //
-// Down tiles (K = I = 640: ten K steps) are short, so the per-tile work of
-// the group split (staging, the hand-over of sums) weighs more: a down tile
-// spans four of the record's 128-row blocks when their count allows (512
-// rows, one group of all sixteen warps, no hand-over) or two (256 rows, two
-// groups of eight), each warp owning 32 rows of one block; a ring slot then
-// holds the same K steps of every block of the tile.
+// Tiles span several 128-row blocks where the record's block count allows:
+// gate/up tiles two (two groups of eight warps), down tiles (K = I = 640: ten
+// K steps, so the per-tile staging and hand-over weigh more) four (one group
+// of all sixteen warps, no hand-over) or two; each warp owns 32 rows of one
+// block, and a ring slot holds the same K steps of every block of the tile.
 constexpr int kGvRows = 4;                     // token rows per tile
 constexpr int kGvN = 8;                        // MMA N: token columns (those past kGvRows are never stored)
 constexpr int kGvGroups = 4;
@@ -76,8 +74,9 @@ struct CfgV {
   static constexpr int kXBytes = kGvRows * (kGvMaxK * 2 + 16);
   static constexpr int kUpFloats = 0;
   static constexpr int kRedFloats = (kGvGroups - 1) * kBM * kGvRows;  // other groups' sums: [G-1][128][4]
-  // per K step, -136 x each staged token row's sum in the MMA accumulator
-  // layout of the two lane classes: [K steps][c0, c1, c0, c1, c2, c3, c2, c3]
+  // per K step, each staged token row's bias correction in the MMA
+  // accumulator layout of the two lane classes:
+  // [K steps][c0, c1, c0, c1, c2, c3, c2, c3]
   static constexpr int kXsFloats = kGvMaxK / 64 * 8;
   static constexpr int kNumBars = 2 * SQmax + 12;
   static constexpr int kSmemBytes = 1024 + SQmax * kQChunk + 2 * kXBytes + 2 * kUpFloats * 4 +
@@ -137,7 +136,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   uint8_t* sQ = base;                                  // [SQ][CPS x 4,352 B] packed codes + scales
   uint8_t* sX = sQ + C::SQmax * kQChunk;               // [2][8 rows][K] bf16 token rows of a tile
   float* sRed = reinterpret_cast<float*>(sX + 2 * C::kXBytes);  // [2][G-1][128][4] other groups' sums
-  float* sXs = sRed + 2 * C::kRedFloats;  // [2][K steps][8]: -136 x each token row's sum over each K step
+  float* sXs = sRed + 2 * C::kRedFloats;  // [2][K steps][8]: each token row's bias correction per K step
   uint64_t* bars = reinterpret_cast<uint64_t*>(sXs + 2 * C::kXsFloats);
   const uint32_t qfull0 = ptx::smem_u32(bars);
   const uint32_t qempty0 = qfull0 + 8 * C::SQmax;
@@ -216,9 +215,10 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   } else if (warp == 1) {
     // ------------------------------------------------ token-row producer
     // Lane 0 stages each tile's token rows (one bulk copy per row); once they
-    // have landed the warp sums every row over every 64-input K step (fp32,
-    // in input order) into the tile's table, which supplies the 136 x sum(x)
-    // correction of the biased codes, and then marks the stage full.
+    // have landed the warp converts them to fp16 in place and sums every row
+    // over every 64-input K step (fp32, input order) into the tile's table,
+    // which supplies the correction of the biased codes, and then marks the
+    // stage full.
     const uint64_t pol = ptx::policy_evict_last();
     uint32_t armed_mask = 0, armed_ph = 0;
     bool ok = true;
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
       // 0x64006400 (fp16 1024 pair), opaque to the compiler so that it stays in a register
       const uint32_t magic = 0x64006400u | (static_cast<uint32_t>(p.ksteps) >> 31);
       const uint8_t* xrow = sX + b * C::kXBytes + (g & (kGvRows - 1)) * (K * 2 + 16) + 32 * q;
-      // -136 x the sums of token columns 2q, 2q + 1 in accumulator order
+      // the corrections of token columns 2q, 2q + 1 in accumulator order
       // (columns past the tile's rows read another column's and are never
       // stored)
       const float* xsum = sXs + b * C::kXsFloats + 4 * (q & 1);
