@@ -233,6 +233,17 @@ def workload_name(cfg):
     return f"{cfg.name}_T{cfg.T}_H{cfg.H}_E{cfg.E}_k{cfg.k}_I{cfg.I}" + ("_zipf" if cfg.bias == "zipf" else "")
 
 
+def layer_config(cfg, NL, world, plain=False):
+    """The `config` object of a single-layer workload's line (both arms)."""
+    rec = cfg.E * 3 * cfg.H * cfg.I * 2 + cfg.E * cfg.H * 2
+    return {"workload": workload_name(cfg), "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+            "router_bias": cfg.bias or "none", "layer_weight_sets": NL,
+            "weights": "plain bf16 records (TMA tensor maps)" if plain else
+                       "tile-packed bf16 records (one bulk copy per stage)",
+            "l2": f"inputs larger than L2: {NL} distinct layer weight sets rotated ({NL * rec / 1e9:.1f} GB)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
     """Reference arm: the CPU oracle as it stands, on the host cores."""
     rank, world, _ = dist_env()
@@ -246,7 +257,8 @@ def run_reference(args):
     d = wl.layer_inputs(cfg, dev, with_x=False)
     hw = host_weights(d)
     del d
-    sample_T = min(cfg.T, 4)
+    # the decode block whole (16 tokens); larger workloads in 16-token samples
+    sample_T = min(cfg.T, 16)
     xs = [oracle.bf16_bits(wl.token_batch(cfg, "cpu", index=i, T=sample_T)) for i in range(4)]
     threads = oracle.threads(0)
     for i in range(args.warmup):
@@ -260,7 +272,8 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": workload_name(cfg), "tokens_per_step": sample_T},
+            "config": layer_config(cfg, args.layers or (8 if args.config == "decode" else 1), world),
+            "tokens_per_step": sample_T,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"{sample_T} tokens of the {cfg.name} workload per step "
                                        f"(route + 10 experts + combine, fp64 C, OpenMP)"},
@@ -369,22 +382,8 @@ def main():
         return u * (gu_w_bytes + dn_w_bytes) + router_bytes + 2 * cfg.T * H * 2 + R * 8
 
     K = args.steps
-    EV_EVERY = 7 if K >= 64 else 1  # coprime with the 8 rotated layers
-    KE = (K + EV_EVERY - 1) // EV_EVERY
-    ev_g0 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
-    ev_g1 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
-    ev_d1 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(gpu_uuid(local))
-    time.sleep(0.3)
-
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    t_issue0 = time.perf_counter()
-    e_start.record(st)
+    # the host-side argument lists of every layer's calls, built before the
+    # timed region
     bound = [layers[l].bound_calls(xs[l], cfg.T, stream=st) for l in range(NL)]
     names = [c[0] for c in bound[0]]
     fused = "moe_expert_swiglu_fused" in names
@@ -397,26 +396,23 @@ def main():
     # the dominant kernel(s): the fused contraction, or gate/up then down
     i_main = names.index("moe_expert_swiglu_fused" if fused else "moe_expert_gateup")
     issue = MoELayer.issue
-    # Per-kernel events bracket the contraction(s) on every EV_EVERY-th step
-    # (an event between kernels ends the overlap that programmatic dependent
-    # launch gives the next kernel, so the other steps run without them).
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_uuid(local))
+    time.sleep(0.3)
+
+    # Headline: K whole steps with nothing between the kernels (an event
+    # between two kernels would end the overlap that programmatic dependent
+    # launch gives the next one), bracketed by two events.
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    t_issue0 = time.perf_counter()
+    e_start.record(st)
     for i in range(K):
-        calls = bound[i % NL]
-        if i % EV_EVERY == 0:
-            j = i // EV_EVERY
-            for c in calls[:i_main]:
-                issue(c)
-            ev_g0[j].record(st)
-            issue(calls[i_main])
-            ev_g1[j].record(st)
-            if not fused:
-                issue(calls[i_main + 1])
-            ev_d1[j].record(st)
-            for c in calls[i_main + (1 if fused else 2):]:
-                issue(c)
-        else:
-            for c in calls:
-                issue(c)
+        for c in bound[i % NL]:
+            issue(c)
     e_end.record(st)
     t_issue1 = time.perf_counter()
     torch.cuda.synchronize()
@@ -424,6 +420,30 @@ def main():
     if world > 1:
         dist.barrier()
     sampler.stop()
+
+    # Instrumented pass, after the headline region: the same steps with
+    # events around the dominant launch(es) of every step, to time that
+    # kernel alone.  Its prologue then no longer overlaps the previous
+    # kernel, so this launch time is an upper bound of the one inside the
+    # headline steps.
+    KE = min(max(K, 64), 2000)
+    ev_g0 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    ev_g1 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    ev_d1 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    EV_EVERY = 1
+    for j in range(KE):
+        calls = bound[j % NL]
+        for c in calls[:i_main]:
+            issue(c)
+        ev_g0[j].record(st)
+        issue(calls[i_main])
+        ev_g1[j].record(st)
+        if not fused:
+            issue(calls[i_main + 1])
+        ev_d1[j].record(st)
+        for c in calls[i_main + (1 if fused else 2):]:
+            issue(c)
+    torch.cuda.synchronize()
 
     total_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
     gu_ms = [ev_g0[j].elapsed_time(ev_g1[j]) for j in range(KE)]
@@ -519,13 +539,8 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded; x~N(0,1), weights~N(0,0.02) bf16)",
-        "config": {"workload": wl_name, "T": cfg.T, "H": H, "E": E, "k": cfg.k, "I": I,
-                   "router_bias": cfg.bias or "none", "layer_weight_sets": NL,
-                   "weights": "plain bf16 records (TMA tensor maps)" if args.plain else
-                              "tile-packed bf16 records (one bulk copy per stage)",
-                   "l2": f"inputs larger than L2: {NL} distinct layer weight sets rotated "
-                         f"({NL * (E * 3 * H * I * 2 + router_bytes) / 1e9:.1f} GB)",
-                   "parallelism": f"replicas x{world}", "unique_experts_per_step": U},
+        "config": layer_config(cfg, NL, world, args.plain),
+        "unique_experts_per_step": U,
         "roofline": roof_main, "roofline_other": roof_other,
         "layer_roofline": {"bytes_per_step": layer_bytes_avg,
                            "achieved_gbs": layer_bytes_avg / (step_ms / 1e3) / 1e9,
@@ -534,7 +549,8 @@ def main():
                            "frac_tensor": flops_step / (step_ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
                            **({} if fused else {"down_avg_us": dn_avg * 1e3})},
         "host_issue_us_per_step": 1e6 * (t_issue1 - t_issue0) / K,
-        "events_every": EV_EVERY,
+        "dominant_kernel_timing": f"separate pass of {KE} steps after the headline region, events around "
+                                  f"the dominant launch of every step; the headline steps carry no events",
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         # route: logits + selection; permute (+ row gather unless the fused
         # launch gathers); experts (fused: one launch; else gate/up, down, combine)
@@ -611,10 +627,8 @@ def run_stack(args, rank, world, local, dev):
         Ul.append(int((stack.layers[l].counts > 0).sum().item()))
     bytes_block = sum(u * rec_bytes for u in Ul) + L * router_bytes
     K = args.steps
-    EV = 7 if K >= 64 else 1
-    KE = (K + EV - 1) // EV
-    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
-    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    # every layer's calls on the fixed stream buffer, built before the timed region
+    lcalls = [stack.layer_calls(xw, l, stream=st) for l in range(L)]
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(gpu_uuid(local))
@@ -623,23 +637,13 @@ def run_stack(args, rank, world, local, dev):
         dist.barrier()
     torch.cuda.synchronize()
     tw0 = time.time()
+    # headline: K blocks through all L layers, no events between the kernels
     e0.record(st)
     for i in range(K):
         xw.copy_(xs[i % NB])
-        lt = i % L
         for l in range(L):
-            calls = stack.layer_calls(xw, l, stream=st)
-            if l == lt and i % EV == 0:
-                for c in calls[:3]:
-                    MoELayer.issue(c)
-                g0[i // EV].record(st)
-                MoELayer.issue(calls[3])
-                g1[i // EV].record(st)
-                for c in calls[4:]:
-                    MoELayer.issue(c)
-            else:
-                for c in calls:
-                    MoELayer.issue(c)
+            for c in lcalls[l]:
+                MoELayer.issue(c)
     e1.record(st)
     torch.cuda.synchronize()
     tw1 = time.time()
@@ -647,6 +651,29 @@ def run_stack(args, rank, world, local, dev):
     total_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     for ml in stack.layers:
         assert ml.read_status() == 0, f"device status {ml.read_status():#x}"
+    # instrumented pass after the headline region: events around one layer's
+    # gate/up launch per block, the layer rotating over the stack
+    KE = min(max(K, 2 * L), 4 * L)
+    EV = 1
+    g0 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    g1 = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    for i in range(KE):
+        xw.copy_(xs[i % NB])
+        lt = i % L
+        for l in range(L):
+            calls = lcalls[l]
+            if l == lt:
+                for c in calls[:3]:
+                    MoELayer.issue(c)
+                g0[i].record(st)
+                MoELayer.issue(calls[3])
+                g1[i].record(st)
+                for c in calls[4:]:
+                    MoELayer.issue(c)
+            else:
+                for c in calls:
+                    MoELayer.issue(c)
+    torch.cuda.synchronize()
     gu = [g0[j].elapsed_time(g1[j]) for j in range(KE)]
     gu_avg = sum(gu) / KE
     R = T * cfg.k

@@ -115,9 +115,12 @@ MOE_API moe_status moe_route(const uint16_t *x, const uint16_t *w_router, const 
  * Same arguments and results as moe_route, without the workspace: the
  * [T,E] fp32 logits scratch lives in a fixed 256 KB array inside the library
  * (held by every GPU that loads it, until exit).  Limits: T <= 64 and
- * E <= 1024; larger calls return MOE_EWORKSPACE and enqueue nothing.  The
- * first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  All
+ * E <= 1024.  T > 64 returns MOE_EWORKSPACE; E > 1024 is beyond the router's
+ * own limit and returns MOE_ENOTSUP; either way nothing is enqueued.  Every
+ * call looks up the array's device address for the current device (a host
+ * lookup, so a reset device never gets a stale address); the first call on a
+ * device may load the library's device code, so make it before any stream
+ * capture.  All
  * calls share the array: calls that overlap on the GPU (e.g. on two streams)
  * race.  Nothing in the array needs to start at zero.  No allocation of any
  * kind is made.

@@ -26,8 +26,9 @@ Functions and the page passages they follow (Hebrus "Agent Field Notes"):
   combine(...)          AFN-019, section "Hypothesis H4" (weighted sum in route-rank order).
   rmsnorm(...)          AFN-001, section "Phase 1" (zero-centred RMS normalisation).
   recall_hits(...)      AFN-019, section "Hypothesis H2" (predicted vs exact top-k).
-  round_bf16_bits(...)  bf16 rounding of the normalised stack input (reading: router and
-                        experts consume bf16 activations).
+  round_bf16_bits(...)  bf16 rounding of the normalised stack input (reading: the layer's
+                        input is bf16 in every workload, and in the stack that input is
+                        RMSNorm(x_l); the residual stream stays fp32).
 
 Parity pins: every function above is pinned in tests/test_oracle_pins.py
 against closed forms, brute force on tiny inputs, special cases reducing to

@@ -305,8 +305,11 @@ void oracle_recall(const int32_t *pred, const int32_t *ref, int T, int k, int32_
 }
 
 /* fp32 -> bf16 bit patterns, round to nearest, ties to even (NaN kept
- * quiet).  The router and experts of a stack layer read the RMS-normalised
- * residual rounded to bf16, as their tensor-core inputs are bf16.           */
+ * quiet).  Reading for the residual stack: the MoE layer's input x is bf16
+ * in every workload of the layer (the Qwen4Exp geometry's tokens are bf16),
+ * and in the stack that input is RMSNorm(x_l); so the normalised residual is
+ * rounded to bf16 once before routing and the experts, while the residual
+ * stream itself stays fp32.                                                 */
 void oracle_round_bf16(const float *x, size_t n, uint16_t *out) {
   for (size_t i = 0; i < n; ++i) {
     uint32_t u;

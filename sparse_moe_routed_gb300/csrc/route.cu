@@ -747,11 +747,14 @@ cudaError_t launch_route_permute(const uint16_t* x, const uint16_t* wr, const fl
 //
 //  * Limit: T <= 64 tokens and E <= 1024 experts (64 x 1024 fp32 = 256 KB).
 //    Every GPU that loads the library holds this array until the process
-//    exits.  Larger calls are rejected with MOE_EWORKSPACE.
-//  * The host-side name g_route_scratch is not a device address; the first
-//    call on a device looks the device address up with
-//    cudaGetSymbolAddress() (with that device current) and remembers it, so
-//    that first call should come before any stream capture.
+//    exits.  T > 64 is rejected with MOE_EWORKSPACE; E > 1024 is beyond the
+//    router's own limit and is rejected first, with MOE_ENOTSUP.
+//  * The host-side name g_route_scratch is not a device address.  Every
+//    call looks the device address up with cudaGetSymbolAddress() for the
+//    device that is current (a host-side lookup, no allocation), so a call
+//    after a device reset or a new context never uses an address from an
+//    earlier one.  The first call on a device may load the library's device
+//    code for that device, so it should come before any stream capture.
 //  * All calls share the array and it keeps the last call's contents.
 //    Nothing in it needs to start at zero: the logits kernel overwrites the
 //    whole [T, E] region before the selection kernel reads it.  Calls that
@@ -764,19 +767,13 @@ constexpr int kNoAllocMaxT = 64;
 constexpr int kNoAllocMaxE = 1024;
 static __device__ __align__(256) float g_route_scratch[kNoAllocMaxT * kNoAllocMaxE];
 
-// Device address of g_route_scratch on the current device (nullptr on error).
+// Device address of g_route_scratch on the current device (nullptr on
+// error).  Looked up on each call rather than cached: after cudaDeviceReset()
+// or a new primary context the module is loaded again and the array can move.
 float* noalloc_scratch_for_current_device() {
-  static std::mutex mu;
-  static float* addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<float*>(p);
-  }
-  return addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return nullptr;
+  return static_cast<float*>(p);
 }
 
 }  // namespace

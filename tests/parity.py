@@ -50,6 +50,12 @@ def compare_routes(ids_gpu, w_gpu, ids_ref, w_ref, gap_ref, logits_ref):
     return {"checked": checked, "near_tie": near_tie, "rank_swaps": rank_swaps, "exact_rows": match_rows}
 
 
+def compare_route_ids(ids_gpu, ids_ref, gap_ref, logits_ref):
+    """compare_routes for a route whose weights are not kept (IDs only)."""
+    w = np.zeros(np.asarray(ids_ref).shape, np.float32)
+    return compare_routes(ids_gpu, w, ids_ref, w, gap_ref, logits_ref)
+
+
 def output_errors(out, ref):
     out = np.asarray(out, np.float64)
     ref = np.asarray(ref, np.float64)

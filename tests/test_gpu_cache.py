@@ -16,6 +16,7 @@ import torch
 
 import oracle
 import workloads as wl
+from parity import assert_output_close, compare_routes
 from sparse_moe_routed_gb300 import CachedMoELayer, MoELayer, _lib, pack_layer_experts
 
 pytestmark = pytest.mark.gpu
@@ -145,6 +146,37 @@ def test_cached_layer_bitwise_qwen_geometry(wave, fetch, policy):
     """Qwen4Exp expert shape (H 2560, I 640) over 64 experts, 40 slots."""
     _, s = run_sequence(QWEN64, S=40, wave=wave, fetch=fetch, calls=8, policy=policy)
     assert s[2] > 0 and s[3] > 40
+
+
+def test_cached_layer_with_misses_against_oracle():
+    """Qwen4Exp expert shape over 64 experts and 40 slots: every call of a
+    sequence with hits, misses and evictions graded directly against the CPU
+    oracle (routes, and the layer output of every token whose route the
+    oracle confirms), not only against the resident layer."""
+    cfg = QWEN64
+    ref, hgu, hdn, d = layers(cfg)
+    lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, cfg.T, I=cfg.I, S=40, wave=2, fetch="wave")
+    wr = oracle.bf16_bits(d["w_router"])
+    wgu = oracle.bf16_bits(d["w_gateup"])
+    wdn = oracle.bf16_bits(d["w_down"])
+    graded = 0
+    for i in range(8):
+        x = wl.token_batch(cfg, DEV, index=[0, 1, 0, 2, 3, 1, 4, 0][i], T=cfg.T)
+        out = lay.forward(x).float().cpu().numpy()
+        torch.cuda.synchronize()
+        assert lay.read_status() == 0
+        xb = oracle.bf16_bits(x)
+        ids_r, w_r, gap_r, L_r = oracle.route(xb, wr, None, cfg.k)
+        rep = compare_routes(lay.ids[:cfg.T].cpu().numpy(), lay.w[:cfg.T].cpu().numpy(), ids_r, w_r, gap_r, L_r)
+        keep = np.array(rep["exact_rows"], dtype=np.int64)
+        if len(keep) == 0:
+            continue
+        want = oracle.experts_combine(oracle.bits_to_f32(xb[keep]), ids_r[keep], w_r[keep], cfg.H, cfg.I,
+                                      wgu_bits=wgu, wd_bits=wdn)
+        assert_output_close(out[keep], want, what=f"cached layer call {i}")
+        graded += len(keep)
+    s = lay.stats.cpu().tolist()
+    assert s[2] > 0 and s[3] > 40 and graded >= 0.9 * 8 * cfg.T, (s, graded)
 
 
 def test_cached_layer_host_graph():

@@ -204,6 +204,58 @@ def test_int4_stack_forced_routes_six_layers():
     print(f"6 layers forced routes: max err {rel_max:.2e} of max|ref|, mean rel {mean_rel:.2e}")
 
 
+def _used_experts_host(w, ids):
+    """Host copies of only the experts that ids name (the oracle reads whole
+    records), and ids renumbered into that subset."""
+    used = np.unique(ids)
+    sel = torch.from_numpy(used.astype(np.int64)).to(DEV)
+    host = {"wgu_q": w["w_gateup_q"].index_select(0, sel).cpu().numpy(),
+            "sgu": oracle.bf16_bits(w["s_gateup"].index_select(0, sel)),
+            "wd_q": w["w_down_q"].index_select(0, sel).cpu().numpy(),
+            "sd": oracle.bf16_bits(w["s_down"].index_select(0, sel))}
+    return host, np.searchsorted(used, ids).astype(np.int32)
+
+
+def test_int4_stack_all_48_layers_teacher_forced():
+    """Every layer of the 48-layer int4 stack (its own router and experts),
+    one decode block of 16 tokens, graded per layer with teacher forcing: the
+    oracle's layer l is fed the GPU's residual x_l, so a legitimate near-tie
+    flip in one layer cannot cascade.  Routes are graded as everywhere else;
+    the residual update of every token whose route matches is graded against
+    the oracle's int4 experts.  One layer's weights are held at a time."""
+    T = 16
+    x = wl.token_batch(CFG, DEV, index=11, T=T).float()
+    graded = near = 0
+    worst = (0.0, 0.0)
+    for l in range(wl.STACK_LAYERS):
+        w = wl.stack_layer_weights(l, DEV)
+        gu, dn = pack_layer_experts(w["w_gateup_q"], w["w_down_q"], _lib.MOE_W_INT4_G64, CFG.E, CFG.H, CFG.I,
+                                    s_gateup=w["s_gateup"], s_down=w["s_down"])
+        ml = MoELayer(w["w_router"], None, gu, dn, CFG.k, T, fmt=_lib.MOE_W_INT4_G64_TILED, I=CFG.I)
+        stack = MoEStack([ml], T)
+        x_l = x.cpu().numpy()
+        stack.forward(x)
+        torch.cuda.synchronize()
+        assert ml.read_status() == 0, l
+        n_bits = oracle.round_bf16_bits(oracle.rmsnorm(x_l, None, eps=1e-6))
+        ids_r, w_r, gap_r, L_r = oracle.route(n_bits, oracle.bf16_bits(w["w_router"]), None, CFG.k)
+        rep = compare_routes(ml.ids[:T].cpu().numpy(), ml.w[:T].cpu().numpy(), ids_r, w_r, gap_r, L_r)
+        keep = np.array(rep["exact_rows"], dtype=np.int64)
+        assert len(keep) >= T - 3, (l, rep)
+        host, local_ids = _used_experts_host(w, ids_r[keep])
+        moe_ref = oracle.experts_combine(oracle.bits_to_f32(n_bits[keep]), local_ids, w_r[keep], CFG.H, CFG.I,
+                                         wgu_q=host["wgu_q"], sgu_bits=host["sgu"], wd_q=host["wd_q"],
+                                         sd_bits=host["sd"])
+        moe_gpu = x.cpu().numpy().astype(np.float64)[keep] - x_l.astype(np.float64)[keep]
+        rel_max, mean_rel = assert_output_close(moe_gpu, moe_ref, what=f"int4 stack layer {l} MoE output")
+        worst = (max(worst[0], rel_max), max(worst[1], mean_rel))
+        graded += len(keep)
+        near += rep["near_tie"]
+        del stack, ml, gu, dn, w
+    print(f"48 layers teacher-forced: {graded}/{48 * T} token-layers graded, {near} near-ties; worst max err "
+          f"{worst[0]:.2e} of max|ref|, worst mean rel {worst[1]:.2e}")
+
+
 def test_stack_is_deterministic():
     T = 16
     stack = make_stack(3, T)

@@ -16,6 +16,7 @@ import oracle
 import workloads as wl
 from sparse_moe_routed_gb300 import MoELayer, MoEStack, _lib, pack_layer_experts
 from sparse_moe_routed_gb300.sweep import route_sweep
+from parity import compare_route_ids
 
 pytestmark = pytest.mark.gpu
 
@@ -67,3 +68,68 @@ def test_sweep_small_stack_properties():
     assert s["recall_native_router_on_prenorm"] >= 0.97, s
     assert 0.002 <= s["recall_linear_predictor"] <= 0.06, s
     print(s)
+
+
+def test_sweep_full_size_against_oracle():
+    """The sweep at its full size (48 layers, 512 tokens) graded layer by
+    layer against the oracle on the same bf16 representations:
+      * native routes: oracle top-10 of bf16(RMSNorm(x_l)) with the layer's router;
+      * linear predictor and native-router-on-pre-norm routes: oracle top-10
+        of bf16(x_l) with Wp_l and with the layer's router;
+    x_l is the GPU's own residual before layer l (the stack is deterministic,
+    so a layer-by-layer rerun reproduces the sweep's bits).  Control (ii) is
+    then checked exactly: RMSNorm with zero gain offset is a positive
+    per-token scale r, so the native logits equal r times the pre-norm logits
+    up to the bf16 rounding of the two inputs, D = Wr (bf16(n) - r bf16(x)),
+    computed here in float64 per token; wherever the oracle's native decision
+    gap exceeds 2 max|D| (plus 1e-3 for fp32 accumulation) both routes hold
+    the same ten experts and the recall must be exactly 1."""
+    cfg = wl.STACK48
+    L, NB = wl.STACK_LAYERS, wl.STACK_BLOCKS
+    T = NB * cfg.T
+    mls, wr_bits = [], []
+    for l in range(L):
+        w = wl.stack_layer_weights(l, DEV)
+        gu, dn = pack_layer_experts(w["w_gateup_q"], w["w_down_q"], _lib.MOE_W_INT4_G64, cfg.E, cfg.H, cfg.I,
+                                    s_gateup=w["s_gateup"], s_down=w["s_down"])
+        mls.append(MoELayer(w["w_router"], None, gu, dn, cfg.k, T, fmt=_lib.MOE_W_INT4_G64_TILED, I=cfg.I))
+        wr_bits.append(oracle.bf16_bits(w["w_router"]))
+        del w
+    stack = MoEStack(mls, T)
+    preds = [wl.predictor_weights(cfg.H, cfg.E, l, DEV) for l in range(L)]
+    x0 = torch.cat([wl.token_batch(cfg, DEV, index=b, T=cfg.T) for b in range(NB)]).float()
+    res = route_sweep(stack, x0, preds)
+    assert res["status"] == 0
+    native = res["native"].cpu().numpy()
+    pred = res["pred"].cpu().numpy()
+    early = res["early"].cpu().numpy()
+    hits_early = res["hits_early"].cpu().numpy()
+    x = x0.clone()
+    checked_exact = near = 0
+    for l in range(L):
+        x_l = x.cpu().numpy()
+        for call in stack.layer_calls(x, l):
+            MoELayer.issue(call)
+        n = oracle.rmsnorm(x_l, None, eps=1e-6)
+        n_bits = oracle.round_bf16_bits(n)
+        raw_bits = oracle.round_bf16_bits(x_l)
+        ids_n, _, gap_n, L_n = oracle.route(n_bits, wr_bits[l], None, cfg.k)
+        ids_p, _, gap_p, L_p = oracle.route(raw_bits, oracle.bf16_bits(preds[l]), None, cfg.k)
+        ids_e, _, gap_e, L_e = oracle.route(raw_bits, wr_bits[l], None, cfg.k)
+        rn = compare_route_ids(native[l], ids_n, gap_n, L_n)
+        compare_route_ids(pred[l], ids_p, gap_p, L_p)
+        compare_route_ids(early[l], ids_e, gap_e, L_e)
+        near += rn["near_tie"]
+        # control (ii), exactly where the rounding bound allows
+        x64 = x_l.astype(np.float64)
+        r = 1.0 / np.sqrt((x64 * x64).mean(axis=1) + 1e-6)
+        dn = oracle.bits_to_f32(n_bits).astype(np.float64) - r[:, None] * oracle.bits_to_f32(raw_bits)
+        D = np.abs(dn @ oracle.bits_to_f32(wr_bits[l]).astype(np.float64).T).max(axis=1)
+        sure = gap_n > 2 * D + 1e-3
+        assert np.all(hits_early[l][sure] == cfg.k), (l, np.nonzero(sure & (hits_early[l] != cfg.k)))
+        checked_exact += int(sure.sum())
+    torch.cuda.synchronize()
+    assert checked_exact >= 0.5 * L * T, checked_exact
+    assert torch.equal(x.view(torch.int32), res["x_final"].view(torch.int32))
+    print(f"sweep 48x512: native near-ties {near}; control (ii) recall exactly 1 on {checked_exact} of "
+          f"{L * T} token-layers; summary {res['summary']['recall_native_router_on_prenorm']:.4f}")

@@ -291,6 +291,94 @@ def test_int4_roundtrip_and_error_bound():
     assert np.array_equal(q2.numpy(), q.numpy())
 
 
+def _pack_int4(codes):
+    """[..., K] signed codes in [-8, 7] -> [..., K/2] bytes, even input in the
+    low nibble (test-side packing, written from the codec's statement)."""
+    c = (np.asarray(codes, np.int64) & 0xF).astype(np.uint8)
+    return np.ascontiguousarray(c[..., 0::2] | (c[..., 1::2] << 4))
+
+
+def _rand_int4_experts(rng, E, H, I, pow2_scales):
+    """Random int4 g64 expert records: codes [E,2I,H/2] / [E,H,I/2] and bf16
+    scales [E,2I,H/64] / [E,H,I/64]; with pow2_scales every scale is a power
+    of two, so each scale * code is exact in bf16."""
+    qgu = rng.integers(-8, 8, size=(E, 2 * I, H))
+    qd = rng.integers(-8, 8, size=(E, H, I))
+    if pow2_scales:
+        sgu = 2.0 ** rng.integers(-9, -4, size=(E, 2 * I, H // 64))
+        sd = 2.0 ** rng.integers(-9, -4, size=(E, H, I // 64))
+    else:
+        sgu = 0.003 * (1 + rng.random((E, 2 * I, H // 64)))
+        sd = 0.003 * (1 + rng.random((E, H, I // 64)))
+    return (qgu, _pack_int4(qgu), bf16_round_bits(sgu.astype(np.float32)),
+            qd, _pack_int4(qd), bf16_round_bits(sd.astype(np.float32)))
+
+
+def test_int4_experts_equal_bf16_experts_on_exact_dequant():
+    """int4 records whose scale * code is exact in bf16 (power-of-two scales):
+    the int4 branch of the expert combine must give the same bits as the bf16
+    branch fed the dequantised weights.  Several experts and routes, so a
+    wrong gate / up / down offset inside an int4 record shows."""
+    rng = np.random.default_rng(21)
+    E, H, I, k, n = 5, 128, 64, 3, 6
+    qgu, pgu, sgu, qd, pd, sd = _rand_int4_experts(rng, E, H, I, pow2_scales=True)
+    # dequantised weights, independently of the oracle: code * scale of its group
+    wgu_f = (qgu * np.repeat(oracle.bits_to_f32(sgu), 64, axis=-1)).astype(np.float32)
+    wd_f = (qd * np.repeat(oracle.bits_to_f32(sd), 64, axis=-1)).astype(np.float32)
+    wgu_b = bf16_round_bits(wgu_f)
+    wd_b = bf16_round_bits(wd_f)
+    assert np.array_equal(oracle.bits_to_f32(wgu_b), wgu_f)  # exact in bf16
+    assert np.array_equal(oracle.bits_to_f32(wd_b), wd_f)
+    x = rng.standard_normal((n, H)).astype(np.float32)
+    ids = np.array([rng.permutation(E)[:k] for _ in range(n)], np.int32)
+    w = rng.random((n, k)).astype(np.float32)
+    out_q = oracle.experts_combine(x, ids, w, H, I, wgu_q=pgu, sgu_bits=sgu, wd_q=pd, sd_bits=sd)
+    out_b = oracle.experts_combine(x, ids, w, H, I, wgu_bits=wgu_b, wd_bits=wd_b)
+    assert np.array_equal(out_q, out_b)
+
+
+def test_int4_experts_match_numpy_layer():
+    """General scales: the int4 expert combine against the layer written with
+    numpy matmuls over weights dequantised in numpy (code * scale per 64
+    inputs of a row), scipy's expit for the sigmoid."""
+    rng = np.random.default_rng(22)
+    E, H, I, k, n = 4, 192, 128, 2, 5
+    qgu, pgu, sgu, qd, pd, sd = _rand_int4_experts(rng, E, H, I, pow2_scales=False)
+    Wgu = qgu * np.repeat(bits_f64(sgu), 64, axis=-1)
+    Wd = qd * np.repeat(bits_f64(sd), 64, axis=-1)
+    x = rng.standard_normal((n, H)).astype(np.float32)
+    ids = np.array([rng.permutation(E)[:k] for _ in range(n)], np.int32)
+    w = rng.random((n, k)).astype(np.float32)
+    out = oracle.experts_combine(x, ids, w, H, I, wgu_q=pgu, sgu_bits=sgu, wd_q=pd, sd_bits=sd)
+    xd = x.astype(np.float64)
+    for t in range(n):
+        ref = np.zeros(H)
+        for j in range(k):
+            e = ids[t, j]
+            g = Wgu[e, :I] @ xd[t]
+            u = Wgu[e, I:] @ xd[t]
+            ref += float(w[t, j]) * (Wd[e] @ (g * scipy.special.expit(g) * u))
+        assert np.allclose(out[t], ref, rtol=1e-5, atol=1e-6 * np.abs(ref).max())
+
+
+def test_logits_f32_input_match_float64_matmul():
+    """Router logits of fp32 input rows (the stack's normalised residual):
+    float64 numpy matmul, a hand dot product, and the bf16-input entry point
+    on rows that are exactly bf16."""
+    rng = np.random.default_rng(23)
+    T, H, E = 6, 160, 40
+    x = rng.standard_normal((T, H)).astype(np.float32)  # not bf16-representable
+    wr = bf16_round_bits((0.02 * rng.standard_normal((E, H))).astype(np.float32))
+    b = rng.standard_normal(E).astype(np.float32)
+    L = oracle.router_logits(x, wr, b)
+    ref = (x.astype(np.float64) @ bits_f64(wr).T + b.astype(np.float64)).astype(np.float32)
+    assert np.max(np.abs(L.astype(np.float64) - ref)) <= 1e-6 * np.max(np.abs(ref))
+    hand = sum(float(x[2, h]) * bits_f64(wr)[7, h] for h in range(H)) + float(b[7])
+    assert abs(float(L[2, 7]) - hand) <= 1e-6 * max(1.0, abs(hand))
+    xb = bf16_round_bits(x)
+    assert np.array_equal(oracle.router_logits(oracle.bits_to_f32(xb), wr, b), oracle.router_logits(xb, wr, b))
+
+
 # --------------------------------------------------------------------------
 # Zero-centred RMSNorm
 # --------------------------------------------------------------------------
