@@ -372,9 +372,9 @@ def main():
 
     def fused_bytes(u):
         # both components of the distinct experts + token rows + h out and back
-        # + y out (+ the row gather's token reads and row writes when the
-        # launch gathers)
-        b = u * (gu_w_bytes + dn_w_bytes) + R * H * 2 + 2 * R * I * 2 + R * H * 4
+        # + y out (fp32, or bf16 rows already weighted) (+ the row gather's
+        # token reads and row writes when the launch gathers)
+        b = u * (gu_w_bytes + dn_w_bytes) + R * H * 2 + 2 * R * I * 2 + R * H * (2 if weighted else 4)
         return b + (cfg.T * H * 2 + R * H * 2 if gather_in_fused else 0)
 
     def layer_bytes(u):
@@ -386,15 +386,18 @@ def main():
     # timed region
     bound = [layers[l].bound_calls(xs[l], cfg.T, stream=st) for l in range(NL)]
     names = [c[0] for c in bound[0]]
-    fused = "moe_expert_swiglu_fused" in names
+    weighted = "moe_expert_swiglu_fused_weighted" in names
+    fused = "moe_expert_swiglu_fused" in names or weighted
     # kernels each boundary call launches in this configuration
     per_call = {"moe_route": 2, "moe_route_permute": 1, "moe_permute": 1 if R <= MoELayer.GATHER_IN_FUSED_MAX_ROWS
                 and fused else 2, "moe_permute_gather": 2, "moe_expert_swiglu_fused": 1, "moe_expert_gateup": 1,
-                "moe_expert_down": 1, "moe_combine": 1}
+                "moe_expert_down": 1, "moe_combine": 1, "moe_expert_swiglu_fused_weighted": 1,
+                "moe_combine_weighted": 1}
     launches_per_step = sum(per_call[n] for n in names)
     gather_in_fused = fused and R <= MoELayer.GATHER_IN_FUSED_MAX_ROWS
     # the dominant kernel(s): the fused contraction, or gate/up then down
-    i_main = names.index("moe_expert_swiglu_fused" if fused else "moe_expert_gateup")
+    i_main = names.index("moe_expert_swiglu_fused_weighted" if weighted else
+                         "moe_expert_swiglu_fused" if fused else "moe_expert_gateup")
     issue = MoELayer.issue
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
@@ -515,8 +518,10 @@ def main():
     wl_name = workload_name(cfg)
     U_ev = sum(U[(j * EV_EVERY) % NL] for j in range(KE)) / KE
     traffic = recorded_traffic("fused" if fused else "gateup", wl_name, U_ev)
-    main_kernel = ("grouped_swiglu_fused_kernel (moe_expert_swiglu_fused: " +
-                   ("row gather, " if gather_in_fused else "") + "gate/up + SwiGLU, down)"
+    main_kernel = ("grouped_swiglu_fused_kernel (" +
+                   ("moe_expert_swiglu_fused_weighted: " if weighted else "moe_expert_swiglu_fused: ") +
+                   ("row gather, " if gather_in_fused else "") + "gate/up + SwiGLU, down" +
+                   (", route-weighted bf16 outputs)" if weighted else ")")
                    if fused else "grouped_gemm_kernel (moe_expert_gateup)")
     roof_hbm = {"bound": "hbm", "kernel": main_kernel,
                 "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",

@@ -254,6 +254,27 @@ MOE_API moe_status moe_expert_swiglu_fused(const uint16_t *x, int k, const int32
                                            int32_t *sync_ws, int32_t *dev_status, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_expert_swiglu_fused_weighted -- moe_expert_swiglu_fused whose down
+ * epilogue also applies the route weight and stores bf16: for every slot s,
+ *   yw_perm[s,:] = bf16( topk_w[perm[s]] * (W_down h[s]) )     [R,H] bf16
+ * in place of the fp32 y_perm.  For prefill-sized calls this halves the bytes
+ * of the expert outputs, written here and read again by the combine
+ * (moe_combine_weighted), at the cost of one bf16 rounding per route term.
+ * Source: AFN-019, section "Hypothesis H4" (results of ready experts go to
+ * separate slots; the weighted sum follows route-rank order).
+ *   perm    [R] int32 from moe_permute (required), k the routes per token,
+ *           R % k == 0;  topk_w [T*k] f32, the route weights of moe_route.
+ * A perm entry outside [0,R) sets MOE_DEV_BAD_EXPERT and leaves that slot's
+ * row unwritten.  Everything else (x, x_perm, h, sync_ws, the persistent
+ * launch) is as moe_expert_swiglu_fused.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_expert_swiglu_fused_weighted(const uint16_t *x, int k, const int32_t *perm,
+                                                    uint16_t *x_perm, const int32_t *offsets, int R, int E, int H,
+                                                    int I, int fmt, const void *w_gateup, const void *w_down,
+                                                    const float *topk_w, uint16_t *h, uint16_t *yw_perm,
+                                                    int32_t *sync_ws, int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Expert records in host memory, served through an HBM slot cache.
  *
  * Source: AFN-019 "Hide SSD misses before the router knows they exist",
@@ -431,6 +452,19 @@ MOE_API moe_status moe_pack_experts(int fmt_in, const void *w, const uint16_t *s
 MOE_API moe_status moe_combine(const float *y_perm, const int32_t *inv_perm, const float *topk_w, int T,
                        int k, int H, const float *residual, uint16_t *out_bf16, float *out_f32,
                        int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_combine_weighted -- moe_combine over expert outputs that already carry
+ * their route weights (yw_perm [T*k,H] bf16 from
+ * moe_expert_swiglu_fused_weighted).  Source as moe_combine.
+ *
+ *   acc[t,:] = sum_{j=0}^{k-1} float(yw_perm[inv_perm[t*k+j], :])
+ *              (fp32, accumulated in j order)
+ *   out_f32 / out_bf16 / residual / dev_status as in moe_combine.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_combine_weighted(const uint16_t *yw_perm, const int32_t *inv_perm, int T, int k, int H,
+                                        const float *residual, uint16_t *out_bf16, float *out_f32,
+                                        int32_t *dev_status, void *stream);
 
 /* ---------------------------------------------------------------------------
  * route_block_dedup -- unique experts per (layer, verifier block) and the

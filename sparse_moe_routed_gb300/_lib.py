@@ -62,6 +62,8 @@ def load(path: str | None = None):
             "moe_expert_down": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
             "moe_grouped_swiglu": ([p, p, i, i, i, i, i, p, p, p, p, p, p, p, p], i),
             "moe_expert_swiglu_fused": ([p, i, p, p, p, i, i, i, i, i, p, p, p, p, p, p, p], i),
+            "moe_expert_swiglu_fused_weighted": ([p, i, p, p, p, i, i, i, i, i, p, p, p, p, p, p, p, p], i),
+            "moe_combine_weighted": ([p, p, i, i, i, p, p, p, p, p], i),
             "moe_route_permute": ([p, p, p, i, i, i, i, p, p, p, p, p, p, p, p, p], i),
             "moe_combine": ([p, p, p, i, i, i, p, p, p, p, p], i),
             "route_block_dedup": ([p, i, i, i, i, i, i, i, p, p, p, p, p, p], i),
@@ -181,6 +183,17 @@ def moe_expert_swiglu_fused(x_perm, offsets, E, H, I, w_gateup, w_down, h, y_per
     _check("moe_expert_swiglu_fused", st)
 
 
+def moe_expert_swiglu_fused_weighted(x_perm, offsets, E, H, I, w_gateup, w_down, topk_w, h, yw_perm, sync_ws,
+                                     dev_status, perm, k, fmt=MOE_W_BF16_TILED, x=None, stream=None):
+    """moe_expert_swiglu_fused whose down epilogue stores bf16 rows already
+    multiplied by their route weights (yw_perm [R, H] bf16)."""
+    R = x_perm.shape[0]
+    st = load().moe_expert_swiglu_fused_weighted(_ptr(x), k, _ptr(perm), _ptr(x_perm), _ptr(offsets), R, E, H, I,
+                                                 fmt, _ptr(w_gateup), _ptr(w_down), _ptr(topk_w), _ptr(h),
+                                                 _ptr(yw_perm), _ptr(sync_ws), _ptr(dev_status), _stream(stream))
+    _check("moe_expert_swiglu_fused_weighted", st)
+
+
 def moe_cache_plan(counts, slot_of, expert_of, hand, miss_list, miss_slot, stats, dev_status,
                    policy=MOE_CACHE_FIFO, decay=0.9, score=None, last_use=None, stream=None):
     E, S = counts.shape[0], expert_of.shape[0]
@@ -264,6 +277,13 @@ def moe_combine(y_perm, inv_perm, topk_w, residual, out_bf16, out_f32, dev_statu
     st = load().moe_combine(_ptr(y_perm), _ptr(inv_perm), _ptr(topk_w), T, k, H, _ptr(residual), _ptr(out_bf16),
                             _ptr(out_f32), _ptr(dev_status), _stream(stream))
     _check("moe_combine", st)
+
+
+def moe_combine_weighted(yw_perm, inv_perm, T, k, residual, out_bf16, out_f32, dev_status, stream=None):
+    H = yw_perm.shape[1]
+    st = load().moe_combine_weighted(_ptr(yw_perm), _ptr(inv_perm), T, k, H, _ptr(residual), _ptr(out_bf16),
+                                     _ptr(out_f32), _ptr(dev_status), _stream(stream))
+    _check("moe_combine_weighted", st)
 
 
 def route_block_dedup(ids, E, block, H, I, mask, U, bytes2, bytes4, dev_status, stream=None):

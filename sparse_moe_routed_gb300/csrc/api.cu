@@ -68,7 +68,7 @@ inline moe_status check_geometry(int H, int E, int k, int I_or_zero) {
 
 extern "C" {
 
-int moe_abi_version(void) { return 100; }
+int moe_abi_version(void) { return 101; }
 
 const char* moe_status_str(moe_status s) {
   switch (s) {
@@ -257,7 +257,26 @@ moe_status moe_expert_swiglu_fused(const uint16_t* x, int k, const int32_t* perm
   if (c != MOE_OK) return c;
   if (R == 0) return MOE_OK;
   return cuda_status(moe::launch_swiglu_fused(x, k, perm, x_perm, offsets, E, R, H, I, w_gateup, w_down, nullptr, h,
-                                              y_perm, sync_ws, dev_status, static_cast<cudaStream_t>(stream)));
+                                              y_perm, nullptr, nullptr, sync_ws, dev_status,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_swiglu_fused_weighted(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
+                                            const int32_t* offsets, int R, int E, int H, int I, int fmt,
+                                            const void* w_gateup, const void* w_down, const float* topk_w,
+                                            uint16_t* h, uint16_t* yw_perm, int32_t* sync_ws, int32_t* dev_status,
+                                            void* stream) {
+  // yw_perm stands in for y_perm in the shared checks (same alignment rule)
+  const moe_status c = check_fused(x, k, perm, x_perm, offsets, R, E, H, I, fmt, w_gateup, w_down, h,
+                                   reinterpret_cast<float*>(yw_perm), sync_ws, dev_status);
+  if (c != MOE_OK) return c;
+  if (k <= 0 || R % k != 0) return MOE_ESHAPE;
+  if (k > moe::kMaxK) return MOE_ENOTSUP;
+  if (!perm || !topk_w || !a4(perm) || !a4(topk_w)) return MOE_EINVAL;
+  if (R == 0) return MOE_OK;
+  return cuda_status(moe::launch_swiglu_fused(x, k, perm, x_perm, offsets, E, R, H, I, w_gateup, w_down, nullptr, h,
+                                              nullptr, topk_w, yw_perm, sync_ws, dev_status,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_expert_swiglu_cached(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
@@ -292,7 +311,8 @@ moe_status moe_expert_swiglu_cached(const uint16_t* x, int k, const int32_t* per
     fc.wave = wave;
   }
   return cuda_status(moe::launch_swiglu_fused(x, k, perm, x_perm, offsets, E, R, H, I, pool_gateup, pool_down, &fc,
-                                              h, y_perm, sync_ws, dev_status, static_cast<cudaStream_t>(stream)));
+                                              h, y_perm, nullptr, nullptr, sync_ws, dev_status,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_cache_plan(const int32_t* counts, int E, int32_t* slot_of, int32_t* expert_of, int S, int32_t* hand,
@@ -421,6 +441,22 @@ moe_status moe_combine(const float* y_perm, const int32_t* inv_perm, const float
   if (T == 0) return MOE_OK;
   return cuda_status(moe::launch_combine(y_perm, inv_perm, topk_w, T, k, H, T * k, residual, out_bf16, out_f32,
                                          dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine_weighted(const uint16_t* yw_perm, const int32_t* inv_perm, int T, int k, int H,
+                                const float* residual, uint16_t* out_bf16, float* out_f32, int32_t* dev_status,
+                                void* stream) {
+  if (T < 0 || k <= 0 || H <= 0) return MOE_ESHAPE;
+  if (k > moe::kMaxK || H % 128 != 0 || H > 16384) return MOE_ENOTSUP;
+  if (static_cast<long long>(T) * k >= (1LL << 31)) return MOE_ENOTSUP;
+  if (!yw_perm || !inv_perm || (!out_bf16 && !out_f32)) return MOE_EINVAL;
+  if (!a16(yw_perm) || !a4(inv_perm)) return MOE_EINVAL;
+  if ((residual && !a16(residual)) || (out_bf16 && !a16(out_bf16)) || (out_f32 && !a16(out_f32)) ||
+      (dev_status && !a4(dev_status)))
+    return MOE_EINVAL;
+  if (T == 0) return MOE_OK;
+  return cuda_status(moe::launch_combine_weighted(yw_perm, inv_perm, T, k, H, T * k, residual, out_bf16, out_f32,
+                                                  dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status route_block_dedup(const int32_t* ids, int L, int T_tot, int k, int E, int block, int H, int I,

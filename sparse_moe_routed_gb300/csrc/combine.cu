@@ -82,6 +82,58 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
 }
 
+// The same sum over expert outputs that the down epilogue already multiplied
+// by their route weights and stored in bf16 (yw [R, H]): acc = sum_j
+// yw[inv[t*k + j]] in j order, fp32.  Four columns per thread (one 8-byte
+// load per row), 512 columns per CTA.
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_weighted_kernel(const uint16_t* __restrict__ yw, const int32_t* __restrict__ inv, int T, int k, int H,
+                            int R, const float* residual, uint16_t* __restrict__ out_bf16, float* out_f32,
+                            int32_t* status) {
+  __shared__ int slot[kMaxK];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.y;
+  if (threadIdx.x < k) {
+    int s = inv[static_cast<size_t>(t) * k + threadIdx.x];
+    if (s < 0 || s >= R) s = -1;
+    slot[threadIdx.x] = s;
+  }
+  __syncthreads();
+  const int c4 = blockIdx.x * kCombineThreads + threadIdx.x;
+  if (c4 * 4 >= H) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  bool bad = false;
+  for (int j = 0; j < k; ++j) {
+    const int s = slot[j];
+    if (s < 0) {
+      bad = true;
+      continue;
+    }
+    const uint2 v = reinterpret_cast<const uint2*>(yw + static_cast<size_t>(s) * H)[c4];
+    acc.x += bf16_to_f32(static_cast<uint16_t>(v.x & 0xffffu));
+    acc.y += bf16_to_f32(static_cast<uint16_t>(v.x >> 16));
+    acc.z += bf16_to_f32(static_cast<uint16_t>(v.y & 0xffffu));
+    acc.w += bf16_to_f32(static_cast<uint16_t>(v.y >> 16));
+  }
+  if (residual) {
+    const float4 r = reinterpret_cast<const float4*>(residual + static_cast<size_t>(t) * H)[c4];
+    acc.x += r.x;
+    acc.y += r.y;
+    acc.z += r.z;
+    acc.w += r.w;
+  }
+  if (status && (bad || !isfinite(acc.x) || !isfinite(acc.y) || !isfinite(acc.z) || !isfinite(acc.w)))
+    set_status(status, bad ? MOE_DEV_BAD_EXPERT : MOE_DEV_NONFINITE);
+  if (out_f32) reinterpret_cast<float4*>(out_f32 + static_cast<size_t>(t) * H)[c4] = acc;
+  if (out_bf16) {
+    uint2 pk;
+    pk.x = static_cast<uint32_t>(f32_to_bf16(acc.x)) | (static_cast<uint32_t>(f32_to_bf16(acc.y)) << 16);
+    pk.y = static_cast<uint32_t>(f32_to_bf16(acc.z)) | (static_cast<uint32_t>(f32_to_bf16(acc.w)) << 16);
+    reinterpret_cast<uint2*>(out_bf16 + static_cast<size_t>(t) * H)[c4] = pk;
+  }
+}
+
 constexpr int kNormThreads = 256;
 
 __global__ void __launch_bounds__(kNormThreads)
@@ -158,6 +210,14 @@ cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, i
   const dim3 grid((H / 4 + kCombineThreads - 1) / kCombineThreads, T);
   return launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, st, y, inv, w, T, k, H, R, residual, out_bf16,
                     out_f32, st_word);
+}
+
+cudaError_t launch_combine_weighted(const uint16_t* yw, const int32_t* inv, int T, int k, int H, int R,
+                                    const float* residual, uint16_t* out_bf16, float* out_f32, int32_t* st_word,
+                                    cudaStream_t st) {
+  const dim3 grid((H / 4 + kCombineThreads - 1) / kCombineThreads, T);
+  return launch_pdl(combine_weighted_kernel, grid, dim3(kCombineThreads), 0, st, yw, inv, T, k, H, R, residual,
+                    out_bf16, out_f32, st_word);
 }
 
 cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, int T, int H, uint16_t* out,

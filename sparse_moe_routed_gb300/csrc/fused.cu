@@ -37,7 +37,12 @@ struct FusedArgs {
   int ks_gu, ks_dn;         // K steps per tile: H/64, I/64
   int mb_gu, mb_dn;         // weight blocks per expert: I/64, H/128
   uint16_t* h;              // [R, I]
-  float* y;                 // [R, H]
+  float* y;                 // [R, H] fp32 expert outputs, or (yw != nullptr) unused
+  // Weighted outputs (yw != nullptr): the down epilogue multiplies slot s's
+  // row by its route weight topk_w[perm[s]] and stores it rounded to bf16 in
+  // yw [R, H], which halves the bytes written here and read by the combine.
+  const float* topk_w;
+  uint16_t* yw;
   int I, H;
   int* ready;               // sync words: [E] per-expert h readiness, then the exit and gather counters
                             // and the tile queue
@@ -77,6 +82,9 @@ struct FusedArgs {
 constexpr int kFetchWarps = 4;
 constexpr int kFusedDynamicRows = 4096;  // launches up to this many rows claim tiles dynamically
 constexpr int kFetchChunk = 32768;
+// launches of at least this many routes per expert (on average) take
+// 256-row token tiles
+constexpr int kFusedWideRowsPerExpert = 256;
 
 // The n-th piece of the fetch plan in wave order (wave width W experts, cg /
 // cd pieces per gate/up / down record): the gate/up records of wave 0, then
@@ -762,6 +770,27 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       }
       if (t < 0) break;
       const FTile tl = tile_of(t);
+      // weighted outputs: the route weight of every column of a down tile,
+      // loaded before the wait for its accumulator so that the two dependent
+      // loads overlap the tile's MMAs (lane l holds columns l, l + 32, ...)
+      constexpr int kWCols = (NMAX + 31) / 32;
+      float wcol[kWCols];
+      if (tl.kind == 1 && p.yw != nullptr) {
+#pragma unroll
+        for (int i = 0; i < kWCols; ++i) {
+          const int c = i * 32 + lane;
+          float wv = 0.f;
+          if (c < tl.nrows) {
+            const int r = p.perm[tl.row0 + c];
+            if (r >= 0 && r < p.R) {
+              wv = p.topk_w[r];
+            } else {
+              set_status(p.status, MOE_DEV_BAD_EXPERT);
+            }
+          }
+          wcol[i] = wv;
+        }
+      }
       const bool ok = wait_bounded<kSleepEpi>(accf0 + 8 * acc, aph, misc + 1, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
@@ -793,7 +822,7 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
         __threadfence();
         __syncwarp();
         if (lane == 0) atomicAdd(p.ready + tl.e, 1);
-      } else {
+      } else if (p.yw == nullptr) {
         const int j = tl.mb * kBM + row_in_tile;
         for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
           float v[16];
@@ -802,6 +831,23 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
           for (int jj = 0; jj < 16; ++jj) {
             const int col = c0 + jj;
             if (col < tl.nrows) p.y[static_cast<size_t>(tl.row0 + col) * p.H + j] = v[jj];
+          }
+        }
+      } else {
+        // weighted bf16 rows (NMAX / 16 column groups, unrolled so that the
+        // weights stay in registers)
+        const int j = tl.mb * kBM + row_in_tile;
+#pragma unroll
+        for (int c0 = 0; c0 < NMAX; c0 += 16) {
+          if (c0 < tl.nrows) {
+            float v[16];
+            ptx::tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int col = c0 + jj;
+              const float wj = __shfl_sync(0xffffffffu, wcol[c0 >> 5], (c0 & 16) + jj);
+              if (col < tl.nrows) p.yw[static_cast<size_t>(tl.row0 + col) * p.H + j] = f32_to_bf16(v[jj] * wj);
+            }
           }
         }
       }
@@ -857,8 +903,9 @@ cudaError_t run_fused(const CUtensorMap& mx, const CUtensorMap& mh, const FusedA
 
 cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
                                 const int32_t* offsets, int E, int R, int H, int I, const void* w_gateup,
-                                const void* w_down, const FusedCache* cache, uint16_t* h, float* y, int32_t* ready,
-                                int32_t* st_word, cudaStream_t st) {
+                                const void* w_down, const FusedCache* cache, uint16_t* h, float* y,
+                                const float* topk_w, uint16_t* yw, int32_t* ready, int32_t* st_word,
+                                cudaStream_t st) {
   CUtensorMap mx, mh;
   if (!make_rows_map(&mx, x_perm, H, R, kBoxRows)) return cudaErrorInvalidValue;
   if (!make_rows_map(&mh, h, I, R, kBoxRows)) return cudaErrorInvalidValue;
@@ -874,6 +921,8 @@ cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, u
   a.mb_dn = H / kBM;
   a.h = h;
   a.y = y;
+  a.topk_w = topk_w;
+  a.yw = yw;
   a.I = I;
   a.H = H;
   a.ready = ready;
@@ -908,6 +957,13 @@ cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, u
       default: return run_fused<128, 2, true>(mx, mh, a, st);
     }
   }
+  // Compute-bound launches (hundreds of token rows per expert): 256-row
+  // token tiles (MMA N = 256, both accumulators filling the 512 TMEM
+  // columns), which halve how often an expert's weights are streamed and
+  // take 48 KB of operands per 128 x 256 x 64 step instead of 32 KB per
+  // 128 x 128 x 64; one K step per stage keeps four stages in 196 KB.
+  if (static_cast<long long>(R) >= static_cast<long long>(kFusedWideRowsPerExpert) * E)
+    return run_fused<256, 1, false>(mx, mh, a, st);
   if (a.ks_gu % 2 == 0 && a.ks_dn % 2 == 0) {
     switch (pick_nmax(R)) {
       case 16: return run_fused<16, 2, false>(mx, mh, a, st);

@@ -119,13 +119,17 @@ struct FusedCache {
 };
 cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, uint16_t* x_perm,
                                 const int32_t* offsets, int E, int R, int H, int I, const void* w_gateup,
-                                const void* w_down, const FusedCache* cache, uint16_t* h, float* y, int32_t* ready,
-                                int32_t* st_word, cudaStream_t st);
+                                const void* w_down, const FusedCache* cache, uint16_t* h, float* y,
+                                const float* topk_w, uint16_t* yw, int32_t* ready, int32_t* st_word,
+                                cudaStream_t st);
 
 // combine.cu
 cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int k, int H,
                            int R, const float* residual, uint16_t* out_bf16, float* out_f32,
                            int32_t* st_word, cudaStream_t st);
+cudaError_t launch_combine_weighted(const uint16_t* yw, const int32_t* inv, int T, int k, int H, int R,
+                                    const float* residual, uint16_t* out_bf16, float* out_f32, int32_t* st_word,
+                                    cudaStream_t st);
 cudaError_t launch_rmsnorm(const float* x, const float* gamma, float eps, int T, int H,
                            uint16_t* out, uint16_t* raw, cudaStream_t st);
 cudaError_t launch_recall(const int32_t* pred, const int32_t* ref, int T, int k, int32_t* hits,

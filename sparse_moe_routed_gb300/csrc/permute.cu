@@ -6,14 +6,20 @@
 // flat route order r = t*k + j, which makes the grouping deterministic and
 // comparable bit for bit.
 //
-// One CTA of up to 32 route-owning warps.  Warp w owns a contiguous run of routes.  Pass 1: each
-// warp counts its routes per expert with __match_any_sync (one shared-memory
-// add per distinct expert per 32 routes, no atomics).  Pass 2: per expert, an
-// exclusive prefix over the 32 warps, then one exclusive scan over experts
-// gives the segment offsets.  Pass 3: each warp replays its run and places
-// every route at offsets[e] + (routes of e in earlier warps) + (earlier routes
-// of e in this warp), which is the stable order.  Integer work only, a few
-// microseconds even at 40,960 routes, so one CTA is enough.
+// One CTA of up to 32 route-owning warps.  Warp w owns a contiguous run of
+// routes.  Pass 1: each warp counts its routes per expert in its own table
+// (shared-memory atomic adds: order does not matter for a count).  Pass 2:
+// per expert, an exclusive prefix over the warps, then one exclusive scan
+// over experts gives the segment offsets.  Pass 3: each warp replays its run
+// 32 routes at a time and places every route at offsets[e] + (routes of e in
+// earlier warps) + (earlier routes of e in this warp), which is the stable
+// order; within a 32-route batch the lanes holding the same expert find one
+// another through a per-warp table of lane masks (each lane ORs its bit into
+// the word of its expert, reads the word back, and the lowest lane clears
+// it), which costs a few instructions whatever the number of distinct
+// experts in the batch.  Each warp loads kUnroll batches of its run before
+// it processes them, so a pass waits for global-load latency once per
+// kUnroll batches.  Integer work only.
 #include <algorithm>
 
 #include "common.cuh"
@@ -24,23 +30,34 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = 32;
+constexpr int kUnroll = 8;                // 32-route batches loaded ahead per warp
+constexpr int kPermuteSmem = 200 * 1024;  // per-warp count and mask tables
+
+// Route-owning warps: one per 32 routes up to 32, fewer when E is so large
+// that two [W][E] tables would not fit in shared memory.
+int permute_warps(int R, int E) {
+  const int w_rows = std::max(1, (R + 31) / 32);
+  const int w_smem = std::max(1, (kPermuteSmem / (4 * E) - 1) / 2);
+  return std::min(kWarps, std::min(w_rows, w_smem));
+}
 
 __global__ void __launch_bounds__(kWarps * 32, 1)
-    permute_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ counts,
+    permute_kernel(const int32_t* __restrict__ ids, int R, int E, int W, int32_t* __restrict__ counts,
                    int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                    int32_t* status) {
   extern __shared__ int32_t sh[];
-  // Only as many warps own routes as there are 32-route steps (a decode
-  // block of 160 routes uses 5), which keeps the per-warp tables small.
-  const int W = min(kWarps, max(1, (R + 31) / 32));
-  int32_t* hist = sh;          // [W][E]
-  int32_t* base = sh + W * E;  // [E]
+  int32_t* hist = sh;                                            // [W][E]
+  int32_t* base = sh + W * E;                                    // [E]
+  unsigned* lmask = reinterpret_cast<unsigned*>(base + E);       // [W][E]
   __shared__ int bad;
   __shared__ int warp_tot[kWarps];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  for (int i = tid; i < W * E; i += blockDim.x) hist[i] = 0;
+  for (int i = tid; i < W * E; i += blockDim.x) {
+    hist[i] = 0;
+    lmask[i] = 0u;
+  }
   if (tid == 0) bad = 0;
   pdl_wait();
   pdl_trigger();
@@ -50,21 +67,27 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const int r0 = (warp < W) ? min(R, warp * per) : R;
   const int r1 = (warp < W) ? min(R, r0 + per) : R;
   int32_t* my_hist = hist + min(warp, W - 1) * E;
+  unsigned* my_mask = lmask + min(warp, W - 1) * E;
 
   // pass 1: per-warp histogram
-  for (int b = r0; b < r1; b += 32) {
-    const int r = b + lane;
-    const bool act = r < r1;
-    int e = act ? ids[r] : -1;
-    if (act && (e < 0 || e >= E)) {
-      bad = 1;
-      e = -1;
+  for (int b = r0; b < r1; b += 32 * kUnroll) {
+    int ev[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int r = b + u * 32 + lane;
+      ev[u] = r < r1 ? ids[r] : 0;
     }
-    // inactive or invalid lanes get a key no valid route can share
-    const int key = (act && e >= 0) ? e : -(lane + 2);
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    if (key >= 0 && lane == __ffs(peers) - 1) my_hist[key] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (b + u * 32 + lane < r1) {
+        const int e = ev[u];
+        if (e < 0 || e >= E) {
+          bad = 1;
+        } else {
+          atomicAdd(&my_hist[e], 1);
+        }
+      }
+    }
   }
   __syncthreads();
   if (bad) {
@@ -113,22 +136,36 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   if (tid == 0) offsets[E] = R;
   __syncthreads();
 
-  // pass 3: stable scatter
-  for (int b = r0; b < r1; b += 32) {
-    const int r = b + lane;
-    const bool act = r < r1;
-    const int key = act ? ids[r] : -(lane + 2);
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    int slot = 0;
-    if (act) {
-      const unsigned lower = peers & ((1u << lane) - 1u);
-      slot = base[key] + my_hist[key] + __popc(lower);
-      perm[slot] = r;
-      inv[r] = slot;
+  // pass 3: stable scatter (every ID is valid here)
+  for (int b = r0; b < r1; b += 32 * kUnroll) {
+    int ev[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int r = b + u * 32 + lane;
+      ev[u] = r < r1 ? ids[r] : 0;
     }
-    __syncwarp();
-    if (act && lane == __ffs(peers) - 1) my_hist[key] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int r = b + u * 32 + lane;
+      const bool act = r < r1;
+      const int key = ev[u];
+      if (act) atomicOr(&my_mask[key], 1u << lane);
+      __syncwarp();
+      // lanes of this batch routed to the same expert as this lane
+      const unsigned peers = act ? my_mask[key] : 0u;
+      if (act) {
+        const unsigned lower = peers & ((1u << lane) - 1u);
+        const int slot = base[key] + my_hist[key] + __popc(lower);
+        perm[slot] = r;
+        inv[r] = slot;
+      }
+      __syncwarp();
+      if (act && lane == __ffs(peers) - 1) {
+        my_hist[key] += __popc(peers);
+        my_mask[key] = 0u;
+      }
+      __syncwarp();
+    }
   }
 }
 
@@ -155,11 +192,11 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t
 cudaError_t launch_permute(const int32_t* ids, int R, int k, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
                            int32_t* inv, int32_t* st_word, cudaStream_t st) {
   (void)k;
-  const int W = std::min(kWarps, std::max(1, (R + 31) / 32));
-  const size_t smem = static_cast<size_t>(W + 1) * E * sizeof(int32_t);
-  cudaError_t e = ensure_smem(permute_kernel, static_cast<int>((kWarps + 1) * kMaxE * sizeof(int32_t)));
+  const int W = permute_warps(R, E);
+  const size_t smem = static_cast<size_t>(2 * W + 1) * E * sizeof(int32_t);
+  cudaError_t e = ensure_smem(permute_kernel, kPermuteSmem + 4 * kMaxE);
   if (e != cudaSuccess) return e;
-  return launch_pdl(permute_kernel, dim3(1), dim3(kWarps * 32), smem, st, ids, R, E, counts, offsets, perm, inv,
+  return launch_pdl(permute_kernel, dim3(1), dim3(kWarps * 32), smem, st, ids, R, E, W, counts, offsets, perm, inv,
                     st_word);
 }
 

@@ -41,6 +41,11 @@ class MoELayer:
 
     GATHER_IN_FUSED_MAX_ROWS = 4096
     ROUTE_PERMUTE_ONE_LAUNCH = False
+    # fused launches of more routes than this store the expert outputs as
+    # bf16 rows already multiplied by their route weights (half the bytes of
+    # fp32 rows, written once and read once by the combine)
+    WEIGHTED_Y_MIN_ROWS = 4097
+    WEIGHTED_Y = True
 
     def __init__(self, w_router, bias, w_gateup, w_down, k: int, T_max: int, fmt: int = _lib.MOE_W_BF16,
                  I: int = None):
@@ -75,6 +80,8 @@ class MoELayer:
         self.x_perm = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
         self.h = torch.empty((R, I), dtype=torch.bfloat16, device=dev)
         self.y_perm = torch.empty((R, H), dtype=torch.float32, device=dev)
+        # the weighted bf16 rows share y_perm's storage (its first R*H*2 bytes)
+        self.yw_perm = self.y_perm.view(-1).view(torch.bfloat16)[:R * H].view(R, H)
         self.out = torch.empty((T_max, H), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.fused = (fmt == _lib.MOE_W_BF16_TILED)
@@ -136,7 +143,13 @@ class MoELayer:
             calls.append(("moe_permute_gather", lib.moe_permute,
                           (P(self.ids), T, k, E, P(x), H, P(self.counts), P(self.offsets), P(self.perm),
                            P(self.inv), P(self.x_perm), P(self.status), st)))
-        if self.fused:
+        weighted = self.fused and self.WEIGHTED_Y and R >= self.WEIGHTED_Y_MIN_ROWS
+        if weighted:
+            calls.append(("moe_expert_swiglu_fused_weighted", lib.moe_expert_swiglu_fused_weighted,
+                          (P(x if gather_in_fused else None), k, P(self.perm), P(self.x_perm), P(self.offsets), R,
+                           E, H, I, self.fmt, P(self.w_gateup), P(self.w_down), P(self.w), P(self.h),
+                           P(self.yw_perm), P(self.sync_ws), P(self.status), st)))
+        elif self.fused:
             calls += self._expert_calls(lib, P, x if gather_in_fused else None, R, st)
         else:
             calls += [
@@ -147,10 +160,14 @@ class MoELayer:
                  (P(self.h), P(self.offsets), R, E, H, I, self.fmt, P(self.w_down), None, P(self.y_perm),
                   P(self.status), st)),
             ]
-        calls += [
-            ("moe_combine", lib.moe_combine,
-             (P(self.y_perm), P(self.inv), P(self.w), T, k, H, P(residual), P(out), P(out_f32), P(self.status), st)),
-        ]
+        if weighted:
+            calls.append(("moe_combine_weighted", lib.moe_combine_weighted,
+                          (P(self.yw_perm), P(self.inv), T, k, H, P(residual), P(out), P(out_f32), P(self.status),
+                           st)))
+        else:
+            calls.append(("moe_combine", lib.moe_combine,
+                          (P(self.y_perm), P(self.inv), P(self.w), T, k, H, P(residual), P(out), P(out_f32),
+                           P(self.status), st)))
         self._bound[key] = calls
         return calls
 
@@ -279,6 +296,8 @@ class CachedMoELayer(MoELayer):
     running totals.  policy: "fifo", "lru" or "score" (moe_cache_plan), decay
     the score policy's use-rate factor.
     """
+
+    WEIGHTED_Y = False  # the cached launches keep fp32 expert outputs
 
     POLICIES = {"fifo": _lib.MOE_CACHE_FIFO, "lru": _lib.MOE_CACHE_LRU, "score": _lib.MOE_CACHE_SCORE}
 

@@ -26,10 +26,10 @@ def lib():
 def test_library_loads_and_exports_every_declared_symbol():
     L = lib()
     names = _lib.declared_functions()
-    assert len(names) == 25
+    assert len(names) == 27
     for n in names:
         assert hasattr(L, n), n
-    assert L.moe_abi_version() == 100
+    assert L.moe_abi_version() == 101
     assert L.moe_status_str(0).decode() == "MOE_OK"
     assert L.moe_status_str(5).decode().startswith("MOE_ENOTSUP")
 
@@ -223,6 +223,42 @@ def test_swiglu_fused_rejections():
     assert call(x=PM, k=10, perm=P) == _lib.MOE_EINVAL
     assert call(R=0) == _lib.MOE_OK
     assert call(R=0, x=P, k=10, perm=P) == _lib.MOE_OK
+
+
+def test_swiglu_fused_weighted_rejections():
+    L = lib()
+    # x, k, perm, x_perm, offsets, R, E, H, I, fmt, w_gateup, w_down, topk_w, h, yw_perm, sync_ws, dev_status,
+    # stream
+    base = [NUL, 10, P, P, P, 40960, 512, 2560, 640, _lib.MOE_W_BF16_TILED, P, P, P, P, P, P, P, NUL]
+    names = ["x", "k", "perm", "xp", "off", "R", "E", "H", "I", "fmt", "wgu", "wd", "w", "h", "yw", "sync", "st"]
+
+    def call(**kw):
+        a = list(base)
+        for n, v in kw.items():
+            a[names.index(n)] = v
+        return L.moe_expert_swiglu_fused_weighted(*a)
+
+    assert call(perm=NUL) == _lib.MOE_EINVAL       # the route of each slot is needed for its weight
+    assert call(w=NUL) == _lib.MOE_EINVAL
+    assert call(w=PM) == _lib.MOE_EINVAL
+    assert call(yw=PM) == _lib.MOE_EINVAL
+    assert call(k=0) == _lib.MOE_ESHAPE
+    assert call(k=7) == _lib.MOE_ESHAPE            # 40960 % 7 != 0
+    assert call(k=40) == _lib.MOE_ENOTSUP
+    assert call(fmt=_lib.MOE_W_BF16) == _lib.MOE_ENOTSUP
+    assert call(sync=NUL) == _lib.MOE_EWORKSPACE
+    assert call(R=0) == _lib.MOE_OK
+
+
+def test_combine_weighted_rejections():
+    L = lib()
+    assert L.moe_combine_weighted(P, P, 16, 10, 2560, NUL, NUL, NUL, NUL, NUL) == _lib.MOE_EINVAL
+    assert L.moe_combine_weighted(PM, P, 16, 10, 2560, NUL, P, NUL, NUL, NUL) == _lib.MOE_EINVAL
+    assert L.moe_combine_weighted(NUL, P, 16, 10, 2560, NUL, P, NUL, NUL, NUL) == _lib.MOE_EINVAL
+    assert L.moe_combine_weighted(P, P, 16, 40, 2560, NUL, P, NUL, NUL, NUL) == _lib.MOE_ENOTSUP
+    assert L.moe_combine_weighted(P, P, 16, 10, 2500, NUL, P, NUL, NUL, NUL) == _lib.MOE_ENOTSUP
+    assert L.moe_combine_weighted(P, P, -1, 10, 2560, NUL, P, NUL, NUL, NUL) == _lib.MOE_ESHAPE
+    assert L.moe_combine_weighted(P, P, 0, 10, 2560, NUL, P, NUL, NUL, NUL) == _lib.MOE_OK
 
 
 def test_route_permute_rejections():

@@ -100,3 +100,60 @@ def test_gather_skips_out_of_range_perm_entry():
         else:
             assert same(xp[s], x[perm[s] // cfg.k])
     assert int(sync.abs().sum().item()) == 0
+
+
+@pytest.mark.parametrize("name,T,gather", [("decode", 16, True), ("decode", 410, False), ("prefill", 4096, False),
+                                           ("tiny", 16, False), ("prefill", 13108, False)])
+def test_weighted_outputs_are_the_rounded_weighted_rows(name, T, gather):
+    """moe_expert_swiglu_fused_weighted stores, per slot, bf16 of (its fp32
+    row times its route weight): bit for bit what the unweighted launch's fp32
+    rows give when multiplied by the same weight in fp32 and rounded to
+    nearest-even bf16 (torch), with h identical."""
+    cfg = wl.with_tokens(wl.CONFIGS[name], T) if name != "tiny" else wl.TINY
+    if name == "prefill":
+        d = wl.layer_inputs(wl.with_tokens(cfg, 16), DEV, with_x=False)
+        gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, cfg.E, cfg.H, cfg.I)
+        del d
+    else:
+        _, gu, dn = weights(name)
+    b = permuted(cfg, T, seed=T + 5)
+    R, E, H, I = b["R"], cfg.E, cfg.H, cfg.I
+    xp0, h0, y0, _ = run(cfg, gu, dn, b, gather=False)
+    topk_w = torch.rand((T, cfg.k), device=DEV)
+    xp = xp0.clone() if not gather else torch.empty_like(xp0)
+    h = torch.empty_like(h0)
+    yw = torch.full((R, H), -3.0, dtype=torch.bfloat16, device=DEV)
+    sync = torch.zeros((E + 3,), dtype=torch.int32, device=DEV)
+    for _ in range(2):
+        _lib.moe_expert_swiglu_fused_weighted(xp, b["offsets"], E, H, I, gu, dn, topk_w, h, yw, sync, b["st"],
+                                              perm=b["perm"], k=cfg.k, x=b["x"] if gather else None)
+        torch.cuda.synchronize()
+        assert b["st"].item() == 0
+        assert int(sync.abs().sum().item()) == 0
+        want = (y0 * topk_w.view(-1)[b["perm"].long()].unsqueeze(1)).to(torch.bfloat16)
+        assert same(h, h0)
+        assert same(yw, want)
+
+
+@pytest.mark.parametrize("T,k,H,residual", [(16, 10, 2560, False), (129, 10, 2560, True), (7, 32, 256, True)])
+def test_combine_weighted_against_oracle(T, k, H, residual):
+    """moe_combine_weighted sums already weighted bf16 rows in rank order:
+    the oracle's combine of the same rows (as fp32) with unit weights."""
+    import oracle
+    rng = np.random.default_rng(T * 3 + k)
+    E = 64 if k <= 10 else 128
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    _, _, _, inv_r = oracle.permute(ids, E)
+    yw_bits = oracle.round_bf16_bits(rng.standard_normal((T * k, H)).astype(np.float32))
+    res_np = rng.standard_normal((T, H)).astype(np.float32) if residual else None
+    ref = oracle.combine(oracle.bits_to_f32(yw_bits), inv_r, np.ones((T, k), np.float32), res_np)
+    yw = torch.from_numpy(yw_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    out_b = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    out_f = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    st = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    _lib.moe_combine_weighted(yw, torch.from_numpy(inv_r).to(DEV), T, k,
+                              torch.from_numpy(res_np).to(DEV) if residual else None, out_b, out_f, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.allclose(out_f.cpu().numpy(), ref, rtol=1e-5, atol=1e-5)
+    assert same(out_b, out_f.to(torch.bfloat16))

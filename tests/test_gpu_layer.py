@@ -330,7 +330,9 @@ def test_combine_nonfinite_flag():
                                                   ("decode", 32, 12, True), ("decode", 33, 12, True),
                                                   ("decode", 64, 12, True), ("decode", 65, 12, True),
                                                   ("decode", 128, 12, True), ("decode", 129, 12, True),
-                                                  ("decode", 409, 12, True), ("decode", 410, 12, True)])
+                                                  ("decode", 409, 12, True), ("decode", 410, 12, True),
+                                                  # 256-row token tiles (from 131,072 routes)
+                                                  ("prefill", 16384, 96, True)])
 def test_layer_parity(name, T, nsample, tiled):
     cfg, d, host = case(name, T)
     layer, out = run_layer(cfg, d, tiled)

@@ -79,7 +79,7 @@ def test_ring_two_layers_against_oracle():
     for ml in ring.stack.layers:
         assert ml.read_status() == 0
     rng = np.random.default_rng(7)
-    toks = np.sort(np.concatenate([rng.choice(T - 1, size=63, replace=False), [T - 1]]))
+    toks = np.sort(np.concatenate([rng.choice(T - 1, size=127, replace=False), [T - 1]]))
     # teacher forcing: layer 0 reads x0; layer 1 reads the GPU's own
     # normalised input of that layer (the stack's bf16 input buffer holds the
     # last layer's), so a legitimate difference in x_1 cannot flip a route
@@ -98,7 +98,9 @@ def test_ring_two_layers_against_oracle():
         ok &= m
         update += oracle.experts_combine(oracle.bits_to_f32(n_bits), ids_r, w_r, cfg.H, cfg.I, wgu_bits=wgu,
                                          wd_bits=wdn)
-    assert ok.sum() >= 0.9 * len(toks)
+    # a token is graded when both of its layers' routes match the oracle in
+    # rank order (near-ties and allowed rank swaps in either layer are not)
+    assert ok.sum() >= 0.8 * len(toks)
     x0_np = x0.cpu().numpy()[toks].astype(np.float64)
     got_np = got.cpu().numpy()[toks].astype(np.float64)
     rel_max, mean_rel = assert_output_close(got_np[ok] - x0_np[ok], update[ok], what="two-layer ring residual update")
