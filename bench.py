@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--decay", type=float, default=0.9, help="offload/trace: the score policy's use-rate factor")
     ap.add_argument("--slots", default="160,192,256", help="offload: HBM expert slot counts")
     ap.add_argument("--waves", default="1,2,4,0", help="offload: wave widths to time (0 = all misses)")
+    ap.add_argument("--int4", action="store_true",
+                    help="offload: int4 g64 expert records (quantised from the same weights), copy-first fetch")
     ap.add_argument("--layers", type=int, default=0, help="distinct layer weight sets rotated (0 = auto)")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (small profiling case)")
     ap.add_argument("--tokens", type=int, default=0,
@@ -745,7 +747,15 @@ def run_offload(args, rank, world, local, dev):
     E, H, I, T = cfg.E, cfg.H, cfg.I, cfg.T
     slots = [int(v) for v in str(args.slots).split(",")]
     d = wl.layer_inputs(cfg, dev, with_x=False)
-    gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, E, H, I)
+    q4 = args.int4
+    fmt = _lib.MOE_W_INT4_G64_TILED if q4 else _lib.MOE_W_BF16_TILED
+    if q4:
+        q_gu, s_gu = wl.quantize_int4_g64(d["w_gateup"])
+        q_d, s_d = wl.quantize_int4_g64(d["w_down"])
+        gu, dn = pack_layer_experts(q_gu, q_d, _lib.MOE_W_INT4_G64, E, H, I, s_gateup=s_gu, s_down=s_d)
+        del q_gu, s_gu, q_d, s_d
+    else:
+        gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, E, H, I)
     del d["w_gateup"], d["w_down"]
     hgu = torch.empty(gu.shape, dtype=torch.uint8, pin_memory=True)
     hdn = torch.empty(dn.shape, dtype=torch.uint8, pin_memory=True)
@@ -759,7 +769,7 @@ def run_offload(args, rank, world, local, dev):
     st = torch.cuda.current_stream()
     K = max(args.steps, 16) if args.steps < 20000 else 256
     W0 = max(args.warmup, 3)
-    resident = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, T, fmt=_lib.MOE_W_BF16_TILED, I=I)
+    resident = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, T, fmt=fmt, I=I)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     # link bandwidth: a copy-engine copy of 1 GiB pinned -> device, and the
@@ -777,7 +787,7 @@ def run_offload(args, rank, world, local, dev):
     del dst
 
     # the all-hit layer: S = E slots, every expert in slot e
-    full = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=E)
+    full = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=E, fmt=fmt)
     ar = torch.arange(E, dtype=torch.int32, device=dev)
     stt = torch.tensor([0, E, 0, 0], dtype=torch.int32, device=dev)
     _lib.moe_cache_fetch(hgu, hdn, rg, rd, ar, ar, stt, full.pool_gu, full.pool_dn)
@@ -826,12 +836,13 @@ def run_offload(args, rank, world, local, dev):
     by_slots = {}
     for S in slots:
         bar = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=S, fetch="barrier",
-                             policy=args.policy, decay=args.decay)
+                             policy=args.policy, decay=args.decay, fmt=fmt)
         bar_ms, io_ms = timed(bar, fetch_events=True)
         hits, misses = [int(v) for v in bar.stats[2:].cpu().tolist()]
         del bar
         waves = {}
-        for w in [int(v) for v in args.waves.split(",")]:
+        # int4 records: copy-first only (the int4 kernels have no fetch warps)
+        for w in ([] if q4 else [int(v) for v in args.waves.split(",")]):
             lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=S,
                                  wave=w if w > 0 else 1 << 20, policy=args.policy, decay=args.decay)
             ms_w, _ = timed(lay)
@@ -841,6 +852,9 @@ def run_offload(args, rank, world, local, dev):
                 "tokens_per_s": T / (ms_w / 1e3), "ms_per_step": ms_w,
                 "hidden_fraction": (1.0 - (ms_w - hit_ms) / io_ms) if io_ms > 0 else None}
         fetched = misses * rec / K
+        if q4:
+            waves["copy_first"] = {"tokens_per_s": T / (bar_ms / 1e3), "ms_per_step": bar_ms,
+                                   "hidden_fraction": (1.0 - (bar_ms - hit_ms) / io_ms) if io_ms > 0 else None}
         best = max(waves.values(), key=lambda v: v["tokens_per_s"])
         by_slots[str(S)] = {
             "hit_rate": hits / max(hits + misses, 1), "misses_per_step": misses / K,
@@ -855,10 +869,12 @@ def run_offload(args, rank, world, local, dev):
     line = {
         "metric": METRIC, "value": head["best_tokens_per_s"], "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W0, "ms_per_step": T / head["best_tokens_per_s"] * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "int4 g64 experts, bf16 router" if q4 else "bf16",
         "data": "synthetic (seeded; 64 independent token blocks in turn)",
-        "config": {"workload": f"offload_{workload_name(cfg)}_S{slots[0]}", "slots": slots, "T": T, "E": E,
-                   "records": f"tile-packed bf16 in pinned host memory; HBM slot cache, {args.policy} replacement",
+        "config": {"workload": f"offload_{workload_name(cfg)}{'_int4' if q4 else ''}_S{slots[0]}", "slots": slots,
+                   "T": T, "E": E,
+                   "records": f"tile-packed {'int4 g64' if q4 else 'bf16'} in pinned host memory; HBM slot cache, "
+                              f"{args.policy} replacement",
                    "policy": args.policy, "decay": args.decay, "record_bytes": rec},
         "resident": {"ms_per_step": res_ms, "tokens_per_s": T / (res_ms / 1e3)},
         "all_hit": {"ms_per_step": hit_ms, "tokens_per_s": T / (hit_ms / 1e3)},

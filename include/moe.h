@@ -254,12 +254,15 @@ MOE_API moe_status moe_expert_swiglu_fused(const uint16_t *x, int k, const int32
                                            int32_t *sync_ws, int32_t *dev_status, void *stream);
 
 /* ---------------------------------------------------------------------------
- * moe_expert_swiglu_fused_weighted -- moe_expert_swiglu_fused whose down
- * epilogue also applies the route weight and stores bf16: for every slot s,
- *   yw_perm[s,:] = bf16( topk_w[perm[s]] * (W_down h[s]) )     [R,H] bf16
- * in place of the fp32 y_perm.  For prefill-sized calls this halves the bytes
- * of the expert outputs, written here and read again by the combine
- * (moe_combine_weighted), at the cost of one bf16 rounding per route term.
+ * moe_expert_swiglu_fused_weighted -- moe_expert_swiglu_fused with the route
+ * weight applied inside the launch and bf16 expert outputs: for every slot s
+ * with route weight w_s = topk_w[perm[s]],
+ *   h[s,:]       = bf16( w_s * silu(g) * u )        [R,I] bf16 (out)
+ *   yw_perm[s,:] = bf16( W_down h[s,:] )            [R,H] bf16 (out)
+ * in place of the fp32 y_perm (W_down is linear, so yw_perm carries the
+ * route weight).  For prefill-sized calls this halves the bytes of the expert
+ * outputs, written here and read again by the combine (moe_combine_weighted),
+ * at the cost of one bf16 rounding per route term.
  * Source: AFN-019, section "Hypothesis H4" (results of ready experts go to
  * separate slots; the weighted sum follows route-rank order).
  *   perm    [R] int32 from moe_permute (required), k the routes per token,
@@ -381,6 +384,22 @@ MOE_API moe_status moe_layer_stream(const void *host_gateup, const void *host_do
                                     size_t bytes_down, void *dev_gateup, void *dev_down, void *stream);
 MOE_API int moe_stream_mode(int U, int E, double record_bytes, double selected_gbs, double layer_gbs,
                             double selected_overhead_us, double *t_selected_us, double *t_layer_us);
+
+/* moe_expert_int4_slots -- moe_expert_gateup (kind 0) or moe_expert_down
+ *   (kind 1) for int4 g64 records held in an HBM slot cache: pool holds S
+ *   tile-packed int4 records of that component (MOE_W_INT4_G64_TILED layout,
+ *   one expert each, 2,611,200 B per expert at the Qwen4Exp shape against
+ *   9,830,400 B in bf16) and expert e's record is record slot_of[e]
+ *   (moe_cache_plan; the misses copied by moe_cache_fetch with the int4
+ *   record sizes).  rows: x_perm [R,H] bf16 (kind 0) or h [R,I] bf16
+ *   (kind 1); out: h [R,I] bf16 (kind 0) or y_perm [R,H] f32 (kind 1).  Same
+ *   arithmetic as the resident int4 path, so the same bits.  A routed expert
+ *   whose slot_of entry is outside [0, S) is read from slot 0 and flags
+ *   MOE_DEV_CACHE_FULL.  Decode-sized launches only (R <= 320 routes, K <=
+ *   2,560 inputs): MOE_ENOTSUP otherwise. */
+MOE_API moe_status moe_expert_int4_slots(int kind, const uint16_t *rows, const int32_t *offsets, int R, int E,
+                                         int H, int I, const void *pool, int S, const int32_t *slot_of, void *out,
+                                         int32_t *dev_status, void *stream);
 
 /* moe_expert_swiglu_cached -- moe_expert_swiglu_fused over slot pools:
  *   pool_gateup / pool_down hold S tile-packed bf16 records (MOE_W_BF16_TILED

@@ -64,6 +64,7 @@ def load(path: str | None = None):
             "moe_expert_swiglu_fused": ([p, i, p, p, p, i, i, i, i, i, p, p, p, p, p, p, p], i),
             "moe_expert_swiglu_fused_weighted": ([p, i, p, p, p, i, i, i, i, i, p, p, p, p, p, p, p, p], i),
             "moe_combine_weighted": ([p, p, i, i, i, p, p, p, p, p], i),
+            "moe_expert_int4_slots": ([i, p, p, i, i, i, i, p, i, p, p, p, p], i),
             "moe_route_permute": ([p, p, p, i, i, i, i, p, p, p, p, p, p, p, p, p], i),
             "moe_combine": ([p, p, p, i, i, i, p, p, p, p, p], i),
             "route_block_dedup": ([p, i, i, i, i, i, i, i, p, p, p, p, p, p], i),
@@ -192,6 +193,15 @@ def moe_expert_swiglu_fused_weighted(x_perm, offsets, E, H, I, w_gateup, w_down,
                                                  fmt, _ptr(w_gateup), _ptr(w_down), _ptr(topk_w), _ptr(h),
                                                  _ptr(yw_perm), _ptr(sync_ws), _ptr(dev_status), _stream(stream))
     _check("moe_expert_swiglu_fused_weighted", st)
+
+
+def moe_expert_int4_slots(kind, rows, offsets, E, H, I, pool, S, slot_of, out, dev_status, stream=None):
+    """int4 gate/up (kind 0) or down (kind 1) with expert e's record at
+    record slot_of[e] of an S-record pool (decode-sized launches)."""
+    R = rows.shape[0]
+    st = load().moe_expert_int4_slots(kind, _ptr(rows), _ptr(offsets), R, E, H, I, _ptr(pool), S, _ptr(slot_of),
+                                      _ptr(out), _ptr(dev_status), _stream(stream))
+    _check("moe_expert_int4_slots", st)
 
 
 def moe_cache_plan(counts, slot_of, expert_of, hand, miss_list, miss_slot, stats, dev_status,

@@ -68,7 +68,7 @@ inline moe_status check_geometry(int H, int E, int k, int I_or_zero) {
 
 extern "C" {
 
-int moe_abi_version(void) { return 101; }
+int moe_abi_version(void) { return 102; }
 
 const char* moe_status_str(moe_status s) {
   switch (s) {
@@ -208,6 +208,23 @@ moe_status moe_expert_down(const uint16_t* h, const int32_t* offsets, int R, int
   if (R == 0) return MOE_OK;
   cudaError_t e = moe::launch_grouped_gemm(moe::GemmKind::kDown, fmt, w_down, s_down, h, offsets, E, R, H, I, 0,
                                            y_perm, dev_status, static_cast<cudaStream_t>(stream));
+  return cuda_status(e);
+}
+
+moe_status moe_expert_int4_slots(int kind, const uint16_t* rows, const int32_t* offsets, int R, int E, int H, int I,
+                                 const void* pool, int S, const int32_t* slot_of, void* out, int32_t* dev_status,
+                                 void* stream) {
+  if (kind != 0 && kind != 1) return MOE_EINVAL;
+  moe_status c = check_expert_args(R, E, H, I, MOE_W_INT4_G64_TILED);
+  if (c != MOE_OK) return c;
+  if (S <= 0) return MOE_ESHAPE;
+  if (S > moe::kMaxE) return MOE_ENOTSUP;
+  if (!rows || !offsets || !pool || !slot_of || !out || !dev_status) return MOE_EINVAL;
+  if (!a16(rows) || !a16(pool) || !a16(out) || !a4(offsets) || !a4(slot_of) || !a4(dev_status)) return MOE_EINVAL;
+  if (R == 0) return MOE_OK;
+  const cudaError_t e = moe::gk::launch_int4_slots(kind, rows, offsets, E, R, H, I, pool, S, slot_of, out, dev_status,
+                                                   static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return MOE_ENOTSUP;
   return cuda_status(e);
 }
 

@@ -130,10 +130,17 @@ struct CfgF {
   static constexpr int kStages = kBudget / kStageBytes < 2 ? 2 : (kBudget / kStageBytes > 10 ? 10 : kBudget / kStageBytes);
   static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
   static constexpr int kTileRing = 4;  // tile ids the producer publishes ahead
+  // token rows per TMA box: 16 (a decode block's rows), or 64 for 256-row
+  // tiles, which then take at most four copies per K step instead of 16
+  static constexpr int kBoxR = NMAX >= 256 ? 64 : kBoxRows;
+  static constexpr int kBoxB = kBoxR * kBK * 2;
   static constexpr int kNumBars = 2 * kStages + 5 + 2 * kTileRing;
   // misc words and the tile-id ring; offsets and the two tile prefixes;
   // cached: also slots and the expert order
-  static constexpr int kTail = 32 + (CACHED ? 5 : 3) * (kMaxE + 1) * 4;
+  // misc words and the tile-id ring; offsets and the two tile prefixes;
+  // cached: also slots and the expert order; then the epilogue warps' route
+  // weights of the current tile's columns (weighted outputs)
+  static constexpr int kTail = 32 + (CACHED ? 5 : 3) * (kMaxE + 1) * 4 + 16 + 4 * NMAX * 4;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + kTail;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -323,6 +330,10 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
   int* soff = pre_dn + (kMaxE + 1);
   int* sslot = soff + (kMaxE + 1);  // cached: slot of each expert
   int* eord = sslot + (kMaxE + 1);  // cached: expert at each position of the tile order
+  // [4 epilogue warps][NMAX] route weights of the current tile's columns
+  // (16-byte aligned: the epilogue reads it four floats at a time)
+  float* swt = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(soff + (CACHED ? 3 : 1) * (kMaxE + 1)) + 15) & ~static_cast<uintptr_t>(15));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -518,8 +529,8 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       for (int q = 0; q < npend; ++q)
         for (int j = 0; j < G; ++j)
           for (int b = 0; b < pend_nblk[q]; ++b)
-            ptx::tma_load_2d(pend_dst[q] + j * C::kBBytes + b * kBBoxBytes, &tmX, pend_bar[q], (pend_ks[q] + j) * kBK,
-                             pend_row[q] + b * kBoxRows, pol_x);
+            ptx::tma_load_2d(pend_dst[q] + j * C::kBBytes + b * C::kBoxB, &tmX, pend_bar[q], (pend_ks[q] + j) * kBK,
+                             pend_row[q] + b * C::kBoxR, pol_x);
       npend = 0;
       return true;
     };
@@ -548,7 +559,7 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       }
       if (t < 0) break;
       const FTile tl = tile_of(t);
-      const int nblk = (tl.nrows + kBoxRows - 1) / kBoxRows;
+      const int nblk = (tl.nrows + C::kBoxR - 1) / C::kBoxR;
       const int KS = tl.kind ? p.ks_dn : p.ks_gu;
       const uint8_t* wt = tl.kind ? p.tiles_dn : p.tiles_gu;
       const CUtensorMap* tb = tl.kind ? &tmH : &tmX;
@@ -618,7 +629,7 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
           break;
         }
         const uint32_t fb = full0 + 8 * s;
-        ptx::mbar_arrive_expect_tx(fb, G * (kABytes + nblk * kBBoxBytes));
+        ptx::mbar_arrive_expect_tx(fb, G * (kABytes + nblk * C::kBoxB));
         armed[s] = static_cast<int>(ph);
         const uint32_t a_dst = ptx::smem_u32(sA + s * G * kABytes);
         const uint32_t b_dst = ptx::smem_u32(sB + s * G * C::kBBytes);
@@ -637,8 +648,8 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
 #pragma unroll
           for (int j = 0; j < G; ++j)
             for (int b = 0; b < nblk; ++b)
-              ptx::tma_load_2d(b_dst + j * C::kBBytes + b * kBBoxBytes, tb, fb, (ks + j) * kBK,
-                               tl.row0 + b * kBoxRows, pol_x);
+              ptx::tma_load_2d(b_dst + j * C::kBBytes + b * C::kBoxB, tb, fb, (ks + j) * kBK,
+                               tl.row0 + b * C::kBoxR, pol_x);
         }
         if (++s == S) {
           s = 0;
@@ -770,32 +781,55 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       }
       if (t < 0) break;
       const FTile tl = tile_of(t);
-      // weighted outputs: the route weight of every column of a down tile,
-      // loaded before the wait for its accumulator so that the two dependent
-      // loads overlap the tile's MMAs (lane l holds columns l, l + 32, ...)
-      constexpr int kWCols = (NMAX + 31) / 32;
-      float wcol[kWCols];
-      if (tl.kind == 1 && p.yw != nullptr) {
-#pragma unroll
-        for (int i = 0; i < kWCols; ++i) {
-          const int c = i * 32 + lane;
+      // weighted outputs: the route weight of every column of a gate/up
+      // tile into this warp's row of swt, loaded before the wait for the
+      // accumulator so that the two dependent loads overlap the tile's MMAs
+      float* wrow = swt + q * NMAX;
+      if (tl.kind == 0 && p.yw != nullptr) {
+        for (int c = lane; c < tl.nrows; c += 32) {
           float wv = 0.f;
-          if (c < tl.nrows) {
-            const int r = p.perm[tl.row0 + c];
-            if (r >= 0 && r < p.R) {
-              wv = p.topk_w[r];
-            } else {
-              set_status(p.status, MOE_DEV_BAD_EXPERT);
-            }
+          const int r = p.perm[tl.row0 + c];
+          if (r >= 0 && r < p.R) {
+            wv = p.topk_w[r];
+          } else {
+            set_status(p.status, MOE_DEV_BAD_EXPERT);
           }
-          wcol[i] = wv;
+          wrow[c] = wv;
         }
+        __syncwarp();
       }
       const bool ok = wait_bounded<kSleepEpi>(accf0 + 8 * acc, aph, misc + 1, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * NMAX);
-      if (tl.kind == 0) {
+      if (tl.kind == 0 && p.yw != nullptr) {
+        // weighted: h[s] = bf16(w_s * silu(g) * u), so the down tile's
+        // accumulator is already w_s * (W_down h[s])
+        const bool up_lane = lane >= 16;
+        const int i = tl.mb * 64 + q * 16 + (lane & 15);
+        for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
+          float v[16];
+          ptx::tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
+          float recv[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const float send = up_lane ? v[jj] : v[8 + jj];
+            recv[jj] = __shfl_xor_sync(0xffffffffu, send, 16);
+          }
+          const float4 wa = *reinterpret_cast<const float4*>(wrow + c0 + (up_lane ? 8 : 0));
+          const float4 wb = *reinterpret_cast<const float4*>(wrow + c0 + (up_lane ? 12 : 4));
+          const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int col = c0 + (up_lane ? 8 : 0) + jj;
+            const float g = up_lane ? recv[jj] : v[jj];
+            const float u = up_lane ? v[8 + jj] : recv[jj];
+            if (col < tl.nrows)
+              p.h[static_cast<size_t>(tl.row0 + col) * p.I + i] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(wv[jj] * (g / (1.0f + expf(-g)) * u)));
+          }
+        }
+      } else if (tl.kind == 0) {
         const bool up_lane = lane >= 16;
         const int i = tl.mb * 64 + q * 16 + (lane & 15);
         for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
@@ -816,6 +850,8 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
               p.h[static_cast<size_t>(tl.row0 + col) * p.I + i] = f32_to_bf16(g / (1.0f + expf(-g)) * u);
           }
         }
+      }
+      if (tl.kind == 0) {
         // publish this warp's h rows to TMA loads in other CTAs: each lane
         // fences its own stores, then one arrival per warp (4 per tile)
         fence_proxy_async_global();
@@ -834,20 +870,17 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
           }
         }
       } else {
-        // weighted bf16 rows (NMAX / 16 column groups, unrolled so that the
-        // weights stay in registers)
+        // weighted: the accumulator already carries the route weight (it
+        // was applied to h); bf16 rows
         const int j = tl.mb * kBM + row_in_tile;
+        for (int c0 = 0; c0 < tl.nrows; c0 += 16) {
+          float v[16];
+          ptx::tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
 #pragma unroll
-        for (int c0 = 0; c0 < NMAX; c0 += 16) {
-          if (c0 < tl.nrows) {
-            float v[16];
-            ptx::tmem_ld16(taddr + static_cast<uint32_t>(c0), v);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int col = c0 + jj;
-              const float wj = __shfl_sync(0xffffffffu, wcol[c0 >> 5], (c0 & 16) + jj);
-              if (col < tl.nrows) p.yw[static_cast<size_t>(tl.row0 + col) * p.H + j] = f32_to_bf16(v[jj] * wj);
-            }
+          for (int jj = 0; jj < 16; ++jj) {
+            const int col = c0 + jj;
+            if (col < tl.nrows)
+              p.yw[static_cast<size_t>(tl.row0 + col) * p.H + j] = __bfloat16_as_ushort(__float2bfloat16_rn(v[jj]));
           }
         }
       }
@@ -962,8 +995,13 @@ cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, u
   // columns), which halve how often an expert's weights are streamed and
   // take 48 KB of operands per 128 x 256 x 64 step instead of 32 KB per
   // 128 x 128 x 64; one K step per stage keeps four stages in 196 KB.
-  if (static_cast<long long>(R) >= static_cast<long long>(kFusedWideRowsPerExpert) * E)
-    return run_fused<256, 1, false>(mx, mh, a, st);
+  if (static_cast<long long>(R) >= static_cast<long long>(kFusedWideRowsPerExpert) * E) {
+    using CW = CfgF<256, 1, false>;
+    CUtensorMap mxw, mhw;
+    if (!make_rows_map(&mxw, x_perm, H, R, CW::kBoxR)) return cudaErrorInvalidValue;
+    if (!make_rows_map(&mhw, h, I, R, CW::kBoxR)) return cudaErrorInvalidValue;
+    return run_fused<256, 1, false>(mxw, mhw, a, st);
+  }
   if (a.ks_gu % 2 == 0 && a.ks_dn % 2 == 0) {
     switch (pick_nmax(R)) {
       case 16: return run_fused<16, 2, false>(mx, mh, a, st);

@@ -627,6 +627,33 @@ int pick_nmax(int rows_hint) {
 
 }  // namespace gk
 
+namespace gk {
+
+cudaError_t launch_int4_slots(int kind, const uint16_t* rows, const int32_t* offsets, int E, int R, int H, int I,
+                              const void* pool, int S, const int32_t* slot_of, void* out, int32_t* st_word,
+                              cudaStream_t st) {
+  const int K = kind == 0 ? H : I;
+  if (!use_gemv_q4(MOE_W_INT4_G64_TILED, R, K)) return cudaErrorNotSupported;
+  GemmArgs args{};
+  args.offsets = offsets;
+  args.E = E;
+  args.R = R;
+  args.status = st_word;
+  args.out = out;
+  args.tiles = static_cast<const uint8_t*>(pool);
+  args.brows = rows;
+  args.slot_of = slot_of;
+  args.S = S;
+  args.ksteps = K / kBK;
+  args.mblocks = kind == 0 ? I / 64 : H / kBM;
+  args.seg_rows = kind == 0 ? 2 * I : H;
+  args.ldo = kind == 0 ? I : H;
+  args.qgroup = args.ksteps % 2 == 0 ? 2 : 1;
+  return launch_gemv_q4(kind, args, st);
+}
+
+}  // namespace gk
+
 cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uint16_t* scales, const uint16_t* b_rows,
                                 const int32_t* offsets, int E, int R, int H, int I, int router_E, void* out,
                                 int32_t* st_word, cudaStream_t st) {

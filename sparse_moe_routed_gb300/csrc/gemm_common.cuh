@@ -98,6 +98,10 @@ struct GemmArgs {
   void* out;
   int ldo;                 // leading dimension of out (elements)
   int32_t* status;
+  // int4 GEMV over an expert cache (slot_of != nullptr): tiles is a pool of
+  // S records and expert e's record is record slot_of[e]
+  const int32_t* slot_of;
+  int S;
 };
 
 // Bounded mbarrier wait.  Polls back off with __nanosleep(kSleepNs) so that

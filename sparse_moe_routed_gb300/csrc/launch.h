@@ -90,6 +90,15 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int R, in
 
 // gemm.cu (tcgen05 grouped GEMM)
 enum class GemmKind { kGateUp = 0, kDown = 1, kRouter = 2 };
+
+// gemm.cu: the int4 GEMV (decode-sized launches only) over a pool of S
+// tile-packed int4 records, expert e read from record slot_of[e];
+// cudaErrorNotSupported for launches the GEMV does not take
+namespace gk {
+cudaError_t launch_int4_slots(int kind, const uint16_t* rows, const int32_t* offsets, int E, int R, int H, int I,
+                              const void* pool, int S, const int32_t* slot_of, void* out, int32_t* st_word,
+                              cudaStream_t st);
+}
 // Grouped weight-stationary GEMM: for every (segment e, 128-row weight block,
 // chunk of token rows) tile, D = W_e[rows] . B[rows of segment]^T on the
 // tensor cores; epilogue per kind.  Returns cudaErrorInvalidValue when a

@@ -187,6 +187,16 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = sc.tile(t);
+      // the expert's record: its own, or its slot in a cache pool (a routed
+      // expert without a slot reads slot 0 and flags MOE_DEV_CACHE_FULL)
+      int rec = tl.e;
+      if (p.slot_of != nullptr) {
+        rec = p.slot_of[tl.e];
+        if (rec < 0 || rec >= p.S) {
+          set_status(p.status, MOE_DEV_CACHE_FULL);
+          rec = 0;
+        }
+      }
       for (int ks = 0; ks < p.ksteps; ks += QG) {
         if (!wait_bounded<kSpin>(qempty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
           ok = false;
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
         armed_ph = (armed_ph & ~(1ull << s)) | (static_cast<uint64_t>(ph) << s);
         ptx::mbar_arrive_expect_tx(fb, CPS * kQChunk);
         // K steps ks .. ks + QG - 1 of each of the tile's BPT 128-row blocks
-        const size_t c0 = (static_cast<size_t>(tl.e) * p.mblocks + BPT * tl.mb) * p.ksteps + ks;
+        const size_t c0 = (static_cast<size_t>(rec) * p.mblocks + BPT * tl.mb) * p.ksteps + ks;
 #pragma unroll
         for (int bb = 0; bb < BPT; ++bb)
           ptx::bulk_load(ptx::smem_u32(sQ + (s * CPS + bb * QG) * kQChunk), p.tiles + (c0 + bb * p.ksteps) * kQChunk,

@@ -152,14 +152,7 @@ class MoELayer:
         elif self.fused:
             calls += self._expert_calls(lib, P, x if gather_in_fused else None, R, st)
         else:
-            calls += [
-                ("moe_expert_gateup", lib.moe_expert_gateup,
-                 (P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt, P(self.w_gateup), None, P(self.h),
-                  P(self.status), st)),
-                ("moe_expert_down", lib.moe_expert_down,
-                 (P(self.h), P(self.offsets), R, E, H, I, self.fmt, P(self.w_down), None, P(self.y_perm),
-                  P(self.status), st)),
-            ]
+            calls += self._two_launch_expert_calls(lib, P, R, st)
         if weighted:
             calls.append(("moe_combine_weighted", lib.moe_combine_weighted,
                           (P(self.yw_perm), P(self.inv), T, k, H, P(residual), P(out), P(out_f32), P(self.status),
@@ -170,6 +163,17 @@ class MoELayer:
                            P(self.status), st)))
         self._bound[key] = calls
         return calls
+
+    def _two_launch_expert_calls(self, lib, P, R, st):
+        E, H, I = self.E, self.H, self.I
+        return [
+            ("moe_expert_gateup", lib.moe_expert_gateup,
+             (P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt, P(self.w_gateup), None, P(self.h),
+              P(self.status), st)),
+            ("moe_expert_down", lib.moe_expert_down,
+             (P(self.h), P(self.offsets), R, E, H, I, self.fmt, P(self.w_down), None, P(self.y_perm),
+              P(self.status), st)),
+        ]
 
     def _expert_calls(self, lib, P, x_gather, R, st):
         return [("moe_expert_swiglu_fused", lib.moe_expert_swiglu_fused,
@@ -279,18 +283,21 @@ class MoELayer:
 class CachedMoELayer(MoELayer):
     """A layer whose expert records live in host memory behind an HBM cache.
 
-    host_gateup / host_down: the tile-packed bf16 records (moe_pack_experts
-    output, MOE_W_BF16_TILED) of all E experts in pinned host memory, which
-    the GPU reads directly over the CPU-GPU link.  S slots of HBM hold recently
-    used experts.  Each call plans hits and misses on the device
-    (moe_cache_plan) and then either fetches the misses in the expert launch
-    itself, in waves of `wave` experts while the resident experts compute
-    (fetch="wave"), or copies them first with moe_cache_fetch and computes
-    after (fetch="barrier").  Outputs are bit-identical to MoELayer over the
-    same records in HBM.
+    host_gateup / host_down: the tile-packed records (moe_pack_experts
+    output, MOE_W_BF16_TILED or MOE_W_INT4_G64_TILED) of all E experts in
+    pinned host memory, which the GPU reads directly over the CPU-GPU link.
+    S slots of HBM hold recently used experts.  Each call plans hits and
+    misses on the device (moe_cache_plan) and then either fetches the misses
+    in the expert launch itself, in waves of `wave` experts while the
+    resident experts compute (fetch="wave", bf16 records), or copies them
+    first with moe_cache_fetch and computes after (fetch="barrier"; int4
+    records, whose misses move 2,611,200 B each at the Qwen4Exp shape
+    against 9,830,400 B in bf16, always take this path).  Outputs are
+    bit-identical to MoELayer over the same records in HBM.
 
         moe_route -> moe_permute -> moe_cache_plan [-> moe_cache_fetch] ->
-        moe_expert_swiglu_cached -> moe_combine
+        moe_expert_swiglu_cached (bf16) | moe_expert_int4_slots x 2 (int4)
+        -> moe_combine
 
     stats [4] int32 on the device: {hits, misses} of the last call and their
     running totals.  policy: "fifo", "lru" or "score" (moe_cache_plan), decay
@@ -302,11 +309,15 @@ class CachedMoELayer(MoELayer):
     POLICIES = {"fifo": _lib.MOE_CACHE_FIFO, "lru": _lib.MOE_CACHE_LRU, "score": _lib.MOE_CACHE_SCORE}
 
     def __init__(self, w_router, bias, host_gateup, host_down, k: int, T_max: int, I: int, S: int,
-                 wave: int = 1 << 20, fetch: str = "wave", policy: str = "fifo", decay: float = 0.9):
+                 wave: int = 1 << 20, fetch: str = "wave", policy: str = "fifo", decay: float = 0.9,
+                 fmt: int = _lib.MOE_W_BF16_TILED):
         assert not host_gateup.is_cuda and host_gateup.is_pinned() and host_down.is_pinned()
         assert fetch in ("wave", "barrier") and policy in self.POLICIES
+        assert fmt in (_lib.MOE_W_BF16_TILED, _lib.MOE_W_INT4_G64_TILED)
+        if fmt == _lib.MOE_W_INT4_G64_TILED:
+            fetch = "barrier"
         self.policy, self.decay = self.POLICIES[policy], float(decay)
-        super().__init__(w_router, bias, host_gateup, host_down, k, T_max, fmt=_lib.MOE_W_BF16_TILED, I=I)
+        super().__init__(w_router, bias, host_gateup, host_down, k, T_max, fmt=fmt, I=I)
         E, H = self.E, self.H
         dev = w_router.device
         self.S, self.wave, self.fetch = S, wave, fetch
@@ -333,17 +344,35 @@ class CachedMoELayer(MoELayer):
         self.last_use.fill_(-1)
         self.stats.zero_()
 
-    def _expert_calls(self, lib, P, x_gather, R, st):
+    def _two_launch_expert_calls(self, lib, P, R, st):
+        # int4 records: plan, copy the misses into their slots, then the
+        # int4 contraction reads every expert from its slot
         E, H, I, S = self.E, self.H, self.I, self.S
+        calls = self._plan_calls(lib, P, st, fetch_first=True)
+        calls += [("moe_expert_int4_slots", lib.moe_expert_int4_slots,
+                   (0, P(self.x_perm), P(self.offsets), R, E, H, I, P(self.pool_gu), S, P(self.slot_of), P(self.h),
+                    P(self.status), st)),
+                  ("moe_expert_int4_slots", lib.moe_expert_int4_slots,
+                   (1, P(self.h), P(self.offsets), R, E, H, I, P(self.pool_dn), S, P(self.slot_of), P(self.y_perm),
+                    P(self.status), st))]
+        return calls
+
+    def _plan_calls(self, lib, P, st, fetch_first):
+        E, S = self.E, self.S
         calls = [("moe_cache_plan", lib.moe_cache_plan,
                   (P(self.counts), E, P(self.slot_of), P(self.expert_of), S, P(self.hand), self.policy,
                    C.c_float(self.decay), P(self.score), P(self.last_use), P(self.miss_list), P(self.miss_slot),
                    P(self.stats), P(self.status), st))]
-        wave = self.fetch == "wave"
-        if not wave:
+        if fetch_first:
             calls.append(("moe_cache_fetch", lib.moe_cache_fetch,
                           (P(self.w_gateup), P(self.w_down), self.rec_gu, self.rec_dn, P(self.miss_list),
                            P(self.miss_slot), P(self.stats), P(self.pool_gu), P(self.pool_dn), st)))
+        return calls
+
+    def _expert_calls(self, lib, P, x_gather, R, st):
+        E, H, I, S = self.E, self.H, self.I, self.S
+        wave = self.fetch == "wave"
+        calls = self._plan_calls(lib, P, st, fetch_first=not wave)
         calls.append(("moe_expert_swiglu_cached", lib.moe_expert_swiglu_cached,
                       (P(x_gather), self.k, P(self.perm), P(self.x_perm), P(self.offsets), R, E, H, I, self.fmt,
                        P(self.pool_gu), P(self.pool_dn), S, P(self.slot_of),

@@ -26,10 +26,10 @@ def lib():
 def test_library_loads_and_exports_every_declared_symbol():
     L = lib()
     names = _lib.declared_functions()
-    assert len(names) == 27
+    assert len(names) == 28
     for n in names:
         assert hasattr(L, n), n
-    assert L.moe_abi_version() == 101
+    assert L.moe_abi_version() == 102
     assert L.moe_status_str(0).decode() == "MOE_OK"
     assert L.moe_status_str(5).decode().startswith("MOE_ENOTSUP")
 
@@ -259,6 +259,30 @@ def test_combine_weighted_rejections():
     assert L.moe_combine_weighted(P, P, 16, 10, 2500, NUL, P, NUL, NUL, NUL) == _lib.MOE_ENOTSUP
     assert L.moe_combine_weighted(P, P, -1, 10, 2560, NUL, P, NUL, NUL, NUL) == _lib.MOE_ESHAPE
     assert L.moe_combine_weighted(P, P, 0, 10, 2560, NUL, P, NUL, NUL, NUL) == _lib.MOE_OK
+
+
+def test_int4_slots_rejections():
+    L = lib()
+    # kind, rows, offsets, R, E, H, I, pool, S, slot_of, out, dev_status, stream
+    base = [0, P, P, 160, 512, 2560, 640, P, 192, P, P, P, NUL]
+    names = ["kind", "rows", "off", "R", "E", "H", "I", "pool", "S", "slot", "out", "st"]
+
+    def call(**kw):
+        a = list(base)
+        for n, v in kw.items():
+            a[names.index(n)] = v
+        return L.moe_expert_int4_slots(*a)
+
+    assert call(kind=2) == _lib.MOE_EINVAL
+    assert call(slot=NUL) == _lib.MOE_EINVAL
+    assert call(pool=PM) == _lib.MOE_EINVAL
+    assert call(st=NUL) == _lib.MOE_EINVAL
+    assert call(S=0) == _lib.MOE_ESHAPE
+    assert call(S=2048) == _lib.MOE_ENOTSUP
+    assert call(I=600) == _lib.MOE_ENOTSUP
+    assert call(R=0) == _lib.MOE_OK
+    # a prefill-sized launch is not the decode GEMV's: rejected before any launch
+    assert call(R=40960) == _lib.MOE_ENOTSUP
 
 
 def test_route_permute_rejections():

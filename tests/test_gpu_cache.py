@@ -249,3 +249,82 @@ def test_merged_requests_equal_separate_calls(name, R):
     torch.cuda.synchronize()
     assert merged.read_status() == 0 and single.read_status() == 0
     assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+# ----------------------------------------------------------------- int4 records
+INT4_SMALL = wl.LayerConfig("cache_int4", T=4, H=512, E=64, k=4, I=256, bias=None, seed=24)
+_Q = {}
+
+
+def int4_layers(cfg):
+    """(resident int4 MoELayer, pinned host int4 records, raw codes/scales)."""
+    if cfg.name not in _Q:
+        d = wl.layer_inputs(cfg, DEV, with_x=False)
+        q_gu, s_gu = wl.quantize_int4_g64(d["w_gateup"])
+        q_d, s_d = wl.quantize_int4_g64(d["w_down"])
+        gu, dn = pack_layer_experts(q_gu, q_d, _lib.MOE_W_INT4_G64, cfg.E, cfg.H, cfg.I, s_gateup=s_gu, s_down=s_d)
+        torch.cuda.synchronize()
+        ref = MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, cfg.T, fmt=_lib.MOE_W_INT4_G64_TILED, I=cfg.I)
+        raw = {"wr": oracle.bf16_bits(d["w_router"]), "wgu_q": q_gu.cpu().numpy(), "sgu": oracle.bf16_bits(s_gu),
+               "wd_q": q_d.cpu().numpy(), "sd": oracle.bf16_bits(s_d)}
+        _Q[cfg.name] = (ref, gu.cpu().pin_memory(), dn.cpu().pin_memory(), d, raw)
+    return _Q[cfg.name]
+
+
+@pytest.mark.parametrize("policy", ["fifo", "lru"])
+def test_cached_int4_layer_bitwise_and_against_oracle(policy):
+    """int4 g64 records in host memory behind 24 HBM slots (4 tokens x 4 routes
+    per call, so a call always fits): every call of a
+    sequence with hits, misses and evictions equals, bit for bit, the
+    resident int4 layer (the record bytes move, the arithmetic does not);
+    misses move int4 records (2,611,200 B per expert at the Qwen4Exp shape);
+    each call is also graded against the oracle's int4 experts."""
+    cfg = INT4_SMALL
+    ref, hgu, hdn, d, raw = int4_layers(cfg)
+    lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, cfg.T, I=cfg.I, S=24, policy=policy,
+                         fmt=_lib.MOE_W_INT4_G64_TILED)
+    assert lay.rec_gu + lay.rec_dn == 3 * cfg.H * cfg.I // 2 + 3 * cfg.H * cfg.I // 64 * 2
+    uniq = 0
+    for i in range(10):
+        x = wl.token_batch(cfg, DEV, index=[0, 1, 0, 2, 3, 1, 4, 0, 5, 2][i], T=cfg.T)
+        want = ref.forward(x).clone()
+        got = lay.forward(x).clone()
+        torch.cuda.synchronize()
+        assert lay.read_status() == 0 and ref.read_status() == 0
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"call {i}"
+        uniq += int((lay.counts > 0).sum().item())
+        xb = oracle.bf16_bits(x)
+        ids_r, w_r, gap_r, L_r = oracle.route(xb, raw["wr"], None, cfg.k)
+        rep = compare_routes(lay.ids[:cfg.T].cpu().numpy(), lay.w[:cfg.T].cpu().numpy(), ids_r, w_r, gap_r, L_r)
+        keep = np.array(rep["exact_rows"], dtype=np.int64)
+        if len(keep):
+            moe = oracle.experts_combine(oracle.bits_to_f32(xb[keep]), ids_r[keep], w_r[keep], cfg.H, cfg.I,
+                                         wgu_q=raw["wgu_q"], sgu_bits=raw["sgu"], wd_q=raw["wd_q"], sd_bits=raw["sd"])
+            assert_output_close(got.float().cpu().numpy()[keep], moe, what=f"cached int4 call {i}")
+    s = lay.stats.cpu().tolist()
+    assert s[2] > 0 and s[3] > 24 and s[2] + s[3] == uniq
+
+
+def test_int4_slots_flag_an_expert_without_a_slot():
+    """A routed expert whose slot entry is -1 reads slot 0 and flags
+    MOE_DEV_CACHE_FULL (every access stays inside the pool)."""
+    cfg = INT4_SMALL
+    ref, hgu, hdn, d, raw = int4_layers(cfg)
+    E, H, I = cfg.E, cfg.H, cfg.I
+    rg = hgu.numel() // E
+    ids = torch.tensor([[3, 5, 7, 9]], dtype=torch.int32, device=DEV)
+    counts = torch.empty((E,), dtype=torch.int32, device=DEV)
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device=DEV)
+    perm = torch.empty((4,), dtype=torch.int32, device=DEV)
+    inv = torch.empty((4,), dtype=torch.int32, device=DEV)
+    xp = torch.empty((4, H), dtype=torch.bfloat16, device=DEV)
+    st = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    x = wl.token_batch(cfg, DEV, index=2, T=1)
+    _lib.moe_permute(ids, E, x, counts, offsets, perm, inv, xp, st)
+    pool = hgu[: 4 * rg].to(DEV)
+    slot_of = torch.full((E,), -1, dtype=torch.int32, device=DEV)
+    slot_of[3], slot_of[5], slot_of[7] = 0, 1, 2  # expert 9 has no slot
+    h = torch.empty((4, I), dtype=torch.bfloat16, device=DEV)
+    _lib.moe_expert_int4_slots(0, xp, offsets, E, H, I, pool, 4, slot_of, h, st)
+    torch.cuda.synchronize()
+    assert st.item() & _lib.MOE_DEV_CACHE_FULL
