@@ -132,7 +132,7 @@ struct CfgF {
   static constexpr int kTileRing = 4;  // tile ids the producer publishes ahead
   // token rows per TMA box: 16 (a decode block's rows), or 64 for 256-row
   // tiles, which then take at most four copies per K step instead of 16
-  static constexpr int kBoxR = NMAX >= 256 ? 64 : kBoxRows;
+  static constexpr int kBoxR = NMAX >= 256 ? 128 : (NMAX >= 128 ? 64 : kBoxRows);
   static constexpr int kBoxB = kBoxR * kBK * 2;
   static constexpr int kNumBars = 2 * kStages + 5 + 2 * kTileRing;
   // misc words and the tile-id ring; offsets and the two tile prefixes;
@@ -921,8 +921,12 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
 }
 
 template <int NMAX, int GG, bool CACHED>
-cudaError_t run_fused(const CUtensorMap& mx, const CUtensorMap& mh, const FusedArgs& args, cudaStream_t st) {
+cudaError_t run_fused(const FusedArgs& args, cudaStream_t st) {
   using C = CfgF<NMAX, GG, CACHED>;
+  // token-row maps with this variant's box height
+  CUtensorMap mx, mh;
+  if (!make_rows_map(&mx, args.x_perm, args.H, args.R, C::kBoxR)) return cudaErrorInvalidValue;
+  if (!make_rows_map(&mh, args.h, args.I, args.R, C::kBoxR)) return cudaErrorInvalidValue;
   auto kern = grouped_swiglu_fused_kernel<NMAX, GG, CACHED>;
   cudaError_t e = ensure_smem(kern, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -939,9 +943,6 @@ cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, u
                                 const void* w_down, const FusedCache* cache, uint16_t* h, float* y,
                                 const float* topk_w, uint16_t* yw, int32_t* ready, int32_t* st_word,
                                 cudaStream_t st) {
-  CUtensorMap mx, mh;
-  if (!make_rows_map(&mx, x_perm, H, R, kBoxRows)) return cudaErrorInvalidValue;
-  if (!make_rows_map(&mh, h, I, R, kBoxRows)) return cudaErrorInvalidValue;
   FusedArgs a{};
   a.offsets = offsets;
   a.E = E;
@@ -984,10 +985,10 @@ cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, u
       a.wave = cache->wave;
     }
     switch (pick_nmax(R)) {
-      case 16: return run_fused<16, 2, true>(mx, mh, a, st);
-      case 32: return run_fused<32, 2, true>(mx, mh, a, st);
-      case 64: return run_fused<64, 2, true>(mx, mh, a, st);
-      default: return run_fused<128, 2, true>(mx, mh, a, st);
+      case 16: return run_fused<16, 2, true>(a, st);
+      case 32: return run_fused<32, 2, true>(a, st);
+      case 64: return run_fused<64, 2, true>(a, st);
+      default: return run_fused<128, 2, true>(a, st);
     }
   }
   // Compute-bound launches (hundreds of token rows per expert): 256-row
@@ -995,26 +996,21 @@ cudaError_t launch_swiglu_fused(const uint16_t* x, int k, const int32_t* perm, u
   // columns), which halve how often an expert's weights are streamed and
   // take 48 KB of operands per 128 x 256 x 64 step instead of 32 KB per
   // 128 x 128 x 64; one K step per stage keeps four stages in 196 KB.
-  if (static_cast<long long>(R) >= static_cast<long long>(kFusedWideRowsPerExpert) * E) {
-    using CW = CfgF<256, 1, false>;
-    CUtensorMap mxw, mhw;
-    if (!make_rows_map(&mxw, x_perm, H, R, CW::kBoxR)) return cudaErrorInvalidValue;
-    if (!make_rows_map(&mhw, h, I, R, CW::kBoxR)) return cudaErrorInvalidValue;
-    return run_fused<256, 1, false>(mxw, mhw, a, st);
-  }
+  if (static_cast<long long>(R) >= static_cast<long long>(kFusedWideRowsPerExpert) * E)
+    return run_fused<256, 1, false>(a, st);
   if (a.ks_gu % 2 == 0 && a.ks_dn % 2 == 0) {
     switch (pick_nmax(R)) {
-      case 16: return run_fused<16, 2, false>(mx, mh, a, st);
-      case 32: return run_fused<32, 2, false>(mx, mh, a, st);
-      case 64: return run_fused<64, 2, false>(mx, mh, a, st);
-      default: return run_fused<128, 2, false>(mx, mh, a, st);
+      case 16: return run_fused<16, 2, false>(a, st);
+      case 32: return run_fused<32, 2, false>(a, st);
+      case 64: return run_fused<64, 2, false>(a, st);
+      default: return run_fused<128, 2, false>(a, st);
     }
   }
   switch (pick_nmax(R)) {
-    case 16: return run_fused<16, 1, false>(mx, mh, a, st);
-    case 32: return run_fused<32, 1, false>(mx, mh, a, st);
-    case 64: return run_fused<64, 1, false>(mx, mh, a, st);
-    default: return run_fused<128, 1, false>(mx, mh, a, st);
+    case 16: return run_fused<16, 1, false>(a, st);
+    case 32: return run_fused<32, 1, false>(a, st);
+    case 64: return run_fused<64, 1, false>(a, st);
+    default: return run_fused<128, 1, false>(a, st);
   }
 }
 
