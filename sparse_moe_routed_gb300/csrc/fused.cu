@@ -132,7 +132,7 @@ struct CfgF {
   static constexpr int kTileRing = 4;  // tile ids the producer publishes ahead
   // token rows per TMA box: 16 (a decode block's rows), or 64 for 256-row
   // tiles, which then take at most four copies per K step instead of 16
-  static constexpr int kBoxR = NMAX >= 256 ? 128 : (NMAX >= 128 ? 64 : kBoxRows);
+  static constexpr int kBoxR = NMAX >= 256 ? 128 : box_rows_for(NMAX);
   static constexpr int kBoxB = kBoxR * kBK * 2;
   static constexpr int kNumBars = 2 * kStages + 5 + 2 * kTileRing;
   // misc words and the tile-id ring; offsets and the two tile prefixes;

@@ -122,14 +122,15 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = sc.tile(t);
-      const int nblk = (tl.nrows + kBoxRows - 1) / kBoxRows;
+      constexpr int BR = box_rows_for(NMAX);
+      const int nblk = (tl.nrows + BR - 1) / BR;
       for (int ks = 0; ks < p.ksteps; ks += G) {
         if (!wait_bounded<kSpin>(empty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
           ok = false;
           break;
         }
         const uint32_t fb = full0 + 8 * s;
-        ptx::mbar_arrive_expect_tx(fb, G * (kABytes + nblk * kBBoxBytes));
+        ptx::mbar_arrive_expect_tx(fb, G * (kABytes + nblk * BR * kBK * 2));
         armed[s] = static_cast<int>(ph);
         const uint32_t a_dst = ptx::smem_u32(sA + s * G * kABytes);
         const uint32_t b_dst = ptx::smem_u32(sB + s * G * C::kBBytes);
@@ -155,8 +156,8 @@ __global__ void __launch_bounds__(kCoreThreads, 1)
 #pragma unroll
         for (int j = 0; j < G; ++j)
           for (int b = 0; b < nblk; ++b)
-            ptx::tma_load_2d(b_dst + j * C::kBBytes + b * kBBoxBytes, &tmB, fb, (ks + j) * kBK,
-                             tl.row0 + b * kBoxRows, pol_x);
+            ptx::tma_load_2d(b_dst + j * C::kBBytes + b * BR * kBK * 2, &tmB, fb, (ks + j) * kBK,
+                             tl.row0 + b * BR, pol_x);
         if (++s == S) {
           s = 0;
           ph ^= 1u;
@@ -306,7 +307,8 @@ __global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = sc.tile(t);
-      const int nblk = (tl.nrows + kBoxRows - 1) / kBoxRows;
+      constexpr int BR = box_rows_for(NMAX);
+      const int nblk = (tl.nrows + BR - 1) / BR;
       for (int ks = 0; ks < p.ksteps; ks += (weights ? QG : 1)) {
         if (!wait_bounded<kSpin>(empty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
           ok = false;
@@ -320,10 +322,10 @@ __global__ void __launch_bounds__(CfgQ<NMAX>::kThreads, 1)
           const size_t chunk = (static_cast<size_t>(tl.e) * p.mblocks + tl.mb) * p.ksteps + ks;
           ptx::bulk_load(ptx::smem_u32(sQ + s * QG * kQChunk), p.tiles + chunk * kQChunk, QG * kQChunk, fb, pol);
         } else {
-          ptx::mbar_arrive_expect_tx(fb, nblk * kBBoxBytes);
+          ptx::mbar_arrive_expect_tx(fb, nblk * BR * kBK * 2);
           const uint32_t b_dst = ptx::smem_u32(sB + s * C::kBBytes);
           for (int b = 0; b < nblk; ++b)
-            ptx::tma_load_2d(b_dst + b * kBBoxBytes, &tmB, fb, ks * kBK, tl.row0 + b * kBoxRows, pol);
+            ptx::tma_load_2d(b_dst + b * BR * kBK * 2, &tmB, fb, ks * kBK, tl.row0 + b * BR, pol);
         }
         if (++s == S) {
           s = 0;
@@ -679,7 +681,7 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uin
         cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)kBoxRows, 2, 1};
         if (!make_map(&ma, w, 4, dims, str, box)) return cudaErrorInvalidValue;
       }
-      if (!make_rows_map(&mb, b_rows, H, R, kBoxRows)) return cudaErrorInvalidValue;
+      if (!make_rows_map(&mb, b_rows, H, R, box_rows_for(pick_nmax(R)))) return cudaErrorInvalidValue;
       args.ksteps = H / kBK;
       args.mblocks = I / 64;
       args.seg_rows = 2 * I;
@@ -688,7 +690,7 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uin
     }
     case GemmKind::kDown: {
       if (plain && !make_rows_map(&ma, w, I, E * H, kBM)) return cudaErrorInvalidValue;
-      if (!make_rows_map(&mb, b_rows, I, R, kBoxRows)) return cudaErrorInvalidValue;
+      if (!make_rows_map(&mb, b_rows, I, R, box_rows_for(pick_nmax(R)))) return cudaErrorInvalidValue;
       args.ksteps = I / kBK;
       args.mblocks = H / kBM;
       args.seg_rows = H;
@@ -698,7 +700,7 @@ cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uin
     case GemmKind::kRouter: {
       // one dense segment: all T token rows against all router_E expert rows
       if (!make_rows_map(&ma, w, H, router_E, kBM)) return cudaErrorInvalidValue;
-      if (!make_rows_map(&mb, b_rows, H, R, kBoxRows)) return cudaErrorInvalidValue;
+      if (!make_rows_map(&mb, b_rows, H, R, box_rows_for(128))) return cudaErrorInvalidValue;
       args.offsets = nullptr;
       args.E = 1;
       args.ksteps = H / kBK;

@@ -23,7 +23,7 @@ constexpr int kBM = 128;                             // weight rows per tile (MM
 constexpr int kBK = 64;                              // K per stage: one 128-byte swizzled row of bf16
 constexpr int kUK = 16;                              // K per MMA instruction
 constexpr int kABytes = kBM * kBK * 2;               // 16 KB bf16 operand tile
-constexpr int kBoxRows = 16;                         // token rows per B TMA box
+constexpr int kBoxRows = 16;                         // token rows per B TMA box (tiles of up to 64 rows)
 constexpr int kBBoxBytes = kBoxRows * kBK * 2;       // 2 KB
 constexpr int kGUBoxBytes = 2 * kBoxRows * kBK * 2;  // 16 gate + 16 up rows: 4 KB
 constexpr int kQBytes = kBM * kBK / 2;               // int4 codes of one stage: 4 KB
@@ -32,6 +32,13 @@ constexpr int kQChunk = kQBytes + kSBytes;           // one packed int4 stage ch
 constexpr int kCoreThreads = 192;                    // producers, MMA, 4 epilogue warps
 constexpr int kSmemTail = 16 + 2 * (kMaxE + 1) * 4;  // misc words + tile prefix + segment offsets
 constexpr uint64_t kWaitNs = 2000000000ull;
+
+// Token rows per B TMA box for tiles of nmax rows: decode-sized tiles hold a
+// few rows per expert, so 16-row boxes; 128-row tiles take 64-row boxes, so
+// that one producer thread issues two copies per K step rather than eight
+// (rows past a tile's end belong to the next expert or are zero-filled past
+// the last row, and are never stored).
+constexpr int box_rows_for(int nmax) { return nmax >= 128 ? 64 : kBoxRows; }
 
 // bf16 weights: one ring; a stage holds G consecutive K steps: A (G x 16 KB)
 // + B (G x NMAX token rows).  Tile-packed weights take G = 2 (one 32 KB bulk
