@@ -841,10 +841,11 @@ def run_offload(args, rank, world, local, dev):
         hits, misses = [int(v) for v in bar.stats[2:].cpu().tolist()]
         del bar
         waves = {}
-        # int4 records: copy-first only (the int4 kernels have no fetch warps)
-        for w in ([] if q4 else [int(v) for v in args.waves.split(",")]):
+        # int4 records: the gate/up launch fetches every miss (gate/up pieces
+        # first, then down): one in-launch variant, width "all"
+        for w in ([0] if q4 else [int(v) for v in args.waves.split(",")]):
             lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, T, I=I, S=S,
-                                 wave=w if w > 0 else 1 << 20, policy=args.policy, decay=args.decay)
+                                 wave=w if w > 0 else 1 << 20, policy=args.policy, decay=args.decay, fmt=fmt)
             ms_w, _ = timed(lay)
             assert tuple(int(v) for v in lay.stats[2:].cpu().tolist()) == (hits, misses), "passes differ"
             del lay
@@ -852,9 +853,6 @@ def run_offload(args, rank, world, local, dev):
                 "tokens_per_s": T / (ms_w / 1e3), "ms_per_step": ms_w,
                 "hidden_fraction": (1.0 - (ms_w - hit_ms) / io_ms) if io_ms > 0 else None}
         fetched = misses * rec / K
-        if q4:
-            waves["copy_first"] = {"tokens_per_s": T / (bar_ms / 1e3), "ms_per_step": bar_ms,
-                                   "hidden_fraction": (1.0 - (bar_ms - hit_ms) / io_ms) if io_ms > 0 else None}
         best = max(waves.values(), key=lambda v: v["tokens_per_s"])
         by_slots[str(S)] = {
             "hit_rate": hits / max(hits + misses, 1), "misses_per_step": misses / K,

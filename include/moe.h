@@ -401,6 +401,27 @@ MOE_API moe_status moe_expert_int4_slots(int kind, const uint16_t *rows, const i
                                          int H, int I, const void *pool, int S, const int32_t *slot_of, void *out,
                                          int32_t *dev_status, void *stream);
 
+/* moe_expert_int4_fetch -- moe_expert_int4_slots(kind 0, gate/up) that also
+ *   fetches the plan of moe_cache_plan (miss_list, miss_slot, stats) from the
+ *   host records (host_gateup / host_down: E tile-packed int4 records each,
+ *   pinned host memory the device can read, 16-byte aligned) into the slot
+ *   pools pool_gateup / pool_down: two extra warps per CTA copy the misses'
+ *   gate/up records, then their down records, over the CPU-GPU link while the
+ *   resident experts compute (their tiles come first); a fetched expert's
+ *   tiles start once their 128-row blocks have landed.  The down launch that
+ *   follows (moe_expert_int4_slots, kind 1) finds every down record in place.
+ *   Source: AFN-019, section "Hypothesis H4" (gate and up of an expert
+ *   together, down once h exists; ready experts compute at once).
+ *   sync_ws: [2 + E * I/64] int32, zero before the first call; every launch
+ *   leaves it zero again (after a launch that flagged MOE_DEV_TIMEOUT, zero
+ *   it).  The CTAs wait on one another's copies (bounded).  Decode-sized
+ *   launches only (MOE_ENOTSUP otherwise). */
+MOE_API moe_status moe_expert_int4_fetch(const uint16_t *x_perm, const int32_t *offsets, int R, int E, int H, int I,
+                                         void *pool_gateup, void *pool_down, int S, const int32_t *slot_of,
+                                         const void *host_gateup, const void *host_down, const int32_t *miss_list,
+                                         const int32_t *miss_slot, const int32_t *stats, uint16_t *h,
+                                         int32_t *sync_ws, int32_t *dev_status, void *stream);
+
 /* moe_expert_swiglu_cached -- moe_expert_swiglu_fused over slot pools:
  *   pool_gateup / pool_down hold S tile-packed bf16 records (MOE_W_BF16_TILED
  *   layout, one expert each) and expert e's records are record slot_of[e].

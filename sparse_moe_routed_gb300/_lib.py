@@ -65,6 +65,7 @@ def load(path: str | None = None):
             "moe_expert_swiglu_fused_weighted": ([p, i, p, p, p, i, i, i, i, i, p, p, p, p, p, p, p, p], i),
             "moe_combine_weighted": ([p, p, i, i, i, p, p, p, p, p], i),
             "moe_expert_int4_slots": ([i, p, p, i, i, i, i, p, i, p, p, p, p], i),
+            "moe_expert_int4_fetch": ([p, p, i, i, i, i, p, p, i, p, p, p, p, p, p, p, p, p, p], i),
             "moe_route_permute": ([p, p, p, i, i, i, i, p, p, p, p, p, p, p, p, p], i),
             "moe_combine": ([p, p, p, i, i, i, p, p, p, p, p], i),
             "route_block_dedup": ([p, i, i, i, i, i, i, i, p, p, p, p, p, p], i),

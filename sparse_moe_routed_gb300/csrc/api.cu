@@ -68,7 +68,7 @@ inline moe_status check_geometry(int H, int E, int k, int I_or_zero) {
 
 extern "C" {
 
-int moe_abi_version(void) { return 102; }
+int moe_abi_version(void) { return 103; }
 
 const char* moe_status_str(moe_status s) {
   switch (s) {
@@ -224,6 +224,31 @@ moe_status moe_expert_int4_slots(int kind, const uint16_t* rows, const int32_t* 
   if (R == 0) return MOE_OK;
   const cudaError_t e = moe::gk::launch_int4_slots(kind, rows, offsets, E, R, H, I, pool, S, slot_of, out, dev_status,
                                                    static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return MOE_ENOTSUP;
+  return cuda_status(e);
+}
+
+moe_status moe_expert_int4_fetch(const uint16_t* x_perm, const int32_t* offsets, int R, int E, int H, int I,
+                                 void* pool_gateup, void* pool_down, int S, const int32_t* slot_of,
+                                 const void* host_gateup, const void* host_down, const int32_t* miss_list,
+                                 const int32_t* miss_slot, const int32_t* stats, uint16_t* h, int32_t* sync_ws,
+                                 int32_t* dev_status, void* stream) {
+  moe_status c = check_expert_args(R, E, H, I, MOE_W_INT4_G64_TILED);
+  if (c != MOE_OK) return c;
+  if (S <= 0) return MOE_ESHAPE;
+  if (S > moe::kMaxE) return MOE_ENOTSUP;
+  if (!x_perm || !offsets || !pool_gateup || !pool_down || !slot_of || !host_gateup || !host_down || !miss_list ||
+      !miss_slot || !stats || !h || !dev_status)
+    return MOE_EINVAL;
+  if (!sync_ws) return MOE_EWORKSPACE;
+  if (!a16(x_perm) || !a16(pool_gateup) || !a16(pool_down) || !a16(host_gateup) || !a16(host_down) || !a16(h) ||
+      !a4(offsets) || !a4(slot_of) || !a4(miss_list) || !a4(miss_slot) || !a4(stats) || !a4(sync_ws) ||
+      !a4(dev_status))
+    return MOE_EINVAL;
+  if (R == 0) return MOE_OK;
+  const cudaError_t e = moe::gk::launch_int4_fetch(x_perm, offsets, E, R, H, I, pool_gateup, pool_down, S, slot_of,
+                                                   host_gateup, host_down, miss_list, miss_slot, stats, h, sync_ws,
+                                                   dev_status, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return MOE_ENOTSUP;
   return cuda_status(e);
 }

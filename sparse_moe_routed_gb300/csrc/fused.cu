@@ -145,16 +145,6 @@ struct CfgF {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 struct FTile {
   int kind;  // 0 gate/up, 1 down
   int j, e;  // position in the expert order, expert

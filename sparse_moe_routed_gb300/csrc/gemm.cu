@@ -654,6 +654,45 @@ cudaError_t launch_int4_slots(int kind, const uint16_t* rows, const int32_t* off
   return launch_gemv_q4(kind, args, st);
 }
 
+cudaError_t launch_int4_fetch(const uint16_t* rows, const int32_t* offsets, int E, int R, int H, int I, void* pool_gu,
+                              void* pool_dn, int S, const int32_t* slot_of, const void* host_gu, const void* host_dn,
+                              const int32_t* miss_list, const int32_t* miss_slot, const int32_t* stats, uint16_t* h,
+                              int32_t* fsync, int32_t* st_word, cudaStream_t st) {
+  if (!use_gemv_q4(MOE_W_INT4_G64_TILED, R, H)) return cudaErrorNotSupported;
+  GemmArgs args{};
+  args.offsets = offsets;
+  args.E = E;
+  args.R = R;
+  args.status = st_word;
+  args.out = h;
+  args.tiles = static_cast<const uint8_t*>(pool_gu);
+  args.brows = rows;
+  args.slot_of = slot_of;
+  args.S = S;
+  args.ksteps = H / kBK;
+  args.mblocks = I / 64;
+  args.seg_rows = 2 * I;
+  args.ldo = I;
+  args.qgroup = args.ksteps % 2 == 0 ? 2 : 1;
+  args.host_gu = static_cast<const uint8_t*>(host_gu);
+  args.host_dn = static_cast<const uint8_t*>(host_dn);
+  args.pool_dn = static_cast<uint8_t*>(pool_dn);
+  args.rec_gu = static_cast<size_t>(args.mblocks) * args.ksteps * kQChunk;
+  args.rec_dn = static_cast<size_t>(H / kBM) * (I / kBK) * kQChunk;
+  int cpp = 1;  // chunks per gate/up piece: the largest divisor of the K steps up to 8
+  for (int c = 8; c >= 1; --c)
+    if (args.ksteps % c == 0) {
+      cpp = c;
+      break;
+    }
+  args.cpp = cpp;
+  args.miss_list = miss_list;
+  args.miss_slot = miss_slot;
+  args.stats = stats;
+  args.fsync = fsync;
+  return launch_gemv_q4(0, args, st);
+}
+
 }  // namespace gk
 
 cudaError_t launch_grouped_gemm(GemmKind kind, int fmt, const void* w, const uint16_t* scales, const uint16_t* b_rows,

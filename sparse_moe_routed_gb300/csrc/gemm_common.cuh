@@ -109,6 +109,21 @@ struct GemmArgs {
   // S records and expert e's record is record slot_of[e]
   const int32_t* slot_of;
   int S;
+  // ... and, for a gate/up launch with host records (host_gu != nullptr),
+  // the planned misses are fetched in the launch: fetch warps copy the
+  // gate/up records (pieces of cpp chunks, counted per 128-row block in
+  // fsync[2 + e * mblocks + block]) and then the down records (into pool_dn,
+  // for the down launch that follows); fsync[0] is the piece queue, fsync[1]
+  // the exit count.
+  const uint8_t* host_gu;
+  const uint8_t* host_dn;
+  uint8_t* pool_dn;
+  size_t rec_gu, rec_dn;
+  int cpp;  // chunks per gate/up piece (divides ksteps)
+  const int32_t* miss_list;
+  const int32_t* miss_slot;
+  const int32_t* stats;
+  int32_t* fsync;
 };
 
 // Bounded mbarrier wait.  Polls back off with __nanosleep(kSleepNs) so that
@@ -135,6 +150,18 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
       }
     }
   }
+}
+
+// Acquire load of a device-wide counter, and the fence that orders generic
+// stores before later bulk/TMA reads of the same bytes (in any CTA).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 constexpr uint32_t kSpin = 0;         // producer / MMA threads
@@ -181,6 +208,7 @@ struct Sched {
   int E;
   int mblocks;
   int nmax;
+  const int* order = nullptr;  // expert at each position of the tile order (null: ID order)
 
   __device__ __forceinline__ Tile tile(int t) const {
     int lo = 0, hi = E;
@@ -190,10 +218,11 @@ struct Sched {
     }
     const int local = t - prefix[lo];
     const int chunk = local / mblocks;
-    const int start = soff[lo];
-    const int len = max(soff[lo + 1] - start, 0);
+    const int e = order != nullptr ? order[lo] : lo;
+    const int start = soff[e];
+    const int len = max(soff[e + 1] - start, 0);
     Tile tl;
-    tl.e = lo;
+    tl.e = e;
     tl.mb = local - chunk * mblocks;
     tl.row0 = start + chunk * nmax;
     tl.nrows = min(nmax, len - chunk * nmax);

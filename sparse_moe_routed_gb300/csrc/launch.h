@@ -98,6 +98,12 @@ namespace gk {
 cudaError_t launch_int4_slots(int kind, const uint16_t* rows, const int32_t* offsets, int E, int R, int H, int I,
                               const void* pool, int S, const int32_t* slot_of, void* out, int32_t* st_word,
                               cudaStream_t st);
+// ... its gate/up launch fetching the planned misses' records (both
+// components) from host memory while the resident experts compute
+cudaError_t launch_int4_fetch(const uint16_t* rows, const int32_t* offsets, int E, int R, int H, int I, void* pool_gu,
+                              void* pool_dn, int S, const int32_t* slot_of, const void* host_gu, const void* host_dn,
+                              const int32_t* miss_list, const int32_t* miss_slot, const int32_t* stats, uint16_t* h,
+                              int32_t* fsync, int32_t* st_word, cudaStream_t st);
 }
 // Grouped weight-stationary GEMM: for every (segment e, 128-row weight block,
 // chunk of token rows) tile, D = W_e[rows] . B[rows of segment]^T on the

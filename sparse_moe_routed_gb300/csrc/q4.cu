@@ -79,8 +79,11 @@ struct CfgV {
   // [K steps][c0, c1, c0, c1, c2, c3, c2, c3]
   static constexpr int kXsFloats = kGvMaxK / 64 * 8;
   static constexpr int kNumBars = 2 * SQmax + 12;
+  // in-launch fetch: the tile order's expert at each position, and a bit per
+  // expert being fetched
+  static constexpr int kFetchTail = kMaxE * 4 + 2 * (kMaxE / 8);
   static constexpr int kSmemBytes = 1024 + SQmax * kQChunk + 2 * kXBytes + 2 * kUpFloats * 4 +
-                                    2 * kRedFloats * 4 + 2 * kXsFloats * 4 + kNumBars * 8 + kSmemTail;
+                                    2 * kRedFloats * 4 + 2 * kXsFloats * 4 + kNumBars * 8 + kSmemTail + kFetchTail;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -117,8 +120,12 @@ __device__ __forceinline__ uint32_t code_pair_f16(uint32_t v, bool lo, uint32_t 
   return d;
 }
 
-template <int KIND, int QG, int BPT>
-__global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
+constexpr int kGvFetchWarps = 2;     // FETCH launches: warps that copy the misses' records
+constexpr int kGvFetchBytes = 32768;  // a down-record piece
+
+template <int KIND, int QG, int BPT, bool FETCH = false>
+__global__ void __launch_bounds__(kGvThreads + (FETCH ? 32 * kGvFetchWarps : 0), 1) gemv_q4_kernel(GemmArgs p) {
+  static_assert(!FETCH || KIND == 0, "the gate/up launch fetches both components");
   using C = CfgV;
   static_assert(kGvGroups % BPT == 0, "groups");
   constexpr int G = kGvGroups / BPT;               // K-step groups
@@ -148,6 +155,9 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + C::kNumBars);
   int* prefix = const_cast<int*>(reinterpret_cast<volatile int*>(misc + 4));
   int* soff = prefix + (kMaxE + 1);
+  int* eord = soff + (kMaxE + 1);                                   // FETCH: tile order
+  uint32_t* mbits = reinterpret_cast<uint32_t*>(eord + kMaxE);      // FETCH: experts being fetched
+  uint32_t* mseen = mbits + kMaxE / 32;                             // FETCH: placed in the order
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -175,7 +185,66 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
   GemmArgs ps = p;  // the schedule counts tiles of RT rows
   ps.mblocks = p.mblocks / BPT;
   const int total = build_schedule<kGvRows>(ps, false, E, prefix, soff);
-  const Sched sc{prefix, soff, E, ps.mblocks, kGvRows};
+  Sched sc{prefix, soff, E, ps.mblocks, kGvRows};
+  const int nmiss = FETCH ? min(max(p.stats[1], 0), min(E, p.S)) : 0;
+  if constexpr (FETCH) {
+    // The experts being fetched come last in the tile order (in plan order),
+    // so that no CTA holds resident work behind a tile that waits for the
+    // link; the prefix is recomputed over that order.
+    for (int i = threadIdx.x; i < (E + 31) / 32; i += blockDim.x) {
+      mbits[i] = 0u;
+      mseen[i] = 0u;
+    }
+    __syncthreads();
+    for (int m = threadIdx.x; m < nmiss; m += blockDim.x) {
+      const int e = p.miss_list[m];
+      if (e >= 0 && e < E) atomicOr(&mbits[e >> 5], 1u << (e & 31));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int run = 0;
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const bool keep = e < E && !((mbits[e0 >> 5] >> lane) & 1u);
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (keep) eord[run + __popc(bal & ((1u << lane) - 1u))] = e;
+        run += __popc(bal);
+      }
+      // then the fetched ones in plan order, each once (an ID outside
+      // [0, E) is flagged by the fetch warps and left out here): the
+      // resident ones and these make up every expert exactly once
+      if (lane == 0) {
+        for (int m = 0; m < nmiss; ++m) {
+          const int e = p.miss_list[m];
+          if (e < 0 || e >= E || ((mseen[e >> 5] >> (e & 31)) & 1u)) continue;
+          mseen[e >> 5] |= 1u << (e & 31);
+          if (run < E) eord[run++] = e;
+        }
+      }
+      __syncwarp();
+      int running = 0;
+      for (int j0 = 0; j0 < E; j0 += 32) {
+        const int j = j0 + lane;
+        int n = 0;
+        if (j < E) {
+          const int e = eord[j];
+          n = max(soff[e + 1] - soff[e], 0);
+        }
+        const int tiles = ((n + kGvRows - 1) / kGvRows) * ps.mblocks;
+        int incl = tiles;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += y;
+        }
+        if (j < E) prefix[j] = running + incl - tiles;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) prefix[E] = running;
+    }
+    __syncthreads();
+    sc.order = eord;
+  }
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ packed chunk producer
@@ -196,6 +265,35 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
           set_status(p.status, MOE_DEV_CACHE_FULL);
           rec = 0;
         }
+      }
+      if (FETCH && ((mbits[tl.e >> 5] >> (tl.e & 31)) & 1u)) {
+        // a fetched expert: wait until the pieces of the tile's blocks have
+        // landed in its slot (bounded)
+        const int target = p.ksteps / p.cpp;
+        for (int bb = 0; bb < BPT && ok; ++bb) {
+          const int* word = p.fsync + 2 + tl.e * p.mblocks + BPT * tl.mb + bb;
+          uint64_t t0 = 0;
+          for (uint32_t it = 0; ld_acquire_gpu(word) < target; ++it) {
+            __nanosleep(64);
+            if ((it & 1023u) == 1023u) {
+              if (misc[1]) {
+                ok = false;
+                break;
+              }
+              const uint64_t now = globaltimer_ns();
+              if (t0 == 0) {
+                t0 = now;
+              } else if (now - t0 > kWaitNs) {
+                misc[1] = 1;
+                set_status(p.status, MOE_DEV_TIMEOUT);
+                ok = false;
+                break;
+              }
+            }
+          }
+        }
+        if (!ok) break;
+        fence_proxy_async_global();
       }
       for (int ks = 0; ks < p.ksteps; ks += QG) {
         if (!wait_bounded<kSpin>(qempty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
@@ -301,6 +399,53 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
     if (lane == 0 && (!ok || misc[1])) {
       for (int q = 0; q < 2; ++q)
         if ((armed_mask >> q) & 1u) wait_drain(xland0 + 8 * q, (armed_ph >> q) & 1u);
+    }
+  } else if (FETCH && warp >= kGvWarps) {
+    // ---------------------------------------------------------- fetch
+    // Each warp claims the next piece of the plan: every gate/up piece of
+    // the misses (in plan order), then every down piece; copies it host ->
+    // slot with eight 16-byte loads in flight per lane, fences for the bulk
+    // copies of other CTAs, and counts a gate/up piece as landed in its
+    // block's word.
+    const int nblk = p.mblocks;
+    const int ppb = p.ksteps / p.cpp;                       // pieces per gate/up block
+    const int pg = nblk * ppb;                              // pieces per gate/up record
+    const int pd = static_cast<int>((p.rec_dn + kGvFetchBytes - 1) / kGvFetchBytes);
+    const int totalp = nmiss * (pg + pd);
+    for (;;) {
+      int qi = 0;
+      if (lane == 0) qi = atomicAdd(p.fsync, 1);
+      qi = __shfl_sync(0xffffffffu, qi, 0);
+      if (qi >= totalp || misc[1]) break;
+      const bool gu = qi < nmiss * pg;
+      const int m = gu ? qi / pg : (qi - nmiss * pg) / pd;
+      const int c = gu ? qi % pg : (qi - nmiss * pg) % pd;
+      const int e = p.miss_list[m], sl = p.miss_slot[m];
+      const bool valid = e >= 0 && e < E && sl >= 0 && sl < p.S;
+      if (valid) {
+        const size_t rec = gu ? p.rec_gu : p.rec_dn;
+        const size_t off = gu ? static_cast<size_t>(c) * p.cpp * kQChunk : static_cast<size_t>(c) * kGvFetchBytes;
+        const size_t len = gu ? static_cast<size_t>(p.cpp) * kQChunk : min(rec - off, size_t(kGvFetchBytes));
+        const int nv = static_cast<int>(len / 16);
+        const uint4* src = reinterpret_cast<const uint4*>((gu ? p.host_gu : p.host_dn) + e * rec + off);
+        uint4* dst = reinterpret_cast<uint4*>((gu ? const_cast<uint8_t*>(p.tiles) : p.pool_dn) + sl * rec + off);
+        constexpr int U = 8;
+        for (int i0 = lane; i0 < nv; i0 += U * 32) {
+          uint4 v[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (i0 + u * 32 < nv) v[u] = src[i0 + u * 32];
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (i0 + u * 32 < nv) dst[i0 + u * 32] = v[u];
+        }
+        fence_proxy_async_global();
+      } else if (lane == 0) {
+        set_status(p.status, MOE_DEV_BAD_EXPERT);
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && valid && gu) atomicAdd(p.fsync + 2 + e * nblk + c / ppb, 1);
     }
   } else if (warp >= 2) {
     // ---------------------------------------------------------- compute
@@ -481,16 +626,46 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_q4_kernel(GemmArgs p) {
     }
   }
   __syncthreads();
+  if constexpr (FETCH) {
+    // the last CTA out resets the piece queue, the exit count and the landed
+    // counts of the fetched experts for the next call
+    if (threadIdx.x == 0) {
+      __threadfence();
+      misc[2] = atomicAdd(p.fsync + 1, 1) == static_cast<int>(gridDim.x) - 1;
+    }
+    __syncthreads();
+    if (misc[2]) {
+      __threadfence();
+      for (int i = threadIdx.x; i < nmiss * p.mblocks; i += blockDim.x) {
+        const int e = p.miss_list[i / p.mblocks];
+        if (e >= 0 && e < E) p.fsync[2 + e * p.mblocks + i % p.mblocks] = 0;
+      }
+      if (threadIdx.x == 0) {
+        p.fsync[0] = 0;
+        p.fsync[1] = 0;
+      }
+      __threadfence();
+    }
+  }
 }
 
-template <int KIND, int QG, int BPT>
+template <int KIND, int QG, int BPT, bool FETCH = false>
 cudaError_t run_gemv_q4_g(const GemmArgs& args, cudaStream_t st) {
-  auto kern = gemv_q4_kernel<KIND, QG, BPT>;
+  auto kern = gemv_q4_kernel<KIND, QG, BPT, FETCH>;
   cudaError_t e = ensure_smem(kern, CfgV::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = sm_count();
   if (grid <= 0) return cudaErrorNoDevice;
-  return launch_pdl(kern, dim3(grid), dim3(kGvThreads), CfgV::kSmemBytes, st, args);
+  return launch_pdl(kern, dim3(grid), dim3(kGvThreads + (FETCH ? 32 * kGvFetchWarps : 0)), CfgV::kSmemBytes, st,
+                    args);
+}
+
+// Gate/up with the in-launch fetch: the same tile shapes as run_gemv_q4<0>.
+cudaError_t run_gemv_q4_fetch(const GemmArgs& args, cudaStream_t st) {
+  const bool even = args.ksteps % 2 == 0;
+  if (args.mblocks % 2 == 0 && args.ksteps % 4 == 0) return run_gemv_q4_g<0, 4, 2, true>(args, st);
+  if (args.ksteps % 4 == 0) return run_gemv_q4_g<0, 4, 1, true>(args, st);
+  return even ? run_gemv_q4_g<0, 2, 1, true>(args, st) : run_gemv_q4_g<0, 1, 1, true>(args, st);
 }
 
 // A ring slot holds as many consecutive K steps as divide the record's
@@ -520,6 +695,7 @@ bool use_gemv_q4(int fmt, int R, int K) {
 }
 
 cudaError_t launch_gemv_q4(int kind, const GemmArgs& args, cudaStream_t st) {
+  if (kind == 0 && args.host_gu != nullptr) return run_gemv_q4_fetch(args, st);
   return kind == 1 ? run_gemv_q4<1>(args, st) : run_gemv_q4<0>(args, st);
 }
 

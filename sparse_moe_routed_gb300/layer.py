@@ -289,15 +289,15 @@ class CachedMoELayer(MoELayer):
     S slots of HBM hold recently used experts.  Each call plans hits and
     misses on the device (moe_cache_plan) and then either fetches the misses
     in the expert launch itself, in waves of `wave` experts while the
-    resident experts compute (fetch="wave", bf16 records), or copies them
-    first with moe_cache_fetch and computes after (fetch="barrier"; int4
-    records, whose misses move 2,611,200 B each at the Qwen4Exp shape
-    against 9,830,400 B in bf16, always take this path).  Outputs are
-    bit-identical to MoELayer over the same records in HBM.
+    resident experts compute (fetch="wave"), or copies them first with
+    moe_cache_fetch and computes after (fetch="barrier").  int4 records move
+    2,611,200 B per miss at the Qwen4Exp shape against 9,830,400 B in bf16;
+    their in-launch fetch is done by the gate/up launch for both components.
+    Outputs are bit-identical to MoELayer over the same records in HBM.
 
         moe_route -> moe_permute -> moe_cache_plan [-> moe_cache_fetch] ->
-        moe_expert_swiglu_cached (bf16) | moe_expert_int4_slots x 2 (int4)
-        -> moe_combine
+        moe_expert_swiglu_cached (bf16) | moe_expert_int4_fetch or
+        moe_expert_int4_slots, then moe_expert_int4_slots (int4) -> moe_combine
 
     stats [4] int32 on the device: {hits, misses} of the last call and their
     running totals.  policy: "fifo", "lru" or "score" (moe_cache_plan), decay
@@ -314,8 +314,6 @@ class CachedMoELayer(MoELayer):
         assert not host_gateup.is_cuda and host_gateup.is_pinned() and host_down.is_pinned()
         assert fetch in ("wave", "barrier") and policy in self.POLICIES
         assert fmt in (_lib.MOE_W_BF16_TILED, _lib.MOE_W_INT4_G64_TILED)
-        if fmt == _lib.MOE_W_INT4_G64_TILED:
-            fetch = "barrier"
         self.policy, self.decay = self.POLICIES[policy], float(decay)
         super().__init__(w_router, bias, host_gateup, host_down, k, T_max, fmt=fmt, I=I)
         E, H = self.E, self.H
@@ -345,16 +343,25 @@ class CachedMoELayer(MoELayer):
         self.stats.zero_()
 
     def _two_launch_expert_calls(self, lib, P, R, st):
-        # int4 records: plan, copy the misses into their slots, then the
-        # int4 contraction reads every expert from its slot
+        # int4 records: plan, then either the gate/up launch fetches the
+        # misses of both components while the resident experts compute
+        # (wave), or the misses are copied first (barrier); the int4
+        # contraction reads every expert from its slot
         E, H, I, S = self.E, self.H, self.I, self.S
-        calls = self._plan_calls(lib, P, st, fetch_first=True)
-        calls += [("moe_expert_int4_slots", lib.moe_expert_int4_slots,
-                   (0, P(self.x_perm), P(self.offsets), R, E, H, I, P(self.pool_gu), S, P(self.slot_of), P(self.h),
-                    P(self.status), st)),
-                  ("moe_expert_int4_slots", lib.moe_expert_int4_slots,
-                   (1, P(self.h), P(self.offsets), R, E, H, I, P(self.pool_dn), S, P(self.slot_of), P(self.y_perm),
-                    P(self.status), st))]
+        wave = self.fetch == "wave"
+        calls = self._plan_calls(lib, P, st, fetch_first=not wave)
+        if wave:
+            calls.append(("moe_expert_int4_fetch", lib.moe_expert_int4_fetch,
+                          (P(self.x_perm), P(self.offsets), R, E, H, I, P(self.pool_gu), P(self.pool_dn), S,
+                           P(self.slot_of), P(self.w_gateup), P(self.w_down), P(self.miss_list), P(self.miss_slot),
+                           P(self.stats), P(self.h), P(self.sync_ws), P(self.status), st)))
+        else:
+            calls.append(("moe_expert_int4_slots", lib.moe_expert_int4_slots,
+                          (0, P(self.x_perm), P(self.offsets), R, E, H, I, P(self.pool_gu), S, P(self.slot_of),
+                           P(self.h), P(self.status), st)))
+        calls.append(("moe_expert_int4_slots", lib.moe_expert_int4_slots,
+                      (1, P(self.h), P(self.offsets), R, E, H, I, P(self.pool_dn), S, P(self.slot_of), P(self.y_perm),
+                       P(self.status), st)))
         return calls
 
     def _plan_calls(self, lib, P, st, fetch_first):

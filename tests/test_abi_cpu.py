@@ -26,10 +26,10 @@ def lib():
 def test_library_loads_and_exports_every_declared_symbol():
     L = lib()
     names = _lib.declared_functions()
-    assert len(names) == 28
+    assert len(names) == 29
     for n in names:
         assert hasattr(L, n), n
-    assert L.moe_abi_version() == 102
+    assert L.moe_abi_version() == 103
     assert L.moe_status_str(0).decode() == "MOE_OK"
     assert L.moe_status_str(5).decode().startswith("MOE_ENOTSUP")
 
@@ -283,6 +283,30 @@ def test_int4_slots_rejections():
     assert call(R=0) == _lib.MOE_OK
     # a prefill-sized launch is not the decode GEMV's: rejected before any launch
     assert call(R=40960) == _lib.MOE_ENOTSUP
+
+
+def test_int4_fetch_rejections():
+    L = lib()
+    # x_perm, offsets, R, E, H, I, pool_gu, pool_dn, S, slot_of, host_gu, host_dn, miss_list, miss_slot, stats,
+    # h, sync_ws, dev_status, stream
+    base = [P, P, 160, 512, 2560, 640, P, P, 160, P, P, P, P, P, P, P, P, P, NUL]
+    names = ["xp", "off", "R", "E", "H", "I", "pgu", "pdn", "S", "slot", "hgu", "hdn", "ml", "ms", "stats", "h",
+             "sync", "st"]
+
+    def call(**kw):
+        a = list(base)
+        for n, v in kw.items():
+            a[names.index(n)] = v
+        return L.moe_expert_int4_fetch(*a)
+
+    assert call(hgu=NUL) == _lib.MOE_EINVAL
+    assert call(hdn=PM) == _lib.MOE_EINVAL
+    assert call(ml=NUL) == _lib.MOE_EINVAL
+    assert call(sync=NUL) == _lib.MOE_EWORKSPACE
+    assert call(S=0) == _lib.MOE_ESHAPE
+    assert call(S=2048) == _lib.MOE_ENOTSUP
+    assert call(R=40960) == _lib.MOE_ENOTSUP      # decode-sized launches only
+    assert call(R=0) == _lib.MOE_OK
 
 
 def test_route_permute_rejections():

@@ -271,8 +271,9 @@ def int4_layers(cfg):
     return _Q[cfg.name]
 
 
-@pytest.mark.parametrize("policy", ["fifo", "lru"])
-def test_cached_int4_layer_bitwise_and_against_oracle(policy):
+@pytest.mark.parametrize("policy,fetch", [("fifo", "barrier"), ("lru", "barrier"), ("fifo", "wave"),
+                                          ("lru", "wave")])
+def test_cached_int4_layer_bitwise_and_against_oracle(policy, fetch):
     """int4 g64 records in host memory behind 24 HBM slots (4 tokens x 4 routes
     per call, so a call always fits): every call of a
     sequence with hits, misses and evictions equals, bit for bit, the
@@ -282,7 +283,7 @@ def test_cached_int4_layer_bitwise_and_against_oracle(policy):
     cfg = INT4_SMALL
     ref, hgu, hdn, d, raw = int4_layers(cfg)
     lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, cfg.T, I=cfg.I, S=24, policy=policy,
-                         fmt=_lib.MOE_W_INT4_G64_TILED)
+                         fetch=fetch, fmt=_lib.MOE_W_INT4_G64_TILED)
     assert lay.rec_gu + lay.rec_dn == 3 * cfg.H * cfg.I // 2 + 3 * cfg.H * cfg.I // 64 * 2
     uniq = 0
     for i in range(10):
@@ -303,6 +304,27 @@ def test_cached_int4_layer_bitwise_and_against_oracle(policy):
             assert_output_close(got.float().cpu().numpy()[keep], moe, what=f"cached int4 call {i}")
     s = lay.stats.cpu().tolist()
     assert s[2] > 0 and s[3] > 24 and s[2] + s[3] == uniq
+    assert int(lay.sync_ws.abs().sum().item()) == 0
+
+
+def test_cached_int4_qwen_geometry_in_launch_fetch():
+    """The Qwen4Exp expert shape (H 2,560, I 640: 40 K steps, pieces of eight
+    chunks) over 64 experts and 40 slots, misses fetched in the gate/up launch:
+    bit-identical to the resident int4 layer call after call."""
+    cfg = wl.LayerConfig("cache_int4_qwen", T=4, H=2560, E=64, k=10, I=640, bias=None, seed=25)
+    ref, hgu, hdn, d, raw = int4_layers(cfg)
+    lay = CachedMoELayer(d["w_router"], d["bias"], hgu, hdn, cfg.k, cfg.T, I=cfg.I, S=40, fetch="wave",
+                         fmt=_lib.MOE_W_INT4_G64_TILED)
+    for i in range(8):
+        x = wl.token_batch(cfg, DEV, index=[0, 1, 0, 2, 3, 1, 4, 0][i], T=cfg.T)
+        want = ref.forward(x).clone()
+        got = lay.forward(x).clone()
+        torch.cuda.synchronize()
+        assert lay.read_status() == 0 and ref.read_status() == 0
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"call {i}"
+    s = lay.stats.cpu().tolist()
+    assert s[2] > 0 and s[3] > 40
+    assert int(lay.sync_ws.abs().sum().item()) == 0
 
 
 def test_int4_slots_flag_an_expert_without_a_slot():
