@@ -72,6 +72,8 @@ def parse():
     ap.add_argument("--plain", action="store_true",
                     help="stream bf16 weights from the plain record layout through TMA tensor maps "
                          "instead of the tile-packed records")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="decode: leave out the other workloads' short runs (other_configs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -322,6 +324,65 @@ def main():
         return run_crossover(args, rank, world, local, dev)
     if args.config == "sidecar":
         return run_sidecar(args, rank, world, local, dev)
+    line = run_layer(args, rank, world, local, dev)
+    if args.config == "decode" and world == 1 and not args.no_extra:
+        line["other_configs"] = other_configs(args, rank, world, local, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def sub_args(args, **over):
+    """A copy of the command line for one of the other workloads' runs."""
+    import copy
+    sub = copy.copy(args)
+    sub.layers, sub.experts, sub.tokens, sub.plain = 0, 0, 0, False
+    sub.no_cpu_baseline, sub.no_e2e, sub.no_extra = True, True, True
+    for k, v in over.items():
+        setattr(sub, k, v)
+    return sub
+
+
+def other_configs(args, rank, world, local, dev):
+    """Short runs of the prefill layer (T = 4,096 and the compute-bound point
+    T = 32,768), the int4 48-layer stack and the route sweep, so that the
+    default line carries a measurement of every workload: the same code
+    paths and timing as their own --config runs, with fewer steps."""
+    import torch
+    out = {}
+    runs = [("prefill", lambda: run_layer(sub_args(args, config="prefill", steps=10, warmup=3), rank, world, local,
+                                          dev)),
+            ("prefill_T32768", lambda: run_layer(sub_args(args, config="prefill", tokens=32768, steps=5, warmup=3),
+                                                 rank, world, local, dev)),
+            ("stack48_and_sweep", lambda: run_stack(sub_args(args, config="stack48", steps=5, warmup=3), rank, world,
+                                                    local, dev, emit=False, with_sweep=True))]
+    keep = ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "config", "roofline", "roofline_other",
+            "layer_roofline", "clocks", "gpu_launches", "sweep", "device_status", "dtype")
+    for name, fn in runs:
+        try:
+            res = fn()
+        except Exception as e:  # report the failure of one extra run, keep the line
+            out[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+            continue
+        for key, line in (res.items() if name == "stack48_and_sweep" else [(name, res)]):
+            out[key] = {k: line[k] for k in keep if k in line}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_layer(args, rank, world, local, dev):
+    """One layer workload (decode or prefill) through the C ABI; returns the
+    JSON line."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import workloads as wl
+    from sparse_moe_routed_gb300 import MoELayer, _lib, pack_layer_experts
+
     cfg = wl.CONFIGS[args.config]
     if args.experts:
         from dataclasses import replace
@@ -563,15 +624,10 @@ def main():
         # launch gathers); experts (fused: one launch; else gate/up, down, combine)
         "gpu_launches": launches_per_step * K,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
-    return 0
+    return line
 
 
-def run_stack(args, rank, world, local, dev):
+def run_stack(args, rank, world, local, dev, emit=True, with_sweep=False):
     """48-layer int4 g64 residual stack over 32 decode blocks of 16 tokens
     (stack48), or the route-prediction / dedup sweep over it (sweep)."""
     import torch
@@ -583,7 +639,8 @@ def run_stack(args, rank, world, local, dev):
     cfg = wl.STACK48
     L = args.layers or wl.STACK_LAYERS
     NB = wl.STACK_BLOCKS
-    T = cfg.T if args.config == "stack48" else NB * cfg.T
+    sweep_too = args.config == "sweep" or with_sweep
+    T = NB * cfg.T if sweep_too else cfg.T  # layers sized for the sweep's 512 tokens serve 16-token blocks too
     mls = []
     for l in range(L):
         w = wl.stack_layer_weights(l, dev)
@@ -598,7 +655,10 @@ def run_stack(args, rank, world, local, dev):
     rec_bytes = 2 * cfg.I * cfg.H // 2 + cfg.H * cfg.I // 2 + (2 * cfg.I * cfg.H // 64 + cfg.H * cfg.I // 64) * 2
     router_bytes = cfg.E * cfg.H * 2
 
-    if args.config == "sweep":
+    T_sweep = T
+
+    def sweep_line():
+        T = T_sweep
         preds = [wl.predictor_weights(cfg.H, cfg.E, l, dev) for l in range(L)]
         x0 = torch.cat([wl.token_batch(cfg, dev, index=b, T=cfg.T) for b in range(NB)]).float()
         for _ in range(max(args.warmup, 1)):
@@ -614,10 +674,15 @@ def run_stack(args, rank, world, local, dev):
                 "vs_baseline": None, "dtype": "int4 g64 experts, bf16 router", "data": "synthetic",
                 "config": {"workload": f"route_sweep_L{L}_T{T}_blocks1-4-16-64", "layers": L, "tokens": T},
                 "sweep": res["summary"], "device_status": res["status"]}
-        if rank == 0:
-            print(json.dumps(line), flush=True)
-        return 0
+        return line
 
+    if args.config == "sweep":
+        line = sweep_line()
+        if rank == 0 and emit:
+            print(json.dumps(line), flush=True)
+        return 0 if emit else {"sweep": line}
+
+    T = cfg.T  # stack48: blocks of 16 tokens
     xs = [wl.token_batch(cfg, dev, index=b, T=T).float() for b in range(NB)]
     xw = torch.empty_like(xs[0])
     for i in range(max(args.warmup, 3)):
@@ -713,12 +778,17 @@ def run_stack(args, rank, world, local, dev):
             # per layer: RMSNorm 1, route 2 (logits, selection), permute 2
             # (grouping, row gather), gate/up 1, down 1, combine 1
             "clocks": sampler.summary(tw0, tw1), "gpu_launches": 8 * L * K}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
-    return 0
+    if emit:
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+    out = {"stack48": line}
+    if with_sweep:
+        out["sweep"] = sweep_line()
+    return out
 
 
 def run_offload(args, rank, world, local, dev):
