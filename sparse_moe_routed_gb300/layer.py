@@ -260,6 +260,69 @@ class MoELayer:
         done.record()
         return done
 
+    def forward_host_pipelined(self, x_host, out_host):
+        """forward_host_submit with the two copies off the compute stream.
+
+        The host-to-device copy of x runs on a copy stream into one of two
+        device input buffers, the layer's launches (a CUDA graph per buffer
+        pair, captured once) on the current stream after that copy, and the
+        copy of the result back on a second copy stream, so that a call's
+        input copy overlaps the previous call's compute and its result copy
+        the next call's.  Returns an event that completes once out_host holds
+        the result; until then the caller leaves x_host and out_host alone.
+        Calls run their layer work in order on the current stream.
+        """
+        T = x_host.shape[0]
+        st = self.__dict__.get("_pipe")
+        if st is None or st["T"] != T:
+            dev = self.w_router.device
+            st = {"T": T, "n": 0,
+                  "h2d": torch.cuda.Stream(device=dev), "d2h": torch.cuda.Stream(device=dev),
+                  # zero-filled: the first call's eager pass (before the capture) reads them
+                  "x": [torch.zeros((T, self.H), dtype=torch.bfloat16, device=dev) for _ in range(2)],
+                  "out": [torch.empty((T, self.H), dtype=torch.bfloat16, device=dev) for _ in range(2)],
+                  "x_ready": [torch.cuda.Event() for _ in range(2)],
+                  "layer_done": [torch.cuda.Event() for _ in range(2)],
+                  "out_free": [torch.cuda.Event() for _ in range(2)],
+                  "graphs": [None, None]}
+            for b in range(2):
+                st["layer_done"][b].record()
+                st["out_free"][b].record()
+            self._pipe = st
+        b = st["n"] & 1
+        st["n"] += 1
+        cur = torch.cuda.current_stream()
+        if st["graphs"][b] is None:
+            s = torch.cuda.Stream(device=cur.device)
+            s.wait_stream(cur)
+            with torch.cuda.stream(s):  # one eager pass: first-call set-up stays out of the capture
+                self.forward(st["x"][b], out=st["out"][b], stream=s)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                self.forward(st["x"][b], out=st["out"][b], stream=s)
+            st["graphs"][b] = g
+        # input copy, once the layer that last read this buffer is done
+        h2d = st["h2d"]
+        h2d.wait_event(st["layer_done"][b])
+        with torch.cuda.stream(h2d):
+            st["x"][b].copy_(x_host, non_blocking=True)
+        st["x_ready"][b].record(h2d)
+        # the layer, once its input has landed and its output buffer is free
+        cur.wait_event(st["x_ready"][b])
+        cur.wait_event(st["out_free"][b])
+        st["graphs"][b].replay()
+        st["layer_done"][b].record(cur)
+        # the result copy
+        d2h = st["d2h"]
+        d2h.wait_event(st["layer_done"][b])
+        with torch.cuda.stream(d2h):
+            out_host.copy_(st["out"][b], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(d2h)
+        st["out_free"][b].record(d2h)
+        return done
+
     @staticmethod
     def wait(done):
         """Block until a call returned by forward_host_submit has finished."""

@@ -443,6 +443,34 @@ def test_forward_host_submit_two_in_flight():
     assert all(l.read_status() == 0 for l in layers)
 
 
+@pytest.mark.parametrize("nlayers", [1, 2])
+def test_forward_host_pipelined_two_in_flight(nlayers):
+    """The pipelined host round trip (input copy on a copy stream, the layer's
+    graph on the compute stream, the result copy on another copy stream,
+    alternating device buffers) gives the eager layer's bits for every call,
+    with the next call queued before the previous one is waited for."""
+    cfg, d, _ = case("decode")
+    gu, dn = pack_layer_experts(d["w_gateup"], d["w_down"], _lib.MOE_W_BF16, cfg.E, cfg.H, cfg.I)
+    layers = [MoELayer(d["w_router"], d["bias"], gu, dn, cfg.k, cfg.T, fmt=_lib.MOE_W_BF16_TILED, I=cfg.I)
+              for _ in range(nlayers)]
+    xs = [wl.token_batch(cfg, DEV, index=80 + i) for i in range(7)]
+    refs = [layers[0].forward(x).clone().cpu() for x in xs]
+    torch.cuda.synchronize()
+    x_host = [torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    out_host = [torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    prev = None
+    for i, x in enumerate(xs):
+        x_host[i % 2].copy_(x.cpu())
+        done = layers[i % nlayers].forward_host_pipelined(x_host[i % 2], out_host[i % 2])
+        if prev is not None:
+            MoELayer.wait(prev[0])
+            assert torch.equal(out_host[prev[1] % 2].view(torch.int16), refs[prev[1]].view(torch.int16)), prev[1]
+        prev = (done, i)
+    MoELayer.wait(prev[0])
+    assert torch.equal(out_host[prev[1] % 2].view(torch.int16), refs[prev[1]].view(torch.int16))
+    assert all(l.read_status() == 0 for l in layers)
+
+
 @pytest.mark.parametrize("tiled", [False, True])
 def test_layer_single_token_and_empty(tiled):
     cfg, d, host = case("tiny")
