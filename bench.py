@@ -453,7 +453,7 @@ def run_layer(args, rank, world, local, dev):
     fused = "moe_expert_swiglu_fused" in names or weighted
     # kernels each boundary call launches in this configuration
     per_call = {"moe_route": 2, "moe_route_permute": 1, "moe_permute": 1 if R <= MoELayer.GATHER_IN_FUSED_MAX_ROWS
-                and fused else 2, "moe_permute_gather": 2, "moe_expert_swiglu_fused": 1, "moe_expert_gateup": 1,
+                and fused else 2, "moe_permute_ws": 4, "moe_permute_gather": 2, "moe_expert_swiglu_fused": 1, "moe_expert_gateup": 1,
                 "moe_expert_down": 1, "moe_combine": 1, "moe_expert_swiglu_fused_weighted": 1,
                 "moe_combine_weighted": 1}
     launches_per_step = sum(per_call[n] for n in names)

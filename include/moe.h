@@ -146,11 +146,34 @@ MOE_API moe_status moe_route_noalloc(const uint16_t *x, const uint16_t *w_router
  *   x_perm[s,:] = x[perm[s] / k, :]  if x_perm != NULL          [R,H] bf16 (out)
  * x may be NULL only when x_perm is NULL.  An ID outside [0,E) sets
  * MOE_DEV_BAD_EXPERT in *dev_status (required, 4 bytes) and the kernel then
- * writes none of counts/offsets/perm/inv_perm/x_perm.
+ * writes none of counts/offsets/perm/inv_perm/x_perm.  The row gather also
+ * writes nothing while *dev_status holds MOE_DEV_BAD_EXPERT from an earlier
+ * call (the word is sticky until the caller clears it).
  * ------------------------------------------------------------------------- */
 MOE_API moe_status moe_permute(const int32_t *topk_ids, int T, int k, int E, const uint16_t *x, int H,
                        int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
                        uint16_t *x_perm, int32_t *dev_status, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_permute_ws -- moe_permute for large route counts, on many CTAs.
+ *
+ * Source: as moe_permute.  Arguments, outputs, dev_status and the result are
+ * exactly those of moe_permute (bit for bit: the slot order is fixed by the
+ * definition).  The routes are cut into chunks of 2,048; one launch counts
+ * each chunk's routes per expert, one CTA scans the counts into offsets and
+ * each chunk's per-expert start, and one launch scatters every chunk.
+ * workspace: device, 16-byte aligned, at least moe_permute_workspace_size(T,
+ * k, E) bytes, owned by the caller, contents on entry do not matter; it must
+ * not be used by another call in flight at the same time.  NULL or too small:
+ * MOE_EWORKSPACE; misaligned: MOE_EINVAL.  An ID outside [0,E) sets
+ * MOE_DEV_BAD_EXPERT and then none of counts/offsets/perm/inv_perm/x_perm
+ * is written.
+ * ------------------------------------------------------------------------- */
+MOE_API size_t moe_permute_workspace_size(int T, int k, int E);
+MOE_API moe_status moe_permute_ws(const int32_t *topk_ids, int T, int k, int E, const uint16_t *x, int H,
+                                  int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                                  uint16_t *x_perm, void *workspace, size_t workspace_bytes,
+                                  int32_t *dev_status, void *stream);
 
 /* ---------------------------------------------------------------------------
  * moe_route_permute -- moe_route followed by moe_permute (without the row

@@ -58,6 +58,8 @@ def load(path: str | None = None):
             "moe_route": ([p, p, p, i, i, i, i, p, p, p, p, sz, p], i),
             "moe_route_noalloc": ([p, p, p, i, i, i, i, p, p, p, p], i),
             "moe_permute": ([p, i, i, i, p, i, p, p, p, p, p, p, p], i),
+            "moe_permute_workspace_size": ([i, i, i], sz),
+            "moe_permute_ws": ([p, i, i, i, p, i, p, p, p, p, p, p, sz, p, p], i),
             "moe_expert_gateup": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
             "moe_expert_down": ([p, p, i, i, i, i, i, p, p, p, p, p], i),
             "moe_grouped_swiglu": ([p, p, i, i, i, i, i, p, p, p, p, p, p, p, p], i),
@@ -148,6 +150,20 @@ def moe_permute(topk_ids, E, x, counts, offsets, perm, inv_perm, x_perm, dev_sta
     st = load().moe_permute(_ptr(topk_ids), T, k, E, _ptr(x), H, _ptr(counts), _ptr(offsets), _ptr(perm),
                             _ptr(inv_perm), _ptr(x_perm), _ptr(dev_status), _stream(stream))
     _check("moe_permute", st)
+
+
+def moe_permute_workspace_size(T, k, E):
+    return load().moe_permute_workspace_size(T, k, E)
+
+
+def moe_permute_ws(topk_ids, E, x, counts, offsets, perm, inv_perm, x_perm, workspace, dev_status, stream=None):
+    T, k = topk_ids.shape
+    H = x.shape[1] if x is not None else 0
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().moe_permute_ws(_ptr(topk_ids), T, k, E, _ptr(x), H, _ptr(counts), _ptr(offsets), _ptr(perm),
+                               _ptr(inv_perm), _ptr(x_perm), _ptr(workspace), nbytes, _ptr(dev_status),
+                               _stream(stream))
+    _check("moe_permute_ws", st)
 
 
 def moe_expert_gateup(x_perm, offsets, E, H, I, w_gateup, h, dev_status, fmt=MOE_W_BF16, s_gateup=None,

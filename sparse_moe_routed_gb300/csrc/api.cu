@@ -68,7 +68,7 @@ inline moe_status check_geometry(int H, int E, int k, int I_or_zero) {
 
 extern "C" {
 
-int moe_abi_version(void) { return 103; }
+int moe_abi_version(void) { return 104; }
 
 const char* moe_status_str(moe_status s) {
   switch (s) {
@@ -159,7 +159,42 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, const uint1
   cudaError_t e = moe::launch_permute(topk_ids, R, k, E, counts, offsets, perm, inv_perm, dev_status, st);
   if (e != cudaSuccess) return MOE_ECUDA;
   if (x_perm) {
-    e = moe::launch_gather_rows(x, perm, R, k, T, H, x_perm, st);
+    e = moe::launch_gather_rows(x, inv_perm, R, k, T, H, x_perm, dev_status, st);
+    if (e != cudaSuccess) return MOE_ECUDA;
+  }
+  return MOE_OK;
+}
+
+size_t moe_permute_workspace_size(int T, int k, int E) {
+  if (T <= 0 || k <= 0 || E <= 0) return 0;
+  return moe::permute_chunked_ws_bytes(T * k, E);
+}
+
+moe_status moe_permute_ws(const int32_t* topk_ids, int T, int k, int E, const uint16_t* x, int H, int32_t* counts,
+                          int32_t* offsets, int32_t* perm, int32_t* inv_perm, uint16_t* x_perm, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (T < 0 || k <= 0 || E <= 0) return MOE_ESHAPE;
+  if (k > moe::kMaxK || k > E || E > moe::kMaxE) return MOE_ENOTSUP;
+  if (static_cast<long long>(T) * k >= (1LL << 31)) return MOE_ENOTSUP;
+  if (!topk_ids || !counts || !offsets || !perm || !inv_perm || !dev_status) return MOE_EINVAL;
+  if (!a4(topk_ids) || !a4(counts) || !a4(offsets) || !a4(perm) || !a4(inv_perm) || !a4(dev_status))
+    return MOE_EINVAL;
+  if (x_perm) {
+    if (!x) return MOE_EINVAL;
+    if (H <= 0) return MOE_ESHAPE;
+    if (H % 128 != 0 || H > 16384) return MOE_ENOTSUP;
+    if (!a16(x) || !a16(x_perm)) return MOE_EINVAL;
+  }
+  if (T == 0) return MOE_OK;
+  if (!workspace || !a16(workspace)) return workspace ? MOE_EINVAL : MOE_EWORKSPACE;
+  if (workspace_bytes < moe_permute_workspace_size(T, k, E)) return MOE_EWORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int R = T * k;
+  cudaError_t e = moe::launch_permute_chunked(topk_ids, R, E, counts, offsets, perm, inv_perm,
+                                              static_cast<int32_t*>(workspace), dev_status, st);
+  if (e != cudaSuccess) return MOE_ECUDA;
+  if (x_perm) {
+    e = moe::launch_gather_rows(x, inv_perm, R, k, T, H, x_perm, dev_status, st);
     if (e != cudaSuccess) return MOE_ECUDA;
   }
   return MOE_OK;

@@ -27,7 +27,8 @@ namespace moe {
 
 namespace {
 
-constexpr int kCombineThreads = 128;  // x 4 floats = 512 columns per CTA
+constexpr int kCombineThreads = 128;  // x 4 floats = 512 columns per CTA (fp32 rows)
+constexpr int kCombineBatch = 8;      // rows whose loads a thread has in flight
 
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const float* __restrict__ w, int T,
@@ -51,18 +52,30 @@ __global__ void __launch_bounds__(kCombineThreads)
   if (c4 * 4 >= H) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   bool bad = false;
-  for (int j = 0; j < k; ++j) {
-    const int s = slot[j];
-    if (s < 0) {
-      bad = true;
-      continue;
+  // kCombineBatch rows' loads in flight, then their terms in j order
+  for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
+    float4 v[kCombineBatch];
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      const int s = j0 + u < k ? slot[j0 + u] : -1;
+      v[u] = s >= 0 ? reinterpret_cast<const float4*>(y + static_cast<size_t>(s) * H)[c4]
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float4 v = reinterpret_cast<const float4*>(y + static_cast<size_t>(s) * H)[c4];
-    const float wj = wt[j];
-    acc.x = fmaf(wj, v.x, acc.x);
-    acc.y = fmaf(wj, v.y, acc.y);
-    acc.z = fmaf(wj, v.z, acc.z);
-    acc.w = fmaf(wj, v.w, acc.w);
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      const int j = j0 + u;
+      if (j < k) {
+        if (slot[j] < 0) {
+          bad = true;
+        } else {
+          const float wj = wt[j];
+          acc.x = fmaf(wj, v[u].x, acc.x);
+          acc.y = fmaf(wj, v[u].y, acc.y);
+          acc.z = fmaf(wj, v[u].z, acc.z);
+          acc.w = fmaf(wj, v[u].w, acc.w);
+        }
+      }
+    }
   }
   if (residual) {
     const float4 r = reinterpret_cast<const float4*>(residual + static_cast<size_t>(t) * H)[c4];
@@ -84,8 +97,8 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 // The same sum over expert outputs that the down epilogue already multiplied
 // by their route weights and stored in bf16 (yw [R, H]): acc = sum_j
-// yw[inv[t*k + j]] in j order, fp32.  Four columns per thread (one 8-byte
-// load per row), 512 columns per CTA.
+// yw[inv[t*k + j]] in j order, fp32.  Eight columns per thread (one 16-byte
+// load per row, kCombineBatch rows in flight), 1,024 columns per CTA.
 __global__ void __launch_bounds__(kCombineThreads)
     combine_weighted_kernel(const uint16_t* __restrict__ yw, const int32_t* __restrict__ inv, int T, int k, int H,
                             int R, const float* residual, uint16_t* __restrict__ out_bf16, float* out_f32,
@@ -100,37 +113,64 @@ __global__ void __launch_bounds__(kCombineThreads)
     slot[threadIdx.x] = s;
   }
   __syncthreads();
-  const int c4 = blockIdx.x * kCombineThreads + threadIdx.x;
-  if (c4 * 4 >= H) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int c8 = blockIdx.x * kCombineThreads + threadIdx.x;
+  if (c8 * 8 >= H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   bool bad = false;
-  for (int j = 0; j < k; ++j) {
-    const int s = slot[j];
-    if (s < 0) {
-      bad = true;
-      continue;
+  for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
+    uint4 v[kCombineBatch];
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      const int s = j0 + u < k ? slot[j0 + u] : -1;
+      v[u] = s >= 0 ? reinterpret_cast<const uint4*>(yw + static_cast<size_t>(s) * H)[c8] : make_uint4(0, 0, 0, 0);
     }
-    const uint2 v = reinterpret_cast<const uint2*>(yw + static_cast<size_t>(s) * H)[c4];
-    acc.x += bf16_to_f32(static_cast<uint16_t>(v.x & 0xffffu));
-    acc.y += bf16_to_f32(static_cast<uint16_t>(v.x >> 16));
-    acc.z += bf16_to_f32(static_cast<uint16_t>(v.y & 0xffffu));
-    acc.w += bf16_to_f32(static_cast<uint16_t>(v.y >> 16));
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      const int j = j0 + u;
+      if (j < k) {
+        if (slot[j] < 0) {
+          bad = true;
+        } else {
+          const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += bf16_to_f32(static_cast<uint16_t>(w4[i] & 0xffffu));
+            acc[2 * i + 1] += bf16_to_f32(static_cast<uint16_t>(w4[i] >> 16));
+          }
+        }
+      }
+    }
   }
   if (residual) {
-    const float4 r = reinterpret_cast<const float4*>(residual + static_cast<size_t>(t) * H)[c4];
-    acc.x += r.x;
-    acc.y += r.y;
-    acc.z += r.z;
-    acc.w += r.w;
+    const float4* rr = reinterpret_cast<const float4*>(residual + static_cast<size_t>(t) * H) + 2 * c8;
+    const float4 r0 = rr[0], r1 = rr[1];
+    acc[0] += r0.x;
+    acc[1] += r0.y;
+    acc[2] += r0.z;
+    acc[3] += r0.w;
+    acc[4] += r1.x;
+    acc[5] += r1.y;
+    acc[6] += r1.z;
+    acc[7] += r1.w;
   }
-  if (status && (bad || !isfinite(acc.x) || !isfinite(acc.y) || !isfinite(acc.z) || !isfinite(acc.w)))
-    set_status(status, bad ? MOE_DEV_BAD_EXPERT : MOE_DEV_NONFINITE);
-  if (out_f32) reinterpret_cast<float4*>(out_f32 + static_cast<size_t>(t) * H)[c4] = acc;
+  bool fin = true;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) fin = fin && isfinite(acc[i]);
+  if (status && (bad || !fin)) set_status(status, bad ? MOE_DEV_BAD_EXPERT : MOE_DEV_NONFINITE);
+  if (out_f32) {
+    float4* o = reinterpret_cast<float4*>(out_f32 + static_cast<size_t>(t) * H) + 2 * c8;
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
   if (out_bf16) {
-    uint2 pk;
-    pk.x = static_cast<uint32_t>(f32_to_bf16(acc.x)) | (static_cast<uint32_t>(f32_to_bf16(acc.y)) << 16);
-    pk.y = static_cast<uint32_t>(f32_to_bf16(acc.z)) | (static_cast<uint32_t>(f32_to_bf16(acc.w)) << 16);
-    reinterpret_cast<uint2*>(out_bf16 + static_cast<size_t>(t) * H)[c4] = pk;
+    uint4 pk;
+    pk.x = static_cast<uint32_t>(f32_to_bf16(acc[0])) | (static_cast<uint32_t>(f32_to_bf16(acc[1])) << 16);
+    pk.y = static_cast<uint32_t>(f32_to_bf16(acc[2])) | (static_cast<uint32_t>(f32_to_bf16(acc[3])) << 16);
+    pk.z = static_cast<uint32_t>(f32_to_bf16(acc[4])) | (static_cast<uint32_t>(f32_to_bf16(acc[5])) << 16);
+    pk.w = static_cast<uint32_t>(f32_to_bf16(acc[6])) | (static_cast<uint32_t>(f32_to_bf16(acc[7])) << 16);
+    reinterpret_cast<uint4*>(out_bf16 + static_cast<size_t>(t) * H)[c8] = pk;
   }
 }
 
@@ -215,7 +255,7 @@ cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, i
 cudaError_t launch_combine_weighted(const uint16_t* yw, const int32_t* inv, int T, int k, int H, int R,
                                     const float* residual, uint16_t* out_bf16, float* out_f32, int32_t* st_word,
                                     cudaStream_t st) {
-  const dim3 grid((H / 4 + kCombineThreads - 1) / kCombineThreads, T);
+  const dim3 grid((H / 8 + kCombineThreads - 1) / kCombineThreads, T);
   return launch_pdl(combine_weighted_kernel, grid, dim3(kCombineThreads), 0, st, yw, inv, T, k, H, R, residual,
                     out_bf16, out_f32, st_word);
 }

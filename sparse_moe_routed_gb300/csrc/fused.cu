@@ -80,7 +80,9 @@ struct FusedArgs {
 };
 
 constexpr int kFetchWarps = 4;
-constexpr int kFusedDynamicRows = 4096;  // launches up to this many rows claim tiles dynamically
+// launches up to this many rows, and every launch of 256-row token tiles,
+// claim tiles dynamically
+constexpr int kFusedDynamicRows = 4096;
 constexpr int kFetchChunk = 32768;
 // launches of at least this many routes per expert (on average) take
 // 256-row token tiles
@@ -221,7 +223,8 @@ struct FOrder {
 // tiles.  A CTA that finishes early takes the next tile, so the CTAs end
 // within about one tile of each other whatever bandwidth each one sees (the
 // static order leaves a spread of several microseconds at the end of a
-// decode launch); on large launches the static order measured faster.  A down tile waits for the gate/up
+// decode launch); on large launches of 128-row tiles the static order
+// measured faster, on 256-row tiles the queue.  A down tile waits for the gate/up
 // tiles of its expert, which all come earlier in the queue and wait for
 // nothing, so every wait ends.  With an expert cache the order is: the
 // resident experts' gate/up tiles, their down tiles, then the fetched
@@ -446,7 +449,11 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
   const int jB = E - nmiss;  // first position of a fetched expert
   const int tguA = pre_gu[jB], tdnA = pre_dn[jB], tguB = total_gu - tguA;
   int* const queue = p.ready + E + 2;  // device-wide tile queue
-  const bool dynamic = p.R <= kFusedDynamicRows;
+  // 256-row tiles: an expert's rows span several chunks that read the same
+  // weight tiles; claimed from the queue, the tiles of one expert run at
+  // nearly the same time on different SMs and share those weights in L2
+  // (the static order lets the CTAs drift apart and re-read them from HBM)
+  const bool dynamic = p.R <= kFusedDynamicRows || NMAX == 256;
   const FSeq seq1(blockIdx.x, gridDim.x, total_gu, pre_dn[E], p.ks_gu, p.ks_dn);
   const FOrder seq2(blockIdx.x, gridDim.x, tguA, tdnA, tguB, pre_dn[E] - tdnA, p.ks_gu, p.ks_dn);
   // the MMA issuer and the epilogue warps follow the producer's tile ids
@@ -481,7 +488,10 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol_w = ptx::policy_evict_first();
+    // weights: read once when the expert's rows fit one tile, else once per
+    // row chunk (kept in L2 for the other chunks' tiles)
+    const uint64_t pol_w1 = ptx::policy_evict_first();
+    const uint64_t pol_wn = ptx::policy_evict_normal();
     const uint64_t pol_x = ptx::policy_evict_last();
     int armed[S];
 #pragma unroll
@@ -613,6 +623,7 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       }
       const int rec = CACHED ? sslot[tl.e] : tl.e;
       const size_t chunk0 = (static_cast<size_t>(rec) * (tl.kind ? p.mb_dn : p.mb_gu) + tl.mb) * KS;
+      const uint64_t pol_w = soff[tl.e + 1] - soff[tl.e] > NMAX ? pol_wn : pol_w1;
       for (int ks = 0; ks < KS; ks += G) {
         if (!wait_bounded<kSpin>(empty0 + 8 * s, ph ^ 1u, misc + 1, p.status)) {
           ok = false;

@@ -41,11 +41,15 @@ int permute_warps(int R, int E) {
   return std::min(kWarps, std::min(w_rows, w_smem));
 }
 
-__global__ void __launch_bounds__(kWarps * 32, 1)
-    permute_kernel(const int32_t* __restrict__ ids, int R, int E, int W, int32_t* __restrict__ counts,
-                   int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                   int32_t* status) {
-  extern __shared__ int32_t sh[];
+// Groups routes [rb, re) of ids in one CTA of up to kWarps warps.  ext ==
+// nullptr: the CTA owns all R routes (rb = 0, re = R) and writes counts and
+// offsets.  ext != nullptr: a chunk of a larger grouping; ext[e] is where
+// this chunk's routes of expert e start (the counts of earlier chunks added
+// to offsets[e]), and counts / offsets are left to the chunk scan.
+__device__ __forceinline__ void group_range(const int32_t* __restrict__ ids, int rb, int re, int R, int E, int W,
+                                            int32_t* sh, const int32_t* ext, int32_t* __restrict__ counts,
+                                            int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                                            int32_t* __restrict__ inv, int32_t* status) {
   int32_t* hist = sh;                                            // [W][E]
   int32_t* base = sh + W * E;                                    // [E]
   unsigned* lmask = reinterpret_cast<unsigned*>(base + E);       // [W][E]
@@ -59,13 +63,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     lmask[i] = 0u;
   }
   if (tid == 0) bad = 0;
-  pdl_wait();
-  pdl_trigger();
   __syncthreads();
 
-  const int per = (R + W - 1) / W;
-  const int r0 = (warp < W) ? min(R, warp * per) : R;
-  const int r1 = (warp < W) ? min(R, r0 + per) : R;
+  const int n = re - rb;
+  const int per = (n + W - 1) / W;
+  const int r0 = (warp < W) ? min(re, rb + warp * per) : re;
+  const int r1 = (warp < W) ? min(re, r0 + per) : re;
   int32_t* my_hist = hist + min(warp, W - 1) * E;
   unsigned* my_mask = lmask + min(warp, W - 1) * E;
 
@@ -96,6 +99,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   }
 
   // pass 2: per-expert prefix over warps, then an exclusive scan over experts
+  // (or, for a chunk, the chunk's given starts)
   for (int e = tid; e < E; e += blockDim.x) {
     int s = 0;
     for (int w = 0; w < W; ++w) {
@@ -103,9 +107,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       hist[w * E + e] = s;
       s += c;
     }
-    base[e] = s;
+    base[e] = ext != nullptr ? ext[e] : s;
   }
   __syncthreads();
+  if (ext == nullptr) {
   // E <= 1024 = blockDim.x: one expert per thread
   const int c = (tid < E) ? base[tid] : 0;
   int incl = c;
@@ -135,6 +140,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   }
   if (tid == 0) offsets[E] = R;
   __syncthreads();
+  }
 
   // pass 3: stable scatter (every ID is valid here)
   for (int b = r0; b < r1; b += 32 * kUnroll) {
@@ -169,21 +175,160 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   }
 }
 
-__global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int R, int k,
-                                   int T, int H, uint16_t* __restrict__ xp) {
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    permute_kernel(const int32_t* __restrict__ ids, int R, int E, int W, int32_t* __restrict__ counts,
+                   int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                   int32_t* status) {
+  extern __shared__ int32_t sh[];
   pdl_wait();
   pdl_trigger();
-  const int vpr = H / 8;
-  const size_t n = static_cast<size_t>(R) * vpr;
-  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n;
-       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const int s = static_cast<int>(idx / vpr);
-    const int c = static_cast<int>(idx - static_cast<size_t>(s) * vpr);
-    const int r = perm[s];
-    if (r < 0 || r >= R) continue;  // routing rejected upstream: leave the row alone
-    const int t = r / k;
-    if (t >= T) continue;
-    reinterpret_cast<uint4*>(xp)[idx] = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H)[c];
+  group_range(ids, 0, R, R, E, W, sh, nullptr, counts, offsets, perm, inv, status);
+}
+
+// Large route counts: chunks of kChunk routes on C CTAs.  Workspace: [C][E]
+// int32 (each chunk's counts, then where its routes of each expert start),
+// [C] bad-ID flags, then one word that tells the scatter to write nothing.
+constexpr int kChunk = 2048;
+
+__global__ void __launch_bounds__(1024) chunk_count_kernel(const int32_t* __restrict__ ids, int R, int E,
+                                                           int32_t* __restrict__ ws) {
+  __shared__ int32_t hist[kMaxE];
+  __shared__ int bad;
+  const int c = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  if (threadIdx.x == 0) bad = 0;
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();
+  const int rb = c * kChunk, re = min(R, rb + kChunk);
+  for (int r = rb + threadIdx.x; r < re; r += blockDim.x) {
+    const int e = ids[r];
+    if (e < 0 || e >= E) {
+      bad = 1;
+    } else {
+      atomicAdd(&hist[e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) ws[static_cast<size_t>(c) * E + e] = hist[e];
+  if (threadIdx.x == 0) ws[static_cast<size_t>(gridDim.x) * E + c] = bad;
+}
+
+// One CTA: counts, offsets (exclusive scan over experts) and, per chunk and
+// expert, where the chunk's routes start; a bad ID anywhere writes nothing.
+__global__ void __launch_bounds__(1024) chunk_scan_kernel(int R, int E, int C, int32_t* __restrict__ ws,
+                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                          int32_t* status) {
+  __shared__ int warp_tot[32];
+  __shared__ int anybad;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) anybad = 0;
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();
+  for (int c = tid; c < C; c += blockDim.x)
+    if (ws[static_cast<size_t>(C) * E + c]) anybad = 1;
+  __syncthreads();
+  if (anybad) {
+    if (tid == 0) {
+      set_status(status, MOE_DEV_BAD_EXPERT);
+      ws[static_cast<size_t>(C) * E + C] = 1;
+    }
+    return;
+  }
+  int tot = 0;
+  if (tid < E)
+    for (int c = 0; c < C; ++c) tot += ws[static_cast<size_t>(c) * E + tid];
+  int incl = tot;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int wt = warp_tot[lane];
+    int wi = wt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, d);
+      if (lane >= d) wi += y;
+    }
+    warp_tot[lane] = wi - wt;
+  }
+  __syncthreads();
+  if (tid < E) {
+    int run = warp_tot[warp] + incl - tot;  // offsets[e]
+    counts[tid] = tot;
+    offsets[tid] = run;
+    for (int c = 0; c < C; ++c) {
+      const size_t i = static_cast<size_t>(c) * E + tid;
+      const int v = ws[i];
+      ws[i] = run;
+      run += v;
+    }
+  }
+  if (tid == 0) {
+    offsets[E] = R;
+    ws[static_cast<size_t>(C) * E + C] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    chunk_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int W, const int32_t* __restrict__ ws,
+                         int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* status) {
+  extern __shared__ int32_t sh[];
+  pdl_wait();
+  pdl_trigger();
+  const int C = gridDim.x;
+  if (ws[static_cast<size_t>(C) * E + C]) return;  // a bad ID: nothing is written
+  const int c = blockIdx.x;
+  group_range(ids, c * kChunk, min(R, (c + 1) * kChunk), R, E, W, sh, ws + static_cast<size_t>(c) * E, nullptr,
+              nullptr, perm, inv, status);
+}
+
+// Rows of x into slot order, one warp per token: the warp reads the token's
+// k slots (inv), then moves the row in pieces of 32 x kGatherVec 16-byte
+// vectors, each piece loaded once and stored to all k slots.  x is read once
+// in token order, and every x_perm row is written once.  After a grouping
+// that met a bad expert ID inv was not written, so nothing is gathered.
+constexpr int kGatherThreads = 256;
+constexpr int kGatherVec = 8;  // 16-byte vectors in flight per lane
+
+__global__ void __launch_bounds__(kGatherThreads)
+    gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ inv, int R, int k, int T, int H,
+                       uint16_t* __restrict__ xp, const int32_t* st_word) {
+  pdl_wait();
+  pdl_trigger();
+  if (*reinterpret_cast<const volatile int32_t*>(st_word) & MOE_DEV_BAD_EXPERT) return;
+  const int lane = threadIdx.x & 31;
+  const int wpb = kGatherThreads / 32;
+  const int stride = gridDim.x * wpb;
+  const int vpr = H / 8;  // 16-byte vectors per row
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += stride) {
+    // lane j < k holds the slot of route (t, j); out of range: left alone
+    int my = lane < k ? inv[static_cast<size_t>(t) * k + lane] : -1;
+    if (my < 0 || my >= R) my = -1;
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    for (int c0 = 0; c0 < vpr; c0 += 32 * kGatherVec) {
+      uint4 v[kGatherVec];
+#pragma unroll
+      for (int u = 0; u < kGatherVec; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < vpr) v[u] = src[c];
+      }
+      for (int j = 0; j < k; ++j) {
+        const int s = __shfl_sync(0xffffffffu, my, j);
+        if (s < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(s) * H);
+#pragma unroll
+        for (int u = 0; u < kGatherVec; ++u) {
+          const int c = c0 + u * 32 + lane;
+          if (c < vpr) dst[c] = v[u];
+        }
+      }
+    }
   }
 }
 
@@ -200,16 +345,36 @@ cudaError_t launch_permute(const int32_t* ids, int R, int k, int E, int32_t* cou
                     st_word);
 }
 
-cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int R, int k, int T, int H, uint16_t* x_perm,
-                               cudaStream_t st) {
-  const size_t n = static_cast<size_t>(R) * (H / 8);
-  const int threads = 256;
-  size_t blocks = (n + threads - 1) / threads;
+size_t permute_chunked_ws_bytes(int R, int E) {
+  const size_t C = (static_cast<size_t>(R) + kChunk - 1) / kChunk;
+  return ((C * E + C + 1) * sizeof(int32_t) + 255) / 256 * 256;
+}
+
+cudaError_t launch_permute_chunked(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                   int32_t* inv, int32_t* ws, int32_t* st_word, cudaStream_t st) {
+  const int C = (R + kChunk - 1) / kChunk;
+  cudaError_t e = launch_pdl(chunk_count_kernel, dim3(C), dim3(1024), 0, st, ids, R, E, ws);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(chunk_scan_kernel, dim3(1), dim3(1024), 0, st, R, E, C, ws, counts, offsets, st_word);
+  if (e != cudaSuccess) return e;
+  const int W = permute_warps(kChunk, E);
+  const size_t smem = static_cast<size_t>(2 * W + 1) * E * sizeof(int32_t);
+  e = ensure_smem(chunk_scatter_kernel, kPermuteSmem + 4 * kMaxE);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(chunk_scatter_kernel, dim3(C), dim3(kWarps * 32), smem, st, ids, R, E, W, ws, perm, inv,
+                    st_word);
+}
+
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* inv, int R, int k, int T, int H, uint16_t* x_perm,
+                               const int32_t* st_word, cudaStream_t st) {
+  if (k > 32) return cudaErrorInvalidValue;  // one lane per route of a token
+  const int wpb = kGatherThreads / 32;
+  size_t blocks = (static_cast<size_t>(T) + wpb - 1) / wpb;
   const size_t cap = static_cast<size_t>(sm_count() > 0 ? sm_count() : 148) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks == 0) blocks = 1;
-  return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, x, perm, R, k, T,
-                    H, x_perm);
+  return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kGatherThreads), 0, st, x, inv,
+                    R, k, T, H, x_perm, st_word);
 }
 
 }  // namespace moe

@@ -45,6 +45,9 @@ class MoELayer:
     # bf16 rows already multiplied by their route weights (half the bytes of
     # fp32 rows, written once and read once by the combine)
     WEIGHTED_Y_MIN_ROWS = 4097
+    # from this many routes the grouping runs in chunks on many CTAs
+    # (moe_permute_ws); below it one CTA does it in one launch
+    PERMUTE_CHUNKED_MIN_ROWS = 8192
     WEIGHTED_Y = True
 
     def __init__(self, w_router, bias, w_gateup, w_down, k: int, T_max: int, fmt: int = _lib.MOE_W_BF16,
@@ -71,7 +74,9 @@ class MoELayer:
         self.ids = torch.empty((T_max, k), dtype=torch.int32, device=dev)
         self.w = torch.empty((T_max, k), dtype=torch.float32, device=dev)
         self.gap = torch.empty((T_max,), dtype=torch.float32, device=dev)
-        ws = _lib.route_workspace_size(T_max, E)
+        # one workspace for the router's logits and, later in the chain, the
+        # chunked grouping's per-chunk counts
+        ws = max(_lib.route_workspace_size(T_max, E), _lib.moe_permute_workspace_size(T_max, k, E))
         self.ws = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev)
         self.counts = torch.empty((E,), dtype=torch.int32, device=dev)
         self.offsets = torch.empty((E + 1,), dtype=torch.int32, device=dev)
@@ -133,7 +138,12 @@ class MoELayer:
         # (a decode block); for many rows moe_permute's gather runs at full
         # occupancy instead
         gather_in_fused = self.fused and R <= self.GATHER_IN_FUSED_MAX_ROWS
-        if not route_and_group:
+        if not route_and_group and R >= self.PERMUTE_CHUNKED_MIN_ROWS:
+            calls.append(("moe_permute_ws", lib.moe_permute_ws,
+                          (P(self.ids), T, k, E, None if gather_in_fused else P(x), H, P(self.counts),
+                           P(self.offsets), P(self.perm), P(self.inv),
+                           None if gather_in_fused else P(self.x_perm), P(self.ws), ws_bytes, P(self.status), st)))
+        elif not route_and_group:
             calls.append(("moe_permute", lib.moe_permute,
                           (P(self.ids), T, k, E, None if gather_in_fused else P(x), H, P(self.counts),
                            P(self.offsets), P(self.perm), P(self.inv),

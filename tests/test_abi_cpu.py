@@ -26,10 +26,10 @@ def lib():
 def test_library_loads_and_exports_every_declared_symbol():
     L = lib()
     names = _lib.declared_functions()
-    assert len(names) == 29
+    assert len(names) == 31
     for n in names:
         assert hasattr(L, n), n
-    assert L.moe_abi_version() == 103
+    assert L.moe_abi_version() == 104
     assert L.moe_status_str(0).decode() == "MOE_OK"
     assert L.moe_status_str(5).decode().startswith("MOE_ENOTSUP")
 
@@ -115,6 +115,44 @@ def _permute(**kw):
 ])
 def test_permute_rejections(kw, code):
     assert _permute(**kw) == code
+
+
+def _permute_ws(**kw):
+    a = dict(ids=P, T=4096, k=10, E=512, x=P, H=2560, counts=P, offsets=P, perm=P, inv=P, xp=P, ws=P,
+             wsb=1 << 20, st=P)
+    a.update(kw)
+    return lib().moe_permute_ws(a["ids"], a["T"], a["k"], a["E"], a["x"], a["H"], a["counts"], a["offsets"],
+                                a["perm"], a["inv"], a["xp"], a["ws"], a["wsb"], a["st"], NUL)
+
+
+def test_permute_workspace_size():
+    L = lib()
+    # 20 chunks of 2,048 routes: [20][512] counts, 20 flags, one abort word
+    assert L.moe_permute_workspace_size(4096, 10, 512) == (20 * 512 + 20 + 1) * 4 // 256 * 256 + 256
+    assert L.moe_permute_workspace_size(1, 1, 1) == 256
+    assert L.moe_permute_workspace_size(0, 10, 512) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ids=NUL), _lib.MOE_EINVAL),
+    (dict(st=NUL), _lib.MOE_EINVAL),
+    (dict(x=NUL), _lib.MOE_EINVAL),
+    (dict(xp=PM), _lib.MOE_EINVAL),
+    (dict(ws=NUL), _lib.MOE_EWORKSPACE),
+    (dict(ws=PM), _lib.MOE_EINVAL),
+    (dict(wsb=1024), _lib.MOE_EWORKSPACE),
+    (dict(T=-3), _lib.MOE_ESHAPE),
+    (dict(k=11, E=10), _lib.MOE_ENOTSUP),
+    (dict(H=100), _lib.MOE_ENOTSUP),
+    (dict(E=2048), _lib.MOE_ENOTSUP),
+    (dict(T=1 << 28, k=10), _lib.MOE_ENOTSUP),
+])
+def test_permute_ws_rejections(kw, code):
+    assert _permute_ws(**kw) == code
+
+
+def test_permute_ws_zero_tokens_is_noop():
+    assert _permute_ws(T=0, ws=NUL, wsb=0) == _lib.MOE_OK
 
 
 def _gateup(**kw):

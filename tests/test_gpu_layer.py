@@ -193,10 +193,25 @@ def seeded_ids(T, k, E, seed, zipf=False):
     return np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
 
 
-@pytest.mark.parametrize("T,k,E,H,zipf", [(1, 4, 64, 256, False), (16, 10, 512, 2560, True),
-                                         (37, 10, 512, 2560, False), (4096, 10, 512, 2560, False),
-                                         (300, 32, 1024, 128, False), (64, 8, 8, 128, False)])
-def test_permute_bit_exact(T, k, E, H, zipf):
+PERMUTE_CASES = [(1, 4, 64, 256, False), (16, 10, 512, 2560, True), (37, 10, 512, 2560, False),
+                 (4096, 10, 512, 2560, False), (300, 32, 1024, 128, False), (64, 8, 8, 128, False),
+                 (8191, 10, 512, 128, True), (32768, 10, 512, 128, False)]
+
+
+def permute_call(chunked, ids, E, x, counts, offsets, perm, inv, xp, st):
+    """moe_permute (one CTA) or moe_permute_ws (chunks on many CTAs): the
+    same outputs bit for bit."""
+    if not chunked:
+        _lib.moe_permute(ids, E, x, counts, offsets, perm, inv, xp, st)
+        return
+    T, k = ids.shape
+    ws = torch.full((_lib.moe_permute_workspace_size(T, k, E) // 4,), -3, dtype=torch.int32, device=DEV)
+    _lib.moe_permute_ws(ids, E, x, counts, offsets, perm, inv, xp, ws, st)
+
+
+@pytest.mark.parametrize("chunked", [False, True])
+@pytest.mark.parametrize("T,k,E,H,zipf", PERMUTE_CASES)
+def test_permute_bit_exact(T, k, E, H, zipf, chunked):
     ids_np = seeded_ids(T, k, E, seed=T * 7 + E, zipf=zipf)
     counts_r, offsets_r, perm_r, inv_r = oracle.permute(ids_np, E)
     R = T * k
@@ -208,7 +223,7 @@ def test_permute_bit_exact(T, k, E, H, zipf):
     inv = torch.full((R,), -7, dtype=torch.int32, device=DEV)
     xp = torch.zeros((R, H), dtype=torch.bfloat16, device=DEV)
     st = torch.zeros((1,), dtype=torch.int32, device=DEV)
-    _lib.moe_permute(ids, E, x, counts, offsets, perm, inv, xp, st)
+    permute_call(chunked, ids, E, x, counts, offsets, perm, inv, xp, st)
     torch.cuda.synchronize()
     assert st.item() == 0
     assert np.array_equal(counts.cpu().numpy(), counts_r)
@@ -219,23 +234,32 @@ def test_permute_bit_exact(T, k, E, H, zipf):
     assert np.array_equal(bits(xp), xb[perm_r // k])
 
 
-def test_permute_bad_id_flags_and_writes_nothing():
-    T, k, E = 8, 4, 16
+@pytest.mark.parametrize("chunked,T,bad_t", [(False, 8, 5), (True, 8, 5), (True, 3000, 1), (True, 3000, 2999)])
+def test_permute_bad_id_flags_and_writes_nothing(chunked, T, bad_t):
+    k, E = 4, 16
     ids_np = seeded_ids(T, k, E, 3)
-    ids_np[5, 2] = E  # out of range
+    ids_np[bad_t, 2] = E  # out of range (first or last of several chunks)
     R = T * k
     ids = torch.from_numpy(ids_np).to(DEV)
     sentinel = -12345
     counts = torch.full((E,), sentinel, dtype=torch.int32, device=DEV)
     offsets = torch.full((E + 1,), sentinel, dtype=torch.int32, device=DEV)
-    perm = torch.full((R,), sentinel, dtype=torch.int32, device=DEV)
-    inv = torch.full((R,), sentinel, dtype=torch.int32, device=DEV)
+    # perm and inv hold valid entries from an earlier call: the row gather
+    # must not follow them
+    perm = torch.arange(R, dtype=torch.int32, device=DEV)
+    inv = torch.arange(R, dtype=torch.int32, device=DEV)
     st = torch.zeros((1,), dtype=torch.int32, device=DEV)
-    _lib.moe_permute(ids, E, None, counts, offsets, perm, inv, None, st)
+    H = 128
+    x = torch.randn((T, H), device=DEV).to(torch.bfloat16)
+    xp = torch.full((R, H), 7.0, dtype=torch.bfloat16, device=DEV)
+    permute_call(chunked, ids, E, x, counts, offsets, perm, inv, xp, st)
     torch.cuda.synchronize()
     assert st.item() & _lib.MOE_DEV_BAD_EXPERT
-    for t in (counts, offsets, perm, inv):
+    for t in (counts, offsets):
         assert bool((t == sentinel).all())
+    assert torch.equal(perm.cpu(), torch.arange(R, dtype=torch.int32))
+    assert torch.equal(inv.cpu(), torch.arange(R, dtype=torch.int32))
+    assert bool((xp == 7.0).all())
 
 
 # --------------------------------------------------------------------------
