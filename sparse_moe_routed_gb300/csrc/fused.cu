@@ -287,6 +287,92 @@ __device__ __forceinline__ void fetch_records(const FusedArgs& p, int E, int n, 
   }
 }
 
+// The in-launch row gather of a decode-sized launch: this CTA's contiguous
+// share of the permuted token rows (x_perm[s] = x[perm[s] / k]), eight
+// 16-byte loads in flight per thread, by the 128 epilogue threads (et = 0 ..
+// 127); then fenced for the async proxy and counted once per CTA, so that
+// the producers can start their token-row loads once every CTA has counted.
+__device__ __forceinline__ void gather_share(const FusedArgs& p, int E, int et) {
+  constexpr int kEpiThreads = 128;
+  const int s0 = static_cast<int>(static_cast<long long>(p.R) * blockIdx.x / gridDim.x);
+  const int s1 = static_cast<int>(static_cast<long long>(p.R) * (blockIdx.x + 1) / gridDim.x);
+  const int vpr = p.H / 8;
+  const int n = (s1 - s0) * vpr;
+  constexpr int U = 8;
+  for (int i0 = et; i0 < n; i0 += U * kEpiThreads) {
+    uint4 v[U];
+    int dst[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * kEpiThreads;
+      dst[u] = -1;
+      if (i < n) {
+        const int sl = s0 + i / vpr;
+        const int c = i - (sl - s0) * vpr;
+        const int r = p.perm[sl];
+        if (r >= 0 && r < p.R) {
+          v[u] = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(r / p.k) * p.H)[c];
+          dst[u] = sl * vpr + c;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (dst[u] >= 0) reinterpret_cast<uint4*>(p.x_perm)[dst[u]] = v[u];
+  }
+  fence_proxy_async_global();
+  __threadfence();
+  asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
+  if (et == 0) atomicAdd(p.ready + E + 1, 1);
+}
+
+// Tile counts per position of the expert order: pre_gu[j] / pre_dn[j] =
+// the gate/up / down tiles of the experts before position j (one warp).
+// Each lane sums a run of consecutive positions, one warp scan places the
+// runs, and each lane writes its run's prefixes.
+template <int NMAX, bool CACHED>
+__device__ __forceinline__ void tile_prefix(const FusedArgs& p, int E, const int* soff, const int* eord, int* pre_gu,
+                                            int* pre_dn, int lane) {
+  const int per = (E + 31) / 32;
+  const int j0 = min(E, lane * per), j1 = min(E, j0 + per);
+  auto chunks = [&](int j) {
+    const int e = CACHED ? eord[j] : j;
+    return (max(soff[e + 1] - soff[e], 0) + NMAX - 1) / NMAX;
+  };
+  int c = 0;
+  for (int j = j0; j < j1; ++j) c += chunks(j);
+  int incl = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  int run = incl - c;
+  for (int j = j0; j < j1; ++j) {
+    pre_gu[j] = run * p.mb_gu;
+    pre_dn[j] = run * p.mb_dn;
+    run += chunks(j);
+  }
+  if (lane == 0) {
+    pre_gu[E] = total * p.mb_gu;
+    pre_dn[E] = total * p.mb_dn;
+  }
+}
+
+// One CTA's check-out from the launch's sync words (one thread): once every
+// CTA has checked out, no producer will read them and no epilogue will count
+// in them again, so the CTA that checks out last zeroes them for the next
+// launch.
+__device__ __forceinline__ void sync_words_check_out(const FusedArgs& p, int E) {
+  __threadfence();
+  if (atomicAdd(p.ready + E, 1) == static_cast<int>(gridDim.x) - 1) {
+    __threadfence();
+    for (int e = 0; e < E + 3; ++e) p.ready[e] = 0;
+    __threadfence();
+  }
+}
+
 template <int NMAX, int GG, bool CACHED>
 __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0), 1)
     grouped_swiglu_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmH,
@@ -347,6 +433,7 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       ptx::mbar_init(tqe0 + 8 * q, 1 + 4);
     }
     misc[1] = 0;
+    misc[3] = 0;  // uncached: roles done with the sync words (producer + 4 epilogue warps)
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmX);
     ptx::prefetch_tmap(&tmH);
@@ -363,6 +450,23 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     // The fetch warps start at once; the compute warps' set-up below syncs
     // on a named barrier of their own.
     fetch_records(p, E, nmiss, lane);
+  } else {
+  if constexpr (!CACHED) {
+    // The epilogue warps gather the token rows at once while warps 0 and 1
+    // read the segment offsets and build the tile prefix (named barrier 3);
+    // then warps 0 and 1 arrive on barrier 4, where the epilogue warps wait.
+    if (warp >= 2) {
+      if (p.x != nullptr) gather_share(p, E, threadIdx.x - 64);
+      asm volatile("bar.sync 4, %0;" ::"n"(kCoreThreads) : "memory");
+    } else {
+      for (int i = threadIdx.x; i <= E; i += 64) soff[i] = min(max(p.offsets[i], 0), p.R);
+      asm volatile("bar.sync 3, 64;" ::: "memory");
+      if (warp == 0) tile_prefix<NMAX, CACHED>(p, E, soff, eord, pre_gu, pre_dn, lane);
+      ptx::tc_fence_before();
+      asm volatile("bar.sync 3, 64;" ::: "memory");
+      asm volatile("bar.arrive 4, %0;" ::"n"(kCoreThreads) : "memory");
+    }
+    ptx::tc_fence_after();
   } else {
   for (int i = threadIdx.x; i <= E; i += kCoreThreads) soff[i] = min(max(p.offsets[i], 0), p.R);
   if constexpr (CACHED) {
@@ -407,42 +511,12 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       }
       __syncwarp();
     }
-    int run_gu = 0, run_dn = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int j = e0 + lane;
-      int n = 0;
-      if (j < E) {
-        const int e = CACHED ? eord[j] : j;
-        n = max(soff[e + 1] - soff[e], 0);
-      }
-      const int chunks = (n + NMAX - 1) / NMAX;
-      int a = chunks * p.mb_gu, b = chunks * p.mb_dn;
-      int ia = a, ib = b;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int ya = __shfl_up_sync(0xffffffffu, ia, d);
-        const int yb = __shfl_up_sync(0xffffffffu, ib, d);
-        if (lane >= d) {
-          ia += ya;
-          ib += yb;
-        }
-      }
-      __syncwarp();
-      if (j < E) {
-        pre_gu[j] = run_gu + ia - a;
-        pre_dn[j] = run_dn + ib - b;
-      }
-      run_gu += __shfl_sync(0xffffffffu, ia, 31);
-      run_dn += __shfl_sync(0xffffffffu, ib, 31);
-    }
-    if (lane == 0) {
-      pre_gu[E] = run_gu;
-      pre_dn[E] = run_dn;
-    }
+    tile_prefix<NMAX, CACHED>(p, E, soff, eord, pre_gu, pre_dn, lane);
   }
   ptx::tc_fence_before();
   compute_sync();
   ptx::tc_fence_after();
+  }
   const uint32_t tmem_base = misc[0];
   const int total_gu = pre_gu[E];
   const int total = total_gu + pre_dn[E];
@@ -456,6 +530,14 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
   const bool dynamic = p.R <= kFusedDynamicRows || NMAX == 256;
   const FSeq seq1(blockIdx.x, gridDim.x, total_gu, pre_dn[E], p.ks_gu, p.ks_dn);
   const FOrder seq2(blockIdx.x, gridDim.x, tguA, tdnA, tguB, pre_dn[E] - tdnA, p.ks_gu, p.ks_dn);
+  // Uncached launches check out of the sync words early: the producer once
+  // it has claimed its last tile, each epilogue warp once it reaches its
+  // first down tile (its gate/up counts are all made); the fifth part checks
+  // the CTA out, so the last CTA zeroes the words while others still compute.
+  auto check_out_part = [&]() {
+    __threadfence();
+    if (atomicAdd(const_cast<uint32_t*>(&misc[3]), 1u) == 4u) sync_words_check_out(p, E);
+  };
   // the MMA issuer and the epilogue warps follow the producer's tile ids
   auto read_tile = [&](int& qs, uint32_t& qph, int* t) -> bool {
     if (!wait_bounded<kSpin>(tqf0 + 8 * qs, qph, misc + 1, p.status)) return false;
@@ -664,6 +746,7 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       for (int q = 0; q < S; ++q)
         if (armed[q] >= 0) wait_drain(full0 + 8 * q, static_cast<uint32_t>(armed[q]));
     }
+    if constexpr (!CACHED) check_out_part();
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     int s = 0;
@@ -725,52 +808,14 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     }
   } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue
-    if (p.x != nullptr) {
-      // Row gather, done here so that it overlaps the first weight loads:
-      // this CTA's contiguous share of the permuted token rows, eight 16-byte
-      // loads in flight per thread.  The producers start their token-row
-      // loads once every CTA has published its share.
-      constexpr int kEpiThreads = 128;
-      const int et = threadIdx.x - 64;
-      const int s0 = static_cast<int>(static_cast<long long>(p.R) * blockIdx.x / gridDim.x);
-      const int s1 = static_cast<int>(static_cast<long long>(p.R) * (blockIdx.x + 1) / gridDim.x);
-      const int vpr = p.H / 8;
-      const int n = (s1 - s0) * vpr;
-      constexpr int U = 8;
-      for (int i0 = et; i0 < n; i0 += U * kEpiThreads) {
-        uint4 v[U];
-        int dst[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int i = i0 + u * kEpiThreads;
-          dst[u] = -1;
-          if (i < n) {
-            const int sl = s0 + i / vpr;
-            const int c = i - (sl - s0) * vpr;
-            const int r = p.perm[sl];
-            if (r >= 0 && r < p.R) {
-              v[u] = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(r / p.k) * p.H)[c];
-              dst[u] = sl * vpr + c;
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (dst[u] >= 0) reinterpret_cast<uint4*>(p.x_perm)[dst[u]] = v[u];
-      }
-      // publish to the TMA loads of every CTA: fence for the async proxy, then
-      // one arrival per CTA
-      fence_proxy_async_global();
-      __threadfence();
-      asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
-      if (et == 0) atomicAdd(p.ready + E + 1, 1);
-    }
+    if (CACHED && p.x != nullptr) gather_share(p, E, threadIdx.x - 64);
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
     int qs = 0;
     uint32_t qph = 0;
+    bool out = CACHED;  // checked out of the sync words (uncached launches)
     for (;;) {
       int t = -1;
       if (!__all_sync(0xffffffffu, read_tile(qs, qph, &t))) break;
@@ -779,6 +824,10 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
       if (++qs == QR) {
         qs = 0;
         qph ^= 1u;
+      }
+      if (!out && (t < 0 || t >= total_gu)) {
+        out = true;
+        if (lane == 0) check_out_part();
       }
       if (t < 0) break;
       const FTile tl = tile_of(t);
@@ -902,6 +951,14 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     ptx::tmem_dealloc(misc[0], C::kTmemCols);
   }
   // The last CTA out resets the sync words for the next call.
+  if constexpr (!CACHED) {
+    // a role that left on an error path: complete the CTA's check-out here
+    if (threadIdx.x == 0 && misc[3] < 5u) {
+      misc[3] = 5u;
+      sync_words_check_out(p, E);
+    }
+    return;
+  }
   if (threadIdx.x == 0) {
     __threadfence();
     misc[2] = atomicAdd(p.ready + E, 1) == static_cast<int>(gridDim.x) - 1;
