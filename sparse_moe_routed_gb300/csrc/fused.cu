@@ -328,19 +328,28 @@ __device__ __forceinline__ void gather_share(const FusedArgs& p, int E, int et) 
 
 // Tile counts per position of the expert order: pre_gu[j] / pre_dn[j] =
 // the gate/up / down tiles of the experts before position j (one warp).
-// Each lane sums a run of consecutive positions, one warp scan places the
-// runs, and each lane writes its run's prefixes.
+// Chunk counts go to pre_dn in position order (coalesced); lane l then sums
+// its run of consecutive positions (starting at a lane-dependent offset so
+// that the lanes' reads fall in different banks), one warp scan places the
+// runs, each lane writes its run's prefixes in order, and a last coalesced
+// pass scales them by the blocks per expert.
 template <int NMAX, bool CACHED>
 __device__ __forceinline__ void tile_prefix(const FusedArgs& p, int E, const int* soff, const int* eord, int* pre_gu,
                                             int* pre_dn, int lane) {
+  for (int j = lane; j < E; j += 32) {
+    const int e = CACHED ? eord[j] : j;
+    pre_dn[j] = (max(soff[e + 1] - soff[e], 0) + NMAX - 1) / NMAX;
+  }
+  __syncwarp();
   const int per = (E + 31) / 32;
   const int j0 = min(E, lane * per), j1 = min(E, j0 + per);
-  auto chunks = [&](int j) {
-    const int e = CACHED ? eord[j] : j;
-    return (max(soff[e + 1] - soff[e], 0) + NMAX - 1) / NMAX;
-  };
+  const int n = j1 - j0;
   int c = 0;
-  for (int j = j0; j < j1; ++j) c += chunks(j);
+  int kk = n > 0 ? lane % n : 0;
+  for (int i = 0; i < n; ++i) {
+    c += pre_dn[j0 + kk];
+    kk = kk + 1 == n ? 0 : kk + 1;
+  }
   int incl = c;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -350,9 +359,15 @@ __device__ __forceinline__ void tile_prefix(const FusedArgs& p, int E, const int
   const int total = __shfl_sync(0xffffffffu, incl, 31);
   int run = incl - c;
   for (int j = j0; j < j1; ++j) {
-    pre_gu[j] = run * p.mb_gu;
-    pre_dn[j] = run * p.mb_dn;
-    run += chunks(j);
+    const int cj = pre_dn[j];
+    pre_gu[j] = run;
+    run += cj;
+  }
+  __syncwarp();
+  for (int j = lane; j < E; j += 32) {
+    const int r = pre_gu[j];
+    pre_gu[j] = r * p.mb_gu;
+    pre_dn[j] = r * p.mb_dn;
   }
   if (lane == 0) {
     pre_gu[E] = total * p.mb_gu;
@@ -452,15 +467,16 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
     fetch_records(p, E, nmiss, lane);
   } else {
   if constexpr (!CACHED) {
-    // The epilogue warps gather the token rows at once while warps 0 and 1
-    // read the segment offsets and build the tile prefix (named barrier 3);
-    // then warps 0 and 1 arrive on barrier 4, where the epilogue warps wait.
+    // Every thread reads the segment offsets; then the epilogue warps gather
+    // the token rows while warp 0 builds the tile prefix (warps 0 and 1 meet
+    // on named barrier 3) and warps 0 and 1 arrive on barrier 4, where the
+    // epilogue warps wait.
+    for (int i = threadIdx.x; i <= E; i += kCoreThreads) soff[i] = min(max(p.offsets[i], 0), p.R);
+    __syncthreads();
     if (warp >= 2) {
       if (p.x != nullptr) gather_share(p, E, threadIdx.x - 64);
       asm volatile("bar.sync 4, %0;" ::"n"(kCoreThreads) : "memory");
     } else {
-      for (int i = threadIdx.x; i <= E; i += 64) soff[i] = min(max(p.offsets[i], 0), p.R);
-      asm volatile("bar.sync 3, 64;" ::: "memory");
       if (warp == 0) tile_prefix<NMAX, CACHED>(p, E, soff, eord, pre_gu, pre_dn, lane);
       ptx::tc_fence_before();
       asm volatile("bar.sync 3, 64;" ::: "memory");
