@@ -468,16 +468,53 @@ __global__ void __launch_bounds__(kCoreThreads + (CACHED ? 32 * kFetchWarps : 0)
   } else {
   if constexpr (!CACHED) {
     // Every thread reads the segment offsets; then the epilogue warps gather
-    // the token rows while warp 0 builds the tile prefix (warps 0 and 1 meet
-    // on named barrier 3) and warps 0 and 1 arrive on barrier 4, where the
-    // epilogue warps wait.
+    // the token rows while warp 0 builds the tile prefix and warp 1 asks L2
+    // for the first weight stages of gate/up tile blockIdx.x (the tile this
+    // CTA takes first in the static order, and one of the first wave's on
+    // the queue), so that HBM starts streaming before the producer's first
+    // claim.  Warp 0 arrives on named barrier 3, where warp 1 waits for the
+    // prefix; warps 0 and 1 arrive on barrier 4, where the epilogue warps
+    // wait.
     for (int i = threadIdx.x; i <= E; i += kCoreThreads) soff[i] = min(max(p.offsets[i], 0), p.R);
     __syncthreads();
     if (warp >= 2) {
       if (p.x != nullptr) gather_share(p, E, threadIdx.x - 64);
       asm volatile("bar.sync 4, %0;" ::"n"(kCoreThreads) : "memory");
+    } else if (warp == 0) {
+      tile_prefix<NMAX, CACHED>(p, E, soff, eord, pre_gu, pre_dn, lane);
+      ptx::tc_fence_before();
+      asm volatile("bar.arrive 3, 64;" ::: "memory");
+      asm volatile("bar.arrive 4, %0;" ::"n"(kCoreThreads) : "memory");
     } else {
-      if (warp == 0) tile_prefix<NMAX, CACHED>(p, E, soff, eord, pre_gu, pre_dn, lane);
+      // gate/up tile g = blockIdx.x: the expert whose tile range holds it,
+      // walking the experts 32 at a time
+      const int g = blockIdx.x;
+      int run = 0;
+      bool found = false;
+      for (int e0 = 0; e0 < E && !found; e0 += 32) {
+        const int e = e0 + lane;
+        const int n = e < E ? max(soff[e + 1] - soff[e], 0) : 0;
+        const int tiles = ((n + NMAX - 1) / NMAX) * p.mb_gu;
+        int incl = tiles;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, tiles > 0 && g >= run + incl - tiles && g < run + incl);
+        if (hit != 0u) {
+          found = true;
+          const int src = __ffs(hit) - 1;
+          const int local = g - run - __shfl_sync(0xffffffffu, incl - tiles, src);
+          const int mb = local % p.mb_gu;
+          if (lane == 0) {
+            const size_t chunk0 = (static_cast<size_t>(e0 + src) * p.mb_gu + mb) * p.ks_gu;
+            const int ks = min(p.ks_gu, C::kStages * G);
+            ptx::bulk_prefetch_l2(p.tiles_gu + chunk0 * kABytes, static_cast<uint32_t>(ks * kABytes));
+          }
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
       ptx::tc_fence_before();
       asm volatile("bar.sync 3, 64;" ::: "memory");
       asm volatile("bar.arrive 4, %0;" ::"n"(kCoreThreads) : "memory");

@@ -99,6 +99,11 @@ __device__ __forceinline__ void cp_async_wait_all() {
 
 // One contiguous global chunk -> shared memory (untiled bulk copy); both
 // addresses 16-byte aligned, size a multiple of 16.
+// Ask L2 for `bytes` (a multiple of 16) at a 16-byte aligned global address.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
                                           uint64_t policy) {
   asm volatile(
