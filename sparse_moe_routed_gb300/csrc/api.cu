@@ -159,7 +159,7 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, const uint1
   cudaError_t e = moe::launch_permute(topk_ids, R, k, E, counts, offsets, perm, inv_perm, dev_status, st);
   if (e != cudaSuccess) return MOE_ECUDA;
   if (x_perm) {
-    e = moe::launch_gather_rows(x, inv_perm, R, k, T, H, x_perm, dev_status, st);
+    e = moe::launch_gather_rows(x, perm, inv_perm, R, k, T, H, x_perm, dev_status, st);
     if (e != cudaSuccess) return MOE_ECUDA;
   }
   return MOE_OK;
@@ -194,7 +194,7 @@ moe_status moe_permute_ws(const int32_t* topk_ids, int T, int k, int E, const ui
                                               static_cast<int32_t*>(workspace), dev_status, st);
   if (e != cudaSuccess) return MOE_ECUDA;
   if (x_perm) {
-    e = moe::launch_gather_rows(x, inv_perm, R, k, T, H, x_perm, dev_status, st);
+    e = moe::launch_gather_rows(x, perm, inv_perm, R, k, T, H, x_perm, dev_status, st);
     if (e != cudaSuccess) return MOE_ECUDA;
   }
   return MOE_OK;

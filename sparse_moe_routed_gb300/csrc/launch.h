@@ -89,8 +89,8 @@ size_t permute_chunked_ws_bytes(int R, int E);
 cudaError_t launch_permute_chunked(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,
                                    int32_t* perm, int32_t* inv, int32_t* ws, int32_t* st_word,
                                    cudaStream_t st);
-cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* inv, int R, int k, int T, int H,
-                               uint16_t* x_perm, const int32_t* st_word, cudaStream_t st);
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, const int32_t* inv, int R, int k, int T,
+                               int H, uint16_t* x_perm, const int32_t* st_word, cudaStream_t st);
 
 // gemm.cu (tcgen05 grouped GEMM)
 enum class GemmKind { kGateUp = 0, kDown = 1, kRouter = 2 };

@@ -332,6 +332,31 @@ __global__ void __launch_bounds__(kGatherThreads)
   }
 }
 
+// The same rows for small launches (a decode block has too few tokens to
+// keep a warp per token busy): one thread per 16-byte vector of x_perm, the
+// slot's route read from perm.
+__global__ void gather_rows_by_slot_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int R,
+                                           int k, int T, int H, uint16_t* __restrict__ xp, const int32_t* st_word) {
+  pdl_wait();
+  pdl_trigger();
+  if (*reinterpret_cast<const volatile int32_t*>(st_word) & MOE_DEV_BAD_EXPERT) return;
+  const int vpr = H / 8;
+  const size_t n = static_cast<size_t>(R) * vpr;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int s = static_cast<int>(idx / vpr);
+    const int c = static_cast<int>(idx - static_cast<size_t>(s) * vpr);
+    const int r = perm[s];
+    if (r < 0 || r >= R) continue;  // routing rejected upstream: leave the row alone
+    const int t = r / k;
+    if (t >= T) continue;
+    reinterpret_cast<uint4*>(xp)[idx] = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H)[c];
+  }
+}
+
+// Below this many tokens the gather runs one thread per vector of x_perm.
+constexpr int kGatherPerTokenMinT = 1024;
+
 }  // namespace
 
 cudaError_t launch_permute(const int32_t* ids, int R, int k, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
@@ -365,8 +390,18 @@ cudaError_t launch_permute_chunked(const int32_t* ids, int R, int E, int32_t* co
                     st_word);
 }
 
-cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* inv, int R, int k, int T, int H, uint16_t* x_perm,
-                               const int32_t* st_word, cudaStream_t st) {
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, const int32_t* inv, int R, int k, int T, int H,
+                               uint16_t* x_perm, const int32_t* st_word, cudaStream_t st) {
+  if (T < kGatherPerTokenMinT) {
+    const size_t n = static_cast<size_t>(R) * (H / 8);
+    const int threads = 256;
+    size_t blocks = (n + threads - 1) / threads;
+    const size_t cap = static_cast<size_t>(sm_count() > 0 ? sm_count() : 148) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    return launch_pdl(gather_rows_by_slot_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, x, perm,
+                      R, k, T, H, x_perm, st_word);
+  }
   if (k > 32) return cudaErrorInvalidValue;  // one lane per route of a token
   const int wpb = kGatherThreads / 32;
   size_t blocks = (static_cast<size_t>(T) + wpb - 1) / wpb;
