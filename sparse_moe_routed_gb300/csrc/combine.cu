@@ -28,7 +28,7 @@ namespace moe {
 namespace {
 
 constexpr int kCombineThreads = 128;  // x 4 floats = 512 columns per CTA (fp32 rows)
-constexpr int kCombineBatch = 8;      // rows whose loads a thread has in flight
+constexpr int kCombineBatch = 16;     // rows whose loads a thread has in flight (k <= 16: one round trip)
 
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const float* __restrict__ w, int T,
