@@ -28,7 +28,8 @@ namespace moe {
 namespace {
 
 constexpr int kCombineThreads = 128;  // x 4 floats = 512 columns per CTA (fp32 rows)
-constexpr int kCombineBatch = 16;     // rows whose loads a thread has in flight (k <= 16: one round trip)
+constexpr int kCombineBatch = 16;     // fp32 rows whose loads a thread has in flight (k <= 16: one round trip)
+constexpr int kCombineBatchW = 8;     // bf16 rows (prefill-sized launches: 16 measured slower)
 
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv, const float* __restrict__ w, int T,
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kCombineThreads)
 // The same sum over expert outputs that the down epilogue already multiplied
 // by their route weights and stored in bf16 (yw [R, H]): acc = sum_j
 // yw[inv[t*k + j]] in j order, fp32.  Eight columns per thread (one 16-byte
-// load per row, kCombineBatch rows in flight), 1,024 columns per CTA.
+// load per row, kCombineBatchW rows in flight), 1,024 columns per CTA.
 __global__ void __launch_bounds__(kCombineThreads)
     combine_weighted_kernel(const uint16_t* __restrict__ yw, const int32_t* __restrict__ inv, int T, int k, int H,
                             int R, const float* residual, uint16_t* __restrict__ out_bf16, float* out_f32,
@@ -119,15 +120,15 @@ __global__ void __launch_bounds__(kCombineThreads)
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   bool bad = false;
-  for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
-    uint4 v[kCombineBatch];
+  for (int j0 = 0; j0 < k; j0 += kCombineBatchW) {
+    uint4 v[kCombineBatchW];
 #pragma unroll
-    for (int u = 0; u < kCombineBatch; ++u) {
+    for (int u = 0; u < kCombineBatchW; ++u) {
       const int s = j0 + u < k ? slot[j0 + u] : -1;
       v[u] = s >= 0 ? reinterpret_cast<const uint4*>(yw + static_cast<size_t>(s) * H)[c8] : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < kCombineBatch; ++u) {
+    for (int u = 0; u < kCombineBatchW; ++u) {
       const int j = j0 + u;
       if (j < k) {
         if (slot[j] < 0) {
