@@ -105,6 +105,12 @@ def whole_job_rate(units_per_rank: float, seconds_max: float, world: int) -> flo
     return units_per_rank * world / seconds_max
 
 
+# nominal GB300 figures, reported beside the measured ones: HBM3e ~7.9 TB/s
+# (the layer's target is quoted against ~8 TB/s) and dense bf16 2.25 PF/s
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -593,13 +599,14 @@ def run_layer(args, rank, world, local, dev):
                    if fused else "grouped_gemm_kernel (moe_expert_gateup)")
     roof_hbm = {"bound": "hbm", "kernel": main_kernel,
                 "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                "peak_source": pk["source"] + " hbm_gbs",
+                "frac": achieved / pk["hbm_gbs"], "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                "traffic": traffic, "peak_source": pk["source"] + " hbm_gbs",
                 "bytes_per_launch": gu_bytes_avg, "avg_launch_us": gu_avg * 1e3, "timed_launches": KE}
     # a launch of several ms inside the step: the sustained bf16 figure
     roof_tensor = {"bound": "tensor", "kernel": main_kernel,
                    "achieved": main_tflops, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                   "frac": main_tflops / pk["bf16_tflops_sustained"], "traffic": traffic,
+                   "frac": main_tflops / pk["bf16_tflops_sustained"],
+                   "frac_of_nominal": main_tflops / NOMINAL_BF16_TFLOPS, "traffic": traffic,
                    "peak_source": pk["source"] + " bf16_tflops_sustained",
                    "flops_per_launch": main_flops, "avg_launch_us": gu_avg * 1e3, "timed_launches": KE}
     # the bound is whichever the launch's arithmetic intensity puts it under
@@ -618,8 +625,10 @@ def run_layer(args, rank, world, local, dev):
         "layer_roofline": {"bytes_per_step": layer_bytes_avg,
                            "achieved_gbs": layer_bytes_avg / (step_ms / 1e3) / 1e9,
                            "frac_hbm": layer_bytes_avg / (step_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                           "frac_hbm_of_nominal": layer_bytes_avg / (step_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                            "tflops": flops_step / (step_ms / 1e3) / 1e12,
                            "frac_tensor": flops_step / (step_ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
+                           "frac_tensor_of_nominal": flops_step / (step_ms / 1e3) / 1e12 / NOMINAL_BF16_TFLOPS,
                            **({} if fused else {"down_avg_us": dn_avg * 1e3})},
         "host_issue_us_per_step": 1e6 * (t_issue1 - t_issue0) / K,
         "dominant_kernel_timing": f"separate pass of {KE} steps after the headline region, events around "
@@ -777,11 +786,13 @@ def run_stack(args, rank, world, local, dev, emit=True, with_sweep=False):
                          "kernel": "gemv_q4_kernel (moe_expert_gateup, warp-level MMA)" if cuda_core_int4 else
                                    "grouped_gemm_q4_kernel (moe_expert_gateup, tcgen05)",
                          "achieved": gu_bytes / (gu_avg / 1e3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gu_bytes / (gu_avg / 1e3) / 1e9 / pk["hbm_gbs"], "traffic": None,
+                         "frac": gu_bytes / (gu_avg / 1e3) / 1e9 / pk["hbm_gbs"],
+                         "frac_of_nominal": gu_bytes / (gu_avg / 1e3) / 1e9 / NOMINAL_HBM_GBS, "traffic": None,
                          "bytes_per_launch": gu_bytes, "avg_launch_us": gu_avg * 1e3},
             "layer_roofline": {"bytes_per_block": bytes_block,
                                "achieved_gbs": bytes_block / (step_ms / 1e3) / 1e9,
-                               "frac_hbm": bytes_block / (step_ms / 1e3) / 1e9 / pk["hbm_gbs"]},
+                               "frac_hbm": bytes_block / (step_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                               "frac_hbm_of_nominal": bytes_block / (step_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS},
             # per layer: RMSNorm 1, route 2 (logits, selection), permute 2
             # (grouping, row gather), gate/up 1, down 1, combine 1
             "clocks": sampler.summary(tw0, tw1), "gpu_launches": 8 * L * K}
