@@ -73,6 +73,12 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t ran
 }
 
 // Store to the same shared-memory word in CTA `rank` of the cluster.
+__device__ __forceinline__ void st_cluster_f32(float* local, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ptx::smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_s32(int* local, uint32_t rank, int v) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(ptx::smem_u32(local)), "r"(rank));
@@ -83,7 +89,10 @@ __global__ void __launch_bounds__(kLogitThreads) router_logits_mma_kernel(const 
                                                                           const uint16_t* __restrict__ wr, int T,
                                                                           int H, int E, float* __restrict__ logits) {
   __shared__ float red[kLogitWarps][kLogitTok][kLogitExp];
-  __shared__ float tile[kLogitTok][kLogitExp];
+  __shared__ float tile[kLogitSplit][kLogitTok][kLogitExp];  // CTA 0: every CTA's K-quarter sums
+  // arrive now, wait before the first store into CTA 0's shared memory: by
+  // then every CTA of the cluster has started
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;  // fragment row group
@@ -146,24 +155,22 @@ __global__ void __launch_bounds__(kLogitThreads) router_logits_mma_kernel(const 
   __syncthreads();
   const int t = threadIdx.x / kLogitExp;
   const int e = threadIdx.x % kLogitExp;
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   if (threadIdx.x < kLogitTok * kLogitExp) {
     float sum = 0.f;
 #pragma unroll
     for (int w = 0; w < kLogitWarps; ++w) sum += red[w][t][e];
-    tile[t][e] = sum;
+    st_cluster_f32(&tile[rank][t][e], 0, sum);  // into CTA 0's slot for this CTA
   }
-  cluster_sync_all();  // every CTA's tile is complete and visible to the cluster
+  // every CTA's sums are in CTA 0's shared memory (release / acquire); the
+  // other CTAs are done, and nothing reads their shared memory afterwards
+  cluster_sync_all();
   if (rank == 0 && threadIdx.x < kLogitTok * kLogitExp) {
-    float part[kLogitSplit];
-    part[0] = tile[t][e];
+    float sum = tile[0][t][e];
 #pragma unroll
-    for (int r = 1; r < kLogitSplit; ++r) part[r] = ld_cluster_f32(&tile[t][e], r);
-    float sum = part[0];
-#pragma unroll
-    for (int r = 1; r < kLogitSplit; ++r) sum += part[r];
+    for (int r = 1; r < kLogitSplit; ++r) sum += tile[r][t][e];
     if (t0 + t < T && e0 + e < E) logits[static_cast<size_t>(t0 + t) * E + e0 + e] = sum;
   }
-  cluster_sync_all();  // keep every tile alive until CTA 0 has read it
 }
 
 // Order-preserving map of a float to an unsigned key (NaN mapped to -inf by
