@@ -122,6 +122,22 @@ def peaks():
             "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# kernels each boundary call launches (the grouping calls also launch the
+# row gather unless their x_perm argument is null)
+PER_CALL = {"moe_route": 2, "moe_route_permute": 1, "moe_permute": 2, "moe_permute_ws": 4, "moe_permute_gather": 2,
+            "moe_expert_swiglu_fused": 1, "moe_expert_gateup": 1, "moe_expert_down": 1,
+            "moe_combine": 1, "moe_expert_swiglu_fused_weighted": 1, "moe_combine_weighted": 1, "moe_rmsnorm": 1}
+
+
+def call_launches(call) -> int:
+    name, _, a = call
+    if name == "moe_permute":
+        return 1 if a[10] is None else 2
+    if name == "moe_permute_ws":
+        return 3 if a[10] is None else 4
+    return PER_CALL[name]
+
+
 # the files whose text a recorded DRAM-traffic figure depends on
 KERNEL_SOURCES = {
     "fused": ["fused.cu", "gemm_common.cuh", "ptx.cuh", "common.cuh"],
@@ -450,11 +466,7 @@ def run_layer(args, rank, world, local, dev):
     weighted = "moe_expert_swiglu_fused_weighted" in names
     fused = "moe_expert_swiglu_fused" in names or weighted
     # kernels each boundary call launches in this configuration
-    per_call = {"moe_route": 2, "moe_route_permute": 1, "moe_permute": 1 if R <= MoELayer.GATHER_IN_FUSED_MAX_ROWS
-                and fused else 2, "moe_permute_ws": 4, "moe_permute_gather": 2, "moe_expert_swiglu_fused": 1, "moe_expert_gateup": 1,
-                "moe_expert_down": 1, "moe_combine": 1, "moe_expert_swiglu_fused_weighted": 1,
-                "moe_combine_weighted": 1}
-    launches_per_step = sum(per_call[n] for n in names)
+    launches_per_step = sum(call_launches(c) for c in bound[0])
     gather_in_fused = fused and R <= MoELayer.GATHER_IN_FUSED_MAX_ROWS
     # the dominant kernel(s): the fused contraction, or gate/up then down
     i_main = names.index("moe_expert_swiglu_fused_weighted" if weighted else
@@ -711,6 +723,7 @@ def run_stack(args, rank, world, local, dev, emit=True, with_sweep=False):
     K = args.steps
     # every layer's calls on the fixed stream buffer, built before the timed region
     lcalls = [stack.layer_calls(xw, l, stream=st) for l in range(L)]
+    launches_per_block = sum(call_launches(c) for l in range(L) for c in lcalls[l])
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(gpu_uuid(local))
@@ -793,9 +806,9 @@ def run_stack(args, rank, world, local, dev, emit=True, with_sweep=False):
                                "achieved_gbs": bytes_block / (step_ms / 1e3) / 1e9,
                                "frac_hbm": bytes_block / (step_ms / 1e3) / 1e9 / pk["hbm_gbs"],
                                "frac_hbm_of_nominal": bytes_block / (step_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS},
-            # per layer: RMSNorm 1, route 2 (logits, selection), permute 2
+            # per layer: RMSNorm 1, route 2 (logits, selection), grouping 2
             # (grouping, row gather), gate/up 1, down 1, combine 1
-            "clocks": sampler.summary(tw0, tw1), "gpu_launches": 8 * L * K}
+            "clocks": sampler.summary(tw0, tw1), "gpu_launches": launches_per_block * K}
     if emit:
         if rank == 0:
             print(json.dumps(line), flush=True)
