@@ -195,7 +195,10 @@ def seeded_ids(T, k, E, seed, zipf=False):
 
 PERMUTE_CASES = [(1, 4, 64, 256, False), (16, 10, 512, 2560, True), (37, 10, 512, 2560, False),
                  (4096, 10, 512, 2560, False), (300, 32, 1024, 128, False), (64, 8, 8, 128, False),
-                 (8191, 10, 512, 128, True), (32768, 10, 512, 128, False)]
+                 (8191, 10, 512, 128, True), (32768, 10, 512, 128, False),
+                 # chunk edges: exactly 4 chunks of 2,048 routes; one route past
+                 # them; 1,024 experts (fewer route warps per chunk)
+                 (2048, 4, 1024, 128, False), (2049, 4, 64, 128, True), (4100, 10, 1024, 128, True)]
 
 
 def permute_call(chunked, ids, E, x, counts, offsets, perm, inv, xp, st):
