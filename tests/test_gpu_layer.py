@@ -329,6 +329,42 @@ def test_combine_parity(T, k, H, residual):
     assert np.array_equal(bits(out_b), bits(out_f.to(torch.bfloat16)))
 
 
+@pytest.mark.parametrize("T,k,H", [(16, 10, 2560), (3, 20, 384), (40, 32, 256)])
+def test_combine_right_after_the_grouping(T, k, H):
+    """moe_combine reads the routes' slots and weights before it waits on
+    the launch before it and checks them after; when that launch is the
+    grouping that rewrites the slots (here several groupings in a row, each
+    followed at once by a combine), the rows must still be the ones the new
+    slots name."""
+    rng = np.random.default_rng(T * k)
+    E = 64
+    R = T * k
+    y_np = rng.standard_normal((R, H)).astype(np.float32)
+    y = torch.from_numpy(y_np).to(DEV)
+    counts = torch.empty((E,), dtype=torch.int32, device=DEV)
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device=DEV)
+    perm = torch.empty((R,), dtype=torch.int32, device=DEV)
+    inv = torch.empty((R,), dtype=torch.int32, device=DEV)
+    st = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    outs, refs = [], []
+    for rep in range(6):
+        ids_np = seeded_ids(T, k, E, seed=1000 * rep + T)
+        _, _, _, inv_r = oracle.permute(ids_np, E)
+        w_np = rng.random((T, k)).astype(np.float32)
+        w = torch.from_numpy(w_np).to(DEV)
+        ids = torch.from_numpy(ids_np).to(DEV)
+        torch.cuda.synchronize()
+        out = torch.empty((T, H), dtype=torch.float32, device=DEV)
+        _lib.moe_permute(ids, E, None, counts, offsets, perm, inv, None, st)
+        _lib.moe_combine(y, inv, w, None, None, out, st)
+        outs.append(out)
+        refs.append(oracle.combine(y_np, inv_r, w_np, None))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for out, ref in zip(outs, refs):
+        assert np.allclose(out.cpu().numpy(), ref, rtol=1e-5, atol=1e-5)
+
+
 def test_combine_nonfinite_flag():
     T, k, H = 2, 2, 128
     y = torch.zeros((T * k, H), device=DEV)
