@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kPlanThreads) cache_plan_kernel(const int32_t*
   __shared__ int warp_sums[32];
   __shared__ int s_missexp[kMaxE];
   __shared__ unsigned long long s_key[kPlanThreads];
-  __shared__ int s_nmiss, s_nelig;
+  __shared__ int s_nmiss;
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x;

@@ -662,6 +662,7 @@ template <int NT, int EPL>
 cudaError_t run_route_permute(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H, int E, int k,
                               int32_t* ids, float* w, float* gap, int32_t* counts, int32_t* offsets, int32_t* perm,
                               int32_t* inv, int32_t* st_word, cudaStream_t st) {
+  static_assert(NT <= kRpMaxNt, "n8 tiles per CTA");
   auto kern = route_permute_kernel<NT, EPL>;
   static std::mutex mu;
   static int ready[64] = {0};  // per device: 1 usable, -1 not
