@@ -138,8 +138,6 @@ struct CfgF {
   static constexpr int kBoxB = kBoxR * kBK * 2;
   static constexpr int kNumBars = 2 * kStages + 5 + 2 * kTileRing;
   // misc words and the tile-id ring; offsets and the two tile prefixes;
-  // cached: also slots and the expert order
-  // misc words and the tile-id ring; offsets and the two tile prefixes;
   // cached: also slots and the expert order; then the epilogue warps' route
   // weights of the current tile's columns (weighted outputs)
   static constexpr int kTail = 32 + (CACHED ? 5 : 3) * (kMaxE + 1) * 4 + 16 + 4 * NMAX * 4;
