@@ -415,6 +415,31 @@ def test_layer_parity(name, T, nsample, tiled):
           f"of max|ref|, mean rel {mean_rel:.2e}")
 
 
+@pytest.mark.parametrize("T,H,E,k,I,tiled", [(16, 1024, 1024, 16, 256, True), (16, 1024, 1024, 16, 256, False),
+                                              (37, 256, 100, 7, 128, True), (5, 512, 1024, 32, 128, True)])
+def test_layer_parity_at_the_expert_count_limits(T, H, E, k, I, tiled):
+    """The whole layer at the largest accepted expert count (E = 1,024: the
+    fused launch's tile prefix and tile search over 32 expert groups, 256
+    routes, and k = 32) and at an expert count that is not a multiple of
+    32, against the oracle on every token."""
+    cfg = wl.LayerConfig("limits", T=T, H=H, E=E, k=k, I=I, bias="zipf", seed=43 + E + k)
+    d = wl.layer_inputs(cfg, DEV)
+    torch.cuda.synchronize()
+    layer, out = run_layer(cfg, d, tiled)
+    xb, wrb = bits(d["x"]), bits(d["w_router"])
+    ids_r, w_r, gap_r, L_r = oracle.route(xb, wrb, d["bias"].cpu().numpy(), k)
+    ids = layer.ids[:T].cpu().numpy()
+    same = np.array([np.array_equal(ids[t], ids_r[t]) for t in range(T)])
+    assert np.all(same | (gap_r <= GAP_TOL) | _adjacent_swap_ok(ids, ids_r, L_r))
+    assert same.sum() >= 0.9 * T
+    ref = oracle.experts_combine(f32_of_bits(xb), ids_r, w_r, H, I, wgu_bits=bits(d["w_gateup"]),
+                                 wd_bits=bits(d["w_down"]))
+    rel_max, mean_rel = assert_output_close(out.float().cpu().numpy()[same], ref[same],
+                                            what=f"layer E={E} k={k} tiled={tiled}")
+    print(f"E={E} k={k} T={T} tiled={tiled}: {same.sum()}/{T} tokens graded, max err {rel_max:.2e} of max|ref|, "
+          f"mean rel {mean_rel:.2e}")
+
+
 def test_layer_with_one_launch_routing():
     """The layer with routing and grouping in one launch (moe_route_permute)
     against the oracle, as test_layer_parity grades the default chain."""
