@@ -123,10 +123,12 @@ ODD_K2 = wl.LayerConfig("int4_odd_k2", T=16, H=384, E=64, k=4, I=128, bias=None,
 # of two blocks with two steps per slot (H = 768: six blocks, I = 128)
 QUAD_K1 = wl.LayerConfig("int4_quad_k1", T=16, H=512, E=64, k=4, I=192, bias=None, seed=37)
 PAIR_K2 = wl.LayerConfig("int4_pair_k2", T=16, H=768, E=64, k=4, I=128, bias=None, seed=41)
-GEOM = {"odd": ODD, "odd_k4": ODD_K4, "odd_k2": ODD_K2, "quad_k1": QUAD_K1, "pair_k2": PAIR_K2}
+# the largest accepted expert count: the tile schedule over 1,024 experts, 256 routes
+WIDE_E = wl.LayerConfig("int4_e1024", T=16, H=1024, E=1024, k=16, I=256, bias=None, seed=47)
+GEOM = {"odd": ODD, "odd_k4": ODD_K4, "odd_k2": ODD_K2, "quad_k1": QUAD_K1, "pair_k2": PAIR_K2, "e1024": WIDE_E}
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode", "odd", "odd_k4", "odd_k2", "quad_k1", "pair_k2"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "odd", "odd_k4", "odd_k2", "quad_k1", "pair_k2", "e1024"])
 def test_int4_skewed_routes_split_tiles(name):
     """Decode-sized int4 launches run on the CUDA-core kernel, which splits an
     expert's rows into tiles of 4: routes skewed so that one expert gets 9
