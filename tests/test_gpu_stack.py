@@ -75,6 +75,31 @@ def test_int4_stack_layer_parity(T):
     print(f"T={T}: {len(keep)}/{T} tokens graded, max err {rel_max:.2e} of max|ref|, mean rel {mean_rel:.2e}")
 
 
+@pytest.mark.parametrize("T", [512, 1024])
+def test_int4_stack_layer_parity_many_routes(T):
+    """int4 layers with many routes run on the tensor-core kernels (64-row
+    token tiles at 5,120 routes, 128-row tiles at 10,240) instead of the
+    CUDA-core one: 48 sampled tokens (the last one always) against the
+    oracle."""
+    stack = make_stack(1, T)
+    x0 = wl.token_batch(CFG, DEV, index=7, T=T).float()
+    x = x0.clone()
+    stack.forward(x)
+    torch.cuda.synchronize()
+    L0 = stack.layers[0]
+    assert L0.read_status() == 0
+    rng = np.random.default_rng(T)
+    toks = np.sort(np.concatenate([rng.choice(T - 1, size=47, replace=False), [T - 1]]))
+    x0_np = x0.cpu().numpy()
+    _, moe_ref, ids_r, w_r, gap_r, L_r = oracle_layer(x0_np[toks], 0)
+    rep = compare_routes(L0.ids[:T].cpu().numpy()[toks], L0.w[:T].cpu().numpy()[toks], ids_r, w_r, gap_r, L_r)
+    keep = np.array(rep["exact_rows"])
+    assert len(keep) >= 0.9 * len(toks), rep
+    moe_gpu = (x.cpu().numpy().astype(np.float64) - x0_np)[toks][keep]
+    rel_max, mean_rel = assert_output_close(moe_gpu, moe_ref[keep], what=f"int4 layer MoE output, T={T}")
+    print(f"T={T}: {len(keep)}/{len(toks)} tokens graded, max err {rel_max:.2e} of max|ref|, mean rel {mean_rel:.2e}")
+
+
 def test_int4_expert_stage_tiny_geometry():
     """int4 contraction on the tiny geometry (two 128-row down blocks, K = 256 / 64)."""
     cfg = wl.TINY
