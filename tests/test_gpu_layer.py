@@ -440,6 +440,32 @@ def test_layer_parity_at_the_expert_count_limits(T, H, E, k, I, tiled):
           f"mean rel {mean_rel:.2e}")
 
 
+@pytest.mark.parametrize("T,H,E,k,I", [(8191, 2560, 64, 8, 640), (4096, 1024, 1024, 16, 256)])
+def test_layer_parity_prefill_shapes(T, H, E, k, I):
+    """Prefill-sized layers off the main geometry, 48 sampled tokens (the
+    last always) against the oracle: 1,024 rows per expert (256-row tiles,
+    four row chunks per expert with a ragged last one) and 1,024 experts
+    with 64 rows each (the levelled static tile order, the chunked grouping
+    and route-weighted outputs over 32 expert groups)."""
+    cfg = wl.LayerConfig("prefill_shape", T=T, H=H, E=E, k=k, I=I, bias=None, seed=53 + E)
+    d = wl.layer_inputs(cfg, DEV)
+    torch.cuda.synchronize()
+    layer, out = run_layer(cfg, d, tiled=True)
+    toks = sample_tokens(T, 48, seed=3)
+    xb = bits(d["x"])
+    ids_r, w_r, gap_r, L_r = oracle.route(xb[toks], bits(d["w_router"]), None, k)
+    ids = layer.ids[:T].cpu().numpy()[toks]
+    same = np.array([np.array_equal(ids[n], ids_r[n]) for n in range(len(toks))])
+    assert np.all(same | (gap_r <= GAP_TOL) | _adjacent_swap_ok(ids, ids_r, L_r))
+    assert same.sum() >= 0.9 * len(toks)
+    ref = oracle.experts_combine(f32_of_bits(xb[toks]), ids_r, w_r, H, I, wgu_bits=bits(d["w_gateup"]),
+                                 wd_bits=bits(d["w_down"]))
+    rel_max, mean_rel = assert_output_close(out.float().cpu().numpy()[toks][same], ref[same],
+                                            what=f"prefill-shaped layer T={T} E={E}")
+    print(f"T={T} E={E} k={k}: {same.sum()}/{len(toks)} tokens graded, max err {rel_max:.2e} of max|ref|, "
+          f"mean rel {mean_rel:.2e}")
+
+
 def test_layer_with_one_launch_routing():
     """The layer with routing and grouping in one launch (moe_route_permute)
     against the oracle, as test_layer_parity grades the default chain."""
