@@ -239,7 +239,7 @@ __device__ __forceinline__ int build_schedule(const GemmArgs& p, bool dense, int
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i <= E; i += blockDim.x)
-    soff[i] = dense ? (i == 0 ? 0 : p.R) : min(max(p.offsets[i], 0), p.R);
+    soff[i] = dense ? (i == 0 ? 0 : p.R) : min(max(__ldcg(p.offsets + i), 0), p.R);
   __syncthreads();
   if (warp == 0) {
     int running = 0;

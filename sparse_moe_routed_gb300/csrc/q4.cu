@@ -180,7 +180,13 @@ __global__ void __launch_bounds__(kGvThreads + (FETCH ? 32 * kGvFetchWarps : 0),
     misc[1] = 0;
     ptx::fence_mbar_init();
   }
-  pdl_wait();
+  // A down launch over resident records reads only its token rows (h) from
+  // the gate/up launch before it; its weights and its routes (offsets,
+  // written two launches back and read past L1) are ready at its start.
+  // Its token-row warp alone waits for that launch, so the weight stream
+  // starts on each SM as soon as a gate/up CTA leaves it.
+  const bool late_wait = KIND == 1 && !FETCH && p.slot_of == nullptr;
+  if (!late_wait) pdl_wait();
   pdl_trigger();
   GemmArgs ps = p;  // the schedule counts tiles of RT rows
   ps.mblocks = p.mblocks / BPT;
@@ -331,6 +337,7 @@ __global__ void __launch_bounds__(kGvThreads + (FETCH ? 32 * kGvFetchWarps : 0),
     uint32_t armed_mask = 0, armed_ph = 0;
     bool ok = true;
     int ntile = 0;
+    if (late_wait) pdl_wait();
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++ntile) {
       const Tile tl = sc.tile(t);
       const int b = ntile & 1;
