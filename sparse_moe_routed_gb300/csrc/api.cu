@@ -45,6 +45,34 @@ cudaError_t ensure_smem_fn(const void* kern, int bytes) {
   return e;
 }
 
+// The token each stream's last launch left (see launch.h), per device.
+namespace {
+std::mutex g_token_mu;
+std::map<std::pair<int, cudaStream_t>, const void*> g_token;
+std::pair<int, cudaStream_t> token_key(cudaStream_t st) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  return std::make_pair(dev, st);
+}
+}  // namespace
+
+void stream_token_set(cudaStream_t st, const void* token) {
+  std::lock_guard<std::mutex> lock(g_token_mu);
+  g_token[token_key(st)] = token;
+}
+
+const void* stream_token_get(cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_token_mu);
+  const auto it = g_token.find(token_key(st));
+  return it == g_token.end() ? nullptr : it->second;
+}
+
+void stream_token_clear(cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_token_mu);
+  const auto it = g_token.find(token_key(st));
+  if (it != g_token.end()) it->second = nullptr;
+}
+
 }  // namespace moe
 
 namespace {

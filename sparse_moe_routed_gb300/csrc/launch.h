@@ -18,6 +18,15 @@ cudaError_t ensure_smem(void (*kern)(KArgs...), int bytes) {
   return ensure_smem_fn(reinterpret_cast<const void*>(kern), bytes);
 }
 
+// A launch may leave a token on its stream: the address of a buffer it read
+// only after its grid-dependency wait and did not write.  Every launch of
+// this library clears its stream's token first, so a token seen before a
+// launch names the launch right before it.  (Launches outside the library
+// do not clear it, but they do not let a later launch start early either.)
+void stream_token_set(cudaStream_t st, const void* token);
+const void* stream_token_get(cudaStream_t st);
+void stream_token_clear(cudaStream_t st);
+
 // Launch with programmatic stream serialization (see pdl_wait in common.cuh).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
@@ -32,6 +41,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  stream_token_clear(st);
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
@@ -53,6 +63,7 @@ cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, di
   attr[1].val.clusterDim.z = cluster.z;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  stream_token_clear(st);
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 

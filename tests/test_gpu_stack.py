@@ -207,6 +207,59 @@ def test_int4_skewed_routes_split_tiles(name):
     assert_output_close(y.cpu().numpy(), ref, what=f"int4 expert outputs, skewed routes ({name})")
 
 
+def test_int4_down_right_after_a_grouping_reads_the_new_routes():
+    """The int4 down launch starts its weight stream before the launch in
+    front of it ends only when that launch is the gate/up launch over the
+    same offsets.  Here the grouping rewrites the offsets (other routes)
+    right before the down launch on the same stream, with nothing in
+    between: the down outputs must be those of the new routes, bit for bit
+    (against the same down launch after a full synchronisation), and the
+    ordinary gate/up -> down pair must match them too."""
+    cfg = QUAD_K1
+    T, k, E, H, I = 16, cfg.k, cfg.E, cfg.H, cfg.I
+    d = wl.layer_inputs(cfg, DEV)
+    q_gu, s_gu = wl.quantize_int4_g64(d["w_gateup"])
+    q_d, s_d = wl.quantize_int4_g64(d["w_down"])
+    gu, dn = pack_layer_experts(q_gu, q_d, _lib.MOE_W_INT4_G64, E, H, I, s_gateup=s_gu, s_down=s_d)
+    fmt = _lib.MOE_W_INT4_G64_TILED
+    R = T * k
+    rng = np.random.default_rng(61)
+    idsA = torch.from_numpy(np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)).to(DEV)
+    idsB = torch.from_numpy(np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)).to(DEV)
+    x = wl.token_batch(cfg, DEV, index=31, T=T)
+    counts = torch.empty((E,), dtype=torch.int32, device=DEV)
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device=DEV)
+    perm = torch.empty((R,), dtype=torch.int32, device=DEV)
+    inv = torch.empty((R,), dtype=torch.int32, device=DEV)
+    xp = torch.empty((R, H), dtype=torch.bfloat16, device=DEV)
+    hB = torch.empty((R, I), dtype=torch.bfloat16, device=DEV)
+    hA = torch.empty((R, I), dtype=torch.bfloat16, device=DEV)
+    st = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    # h of routes B, and the reference down outputs after a full sync
+    _lib.moe_permute(idsB, E, x, counts, offsets, perm, inv, xp, st)
+    _lib.moe_expert_gateup(xp, offsets, E, H, I, gu, hB, st, fmt=fmt)
+    torch.cuda.synchronize()
+    y_ref = torch.empty((R, H), dtype=torch.float32, device=DEV)
+    _lib.moe_expert_down(hB, offsets, E, H, I, dn, y_ref, st, fmt=fmt)
+    torch.cuda.synchronize()
+    offsB = offsets.clone()
+    for rep in range(3):
+        # the gate/up -> down pair of routes A leaves the offsets of A ...
+        _lib.moe_permute(idsA, E, x, counts, offsets, perm, inv, xp, st)
+        _lib.moe_expert_gateup(xp, offsets, E, H, I, gu, hA, st, fmt=fmt)
+        yA = torch.full((R, H), float("nan"), dtype=torch.float32, device=DEV)
+        _lib.moe_expert_down(hA, offsets, E, H, I, dn, yA, st, fmt=fmt)
+        # ... then the grouping of routes B and the down launch right after it
+        _lib.moe_permute(idsB, E, None, counts, offsets, perm, inv, None, st)
+        y = torch.full((R, H), float("nan"), dtype=torch.float32, device=DEV)
+        _lib.moe_expert_down(hB, offsets, E, H, I, dn, y, st, fmt=fmt)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        assert torch.equal(offsets, offsB)
+        assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32)), rep
+        assert torch.isfinite(yA).all()
+
+
 def test_int4_stack_forced_routes_six_layers():
     """Six layers free-running with the oracle's routes imposed on the GPU:
     the residual streams must agree to the stated tolerance."""
