@@ -189,6 +189,9 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int k, int E, const uint1
   if (x_perm) {
     e = moe::launch_gather_rows(x, perm, inv_perm, R, k, T, H, x_perm, dev_status, st);
     if (e != cudaSuccess) return MOE_ECUDA;
+    // the row gather neither writes the offsets nor starts before they are
+    // complete: the contraction after it may read them at its start
+    moe::stream_token_set(st, offsets);
   }
   return MOE_OK;
 }
@@ -224,6 +227,9 @@ moe_status moe_permute_ws(const int32_t* topk_ids, int T, int k, int E, const ui
   if (x_perm) {
     e = moe::launch_gather_rows(x, perm, inv_perm, R, k, T, H, x_perm, dev_status, st);
     if (e != cudaSuccess) return MOE_ECUDA;
+    // the row gather neither writes the offsets nor starts before they are
+    // complete: the contraction after it may read them at its start
+    moe::stream_token_set(st, offsets);
   }
   return MOE_OK;
 }

@@ -125,7 +125,7 @@ constexpr int kGvFetchBytes = 32768;  // a down-record piece
 
 template <int KIND, int QG, int BPT, bool FETCH = false>
 __global__ void __launch_bounds__(kGvThreads + (FETCH ? 32 * kGvFetchWarps : 0), 1)
-    gemv_q4_kernel(GemmArgs p, int after_gateup) {
+    gemv_q4_kernel(GemmArgs p, int early) {
   static_assert(!FETCH || KIND == 0, "the gate/up launch fetches both components");
   using C = CfgV;
   static_assert(kGvGroups % BPT == 0, "groups");
@@ -181,13 +181,15 @@ __global__ void __launch_bounds__(kGvThreads + (FETCH ? 32 * kGvFetchWarps : 0),
     misc[1] = 0;
     ptx::fence_mbar_init();
   }
-  // A down launch over resident records right after the gate/up launch
-  // over the same routes (after_gateup) reads only its token rows (h) from
-  // that launch; its weights and its routes (offsets, complete before the
-  // gate/up launch read them, read here past L1) are ready at its start.
-  // Its token-row warp alone waits for the gate/up launch, so the weight
-  // stream starts on each SM as soon as a gate/up CTA leaves it.
-  const bool late_wait = KIND == 1 && !FETCH && after_gateup != 0 && p.slot_of == nullptr;
+  // A launch over resident records right after a launch that left this
+  // launch's offsets as its stream's token (early: the gate/up launch before
+  // a down launch, the row gather before a gate/up launch) reads only its
+  // token rows (h or x_perm) from that launch; its weights and its routes
+  // (offsets, complete before that launch started, read here past L1) are
+  // ready at its start.  Its token-row warp alone waits for the launch
+  // before, so the weight stream starts on each SM as soon as one of that
+  // launch's CTAs leaves it.
+  const bool late_wait = !FETCH && early != 0 && p.slot_of == nullptr;
   if (!late_wait) pdl_wait();
   pdl_trigger();
   GemmArgs ps = p;  // the schedule counts tiles of RT rows
@@ -665,11 +667,12 @@ cudaError_t run_gemv_q4_g(const GemmArgs& args, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int grid = sm_count();
   if (grid <= 0) return cudaErrorNoDevice;
-  // the gate/up launch leaves its offsets as its stream's token; a down
-  // launch that finds the same offsets there follows it directly
-  const int after_gateup = (KIND == 1 && stream_token_get(st) == args.offsets) ? 1 : 0;
+  // the gate/up launch leaves its offsets as its stream's token (so does
+  // the row gather); a launch that finds its own offsets there follows
+  // such a launch directly
+  const int early = stream_token_get(st) == args.offsets ? 1 : 0;
   e = launch_pdl(kern, dim3(grid), dim3(kGvThreads + (FETCH ? 32 * kGvFetchWarps : 0)), CfgV::kSmemBytes, st, args,
-                 after_gateup);
+                 early);
   if (e == cudaSuccess && KIND == 0) stream_token_set(st, args.offsets);
   return e;
 }

@@ -207,14 +207,15 @@ def test_int4_skewed_routes_split_tiles(name):
     assert_output_close(y.cpu().numpy(), ref, what=f"int4 expert outputs, skewed routes ({name})")
 
 
-def test_int4_down_right_after_a_grouping_reads_the_new_routes():
-    """The int4 down launch starts its weight stream before the launch in
-    front of it ends only when that launch is the gate/up launch over the
-    same offsets.  Here the grouping rewrites the offsets (other routes)
-    right before the down launch on the same stream, with nothing in
-    between: the down outputs must be those of the new routes, bit for bit
-    (against the same down launch after a full synchronisation), and the
-    ordinary gate/up -> down pair must match them too."""
+def test_int4_launches_right_after_a_grouping_read_the_new_routes():
+    """The int4 contractions start their weight stream before the launch in
+    front of them ends only when that launch left their offsets as its
+    token (the gate/up launch before a down launch, the row gather before a
+    gate/up launch).  Here a grouping rewrites the offsets (other routes)
+    right before a down launch, and right before a gate/up launch, on the
+    same stream with nothing in between: the outputs must be those of the
+    new routes, bit for bit (against the same launches after a full
+    synchronisation)."""
     cfg = QUAD_K1
     T, k, E, H, I = 16, cfg.k, cfg.E, cfg.H, cfg.I
     d = wl.layer_inputs(cfg, DEV)
@@ -239,6 +240,7 @@ def test_int4_down_right_after_a_grouping_reads_the_new_routes():
     _lib.moe_permute(idsB, E, x, counts, offsets, perm, inv, xp, st)
     _lib.moe_expert_gateup(xp, offsets, E, H, I, gu, hB, st, fmt=fmt)
     torch.cuda.synchronize()
+    xpB = xp.clone()
     y_ref = torch.empty((R, H), dtype=torch.float32, device=DEV)
     _lib.moe_expert_down(hB, offsets, E, H, I, dn, y_ref, st, fmt=fmt)
     torch.cuda.synchronize()
@@ -253,10 +255,17 @@ def test_int4_down_right_after_a_grouping_reads_the_new_routes():
         _lib.moe_permute(idsB, E, None, counts, offsets, perm, inv, None, st)
         y = torch.full((R, H), float("nan"), dtype=torch.float32, device=DEV)
         _lib.moe_expert_down(hB, offsets, E, H, I, dn, y, st, fmt=fmt)
+        # and routes A regrouped (no row gather) right before a gate/up
+        # launch over routes B's rows: it must wait, and then read B's offsets
+        _lib.moe_permute(idsA, E, None, counts, offsets, perm, inv, None, st)
+        _lib.moe_permute(idsB, E, None, counts, offsets, perm, inv, None, st)
+        h2 = torch.full((R, I), float("nan"), dtype=torch.bfloat16, device=DEV)
+        _lib.moe_expert_gateup(xpB, offsets, E, H, I, gu, h2, st, fmt=fmt)
         torch.cuda.synchronize()
         assert st.item() == 0
         assert torch.equal(offsets, offsB)
         assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32)), rep
+        assert torch.equal(h2.view(torch.int16), hB.view(torch.int16)), rep
         assert torch.isfinite(yA).all()
 
 
