@@ -238,6 +238,16 @@ MOE_API moe_status moe_route_permute(const uint16_t *x, const uint16_t *w_router
  * R is T*k of the routing call; slots past offsets[E] are not touched.
  * dev_status (4 bytes, required) gets MOE_DEV_TIMEOUT if a bounded pipeline
  * wait ran out (the kernel then stops early; outputs are incomplete).
+ *
+ * Launch overlap (decode-sized int4 launches over resident records): a
+ * gate/up call issued right after moe_permute's row gather, and a down
+ * call issued right after a gate/up call, over the same offsets on the same
+ * stream, start streaming their weights before the call in front of them
+ * has finished; they wait for it only where they read its output (x_perm
+ * or h).  The library decides this from its own launch order on the
+ * stream, so any other order is safe and simply waits: it needs no action
+ * from the caller.  Calls that share a stream are issued from one host
+ * thread at a time, as their order on the stream requires anyway.
  * ------------------------------------------------------------------------- */
 MOE_API moe_status moe_expert_gateup(const uint16_t *x_perm, const int32_t *offsets, int R, int E, int H,
                              int I, int fmt, const void *w_gateup, const uint16_t *s_gateup,
